@@ -1,0 +1,424 @@
+"""Benchmark of the hot path: ragged GQA prefill + paged GQA decode on GB300.
+
+One step = one ragged prefill over the 16-request hd128 workload (16 requests, lengths
+U{128..4096}, 32 qo / 8 kv heads, causal) followed by one paged decode over the
+256-request workload (kv U{512..32768}, page 16, 32 / 8 heads, split-KV + merge), both
+through the C ABI (libpgqa) on inputs already resident in HBM.  Both inputs exceed the
+129 MB L2 (0.42 GB and 17.4 GB), so no flush is needed between steps.
+
+Printed (rank 0, one JSON line): value = prefill TFLOP/s (causal-visible pairs only,
+4 * d flops per pair and query head); the decode KV GB/s sits under "secondary".  Each
+carries its roofline against MEASURED_PEAKS.json.  `e2e` repeats the measurement with
+host-resident inputs copied in (pinned memory) and outputs copied out every step.
+`cpu_baseline` times the float64 oracle on a bounded row sample on the host cores.
+
+--impl reference times that oracle as the reference arm on the same workload and metric.
+Multi-GPU (torchrun): every rank runs the same per-GPU workload (requests are
+independent; replicas, no data-path collective), value = all ranks' work / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "ragged prefill TFLOP/s (% BF16 peak); paged decode KV GB/s (% HBM peak)"
+PREFILL_WORKLOAD = "prefill_hd128"
+DECODE_WORKLOAD = "decode"
+
+
+# ------------------------------------------------------------------ work accounting
+def visible_pairs(qo, kv, causal=True):
+    """Number of (query row, key) pairs a request attends to (per query head)."""
+    if not causal:
+        return qo * kv
+    tot = 0
+    for i in range(qo):
+        tot += min(kv, max(0, i + kv - qo + 1))
+    return tot
+
+
+def prefill_flops(qo_lens, kv_lens, hq, d, causal=True):
+    return sum(4 * d * hq * visible_pairs(a, b, causal) for a, b in zip(qo_lens, kv_lens))
+
+
+def decode_kv_bytes(kv_lens, hk, d):
+    return sum(kv_lens) * hk * d * 2 * 2
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def load_traffic():
+    """Per-launch DRAM bytes of each kernel from the committed ncu summary, if current."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return {}
+
+
+# ------------------------------------------------------------------ distributed
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(ws, backend):
+    if ws > 1 and not torch.distributed.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group(backend=backend)
+
+
+def reduce_max(x: float, device) -> float:
+    """Max of a scalar over ranks (identity without a process group)."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(device):
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        reduce_max(0.0, device)
+
+
+# ------------------------------------------------------------------ clocks
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu_index = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ CPU baseline
+def oracle_sample_prefill(case, budget_rows, seed=0):
+    """A bounded row sample of the prefill workload and its flops."""
+    rng = np.random.default_rng(seed)
+    total_rows = case.total_q * case.num_qo_heads
+    rows = np.sort(rng.choice(total_rows, size=min(budget_rows, total_rows), replace=False))
+    qi = case.q_indptr.cpu().numpy()
+    flops = 0
+    for r in rows:
+        t = r // case.num_qo_heads
+        b = int(np.searchsorted(qi, t, side="right") - 1)
+        i = t - qi[b]
+        qo, kv = case.qo_lens[b], case.kv_lens[b]
+        n = kv if not case.causal else min(kv, max(0, i + kv - qo + 1))
+        flops += 4 * case.head_dim * n
+    return rows.astype(np.int64), flops
+
+
+def run_oracle_sample(case, host, rows):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.ragged_attention(host["q"], host["k"], host["v"], host["qi"], host["ki"],
+                            case.num_qo_heads, case.num_kv_heads, case.causal, case.sm_scale,
+                            rows=rows)
+    return time.perf_counter() - t0
+
+
+def host_copies(case):
+    return {"q": case.q.cpu(), "k": case.k.cpu(), "v": case.v.cpu(),
+            "qi": case.q_indptr.cpu(), "ki": case.kv_indptr.cpu()}
+
+
+# ------------------------------------------------------------------ main arms
+def bench_reference(args, ws, rank):
+    """The float64 oracle, timed on the host cores, on a row sample per step."""
+    if rank != 0:
+        return 0
+    import oracle
+    from paged_gqa_attention_varlen_gb300 import workloads as W
+    case = W.config(PREFILL_WORKLOAD, device="cpu")
+    host = host_copies(case)
+    rows, flops = oracle_sample_prefill(case, args.ref_rows, seed=1)
+    for _ in range(args.warmup):
+        run_oracle_sample(case, host, rows[: max(1, len(rows) // 8)])
+    times = [run_oracle_sample(case, host, rows) for _ in range(args.steps)]
+    total = sum(times)
+    value = flops * args.steps / total / 1e12
+    sample = (f"{len(rows)} random (token, head) rows of the {PREFILL_WORKLOAD} workload per "
+              f"step ({flops / 1e9:.2f} GFLOP of visible pairs)")
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": PREFILL_WORKLOAD, "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def bench_gpu(args, ws, rank, local):
+    from paged_gqa_attention_varlen_gb300 import api
+    from paged_gqa_attention_varlen_gb300 import workloads as W
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peaks = load_peaks()
+    traffic = load_traffic()
+
+    pf = W.config(PREFILL_WORKLOAD, device=dev)
+    dc = W.config(DECODE_WORKLOAD, device=dev)
+    pf_flops = prefill_flops(pf.qo_lens, pf.kv_lens, pf.num_qo_heads, pf.head_dim)
+    dc_bytes = decode_kv_bytes(dc.kv_lens, dc.num_kv_heads, dc.head_dim)
+    o_pf = torch.empty_like(pf.q)
+    l_pf = torch.empty(pf.q.shape[:2], dtype=torch.float32, device=dev)
+    o_dc = torch.empty_like(dc.q)
+    l_dc = torch.empty(dc.q.shape[:2], dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def prefill():
+        api.ragged_prefill(pf.q, pf.k, pf.v, pf.q_indptr, pf.kv_indptr, causal=True,
+                           sm_scale=pf.sm_scale, out=o_pf, lse=l_pf, stream=stream)
+
+    def decode():
+        api.paged_decode(dc.q, dc.k_pages, dc.v_pages, dc.page_table, dc.kv_lens_t,
+                         sm_scale=dc.sm_scale, out=o_dc, lse=l_dc, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        prefill()
+        decode()
+    torch.cuda.synchronize(dev)
+    if api.device_status() != 0:
+        raise RuntimeError("device status after warm-up is not ok")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    barrier(dev)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)  # let the sampler start before the timed region
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_begin.record(stream)
+    for s in range(args.steps):
+        ev[s][0].record(stream)
+        prefill()
+        ev[s][1].record(stream)
+        decode()
+        ev[s][2].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(dev)
+    clk = clocks.stop()
+    total_ms = reduce_max(t_begin.elapsed_time(t_end), dev)
+    pf_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    dc_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    pf_total = reduce_max(sum(pf_ms), dev)
+    dc_total = reduce_max(sum(dc_ms), dev)
+    status = api.device_status()
+
+    value = pf_flops * ws * args.steps / (pf_total / 1e3) / 1e12
+    dc_gbs = dc_bytes * ws * args.steps / (dc_total / 1e3) / 1e9
+    pf_launch_ms = pf_total / args.steps
+    dc_launch_ms = dc_total / args.steps
+    pf_achieved = pf_flops / (pf_launch_ms / 1e3) / 1e12
+    dc_achieved = dc_bytes / (dc_launch_ms / 1e3) / 1e9
+
+    # end to end: pinned host inputs copied in and outputs copied out every step
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    hq = {k: v.cpu().pin_memory() for k, v in
+          (("q", pf.q), ("k", pf.k), ("v", pf.v), ("qi", pf.q_indptr), ("ki", pf.kv_indptr))}
+    ho = torch.empty(o_pf.shape, dtype=o_pf.dtype).pin_memory()
+    hl = torch.empty(l_pf.shape, dtype=l_pf.dtype).pin_memory()
+    dq = {k: torch.empty_like(v, device=dev) for k, v in hq.items()}
+    h2d = sum(v.numel() * v.element_size() for v in hq.values())
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for k in hq:
+            dq[k].copy_(hq[k], non_blocking=True)
+        api.ragged_prefill(dq["q"], dq["k"], dq["v"], dq["qi"], dq["ki"], causal=True,
+                           sm_scale=pf.sm_scale, out=o_pf, lse=l_pf, stream=stream)
+        ho.copy_(o_pf, non_blocking=True)
+        hl.copy_(l_pf, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = reduce_max(e0.elapsed_time(e1), dev)
+    e2e_value = pf_flops * ws * e2e_steps / (e2e_ms / 1e3) / 1e12
+
+    # decode end to end: per-step inputs (q, page table, lengths) in, output out; the
+    # paged KV cache is serving state that stays resident in HBM
+    dh = {k: v.cpu().pin_memory() for k, v in
+          (("q", dc.q), ("pt", dc.page_table), ("kl", dc.kv_lens_t))}
+    dd = {k: torch.empty_like(v, device=dev) for k, v in dh.items()}
+    dho = torch.empty(o_dc.shape, dtype=o_dc.dtype).pin_memory()
+    dhl = torch.empty(l_dc.shape, dtype=l_dc.dtype).pin_memory()
+    d_h2d = sum(v.numel() * v.element_size() for v in dh.values())
+    d_d2h = dho.numel() * dho.element_size() + dhl.numel() * dhl.element_size()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for k in dh:
+            dd[k].copy_(dh[k], non_blocking=True)
+        api.paged_decode(dd["q"], dc.k_pages, dc.v_pages, dd["pt"], dd["kl"],
+                         sm_scale=dc.sm_scale, out=o_dc, lse=l_dc, stream=stream)
+        dho.copy_(o_dc, non_blocking=True)
+        dhl.copy_(l_dc, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    d_e2e_ms = reduce_max(e0.elapsed_time(e1), dev)
+    d_e2e_value = dc_bytes * ws * e2e_steps / (d_e2e_ms / 1e3) / 1e9
+
+    if rank != 0:
+        return 0
+
+    # CPU baseline: the oracle on a bounded row sample of the same prefill workload
+    cpu = None
+    if not args.no_cpu_baseline and ws == 1:
+        import oracle
+        case_h = W.RaggedCase(pf.name, pf.q, pf.k, pf.v, pf.q_indptr.cpu(), pf.kv_indptr.cpu(),
+                              pf.qo_lens, pf.kv_lens, pf.num_qo_heads, pf.num_kv_heads,
+                              pf.head_dim, True, pf.sm_scale)
+        host = host_copies(case_h)
+        rows, flops = oracle_sample_prefill(case_h, args.cpu_rows, seed=1)
+        secs = run_oracle_sample(case_h, host, rows)
+        cpu = {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": oracle.threads(),
+               "kind": "oracle",
+               "sample": f"{len(rows)} random (token, head) rows of {PREFILL_WORKLOAD} "
+                         f"({flops / 1e9:.2f} GFLOP, {secs:.1f} s)"}
+
+    pf_tr = traffic.get("prefill_attention")
+    dc_tr = traffic.get("decode")
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"{PREFILL_WORKLOAD} + {DECODE_WORKLOAD}",
+                   "prefill": {"batch": pf.batch, "total_q": pf.total_q,
+                               "num_qo_heads": pf.num_qo_heads, "num_kv_heads": pf.num_kv_heads,
+                               "head_dim": pf.head_dim, "causal": True,
+                               "flops": pf_flops},
+                   "decode": {"batch": dc.batch, "sum_kv": int(sum(dc.kv_lens)),
+                              "page_size": dc.page_size, "num_qo_heads": dc.num_qo_heads,
+                              "num_kv_heads": dc.num_kv_heads, "head_dim": dc.head_dim,
+                              "kv_bytes": dc_bytes},
+                   "l2": "inputs larger than L2 (0.42 GB prefill, 17.4 GB decode), no flush"},
+        "roofline": {"bound": "tensor", "kernel": "prefill (plan + attention launch pair)",
+                     "achieved": pf_achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": pf_achieved / peaks["bf16_tflops"],
+                     "peak_source": peaks["source"] + " burst bf16",
+                     "traffic": pf_tr},
+        "secondary": {
+            "metric": "paged decode KV GB/s", "value": dc_gbs, "unit": "GB/s",
+            "ms_per_launch": dc_launch_ms,
+            "roofline": {"bound": "hbm", "kernel": "decode (plan + split-KV + merge)",
+                         "achieved": dc_achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": dc_achieved / peaks["hbm_gbs"],
+                         "peak_source": peaks["source"] + " copy bandwidth",
+                         "traffic": dc_tr},
+            "e2e": {"value": d_e2e_value, "unit": "GB/s", "h2d_bytes_per_step": d_h2d,
+                    "d2h_bytes_per_step": d_d2h,
+                    "note": "KV cache resident (serving state); q, page table, lengths in"}},
+        "prefill_ms_per_launch": pf_launch_ms,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": args.steps * (2 + 3),
+        "clocks": clk,
+        "device_status": status,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--ref-rows", type=int, default=3000,
+                    help="oracle rows per CPU-baseline / reference step")
+    ap.add_argument("--cpu-rows", type=int, default=150000,
+                    help="oracle rows timed for the cpu_baseline object (about 10-30 s)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        return bench_reference(args, ws, rank)
+    init_dist(ws, "nccl")
+    try:
+        return bench_gpu(args, ws, rank, local)
+    finally:
+        if torch.distributed.is_available() and torch.distributed.is_initialized():
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,178 @@
+/*
+ * pgqa.h -- C ABI of libpgqa: ragged (varlen) GQA prefill and paged GQA decode on
+ * GB300 (sm_103a).
+ *
+ * Every entry point takes plain device pointers, sizes and a CUDA stream; no C++ or
+ * framework types cross this boundary and nothing is thrown.  All calls are
+ * asynchronous on `stream`: they enqueue kernels and return a status code without
+ * synchronising.  Argument checks that need no device data happen on the host and
+ * return an error before anything is enqueued; checks of device-resident data
+ * (indptr arrays, page ids) happen in the kernels, which record failures in a device
+ * status word that pgqa_get_device_status() reads.
+ *
+ * Conventions shared by all calls
+ *   - bf16 tensors are contiguous, row-major, NHD ("token, head, dim") and 16-byte
+ *     aligned.  Element [t, h, c] of a [T, H, D] tensor is at ((t * H) + h) * D + c.
+ *   - Query head h reads KV head h / (num_qo_heads / num_kv_heads): consecutive query
+ *     heads share a KV head (grouped-query attention).
+ *   - lse is the natural-log log-sum-exp of the *scaled* scores of each output row,
+ *     lse = ln sum_j exp(sm_scale * q.k_j), in fp32.  A row with no visible key gets
+ *     an output of exact zeros and lse = -inf.  lse may be NULL (not written).
+ *   - The caller owns every tensor.  The library owns only its workspace (below).
+ *   - Calls that share a workspace must be ordered (same stream, or synchronised):
+ *     two in flight at once race on it.
+ *
+ * Sources (restated): Atlas "Module flashinfer" API page (ragged_prefill_bf16_hd128,
+ * ragged_prefill_bf16_hd256: one varlen launch over q_indptr / kv_indptr, bf16, GQA,
+ * causal selectable; callers pass device pointers plus a cudaStream_t);
+ * vllm-rlt pull request "feat: add FlashInfer attention backend for SM120 decode"
+ * (Scope and Design notes: paged NHD decode, block size 16, empty batch returns early,
+ * padding in the block table is never visible, lazily allocated kernel workspace);
+ * FlashInfer documentation (flashinfer_benchmark.py Attention Flags: bottom-right
+ * causal masking; flashinfer.cascade "Merge Attention States": merging partial
+ * (output, lse) pairs, used by the split-KV decode).
+ */
+#ifndef PGQA_H_
+#define PGQA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ABI-compatible with cudaStream_t / CUstream (NULL = the legacy default stream). */
+typedef struct CUstream_st* pgqa_stream_t;
+
+/* Status codes returned by every call (0 = success). */
+enum {
+    PGQA_OK = 0,
+    PGQA_ERR_INVALID_ARG = -1,    /* NULL pointer, negative size, misaligned tensor */
+    PGQA_ERR_UNSUPPORTED = -2,    /* shape outside the supported set (see each call) */
+    PGQA_ERR_WORKSPACE = -3,      /* workspace too small and allocation not allowed */
+    PGQA_ERR_CUDA = -4,           /* a CUDA runtime/driver call failed */
+    PGQA_ERR_DEVICE_TIMEOUT = -5, /* a kernel's bounded wait expired (device status) */
+    PGQA_ERR_DEVICE_BOUNDS = -6,  /* bad indptr / page id seen on the device */
+    PGQA_ERR_NO_DEVICE = -7       /* no usable sm_103 GPU for this call */
+};
+
+/*
+ * Ragged (varlen) batched prefill attention in one launch.
+ *
+ * Defined by: Atlas "Module flashinfer" API page, functions ragged_prefill_bf16_hd128 and
+ * ragged_prefill_bf16_hd256 (batched varlen prefill over q_indptr / kv_indptr offsets);
+ * causal alignment from FlashInfer documentation, flashinfer_benchmark.py "Attention
+ * Flags" (--causal, bottom-right masking).
+ *
+ *   q  [total_q, num_qo_heads, head_dim]  bf16, device     (read)
+ *   k  [total_kv, num_kv_heads, head_dim] bf16, device     (read)
+ *   v  [total_kv, num_kv_heads, head_dim] bf16, device     (read)
+ *   o  [total_q, num_qo_heads, head_dim]  bf16, device     (written, rows of requests)
+ *   lse [total_q, num_qo_heads]           fp32, device or NULL (written)
+ *   q_indptr, kv_indptr [batch + 1] int32, device: request b owns query rows
+ *       q_indptr[b] .. q_indptr[b+1]-1 and key rows kv_indptr[b] .. kv_indptr[b+1]-1.
+ *       Both must be non-decreasing and non-negative; total_q = q_indptr[batch] and
+ *       total_kv = kv_indptr[batch] are read on the device, never on the host.
+ *   causal != 0: query row i of a request (0-based) sees key j iff
+ *       j <= i + kv_len - qo_len  (bottom-right aligned); else every key of its request.
+ *   sm_scale: scores are sm_scale * q.k (any finite value, 0 allowed).
+ *
+ * Supported: head_dim 128 or 256; num_qo_heads a multiple of num_kv_heads with group
+ * size G = num_qo_heads / num_kv_heads dividing 128.  batch == 0 returns PGQA_OK at once.
+ * Errors: PGQA_ERR_INVALID_ARG for NULL/misaligned pointers or bad counts,
+ * PGQA_ERR_UNSUPPORTED for other shapes, PGQA_ERR_WORKSPACE if the workspace is too
+ * small while the stream is being captured, PGQA_ERR_CUDA on a launch failure.  A
+ * decreasing or negative indptr is reported later as PGQA_ERR_DEVICE_BOUNDS by
+ * pgqa_get_device_status() and nothing is written.
+ */
+int pgqa_ragged_prefill_bf16(const void* q, const void* k, const void* v, void* o, float* lse,
+                             const int32_t* q_indptr, const int32_t* kv_indptr, int batch,
+                             int num_qo_heads, int num_kv_heads, int head_dim, int causal,
+                             float sm_scale, pgqa_stream_t stream);
+
+/*
+ * Paged decode: one query row per request over a paged NHD KV cache, split along the
+ * keys (split-KV) with the partial results merged by log-sum-exp weights.
+ *
+ * Defined by: vllm-rlt pull request "feat: add FlashInfer attention backend for SM120
+ * decode" (Scope: paged decode; Design notes: block tables with -1 / zero / stale
+ * padding stay invisible, kv_layout "NHD", empty batch returns early) and FlashInfer
+ * documentation, flashinfer.decode (BatchDecodeWithPagedKVCacheWrapper) and
+ * flashinfer.cascade "Merge Attention States" (the split-KV merge).
+ *
+ *   q       [batch, num_qo_heads, head_dim]                 bf16, device (read)
+ *   k_pages [num_pages, page_size, num_kv_heads, head_dim]  bf16, device (read)
+ *   v_pages [num_pages, page_size, num_kv_heads, head_dim]  bf16, device (read)
+ *   page_table [batch, page_table_stride] int32, device: key j of request b is slot
+ *       j % page_size of page page_table[b * page_table_stride + j / page_size].
+ *       Entries at index >= ceil(kv_lens[b] / page_size) are never read.
+ *   kv_lens [batch] int32, device: 0 <= kv_lens[b] <= page_table_stride * page_size.
+ *   o   [batch, num_qo_heads, head_dim] bf16, device (written)
+ *   lse [batch, num_qo_heads] fp32, device or NULL (written)
+ *   Key slots past kv_lens[b] in a request's last page are never read, so whatever
+ *   they hold (even NaN) cannot reach the output.
+ *
+ * Supported: head_dim 128; page_size 16; G = num_qo_heads / num_kv_heads in {1,2,4,8}.
+ * Errors as for pgqa_ragged_prefill_bf16; a page id outside 0..num_pages-1 or a
+ * kv_len outside its range is reported as PGQA_ERR_DEVICE_BOUNDS by
+ * pgqa_get_device_status(), and the affected request's keys are skipped.
+ */
+int pgqa_paged_decode_bf16(const void* q, const void* k_pages, const void* v_pages,
+                           const int32_t* page_table, const int32_t* kv_lens, int page_size,
+                           int page_table_stride, int num_pages, void* o, float* lse,
+                           int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                           float sm_scale, pgqa_stream_t stream);
+
+/* Same calls under the short names used by serving integrations. */
+int ragged_prefill_bf16(const void* q, const void* k, const void* v, void* o, float* lse,
+                        const int32_t* q_indptr, const int32_t* kv_indptr, int batch,
+                        int num_qo_heads, int num_kv_heads, int head_dim, int causal,
+                        float sm_scale, pgqa_stream_t stream);
+int paged_decode_bf16(const void* q, const void* k_pages, const void* v_pages,
+                      const int32_t* page_table, const int32_t* kv_lens, int page_size,
+                      int page_table_stride, int num_pages, void* o, float* lse, int batch,
+                      int num_qo_heads, int num_kv_heads, int head_dim, float sm_scale,
+                      pgqa_stream_t stream);
+
+/*
+ * Workspace.  Both calls need device scratch: the prefill for its work list and tensor
+ * maps, the decode for its split-KV partial results.  Unless the caller supplies one,
+ * the library allocates it lazily on the first call that needs it (per device; 128 MiB
+ * or more if the call needs more) and grows it when a call needs more -- except while
+ * `stream` is being captured into a CUDA graph, where it returns PGQA_ERR_WORKSPACE
+ * instead of allocating (run one call before capturing, as with the pages' lazily
+ * allocated 128 MiB workspace: vllm-rlt PR, Design notes).
+ *
+ * pgqa_set_workspace: use caller-owned device memory `ptr` of `bytes` bytes (256-byte
+ *   aligned) on the current device from now on; the library frees its own buffer.
+ *   ptr == NULL drops a caller buffer and returns to lazy allocation.  The buffer must
+ *   stay valid until replaced and must not be used by anything else meanwhile.
+ * pgqa_workspace_bytes_*: upper bound of the bytes a call with these sizes needs.
+ *   For the prefill, max_total_q bounds q_indptr[batch].
+ */
+int pgqa_set_workspace(void* ptr, size_t bytes);
+size_t pgqa_workspace_bytes_prefill(int batch, int64_t max_total_q, int num_qo_heads,
+                                    int num_kv_heads);
+size_t pgqa_workspace_bytes_decode(int batch, int page_table_stride, int page_size,
+                                   int num_qo_heads, int head_dim);
+
+/*
+ * Device status: synchronises `stream`, returns the first error the kernels recorded on
+ * the current device since the last call (PGQA_OK, PGQA_ERR_DEVICE_TIMEOUT,
+ * PGQA_ERR_DEVICE_BOUNDS) and clears it.  Returns PGQA_ERR_CUDA if the stream itself
+ * reports an error.
+ */
+int pgqa_get_device_status(pgqa_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char* pgqa_status_string(int status);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int pgqa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PGQA_H_ */

@@ -1,0 +1,196 @@
+"""Python binding of libpgqa (include/pgqa.h): argument marshalling only.
+
+Every step of the attention path runs in the CUDA library; this module checks tensor
+dtypes/shapes/devices, allocates outputs with torch, and passes raw pointers and the
+current CUDA stream through ctypes.  There is no fallback: if the library is missing
+or cannot be loaded, importing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+from pathlib import Path
+
+import torch
+
+from . import build as _build
+
+_LIB_PATH = _build.LIB
+
+PGQA_OK = 0
+STATUS_NAMES = {
+    0: "ok", -1: "invalid argument", -2: "unsupported shape", -3: "workspace",
+    -4: "CUDA error", -5: "device timeout", -6: "device bounds", -7: "no device",
+}
+
+ABI_FUNCTIONS = (
+    "pgqa_ragged_prefill_bf16", "pgqa_paged_decode_bf16", "ragged_prefill_bf16",
+    "paged_decode_bf16", "pgqa_set_workspace", "pgqa_workspace_bytes_prefill",
+    "pgqa_workspace_bytes_decode", "pgqa_get_device_status", "pgqa_status_string",
+    "pgqa_version",
+)
+
+
+class PgqaError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: status {code} ({STATUS_NAMES.get(code, 'unknown')})")
+        self.code = code
+
+
+def _load(path: Path):
+    if not path.exists():
+        raise ImportError(
+            f"libpgqa not built ({path} missing): run `python -c \"import __graft_entry__ as g; "
+            f"g.build()\"` first; there is no CPU fallback")
+    lib = ctypes.CDLL(str(path))
+    p, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    sz, i64 = ctypes.c_size_t, ctypes.c_int64
+    prefill_args = [p, p, p, p, p, p, p, i, i, i, i, i, f, p]
+    decode_args = [p, p, p, p, p, i, i, i, p, p, i, i, i, i, f, p]
+    for name in ("pgqa_ragged_prefill_bf16", "ragged_prefill_bf16"):
+        fn = getattr(lib, name)
+        fn.argtypes, fn.restype = prefill_args, i
+    for name in ("pgqa_paged_decode_bf16", "paged_decode_bf16"):
+        fn = getattr(lib, name)
+        fn.argtypes, fn.restype = decode_args, i
+    lib.pgqa_set_workspace.argtypes, lib.pgqa_set_workspace.restype = [p, sz], i
+    lib.pgqa_workspace_bytes_prefill.argtypes = [i, i64, i, i]
+    lib.pgqa_workspace_bytes_prefill.restype = sz
+    lib.pgqa_workspace_bytes_decode.argtypes = [i, i, i, i, i]
+    lib.pgqa_workspace_bytes_decode.restype = sz
+    lib.pgqa_get_device_status.argtypes, lib.pgqa_get_device_status.restype = [p], i
+    lib.pgqa_status_string.argtypes, lib.pgqa_status_string.restype = [i], ctypes.c_char_p
+    lib.pgqa_version.argtypes, lib.pgqa_version.restype = [], i
+    return lib
+
+
+lib = _load(_LIB_PATH)
+
+
+def library_path() -> str:
+    return str(_LIB_PATH)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(t, name, dtype, dim=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dim is not None and t.dim() != dim:
+        raise ValueError(f"{name} must have {dim} dims, got {t.dim()}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def ragged_prefill(q, k, v, q_indptr, kv_indptr, causal=True, sm_scale=None, out=None,
+                   lse=None, return_lse=True, stream=None):
+    """Ragged batched prefill (pgqa_ragged_prefill_bf16).
+
+    q [total_q, Hq, d], k/v [total_kv, Hk, d] bf16 on one CUDA device; q_indptr /
+    kv_indptr [batch + 1] int32 on the same device.  Returns (o, lse) with
+    o [total_q, Hq, d] bf16 and lse [total_q, Hq] fp32 (None if return_lse is False).
+    """
+    dev = q.device
+    _check(q, "q", torch.bfloat16, 3, dev)
+    _check(k, "k", torch.bfloat16, 3, dev)
+    _check(v, "v", torch.bfloat16, 3, dev)
+    _check(q_indptr, "q_indptr", torch.int32, 1, dev)
+    _check(kv_indptr, "kv_indptr", torch.int32, 1, dev)
+    total_q, hq, d = q.shape
+    hk = k.shape[1]
+    if k.shape != v.shape or k.shape[2] != d:
+        raise ValueError("k and v must be [total_kv, Hk, d] with q's d")
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    _check(out, "out", torch.bfloat16, 3, dev)
+    if lse is None and return_lse:
+        lse = torch.empty((total_q, hq), dtype=torch.float32, device=dev)
+    if lse is not None:
+        _check(lse, "lse", torch.float32, 2, dev)
+    batch = q_indptr.numel() - 1
+    rc = lib.pgqa_ragged_prefill_bf16(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                                      _ptr(q_indptr), _ptr(kv_indptr), batch, hq, hk, d,
+                                      int(bool(causal)), float(sm_scale), _stream(stream))
+    if rc != PGQA_OK:
+        raise PgqaError(rc, "pgqa_ragged_prefill_bf16")
+    return out, lse
+
+
+def paged_decode(q, k_pages, v_pages, page_table, kv_lens, sm_scale=None, out=None, lse=None,
+                 return_lse=True, stream=None):
+    """Paged decode (pgqa_paged_decode_bf16).
+
+    q [batch, Hq, d]; k_pages / v_pages [num_pages, page_size, Hk, d] bf16;
+    page_table [batch, stride] int32; kv_lens [batch] int32; all on one CUDA device.
+    Returns (o [batch, Hq, d] bf16, lse [batch, Hq] fp32 or None).
+    """
+    dev = q.device
+    _check(q, "q", torch.bfloat16, 3, dev)
+    _check(k_pages, "k_pages", torch.bfloat16, 4, dev)
+    _check(v_pages, "v_pages", torch.bfloat16, 4, dev)
+    _check(page_table, "page_table", torch.int32, 2, dev)
+    _check(kv_lens, "kv_lens", torch.int32, 1, dev)
+    batch, hq, d = q.shape
+    num_pages, page_size, hk, dk = k_pages.shape
+    if v_pages.shape != k_pages.shape or dk != d:
+        raise ValueError("k_pages / v_pages must be [num_pages, page_size, Hk, d]")
+    if page_table.shape[0] != batch or kv_lens.numel() != batch:
+        raise ValueError("page_table / kv_lens must have one row per request")
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    _check(out, "out", torch.bfloat16, 3, dev)
+    if lse is None and return_lse:
+        lse = torch.empty((batch, hq), dtype=torch.float32, device=dev)
+    if lse is not None:
+        _check(lse, "lse", torch.float32, 2, dev)
+    rc = lib.pgqa_paged_decode_bf16(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table),
+                                    _ptr(kv_lens), page_size, page_table.shape[1], num_pages,
+                                    _ptr(out), _ptr(lse), batch, hq, hk, d, float(sm_scale),
+                                    _stream(stream))
+    if rc != PGQA_OK:
+        raise PgqaError(rc, "pgqa_paged_decode_bf16")
+    return out, lse
+
+
+def device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status code."""
+    return lib.pgqa_get_device_status(_stream(stream))
+
+
+def set_workspace(buf: torch.Tensor | None):
+    """Use a caller-owned uint8 CUDA tensor as the workspace (None: back to lazy)."""
+    if buf is None:
+        rc = lib.pgqa_set_workspace(None, 0)
+    else:
+        if buf.dtype != torch.uint8 or not buf.is_cuda or not buf.is_contiguous():
+            raise ValueError("workspace must be a contiguous uint8 CUDA tensor")
+        rc = lib.pgqa_set_workspace(_ptr(buf), buf.numel())
+    if rc != PGQA_OK:
+        raise PgqaError(rc, "pgqa_set_workspace")
+
+
+def workspace_bytes_decode(batch, page_table_stride, page_size, num_qo_heads, head_dim):
+    return lib.pgqa_workspace_bytes_decode(batch, page_table_stride, page_size, num_qo_heads,
+                                           head_dim)
+
+
+def workspace_bytes_prefill(batch, max_total_q, num_qo_heads, num_kv_heads):
+    return lib.pgqa_workspace_bytes_prefill(batch, max_total_q, num_qo_heads, num_kv_heads)

@@ -1,0 +1,435 @@
+// api.cu -- the C ABI of libpgqa (declared in include/pgqa.h): argument checks,
+// per-device workspace, TMA tensor-map templates, and the kernel launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/pgqa.h"
+#include "internal.h"
+
+namespace pgqa {
+namespace prefill {
+cudaError_t launch_plan(const PlanParams&, const CUtensorMap&, const CUtensorMap&,
+                        const CUtensorMap&, cudaStream_t);
+template <int D>
+cudaError_t launch_attention(const Params&, int, cudaStream_t);
+}  // namespace prefill
+namespace decode {
+cudaError_t launch_plan(const PlanParams&, cudaStream_t);
+cudaError_t launch_decode(const Params&, int group, int num_sms, cudaStream_t);
+cudaError_t launch_merge(const Params&, cudaStream_t);
+}  // namespace decode
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool probed = false;
+    bool supported = false;
+    int num_sms = 0;
+    void* ws = nullptr;
+    size_t ws_bytes = 0;
+    bool ws_owned = false;
+};
+
+std::mutex g_mutex;
+DeviceState g_dev[kMaxDevices];
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+int map_cuda(cudaError_t e) { return e == cudaSuccess ? PGQA_OK : PGQA_ERR_CUDA; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Current device, its properties (cached) and whether it is an sm_103 part.
+int current_device(int* dev_out, DeviceState** st_out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return PGQA_ERR_NO_DEVICE;
+    }
+    DeviceState& st = g_dev[dev];
+    if (!st.probed) {
+        cudaDeviceProp prop;
+        if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return PGQA_ERR_NO_DEVICE;
+        }
+        st.supported = prop.major == 10 && prop.minor == 3;
+        st.num_sms = prop.multiProcessorCount;
+        st.probed = true;
+    }
+    if (!st.supported) return PGQA_ERR_NO_DEVICE;
+    *dev_out = dev;
+    *st_out = &st;
+    return PGQA_OK;
+}
+
+int get_encoder() {
+    if (g_encode) return PGQA_OK;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr) {
+        cudaGetLastError();
+        return PGQA_ERR_CUDA;
+    }
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    return PGQA_OK;
+}
+
+// Make sure the device workspace holds at least `need` bytes.  Allocation happens only
+// outside stream capture; a fresh buffer starts with a cleared header.
+int ensure_workspace(DeviceState& st, size_t need, cudaStream_t stream) {
+    if (st.ws != nullptr && st.ws_bytes >= need) return PGQA_OK;
+    if (st.ws != nullptr && !st.ws_owned) return PGQA_ERR_WORKSPACE;  // caller buffer too small
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return PGQA_ERR_CUDA;
+    }
+    if (cs != cudaStreamCaptureStatusNone) return PGQA_ERR_WORKSPACE;
+    size_t bytes = need > kDefaultWorkspace ? align_up(need, 1u << 20) : kDefaultWorkspace;
+    if (st.ws != nullptr) {
+        cudaFree(st.ws);  // synchronises the device: no kernel still uses the old buffer
+        st.ws = nullptr;
+        st.ws_bytes = 0;
+    }
+    void* p = nullptr;
+    if (cudaMalloc(&p, bytes) != cudaSuccess) {
+        cudaGetLastError();
+        return PGQA_ERR_WORKSPACE;
+    }
+    if (cudaMemset(p, 0, kWsArrays) != cudaSuccess) {
+        cudaFree(p);
+        return PGQA_ERR_CUDA;
+    }
+    st.ws = p;
+    st.ws_bytes = bytes;
+    st.ws_owned = true;
+    return PGQA_OK;
+}
+
+int encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
+              uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows) {
+    const cuuint64_t dims[2] = {inner, rows};
+    const cuuint64_t strides[1] = {row_stride_bytes};
+    const cuuint32_t box[2] = {box_inner, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PGQA_OK : PGQA_ERR_INVALID_ARG;
+}
+
+int encode_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+              uint64_t s1_bytes, uint64_t s2_bytes, uint32_t b0, uint32_t b1, uint32_t b2) {
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {s1_bytes, s2_bytes};
+    const cuuint32_t box[3] = {b0, b1, b2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PGQA_OK : PGQA_ERR_INVALID_ARG;
+}
+
+size_t prefill_ws_bytes(int batch, long long max_items) {
+    const size_t tile_off = align_up((size_t)(batch + 1) * sizeof(int), 256);
+    return kWsArrays + tile_off + (size_t)max_items * sizeof(int4);
+}
+
+size_t decode_ws_bytes(int batch, int stride, int page_size, int hq, int d) {
+    const long long max_kv = (long long)stride * page_size;
+    const long long chunks_per_req =
+        max_kv > 0 ? (max_kv + decode::CHUNK - 1) / decode::CHUNK : 1;
+    const long long chunks = (long long)batch * chunks_per_req;
+    const size_t ints = align_up((size_t)(2 * batch + 1) * sizeof(int), 256);
+    return kWsArrays + ints + align_up((size_t)chunks * hq * sizeof(float), 256) +
+           (size_t)chunks * hq * d * sizeof(float);
+}
+
+}  // namespace
+}  // namespace pgqa
+
+using namespace pgqa;
+
+extern "C" {
+
+int pgqa_version(void) { return 10000; }
+
+const char* pgqa_status_string(int s) {
+    switch (s) {
+        case PGQA_OK: return "ok";
+        case PGQA_ERR_INVALID_ARG: return "invalid argument";
+        case PGQA_ERR_UNSUPPORTED: return "unsupported shape";
+        case PGQA_ERR_WORKSPACE: return "workspace too small (allocation not allowed)";
+        case PGQA_ERR_CUDA: return "CUDA error";
+        case PGQA_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+        case PGQA_ERR_DEVICE_BOUNDS: return "bad index data seen on the device";
+        case PGQA_ERR_NO_DEVICE: return "no usable sm_103 device";
+        default: return "unknown status";
+    }
+}
+
+size_t pgqa_workspace_bytes_prefill(int batch, int64_t max_total_q, int num_qo_heads,
+                                    int num_kv_heads) {
+    if (batch < 0 || max_total_q < 0 || num_kv_heads <= 0 || num_qo_heads <= 0) return 0;
+    const long long g = num_qo_heads / num_kv_heads;
+    const long long tiles = (max_total_q * g + prefill::BM - 1) / prefill::BM + batch;
+    return prefill_ws_bytes(batch, tiles * num_kv_heads);
+}
+
+size_t pgqa_workspace_bytes_decode(int batch, int page_table_stride, int page_size,
+                                   int num_qo_heads, int head_dim) {
+    if (batch < 0 || page_table_stride < 0 || page_size <= 0 || num_qo_heads <= 0 ||
+        head_dim <= 0)
+        return 0;
+    return decode_ws_bytes(batch, page_table_stride, page_size, num_qo_heads, head_dim);
+}
+
+int pgqa_set_workspace(void* ptr, size_t bytes) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return PGQA_ERR_NO_DEVICE;
+    }
+    DeviceState& st = g_dev[dev];
+    if (ptr != nullptr && ((reinterpret_cast<uintptr_t>(ptr) & 255u) != 0 || bytes < kWsArrays + 4096))
+        return PGQA_ERR_INVALID_ARG;
+    if (st.ws != nullptr && st.ws_owned) cudaFree(st.ws);
+    st.ws = nullptr;
+    st.ws_bytes = 0;
+    st.ws_owned = false;
+    if (ptr != nullptr) {
+        if (cudaMemset(ptr, 0, kWsArrays) != cudaSuccess) {
+            cudaGetLastError();
+            return PGQA_ERR_CUDA;
+        }
+        st.ws = ptr;
+        st.ws_bytes = bytes;
+    }
+    return PGQA_OK;
+}
+
+int pgqa_get_device_status(pgqa_stream_t stream) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return PGQA_ERR_CUDA;
+    }
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PGQA_ERR_NO_DEVICE;
+    DeviceState& st = g_dev[dev];
+    if (st.ws == nullptr) return PGQA_OK;
+    int word = 0;
+    if (cudaMemcpy(&word, st.ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return PGQA_ERR_CUDA;
+    }
+    if (word != 0) {
+        const int zero = 0;
+        cudaMemcpy(st.ws, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    }
+    if (word & PGQA_DEV_TIMEOUT) return PGQA_ERR_DEVICE_TIMEOUT;
+    if (word & (PGQA_DEV_BOUNDS | PGQA_DEV_CAPACITY)) return PGQA_ERR_DEVICE_BOUNDS;
+    return PGQA_OK;
+}
+
+int pgqa_ragged_prefill_bf16(const void* q, const void* k, const void* v, void* o, float* lse,
+                             const int32_t* q_indptr, const int32_t* kv_indptr, int batch,
+                             int num_qo_heads, int num_kv_heads, int head_dim, int causal,
+                             float sm_scale, pgqa_stream_t stream) {
+    if (batch < 0 || num_qo_heads <= 0 || num_kv_heads <= 0) return PGQA_ERR_INVALID_ARG;
+    if (batch == 0) return PGQA_OK;
+    if (!q || !k || !v || !o || !q_indptr || !kv_indptr) return PGQA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(q_indptr) & 3u) ||
+        (reinterpret_cast<uintptr_t>(kv_indptr) & 3u))
+        return PGQA_ERR_INVALID_ARG;
+    if (head_dim != 128 && head_dim != 256) return PGQA_ERR_UNSUPPORTED;
+    if (num_qo_heads % num_kv_heads != 0) return PGQA_ERR_UNSUPPORTED;
+    const int group = num_qo_heads / num_kv_heads;
+    if (group > prefill::BM || prefill::BM % group != 0) return PGQA_ERR_UNSUPPORTED;
+    if (!(sm_scale == sm_scale) || sm_scale > 3.0e38f || sm_scale < -3.0e38f)
+        return PGQA_ERR_INVALID_ARG;
+
+    std::lock_guard<std::mutex> lock(g_mutex);
+    int dev;
+    DeviceState* st;
+    int rc = current_device(&dev, &st);
+    if (rc != PGQA_OK) return rc;
+    if ((rc = get_encoder()) != PGQA_OK) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // at least room for the tile offsets and a work list; the plan kernel checks the
+    // list against what is there and reports overflow through the status word
+    rc = ensure_workspace(*st, prefill_ws_bytes(batch, 4096), s);
+    if (rc != PGQA_OK) return rc;
+
+    uint8_t* ws = static_cast<uint8_t*>(st->ws);
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(ws + kWsHeader);
+    CUtensorMap* tmaps = reinterpret_cast<CUtensorMap*>(ws + kWsTmapOffset);
+    int* tile_off = reinterpret_cast<int*>(ws + kWsArrays);
+    const size_t items_off = kWsArrays + align_up((size_t)(batch + 1) * sizeof(int), 256);
+    int4* items = reinterpret_cast<int4*>(ws + items_off);
+    const long long capacity = (long long)((st->ws_bytes - items_off) / sizeof(int4));
+
+    // Tensor-map templates: row extents are placeholders (one box), patched on the
+    // device from q_indptr[batch] / kv_indptr[batch] by the plan kernel.
+    CUtensorMap tq, tk, tv;
+    const uint32_t tpt = prefill::BM / group;
+    if ((rc = encode_3d(&tq, q, head_dim, num_qo_heads, tpt, (uint64_t)head_dim * 2,
+                        (uint64_t)num_qo_heads * head_dim * 2, 64, group, tpt)) != PGQA_OK)
+        return rc;
+    if ((rc = encode_2d(&tk, k, (uint64_t)num_kv_heads * head_dim, prefill::BN,
+                        (uint64_t)num_kv_heads * head_dim * 2, 64, prefill::BN)) != PGQA_OK)
+        return rc;
+    if ((rc = encode_2d(&tv, v, (uint64_t)num_kv_heads * head_dim, prefill::BN,
+                        (uint64_t)num_kv_heads * head_dim * 2, 64, prefill::BN)) != PGQA_OK)
+        return rc;
+
+    prefill::PlanParams pp;
+    pp.q_indptr = q_indptr;
+    pp.kv_indptr = kv_indptr;
+    pp.batch = batch;
+    pp.num_kv_heads = num_kv_heads;
+    pp.group = group;
+    pp.causal = causal ? 1 : 0;
+    pp.hdr = hdr;
+    pp.tile_off = tile_off;
+    pp.items = items;
+    pp.item_capacity = capacity;
+    pp.tm_out = tmaps;
+    cudaError_t e = prefill::launch_plan(pp, tq, tk, tv, s);
+    if (e != cudaSuccess) return PGQA_ERR_CUDA;
+
+    prefill::Params p;
+    p.tm_q = tmaps + 0;
+    p.tm_k = tmaps + 1;
+    p.tm_v = tmaps + 2;
+    p.o = o;
+    p.lse = lse;
+    p.q_indptr = q_indptr;
+    p.kv_indptr = kv_indptr;
+    p.items = items;
+    p.hdr = hdr;
+    p.status = &hdr->status;
+    p.num_qo_heads = num_qo_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.group = group;
+    p.causal = causal ? 1 : 0;
+    p.scale_log2 = sm_scale * 1.4426950408889634f;
+    e = head_dim == 128 ? prefill::launch_attention<128>(p, st->num_sms, s)
+                        : prefill::launch_attention<256>(p, st->num_sms, s);
+    return map_cuda(e);
+}
+
+int pgqa_paged_decode_bf16(const void* q, const void* k_pages, const void* v_pages,
+                           const int32_t* page_table, const int32_t* kv_lens, int page_size,
+                           int page_table_stride, int num_pages, void* o, float* lse,
+                           int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                           float sm_scale, pgqa_stream_t stream) {
+    if (batch < 0 || num_qo_heads <= 0 || num_kv_heads <= 0 || page_table_stride < 0 ||
+        num_pages < 0)
+        return PGQA_ERR_INVALID_ARG;
+    if (batch == 0) return PGQA_OK;
+    if (!q || !k_pages || !v_pages || !o || !kv_lens || (!page_table && page_table_stride > 0))
+        return PGQA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(page_table) & 3u) ||
+        (reinterpret_cast<uintptr_t>(kv_lens) & 3u))
+        return PGQA_ERR_INVALID_ARG;
+    if (head_dim != decode::HEAD_DIM || page_size != decode::PAGE) return PGQA_ERR_UNSUPPORTED;
+    if (num_qo_heads % num_kv_heads != 0) return PGQA_ERR_UNSUPPORTED;
+    const int group = num_qo_heads / num_kv_heads;
+    if (group != 1 && group != 2 && group != 4 && group != 8) return PGQA_ERR_UNSUPPORTED;
+    if (!(sm_scale == sm_scale) || sm_scale > 3.0e38f || sm_scale < -3.0e38f)
+        return PGQA_ERR_INVALID_ARG;
+    if ((long long)page_table_stride * page_size > 0x7fffffffLL) return PGQA_ERR_UNSUPPORTED;
+
+    std::lock_guard<std::mutex> lock(g_mutex);
+    int dev;
+    DeviceState* st;
+    int rc = current_device(&dev, &st);
+    if (rc != PGQA_OK) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const size_t need = decode_ws_bytes(batch, page_table_stride, page_size, num_qo_heads, head_dim);
+    rc = ensure_workspace(*st, need, s);
+    if (rc != PGQA_OK) return rc;
+
+    uint8_t* ws = static_cast<uint8_t*>(st->ws);
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(ws + kWsHeader);
+    int* chunk_off = reinterpret_cast<int*>(ws + kWsArrays);
+    int* kv_eff = chunk_off + (batch + 1);
+    const size_t lse_off = kWsArrays + align_up((size_t)(2 * batch + 1) * sizeof(int), 256);
+    const long long max_kv = (long long)page_table_stride * page_size;
+    const long long chunks =
+        (long long)batch * (max_kv > 0 ? (max_kv + decode::CHUNK - 1) / decode::CHUNK : 1);
+    float* part_lse = reinterpret_cast<float*>(ws + lse_off);
+    float* part_o = reinterpret_cast<float*>(
+        ws + lse_off + align_up((size_t)chunks * num_qo_heads * sizeof(float), 256));
+
+    decode::PlanParams pp;
+    pp.kv_lens = kv_lens;
+    pp.kv_eff = kv_eff;
+    pp.chunk_off = chunk_off;
+    pp.status = &hdr->status;
+    pp.batch = batch;
+    pp.max_kv = (int)max_kv;
+    cudaError_t e = decode::launch_plan(pp, s);
+    if (e != cudaSuccess) return PGQA_ERR_CUDA;
+
+    decode::Params p;
+    p.q = q;
+    p.k_pages = k_pages;
+    p.v_pages = v_pages;
+    p.page_table = page_table;
+    p.kv_eff = kv_eff;
+    p.chunk_off = chunk_off;
+    p.o = o;
+    p.lse = lse;
+    p.part_o = part_o;
+    p.part_lse = part_lse;
+    p.status = &hdr->status;
+    p.batch = batch;
+    p.page_table_stride = page_table_stride;
+    p.num_pages = num_pages;
+    p.num_qo_heads = num_qo_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.scale_log2 = sm_scale * 1.4426950408889634f;
+    p.chunk_capacity = chunks;
+    e = decode::launch_decode(p, group, st->num_sms, s);
+    if (e != cudaSuccess) return PGQA_ERR_CUDA;
+    return map_cuda(decode::launch_merge(p, s));
+}
+
+int ragged_prefill_bf16(const void* q, const void* k, const void* v, void* o, float* lse,
+                        const int32_t* q_indptr, const int32_t* kv_indptr, int batch,
+                        int num_qo_heads, int num_kv_heads, int head_dim, int causal,
+                        float sm_scale, pgqa_stream_t stream) {
+    return pgqa_ragged_prefill_bf16(q, k, v, o, lse, q_indptr, kv_indptr, batch, num_qo_heads,
+                                    num_kv_heads, head_dim, causal, sm_scale, stream);
+}
+
+int paged_decode_bf16(const void* q, const void* k_pages, const void* v_pages,
+                      const int32_t* page_table, const int32_t* kv_lens, int page_size,
+                      int page_table_stride, int num_pages, void* o, float* lse, int batch,
+                      int num_qo_heads, int num_kv_heads, int head_dim, float sm_scale,
+                      pgqa_stream_t stream) {
+    return pgqa_paged_decode_bf16(q, k_pages, v_pages, page_table, kv_lens, page_size,
+                                  page_table_stride, num_pages, o, lse, batch, num_qo_heads,
+                                  num_kv_heads, head_dim, sm_scale, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,118 @@
+// internal.h -- definitions shared by the host side and the kernels of libpgqa.
+#pragma once
+
+#include <cuda.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pgqa {
+
+// Device status word bits (first int of the workspace).
+constexpr int PGQA_DEV_TIMEOUT = 1;    // a bounded mbarrier wait expired
+constexpr int PGQA_DEV_BOUNDS = 2;     // bad indptr / kv_len / page id
+constexpr int PGQA_DEV_CAPACITY = 4;   // work list larger than the workspace
+
+constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s per wait
+
+// ------------------------------------------------------------------ workspace layout
+// [0, 256)      header: status word, counters
+// [256, 640)    three tensor maps (prefill Q, K, V), 128-byte aligned
+// [1024, ...)   per-call arrays (prefill: tile offsets + work items; decode: chunk
+//               offsets, sanitised kv lengths, partial results)
+constexpr size_t kWsHeader = 0;
+constexpr size_t kWsTmapOffset = 256;
+constexpr size_t kWsArrays = 1024;
+constexpr size_t kDefaultWorkspace = 128ull << 20;
+
+struct WsHeader {
+    int status;
+    int n_items;      // prefill: number of work items written by the plan
+    int total_q;
+    int total_kv;
+    int pad[60];
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ------------------------------------------------------------------ prefill
+namespace prefill {
+constexpr int BM = 128;          // packed query rows (token x group head) per tile
+constexpr int BN = 128;          // keys per K/V tile
+constexpr int THREADS = 256;     // warp 0 TMA, warp 1 MMA, warps 4-7 softmax/epilogue
+constexpr int PLAN_THREADS = 1024;
+constexpr int COST_BUCKETS = 4096;
+
+struct Params {
+    const CUtensorMap* tm_q;   // in the workspace, patched by the plan kernel
+    const CUtensorMap* tm_k;
+    const CUtensorMap* tm_v;
+    void* o;
+    float* lse;
+    const int* q_indptr;
+    const int* kv_indptr;
+    const int4* items;         // {request, kv head, q tile, kv tiles}
+    const WsHeader* hdr;
+    int* status;
+    int num_qo_heads;
+    int num_kv_heads;
+    int group;
+    int causal;
+    float scale_log2;          // sm_scale * log2(e)
+};
+
+struct PlanParams {
+    const int* q_indptr;
+    const int* kv_indptr;
+    int batch;
+    int num_kv_heads;
+    int group;
+    int causal;
+    WsHeader* hdr;
+    int* tile_off;             // [batch + 1]
+    int4* items;
+    long long item_capacity;
+    CUtensorMap* tm_out;       // 3 maps: Q, K, V
+};
+}  // namespace prefill
+
+// ------------------------------------------------------------------ decode
+namespace decode {
+constexpr int PAGE = 16;           // tokens per page
+constexpr int CHUNK = 1024;        // tokens per split-KV chunk (fixed: depends on nothing
+                                   // but the request, so results do not depend on the batch)
+constexpr int HEAD_DIM = 128;
+constexpr int WARPS = 4;           // warps per CTA, one work item per warp
+constexpr int PLAN_THREADS = 1024;
+
+struct Params {
+    const void* q;
+    const void* k_pages;
+    const void* v_pages;
+    const int* page_table;
+    const int* kv_eff;          // sanitised kv lengths [batch]
+    const int* chunk_off;       // [batch + 1]
+    void* o;
+    float* lse;
+    float* part_o;              // [total_chunks, Hq, D]
+    float* part_lse;            // [total_chunks, Hq]
+    int* status;
+    int batch;
+    int page_table_stride;
+    int num_pages;
+    int num_qo_heads;
+    int num_kv_heads;
+    float scale_log2;
+    long long chunk_capacity;
+};
+
+struct PlanParams {
+    const int* kv_lens;
+    int* kv_eff;
+    int* chunk_off;
+    int* status;
+    int batch;
+    int max_kv;                 // page_table_stride * page_size
+};
+}  // namespace decode
+
+}  // namespace pgqa

@@ -1,0 +1,584 @@
+// prefill.cu -- ragged (varlen) GQA prefill attention for sm_103a.
+//
+// What it computes: for every request b (query rows q_indptr[b]..q_indptr[b+1]-1, key
+// rows kv_indptr[b]..kv_indptr[b+1]-1), every query head h and query row i,
+//   o[i,h] = softmax_j(sm_scale * q[i,h] . k[j, h/G]) v[j, h/G]   over visible keys j,
+//   lse[i,h] = ln sum_j exp(sm_scale * q[i,h] . k[j, h/G]),
+// with key j visible iff j < kv_len and, when causal, j <= i + kv_len - qo_len
+// (bottom-right alignment).  Sources: Atlas "Module flashinfer" API page
+// (ragged_prefill_bf16_hd128 / _hd256: one batched varlen launch addressed by
+// q_indptr / kv_indptr); FlashInfer documentation, flashinfer_benchmark.py "Attention
+// Flags" (--causal, bottom-right masking).
+//
+// Design (GB300-first, not the SM80 mma.sync kernel the pages describe):
+//  * plan_kernel (1 CTA) validates the indptr arrays, turns them into a work list of
+//    (request, kv head, q tile) items sorted by their number of K/V tiles (longest
+//    first), and patches the global extents of the TMA tensor maps from
+//    q_indptr[batch] / kv_indptr[batch], so the host never reads device data.
+//  * attention_kernel is persistent (one CTA per SM) and warp-specialised:
+//      warp 0   TMA producer: Q tile once per item, then K/V tiles through a ring of
+//               shared-memory stages (mbarrier full/empty pairs);
+//      warp 1   tcgen05.mma issuer: S = Q K^T into tensor memory (two S buffers), then
+//               O += P V with P read straight from tensor memory;
+//      warps 4-7 softmax: one thread per packed query row (= TMEM lane): masking on the
+//               diagonal tiles only, online max / sum, P written back to TMEM as bf16,
+//               O rescaled in TMEM when the running max grows, then the epilogue.
+//  * GQA packing: a 128-row Q tile holds 128/G tokens x the G query heads that share a
+//    KV head (3-D TMA box), so each K/V tile is read once for all G heads.
+#include "ptx.cuh"
+
+namespace pgqa {
+namespace prefill {
+
+struct Geo {
+    int q_start, qo_len, kv_start, kv_len;
+    int t0;          // first token (within the request) of the item's q tile
+    int n_tiles;     // K/V tiles with at least one visible key for some row of the tile
+    int n_unmasked;  // leading tiles in which every row sees every key
+};
+
+__device__ __forceinline__ Geo item_geometry(const int* q_indptr, const int* kv_indptr, int b,
+                                             int qt, int group, int causal) {
+    Geo x;
+    x.q_start = q_indptr[b];
+    x.qo_len = q_indptr[b + 1] - x.q_start;
+    x.kv_start = kv_indptr[b];
+    x.kv_len = kv_indptr[b + 1] - x.kv_start;
+    const int tpt = BM / group;
+    x.t0 = qt * tpt;
+    const int t1 = min(x.qo_len, x.t0 + tpt);
+    int n_keys = x.kv_len;
+    if (causal) n_keys = max(0, min(x.kv_len, t1 + x.kv_len - x.qo_len));
+    x.n_tiles = (n_keys + BN - 1) / BN;
+    const int lim = causal ? min(x.t0 + x.kv_len - x.qo_len, x.kv_len - 1) : x.kv_len - 1;
+    x.n_unmasked = lim >= 0 ? min((lim + 1) / BN, x.n_tiles) : 0;
+    return x;
+}
+
+__device__ __forceinline__ int find_segment(const int* off, int n, int f) {
+    // largest b in [0, n) with off[b] <= f
+    int lo = 0, hi = n - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (off[mid] <= f) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+// ---------------------------------------------------------------------------- plan
+__global__ void __launch_bounds__(PLAN_THREADS)
+    plan_kernel(PlanParams p, const __grid_constant__ CUtensorMap tq,
+                const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv) {
+    __shared__ int hist[COST_BUCKETS];
+    __shared__ int scan[PLAN_THREADS];
+    __shared__ alignas(128) CUtensorMap smap[3];
+    const int tid = threadIdx.x;
+    const int nthr = blockDim.x;
+
+    int bad = 0;
+    for (int b = tid; b < p.batch; b += nthr) {
+        const int q0 = p.q_indptr[b], q1 = p.q_indptr[b + 1];
+        const int k0 = p.kv_indptr[b], k1 = p.kv_indptr[b + 1];
+        if (q0 < 0 || k0 < 0 || q1 < q0 || k1 < k0) bad = 1;
+    }
+    if (__syncthreads_or(bad)) {
+        if (tid == 0) {
+            atomicOr(&p.hdr->status, PGQA_DEV_BOUNDS);
+            p.hdr->n_items = 0;
+        }
+        return;
+    }
+
+    // exclusive scan of per-request q-tile counts -> tile_off
+    int running = 0;
+    for (int base = 0; base < p.batch; base += nthr) {
+        const int b = base + tid;
+        int cnt = 0;
+        if (b < p.batch) {
+            const long long qo = p.q_indptr[b + 1] - p.q_indptr[b];
+            cnt = (int)((qo * p.group + BM - 1) / BM);
+        }
+        scan[tid] = cnt;
+        __syncthreads();
+        for (int off = 1; off < nthr; off <<= 1) {
+            const int v = tid >= off ? scan[tid - off] : 0;
+            __syncthreads();
+            scan[tid] += v;
+            __syncthreads();
+        }
+        if (b < p.batch) p.tile_off[b] = running + scan[tid] - cnt;
+        running += scan[nthr - 1];
+        __syncthreads();
+    }
+    const int total_tiles = running;
+    const long long n_items = (long long)total_tiles * p.num_kv_heads;
+    if (tid == 0) p.tile_off[p.batch] = total_tiles;
+    if (n_items > p.item_capacity) {
+        if (tid == 0) {
+            atomicOr(&p.hdr->status, PGQA_DEV_CAPACITY);
+            p.hdr->n_items = 0;
+        }
+        return;
+    }
+    for (int i = tid; i < COST_BUCKETS; i += nthr) hist[i] = 0;
+    __syncthreads();
+
+    // histogram of item costs (K/V tiles per q tile)
+    for (int f = tid; f < total_tiles; f += nthr) {
+        const int b = find_segment(p.tile_off, p.batch, f);
+        const Geo x = item_geometry(p.q_indptr, p.kv_indptr, b, f - p.tile_off[b], p.group,
+                                    p.causal);
+        atomicAdd(&hist[min(x.n_tiles, COST_BUCKETS - 1)], 1);
+    }
+    __syncthreads();
+
+    // descending exclusive scan: start[c] = number of q tiles with a larger cost
+    constexpr int PER = COST_BUCKETS / PLAN_THREADS;
+    int local[PER];
+    int sum = 0;
+    if (tid < COST_BUCKETS / PER) {
+#pragma unroll
+        for (int e = 0; e < PER; ++e) {
+            local[e] = hist[COST_BUCKETS - 1 - (tid * PER + e)];
+            sum += local[e];
+        }
+    }
+    scan[tid] = sum;
+    __syncthreads();
+    for (int off = 1; off < nthr; off <<= 1) {
+        const int v = tid >= off ? scan[tid - off] : 0;
+        __syncthreads();
+        scan[tid] += v;
+        __syncthreads();
+    }
+    if (tid < COST_BUCKETS / PER) {
+        int acc = scan[tid] - sum;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) {
+            hist[COST_BUCKETS - 1 - (tid * PER + e)] = acc;
+            acc += local[e];
+        }
+    }
+    __syncthreads();
+
+    // scatter: the kv heads of one q tile take consecutive slots
+    for (int f = tid; f < total_tiles; f += nthr) {
+        const int b = find_segment(p.tile_off, p.batch, f);
+        const int qt = f - p.tile_off[b];
+        const Geo x = item_geometry(p.q_indptr, p.kv_indptr, b, qt, p.group, p.causal);
+        const int slot = atomicAdd(&hist[min(x.n_tiles, COST_BUCKETS - 1)], 1);
+        for (int g = 0; g < p.num_kv_heads; ++g)
+            p.items[(long long)slot * p.num_kv_heads + g] = make_int4(b, g, qt, x.n_tiles);
+    }
+
+    // tensor maps with the real row extents
+    if (tid < 32) {
+        const int total_q = p.q_indptr[p.batch];
+        const int total_kv = p.kv_indptr[p.batch];
+        if (tid == 0) {
+            smap[0] = tq;
+            smap[1] = tk;
+            smap[2] = tv;
+            tensormap_set_dim_smem<2>(smem_u32(&smap[0]), (uint32_t)max(total_q, 1));
+            tensormap_set_dim_smem<1>(smem_u32(&smap[1]), (uint32_t)max(total_kv, 1));
+            tensormap_set_dim_smem<1>(smem_u32(&smap[2]), (uint32_t)max(total_kv, 1));
+            p.hdr->n_items = (int)n_items;
+            p.hdr->total_q = total_q;
+            p.hdr->total_kv = total_kv;
+        }
+        __syncwarp();
+        tensormap_publish(p.tm_out + 0, smem_u32(&smap[0]));
+        tensormap_publish(p.tm_out + 1, smem_u32(&smap[1]));
+        tensormap_publish(p.tm_out + 2, smem_u32(&smap[2]));
+    }
+}
+
+// ---------------------------------------------------------------------- attention
+template <int D>
+struct Cfg {
+    static constexpr int CHUNKS = D / 64;              // 64-element (128-byte) swizzle chunks
+    static constexpr int CHUNK_BYTES = BM * 128;       // one chunk of a 128-row tile
+    static constexpr int TILE_BYTES = BM * D * 2;      // Q tile = K tile = V tile
+    static constexpr int STAGES = D == 128 ? 4 : 2;
+    static constexpr int TMEM_O = 256;                 // S buffers at columns 0 and 128
+    static constexpr int TMEM_COLS = 512;
+    static constexpr int NUM_BARS = 2 + 2 * STAGES + 7;
+    static constexpr int SMEM_BYTES = 1024 + TILE_BYTES * (1 + STAGES) + 8 * NUM_BARS + 16;
+};
+
+// The wait on tcgen05.ld results names the destination registers, so no use of them can
+// be scheduled before the wait.
+__device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.wait::ld.sync.aligned;"
+        : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+          "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]),
+          "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]),
+          "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]),
+          "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]),
+          "+r"(r[31])
+        :
+        : "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    const uint32_t sQ = smem_u32(smem);
+    const uint32_t sKV = sQ + C::TILE_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::TILE_BYTES * (1 + C::STAGES));
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const uint32_t bar0 = smem_u32(bars);
+    auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
+    const int Q_FULL = 0, Q_EMPTY = 1, KV_FULL = 2, KV_EMPTY = 2 + C::STAGES;
+    const int S_FULL = 2 + 2 * C::STAGES, P_FULL = S_FULL + 2, PV_DONE = P_FULL + 2,
+              O_EMPTY = PV_DONE + 1, MMA_DRAIN = O_EMPTY + 1;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        mbar_init(BAR(Q_FULL), 1);
+        mbar_init(BAR(Q_EMPTY), 1);
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(BAR(KV_FULL + s), 1);
+            mbar_init(BAR(KV_EMPTY + s), 1);
+        }
+        mbar_init(BAR(S_FULL), 1);
+        mbar_init(BAR(S_FULL + 1), 1);
+        mbar_init(BAR(P_FULL), 128);
+        mbar_init(BAR(P_FULL + 1), 128);
+        mbar_init(BAR(PV_DONE), 1);
+        mbar_init(BAR(O_EMPTY), 128);
+        mbar_init(BAR(MMA_DRAIN), 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int n_items = p.hdr->n_items;
+    const int G = p.group;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tensormap_acquire(p.tm_q);
+            tensormap_acquire(p.tm_k);
+            tensormap_acquire(p.tm_v);
+            uint32_t load_idx = 0, q_count = 0;
+            bool ok = true;
+            for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+                const int4 w = p.items[it];
+                const Geo x = item_geometry(p.q_indptr, p.kv_indptr, w.x, w.z, G, p.causal);
+                if (x.n_tiles == 0) continue;
+                ok = mbar_wait_bounded(BAR(Q_EMPTY), (q_count & 1) ^ 1, abort_flag, p.status);
+                if (!ok) break;
+                mbar_arrive_expect_tx(BAR(Q_FULL), C::TILE_BYTES);
+#pragma unroll
+                for (int c = 0; c < C::CHUNKS; ++c)
+                    tma_load_3d(sQ + c * C::CHUNK_BYTES, p.tm_q, BAR(Q_FULL), c * 64, w.y * G,
+                                x.q_start + x.t0);
+                ++q_count;
+                // consumption order of the MMA warp: K0, (K1, V0), (K2, V1), ..., V_{n-1}
+                const int nl = 2 * x.n_tiles;
+                for (int s = 0; s < nl; ++s) {
+                    int j;
+                    bool is_k;
+                    if (s == 0) {
+                        j = 0;
+                        is_k = true;
+                    } else if (s == nl - 1) {
+                        j = x.n_tiles - 1;
+                        is_k = false;
+                    } else {
+                        const int pr = (s - 1) >> 1;
+                        is_k = ((s - 1) & 1) == 0;
+                        j = is_k ? pr + 1 : pr;
+                    }
+                    const uint32_t st = load_idx % C::STAGES;
+                    ok = mbar_wait_bounded(BAR(KV_EMPTY + st), ((load_idx / C::STAGES) & 1) ^ 1,
+                                           abort_flag, p.status);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(BAR(KV_FULL + st), C::TILE_BYTES);
+                    const CUtensorMap* tm = is_k ? p.tm_k : p.tm_v;
+#pragma unroll
+                    for (int c = 0; c < C::CHUNKS; ++c)
+                        tma_load_2d(sKV + st * C::TILE_BYTES + c * C::CHUNK_BYTES, tm,
+                                    BAR(KV_FULL + st), w.y * D + c * 64, x.kv_start + j * BN);
+                    ++load_idx;
+                }
+            }
+            if (!ok) {
+                // let every copy already issued land before the CTA exits
+                const uint32_t first = load_idx > (uint32_t)C::STAGES ? load_idx - C::STAGES : 0;
+                for (uint32_t k = first; k < load_idx; ++k)
+                    mbar_wait_bounded(BAR(KV_FULL + k % C::STAGES), (k / C::STAGES) & 1, nullptr,
+                                      p.status);
+                if (q_count > 0)
+                    mbar_wait_bounded(BAR(Q_FULL), (q_count - 1) & 1, nullptr, p.status);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, false);
+            constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, true);
+            uint32_t load_idx = 0, q_count = 0, tile_ctr = 0, item_cnt = 0;
+            bool ok = true;
+            auto issue_pv = [&](int jj, int n) -> bool {
+                (void)n;
+                const uint32_t ctr = tile_ctr + jj;
+                if (!mbar_wait_bounded(BAR(P_FULL + (ctr & 1)), (ctr >> 1) & 1, abort_flag,
+                                       p.status))
+                    return false;
+                const uint32_t st = load_idx % C::STAGES;
+                if (!mbar_wait_bounded(BAR(KV_FULL + st), (load_idx / C::STAGES) & 1, abort_flag,
+                                       p.status))
+                    return false;
+                ++load_idx;
+                if (jj == 0 && item_cnt > 0 &&
+                    !mbar_wait_bounded(BAR(O_EMPTY), (item_cnt - 1) & 1, abort_flag, p.status))
+                    return false;
+                tc_fence_after();
+                const uint32_t p_col = (ctr & 1) ? 128u : 0u;
+                const uint32_t v_base = sKV + st * C::TILE_BYTES;
+#pragma unroll
+                for (int k = 0; k < BN / 16; ++k) {
+                    // V tile, MN-major: 16 keys = two 8-row swizzle groups (2048 bytes);
+                    // consecutive 64-column chunks of the head dim are CHUNK_BYTES apart.
+                    const uint64_t bd = sdesc_sw128(v_base + k * 2048, C::CHUNK_BYTES, 1024);
+                    mma_ts(tmem_base + C::TMEM_O, tmem_base + p_col + k * 8, bd, IDESC_PV,
+                           (jj > 0 || k > 0) ? 1u : 0u);
+                }
+                mma_commit(BAR(KV_EMPTY + st));
+                mma_commit(BAR(PV_DONE));
+                return true;
+            };
+            for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+                const int4 w = p.items[it];
+                const Geo x = item_geometry(p.q_indptr, p.kv_indptr, w.x, w.z, G, p.causal);
+                const int n = x.n_tiles;
+                if (n == 0) continue;
+                ok = mbar_wait_bounded(BAR(Q_FULL), q_count & 1, abort_flag, p.status);
+                ++q_count;
+                if (!ok) break;
+                tc_fence_after();
+                for (int j = 0; j < n; ++j) {
+                    const uint32_t st = load_idx % C::STAGES;
+                    ok = mbar_wait_bounded(BAR(KV_FULL + st), (load_idx / C::STAGES) & 1,
+                                           abort_flag, p.status);
+                    if (!ok) break;
+                    ++load_idx;
+                    tc_fence_after();
+                    const uint32_t ctr = tile_ctr + j;
+                    const uint32_t s_col = (ctr & 1) ? 128u : 0u;
+                    const uint32_t k_base = sKV + st * C::TILE_BYTES;
+#pragma unroll
+                    for (int k = 0; k < D / 16; ++k) {
+                        const uint32_t off = (k >> 2) * C::CHUNK_BYTES + (k & 3) * 32;
+                        const uint64_t ad = sdesc_sw128(sQ + off, 16, 1024);
+                        const uint64_t bd = sdesc_sw128(k_base + off, 16, 1024);
+                        mma_ss(tmem_base + s_col, ad, bd, IDESC_QK, k > 0 ? 1u : 0u);
+                    }
+                    mma_commit(BAR(KV_EMPTY + st));
+                    mma_commit(BAR(S_FULL + (ctr & 1)));
+                    if (j == n - 1) mma_commit(BAR(Q_EMPTY));
+                    if (j >= 1) {
+                        ok = issue_pv(j - 1, n);
+                        if (!ok) break;
+                    }
+                }
+                if (ok) ok = issue_pv(n - 1, n);
+                tile_ctr += n;
+                ++item_cnt;
+            }
+            // every MMA issued has completed before tensor memory is released
+            mma_commit(BAR(MMA_DRAIN));
+            mbar_wait_bounded(BAR(MMA_DRAIN), 0, nullptr, p.status);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ softmax / epilogue
+        const int r = threadIdx.x - 128;                       // packed row = TMEM lane
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        const int Hq = p.num_qo_heads;
+        uint32_t tile_ctr = 0;
+        bool ok = true;
+        for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+            const int4 w = p.items[it];
+            const Geo x = item_geometry(p.q_indptr, p.kv_indptr, w.x, w.z, G, p.causal);
+            const int row_t = x.t0 + r / G;
+            const int row_h = w.y * G + r % G;
+            const bool valid = row_t < x.qo_len;
+            const size_t out_row = (size_t)(x.q_start + row_t) * Hq + row_h;
+            if (x.n_tiles == 0) {
+                if (valid) {
+                    uint4* op = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) +
+                                                         out_row * D);
+#pragma unroll
+                    for (int c = 0; c < D / 8; ++c) op[c] = make_uint4(0, 0, 0, 0);
+                    if (p.lse) p.lse[out_row] = -INFINITY;
+                }
+                continue;
+            }
+            const int klim = p.causal ? min(row_t + x.kv_len - x.qo_len, x.kv_len - 1)
+                                      : x.kv_len - 1;
+            float m = -INFINITY, l = 0.f;
+            for (int j = 0; j < x.n_tiles; ++j) {
+                const uint32_t ctr = tile_ctr + j;
+                const uint32_t buf = ctr & 1;
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(S_FULL + buf), (ctr >> 1) & 1,
+                                                               abort_flag, p.status));
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t s_addr = tmem_base + lane_base + (buf ? 128u : 0u);
+                float s[BN];
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t u[32];
+                    tmem_ld32(s_addr + c * 32, u);
+                    tmem_wait_ld_regs(u);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(u[i]) * p.scale_log2;
+                }
+                if (j >= x.n_unmasked) {
+                    const int key0 = j * BN;
+#pragma unroll
+                    for (int i = 0; i < BN; ++i)
+                        if (key0 + i > klim) s[i] = -INFINITY;
+                }
+                float mt = s[0];
+#pragma unroll
+                for (int i = 1; i < BN; ++i) mt = fmaxf(mt, s[i]);
+                const float m_new = fmaxf(m, mt);
+                const float m_use = m_new == -INFINITY ? 0.f : m_new;
+                const float alpha = ex2_approx(m - m_use);
+                float rs = 0.f;
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float p0 = ex2_approx(s[c * 64 + 2 * i] - m_use);
+                        const float p1 = ex2_approx(s[c * 64 + 2 * i + 1] - m_use);
+                        rs += p0 + p1;
+                        pk[i] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st32(s_addr + c * 32, pk);
+                }
+                l = l * alpha + rs;
+                if (j > 0) {
+                    ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(PV_DONE), (ctr - 1) & 1,
+                                                                   abort_flag, p.status));
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (__any_sync(0xffffffffu, alpha < 1.f)) {
+                        const uint32_t o_addr = tmem_base + lane_base + C::TMEM_O;
+#pragma unroll 1
+                        for (int c = 0; c < D / 32; ++c) {
+                            uint32_t u[32];
+                            tmem_ld32(o_addr + c * 32, u);
+                            tmem_wait_ld_regs(u);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+                            tmem_st32(o_addr + c * 32, u);
+                        }
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(BAR(P_FULL + buf));
+                m = m_new;
+            }
+            if (!ok) break;
+            tile_ctr += x.n_tiles;
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(PV_DONE), (tile_ctr - 1) & 1,
+                                                           abort_flag, p.status));
+            if (!ok) break;
+            tc_fence_after();
+            const float inv_l = l > 0.f ? 1.f / l : 0.f;
+            const uint32_t o_addr = tmem_base + lane_base + C::TMEM_O;
+            uint4* op = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + out_row * D);
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t u[32];
+                tmem_ld32(o_addr + c * 32, u);
+                tmem_wait_ld_regs(u);
+                if (valid) {
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4) {
+                        uint4 q;
+                        q.x = pack_bf16x2(__uint_as_float(u[v4 * 8 + 0]) * inv_l,
+                                          __uint_as_float(u[v4 * 8 + 1]) * inv_l);
+                        q.y = pack_bf16x2(__uint_as_float(u[v4 * 8 + 2]) * inv_l,
+                                          __uint_as_float(u[v4 * 8 + 3]) * inv_l);
+                        q.z = pack_bf16x2(__uint_as_float(u[v4 * 8 + 4]) * inv_l,
+                                          __uint_as_float(u[v4 * 8 + 5]) * inv_l);
+                        q.w = pack_bf16x2(__uint_as_float(u[v4 * 8 + 6]) * inv_l,
+                                          __uint_as_float(u[v4 * 8 + 7]) * inv_l);
+                        op[c * 4 + v4] = q;
+                    }
+                }
+            }
+            if (valid && p.lse)
+                p.lse[out_row] = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+            tc_fence_before();
+            mbar_arrive(BAR(O_EMPTY));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ host launchers
+template <int D>
+int smem_bytes() {
+    return Cfg<D>::SMEM_BYTES;
+}
+
+template <int D>
+cudaError_t launch_attention(const Params& p, int grid, cudaStream_t stream) {
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(attention_kernel<D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Cfg<D>::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    attention_kernel<D><<<grid, THREADS, Cfg<D>::SMEM_BYTES, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_plan(const PlanParams& pp, const CUtensorMap& tq, const CUtensorMap& tk,
+                        const CUtensorMap& tv, cudaStream_t stream) {
+    plan_kernel<<<1, PLAN_THREADS, 0, stream>>>(pp, tq, tk, tv);
+    return cudaGetLastError();
+}
+
+template cudaError_t launch_attention<128>(const Params&, int, cudaStream_t);
+template cudaError_t launch_attention<256>(const Params&, int, cudaStream_t);
+
+}  // namespace prefill
+}  // namespace pgqa

@@ -1,0 +1,133 @@
+"""The C ABI without a GPU: the library builds, loads, exports every function the public
+header declares, and its host-side argument checks return the documented status codes
+before any CUDA call is made (pointers below are never dereferenced)."""
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+ROOT = Path(__file__).resolve().parents[1]
+HEADERS = sorted((ROOT / "include").glob("*.h"))
+
+
+def declared_functions():
+    names = []
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", h.read_text(), flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        for m in re.finditer(r"\b([A-Za-z_]\w*)\s*\(([^;{}]*)\)\s*;", text):
+            if m.group(1) not in ("if", "while", "return", "sizeof"):
+                names.append(m.group(1))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_gqa_attention_varlen_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(str(path))
+
+
+@pytest.fixture(scope="module")
+def api():
+    from paged_gqa_attention_varlen_gb300 import api
+    return api
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("pgqa_ragged_prefill_bf16", "pgqa_paged_decode_bf16", "ragged_prefill_bf16",
+              "paged_decode_bf16", "pgqa_set_workspace", "pgqa_get_device_status"):
+        assert n in names
+
+
+def test_library_exports_every_declared_function(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_lists_every_declared_function(api):
+    assert set(declared_functions()) <= set(api.ABI_FUNCTIONS)
+
+
+def test_version_and_status_strings(api):
+    assert api.lib.pgqa_version() >= 10000
+    for code in range(-7, 1):
+        assert api.lib.pgqa_status_string(code).decode()
+    assert api.lib.pgqa_status_string(123) == b"unknown status"
+
+
+A = 1 << 20  # a 16-byte aligned fake device address (never dereferenced)
+
+
+def prefill(api, **kw):
+    args = dict(q=A, k=A, v=A, o=A, lse=A, qi=A, ki=A, batch=2, hq=8, hk=2, d=128, causal=1,
+                scale=0.1)
+    args.update(kw)
+    p = ctypes.c_void_p
+    return api.lib.pgqa_ragged_prefill_bf16(
+        p(args["q"]), p(args["k"]), p(args["v"]), p(args["o"]), p(args["lse"]), p(args["qi"]),
+        p(args["ki"]), args["batch"], args["hq"], args["hk"], args["d"], args["causal"],
+        args["scale"], None)
+
+
+def decode(api, **kw):
+    args = dict(q=A, kp=A, vp=A, pt=A, kl=A, ps=16, stride=8, npages=100, o=A, lse=A, batch=4,
+                hq=32, hk=8, d=128, scale=0.1)
+    args.update(kw)
+    p = ctypes.c_void_p
+    return api.lib.pgqa_paged_decode_bf16(
+        p(args["q"]), p(args["kp"]), p(args["vp"]), p(args["pt"]), p(args["kl"]), args["ps"],
+        args["stride"], args["npages"], p(args["o"]), p(args["lse"]), args["batch"], args["hq"],
+        args["hk"], args["d"], args["scale"], None)
+
+
+def test_prefill_host_validation(api):
+    assert prefill(api, batch=0) == 0                       # empty batch: early return
+    assert prefill(api, batch=-1) == -1
+    assert prefill(api, q=0) == -1
+    assert prefill(api, o=A + 8) == -1                      # misaligned output
+    assert prefill(api, d=64) == -2
+    assert prefill(api, d=192) == -2
+    assert prefill(api, hq=6, hk=4) == -2                   # not a multiple
+    assert prefill(api, hq=24, hk=8) == -2                  # group 3 does not divide 128
+    assert prefill(api, scale=float("nan")) == -1
+
+
+def test_decode_host_validation(api):
+    assert decode(api, batch=0) == 0
+    assert decode(api, batch=-3) == -1
+    assert decode(api, kl=0) == -1
+    assert decode(api, ps=32) == -2
+    assert decode(api, d=256) == -2
+    assert decode(api, hq=48, hk=8) == -2                   # group 6
+    assert decode(api, hq=128, hk=8) == -2                  # group 16
+    assert decode(api, q=A + 4) == -1
+
+
+def test_valid_calls_without_a_gpu_report_no_device(api):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert prefill(api) == -7
+    assert decode(api) == -7
+
+
+def test_workspace_size_queries(api):
+    lib = api.lib
+    n = lib.pgqa_workspace_bytes_decode(256, 2048, 16, 32, 128)
+    # 256 requests x 32 chunks x 32 heads x (128 + 1) floats of partial results
+    assert n >= 256 * 32 * 32 * 129 * 4
+    assert lib.pgqa_workspace_bytes_decode(-1, 1, 16, 1, 128) == 0
+    m = lib.pgqa_workspace_bytes_prefill(16, 33_000, 32, 8)
+    assert m >= (33_000 * 4 // 128) * 8 * 16
+    assert lib.pgqa_workspace_bytes_prefill(1, -5, 32, 8) == 0
+
+
+def test_binding_refuses_cpu_tensors(api):
+    import torch
+    q = torch.zeros(4, 2, 128, dtype=torch.bfloat16)
+    ip = torch.tensor([0, 4], dtype=torch.int32)
+    with pytest.raises((ValueError, TypeError, RuntimeError, AssertionError)):
+        api.ragged_prefill(q, q[:, :1].contiguous(), q[:, :1].contiguous(), ip, ip)

@@ -1,0 +1,115 @@
+"""GPU parity of the paged split-KV decode (pgqa_paged_decode_bf16) against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_gqa_attention_varlen_gb300 import workloads as W
+from gpu_util import check_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def run_gpu(api, pc, **kw):
+    o, lse = api.paged_decode(pc.q, pc.k_pages, pc.v_pages, pc.page_table, pc.kv_lens_t,
+                              sm_scale=pc.sm_scale, **kw)
+    torch.cuda.synchronize()
+    return o, lse
+
+
+def oracle_decode(pc):
+    return oracle.paged_attention(pc.q, pc.q_indptr, pc.k_pages, pc.v_pages, pc.page_table,
+                                  pc.kv_lens_t, pc.num_qo_heads, pc.num_kv_heads, True,
+                                  pc.sm_scale)
+
+
+LENS = [0, 1, 15, 16, 17, 100, 1023, 1024, 1025, 2048, 3000, 4097]
+
+
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_decode_lengths_and_groups(cuda_lib, G):
+    hk = 8 // G if G < 8 else 2
+    pc = W.paged_case(LENS, G * hk, hk, 128, page_size=16, seed=G, device="cuda")
+    o, lse = run_gpu(cuda_lib, pc)
+    assert cuda_lib.device_status() == 0
+    ro, rl = oracle_decode(pc)
+    check_rows(o.reshape(-1, 128).float().cpu(), lse.reshape(-1).cpu(), ro, rl, f"G={G}")
+
+
+def test_decode_single_request_long(cuda_lib):
+    pc = W.paged_case([32768], 32, 8, 128, page_size=16, seed=11, device="cuda")
+    o, lse = run_gpu(cuda_lib, pc)
+    ro, rl = oracle_decode(pc)
+    check_rows(o.reshape(-1, 128).float().cpu(), lse.reshape(-1).cpu(), ro, rl, "32k")
+
+
+def test_decode_workload_sampled_requests(cuda_lib):
+    """The full 256-request decode workload runs on the GPU in the benchmark's launch
+    configuration; 24 requests (their pages gathered to the host) are checked."""
+    pc = W.config("decode", device="cuda")
+    o, lse = run_gpu(cuda_lib, pc)
+    assert cuda_lib.device_status() == 0
+    rng = np.random.default_rng(0)
+    pick = sorted(set([0, pc.batch - 1] + rng.choice(pc.batch, 22, replace=False).tolist()))
+    for b in pick:
+        n = pc.kv_lens[b]
+        npg = (n + 15) // 16
+        pages = pc.page_table[b, :npg].long()
+        sub = W.PagedCase("sub", pc.q[b:b + 1], torch.tensor([0, 1], dtype=torch.int32),
+                          pc.k_pages[pages], pc.v_pages[pages],
+                          torch.arange(npg, dtype=torch.int32).reshape(1, -1),
+                          torch.tensor([n], dtype=torch.int32), [n], [1], 16,
+                          pc.num_qo_heads, pc.num_kv_heads, 128, True, pc.sm_scale)
+        ro, rl = oracle_decode(sub)
+        check_rows(o[b].float().cpu(), lse[b].cpu(), ro, rl, f"request {b} (kv {n})")
+
+
+def test_page_table_padding_is_bitwise_invisible(cuda_lib):
+    outs = []
+    for pad in (-1, 0, 77):
+        pc = W.paged_case([40, 1500, 7], 16, 4, 128, page_size=16, pad=pad, stride=130,
+                          seed=13, device="cuda")
+        outs.append(run_gpu(cuda_lib, pc))
+        assert cuda_lib.device_status() == 0
+    for o, l in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
+
+
+def test_nan_in_unused_tail_slots_is_invisible(cuda_lib):
+    pc = W.paged_case([20, 1030], 8, 2, 128, page_size=16, seed=17, device="cuda")
+    o1, l1 = run_gpu(cuda_lib, pc)
+    for b, n in enumerate(pc.kv_lens):
+        last = int(pc.page_table[b, (n - 1) // 16])
+        pc.k_pages[last, n % 16:] = float("nan")
+        pc.v_pages[last, n % 16:] = float("nan")
+    o2, l2 = run_gpu(cuda_lib, pc)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_zero_length_rows_are_exact_zeros(cuda_lib):
+    pc = W.paged_case([0, 5, 0], 8, 2, 128, page_size=16, seed=19, device="cuda")
+    o, l = run_gpu(cuda_lib, pc)
+    assert torch.all(o[0] == 0) and torch.all(o[2] == 0)
+    assert torch.all(torch.isneginf(l[0])) and torch.all(torch.isneginf(l[2]))
+
+
+def test_batch_composition_is_bitwise_invariant(cuda_lib):
+    pc = W.paged_case([3000, 64, 1025], 32, 8, 128, page_size=16, seed=23, device="cuda")
+    o, l = run_gpu(cuda_lib, pc)
+    for b in range(3):
+        sub_o, sub_l = cuda_lib.paged_decode(pc.q[b:b + 1].contiguous(), pc.k_pages, pc.v_pages,
+                                             pc.page_table[b:b + 1].contiguous(),
+                                             pc.kv_lens_t[b:b + 1].contiguous(),
+                                             sm_scale=pc.sm_scale)
+        torch.cuda.synchronize()
+        assert torch.equal(sub_o[0], o[b]) and torch.equal(sub_l[0], l[b])
+
+
+def test_bad_page_id_reports_bounds_status(cuda_lib):
+    pc = W.paged_case([40], 8, 2, 128, page_size=16, seed=29, device="cuda")
+    pc.page_table[0, 1] = pc.num_pages + 5
+    run_gpu(cuda_lib, pc)
+    assert cuda_lib.device_status() == -6
+    pc.page_table[0, 1] = 0
+    run_gpu(cuda_lib, pc)
+    assert cuda_lib.device_status() == 0
