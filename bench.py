@@ -69,14 +69,31 @@ def load_peaks():
                 "source": "fallback"}
 
 
+KERNEL_SOURCES = {"prefill_attention": "paged_gqa_attention_varlen_gb300/csrc/prefill.cu",
+                  "decode": "paged_gqa_attention_varlen_gb300/csrc/decode.cu"}
+
+
 def load_traffic():
-    """Per-launch DRAM bytes of each kernel from the committed ncu summary, if current."""
+    """Per-launch DRAM bytes (ncu dram__bytes_read.sum + dram__bytes_write.sum) of each
+    kernel from profiles/traffic.json -- None for a kernel whose source changed since the
+    counters were taken (the file records the source's md5)."""
+    import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
-            return json.load(f)
+            rec = json.load(f)
     except (OSError, ValueError):
         return {}
+    out = {}
+    for key, src in KERNEL_SOURCES.items():
+        r = rec.get(key)
+        try:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                md5 = hashlib.md5(f.read()).hexdigest()
+        except OSError:
+            md5 = None
+        out[key] = r["bytes_per_launch"] if r and r.get("source_md5") == md5 else None
+    return out
 
 
 # ------------------------------------------------------------------ distributed
@@ -396,6 +413,33 @@ def bench_gpu(args, ws, rank, local):
     return 0
 
 
+def profile_case(args):
+    """Run one bounded case of a hot-path kernel `--reps` times (for ncu captures)."""
+    from paged_gqa_attention_varlen_gb300 import api
+    from paged_gqa_attention_varlen_gb300 import workloads as W
+    dev = torch.device("cuda", 0)
+    if args.profile in ("prefill_hd128", "prefix_hd256", "long", "tiny"):
+        c = W.config(args.profile, device=dev)
+        o = torch.empty_like(c.q)
+        lse = torch.empty(c.q.shape[:2], dtype=torch.float32, device=dev)
+        for _ in range(args.reps):
+            api.ragged_prefill(c.q, c.k, c.v, c.q_indptr, c.kv_indptr, causal=c.causal,
+                               sm_scale=c.sm_scale, out=o, lse=lse)
+    else:  # decode slice: the first --decode-batch requests of the decode workload
+        kv = W.config_lengths("decode")[1][:args.decode_batch]
+        c = W.paged_case(kv, 32, 8, 128, page_size=16, seed=0, device=dev)
+        o = torch.empty_like(c.q)
+        lse = torch.empty(c.q.shape[:2], dtype=torch.float32, device=dev)
+        for _ in range(args.reps):
+            api.paged_decode(c.q, c.k_pages, c.v_pages, c.page_table, c.kv_lens_t,
+                             sm_scale=c.sm_scale, out=o, lse=lse)
+    torch.cuda.synchronize(dev)
+    st = api.device_status()
+    print(json.dumps({"profile": args.profile, "reps": args.reps, "status": st,
+                      "max_mem_gb": torch.cuda.max_memory_allocated(dev) / 1e9}))
+    return 0 if st == 0 else 1
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -408,7 +452,14 @@ def main(argv=None):
     ap.add_argument("--cpu-rows", type=int, default=150000,
                     help="oracle rows timed for the cpu_baseline object (about 10-30 s)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", choices=["prefill_hd128", "prefix_hd256", "long", "tiny",
+                                          "decode"], default=None,
+                    help="run one bounded case --reps times and exit (ncu captures)")
+    ap.add_argument("--reps", type=int, default=4)
+    ap.add_argument("--decode-batch", type=int, default=32)
     args = ap.parse_args(argv)
+    if args.profile:
+        return profile_case(args)
     ws, rank, local = dist_env()
     if args.impl == "reference":
         return bench_reference(args, ws, rank)
