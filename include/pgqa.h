@@ -136,6 +136,41 @@ int paged_decode_bf16(const void* q, const void* k_pages, const void* v_pages,
                       pgqa_stream_t stream);
 
 /*
+ * Paged decode that allocates nothing (the source pages describe no such call; it is an
+ * addition of this library).
+ *
+ * Same arguments, results and supported shapes as pgqa_paged_decode_bf16, which lazily
+ * cudaMalloc's a workspace for its split-KV partial results.  Callers that must not
+ * allocate device memory use this one instead: work enqueued while a stream is being
+ * captured into a CUDA graph, engines that give all device memory to their own pool at
+ * start-up, and deployments that forbid allocation after initialisation.  Its scratch is a
+ * fixed 16 MiB array in the library's own static device memory, which every GPU that
+ * loads the library holds until the process exits.  The caller still passes (and owns)
+ * every input and output.
+ *
+ *   - Set-up: the first call on each device, with that device current, looks up the
+ *     array's device address (cudaGetSymbolAddress).  Make that first call before any
+ *     stream capture.
+ *   - Limit: returns PGQA_ERR_WORKSPACE, enqueueing nothing, when
+ *       1024 + 256-rounded (2*batch+1)*4 + 256-rounded C*Hq*4 + C*Hq*head_dim*4 > 16 MiB,
+ *     with C = batch * ceil(page_table_stride * page_size / 1024) partial chunks
+ *     (e.g. batch 32 with 32k-key tables at 32 query heads fits).
+ *   - Sharing: every call on a device uses the same array and leaves its contents
+ *     behind; calls that overlap on the GPU (different streams without ordering) race
+ *     and corrupt each other's results.  Order them.
+ *   - Device-side index errors (bad page id, bad kv_len) are handled as in
+ *     pgqa_paged_decode_bf16 (the bad keys are skipped) but are not reported through
+ *     pgqa_get_device_status.
+ * No cudaMalloc, cudaFree or other allocating call is made.
+ */
+int pgqa_paged_decode_bf16_noalloc(const void* q, const void* k_pages, const void* v_pages,
+                                   const int32_t* page_table, const int32_t* kv_lens,
+                                   int page_size, int page_table_stride, int num_pages,
+                                   void* o, float* lse, int batch, int num_qo_heads,
+                                   int num_kv_heads, int head_dim, float sm_scale,
+                                   pgqa_stream_t stream);
+
+/*
  * Workspace.  Both calls need device scratch: the prefill for its work list and tensor
  * maps, the decode for its split-KV partial results.  Unless the caller supplies one,
  * the library allocates it lazily on the first call that needs it (per device; 128 MiB

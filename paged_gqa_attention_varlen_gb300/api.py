@@ -27,7 +27,7 @@ ABI_FUNCTIONS = (
     "pgqa_ragged_prefill_bf16", "pgqa_paged_decode_bf16", "ragged_prefill_bf16",
     "paged_decode_bf16", "pgqa_set_workspace", "pgqa_workspace_bytes_prefill",
     "pgqa_workspace_bytes_decode", "pgqa_get_device_status", "pgqa_status_string",
-    "pgqa_version",
+    "pgqa_version", "pgqa_paged_decode_bf16_noalloc",
 )
 
 
