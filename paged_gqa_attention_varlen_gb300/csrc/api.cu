@@ -14,6 +14,7 @@ cudaError_t launch_plan(const PlanParams&, const CUtensorMap&, const CUtensorMap
                         const CUtensorMap&, cudaStream_t);
 template <int D>
 cudaError_t launch_attention(const Params&, int, cudaStream_t);
+cudaError_t launch_attention_pair(const Params&, int, cudaStream_t);
 }  // namespace prefill
 namespace decode {
 cudaError_t launch_plan(const PlanParams&, cudaStream_t);
@@ -306,6 +307,9 @@ int pgqa_ragged_prefill_bf16(const void* q, const void* k, const void* v, void* 
     pp.num_kv_heads = num_kv_heads;
     pp.group = group;
     pp.causal = causal ? 1 : 0;
+    // hd128 runs two q tiles per work item (two softmax warpgroups share one K/V
+    // stream); hd256 needs all of tensor memory for one tile
+    pp.tiles_per_item = head_dim == 128 ? 2 : 1;
     pp.hdr = hdr;
     pp.tile_off = tile_off;
     pp.items = items;
@@ -330,7 +334,7 @@ int pgqa_ragged_prefill_bf16(const void* q, const void* k, const void* v, void* 
     p.group = group;
     p.causal = causal ? 1 : 0;
     p.scale_log2 = sm_scale * 1.4426950408889634f;
-    e = head_dim == 128 ? prefill::launch_attention<128>(p, st->num_sms, s)
+    e = head_dim == 128 ? prefill::launch_attention_pair(p, st->num_sms, s)
                         : prefill::launch_attention<256>(p, st->num_sms, s);
     return map_cuda(e);
 }

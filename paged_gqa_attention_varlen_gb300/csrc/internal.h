@@ -39,6 +39,7 @@ namespace prefill {
 constexpr int BM = 128;          // packed query rows (token x group head) per tile
 constexpr int BN = 128;          // keys per K/V tile
 constexpr int THREADS = 256;     // warp 0 TMA, warp 1 MMA, warps 4-7 softmax/epilogue
+constexpr int PAIR_THREADS = 384;  // + warps 8-11: softmax of the second q tile
 constexpr int PLAN_THREADS = 1024;
 constexpr int COST_BUCKETS = 4096;
 
@@ -67,6 +68,7 @@ struct PlanParams {
     int num_kv_heads;
     int group;
     int causal;
+    int tiles_per_item;        // consecutive q tiles one work item covers (1 or 2)
     WsHeader* hdr;
     int* tile_off;             // [batch + 1]
     int4* items;

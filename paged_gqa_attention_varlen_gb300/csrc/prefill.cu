@@ -66,6 +66,14 @@ __device__ __forceinline__ int find_segment(const int* off, int n, int f) {
     return lo;
 }
 
+// K/V tiles of the longest q tile of an item (the item covers tiles qt..qt+tpi-1 that exist)
+__device__ __forceinline__ int item_cost(const PlanParams& p, int b, int qt) {
+    const long long qo = p.q_indptr[b + 1] - p.q_indptr[b];
+    const int tiles = (int)((qo * p.group + BM - 1) / BM);
+    const int last = min(qt + p.tiles_per_item, tiles) - 1;
+    return item_geometry(p.q_indptr, p.kv_indptr, b, last, p.group, p.causal).n_tiles;
+}
+
 // ---------------------------------------------------------------------------- plan
 __global__ void __launch_bounds__(PLAN_THREADS)
     plan_kernel(PlanParams p, const __grid_constant__ CUtensorMap tq,
@@ -97,7 +105,8 @@ __global__ void __launch_bounds__(PLAN_THREADS)
         int cnt = 0;
         if (b < p.batch) {
             const long long qo = p.q_indptr[b + 1] - p.q_indptr[b];
-            cnt = (int)((qo * p.group + BM - 1) / BM);
+            const int tiles = (int)((qo * p.group + BM - 1) / BM);
+            cnt = (tiles + p.tiles_per_item - 1) / p.tiles_per_item;
         }
         scan[tid] = cnt;
         __syncthreads();
@@ -127,9 +136,8 @@ __global__ void __launch_bounds__(PLAN_THREADS)
     // histogram of item costs (K/V tiles per q tile)
     for (int f = tid; f < total_tiles; f += nthr) {
         const int b = find_segment(p.tile_off, p.batch, f);
-        const Geo x = item_geometry(p.q_indptr, p.kv_indptr, b, f - p.tile_off[b], p.group,
-                                    p.causal);
-        atomicAdd(&hist[min(x.n_tiles, COST_BUCKETS - 1)], 1);
+        const int qt = (f - p.tile_off[b]) * p.tiles_per_item;
+        atomicAdd(&hist[min(item_cost(p, b, qt), COST_BUCKETS - 1)], 1);
     }
     __syncthreads();
 
@@ -165,11 +173,11 @@ __global__ void __launch_bounds__(PLAN_THREADS)
     // scatter: the kv heads of one q tile take consecutive slots
     for (int f = tid; f < total_tiles; f += nthr) {
         const int b = find_segment(p.tile_off, p.batch, f);
-        const int qt = f - p.tile_off[b];
-        const Geo x = item_geometry(p.q_indptr, p.kv_indptr, b, qt, p.group, p.causal);
-        const int slot = atomicAdd(&hist[min(x.n_tiles, COST_BUCKETS - 1)], 1);
+        const int qt = (f - p.tile_off[b]) * p.tiles_per_item;
+        const int cost = item_cost(p, b, qt);
+        const int slot = atomicAdd(&hist[min(cost, COST_BUCKETS - 1)], 1);
         for (int g = 0; g < p.num_kv_heads; ++g)
-            p.items[(long long)slot * p.num_kv_heads + g] = make_int4(b, g, qt, x.n_tiles);
+            p.items[(long long)slot * p.num_kv_heads + g] = make_int4(b, g, qt, cost);
     }
 
     // tensor maps with the real row extents
@@ -549,6 +557,368 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
     }
 }
 
+// ------------------------------------------------------------ two-tile kernel (hd128)
+// One work item = two consecutive q tiles (A, B) of one (request, kv head).  Both tiles
+// share every K/V tile the producer streams in, so K/V shared-memory traffic per flop
+// halves, and the tensor core alternates between the two tiles: while warpgroup A runs
+// the softmax of its tile, the MMA warp runs B's P.V and Q.K^T, and vice versa.
+// TMEM columns: S_A 0..127, S_B 128..255, O_A 256..383, O_B 384..511.
+struct PairCfg {
+    static constexpr int D = 128;
+    static constexpr int CHUNKS = 2;
+    static constexpr int CHUNK_BYTES = BM * 128;
+    static constexpr int TILE_BYTES = BM * D * 2;
+    static constexpr int STAGES = 4;
+    static constexpr int NUM_BARS = 19;
+    static constexpr int SMEM_BYTES = 1024 + TILE_BYTES * (2 + STAGES) + 8 * NUM_BARS + 16;
+};
+
+// Growth of the running max (log2 units) below which O and l keep their old scale:
+// probabilities then stay below 2^8 and the fp32 accumulators are unaffected, while the
+// O rescale in tensor memory is skipped for most tiles.
+constexpr float kRescaleThreshold = 8.0f;
+
+__global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const Params p) {
+    using C = PairCfg;
+    constexpr int D = C::D;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    const uint32_t sQ = smem_u32(smem);  // tile A at sQ, tile B at sQ + TILE_BYTES
+    const uint32_t sKV = sQ + 2 * C::TILE_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::TILE_BYTES * (2 + C::STAGES));
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const uint32_t bar0 = smem_u32(bars);
+    auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
+    constexpr int Q_FULL = 0, Q_EMPTY = 1, KV_FULL = 2, KV_EMPTY = 2 + C::STAGES,
+                  S_FULL = 2 + 2 * C::STAGES, P_FULL = S_FULL + 2, PV_DONE = P_FULL + 2,
+                  O_EMPTY = PV_DONE + 2, MMA_DRAIN = O_EMPTY + 2;
+    static_assert(MMA_DRAIN + 1 == C::NUM_BARS, "barrier count");
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        mbar_init(BAR(Q_FULL), 1);
+        mbar_init(BAR(Q_EMPTY), 1);
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(BAR(KV_FULL + s), 1);
+            mbar_init(BAR(KV_EMPTY + s), 1);
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(BAR(S_FULL + x), 1);
+            mbar_init(BAR(P_FULL + x), 128);
+            mbar_init(BAR(PV_DONE + x), 1);
+            mbar_init(BAR(O_EMPTY + x), 128);
+        }
+        mbar_init(BAR(MMA_DRAIN), 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int n_items = p.hdr->n_items;
+    const int G = p.group;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tensormap_acquire(p.tm_q);
+            tensormap_acquire(p.tm_k);
+            tensormap_acquire(p.tm_v);
+            uint32_t load_idx = 0, q_count = 0;
+            bool ok = true;
+            for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+                const int4 w = p.items[it];
+                const Geo a = item_geometry(p.q_indptr, p.kv_indptr, w.x, w.z, G, p.causal);
+                const Geo bq = item_geometry(p.q_indptr, p.kv_indptr, w.x, w.z + 1, G, p.causal);
+                const int nA = a.n_tiles;
+                const int nB = bq.t0 < bq.qo_len ? bq.n_tiles : 0;
+                const int nmax = max(nA, nB);
+                if (nmax == 0) continue;
+                ok = mbar_wait_bounded(BAR(Q_EMPTY), (q_count & 1) ^ 1, abort_flag, p.status);
+                if (!ok) break;
+                mbar_arrive_expect_tx(BAR(Q_FULL), C::TILE_BYTES * (nB > 0 ? 2 : 1));
+#pragma unroll
+                for (int c = 0; c < C::CHUNKS; ++c)
+                    tma_load_3d(sQ + c * C::CHUNK_BYTES, p.tm_q, BAR(Q_FULL), c * 64, w.y * G,
+                                a.q_start + a.t0);
+                if (nB > 0) {
+#pragma unroll
+                    for (int c = 0; c < C::CHUNKS; ++c)
+                        tma_load_3d(sQ + C::TILE_BYTES + c * C::CHUNK_BYTES, p.tm_q, BAR(Q_FULL),
+                                    c * 64, w.y * G, bq.q_start + bq.t0);
+                }
+                ++q_count;
+                for (int s = 0; s < 2 * nmax; ++s) {
+                    const int j = s >> 1;
+                    const CUtensorMap* tm = (s & 1) ? p.tm_v : p.tm_k;
+                    const uint32_t st = load_idx % C::STAGES;
+                    ok = mbar_wait_bounded(BAR(KV_EMPTY + st), ((load_idx / C::STAGES) & 1) ^ 1,
+                                           abort_flag, p.status);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(BAR(KV_FULL + st), C::TILE_BYTES);
+#pragma unroll
+                    for (int c = 0; c < C::CHUNKS; ++c)
+                        tma_load_2d(sKV + st * C::TILE_BYTES + c * C::CHUNK_BYTES, tm,
+                                    BAR(KV_FULL + st), w.y * D + c * 64, a.kv_start + j * BN);
+                    ++load_idx;
+                }
+            }
+            if (!ok) {
+                const uint32_t first = load_idx > (uint32_t)C::STAGES ? load_idx - C::STAGES : 0;
+                for (uint32_t k = first; k < load_idx; ++k)
+                    mbar_wait_bounded(BAR(KV_FULL + k % C::STAGES), (k / C::STAGES) & 1, nullptr,
+                                      p.status);
+                if (q_count > 0)
+                    mbar_wait_bounded(BAR(Q_FULL), (q_count - 1) & 1, nullptr, p.status);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, false);
+            constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, true);
+            uint32_t load_idx = 0, q_count = 0;
+            uint32_t ctr[2] = {0, 0}, items_x[2] = {0, 0};
+            bool ok = true;
+            auto qk = [&](int x, uint32_t kst) {
+                const uint32_t k_base = sKV + kst * C::TILE_BYTES;
+                const uint32_t q_base = sQ + x * C::TILE_BYTES;
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = (k >> 2) * C::CHUNK_BYTES + (k & 3) * 32;
+                    mma_ss(tmem_base + 128u * x, sdesc_sw128(q_base + off, 16, 1024),
+                           sdesc_sw128(k_base + off, 16, 1024), IDESC_QK, k > 0 ? 1u : 0u);
+                }
+                mma_commit(BAR(S_FULL + x));
+            };
+            auto pv = [&](int x, int jj, uint32_t vst) -> bool {
+                const uint32_t c = ctr[x] + jj;
+                if (!mbar_wait_bounded(BAR(P_FULL + x), c & 1, abort_flag, p.status)) return false;
+                if (jj == 0 && items_x[x] > 0 &&
+                    !mbar_wait_bounded(BAR(O_EMPTY + x), (items_x[x] - 1) & 1, abort_flag, p.status))
+                    return false;
+                tc_fence_after();
+                const uint32_t v_base = sKV + vst * C::TILE_BYTES;
+#pragma unroll
+                for (int k = 0; k < BN / 16; ++k) {
+                    const uint64_t bd = sdesc_sw128(v_base + k * 2048, C::CHUNK_BYTES, 1024);
+                    mma_ts(tmem_base + 256u + 128u * x, tmem_base + 128u * x + k * 8, bd, IDESC_PV,
+                           (jj > 0 || k > 0) ? 1u : 0u);
+                }
+                mma_commit(BAR(PV_DONE + x));
+                return true;
+            };
+            for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+                const int4 w = p.items[it];
+                const Geo a = item_geometry(p.q_indptr, p.kv_indptr, w.x, w.z, G, p.causal);
+                const Geo bq = item_geometry(p.q_indptr, p.kv_indptr, w.x, w.z + 1, G, p.causal);
+                const int nx[2] = {a.n_tiles, bq.t0 < bq.qo_len ? bq.n_tiles : 0};
+                const int nmax = max(nx[0], nx[1]);
+                if (nmax == 0) continue;
+                ok = mbar_wait_bounded(BAR(Q_FULL), q_count & 1, abort_flag, p.status);
+                ++q_count;
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t L0 = load_idx;
+                for (int j = 0; j <= nmax; ++j) {
+                    uint32_t vst = 0, kst = 0;
+                    if (j >= 1) {
+                        const uint32_t li = L0 + 2 * (j - 1) + 1;
+                        vst = li % C::STAGES;
+                        ok = mbar_wait_bounded(BAR(KV_FULL + vst), (li / C::STAGES) & 1, abort_flag,
+                                               p.status);
+                        if (!ok) break;
+                    }
+                    if (j >= 1 && j - 1 < nx[0]) {
+                        ok = pv(0, j - 1, vst);
+                        if (!ok) break;
+                    }
+                    if (j < nmax) {
+                        const uint32_t li = L0 + 2 * j;
+                        kst = li % C::STAGES;
+                        ok = mbar_wait_bounded(BAR(KV_FULL + kst), (li / C::STAGES) & 1, abort_flag,
+                                               p.status);
+                        if (!ok) break;
+                        tc_fence_after();
+                    }
+                    if (j < nx[0]) qk(0, kst);
+                    if (j >= 1 && j - 1 < nx[1]) {
+                        ok = pv(1, j - 1, vst);
+                        if (!ok) break;
+                    }
+                    if (j < nx[1]) qk(1, kst);
+                    if (j >= 1) mma_commit(BAR(KV_EMPTY + vst));
+                    if (j < nmax) mma_commit(BAR(KV_EMPTY + kst));
+                    if (j == nmax - 1) mma_commit(BAR(Q_EMPTY));
+                }
+                load_idx = L0 + 2 * nmax;
+                for (int x = 0; x < 2; ++x) {
+                    ctr[x] += nx[x];
+                    if (nx[x] > 0) ++items_x[x];
+                }
+            }
+            mma_commit(BAR(MMA_DRAIN));
+            mbar_wait_bounded(BAR(MMA_DRAIN), 0, nullptr, p.status);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ softmax / epilogue
+        const int X = warp >= 8 ? 1 : 0;
+        const int r = threadIdx.x - 128 - 128 * X;
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        const uint32_t s_addr = tmem_base + lane_base + 128u * X;
+        const uint32_t o_addr = tmem_base + lane_base + 256u + 128u * X;
+        const int Hq = p.num_qo_heads;
+        const bool fast_scale = p.scale_log2 > 0.f;
+        const float c_eff = fast_scale ? p.scale_log2 : 1.f;
+        uint32_t ctr = 0;
+        bool ok = true;
+        for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+            const int4 w = p.items[it];
+            const Geo x = item_geometry(p.q_indptr, p.kv_indptr, w.x, w.z + X, G, p.causal);
+            if (x.t0 >= x.qo_len) continue;  // this item has no tile B
+            const int row_t = x.t0 + r / G;
+            const int row_h = w.y * G + r % G;
+            const bool valid = row_t < x.qo_len;
+            const size_t out_row = (size_t)(x.q_start + row_t) * Hq + row_h;
+            if (x.n_tiles == 0) {
+                if (valid) {
+                    uint4* op = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) +
+                                                         out_row * D);
+#pragma unroll
+                    for (int c = 0; c < D / 8; ++c) op[c] = make_uint4(0, 0, 0, 0);
+                    if (p.lse) p.lse[out_row] = -INFINITY;
+                }
+                continue;
+            }
+            const int klim = p.causal ? min(row_t + x.kv_len - x.qo_len, x.kv_len - 1)
+                                      : x.kv_len - 1;
+            float m_used = -INFINITY, l = 0.f;
+            for (int j = 0; j < x.n_tiles; ++j) {
+                const uint32_t c = ctr + j;
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(S_FULL + X), c & 1, abort_flag,
+                                                               p.status));
+                if (!ok) break;
+                tc_fence_after();
+                float s[BN];
+#pragma unroll
+                for (int cc = 0; cc < BN / 32; ++cc) {
+                    uint32_t u[32];
+                    tmem_ld32(s_addr + cc * 32, u);
+                    tmem_wait_ld_regs(u);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) s[cc * 32 + i] = __uint_as_float(u[i]);
+                }
+                if (!fast_scale) {
+#pragma unroll
+                    for (int i = 0; i < BN; ++i) s[i] *= p.scale_log2;
+                }
+                if (j >= x.n_unmasked) {
+                    const int key0 = j * BN;
+#pragma unroll
+                    for (int i = 0; i < BN; ++i)
+                        if (key0 + i > klim) s[i] = -INFINITY;
+                }
+                float mx[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) mx[k] = s[k];
+#pragma unroll
+                for (int i = 8; i < BN; ++i) mx[i & 7] = fmaxf(mx[i & 7], s[i]);
+                const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * c_eff;
+                const bool grow = mt > m_used + kRescaleThreshold;
+                const float m_new = grow ? mt : m_used;
+                const float alpha = grow ? ex2_approx(m_used - m_new) : 1.f;
+                const float neg = m_new == -INFINITY ? 0.f : -m_new;
+                float sum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float p0 = ex2_approx(fmaf(s[cc * 64 + 2 * i], c_eff, neg));
+                        const float p1 = ex2_approx(fmaf(s[cc * 64 + 2 * i + 1], c_eff, neg));
+                        sum[i & 3] += p0 + p1;
+                        pk[i] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st32(s_addr + cc * 32, pk);
+                }
+                l = l * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
+                if (j > 0) {
+                    ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(PV_DONE + X), (c - 1) & 1,
+                                                                   abort_flag, p.status));
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (__any_sync(0xffffffffu, grow)) {
+#pragma unroll 1
+                        for (int cc = 0; cc < D / 32; ++cc) {
+                            uint32_t u[32];
+                            tmem_ld32(o_addr + cc * 32, u);
+                            tmem_wait_ld_regs(u);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+                            tmem_st32(o_addr + cc * 32, u);
+                        }
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(BAR(P_FULL + X));
+                m_used = m_new;
+            }
+            if (!ok) break;
+            ctr += x.n_tiles;
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(PV_DONE + X), (ctr - 1) & 1,
+                                                           abort_flag, p.status));
+            if (!ok) break;
+            tc_fence_after();
+            const float inv_l = l > 0.f ? 1.f / l : 0.f;
+            uint4* op = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + out_row * D);
+#pragma unroll 1
+            for (int cc = 0; cc < D / 32; ++cc) {
+                uint32_t u[32];
+                tmem_ld32(o_addr + cc * 32, u);
+                tmem_wait_ld_regs(u);
+                if (valid) {
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4) {
+                        uint4 q;
+                        q.x = pack_bf16x2(__uint_as_float(u[v4 * 8 + 0]) * inv_l,
+                                          __uint_as_float(u[v4 * 8 + 1]) * inv_l);
+                        q.y = pack_bf16x2(__uint_as_float(u[v4 * 8 + 2]) * inv_l,
+                                          __uint_as_float(u[v4 * 8 + 3]) * inv_l);
+                        q.z = pack_bf16x2(__uint_as_float(u[v4 * 8 + 4]) * inv_l,
+                                          __uint_as_float(u[v4 * 8 + 5]) * inv_l);
+                        q.w = pack_bf16x2(__uint_as_float(u[v4 * 8 + 6]) * inv_l,
+                                          __uint_as_float(u[v4 * 8 + 7]) * inv_l);
+                        op[cc * 4 + v4] = q;
+                    }
+                }
+            }
+            if (valid && p.lse)
+                p.lse[out_row] = l > 0.f ? (m_used + log2f(l)) * 0.69314718055994531f : -INFINITY;
+            tc_fence_before();
+            mbar_arrive(BAR(O_EMPTY + X));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 512);
+    }
+}
+
 // ------------------------------------------------------------------ host launchers
 template <int D>
 int smem_bytes() {
@@ -568,6 +938,21 @@ cudaError_t launch_attention(const Params& p, int grid, cudaStream_t stream) {
         configured[dev] = true;
     }
     attention_kernel<D><<<grid, THREADS, Cfg<D>::SMEM_BYTES, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_attention_pair(const Params& p, int grid, cudaStream_t stream) {
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(attention_pair_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             PairCfg::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    attention_pair_kernel<<<grid, PAIR_THREADS, PairCfg::SMEM_BYTES, stream>>>(p);
     return cudaGetLastError();
 }
 
