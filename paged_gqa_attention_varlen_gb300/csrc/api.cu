@@ -146,7 +146,7 @@ int encode_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint
 
 size_t prefill_ws_bytes(int batch, long long max_items) {
     const size_t tile_off = align_up((size_t)(batch + 1) * sizeof(int), 256);
-    return kWsArrays + tile_off + (size_t)max_items * sizeof(int4);
+    return kWsArrays + tile_off + (size_t)max_items * sizeof(prefill::WorkItem);
 }
 
 size_t decode_ws_bytes(int batch, int stride, int page_size, int hq, int d) {
@@ -283,8 +283,9 @@ int pgqa_ragged_prefill_bf16(const void* q, const void* k, const void* v, void* 
     CUtensorMap* tmaps = reinterpret_cast<CUtensorMap*>(ws + kWsTmapOffset);
     int* tile_off = reinterpret_cast<int*>(ws + kWsArrays);
     const size_t items_off = kWsArrays + align_up((size_t)(batch + 1) * sizeof(int), 256);
-    int4* items = reinterpret_cast<int4*>(ws + items_off);
-    const long long capacity = (long long)((st->ws_bytes - items_off) / sizeof(int4));
+    prefill::WorkItem* items = reinterpret_cast<prefill::WorkItem*>(ws + items_off);
+    const long long capacity =
+        (long long)((st->ws_bytes - items_off) / sizeof(prefill::WorkItem));
 
     // Tensor-map templates: row extents are placeholders (one box), patched on the
     // device from q_indptr[batch] / kv_indptr[batch] by the plan kernel.

@@ -43,6 +43,14 @@ constexpr int PAIR_THREADS = 384;  // + warps 8-11: softmax of the second q tile
 constexpr int PLAN_THREADS = 1024;
 constexpr int COST_BUCKETS = 4096;
 
+// One work item of the prefill: a (request, kv head, first q tile) triple plus the
+// request's offsets, written by the plan kernel so the attention roles need no further
+// global loads to place it.
+struct alignas(16) WorkItem {
+    int b, g, qt, cost;
+    int q_start, qo_len, kv_start, kv_len;
+};
+
 struct Params {
     const CUtensorMap* tm_q;   // in the workspace, patched by the plan kernel
     const CUtensorMap* tm_k;
@@ -51,7 +59,7 @@ struct Params {
     float* lse;
     const int* q_indptr;
     const int* kv_indptr;
-    const int4* items;         // {request, kv head, q tile, kv tiles}
+    const WorkItem* items;     // sorted longest first
     const WsHeader* hdr;
     int* status;
     int num_qo_heads;
@@ -71,7 +79,7 @@ struct PlanParams {
     int tiles_per_item;        // consecutive q tiles one work item covers (1 or 2)
     WsHeader* hdr;
     int* tile_off;             // [batch + 1]
-    int4* items;
+    WorkItem* items;
     long long item_capacity;
     CUtensorMap* tm_out;       // 3 maps: Q, K, V
 };

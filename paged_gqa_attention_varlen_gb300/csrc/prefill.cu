@@ -37,13 +37,13 @@ struct Geo {
     int n_unmasked;  // leading tiles in which every row sees every key
 };
 
-__device__ __forceinline__ Geo item_geometry(const int* q_indptr, const int* kv_indptr, int b,
+__device__ __forceinline__ Geo tile_geometry(int q_start, int qo_len, int kv_start, int kv_len,
                                              int qt, int group, int causal) {
     Geo x;
-    x.q_start = q_indptr[b];
-    x.qo_len = q_indptr[b + 1] - x.q_start;
-    x.kv_start = kv_indptr[b];
-    x.kv_len = kv_indptr[b + 1] - x.kv_start;
+    x.q_start = q_start;
+    x.qo_len = qo_len;
+    x.kv_start = kv_start;
+    x.kv_len = kv_len;
     const int tpt = BM / group;
     x.t0 = qt * tpt;
     const int t1 = min(x.qo_len, x.t0 + tpt);
@@ -53,6 +53,43 @@ __device__ __forceinline__ Geo item_geometry(const int* q_indptr, const int* kv_
     const int lim = causal ? min(x.t0 + x.kv_len - x.qo_len, x.kv_len - 1) : x.kv_len - 1;
     x.n_unmasked = lim >= 0 ? min((lim + 1) / BN, x.n_tiles) : 0;
     return x;
+}
+
+__device__ __forceinline__ Geo item_geometry(const int* q_indptr, const int* kv_indptr, int b,
+                                             int qt, int group, int causal) {
+    return tile_geometry(q_indptr[b], q_indptr[b + 1] - q_indptr[b], kv_indptr[b],
+                         kv_indptr[b + 1] - kv_indptr[b], qt, group, causal);
+}
+
+// geometry of q tile (w.qt + dt) of a work item
+__device__ __forceinline__ Geo geo_of(const WorkItem& w, int dt, int group, int causal) {
+    return tile_geometry(w.q_start, w.qo_len, w.kv_start, w.kv_len, w.qt + dt, group, causal);
+}
+
+__device__ __forceinline__ WorkItem load_item(const WorkItem* items, int i) {
+    const int4* v = reinterpret_cast<const int4*>(items + i);
+    const int4 a = __ldg(v), c = __ldg(v + 1);
+    WorkItem w;
+    w.b = a.x; w.g = a.y; w.qt = a.z; w.cost = a.w;
+    w.q_start = c.x; w.qo_len = c.y; w.kv_start = c.z; w.kv_len = c.w;
+    return w;
+}
+
+__device__ __forceinline__ void prefetch_l1(const void* ptr) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(ptr));
+}
+
+// Items are sorted longest first; CTA c walks them in "snake" order (rounds of gridDim
+// items, alternate rounds reversed), which balances the per-CTA totals of an LPT-sorted
+// list far better than a plain stride.  Every role of a CTA walks the same sequence.
+__device__ __forceinline__ int snake_next(int& r, int n) {
+    const int ncta = gridDim.x, cta = blockIdx.x;
+    for (;;) {
+        ++r;
+        if ((long long)r * ncta >= n) return -1;
+        const int idx = r * ncta + ((r & 1) ? ncta - 1 - cta : cta);
+        if (idx < n) return idx;
+    }
 }
 
 __device__ __forceinline__ int find_segment(const int* off, int n, int f) {
@@ -176,8 +213,19 @@ __global__ void __launch_bounds__(PLAN_THREADS)
         const int qt = (f - p.tile_off[b]) * p.tiles_per_item;
         const int cost = item_cost(p, b, qt);
         const int slot = atomicAdd(&hist[min(cost, COST_BUCKETS - 1)], 1);
-        for (int g = 0; g < p.num_kv_heads; ++g)
-            p.items[(long long)slot * p.num_kv_heads + g] = make_int4(b, g, qt, cost);
+        const int q0 = p.q_indptr[b], k0 = p.kv_indptr[b];
+        WorkItem w;
+        w.b = b;
+        w.qt = qt;
+        w.cost = cost;
+        w.q_start = q0;
+        w.qo_len = p.q_indptr[b + 1] - q0;
+        w.kv_start = k0;
+        w.kv_len = p.kv_indptr[b + 1] - k0;
+        for (int g = 0; g < p.num_kv_heads; ++g) {
+            w.g = g;
+            p.items[(long long)slot * p.num_kv_heads + g] = w;
+        }
     }
 
     // tensor maps with the real row extents
@@ -288,16 +336,20 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
             tensormap_acquire(p.tm_v);
             uint32_t load_idx = 0, q_count = 0;
             bool ok = true;
-            for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
-                const int4 w = p.items[it];
-                const Geo x = item_geometry(p.q_indptr, p.kv_indptr, w.x, w.z, G, p.causal);
+            int rr = -1;
+            int it = snake_next(rr, n_items);
+            while (ok && it >= 0) {
+                const WorkItem w = load_item(p.items, it);
+                it = snake_next(rr, n_items);
+                if (it >= 0) prefetch_l1(p.items + it);
+                const Geo x = geo_of(w, 0, G, p.causal);
                 if (x.n_tiles == 0) continue;
                 ok = mbar_wait_bounded(BAR(Q_EMPTY), (q_count & 1) ^ 1, abort_flag, p.status);
                 if (!ok) break;
                 mbar_arrive_expect_tx(BAR(Q_FULL), C::TILE_BYTES);
 #pragma unroll
                 for (int c = 0; c < C::CHUNKS; ++c)
-                    tma_load_3d(sQ + c * C::CHUNK_BYTES, p.tm_q, BAR(Q_FULL), c * 64, w.y * G,
+                    tma_load_3d(sQ + c * C::CHUNK_BYTES, p.tm_q, BAR(Q_FULL), c * 64, w.g * G,
                                 x.q_start + x.t0);
                 ++q_count;
                 // consumption order of the MMA warp: K0, (K1, V0), (K2, V1), ..., V_{n-1}
@@ -325,7 +377,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
 #pragma unroll
                     for (int c = 0; c < C::CHUNKS; ++c)
                         tma_load_2d(sKV + st * C::TILE_BYTES + c * C::CHUNK_BYTES, tm,
-                                    BAR(KV_FULL + st), w.y * D + c * 64, x.kv_start + j * BN);
+                                    BAR(KV_FULL + st), w.g * D + c * 64, x.kv_start + j * BN);
                     ++load_idx;
                 }
             }
@@ -375,9 +427,13 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
                 mma_commit(BAR(PV_DONE));
                 return true;
             };
-            for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
-                const int4 w = p.items[it];
-                const Geo x = item_geometry(p.q_indptr, p.kv_indptr, w.x, w.z, G, p.causal);
+            int rr = -1;
+            int it = snake_next(rr, n_items);
+            while (ok && it >= 0) {
+                const WorkItem w = load_item(p.items, it);
+                it = snake_next(rr, n_items);
+                if (it >= 0) prefetch_l1(p.items + it);
+                const Geo x = geo_of(w, 0, G, p.causal);
                 const int n = x.n_tiles;
                 if (n == 0) continue;
                 ok = mbar_wait_bounded(BAR(Q_FULL), q_count & 1, abort_flag, p.status);
@@ -424,11 +480,15 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
         const int Hq = p.num_qo_heads;
         uint32_t tile_ctr = 0;
         bool ok = true;
-        for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
-            const int4 w = p.items[it];
-            const Geo x = item_geometry(p.q_indptr, p.kv_indptr, w.x, w.z, G, p.causal);
+        int rr = -1;
+        int it = snake_next(rr, n_items);
+        while (ok && it >= 0) {
+            const WorkItem w = load_item(p.items, it);
+            it = snake_next(rr, n_items);
+            if (it >= 0) prefetch_l1(p.items + it);
+            const Geo x = geo_of(w, 0, G, p.causal);
             const int row_t = x.t0 + r / G;
-            const int row_h = w.y * G + r % G;
+            const int row_h = w.g * G + r % G;
             const bool valid = row_t < x.qo_len;
             const size_t out_row = (size_t)(x.q_start + row_t) * Hq + row_h;
             if (x.n_tiles == 0) {
@@ -578,6 +638,7 @@ struct PairCfg {
 // O rescale in tensor memory is skipped for most tiles.
 constexpr float kRescaleThreshold = 8.0f;
 
+
 __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const Params p) {
     using C = PairCfg;
     constexpr int D = C::D;
@@ -625,7 +686,6 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
     const uint32_t tmem_base = *tmem_slot;
     const int n_items = p.hdr->n_items;
     const int G = p.group;
-
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
@@ -634,10 +694,14 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
             tensormap_acquire(p.tm_v);
             uint32_t load_idx = 0, q_count = 0;
             bool ok = true;
-            for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
-                const int4 w = p.items[it];
-                const Geo a = item_geometry(p.q_indptr, p.kv_indptr, w.x, w.z, G, p.causal);
-                const Geo bq = item_geometry(p.q_indptr, p.kv_indptr, w.x, w.z + 1, G, p.causal);
+            int rr = -1;
+            int it = snake_next(rr, n_items);
+            while (ok && it >= 0) {
+                const WorkItem w = load_item(p.items, it);
+                it = snake_next(rr, n_items);
+                if (it >= 0) prefetch_l1(p.items + it);
+                const Geo a = geo_of(w, 0, G, p.causal);
+                const Geo bq = geo_of(w, 1, G, p.causal);
                 const int nA = a.n_tiles;
                 const int nB = bq.t0 < bq.qo_len ? bq.n_tiles : 0;
                 const int nmax = max(nA, nB);
@@ -647,13 +711,13 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
                 mbar_arrive_expect_tx(BAR(Q_FULL), C::TILE_BYTES * (nB > 0 ? 2 : 1));
 #pragma unroll
                 for (int c = 0; c < C::CHUNKS; ++c)
-                    tma_load_3d(sQ + c * C::CHUNK_BYTES, p.tm_q, BAR(Q_FULL), c * 64, w.y * G,
+                    tma_load_3d(sQ + c * C::CHUNK_BYTES, p.tm_q, BAR(Q_FULL), c * 64, w.g * G,
                                 a.q_start + a.t0);
                 if (nB > 0) {
 #pragma unroll
                     for (int c = 0; c < C::CHUNKS; ++c)
                         tma_load_3d(sQ + C::TILE_BYTES + c * C::CHUNK_BYTES, p.tm_q, BAR(Q_FULL),
-                                    c * 64, w.y * G, bq.q_start + bq.t0);
+                                    c * 64, w.g * G, bq.q_start + bq.t0);
                 }
                 ++q_count;
                 for (int s = 0; s < 2 * nmax; ++s) {
@@ -667,7 +731,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
 #pragma unroll
                     for (int c = 0; c < C::CHUNKS; ++c)
                         tma_load_2d(sKV + st * C::TILE_BYTES + c * C::CHUNK_BYTES, tm,
-                                    BAR(KV_FULL + st), w.y * D + c * 64, a.kv_start + j * BN);
+                                    BAR(KV_FULL + st), w.g * D + c * 64, a.kv_start + j * BN);
                     ++load_idx;
                 }
             }
@@ -716,10 +780,14 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
                 mma_commit(BAR(PV_DONE + x));
                 return true;
             };
-            for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
-                const int4 w = p.items[it];
-                const Geo a = item_geometry(p.q_indptr, p.kv_indptr, w.x, w.z, G, p.causal);
-                const Geo bq = item_geometry(p.q_indptr, p.kv_indptr, w.x, w.z + 1, G, p.causal);
+            int rr = -1;
+            int it = snake_next(rr, n_items);
+            while (ok && it >= 0) {
+                const WorkItem w = load_item(p.items, it);
+                it = snake_next(rr, n_items);
+                if (it >= 0) prefetch_l1(p.items + it);
+                const Geo a = geo_of(w, 0, G, p.causal);
+                const Geo bq = geo_of(w, 1, G, p.causal);
                 const int nx[2] = {a.n_tiles, bq.t0 < bq.qo_len ? bq.n_tiles : 0};
                 const int nmax = max(nx[0], nx[1]);
                 if (nmax == 0) continue;
@@ -780,12 +848,16 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
         const float c_eff = fast_scale ? p.scale_log2 : 1.f;
         uint32_t ctr = 0;
         bool ok = true;
-        for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
-            const int4 w = p.items[it];
-            const Geo x = item_geometry(p.q_indptr, p.kv_indptr, w.x, w.z + X, G, p.causal);
+        int rr = -1;
+        int it = snake_next(rr, n_items);
+        while (ok && it >= 0) {
+            const WorkItem w = load_item(p.items, it);
+            it = snake_next(rr, n_items);
+            if (it >= 0) prefetch_l1(p.items + it);
+            const Geo x = geo_of(w, X, G, p.causal);
             if (x.t0 >= x.qo_len) continue;  // this item has no tile B
             const int row_t = x.t0 + r / G;
-            const int row_h = w.y * G + r % G;
+            const int row_h = w.g * G + r % G;
             const bool valid = row_t < x.qo_len;
             const size_t out_row = (size_t)(x.q_start + row_t) * Hq + row_h;
             if (x.n_tiles == 0) {
@@ -807,18 +879,22 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
                                                                p.status));
                 if (!ok) break;
                 tc_fence_after();
+                // S row: four 32-column TMEM loads in flight, one wait
+                uint32_t u[4][32];
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) tmem_ld32(s_addr + cc * 32, u[cc]);
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) tmem_wait_ld_regs(u[cc]);
                 float s[BN];
 #pragma unroll
-                for (int cc = 0; cc < BN / 32; ++cc) {
-                    uint32_t u[32];
-                    tmem_ld32(s_addr + cc * 32, u);
-                    tmem_wait_ld_regs(u);
+                for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) s[cc * 32 + i] = __uint_as_float(u[i]);
-                }
+                    for (int i = 0; i < 32; ++i) s[cc * 32 + i] = __uint_as_float(u[cc][i]);
                 if (!fast_scale) {
+                    const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2);
 #pragma unroll
-                    for (int i = 0; i < BN; ++i) s[i] *= p.scale_log2;
+                    for (int i = 0; i < BN; i += 2)
+                        f2_unpack(f2_mul(f2_pack(s[i], s[i + 1]), c2), s[i], s[i + 1]);
                 }
                 if (j >= x.n_unmasked) {
                     const int key0 = j * BN;
@@ -828,29 +904,38 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
                 }
                 float mx[8];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) mx[k] = s[k];
+                for (int k = 0; k < 8; ++k) mx[k] = fmaxf(s[k], s[8 + k]);
 #pragma unroll
-                for (int i = 8; i < BN; ++i) mx[i & 7] = fmaxf(mx[i & 7], s[i]);
-                const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * c_eff;
+                for (int i = 16; i < BN; i += 16)
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) mx[k] = fmax3(mx[k], s[i + k], s[i + 8 + k]);
+                const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                                       fmaxf(mx[6], mx[7])) * c_eff;
                 const bool grow = mt > m_used + kRescaleThreshold;
                 const float m_new = grow ? mt : m_used;
                 const float alpha = grow ? ex2_approx(m_used - m_new) : 1.f;
                 const float neg = m_new == -INFINITY ? 0.f : -m_new;
-                float sum[4] = {0.f, 0.f, 0.f, 0.f};
+                const uint64_t c2 = f2_pack(c_eff, c_eff), n2 = f2_pack(neg, neg);
+                uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
                     uint32_t pk[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        const float p0 = ex2_approx(fmaf(s[cc * 64 + 2 * i], c_eff, neg));
-                        const float p1 = ex2_approx(fmaf(s[cc * 64 + 2 * i + 1], c_eff, neg));
-                        sum[i & 3] += p0 + p1;
+                        const int e = cc * 64 + 2 * i;
+                        float t0, t1;
+                        f2_unpack(f2_fma(f2_pack(s[e], s[e + 1]), c2, n2), t0, t1);
+                        const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
+                        if (i & 1) acc1 = f2_add(acc1, f2_pack(p0, p1));
+                        else acc0 = f2_add(acc0, f2_pack(p0, p1));
                         pk[i] = pack_bf16x2(p0, p1);
                     }
                     tmem_st32(s_addr + cc * 32, pk);
                 }
-                l = l * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
+                float a0, a1, a2, a3;
+                f2_unpack(acc0, a0, a1);
+                f2_unpack(acc1, a2, a3);
+                l = l * alpha + ((a0 + a1) + (a2 + a3));
                 if (j > 0) {
                     ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(PV_DONE + X), (c - 1) & 1,
                                                                    abort_flag, p.status));
@@ -862,9 +947,14 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
                             uint32_t u[32];
                             tmem_ld32(o_addr + cc * 32, u);
                             tmem_wait_ld_regs(u);
+                            const uint64_t al2 = f2_pack(alpha, alpha);
 #pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+                            for (int i = 0; i < 32; i += 2) {
+                                float o0, o1;
+                                f2_unpack(f2_mul(f2_pack(__uint_as_float(u[i]), __uint_as_float(u[i + 1])), al2), o0, o1);
+                                u[i] = __float_as_uint(o0);
+                                u[i + 1] = __float_as_uint(o1);
+                            }
                             tmem_st32(o_addr + cc * 32, u);
                         }
                     }
@@ -962,7 +1052,6 @@ cudaError_t launch_plan(const PlanParams& pp, const CUtensorMap& tq, const CUten
     return cudaGetLastError();
 }
 
-template cudaError_t launch_attention<128>(const Params&, int, cudaStream_t);
 template cudaError_t launch_attention<256>(const Params&, int, cudaStream_t);
 
 }  // namespace prefill
