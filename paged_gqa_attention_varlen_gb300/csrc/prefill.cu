@@ -629,7 +629,7 @@ struct PairCfg {
     static constexpr int CHUNK_BYTES = BM * 128;
     static constexpr int TILE_BYTES = BM * D * 2;
     static constexpr int STAGES = 4;
-    static constexpr int NUM_BARS = 19;
+    static constexpr int NUM_BARS = 15;
     static constexpr int SMEM_BYTES = 1024 + TILE_BYTES * (2 + STAGES) + 8 * NUM_BARS + 16;
 };
 
@@ -652,9 +652,11 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const uint32_t bar0 = smem_u32(bars);
     auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
-    constexpr int Q_FULL = 0, Q_EMPTY = 1, KV_FULL = 2, KV_EMPTY = 2 + C::STAGES,
-                  S_FULL = 2 + 2 * C::STAGES, P_FULL = S_FULL + 2, PV_DONE = P_FULL + 2,
-                  O_EMPTY = PV_DONE + 2, MMA_DRAIN = O_EMPTY + 2;
+    // STEP_FULL[t % 2]: the K/V tiles one MMA step consumes have landed (TMA tx count);
+    // STEP_DONE[t % 2]: every MMA of step t has completed, so its stages may be reused.
+    constexpr int Q_FULL = 0, Q_EMPTY = 1, STEP_FULL = 2, STEP_DONE = 4, S_FULL = 6,
+                  P_FULL = S_FULL + 2, PV_DONE = P_FULL + 2, O_EMPTY = PV_DONE + 2,
+                  MMA_DRAIN = O_EMPTY + 2;
     static_assert(MMA_DRAIN + 1 == C::NUM_BARS, "barrier count");
 
     const int warp = threadIdx.x >> 5;
@@ -662,11 +664,9 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
     if (threadIdx.x == 0) {
         mbar_init(BAR(Q_FULL), 1);
         mbar_init(BAR(Q_EMPTY), 1);
-        for (int s = 0; s < C::STAGES; ++s) {
-            mbar_init(BAR(KV_FULL + s), 1);
-            mbar_init(BAR(KV_EMPTY + s), 1);
-        }
         for (int x = 0; x < 2; ++x) {
+            mbar_init(BAR(STEP_FULL + x), 1);
+            mbar_init(BAR(STEP_DONE + x), 1);
             mbar_init(BAR(S_FULL + x), 1);
             mbar_init(BAR(P_FULL + x), 128);
             mbar_init(BAR(PV_DONE + x), 1);
@@ -688,11 +688,13 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
     const int G = p.group;
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
+        // An item of n K/V tiles is n + 1 MMA steps: step t consumes V_{t-1} and K_t.  The
+        // loads of step t go out once step t - 2 is done, which frees both their stages.
         if (lane == 0) {
             tensormap_acquire(p.tm_q);
             tensormap_acquire(p.tm_k);
             tensormap_acquire(p.tm_v);
-            uint32_t load_idx = 0, q_count = 0;
+            uint32_t load_idx = 0, q_count = 0, step = 0;
             bool ok = true;
             int rr = -1;
             int it = snake_next(rr, n_items);
@@ -720,66 +722,52 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
                                     c * 64, w.g * G, bq.q_start + bq.t0);
                 }
                 ++q_count;
-                for (int s = 0; s < 2 * nmax; ++s) {
-                    const int j = s >> 1;
-                    const CUtensorMap* tm = (s & 1) ? p.tm_v : p.tm_k;
-                    const uint32_t st = load_idx % C::STAGES;
-                    ok = mbar_wait_bounded(BAR(KV_EMPTY + st), ((load_idx / C::STAGES) & 1) ^ 1,
-                                           abort_flag, p.status);
-                    if (!ok) break;
-                    mbar_arrive_expect_tx(BAR(KV_FULL + st), C::TILE_BYTES);
+                const uint32_t L0 = load_idx;
+                for (int t = 0; t <= nmax; ++t, ++step) {
+                    if (step >= 2) {
+                        ok = mbar_wait_bounded(BAR(STEP_DONE + (step & 1)), ((step - 2) >> 1) & 1,
+                                               abort_flag, p.status);
+                        if (!ok) break;
+                    }
+                    const uint32_t bar = BAR(STEP_FULL + (step & 1));
+                    mbar_arrive_expect_tx(bar, C::TILE_BYTES * ((t >= 1) + (t < nmax)));
+                    if (t >= 1) {  // V_{t-1}
+                        const uint32_t st = (L0 + 2 * (t - 1) + 1) % C::STAGES;
 #pragma unroll
-                    for (int c = 0; c < C::CHUNKS; ++c)
-                        tma_load_2d(sKV + st * C::TILE_BYTES + c * C::CHUNK_BYTES, tm,
-                                    BAR(KV_FULL + st), w.g * D + c * 64, a.kv_start + j * BN);
-                    ++load_idx;
+                        for (int c = 0; c < C::CHUNKS; ++c)
+                            tma_load_2d(sKV + st * C::TILE_BYTES + c * C::CHUNK_BYTES, p.tm_v, bar,
+                                        w.g * D + c * 64, a.kv_start + (t - 1) * BN);
+                    }
+                    if (t < nmax) {  // K_t
+                        const uint32_t st = (L0 + 2 * t) % C::STAGES;
+#pragma unroll
+                        for (int c = 0; c < C::CHUNKS; ++c)
+                            tma_load_2d(sKV + st * C::TILE_BYTES + c * C::CHUNK_BYTES, p.tm_k, bar,
+                                        w.g * D + c * 64, a.kv_start + t * BN);
+                    }
                 }
+                load_idx = L0 + 2 * nmax;
             }
             if (!ok) {
-                const uint32_t first = load_idx > (uint32_t)C::STAGES ? load_idx - C::STAGES : 0;
-                for (uint32_t k = first; k < load_idx; ++k)
-                    mbar_wait_bounded(BAR(KV_FULL + k % C::STAGES), (k / C::STAGES) & 1, nullptr,
-                                      p.status);
+                // let every copy already issued land before the CTA exits
+                for (uint32_t s = step > 2 ? step - 2 : 0; s < step; ++s)
+                    mbar_wait_bounded(BAR(STEP_FULL + (s & 1)), (s >> 1) & 1, nullptr, p.status);
                 if (q_count > 0)
                     mbar_wait_bounded(BAR(Q_FULL), (q_count - 1) & 1, nullptr, p.status);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        // Step t of an item: P.V of A's tile t-1, Q.K^T of A's tile t, then the same for B.
+        // tcgen05.mma issue paces the tensor core, so this thread keeps its own waits and
+        // commits per step to a minimum: one wait for the step's K/V, one per P tile, and
+        // commits for S_A, S_B and the step (PV_DONE only after an item's last P.V).
         if (lane == 0) {
             constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, false);
             constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, true);
-            uint32_t load_idx = 0, q_count = 0;
+            uint32_t load_idx = 0, q_count = 0, step = 0;
             uint32_t ctr[2] = {0, 0}, items_x[2] = {0, 0};
             bool ok = true;
-            auto qk = [&](int x, uint32_t kst) {
-                const uint32_t k_base = sKV + kst * C::TILE_BYTES;
-                const uint32_t q_base = sQ + x * C::TILE_BYTES;
-#pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = (k >> 2) * C::CHUNK_BYTES + (k & 3) * 32;
-                    mma_ss(tmem_base + 128u * x, sdesc_sw128(q_base + off, 16, 1024),
-                           sdesc_sw128(k_base + off, 16, 1024), IDESC_QK, k > 0 ? 1u : 0u);
-                }
-                mma_commit(BAR(S_FULL + x));
-            };
-            auto pv = [&](int x, int jj, uint32_t vst) -> bool {
-                const uint32_t c = ctr[x] + jj;
-                if (!mbar_wait_bounded(BAR(P_FULL + x), c & 1, abort_flag, p.status)) return false;
-                if (jj == 0 && items_x[x] > 0 &&
-                    !mbar_wait_bounded(BAR(O_EMPTY + x), (items_x[x] - 1) & 1, abort_flag, p.status))
-                    return false;
-                tc_fence_after();
-                const uint32_t v_base = sKV + vst * C::TILE_BYTES;
-#pragma unroll
-                for (int k = 0; k < BN / 16; ++k) {
-                    const uint64_t bd = sdesc_sw128(v_base + k * 2048, C::CHUNK_BYTES, 1024);
-                    mma_ts(tmem_base + 256u + 128u * x, tmem_base + 128u * x + k * 8, bd, IDESC_PV,
-                           (jj > 0 || k > 0) ? 1u : 0u);
-                }
-                mma_commit(BAR(PV_DONE + x));
-                return true;
-            };
             int rr = -1;
             int it = snake_next(rr, n_items);
             while (ok && it >= 0) {
@@ -794,45 +782,59 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
                 ok = mbar_wait_bounded(BAR(Q_FULL), q_count & 1, abort_flag, p.status);
                 ++q_count;
                 if (!ok) break;
-                tc_fence_after();
                 const uint32_t L0 = load_idx;
-                for (int j = 0; j <= nmax; ++j) {
-                    uint32_t vst = 0, kst = 0;
-                    if (j >= 1) {
-                        const uint32_t li = L0 + 2 * (j - 1) + 1;
-                        vst = li % C::STAGES;
-                        ok = mbar_wait_bounded(BAR(KV_FULL + vst), (li / C::STAGES) & 1, abort_flag,
-                                               p.status);
-                        if (!ok) break;
+                for (int t = 0; t <= nmax; ++t, ++step) {
+                    ok = mbar_wait_bounded(BAR(STEP_FULL + (step & 1)), (step >> 1) & 1, abort_flag,
+                                           p.status);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t vst = (L0 + 2 * (t - 1) + 1) % C::STAGES;
+                    const uint32_t kst = (L0 + 2 * t) % C::STAGES;
+#pragma unroll
+                    for (int x = 0; x < 2; ++x) {
+                        if (t >= 1 && t - 1 < nx[x]) {
+                            const int jj = t - 1;
+                            ok = mbar_wait_bounded(BAR(P_FULL + x), (ctr[x] + jj) & 1, abort_flag,
+                                                   p.status);
+                            if (ok && jj == 0 && items_x[x] > 0)
+                                ok = mbar_wait_bounded(BAR(O_EMPTY + x), (items_x[x] - 1) & 1,
+                                                       abort_flag, p.status);
+                            if (!ok) break;
+                            tc_fence_after();
+                            const uint32_t v_base = sKV + vst * C::TILE_BYTES;
+#pragma unroll
+                            for (int k = 0; k < BN / 16; ++k)
+                                mma_ts(tmem_base + 256u + 128u * x, tmem_base + 128u * x + k * 8,
+                                       sdesc_sw128(v_base + k * 2048, C::CHUNK_BYTES, 1024),
+                                       IDESC_PV, (jj > 0 || k > 0) ? 1u : 0u);
+                            if (jj == nx[x] - 1) mma_commit(BAR(PV_DONE + x));
+                        }
+                        if (t < nx[x]) {
+                            const uint32_t k_base = sKV + kst * C::TILE_BYTES;
+                            const uint32_t q_base = sQ + x * C::TILE_BYTES;
+#pragma unroll
+                            for (int k = 0; k < D / 16; ++k) {
+                                const uint32_t off = (k >> 2) * C::CHUNK_BYTES + (k & 3) * 32;
+                                mma_ss(tmem_base + 128u * x, sdesc_sw128(q_base + off, 16, 1024),
+                                       sdesc_sw128(k_base + off, 16, 1024), IDESC_QK,
+                                       k > 0 ? 1u : 0u);
+                            }
+                            mma_commit(BAR(S_FULL + x));
+                        }
                     }
-                    if (j >= 1 && j - 1 < nx[0]) {
-                        ok = pv(0, j - 1, vst);
-                        if (!ok) break;
-                    }
-                    if (j < nmax) {
-                        const uint32_t li = L0 + 2 * j;
-                        kst = li % C::STAGES;
-                        ok = mbar_wait_bounded(BAR(KV_FULL + kst), (li / C::STAGES) & 1, abort_flag,
-                                               p.status);
-                        if (!ok) break;
-                        tc_fence_after();
-                    }
-                    if (j < nx[0]) qk(0, kst);
-                    if (j >= 1 && j - 1 < nx[1]) {
-                        ok = pv(1, j - 1, vst);
-                        if (!ok) break;
-                    }
-                    if (j < nx[1]) qk(1, kst);
-                    if (j >= 1) mma_commit(BAR(KV_EMPTY + vst));
-                    if (j < nmax) mma_commit(BAR(KV_EMPTY + kst));
-                    if (j == nmax - 1) mma_commit(BAR(Q_EMPTY));
+                    if (!ok) break;
+                    if (t == nmax - 1) mma_commit(BAR(Q_EMPTY));
+                    mma_commit(BAR(STEP_DONE + (step & 1)));
                 }
+                if (!ok) break;
                 load_idx = L0 + 2 * nmax;
+#pragma unroll
                 for (int x = 0; x < 2; ++x) {
                     ctr[x] += nx[x];
                     if (nx[x] > 0) ++items_x[x];
                 }
             }
+            // every MMA issued has completed before tensor memory is released
             mma_commit(BAR(MMA_DRAIN));
             mbar_wait_bounded(BAR(MMA_DRAIN), 0, nullptr, p.status);
         }
@@ -846,7 +848,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
         const int Hq = p.num_qo_heads;
         const bool fast_scale = p.scale_log2 > 0.f;
         const float c_eff = fast_scale ? p.scale_log2 : 1.f;
-        uint32_t ctr = 0;
+        uint32_t ctr = 0, items_done = 0;
         bool ok = true;
         int rr = -1;
         int it = snake_next(rr, n_items);
@@ -936,11 +938,9 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
                 f2_unpack(acc0, a0, a1);
                 f2_unpack(acc1, a2, a3);
                 l = l * alpha + ((a0 + a1) + (a2 + a3));
+                // O may be rescaled now: S_FULL of this tile was committed after the previous
+                // P.V by the same issuing thread, so that P.V has completed
                 if (j > 0) {
-                    ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(PV_DONE + X), (c - 1) & 1,
-                                                                   abort_flag, p.status));
-                    if (!ok) break;
-                    tc_fence_after();
                     if (__any_sync(0xffffffffu, grow)) {
 #pragma unroll 1
                         for (int cc = 0; cc < D / 32; ++cc) {
@@ -966,8 +966,9 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
             }
             if (!ok) break;
             ctr += x.n_tiles;
-            ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(PV_DONE + X), (ctr - 1) & 1,
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(PV_DONE + X), items_done & 1,
                                                            abort_flag, p.status));
+            ++items_done;
             if (!ok) break;
             tc_fence_after();
             const float inv_l = l > 0.f ? 1.f / l : 0.f;
