@@ -846,6 +846,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
         const uint32_t s_addr = tmem_base + lane_base + 128u * X;
         const uint32_t o_addr = tmem_base + lane_base + 256u + 128u * X;
         const int Hq = p.num_qo_heads;
+        const bool o32 = (reinterpret_cast<uintptr_t>(p.o) & 31) == 0;
         const bool fast_scale = p.scale_log2 > 0.f;
         const float c_eff = fast_scale ? p.scale_log2 : 1.f;
         uint32_t ctr = 0, items_done = 0;
@@ -979,18 +980,20 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
                 tmem_ld32(o_addr + cc * 32, u);
                 tmem_wait_ld_regs(u);
                 if (valid) {
+                    uint32_t pk[16];
 #pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4) {
-                        uint4 q;
-                        q.x = pack_bf16x2(__uint_as_float(u[v4 * 8 + 0]) * inv_l,
-                                          __uint_as_float(u[v4 * 8 + 1]) * inv_l);
-                        q.y = pack_bf16x2(__uint_as_float(u[v4 * 8 + 2]) * inv_l,
-                                          __uint_as_float(u[v4 * 8 + 3]) * inv_l);
-                        q.z = pack_bf16x2(__uint_as_float(u[v4 * 8 + 4]) * inv_l,
-                                          __uint_as_float(u[v4 * 8 + 5]) * inv_l);
-                        q.w = pack_bf16x2(__uint_as_float(u[v4 * 8 + 6]) * inv_l,
-                                          __uint_as_float(u[v4 * 8 + 7]) * inv_l);
-                        op[cc * 4 + v4] = q;
+                    for (int e = 0; e < 16; ++e)
+                        pk[e] = pack_bf16x2(__uint_as_float(u[2 * e]) * inv_l,
+                                            __uint_as_float(u[2 * e + 1]) * inv_l);
+                    if (o32) {  // 32-byte stores: whole sectors, half the store instructions
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+                            st_global_v8(op + cc * 4 + h * 2, pk + 8 * h);
+                    } else {
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4)
+                            op[cc * 4 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2],
+                                                         pk[4 * v4 + 3]);
                     }
                 }
             }
