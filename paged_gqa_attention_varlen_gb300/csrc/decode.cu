@@ -16,14 +16,10 @@
 //  * plan_kernel: sanitises kv_lens and cuts each request into chunks of CHUNK keys.
 //    The cut depends on the request alone, so a request's result does not depend on
 //    what else is in the batch.
-//  * decode_kernel: one warp per (chunk, kv head).  Lane i holds head_dim elements
-//    4i..4i+3 of the G query heads; each page's 16 K rows and 16 V rows are fetched
-//    with 8-byte loads (a 256-byte row per warp instruction), the next page's rows are
-//    prefetched into registers while the current page is computed, the G x 16 partial
-//    dot products are reduced across lanes by a transposing butterfly (62 shuffles for
-//    G = 4), and the online softmax keeps a running max and sum per head.  A request
-//    with a single chunk writes its bf16 output directly; otherwise each chunk writes a
-//    normalised fp32 partial output and its lse.
+//  * decode_tma_kernel: one warp per (chunk, kv head).  Pages stream through a per-warp
+//    TMA ring in shared memory; the online softmax keeps a running max and sum per
+//    head.  A request with a single chunk writes its bf16 output directly; otherwise
+//    each chunk writes a normalised fp32 partial output and its lse.
 //  * merge_kernel: one warp per (request, head) with more than one chunk combines the
 //    partials with weights exp(lse_c - max lse).
 #include "ptx.cuh"
@@ -76,14 +72,6 @@ __device__ __forceinline__ int find_request(const int* off, int batch, int f) {
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
 
-__device__ __forceinline__ uint2 ldg_nc_v2(const void* ptr) {
-    uint2 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
-                 : "=r"(r.x), "=r"(r.y)
-                 : "l"(ptr));
-    return r;
-}
-
 // One butterfly step of the transposing reduction: N values per lane become N/2, each
 // the sum over the lane pair (lane, lane ^ OFF); the lane with bit OFF set keeps the
 // upper half.  With N == 1 it is a plain butterfly add.
@@ -116,35 +104,71 @@ __device__ __forceinline__ void transpose_reduce(float* a, int lane) {
     tr_step<cmax(N / 16, 1), 1>(a, lane);
 }
 
+// ------------------------------------------------------------ TMA-staged decode
+// One warp per (chunk, kv head) item.  The warp streams its pages with TMA (one 4 KB box
+// per page for K and one for V) into a private two-stage ring in shared memory; lane 0
+// issues the copies and refills a stage as soon as the warp has finished reading it.
+// Lane (tp, ds) = (lane / 16, lane % 16) works on head-dim elements 8*ds .. 8*ds+7 of
+// the page's tokens with parity tp: 16-byte shared-memory reads of two whole K (V) rows
+// per warp instruction, packed f32x2 FMAs, and a transposing reduction of the 8*G
+// partial dot products over the 16 lanes of a parity (30 shuffles for G = 4).
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+// 8 bf16 -> 4 packed fp32 pairs (element 2k in the low half of pair k)
+__device__ __forceinline__ void bf16x8_to_pairs(const uint4& r, uint64_t (&o)[4]) {
+    o[0] = f2_pack(bf_lo(r.x), bf_hi(r.x));
+    o[1] = f2_pack(bf_lo(r.y), bf_hi(r.y));
+    o[2] = f2_pack(bf_lo(r.z), bf_hi(r.z));
+    o[3] = f2_pack(bf_lo(r.w), bf_hi(r.w));
+}
+
 template <int G>
-__global__ void __launch_bounds__(WARPS * 32) decode_kernel(const Params p) {
+__global__ void __launch_bounds__(WARPS * 32, G >= 8 ? 2 : 3)
+    decode_tma_kernel(const __grid_constant__ Params p) {
     constexpr int D = HEAD_DIM;
-    constexpr int NV = 16 * G;                       // scores per page
-    constexpr int VPL = NV >= 32 ? NV / 32 : 1;      // scores held per lane after reduction
-    constexpr int GS = 32 / G;                       // lanes holding one head's scores
-    __shared__ float ps_all[WARPS][16 * G];
+    constexpr int NV = 8 * G;                     // partial dot products per lane per page
+    constexpr int VPL = NV >= 16 ? NV / 16 : 1;   // full scores per lane after the reduction
+    constexpr int GS = 16 / G;                    // d-slices per head among the score lanes
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
     const int lane = threadIdx.x & 31;
     const int wib = threadIdx.x >> 5;
-    float* ps = ps_all[wib];
+    const int tp = lane >> 4, ds = lane & 15;
+    uint8_t* wsm = smem + wib * WARP_SMEM;
+    const uint32_t stage0 = smem_u32(wsm);
+    float* ps = reinterpret_cast<float*>(wsm + STAGES * STAGE_BYTES);  // [16 tokens][G]
+    const uint32_t full0 = smem_u32(wsm + STAGES * STAGE_BYTES + 512);
+    if (lane == 0) {
+        for (int s = 0; s < STAGES; ++s) mbar_init(full0 + 8 * s, 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+
     const int Hq = p.num_qo_heads, Hk = p.num_kv_heads;
     const int total_chunks = __ldg(p.chunk_off + p.batch);
     const long long n_items = (long long)total_chunks * Hk;
-    const long long row_stride = (long long)Hk * D;  // elements between consecutive slots
-    const __nv_bfloat16* kp = reinterpret_cast<const __nv_bfloat16*>(p.k_pages);
-    const __nv_bfloat16* vp = reinterpret_cast<const __nv_bfloat16*>(p.v_pages);
 
     // head / token of each score this lane holds after the reduction
-    int my_h[VPL], my_t[VPL];
+    int my_h[VPL], my_i[VPL];
 #pragma unroll
     for (int x = 0; x < VPL; ++x) {
-        const int v = NV >= 32 ? lane * VPL + x : lane >> 1;
-        my_h[x] = v / 16;
-        my_t[x] = v % 16;
+        const int v = NV >= 16 ? ds * VPL + x : ds >> 1;
+        my_h[x] = v / 8;
+        my_i[x] = v % 8;
     }
     const int head_of_lane = my_h[0];
-    const bool dup_lane = NV < 32 && (lane & 1);
+    const bool dup_lane = NV < 16 && (ds & 1);
+    uint32_t issued = 0, consumed = 0;  // pages this warp loaded / used (ring position)
+    bool ok = true;
 
-    for (long long item = (long long)blockIdx.x * WARPS + wib; item < n_items;
+    for (long long item = (long long)blockIdx.x * WARPS + wib; ok && item < n_items;
          item += (long long)gridDim.x * WARPS) {
         const int f = (int)(item / Hk);
         const int g = (int)(item % Hk);
@@ -154,82 +178,98 @@ __global__ void __launch_bounds__(WARPS * 32) decode_kernel(const Params p) {
         const int kv_len = __ldg(p.kv_eff + b);
         const int tok0 = c * CHUNK;
         const int tok1 = min(kv_len, tok0 + CHUNK);
+        const int page0 = tok0 / PAGE;
+        const int np = (tok1 - tok0 + PAGE - 1) / PAGE;
+        const int* pt_row = p.page_table + (size_t)b * p.page_table_stride;
 
-        float q[G][4];
+        auto issue = [&](int page) {  // lane 0 only
+            const int pid = __ldg(pt_row + page);
+            const uint32_t st = issued % STAGES;
+            const uint32_t bar = full0 + 8 * st;
+            if (pid >= 0 && pid < p.num_pages) {
+                mbar_arrive_expect_tx(bar, STAGE_BYTES);
+                const uint32_t dst = stage0 + st * STAGE_BYTES;
+                tma_load_2d(dst, &p.tm_kpages, bar, g * D, pid * PAGE);
+                tma_load_2d(dst + PAGE_HEAD_BYTES, &p.tm_vpages, bar, g * D, pid * PAGE);
+            } else {
+                atomicOr(p.status, PGQA_DEV_BOUNDS);
+                mbar_arrive(bar);  // the page is skipped; keep the ring in phase
+            }
+        };
+        const int prime = min(np, STAGES);
+        for (int k = 0; k < prime; ++k) {
+            if (lane == 0) issue(page0 + k);
+            ++issued;
+        }
+
+        uint64_t q2[G][4];
         {
-            const uint2* qp = reinterpret_cast<const uint2*>(
+            const uint4* qp = reinterpret_cast<const uint4*>(
                 reinterpret_cast<const __nv_bfloat16*>(p.q) + ((size_t)b * Hq + g * G) * D);
+            const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-                const uint2 u = __ldg(qp + h * (D / 4) + lane);
-                q[h][0] = bf_lo(u.x) * p.scale_log2;
-                q[h][1] = bf_hi(u.x) * p.scale_log2;
-                q[h][2] = bf_lo(u.y) * p.scale_log2;
-                q[h][3] = bf_hi(u.y) * p.scale_log2;
+                uint64_t t[4];
+                bf16x8_to_pairs(__ldg(qp + h * (D / 8) + ds), t);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) q2[h][e] = f2_mul(t[e], sc2);
             }
         }
-        float o[G][4];
+        uint64_t o2[G][4];
         float m[G];
+        const uint64_t zero2 = f2_pack(0.f, 0.f);
 #pragma unroll
         for (int h = 0; h < G; ++h) {
             m[h] = -INFINITY;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) o[h][e] = 0.f;
+            for (int e = 0; e < 4; ++e) o2[h][e] = zero2;
         }
         float lp = 0.f;
 
-        const int page0 = tok0 / PAGE;
-        const int page1 = (tok1 + PAGE - 1) / PAGE;  // exclusive
-        const int* pt_row = p.page_table + (size_t)b * p.page_table_stride;
-
-        uint2 kr[16], vr[16];
-        auto load_page = [&](int page) {
-            int pid = __ldg(pt_row + page);
-            const bool ok = pid >= 0 && pid < p.num_pages;
-            if (!ok && lane == 0) atomicOr(p.status, PGQA_DEV_BOUNDS);
-            const int base_tok = page * PAGE;
-            const size_t base = ((size_t)(ok ? pid : 0) * PAGE * Hk + g) * D + lane * 4;
-#pragma unroll
-            for (int t = 0; t < 16; ++t) {
-                const bool valid = ok && (base_tok + t < tok1);
-                kr[t] = valid ? ldg_nc_v2(kp + base + t * row_stride) : make_uint2(0, 0);
-                vr[t] = valid ? ldg_nc_v2(vp + base + t * row_stride) : make_uint2(0, 0);
-            }
-        };
-        if (page0 < page1) load_page(page0);
-        for (int page = page0; page < page1; ++page) {
-            uint2 kc[16], vc[16];
-#pragma unroll
-            for (int t = 0; t < 16; ++t) {
-                kc[t] = kr[t];
-                vc[t] = vr[t];
-            }
-            if (page + 1 < page1) load_page(page + 1);
-            const int base_tok = page * PAGE;
+        for (int pi = 0; pi < np; ++pi) {
+            const uint32_t st = consumed % STAGES;
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(full0 + 8 * st, (consumed / STAGES) & 1,
+                                                           nullptr, p.status));
+            if (!ok) break;
+            ++consumed;
+            const int page = page0 + pi;
+            const int pid = __ldg(pt_row + page);
+            const int nvalid = (pid >= 0 && pid < p.num_pages) ? min(PAGE, tok1 - page * PAGE) : 0;
+            const uint32_t kbase = stage0 + st * STAGE_BYTES + ds * 16;
+            const uint32_t vbase = kbase + PAGE_HEAD_BYTES;
 
             float part[NV];
 #pragma unroll
-            for (int t = 0; t < 16; ++t) {
-                const float k0 = bf_lo(kc[t].x), k1 = bf_hi(kc[t].x);
-                const float k2 = bf_lo(kc[t].y), k3 = bf_hi(kc[t].y);
+            for (int i = 0; i < 8; ++i) {
+                uint64_t k2[4];
+                bf16x8_to_pairs(lds128(kbase + (2 * i + tp) * (D * 2)), k2);
 #pragma unroll
-                for (int h = 0; h < G; ++h)
-                    part[h * 16 + t] = fmaf(q[h][0], k0, fmaf(q[h][1], k1,
-                                            fmaf(q[h][2], k2, q[h][3] * k3)));
+                for (int h = 0; h < G; ++h) {
+                    uint64_t acc = f2_mul(q2[h][0], k2[0]);
+                    acc = f2_fma(q2[h][1], k2[1], acc);
+                    acc = f2_fma(q2[h][2], k2[2], acc);
+                    acc = f2_fma(q2[h][3], k2[3], acc);
+                    float a0, a1;
+                    f2_unpack(acc, a0, a1);
+                    part[h * 8 + i] = a0 + a1;
+                }
             }
-            transpose_reduce<NV>(part, lane);
+            tr_step<NV, 8>(part, lane);
+            tr_step<cmax(NV / 2, 1), 4>(part, lane);
+            tr_step<cmax(NV / 4, 1), 2>(part, lane);
+            tr_step<cmax(NV / 8, 1), 1>(part, lane);
 
             float sc[VPL];
             float gmax = -INFINITY;
 #pragma unroll
             for (int x = 0; x < VPL; ++x) {
-                const bool valid = base_tok + my_t[x] < tok1;
-                sc[x] = valid ? part[x] : -INFINITY;
+                sc[x] = 2 * my_i[x] + tp < nvalid ? part[x] : -INFINITY;
                 gmax = fmaxf(gmax, sc[x]);
             }
 #pragma unroll
-            for (int off = GS / 2; off >= 1; off >>= 1)
+            for (int off = 1; off < GS; off <<= 1)
                 gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, off));
+            gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, 16));
             float alpha[G];
             float m_use_mine = 0.f, alpha_mine = 1.f;
 #pragma unroll
@@ -249,18 +289,25 @@ __global__ void __launch_bounds__(WARPS * 32) decode_kernel(const Params p) {
             for (int x = 0; x < VPL; ++x) {
                 const float pv = ex2_approx(sc[x] - m_use_mine);
                 psum += pv;
-                ps[my_t[x] * G + my_h[x]] = pv;
+                ps[(2 * my_i[x] + tp) * G + my_h[x]] = pv;
             }
             lp = lp * alpha_mine + (dup_lane ? 0.f : psum);
             __syncwarp();
 #pragma unroll
-            for (int h = 0; h < G; ++h)
+            for (int h = 0; h < G; ++h) {
+                const uint64_t a2 = f2_pack(alpha[h], alpha[h]);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) o[h][e] *= alpha[h];
+                for (int e = 0; e < 4; ++e) o2[h][e] = f2_mul(o2[h][e], a2);
+            }
 #pragma unroll
-            for (int t = 0; t < 16; ++t) {
-                const float v0 = bf_lo(vc[t].x), v1 = bf_hi(vc[t].x);
-                const float v2 = bf_lo(vc[t].y), v3 = bf_hi(vc[t].y);
+            for (int i = 0; i < 8; ++i) {
+                const int t = 2 * i + tp;
+                uint64_t v2[4];
+                bf16x8_to_pairs(lds128(vbase + t * (D * 2)), v2);
+                if (nvalid < PAGE && t >= nvalid) {  // slots past kv_len may hold anything
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) v2[e] = zero2;
+                }
                 float pr[G];
                 if constexpr (G % 4 == 0) {
 #pragma unroll
@@ -277,40 +324,70 @@ __global__ void __launch_bounds__(WARPS * 32) decode_kernel(const Params p) {
                 }
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
-                    o[h][0] = fmaf(pr[h], v0, o[h][0]);
-                    o[h][1] = fmaf(pr[h], v1, o[h][1]);
-                    o[h][2] = fmaf(pr[h], v2, o[h][2]);
-                    o[h][3] = fmaf(pr[h], v3, o[h][3]);
+                    const uint64_t pp = f2_pack(pr[h], pr[h]);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) o2[h][e] = f2_fma(pp, v2[e], o2[h][e]);
                 }
             }
-            __syncwarp();
+            __syncwarp();  // every lane is done with this stage and with ps
+            if (pi + STAGES < np) {
+                if (lane == 0) {
+                    fence_async_smem();
+                    issue(page0 + pi + STAGES);
+                }
+                ++issued;
+            }
         }
+        if (!ok) break;
 
-        // finish: per-head sums, normalise, write
+        // the two token parities hold partial sums of the same outputs: combine them
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                o2[h][e] = f2_add(o2[h][e], __shfl_xor_sync(0xffffffffu, o2[h][e], 16));
         float lsum = lp;
 #pragma unroll
-        for (int off = GS / 2; off >= 1; off >>= 1)
-            lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+        for (int off = 1; off < GS; off <<= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+        lsum += __shfl_xor_sync(0xffffffffu, lsum, 16);
 #pragma unroll
         for (int h = 0; h < G; ++h) {
             const float l = __shfl_sync(0xffffffffu, lsum, h * GS);
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const float lse_v = l > 0.f ? (m[h] + log2f(l)) * 0.69314718055994531f : -INFINITY;
             const int hq = g * G + h;
-            if (nch == 1) {
-                __nv_bfloat16* op = reinterpret_cast<__nv_bfloat16*>(p.o) + ((size_t)b * Hq + hq) * D;
-                uint2 u;
-                u.x = pack_bf16x2(o[h][0] * inv, o[h][1] * inv);
-                u.y = pack_bf16x2(o[h][2] * inv, o[h][3] * inv);
-                *reinterpret_cast<uint2*>(op + lane * 4) = u;
-                if (lane == 0 && p.lse) p.lse[(size_t)b * Hq + hq] = lse_v;
-            } else {
-                float* op = p.part_o + ((size_t)f * Hq + hq) * D;
-                *reinterpret_cast<float4*>(op + lane * 4) =
-                    make_float4(o[h][0] * inv, o[h][1] * inv, o[h][2] * inv, o[h][3] * inv);
-                if (lane == 0) p.part_lse[(size_t)f * Hq + hq] = lse_v;
+            float o[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) f2_unpack(o2[h][e], o[2 * e], o[2 * e + 1]);
+            if (tp == 0) {
+                if (nch == 1) {
+                    uint4 u;
+                    u.x = pack_bf16x2(o[0] * inv, o[1] * inv);
+                    u.y = pack_bf16x2(o[2] * inv, o[3] * inv);
+                    u.z = pack_bf16x2(o[4] * inv, o[5] * inv);
+                    u.w = pack_bf16x2(o[6] * inv, o[7] * inv);
+                    reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) +
+                                             ((size_t)b * Hq + hq) * D)[ds] = u;
+                } else {
+                    float4* op = reinterpret_cast<float4*>(p.part_o + ((size_t)f * Hq + hq) * D);
+                    op[2 * ds] = make_float4(o[0] * inv, o[1] * inv, o[2] * inv, o[3] * inv);
+                    op[2 * ds + 1] = make_float4(o[4] * inv, o[5] * inv, o[6] * inv, o[7] * inv);
+                }
+            }
+            if (lane == 0) {
+                if (nch == 1) {
+                    if (p.lse) p.lse[(size_t)b * Hq + hq] = lse_v;
+                } else {
+                    p.part_lse[(size_t)f * Hq + hq] = lse_v;
+                }
             }
         }
+    }
+    // copies still in flight (an aborted item) land before the warp exits
+    while (consumed < issued) {
+        mbar_wait_bounded(full0 + 8 * (consumed % STAGES), (consumed / STAGES) & 1, nullptr,
+                          p.status);
+        ++consumed;
     }
 }
 
@@ -358,6 +435,42 @@ cudaError_t launch_plan(const PlanParams& pp, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// Tensor maps over the paged K and V caches viewed as [num_pages * PAGE, Hk * D] bf16;
+// one box is one page of one kv head (PAGE rows x D elements, 4 KB).
+cudaError_t prepare_page_maps(Params& p, const void* k_pages, const void* v_pages,
+                              int num_pages, int num_kv_heads) {
+    static EncodeTiledFn encode = nullptr;
+    if (encode == nullptr) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                         cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
+            return e != cudaSuccess ? e : cudaErrorNotSupported;
+        encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    const cuuint64_t dims[2] = {(cuuint64_t)num_kv_heads * HEAD_DIM,
+                                (cuuint64_t)(num_pages > 0 ? num_pages : 1) * PAGE};
+    const cuuint64_t strides[1] = {(cuuint64_t)num_kv_heads * HEAD_DIM * 2};
+    const cuuint32_t box[2] = {HEAD_DIM, PAGE};
+    const cuuint32_t estr[2] = {1, 1};
+    CUtensorMap* maps[2] = {&p.tm_kpages, &p.tm_vpages};
+    const void* bases[2] = {k_pages, v_pages};
+    for (int i = 0; i < 2; ++i) {
+        CUresult r = encode(maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(bases[i]),
+                            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    return cudaSuccess;
+}
+
 template <int G>
 static cudaError_t launch_decode_g(const Params& p, int num_sms, cudaStream_t stream) {
     static int blocks_per_sm[64] = {};
@@ -365,14 +478,17 @@ static cudaError_t launch_decode_g(const Params& p, int num_sms, cudaStream_t st
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) dev = 0;
     if (blocks_per_sm[dev] == 0) {
+        cudaError_t e = cudaFuncSetAttribute(decode_tma_kernel<G>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e != cudaSuccess) return e;
         int n = 0;
-        cudaError_t e =
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<G>, WARPS * 32, 0);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_tma_kernel<G>, WARPS * 32,
+                                                          SMEM_BYTES);
         if (e != cudaSuccess) return e;
         blocks_per_sm[dev] = n > 0 ? n : 1;
     }
     const int grid = num_sms * blocks_per_sm[dev];
-    decode_kernel<G><<<grid, WARPS * 32, 0, stream>>>(p);
+    decode_tma_kernel<G><<<grid, WARPS * 32, SMEM_BYTES, stream>>>(p);
     return cudaGetLastError();
 }
 

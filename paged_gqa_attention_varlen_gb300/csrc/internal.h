@@ -92,9 +92,16 @@ constexpr int CHUNK = 1024;        // tokens per split-KV chunk (fixed: depends 
                                    // but the request, so results do not depend on the batch)
 constexpr int HEAD_DIM = 128;
 constexpr int WARPS = 4;           // warps per CTA, one work item per warp
+constexpr int STAGES = 2;          // pages in flight per warp (TMA ring in shared memory)
+constexpr int PAGE_HEAD_BYTES = PAGE * HEAD_DIM * 2;               // 4 KB
+constexpr int STAGE_BYTES = 2 * PAGE_HEAD_BYTES;                   // K and V of one page
+constexpr int WARP_SMEM = STAGES * STAGE_BYTES + 1024;             // + scores, barriers
+constexpr int SMEM_BYTES = 1024 + WARPS * WARP_SMEM;
 constexpr int PLAN_THREADS = 1024;
 
 struct Params {
+    CUtensorMap tm_kpages;      // [num_pages * PAGE rows, Hk * D] bf16, box one page of one head
+    CUtensorMap tm_vpages;
     const void* q;
     const void* k_pages;
     const void* v_pages;

@@ -122,6 +122,12 @@ __device__ __forceinline__ void regs_alloc() {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+// make this thread's generic-proxy shared-memory accesses visible / ordered before later
+// async-proxy (TMA) accesses to the same memory
+__device__ __forceinline__ void fence_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // 32-byte global store (sm_100+); the address must be 32-byte aligned.
 __device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t* v) {
     asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(ptr), "r"(v[0]),
