@@ -449,7 +449,7 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--ref-rows", type=int, default=3000,
                     help="oracle rows per CPU-baseline / reference step")
-    ap.add_argument("--cpu-rows", type=int, default=150000,
+    ap.add_argument("--cpu-rows", type=int, default=800000,
                     help="oracle rows timed for the cpu_baseline object (about 10-30 s)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", choices=["prefill_hd128", "prefix_hd256", "long", "tiny",
