@@ -42,6 +42,7 @@ constexpr int THREADS = 256;     // warp 0 TMA, warp 1 MMA, warps 4-7 softmax/ep
 constexpr int PAIR_THREADS = 384;  // + warps 8-11: softmax of the second q tile
 constexpr int PLAN_THREADS = 1024;
 constexpr int COST_BUCKETS = 4096;
+constexpr int PLAN_SMEM_BATCH = 2048;  // batches up to this size plan out of shared memory
 
 // One work item of the prefill: a (request, kv head, first q tile) triple plus the
 // request's offsets, written by the plan kernel so the attention roles need no further

@@ -104,27 +104,45 @@ __device__ __forceinline__ int find_segment(const int* off, int n, int f) {
 }
 
 // K/V tiles of the longest q tile of an item (the item covers tiles qt..qt+tpi-1 that exist)
-__device__ __forceinline__ int item_cost(const PlanParams& p, int b, int qt) {
-    const long long qo = p.q_indptr[b + 1] - p.q_indptr[b];
+__device__ __forceinline__ int item_cost(const PlanParams& p, const int* qi, const int* ki, int b,
+                                         int qt) {
+    const long long qo = qi[b + 1] - qi[b];
     const int tiles = (int)((qo * p.group + BM - 1) / BM);
     const int last = min(qt + p.tiles_per_item, tiles) - 1;
-    return item_geometry(p.q_indptr, p.kv_indptr, b, last, p.group, p.causal).n_tiles;
+    return item_geometry(qi, ki, b, last, p.group, p.causal).n_tiles;
 }
 
 // ---------------------------------------------------------------------------- plan
 __global__ void __launch_bounds__(PLAN_THREADS)
     plan_kernel(PlanParams p, const __grid_constant__ CUtensorMap tq,
                 const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv) {
+    // the attention kernel may launch now; it waits for this grid before reading the plan
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __shared__ int hist[COST_BUCKETS];
     __shared__ int scan[PLAN_THREADS];
     __shared__ alignas(128) CUtensorMap smap[3];
+    // batches up to PLAN_SMEM_BATCH keep indptr and the per-request item offsets in shared
+    // memory, so the binary searches below do not wait on L2
+    __shared__ int s_qi[PLAN_SMEM_BATCH + 1], s_ki[PLAN_SMEM_BATCH + 1],
+        s_off[PLAN_SMEM_BATCH + 1];
     const int tid = threadIdx.x;
     const int nthr = blockDim.x;
+    const bool small = p.batch <= PLAN_SMEM_BATCH;
+    if (small) {
+        for (int b = tid; b <= p.batch; b += nthr) {
+            s_qi[b] = p.q_indptr[b];
+            s_ki[b] = p.kv_indptr[b];
+        }
+        __syncthreads();
+    }
+    const int* qi = small ? s_qi : p.q_indptr;
+    const int* ki = small ? s_ki : p.kv_indptr;
+    int* toff = small ? s_off : p.tile_off;
 
     int bad = 0;
     for (int b = tid; b < p.batch; b += nthr) {
-        const int q0 = p.q_indptr[b], q1 = p.q_indptr[b + 1];
-        const int k0 = p.kv_indptr[b], k1 = p.kv_indptr[b + 1];
+        const int q0 = qi[b], q1 = qi[b + 1];
+        const int k0 = ki[b], k1 = ki[b + 1];
         if (q0 < 0 || k0 < 0 || q1 < q0 || k1 < k0) bad = 1;
     }
     if (__syncthreads_or(bad)) {
@@ -135,13 +153,13 @@ __global__ void __launch_bounds__(PLAN_THREADS)
         return;
     }
 
-    // exclusive scan of per-request q-tile counts -> tile_off
+    // exclusive scan of per-request item counts -> toff
     int running = 0;
     for (int base = 0; base < p.batch; base += nthr) {
         const int b = base + tid;
         int cnt = 0;
         if (b < p.batch) {
-            const long long qo = p.q_indptr[b + 1] - p.q_indptr[b];
+            const long long qo = qi[b + 1] - qi[b];
             const int tiles = (int)((qo * p.group + BM - 1) / BM);
             cnt = (tiles + p.tiles_per_item - 1) / p.tiles_per_item;
         }
@@ -153,13 +171,13 @@ __global__ void __launch_bounds__(PLAN_THREADS)
             scan[tid] += v;
             __syncthreads();
         }
-        if (b < p.batch) p.tile_off[b] = running + scan[tid] - cnt;
+        if (b < p.batch) toff[b] = running + scan[tid] - cnt;
         running += scan[nthr - 1];
         __syncthreads();
     }
     const int total_tiles = running;
     const long long n_items = (long long)total_tiles * p.num_kv_heads;
-    if (tid == 0) p.tile_off[p.batch] = total_tiles;
+    if (tid == 0) toff[p.batch] = total_tiles;
     if (n_items > p.item_capacity) {
         if (tid == 0) {
             atomicOr(&p.hdr->status, PGQA_DEV_CAPACITY);
@@ -170,15 +188,15 @@ __global__ void __launch_bounds__(PLAN_THREADS)
     for (int i = tid; i < COST_BUCKETS; i += nthr) hist[i] = 0;
     __syncthreads();
 
-    // histogram of item costs (K/V tiles per q tile)
+    // histogram of item costs (K/V tiles of the item's longest q tile)
     for (int f = tid; f < total_tiles; f += nthr) {
-        const int b = find_segment(p.tile_off, p.batch, f);
-        const int qt = (f - p.tile_off[b]) * p.tiles_per_item;
-        atomicAdd(&hist[min(item_cost(p, b, qt), COST_BUCKETS - 1)], 1);
+        const int b = find_segment(toff, p.batch, f);
+        const int qt = (f - toff[b]) * p.tiles_per_item;
+        atomicAdd(&hist[min(item_cost(p, qi, ki, b, qt), COST_BUCKETS - 1)], 1);
     }
     __syncthreads();
 
-    // descending exclusive scan: start[c] = number of q tiles with a larger cost
+    // descending exclusive scan: start[c] = number of items with a larger cost
     constexpr int PER = COST_BUCKETS / PLAN_THREADS;
     int local[PER];
     int sum = 0;
@@ -209,19 +227,19 @@ __global__ void __launch_bounds__(PLAN_THREADS)
 
     // scatter: the kv heads of one q tile take consecutive slots
     for (int f = tid; f < total_tiles; f += nthr) {
-        const int b = find_segment(p.tile_off, p.batch, f);
-        const int qt = (f - p.tile_off[b]) * p.tiles_per_item;
-        const int cost = item_cost(p, b, qt);
+        const int b = find_segment(toff, p.batch, f);
+        const int qt = (f - toff[b]) * p.tiles_per_item;
+        const int cost = item_cost(p, qi, ki, b, qt);
         const int slot = atomicAdd(&hist[min(cost, COST_BUCKETS - 1)], 1);
-        const int q0 = p.q_indptr[b], k0 = p.kv_indptr[b];
+        const int q0 = qi[b], k0 = ki[b];
         WorkItem w;
         w.b = b;
         w.qt = qt;
         w.cost = cost;
         w.q_start = q0;
-        w.qo_len = p.q_indptr[b + 1] - q0;
+        w.qo_len = qi[b + 1] - q0;
         w.kv_start = k0;
-        w.kv_len = p.kv_indptr[b + 1] - k0;
+        w.kv_len = ki[b + 1] - k0;
         for (int g = 0; g < p.num_kv_heads; ++g) {
             w.g = g;
             p.items[(long long)slot * p.num_kv_heads + g] = w;
@@ -230,8 +248,8 @@ __global__ void __launch_bounds__(PLAN_THREADS)
 
     // tensor maps with the real row extents
     if (tid < 32) {
-        const int total_q = p.q_indptr[p.batch];
-        const int total_kv = p.kv_indptr[p.batch];
+        const int total_q = qi[p.batch];
+        const int total_kv = ki[p.batch];
         if (tid == 0) {
             smap[0] = tq;
             smap[1] = tk;
@@ -323,6 +341,8 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // the prologue above overlapped the plan kernel; its outputs are read from here on
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint32_t tmem_base = *tmem_slot;
 
     const int n_items = p.hdr->n_items;
@@ -414,15 +434,14 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
                     return false;
                 tc_fence_after();
                 const uint32_t p_col = (ctr & 1) ? 128u : 0u;
-                const uint32_t v_base = sKV + st * C::TILE_BYTES;
+                // V tile, MN-major: 16 keys = two 8-row swizzle groups (2048 bytes);
+                // consecutive 64-column chunks of the head dim are CHUNK_BYTES apart.
+                // A descriptor's address field is addr / 16, so offsets add to it directly.
+                const uint64_t vdesc = sdesc_sw128(sKV + st * C::TILE_BYTES, C::CHUNK_BYTES, 1024);
 #pragma unroll
-                for (int k = 0; k < BN / 16; ++k) {
-                    // V tile, MN-major: 16 keys = two 8-row swizzle groups (2048 bytes);
-                    // consecutive 64-column chunks of the head dim are CHUNK_BYTES apart.
-                    const uint64_t bd = sdesc_sw128(v_base + k * 2048, C::CHUNK_BYTES, 1024);
-                    mma_ts(tmem_base + C::TMEM_O, tmem_base + p_col + k * 8, bd, IDESC_PV,
-                           (jj > 0 || k > 0) ? 1u : 0u);
-                }
+                for (int k = 0; k < BN / 16; ++k)
+                    mma_ts(tmem_base + C::TMEM_O, tmem_base + p_col + k * 8,
+                           vdesc + (uint64_t)(k * 2048 / 16), IDESC_PV, (jj > 0 || k > 0) ? 1u : 0u);
                 mma_commit(BAR(KV_EMPTY + st));
                 mma_commit(BAR(PV_DONE));
                 return true;
@@ -449,13 +468,12 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
                     tc_fence_after();
                     const uint32_t ctr = tile_ctr + j;
                     const uint32_t s_col = (ctr & 1) ? 128u : 0u;
-                    const uint32_t k_base = sKV + st * C::TILE_BYTES;
+                    const uint64_t kdesc = sdesc_sw128(sKV + st * C::TILE_BYTES, 16, 1024);
+                    const uint64_t qdesc = sdesc_sw128(sQ, 16, 1024);
 #pragma unroll
                     for (int k = 0; k < D / 16; ++k) {
-                        const uint32_t off = (k >> 2) * C::CHUNK_BYTES + (k & 3) * 32;
-                        const uint64_t ad = sdesc_sw128(sQ + off, 16, 1024);
-                        const uint64_t bd = sdesc_sw128(k_base + off, 16, 1024);
-                        mma_ss(tmem_base + s_col, ad, bd, IDESC_QK, k > 0 ? 1u : 0u);
+                        const uint64_t off = ((k >> 2) * C::CHUNK_BYTES + (k & 3) * 32) / 16;
+                        mma_ss(tmem_base + s_col, qdesc + off, kdesc + off, IDESC_QK, k > 0 ? 1u : 0u);
                     }
                     mma_commit(BAR(KV_EMPTY + st));
                     mma_commit(BAR(S_FULL + (ctr & 1)));
@@ -683,6 +701,8 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // the prologue above overlapped the plan kernel; its outputs are read from here on
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint32_t tmem_base = *tmem_slot;
     const int n_items = p.hdr->n_items;
     const int G = p.group;
@@ -765,6 +785,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
         if (lane == 0) {
             constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, false);
             constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, true);
+            const uint64_t qdesc0 = sdesc_sw128(sQ, 16, 1024);
             uint32_t load_idx = 0, q_count = 0, step = 0;
             uint32_t ctr[2] = {0, 0}, items_x[2] = {0, 0};
             bool ok = true;
@@ -801,22 +822,23 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
                                                        abort_flag, p.status);
                             if (!ok) break;
                             tc_fence_after();
-                            const uint32_t v_base = sKV + vst * C::TILE_BYTES;
+                            // descriptor of a 16-key slice = base + byte offset / 16
+                            const uint64_t vdesc =
+                                sdesc_sw128(sKV + vst * C::TILE_BYTES, C::CHUNK_BYTES, 1024);
 #pragma unroll
                             for (int k = 0; k < BN / 16; ++k)
                                 mma_ts(tmem_base + 256u + 128u * x, tmem_base + 128u * x + k * 8,
-                                       sdesc_sw128(v_base + k * 2048, C::CHUNK_BYTES, 1024),
-                                       IDESC_PV, (jj > 0 || k > 0) ? 1u : 0u);
+                                       vdesc + (uint64_t)(k * 2048 / 16), IDESC_PV,
+                                       (jj > 0 || k > 0) ? 1u : 0u);
                             if (jj == nx[x] - 1) mma_commit(BAR(PV_DONE + x));
                         }
                         if (t < nx[x]) {
-                            const uint32_t k_base = sKV + kst * C::TILE_BYTES;
-                            const uint32_t q_base = sQ + x * C::TILE_BYTES;
+                            const uint64_t kdesc = sdesc_sw128(sKV + kst * C::TILE_BYTES, 16, 1024);
+                            const uint64_t qdesc = qdesc0 + (uint64_t)(x * C::TILE_BYTES / 16);
 #pragma unroll
                             for (int k = 0; k < D / 16; ++k) {
-                                const uint32_t off = (k >> 2) * C::CHUNK_BYTES + (k & 3) * 32;
-                                mma_ss(tmem_base + 128u * x, sdesc_sw128(q_base + off, 16, 1024),
-                                       sdesc_sw128(k_base + off, 16, 1024), IDESC_QK,
+                                const uint64_t off = ((k >> 2) * C::CHUNK_BYTES + (k & 3) * 32) / 16;
+                                mma_ss(tmem_base + 128u * x, qdesc + off, kdesc + off, IDESC_QK,
                                        k > 0 ? 1u : 0u);
                             }
                             mma_commit(BAR(S_FULL + x));
@@ -1014,6 +1036,24 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
 }
 
 // ------------------------------------------------------------------ host launchers
+// Launch with programmatic dependent launch: the grid may start while the previous kernel
+// in the stream (the plan) still runs; it calls griddepcontrol.wait before using its output.
+template <typename Kernel>
+static cudaError_t launch_dependent(Kernel kernel, int grid, int threads, int smem,
+                                   cudaStream_t stream, const Params& p) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
 template <int D>
 int smem_bytes() {
     return Cfg<D>::SMEM_BYTES;
@@ -1031,8 +1071,7 @@ cudaError_t launch_attention(const Params& p, int grid, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    attention_kernel<D><<<grid, THREADS, Cfg<D>::SMEM_BYTES, stream>>>(p);
-    return cudaGetLastError();
+    return launch_dependent(attention_kernel<D>, grid, THREADS, Cfg<D>::SMEM_BYTES, stream, p);
 }
 
 cudaError_t launch_attention_pair(const Params& p, int grid, cudaStream_t stream) {
@@ -1046,8 +1085,8 @@ cudaError_t launch_attention_pair(const Params& p, int grid, cudaStream_t stream
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    attention_pair_kernel<<<grid, PAIR_THREADS, PairCfg::SMEM_BYTES, stream>>>(p);
-    return cudaGetLastError();
+    return launch_dependent(attention_pair_kernel, grid, PAIR_THREADS, PairCfg::SMEM_BYTES, stream,
+                            p);
 }
 
 cudaError_t launch_plan(const PlanParams& pp, const CUtensorMap& tq, const CUtensorMap& tk,
