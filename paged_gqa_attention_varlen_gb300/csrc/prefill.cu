@@ -647,7 +647,7 @@ struct PairCfg {
     static constexpr int CHUNK_BYTES = BM * 128;
     static constexpr int TILE_BYTES = BM * D * 2;
     static constexpr int STAGES = 4;
-    static constexpr int NUM_BARS = 15;
+    static constexpr int NUM_BARS = 13;
     static constexpr int SMEM_BYTES = 1024 + TILE_BYTES * (2 + STAGES) + 8 * NUM_BARS + 16;
 };
 
@@ -671,8 +671,10 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
     const uint32_t bar0 = smem_u32(bars);
     auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
     // STEP_FULL[t % 2]: the K/V tiles one MMA step consumes have landed (TMA tx count);
-    // STEP_DONE[t % 2]: every MMA of step t has completed, so its stages may be reused.
-    constexpr int Q_FULL = 0, Q_EMPTY = 1, STEP_FULL = 2, STEP_DONE = 4, S_FULL = 6,
+    // A step's stages are free again once its last MMA group has completed: that group's
+    // commit is S_FULL of tile B (tile A for items without B) or, on an item's final step,
+    // PV_DONE; the producer waits on those, so the MMA warp issues no extra commit.
+    constexpr int Q_FULL = 0, Q_EMPTY = 1, STEP_FULL = 2, S_FULL = 4,
                   P_FULL = S_FULL + 2, PV_DONE = P_FULL + 2, O_EMPTY = PV_DONE + 2,
                   MMA_DRAIN = O_EMPTY + 2;
     static_assert(MMA_DRAIN + 1 == C::NUM_BARS, "barrier count");
@@ -684,7 +686,6 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
         mbar_init(BAR(Q_EMPTY), 1);
         for (int x = 0; x < 2; ++x) {
             mbar_init(BAR(STEP_FULL + x), 1);
-            mbar_init(BAR(STEP_DONE + x), 1);
             mbar_init(BAR(S_FULL + x), 1);
             mbar_init(BAR(P_FULL + x), 128);
             mbar_init(BAR(PV_DONE + x), 1);
@@ -715,6 +716,8 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
             tensormap_acquire(p.tm_k);
             tensormap_acquire(p.tm_v);
             uint32_t load_idx = 0, q_count = 0, step = 0;
+            uint32_t ctr[2] = {0, 0}, items_x[2] = {0, 0};
+            uint32_t done_bar[2] = {0, 0}, done_par[2] = {0, 0};  // completion of steps t, t-1
             bool ok = true;
             int rr = -1;
             int it = snake_next(rr, n_items);
@@ -728,6 +731,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
                 const int nB = bq.t0 < bq.qo_len ? bq.n_tiles : 0;
                 const int nmax = max(nA, nB);
                 if (nmax == 0) continue;
+                const int lx = nB > 0 ? 1 : 0;  // tile whose MMAs close every step
                 ok = mbar_wait_bounded(BAR(Q_EMPTY), (q_count & 1) ^ 1, abort_flag, p.status);
                 if (!ok) break;
                 mbar_arrive_expect_tx(BAR(Q_FULL), C::TILE_BYTES * (nB > 0 ? 2 : 1));
@@ -745,9 +749,16 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
                 const uint32_t L0 = load_idx;
                 for (int t = 0; t <= nmax; ++t, ++step) {
                     if (step >= 2) {
-                        ok = mbar_wait_bounded(BAR(STEP_DONE + (step & 1)), ((step - 2) >> 1) & 1,
-                                               abort_flag, p.status);
+                        ok = mbar_wait_bounded(done_bar[step & 1], done_par[step & 1], abort_flag,
+                                               p.status);
                         if (!ok) break;
+                    }
+                    if (t < nmax) {
+                        done_bar[step & 1] = BAR(S_FULL + lx);
+                        done_par[step & 1] = (ctr[lx] + t) & 1;
+                    } else {
+                        done_bar[step & 1] = BAR(PV_DONE + lx);
+                        done_par[step & 1] = items_x[lx] & 1;
                     }
                     const uint32_t bar = BAR(STEP_FULL + (step & 1));
                     mbar_arrive_expect_tx(bar, C::TILE_BYTES * ((t >= 1) + (t < nmax)));
@@ -767,6 +778,10 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
                     }
                 }
                 load_idx = L0 + 2 * nmax;
+                ctr[0] += nA;
+                ctr[1] += nB;
+                if (nA > 0) ++items_x[0];
+                if (nB > 0) ++items_x[1];
             }
             if (!ok) {
                 // let every copy already issued land before the CTA exits
@@ -846,7 +861,6 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
                     }
                     if (!ok) break;
                     if (t == nmax - 1) mma_commit(BAR(Q_EMPTY));
-                    mma_commit(BAR(STEP_DONE + (step & 1)));
                 }
                 if (!ok) break;
                 load_idx = L0 + 2 * nmax;
