@@ -112,6 +112,34 @@ __device__ __forceinline__ int item_cost(const PlanParams& p, const int* qi, con
     return item_geometry(qi, ki, b, last, p.group, p.causal).n_tiles;
 }
 
+// Block-wide inclusive scan of one int per thread (blockDim.x == PLAN_THREADS): warp
+// shuffles, then a scan of the 32 warp totals.  `wsum` is 32 ints of shared memory.
+// Returns the inclusive prefix; *total receives the block total.
+__device__ __forceinline__ int block_inclusive_scan(int v, int* wsum, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += n;
+    }
+    if (lane == 31) wsum[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        int w = wsum[lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, w, off);
+            if (lane >= off) w += n;
+        }
+        wsum[lane] = w;
+    }
+    __syncthreads();
+    const int r = v + (warp > 0 ? wsum[warp - 1] : 0);
+    *total = wsum[31];
+    __syncthreads();  // wsum may be reused by the next call
+    return r;
+}
+
 // ---------------------------------------------------------------------------- plan
 __global__ void __launch_bounds__(PLAN_THREADS)
     plan_kernel(PlanParams p, const __grid_constant__ CUtensorMap tq,
@@ -163,17 +191,10 @@ __global__ void __launch_bounds__(PLAN_THREADS)
             const int tiles = (int)((qo * p.group + BM - 1) / BM);
             cnt = (tiles + p.tiles_per_item - 1) / p.tiles_per_item;
         }
-        scan[tid] = cnt;
-        __syncthreads();
-        for (int off = 1; off < nthr; off <<= 1) {
-            const int v = tid >= off ? scan[tid - off] : 0;
-            __syncthreads();
-            scan[tid] += v;
-            __syncthreads();
-        }
-        if (b < p.batch) toff[b] = running + scan[tid] - cnt;
-        running += scan[nthr - 1];
-        __syncthreads();
+        int tot;
+        const int inc = block_inclusive_scan(cnt, scan, &tot);
+        if (b < p.batch) toff[b] = running + inc - cnt;
+        running += tot;
     }
     const int total_tiles = running;
     const long long n_items = (long long)total_tiles * p.num_kv_heads;
@@ -207,16 +228,10 @@ __global__ void __launch_bounds__(PLAN_THREADS)
             sum += local[e];
         }
     }
-    scan[tid] = sum;
-    __syncthreads();
-    for (int off = 1; off < nthr; off <<= 1) {
-        const int v = tid >= off ? scan[tid - off] : 0;
-        __syncthreads();
-        scan[tid] += v;
-        __syncthreads();
-    }
+    int tot;
+    const int inc = block_inclusive_scan(sum, scan, &tot);
     if (tid < COST_BUCKETS / PER) {
-        int acc = scan[tid] - sum;
+        int acc = inc - sum;
 #pragma unroll
         for (int e = 0; e < PER; ++e) {
             hist[COST_BUCKETS - 1 - (tid * PER + e)] = acc;
