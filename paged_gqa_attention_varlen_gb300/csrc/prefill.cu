@@ -662,7 +662,7 @@ struct PairCfg {
     static constexpr int CHUNK_BYTES = BM * 128;
     static constexpr int TILE_BYTES = BM * D * 2;
     static constexpr int STAGES = 4;
-    static constexpr int NUM_BARS = 13;
+    static constexpr int NUM_BARS = 11;
     static constexpr int SMEM_BYTES = 1024 + TILE_BYTES * (2 + STAGES) + 8 * NUM_BARS + 16;
 };
 
@@ -690,8 +690,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
     // commit is S_FULL of tile B (tile A for items without B) or, on an item's final step,
     // PV_DONE; the producer waits on those, so the MMA warp issues no extra commit.
     constexpr int Q_FULL = 0, Q_EMPTY = 1, STEP_FULL = 2, S_FULL = 4,
-                  P_FULL = S_FULL + 2, PV_DONE = P_FULL + 2, O_EMPTY = PV_DONE + 2,
-                  MMA_DRAIN = O_EMPTY + 2;
+                  P_FULL = S_FULL + 2, PV_DONE = P_FULL + 2, MMA_DRAIN = PV_DONE + 2;
     static_assert(MMA_DRAIN + 1 == C::NUM_BARS, "barrier count");
 
     const int warp = threadIdx.x >> 5;
@@ -704,7 +703,6 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
             mbar_init(BAR(S_FULL + x), 1);
             mbar_init(BAR(P_FULL + x), 128);
             mbar_init(BAR(PV_DONE + x), 1);
-            mbar_init(BAR(O_EMPTY + x), 128);
         }
         mbar_init(BAR(MMA_DRAIN), 1);
         *abort_flag = 0;
@@ -845,11 +843,10 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
                     for (int x = 0; x < 2; ++x) {
                         if (t >= 1 && t - 1 < nx[x]) {
                             const int jj = t - 1;
+                            // P_FULL of an item's first tile also says that the previous
+                            // item's O has been read out, so this P.V may overwrite it
                             ok = mbar_wait_bounded(BAR(P_FULL + x), (ctr[x] + jj) & 1, abort_flag,
                                                    p.status);
-                            if (ok && jj == 0 && items_x[x] > 0)
-                                ok = mbar_wait_bounded(BAR(O_EMPTY + x), (items_x[x] - 1) & 1,
-                                                       abort_flag, p.status);
                             if (!ok) break;
                             tc_fence_after();
                             // descriptor of a 16-key slice = base + byte offset / 16
@@ -891,6 +888,10 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------------ softmax / epilogue
+        // The epilogue of an item (O / l -> bf16 rows, lse) runs inside the next item's
+        // first tile: once that tile's P is in tensor memory, the warpgroup reads the
+        // previous O, releases O and P together, and then stores, so the stores overlap the
+        // tensor core's next P.V instead of delaying it.
         const int X = warp >= 8 ? 1 : 0;
         const int r = threadIdx.x - 128 - 128 * X;
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
@@ -901,6 +902,49 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
         const bool fast_scale = p.scale_log2 > 0.f;
         const float c_eff = fast_scale ? p.scale_log2 : 1.f;
         uint32_t ctr = 0, items_done = 0;
+        // the item whose epilogue is pending
+        bool pend = false, pend_valid = false;
+        float pend_l = 0.f, pend_m = 0.f;
+        size_t pend_row = 0;
+        // Wait for the pending item's last P.V and read its O row out of tensor memory.
+        auto read_pending = [&](uint32_t (&u)[4][32]) -> bool {
+            const bool okw = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(PV_DONE + X),
+                                                                        items_done & 1,
+                                                                        abort_flag, p.status));
+            ++items_done;
+            if (!okw) return false;
+            tc_fence_after();
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) tmem_ld32(o_addr + cc * 32, u[cc]);
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) tmem_wait_ld_regs(u[cc]);
+            return true;
+        };
+        auto store_pending = [&](const uint32_t (&u)[4][32]) {
+            if (!pend_valid) return;
+            const float inv_l = pend_l > 0.f ? 1.f / pend_l : 0.f;
+            uint4* op = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + pend_row * D);
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    pk[e] = pack_bf16x2(__uint_as_float(u[cc][2 * e]) * inv_l,
+                                        __uint_as_float(u[cc][2 * e + 1]) * inv_l);
+                if (o32) {  // 32-byte stores: whole sectors, half the store instructions
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) st_global_v8(op + cc * 4 + h * 2, pk + 8 * h);
+                } else {
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4)
+                        op[cc * 4 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2],
+                                                     pk[4 * v4 + 3]);
+                }
+            }
+            if (p.lse)
+                p.lse[pend_row] =
+                    pend_l > 0.f ? (pend_m + log2f(pend_l)) * 0.69314718055994531f : -INFINITY;
+        };
         bool ok = true;
         int rr = -1;
         int it = snake_next(rr, n_items);
@@ -996,62 +1040,50 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
                     if (__any_sync(0xffffffffu, grow)) {
 #pragma unroll 1
                         for (int cc = 0; cc < D / 32; ++cc) {
-                            uint32_t u[32];
-                            tmem_ld32(o_addr + cc * 32, u);
-                            tmem_wait_ld_regs(u);
+                            uint32_t v[32];
+                            tmem_ld32(o_addr + cc * 32, v);
+                            tmem_wait_ld_regs(v);
                             const uint64_t al2 = f2_pack(alpha, alpha);
 #pragma unroll
                             for (int i = 0; i < 32; i += 2) {
                                 float o0, o1;
-                                f2_unpack(f2_mul(f2_pack(__uint_as_float(u[i]), __uint_as_float(u[i + 1])), al2), o0, o1);
-                                u[i] = __float_as_uint(o0);
-                                u[i + 1] = __float_as_uint(o1);
+                                f2_unpack(f2_mul(f2_pack(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), al2), o0, o1);
+                                v[i] = __float_as_uint(o0);
+                                v[i + 1] = __float_as_uint(o1);
                             }
-                            tmem_st32(o_addr + cc * 32, u);
+                            tmem_st32(o_addr + cc * 32, v);
                         }
                     }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(BAR(P_FULL + X));
+                } else if (pend) {
+                    // first tile of an item with an epilogue pending: read the previous O
+                    // (its last P.V is done), release O and this tile's P, then store
+                    ok = read_pending(u);
+                    if (!ok) break;
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(BAR(P_FULL + X));
+                    store_pending(u);
+                } else {
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(BAR(P_FULL + X));
                 }
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(BAR(P_FULL + X));
                 m_used = m_new;
             }
             if (!ok) break;
             ctr += x.n_tiles;
-            ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(PV_DONE + X), items_done & 1,
-                                                           abort_flag, p.status));
-            ++items_done;
-            if (!ok) break;
-            tc_fence_after();
-            const float inv_l = l > 0.f ? 1.f / l : 0.f;
-            uint4* op = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + out_row * D);
-#pragma unroll 1
-            for (int cc = 0; cc < D / 32; ++cc) {
-                uint32_t u[32];
-                tmem_ld32(o_addr + cc * 32, u);
-                tmem_wait_ld_regs(u);
-                if (valid) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        pk[e] = pack_bf16x2(__uint_as_float(u[2 * e]) * inv_l,
-                                            __uint_as_float(u[2 * e + 1]) * inv_l);
-                    if (o32) {  // 32-byte stores: whole sectors, half the store instructions
-#pragma unroll
-                        for (int h = 0; h < 2; ++h)
-                            st_global_v8(op + cc * 4 + h * 2, pk + 8 * h);
-                    } else {
-#pragma unroll
-                        for (int v4 = 0; v4 < 4; ++v4)
-                            op[cc * 4 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2],
-                                                         pk[4 * v4 + 3]);
-                    }
-                }
-            }
-            if (valid && p.lse)
-                p.lse[out_row] = l > 0.f ? (m_used + log2f(l)) * 0.69314718055994531f : -INFINITY;
-            tc_fence_before();
-            mbar_arrive(BAR(O_EMPTY + X));
+            pend = true;
+            pend_valid = valid;
+            pend_l = l;
+            pend_m = m_used;
+            pend_row = out_row;
+        }
+        if (ok && pend) {
+            uint32_t u[4][32];
+            if (read_pending(u)) store_pending(u);
         }
     }
 
