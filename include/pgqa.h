@@ -92,6 +92,48 @@ int pgqa_ragged_prefill_bf16(const void* q, const void* k, const void* v, void* 
                              float sm_scale, pgqa_stream_t stream);
 
 /*
+ * Paged prefill / append: ragged query rows over a paged NHD KV cache in one launch.  The
+ * keys of request b are its cached prefix followed by the new tokens' keys, already
+ * written into its pages by the caller, kv_lens[b] keys in all; its qo_len query rows are
+ * the last qo_len positions (bottom-right causal alignment).  Decode of several tokens per
+ * request (speculative verification) is the case of small qo_len.
+ *
+ * Defined by: FlashInfer documentation, flashinfer.prefill
+ * (BatchPrefillWithPagedKVCacheWrapper: batched prefill / append attention of ragged
+ * queries over a paged KV cache with page_size, NHD layout, causal masking aligned to the
+ * bottom right, flashinfer_benchmark.py "Attention Flags"); the page-table addressing and
+ * padding rules are those of the paged decode below (vllm-rlt pull request "feat: add
+ * FlashInfer attention backend for SM120 decode", Design notes).
+ *
+ *   q  [total_q, num_qo_heads, head_dim] bf16, device (read); rows of request b are
+ *       q_indptr[b] .. q_indptr[b+1]-1 (q_indptr [batch + 1] int32, device, as for
+ *       pgqa_ragged_prefill_bf16; total_q = q_indptr[batch] is read on the device)
+ *   k_pages, v_pages [num_pages, page_size, num_kv_heads, head_dim] bf16, device (read)
+ *   page_table [batch, page_table_stride] int32, device: key j of request b is slot
+ *       j % page_size of page page_table[b * page_table_stride + j / page_size]; entries at
+ *       index >= ceil(kv_lens[b] / page_size) are never read.
+ *   kv_lens [batch] int32, device: 0 <= kv_lens[b] <= page_table_stride * page_size.
+ *   o [total_q, num_qo_heads, head_dim] bf16, lse [total_q, num_qo_heads] fp32 or NULL:
+ *       written for every query row, as for pgqa_ragged_prefill_bf16.
+ *   causal != 0: query row i (0-based within its request) sees key j iff
+ *       j <= i + kv_len - qo_len; else every key of its request.
+ *   Key slots past kv_lens[b] in a request's last page are never used, so whatever they
+ *   hold (even NaN) cannot reach the output.
+ *
+ * Supported: head_dim 128 or 256; page_size 16, 32, 64 or 128; G = num_qo_heads /
+ * num_kv_heads dividing 128.  batch == 0 returns PGQA_OK at once.  Errors as for
+ * pgqa_ragged_prefill_bf16; a kv_len outside its range or a decreasing q_indptr is
+ * reported as PGQA_ERR_DEVICE_BOUNDS by pgqa_get_device_status() and nothing is written;
+ * a page id outside 0..num_pages-1 is reported the same way and that page is not read
+ * (the rows that need it are then undefined).
+ */
+int pgqa_paged_prefill_bf16(const void* q, const void* k_pages, const void* v_pages, void* o,
+                            float* lse, const int32_t* q_indptr, const int32_t* page_table,
+                            int page_table_stride, const int32_t* kv_lens, int page_size,
+                            int num_pages, int batch, int num_qo_heads, int num_kv_heads,
+                            int head_dim, int causal, float sm_scale, pgqa_stream_t stream);
+
+/*
  * Paged decode: one query row per request over a paged NHD KV cache, split along the
  * keys (split-KV) with the partial results merged by log-sum-exp weights.
  *
@@ -129,6 +171,11 @@ int ragged_prefill_bf16(const void* q, const void* k, const void* v, void* o, fl
                         const int32_t* q_indptr, const int32_t* kv_indptr, int batch,
                         int num_qo_heads, int num_kv_heads, int head_dim, int causal,
                         float sm_scale, pgqa_stream_t stream);
+int paged_prefill_bf16(const void* q, const void* k_pages, const void* v_pages, void* o,
+                       float* lse, const int32_t* q_indptr, const int32_t* page_table,
+                       int page_table_stride, const int32_t* kv_lens, int page_size,
+                       int num_pages, int batch, int num_qo_heads, int num_kv_heads,
+                       int head_dim, int causal, float sm_scale, pgqa_stream_t stream);
 int paged_decode_bf16(const void* q, const void* k_pages, const void* v_pages,
                       const int32_t* page_table, const int32_t* kv_lens, int page_size,
                       int page_table_stride, int num_pages, void* o, float* lse, int batch,
@@ -171,8 +218,8 @@ int pgqa_paged_decode_bf16_noalloc(const void* q, const void* k_pages, const voi
                                    pgqa_stream_t stream);
 
 /*
- * Workspace.  Both calls need device scratch: the prefill for its work list and tensor
- * maps, the decode for its split-KV partial results.  Unless the caller supplies one,
+ * Workspace.  Every call needs device scratch: the prefills for their work list and
+ * tensor maps, the decode for its split-KV partial results.  Unless the caller supplies one,
  * the library allocates it lazily on the first call that needs it (per device; 128 MiB
  * or more if the call needs more) and grows it when a call needs more -- except while
  * `stream` is being captured into a CUDA graph, where it returns PGQA_ERR_WORKSPACE
@@ -184,7 +231,7 @@ int pgqa_paged_decode_bf16_noalloc(const void* q, const void* k_pages, const voi
  *   ptr == NULL drops a caller buffer and returns to lazy allocation.  The buffer must
  *   stay valid until replaced and must not be used by anything else meanwhile.
  * pgqa_workspace_bytes_*: upper bound of the bytes a call with these sizes needs.
- *   For the prefill, max_total_q bounds q_indptr[batch].
+ *   For the prefills (ragged and paged), max_total_q bounds q_indptr[batch].
  */
 int pgqa_set_workspace(void* ptr, size_t bytes);
 size_t pgqa_workspace_bytes_prefill(int batch, int64_t max_total_q, int num_qo_heads,

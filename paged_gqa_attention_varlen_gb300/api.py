@@ -24,8 +24,8 @@ STATUS_NAMES = {
 }
 
 ABI_FUNCTIONS = (
-    "pgqa_ragged_prefill_bf16", "pgqa_paged_decode_bf16", "ragged_prefill_bf16",
-    "paged_decode_bf16", "pgqa_set_workspace", "pgqa_workspace_bytes_prefill",
+    "pgqa_ragged_prefill_bf16", "pgqa_paged_prefill_bf16", "pgqa_paged_decode_bf16",
+    "ragged_prefill_bf16", "paged_prefill_bf16", "paged_decode_bf16", "pgqa_set_workspace", "pgqa_workspace_bytes_prefill",
     "pgqa_workspace_bytes_decode", "pgqa_get_device_status", "pgqa_status_string",
     "pgqa_version", "pgqa_paged_decode_bf16_noalloc",
 )
@@ -53,6 +53,10 @@ def _load(path: Path):
     for name in ("pgqa_paged_decode_bf16", "paged_decode_bf16"):
         fn = getattr(lib, name)
         fn.argtypes, fn.restype = decode_args, i
+    paged_prefill_args = [p, p, p, p, p, p, p, i, p, i, i, i, i, i, i, i, f, p]
+    for name in ("pgqa_paged_prefill_bf16", "paged_prefill_bf16"):
+        fn = getattr(lib, name)
+        fn.argtypes, fn.restype = paged_prefill_args, i
     lib.pgqa_set_workspace.argtypes, lib.pgqa_set_workspace.restype = [p, sz], i
     lib.pgqa_workspace_bytes_prefill.argtypes = [i, i64, i, i]
     lib.pgqa_workspace_bytes_prefill.restype = sz
@@ -129,6 +133,47 @@ def ragged_prefill(q, k, v, q_indptr, kv_indptr, causal=True, sm_scale=None, out
                                       int(bool(causal)), float(sm_scale), _stream(stream))
     if rc != PGQA_OK:
         raise PgqaError(rc, "pgqa_ragged_prefill_bf16")
+    return out, lse
+
+
+def paged_prefill(q, k_pages, v_pages, q_indptr, page_table, kv_lens, causal=True, sm_scale=None,
+                  out=None, lse=None, return_lse=True, stream=None):
+    """Paged prefill / append (pgqa_paged_prefill_bf16).
+
+    q [total_q, Hq, d] bf16 with q_indptr [batch + 1] int32; k_pages / v_pages
+    [num_pages, page_size, Hk, d] bf16; page_table [batch, stride] int32; kv_lens [batch]
+    int32 (keys per request, the cached prefix plus the new tokens); all on one CUDA device.
+    Returns (o [total_q, Hq, d] bf16, lse [total_q, Hq] fp32 or None).
+    """
+    dev = q.device
+    _check(q, "q", torch.bfloat16, 3, dev)
+    _check(k_pages, "k_pages", torch.bfloat16, 4, dev)
+    _check(v_pages, "v_pages", torch.bfloat16, 4, dev)
+    _check(q_indptr, "q_indptr", torch.int32, 1, dev)
+    _check(page_table, "page_table", torch.int32, 2, dev)
+    _check(kv_lens, "kv_lens", torch.int32, 1, dev)
+    total_q, hq, d = q.shape
+    num_pages, page_size, hk, dk = k_pages.shape
+    batch = q_indptr.numel() - 1
+    if v_pages.shape != k_pages.shape or dk != d:
+        raise ValueError("k_pages / v_pages must be [num_pages, page_size, Hk, d]")
+    if page_table.shape[0] != batch or kv_lens.numel() != batch:
+        raise ValueError("page_table / kv_lens must have one row per request")
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    _check(out, "out", torch.bfloat16, 3, dev)
+    if lse is None and return_lse:
+        lse = torch.empty((total_q, hq), dtype=torch.float32, device=dev)
+    if lse is not None:
+        _check(lse, "lse", torch.float32, 2, dev)
+    rc = lib.pgqa_paged_prefill_bf16(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(out), _ptr(lse),
+                                     _ptr(q_indptr), _ptr(page_table), page_table.shape[1],
+                                     _ptr(kv_lens), page_size, num_pages, batch, hq, hk, d,
+                                     int(bool(causal)), float(sm_scale), _stream(stream))
+    if rc != PGQA_OK:
+        raise PgqaError(rc, "pgqa_paged_prefill_bf16")
     return out, lse
 
 

@@ -12,8 +12,9 @@ namespace pgqa {
 namespace prefill {
 cudaError_t launch_plan(const PlanParams&, const CUtensorMap&, const CUtensorMap&,
                         const CUtensorMap&, cudaStream_t);
-template <int D>
+template <int D, bool PAGED>
 cudaError_t launch_attention(const Params&, int, cudaStream_t);
+template <bool PAGED>
 cudaError_t launch_attention_pair(const Params&, int, cudaStream_t);
 }  // namespace prefill
 namespace decode {
@@ -188,7 +189,9 @@ size_t pgqa_workspace_bytes_prefill(int batch, int64_t max_total_q, int num_qo_h
     if (batch < 0 || max_total_q < 0 || num_kv_heads <= 0 || num_qo_heads <= 0) return 0;
     const long long g = num_qo_heads / num_kv_heads;
     const long long tiles = (max_total_q * g + prefill::BM - 1) / prefill::BM + batch;
-    return prefill_ws_bytes(batch, tiles * num_kv_heads);
+    // + the per-request key offsets the paged prefill keeps
+    return prefill_ws_bytes(batch, tiles * num_kv_heads) +
+           align_up((size_t)(batch + 1) * sizeof(int), 256);
 }
 
 size_t pgqa_workspace_bytes_decode(int batch, int page_table_stride, int page_size,
@@ -305,6 +308,9 @@ int pgqa_ragged_prefill_bf16(const void* q, const void* k, const void* v, void* 
     prefill::PlanParams pp;
     pp.q_indptr = q_indptr;
     pp.kv_indptr = kv_indptr;
+    pp.kv_lens = nullptr;
+    pp.max_kv = 0;
+    pp.kv_off = nullptr;
     pp.batch = batch;
     pp.num_kv_heads = num_kv_heads;
     pp.group = group;
@@ -336,8 +342,123 @@ int pgqa_ragged_prefill_bf16(const void* q, const void* k, const void* v, void* 
     p.group = group;
     p.causal = causal ? 1 : 0;
     p.scale_log2 = sm_scale * 1.4426950408889634f;
-    e = head_dim == 128 ? prefill::launch_attention_pair(p, st->num_sms, s)
-                        : prefill::launch_attention<256>(p, st->num_sms, s);
+    p.page_table = nullptr;
+    p.page_table_stride = 0;
+    p.page_size = 0;
+    p.num_pages = 0;
+    e = head_dim == 128 ? prefill::launch_attention_pair<false>(p, st->num_sms, s)
+                        : prefill::launch_attention<256, false>(p, st->num_sms, s);
+    return map_cuda(e);
+}
+
+int pgqa_paged_prefill_bf16(const void* q, const void* k_pages, const void* v_pages, void* o,
+                            float* lse, const int32_t* q_indptr, const int32_t* page_table,
+                            int page_table_stride, const int32_t* kv_lens, int page_size,
+                            int num_pages, int batch, int num_qo_heads, int num_kv_heads,
+                            int head_dim, int causal, float sm_scale, pgqa_stream_t stream) {
+    if (batch < 0 || num_qo_heads <= 0 || num_kv_heads <= 0 || page_table_stride < 0 ||
+        num_pages < 0)
+        return PGQA_ERR_INVALID_ARG;
+    if (batch == 0) return PGQA_OK;
+    if (!q || !k_pages || !v_pages || !o || !q_indptr || !kv_lens ||
+        (!page_table && page_table_stride > 0))
+        return PGQA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(q_indptr) & 3u) ||
+        (reinterpret_cast<uintptr_t>(page_table) & 3u) ||
+        (reinterpret_cast<uintptr_t>(kv_lens) & 3u))
+        return PGQA_ERR_INVALID_ARG;
+    if (head_dim != 128 && head_dim != 256) return PGQA_ERR_UNSUPPORTED;
+    if (page_size != 16 && page_size != 32 && page_size != 64 && page_size != 128)
+        return PGQA_ERR_UNSUPPORTED;
+    if (num_qo_heads % num_kv_heads != 0) return PGQA_ERR_UNSUPPORTED;
+    const int group = num_qo_heads / num_kv_heads;
+    if (group > prefill::BM || prefill::BM % group != 0) return PGQA_ERR_UNSUPPORTED;
+    if (!(sm_scale == sm_scale) || sm_scale > 3.0e38f || sm_scale < -3.0e38f)
+        return PGQA_ERR_INVALID_ARG;
+    if ((long long)page_table_stride * page_size > 0x7fffffffLL ||
+        (long long)num_pages * page_size > 0x7fffffffLL)
+        return PGQA_ERR_UNSUPPORTED;
+
+    std::lock_guard<std::mutex> lock(g_mutex);
+    int dev;
+    DeviceState* st;
+    int rc = current_device(&dev, &st);
+    if (rc != PGQA_OK) return rc;
+    if ((rc = get_encoder()) != PGQA_OK) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const size_t kvoff_bytes = align_up((size_t)(batch + 1) * sizeof(int), 256);
+    rc = ensure_workspace(*st, prefill_ws_bytes(batch, 4096) + kvoff_bytes, s);
+    if (rc != PGQA_OK) return rc;
+
+    uint8_t* ws = static_cast<uint8_t*>(st->ws);
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(ws + kWsHeader);
+    CUtensorMap* tmaps = reinterpret_cast<CUtensorMap*>(ws + kWsTmapOffset);
+    int* tile_off = reinterpret_cast<int*>(ws + kWsArrays);
+    int* kv_off = reinterpret_cast<int*>(ws + kWsArrays +
+                                         align_up((size_t)(batch + 1) * sizeof(int), 256));
+    const size_t items_off = kWsArrays + align_up((size_t)(batch + 1) * sizeof(int), 256) +
+                             kvoff_bytes;
+    prefill::WorkItem* items = reinterpret_cast<prefill::WorkItem*>(ws + items_off);
+    const long long capacity =
+        (long long)((st->ws_bytes - items_off) / sizeof(prefill::WorkItem));
+
+    // Q as for the ragged call (row extent patched on the device); K/V over the page pool
+    // [num_pages * page_size rows, Hk * d], one box = one page of one 64-column chunk.
+    CUtensorMap tq, tk, tv;
+    const uint32_t tpt = prefill::BM / group;
+    const uint64_t pool_rows = (uint64_t)(num_pages > 0 ? num_pages : 1) * page_size;
+    if ((rc = encode_3d(&tq, q, head_dim, num_qo_heads, tpt, (uint64_t)head_dim * 2,
+                        (uint64_t)num_qo_heads * head_dim * 2, 64, group, tpt)) != PGQA_OK)
+        return rc;
+    if ((rc = encode_2d(&tk, k_pages, (uint64_t)num_kv_heads * head_dim, pool_rows,
+                        (uint64_t)num_kv_heads * head_dim * 2, 64, page_size)) != PGQA_OK)
+        return rc;
+    if ((rc = encode_2d(&tv, v_pages, (uint64_t)num_kv_heads * head_dim, pool_rows,
+                        (uint64_t)num_kv_heads * head_dim * 2, 64, page_size)) != PGQA_OK)
+        return rc;
+
+    prefill::PlanParams pp;
+    pp.q_indptr = q_indptr;
+    pp.kv_indptr = nullptr;
+    pp.kv_lens = kv_lens;
+    pp.max_kv = page_table_stride * page_size;
+    pp.kv_off = kv_off;
+    pp.batch = batch;
+    pp.num_kv_heads = num_kv_heads;
+    pp.group = group;
+    pp.causal = causal ? 1 : 0;
+    pp.tiles_per_item = head_dim == 128 ? 2 : 1;
+    pp.hdr = hdr;
+    pp.tile_off = tile_off;
+    pp.items = items;
+    pp.item_capacity = capacity;
+    pp.tm_out = tmaps;
+    cudaError_t e = prefill::launch_plan(pp, tq, tk, tv, s);
+    if (e != cudaSuccess) return PGQA_ERR_CUDA;
+
+    prefill::Params p;
+    p.tm_q = tmaps + 0;
+    p.tm_k = tmaps + 1;
+    p.tm_v = tmaps + 2;
+    p.o = o;
+    p.lse = lse;
+    p.q_indptr = q_indptr;
+    p.kv_indptr = nullptr;
+    p.items = items;
+    p.hdr = hdr;
+    p.status = &hdr->status;
+    p.num_qo_heads = num_qo_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.group = group;
+    p.causal = causal ? 1 : 0;
+    p.scale_log2 = sm_scale * 1.4426950408889634f;
+    p.page_table = page_table;
+    p.page_table_stride = page_table_stride;
+    p.page_size = page_size;
+    p.num_pages = num_pages;
+    e = head_dim == 128 ? prefill::launch_attention_pair<true>(p, st->num_sms, s)
+                        : prefill::launch_attention<256, true>(p, st->num_sms, s);
     return map_cuda(e);
 }
 
@@ -428,6 +549,16 @@ int ragged_prefill_bf16(const void* q, const void* k, const void* v, void* o, fl
                         float sm_scale, pgqa_stream_t stream) {
     return pgqa_ragged_prefill_bf16(q, k, v, o, lse, q_indptr, kv_indptr, batch, num_qo_heads,
                                     num_kv_heads, head_dim, causal, sm_scale, stream);
+}
+
+int paged_prefill_bf16(const void* q, const void* k_pages, const void* v_pages, void* o,
+                       float* lse, const int32_t* q_indptr, const int32_t* page_table,
+                       int page_table_stride, const int32_t* kv_lens, int page_size,
+                       int num_pages, int batch, int num_qo_heads, int num_kv_heads,
+                       int head_dim, int causal, float sm_scale, pgqa_stream_t stream) {
+    return pgqa_paged_prefill_bf16(q, k_pages, v_pages, o, lse, q_indptr, page_table,
+                                   page_table_stride, kv_lens, page_size, num_pages, batch,
+                                   num_qo_heads, num_kv_heads, head_dim, causal, sm_scale, stream);
 }
 
 int paged_decode_bf16(const void* q, const void* k_pages, const void* v_pages,

@@ -68,11 +68,20 @@ struct Params {
     int group;
     int causal;
     float scale_log2;          // sm_scale * log2(e)
+    // paged K/V (paged kernels only): key j of request b is slot j % page_size of page
+    // page_table[b * page_table_stride + j / page_size]; the K/V maps view the page pool
+    // as [num_pages * page_size rows, Hk * D] with a box of one page (page_size rows)
+    const int* page_table;
+    int page_table_stride;
+    int page_size;             // 16, 32, 64 or 128
+    int num_pages;
 };
 
 struct PlanParams {
     const int* q_indptr;
-    const int* kv_indptr;
+    const int* kv_indptr;      // ragged K/V; nullptr when kv_lens is given
+    const int* kv_lens;        // paged K/V: keys per request [batch]
+    int max_kv;                // paged: page_table_stride * page_size
     int batch;
     int num_kv_heads;
     int group;
@@ -80,6 +89,7 @@ struct PlanParams {
     int tiles_per_item;        // consecutive q tiles one work item covers (1 or 2)
     WsHeader* hdr;
     int* tile_off;             // [batch + 1]
+    int* kv_off;               // paged: [batch + 1] prefix sums of kv_lens (workspace)
     WorkItem* items;
     long long item_capacity;
     CUtensorMap* tm_out;       // 3 maps: Q, K, V

@@ -156,10 +156,11 @@ __global__ void __launch_bounds__(PLAN_THREADS)
     const int tid = threadIdx.x;
     const int nthr = blockDim.x;
     const bool small = p.batch <= PLAN_SMEM_BATCH;
+    const bool paged = p.kv_lens != nullptr;
     if (small) {
         for (int b = tid; b <= p.batch; b += nthr) {
             s_qi[b] = p.q_indptr[b];
-            s_ki[b] = p.kv_indptr[b];
+            if (!paged) s_ki[b] = p.kv_indptr[b];
         }
         __syncthreads();
     }
@@ -168,10 +169,38 @@ __global__ void __launch_bounds__(PLAN_THREADS)
     int* toff = small ? s_off : p.tile_off;
 
     int bad = 0;
+    if (paged) {
+        // keys per request from kv_lens (0 <= kv_len <= page_table_stride * page_size),
+        // turned into offsets so the rest of the plan reads them like kv_indptr; only
+        // differences of these offsets are used, so unsigned wrap-around is harmless
+        int* kvp = small ? s_ki : p.kv_off;
+        unsigned running = 0;
+        for (int base = 0; base < p.batch; base += nthr) {
+            const int b = base + tid;
+            int n = 0;
+            if (b < p.batch) {
+                n = p.kv_lens[b];
+                if (n < 0 || n > p.max_kv) {
+                    bad = 1;
+                    n = 0;
+                }
+            }
+            int tot;
+            const int inc = block_inclusive_scan(n, scan, &tot);
+            if (b < p.batch) kvp[b + 1] = (int)(running + (unsigned)inc);
+            running += (unsigned)tot;
+        }
+        if (tid == 0) kvp[0] = 0;
+        __syncthreads();
+        ki = kvp;
+    }
     for (int b = tid; b < p.batch; b += nthr) {
         const int q0 = qi[b], q1 = qi[b + 1];
-        const int k0 = ki[b], k1 = ki[b + 1];
-        if (q0 < 0 || k0 < 0 || q1 < q0 || k1 < k0) bad = 1;
+        if (q0 < 0 || q1 < q0) bad = 1;
+        if (!paged) {
+            const int k0 = ki[b], k1 = ki[b + 1];
+            if (k0 < 0 || k1 < k0) bad = 1;
+        }
     }
     if (__syncthreads_or(bad)) {
         if (tid == 0) {
@@ -270,8 +299,10 @@ __global__ void __launch_bounds__(PLAN_THREADS)
             smap[1] = tk;
             smap[2] = tv;
             tensormap_set_dim_smem<2>(smem_u32(&smap[0]), (uint32_t)max(total_q, 1));
-            tensormap_set_dim_smem<1>(smem_u32(&smap[1]), (uint32_t)max(total_kv, 1));
-            tensormap_set_dim_smem<1>(smem_u32(&smap[2]), (uint32_t)max(total_kv, 1));
+            if (!paged) {  // paged maps span the page pool, whose size the host knows
+                tensormap_set_dim_smem<1>(smem_u32(&smap[1]), (uint32_t)max(total_kv, 1));
+                tensormap_set_dim_smem<1>(smem_u32(&smap[2]), (uint32_t)max(total_kv, 1));
+            }
             p.hdr->n_items = (int)n_items;
             p.hdr->total_q = total_q;
             p.hdr->total_kv = total_kv;
@@ -283,6 +314,69 @@ __global__ void __launch_bounds__(PLAN_THREADS)
     }
 }
 
+// ------------------------------------------------------------------ paged K/V
+// Page ids of the pages of K/V tile j (keys j*BN .. j*BN+BN-1) that hold keys below
+// kv_len; pages past a request's last key are never read.  An id outside the page pool
+// is reported (PGQA_DEV_BOUNDS) and recorded as -1: that page is not loaded.  Returns the
+// number of pages in use (the tile's first n pages).
+__device__ __forceinline__ int tile_pages(int (&pid)[BN / 16], const Params& p, const int* pt_row,
+                                          int j, int kv_len) {
+    const int ps = p.page_size;
+    const int ppt = BN / ps;
+    const int first = j * ppt;
+    const int n = min(ppt, (kv_len + ps - 1) / ps - first);
+#pragma unroll
+    for (int i = 0; i < BN / 16; ++i) {
+        pid[i] = -1;
+        if (i < n) {
+            const int id = __ldg(pt_row + first + i);
+            if (id >= 0 && id < p.num_pages) pid[i] = id;
+            else atomicOr(p.status, PGQA_DEV_BOUNDS);
+        }
+    }
+    return n;
+}
+
+// Bytes the TMA copies of tile_pages() will deliver.
+template <int CHUNKS>
+__device__ __forceinline__ uint32_t tile_page_bytes(const int (&pid)[BN / 16], int n, int ps) {
+    uint32_t b = 0;
+#pragma unroll
+    for (int i = 0; i < BN / 16; ++i)
+        if (i < n && pid[i] >= 0) b += (uint32_t)(CHUNKS * ps * 128);
+    return b;
+}
+
+// One box per page and 64-column chunk: page i of the tile lands at rows i*ps.. of every
+// chunk of the stage, the layout a single 128-row box would have written.
+template <int CHUNKS, int CHUNK_BYTES>
+__device__ __forceinline__ void load_tile_pages(uint32_t dst, const CUtensorMap* tm, uint32_t bar,
+                                                const int (&pid)[BN / 16], int n, int ps, int col0) {
+#pragma unroll
+    for (int i = 0; i < BN / 16; ++i) {
+        if (i < n && pid[i] >= 0) {
+#pragma unroll
+            for (int c = 0; c < CHUNKS; ++c)
+                tma_load_2d(dst + c * CHUNK_BYTES + i * ps * 128, tm, bar, col0 + c * 64, pid[i] * ps);
+        }
+    }
+}
+
+// Zero rows r0..BM-1 of every chunk of a K/V stage (warp-collective).  With the 128-byte
+// swizzle each row's 128 bytes stay within its own 128-byte line, so whole lines are
+// cleared.  The writes are then fenced for the tensor core's async-proxy reads.
+template <int CHUNKS, int CHUNK_BYTES>
+__device__ __forceinline__ void zero_stage_rows(uint32_t stage, int r0, int lane) {
+    const int n16 = (BM - r0) * 8;  // 16-byte units per chunk
+    for (int c = 0; c < CHUNKS; ++c) {
+        const uint32_t base = stage + c * CHUNK_BYTES + r0 * 128;
+        for (int u = lane; u < n16; u += 32)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(base + u * 16), "r"(0)
+                         : "memory");
+    }
+    fence_async_smem();
+}
+
 // ---------------------------------------------------------------------- attention
 template <int D>
 struct Cfg {
@@ -292,7 +386,7 @@ struct Cfg {
     static constexpr int STAGES = D == 128 ? 4 : 2;
     static constexpr int TMEM_O = 256;                 // S buffers at columns 0 and 128
     static constexpr int TMEM_COLS = 512;
-    static constexpr int NUM_BARS = 2 + 2 * STAGES + 7;
+    static constexpr int NUM_BARS = 2 + 2 * STAGES + 9;
     static constexpr int SMEM_BYTES = 1024 + TILE_BYTES * (1 + STAGES) + 8 * NUM_BARS + 16;
 };
 
@@ -311,7 +405,7 @@ __device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&r)[32]) {
         : "memory");
 }
 
-template <int D>
+template <int D, bool PAGED>
 __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -326,8 +420,11 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
     const uint32_t bar0 = smem_u32(bars);
     auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
     const int Q_FULL = 0, Q_EMPTY = 1, KV_FULL = 2, KV_EMPTY = 2 + C::STAGES;
+    // FIX_READY / V_FIXED: paged K/V only, as in the two-tile kernel (warp 2 zeroes the
+    // rows past kv_len of an item's last V tile before its P.V)
     const int S_FULL = 2 + 2 * C::STAGES, P_FULL = S_FULL + 2, PV_DONE = P_FULL + 2,
-              O_EMPTY = PV_DONE + 1, MMA_DRAIN = O_EMPTY + 1;
+              O_EMPTY = PV_DONE + 1, MMA_DRAIN = O_EMPTY + 1, FIX_READY = MMA_DRAIN + 1,
+              V_FIXED = FIX_READY + 1;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -346,6 +443,8 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
         mbar_init(BAR(PV_DONE), 1);
         mbar_init(BAR(O_EMPTY), 128);
         mbar_init(BAR(MMA_DRAIN), 1);
+        mbar_init(BAR(FIX_READY), 1);
+        mbar_init(BAR(V_FIXED), 32);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -387,6 +486,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
                     tma_load_3d(sQ + c * C::CHUNK_BYTES, p.tm_q, BAR(Q_FULL), c * 64, w.g * G,
                                 x.q_start + x.t0);
                 ++q_count;
+                const int* pt_row = PAGED ? p.page_table + (size_t)w.b * p.page_table_stride : nullptr;
                 // consumption order of the MMA warp: K0, (K1, V0), (K2, V1), ..., V_{n-1}
                 const int nl = 2 * x.n_tiles;
                 for (int s = 0; s < nl; ++s) {
@@ -407,12 +507,23 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
                     ok = mbar_wait_bounded(BAR(KV_EMPTY + st), ((load_idx / C::STAGES) & 1) ^ 1,
                                            abort_flag, p.status);
                     if (!ok) break;
-                    mbar_arrive_expect_tx(BAR(KV_FULL + st), C::TILE_BYTES);
                     const CUtensorMap* tm = is_k ? p.tm_k : p.tm_v;
+                    if constexpr (PAGED) {
+                        int pid[BN / 16];
+                        const int np = tile_pages(pid, p, pt_row, j, x.kv_len);
+                        mbar_arrive_expect_tx(BAR(KV_FULL + st),
+                                              tile_page_bytes<C::CHUNKS>(pid, np, p.page_size));
+                        load_tile_pages<C::CHUNKS, C::CHUNK_BYTES>(sKV + st * C::TILE_BYTES, tm,
+                                                                   BAR(KV_FULL + st), pid, np,
+                                                                   p.page_size, w.g * D);
+                        if (s == nl - 1 && x.n_tiles * BN > x.kv_len) mbar_arrive(BAR(FIX_READY));
+                    } else {
+                        mbar_arrive_expect_tx(BAR(KV_FULL + st), C::TILE_BYTES);
 #pragma unroll
-                    for (int c = 0; c < C::CHUNKS; ++c)
-                        tma_load_2d(sKV + st * C::TILE_BYTES + c * C::CHUNK_BYTES, tm,
-                                    BAR(KV_FULL + st), w.g * D + c * 64, x.kv_start + j * BN);
+                        for (int c = 0; c < C::CHUNKS; ++c)
+                            tma_load_2d(sKV + st * C::TILE_BYTES + c * C::CHUNK_BYTES, tm,
+                                        BAR(KV_FULL + st), w.g * D + c * 64, x.kv_start + j * BN);
+                    }
                     ++load_idx;
                 }
             }
@@ -431,18 +542,22 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
         if (lane == 0) {
             constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, false);
             constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, true);
-            uint32_t load_idx = 0, q_count = 0, tile_ctr = 0, item_cnt = 0;
+            uint32_t load_idx = 0, q_count = 0, tile_ctr = 0, item_cnt = 0, fixes = 0;
             bool ok = true;
-            auto issue_pv = [&](int jj, int n) -> bool {
-                (void)n;
+            auto issue_pv = [&](int jj, int n, bool fix) -> bool {
                 const uint32_t ctr = tile_ctr + jj;
                 if (!mbar_wait_bounded(BAR(P_FULL + (ctr & 1)), (ctr >> 1) & 1, abort_flag,
                                        p.status))
                     return false;
                 const uint32_t st = load_idx % C::STAGES;
-                if (!mbar_wait_bounded(BAR(KV_FULL + st), (load_idx / C::STAGES) & 1, abort_flag,
-                                       p.status))
+                if (fix && jj == n - 1) {  // the last V tile, its tail rows zeroed
+                    if (!mbar_wait_bounded(BAR(V_FIXED), fixes & 1, abort_flag, p.status))
+                        return false;
+                    ++fixes;
+                } else if (!mbar_wait_bounded(BAR(KV_FULL + st), (load_idx / C::STAGES) & 1,
+                                              abort_flag, p.status)) {
                     return false;
+                }
                 ++load_idx;
                 if (jj == 0 && item_cnt > 0 &&
                     !mbar_wait_bounded(BAR(O_EMPTY), (item_cnt - 1) & 1, abort_flag, p.status))
@@ -470,6 +585,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
                 const Geo x = geo_of(w, 0, G, p.causal);
                 const int n = x.n_tiles;
                 if (n == 0) continue;
+                const bool fix = PAGED && n * BN > x.kv_len;
                 ok = mbar_wait_bounded(BAR(Q_FULL), q_count & 1, abort_flag, p.status);
                 ++q_count;
                 if (!ok) break;
@@ -494,17 +610,43 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
                     mma_commit(BAR(S_FULL + (ctr & 1)));
                     if (j == n - 1) mma_commit(BAR(Q_EMPTY));
                     if (j >= 1) {
-                        ok = issue_pv(j - 1, n);
+                        ok = issue_pv(j - 1, n, fix);
                         if (!ok) break;
                     }
                 }
-                if (ok) ok = issue_pv(n - 1, n);
+                if (ok) ok = issue_pv(n - 1, n, fix);
                 tile_ctr += n;
                 ++item_cnt;
             }
             // every MMA issued has completed before tensor memory is released
             mma_commit(BAR(MMA_DRAIN));
             mbar_wait_bounded(BAR(MMA_DRAIN), 0, nullptr, p.status);
+        }
+    } else if (PAGED && warp == 2) {
+        // ------------------------------------------------------------ V tail fixer
+        uint32_t load_idx = 0, fixes = 0;
+        bool ok = true;
+        int rr = -1;
+        int it = snake_next(rr, n_items);
+        while (ok && it >= 0) {
+            const WorkItem w = load_item(p.items, it);
+            it = snake_next(rr, n_items);
+            const Geo x = geo_of(w, 0, G, p.causal);
+            if (x.n_tiles == 0) continue;
+            const uint32_t last = load_idx + 2 * (uint32_t)x.n_tiles - 1;  // V_{n-1}
+            load_idx += 2 * (uint32_t)x.n_tiles;
+            if (x.n_tiles * BN <= x.kv_len) continue;
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(FIX_READY), fixes & 1, abort_flag,
+                                                           p.status));
+            if (ok)
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait_bounded(BAR(KV_FULL + last % C::STAGES),
+                                                  (last / C::STAGES) & 1, abort_flag, p.status));
+            if (!ok) break;
+            ++fixes;
+            zero_stage_rows<C::CHUNKS, C::CHUNK_BYTES>(sKV + (last % C::STAGES) * C::TILE_BYTES,
+                                                       x.kv_len - (x.n_tiles - 1) * BN, lane);
+            mbar_arrive(BAR(V_FIXED));
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------------ softmax / epilogue
@@ -662,7 +804,7 @@ struct PairCfg {
     static constexpr int CHUNK_BYTES = BM * 128;
     static constexpr int TILE_BYTES = BM * D * 2;
     static constexpr int STAGES = 4;
-    static constexpr int NUM_BARS = 11;
+    static constexpr int NUM_BARS = 13;
     static constexpr int SMEM_BYTES = 1024 + TILE_BYTES * (2 + STAGES) + 8 * NUM_BARS + 16;
 };
 
@@ -672,6 +814,7 @@ struct PairCfg {
 constexpr float kRescaleThreshold = 8.0f;
 
 
+template <bool PAGED>
 __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const Params p) {
     using C = PairCfg;
     constexpr int D = C::D;
@@ -689,9 +832,15 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
     // A step's stages are free again once its last MMA group has completed: that group's
     // commit is S_FULL of tile B (tile A for items without B) or, on an item's final step,
     // PV_DONE; the producer waits on those, so the MMA warp issues no extra commit.
+    // Paged K/V only: slots past kv_len in an item's last V tile hold whatever the cache
+    // holds there (or stale data of an earlier tile), and P.V would turn a NaN there into
+    // a NaN result even with P = 0.  The producer arrives on FIX_READY once it has issued
+    // the loads of such a last step; warp 2 then waits for them, zeroes those V rows and
+    // arrives on V_FIXED, which the MMA warp waits for instead of the step's STEP_FULL.
     constexpr int Q_FULL = 0, Q_EMPTY = 1, STEP_FULL = 2, S_FULL = 4,
-                  P_FULL = S_FULL + 2, PV_DONE = P_FULL + 2, MMA_DRAIN = PV_DONE + 2;
-    static_assert(MMA_DRAIN + 1 == C::NUM_BARS, "barrier count");
+                  P_FULL = S_FULL + 2, PV_DONE = P_FULL + 2, MMA_DRAIN = PV_DONE + 2,
+                  FIX_READY = MMA_DRAIN + 1, V_FIXED = FIX_READY + 1;
+    static_assert(V_FIXED + 1 == C::NUM_BARS, "barrier count");
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -705,6 +854,8 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
             mbar_init(BAR(PV_DONE + x), 1);
         }
         mbar_init(BAR(MMA_DRAIN), 1);
+        mbar_init(BAR(FIX_READY), 1);
+        mbar_init(BAR(V_FIXED), 32);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -760,6 +911,8 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
                 }
                 ++q_count;
                 const uint32_t L0 = load_idx;
+                const int* pt_row = PAGED ? p.page_table + (size_t)w.b * p.page_table_stride : nullptr;
+                int kp[BN / 16], nkp = 0;  // page ids of the K tile of the previous step
                 for (int t = 0; t <= nmax; ++t, ++step) {
                     if (step >= 2) {
                         ok = mbar_wait_bounded(done_bar[step & 1], done_par[step & 1], abort_flag,
@@ -774,20 +927,36 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
                         done_par[step & 1] = items_x[lx] & 1;
                     }
                     const uint32_t bar = BAR(STEP_FULL + (step & 1));
-                    mbar_arrive_expect_tx(bar, C::TILE_BYTES * ((t >= 1) + (t < nmax)));
-                    if (t >= 1) {  // V_{t-1}
-                        const uint32_t st = (L0 + 2 * (t - 1) + 1) % C::STAGES;
+                    const uint32_t vst = (L0 + 2 * (t - 1) + 1) % C::STAGES;
+                    const uint32_t kst = (L0 + 2 * t) % C::STAGES;
+                    if constexpr (PAGED) {
+                        // V_{t-1} uses the page ids read for K_{t-1} one step earlier
+                        int vp[BN / 16];
 #pragma unroll
-                        for (int c = 0; c < C::CHUNKS; ++c)
-                            tma_load_2d(sKV + st * C::TILE_BYTES + c * C::CHUNK_BYTES, p.tm_v, bar,
-                                        w.g * D + c * 64, a.kv_start + (t - 1) * BN);
-                    }
-                    if (t < nmax) {  // K_t
-                        const uint32_t st = (L0 + 2 * t) % C::STAGES;
+                        for (int i = 0; i < BN / 16; ++i) vp[i] = kp[i];
+                        const int nv = t >= 1 ? nkp : 0;
+                        nkp = t < nmax ? tile_pages(kp, p, pt_row, t, a.kv_len) : 0;
+                        mbar_arrive_expect_tx(bar, tile_page_bytes<C::CHUNKS>(vp, nv, p.page_size) +
+                                                       tile_page_bytes<C::CHUNKS>(kp, nkp, p.page_size));
+                        load_tile_pages<C::CHUNKS, C::CHUNK_BYTES>(sKV + vst * C::TILE_BYTES, p.tm_v,
+                                                                   bar, vp, nv, p.page_size, w.g * D);
+                        load_tile_pages<C::CHUNKS, C::CHUNK_BYTES>(sKV + kst * C::TILE_BYTES, p.tm_k,
+                                                                   bar, kp, nkp, p.page_size, w.g * D);
+                        if (t == nmax && nmax * BN > a.kv_len) mbar_arrive(BAR(FIX_READY));
+                    } else {
+                        mbar_arrive_expect_tx(bar, C::TILE_BYTES * ((t >= 1) + (t < nmax)));
+                        if (t >= 1) {  // V_{t-1}
 #pragma unroll
-                        for (int c = 0; c < C::CHUNKS; ++c)
-                            tma_load_2d(sKV + st * C::TILE_BYTES + c * C::CHUNK_BYTES, p.tm_k, bar,
-                                        w.g * D + c * 64, a.kv_start + t * BN);
+                            for (int c = 0; c < C::CHUNKS; ++c)
+                                tma_load_2d(sKV + vst * C::TILE_BYTES + c * C::CHUNK_BYTES, p.tm_v,
+                                            bar, w.g * D + c * 64, a.kv_start + (t - 1) * BN);
+                        }
+                        if (t < nmax) {  // K_t
+#pragma unroll
+                            for (int c = 0; c < C::CHUNKS; ++c)
+                                tma_load_2d(sKV + kst * C::TILE_BYTES + c * C::CHUNK_BYTES, p.tm_k,
+                                            bar, w.g * D + c * 64, a.kv_start + t * BN);
+                        }
                     }
                 }
                 load_idx = L0 + 2 * nmax;
@@ -814,7 +983,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
             constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, false);
             constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, true);
             const uint64_t qdesc0 = sdesc_sw128(sQ, 16, 1024);
-            uint32_t load_idx = 0, q_count = 0, step = 0;
+            uint32_t load_idx = 0, q_count = 0, step = 0, fixes = 0;
             uint32_t ctr[2] = {0, 0}, items_x[2] = {0, 0};
             bool ok = true;
             int rr = -1;
@@ -832,9 +1001,15 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
                 ++q_count;
                 if (!ok) break;
                 const uint32_t L0 = load_idx;
+                const bool fix = PAGED && nmax * BN > a.kv_len;
                 for (int t = 0; t <= nmax; ++t, ++step) {
-                    ok = mbar_wait_bounded(BAR(STEP_FULL + (step & 1)), (step >> 1) & 1, abort_flag,
-                                           p.status);
+                    if (fix && t == nmax) {  // the last V tile, its tail rows zeroed
+                        ok = mbar_wait_bounded(BAR(V_FIXED), fixes & 1, abort_flag, p.status);
+                        ++fixes;
+                    } else {
+                        ok = mbar_wait_bounded(BAR(STEP_FULL + (step & 1)), (step >> 1) & 1,
+                                               abort_flag, p.status);
+                    }
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t vst = (L0 + 2 * (t - 1) + 1) % C::STAGES;
@@ -885,6 +1060,37 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
             // every MMA issued has completed before tensor memory is released
             mma_commit(BAR(MMA_DRAIN));
             mbar_wait_bounded(BAR(MMA_DRAIN), 0, nullptr, p.status);
+        }
+    } else if (PAGED && warp == 2) {
+        // ------------------------------------------------------------ V tail fixer
+        uint32_t step = 0, load_idx = 0, fixes = 0;
+        bool ok = true;
+        int rr = -1;
+        int it = snake_next(rr, n_items);
+        while (ok && it >= 0) {
+            const WorkItem w = load_item(p.items, it);
+            it = snake_next(rr, n_items);
+            const Geo a = geo_of(w, 0, G, p.causal);
+            const Geo bq = geo_of(w, 1, G, p.causal);
+            const int nmax = max(a.n_tiles, bq.t0 < bq.qo_len ? bq.n_tiles : 0);
+            if (nmax == 0) continue;
+            const uint32_t L0 = load_idx;
+            const uint32_t fin = step + (uint32_t)nmax;  // the item's last step: V_{nmax-1}
+            step += (uint32_t)nmax + 1;
+            load_idx = L0 + 2 * (uint32_t)nmax;
+            if (nmax * BN <= a.kv_len) continue;
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(FIX_READY), fixes & 1, abort_flag,
+                                                           p.status));
+            if (ok)
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait_bounded(BAR(STEP_FULL + (fin & 1)), (fin >> 1) & 1,
+                                                  abort_flag, p.status));
+            if (!ok) break;
+            ++fixes;
+            const uint32_t st = (L0 + 2 * (uint32_t)(nmax - 1) + 1) % C::STAGES;
+            zero_stage_rows<C::CHUNKS, C::CHUNK_BYTES>(sKV + st * C::TILE_BYTES,
+                                                       a.kv_len - (nmax - 1) * BN, lane);
+            mbar_arrive(BAR(V_FIXED));
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------------ softmax / epilogue
@@ -1115,39 +1321,36 @@ static cudaError_t launch_dependent(Kernel kernel, int grid, int threads, int sm
     return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
-template <int D>
-int smem_bytes() {
-    return Cfg<D>::SMEM_BYTES;
-}
-
-template <int D>
+template <int D, bool PAGED>
 cudaError_t launch_attention(const Params& p, int grid, cudaStream_t stream) {
     static bool configured[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(attention_kernel<D>,
+        cudaError_t e = cudaFuncSetAttribute(attention_kernel<D, PAGED>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              Cfg<D>::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    return launch_dependent(attention_kernel<D>, grid, THREADS, Cfg<D>::SMEM_BYTES, stream, p);
+    return launch_dependent(attention_kernel<D, PAGED>, grid, THREADS, Cfg<D>::SMEM_BYTES, stream,
+                            p);
 }
 
+template <bool PAGED>
 cudaError_t launch_attention_pair(const Params& p, int grid, cudaStream_t stream) {
     static bool configured[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(attention_pair_kernel,
+        cudaError_t e = cudaFuncSetAttribute(attention_pair_kernel<PAGED>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              PairCfg::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    return launch_dependent(attention_pair_kernel, grid, PAIR_THREADS, PairCfg::SMEM_BYTES, stream,
-                            p);
+    return launch_dependent(attention_pair_kernel<PAGED>, grid, PAIR_THREADS, PairCfg::SMEM_BYTES,
+                            stream, p);
 }
 
 cudaError_t launch_plan(const PlanParams& pp, const CUtensorMap& tq, const CUtensorMap& tk,
@@ -1156,7 +1359,10 @@ cudaError_t launch_plan(const PlanParams& pp, const CUtensorMap& tq, const CUten
     return cudaGetLastError();
 }
 
-template cudaError_t launch_attention<256>(const Params&, int, cudaStream_t);
+template cudaError_t launch_attention<256, false>(const Params&, int, cudaStream_t);
+template cudaError_t launch_attention<256, true>(const Params&, int, cudaStream_t);
+template cudaError_t launch_attention_pair<false>(const Params&, int, cudaStream_t);
+template cudaError_t launch_attention_pair<true>(const Params&, int, cudaStream_t);
 
 }  // namespace prefill
 }  // namespace pgqa

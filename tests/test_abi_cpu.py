@@ -37,8 +37,9 @@ def api():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for n in ("pgqa_ragged_prefill_bf16", "pgqa_paged_decode_bf16", "ragged_prefill_bf16",
-              "paged_decode_bf16", "pgqa_set_workspace", "pgqa_get_device_status"):
+    for n in ("pgqa_ragged_prefill_bf16", "pgqa_paged_prefill_bf16", "pgqa_paged_decode_bf16",
+              "ragged_prefill_bf16", "paged_prefill_bf16", "paged_decode_bf16",
+              "pgqa_set_workspace", "pgqa_get_device_status"):
         assert n in names
 
 
@@ -83,6 +84,34 @@ def decode(api, **kw):
         args["hk"], args["d"], args["scale"], None)
 
 
+def paged_prefill(api, **kw):
+    args = dict(q=A, kp=A, vp=A, o=A, lse=A, qi=A, pt=A, stride=8, kl=A, ps=16, npages=100,
+                batch=2, hq=8, hk=2, d=128, causal=1, scale=0.1)
+    args.update(kw)
+    p = ctypes.c_void_p
+    return api.lib.pgqa_paged_prefill_bf16(
+        p(args["q"]), p(args["kp"]), p(args["vp"]), p(args["o"]), p(args["lse"]), p(args["qi"]),
+        p(args["pt"]), args["stride"], p(args["kl"]), args["ps"], args["npages"], args["batch"],
+        args["hq"], args["hk"], args["d"], args["causal"], args["scale"], None)
+
+
+def test_paged_prefill_host_validation(api):
+    assert paged_prefill(api, batch=0) == 0
+    assert paged_prefill(api, batch=-2) == -1
+    assert paged_prefill(api, kl=0) == -1
+    assert paged_prefill(api, qi=0) == -1
+    assert paged_prefill(api, pt=A + 2) == -1               # misaligned page table
+    assert paged_prefill(api, kp=A + 8) == -1
+    assert paged_prefill(api, ps=8) == -2
+    assert paged_prefill(api, ps=48) == -2
+    assert paged_prefill(api, ps=256) == -2
+    assert paged_prefill(api, d=64) == -2
+    assert paged_prefill(api, hq=24, hk=8) == -2
+    assert paged_prefill(api, scale=float("inf")) == -1
+    assert paged_prefill(api, npages=-1) == -1
+    assert paged_prefill(api, stride=1 << 28, ps=128) == -2  # keys per request overflow int32
+
+
 def test_prefill_host_validation(api):
     assert prefill(api, batch=0) == 0                       # empty batch: early return
     assert prefill(api, batch=-1) == -1
@@ -112,6 +141,9 @@ def test_valid_calls_without_a_gpu_report_no_device(api):
         pytest.skip("a GPU is present")
     assert prefill(api) == -7
     assert decode(api) == -7
+    for ps in (16, 32, 64, 128):
+        assert paged_prefill(api, ps=ps) == -7
+    assert paged_prefill(api, d=256) == -7
 
 
 def test_workspace_size_queries(api):

@@ -1,0 +1,165 @@
+"""GPU parity of the paged prefill / append (pgqa_paged_prefill_bf16) against the oracle.
+
+Ragged query rows attend over a paged NHD KV cache addressed by a page table (FlashInfer
+documentation, flashinfer.prefill, BatchPrefillWithPagedKVCacheWrapper; page-table rules
+of the vllm-rlt pull request "feat: add FlashInfer attention backend for SM120 decode").
+Small cases are compared on every row; the cached-prefix hd256 serving shape and a
+4-token-per-request decode (speculative verification) are compared on sampled rows.
+Invariants: the result equals the ragged prefill over the same keys laid out
+contiguously (bit for bit), and page-table padding and NaN in unused key slots of a
+request's last page are invisible.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_gqa_attention_varlen_gb300 import workloads as W
+from gpu_util import check_rows, gather_rows, sample_prefill_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def run_gpu(api, pc, **kw):
+    o, lse = api.paged_prefill(pc.q, pc.k_pages, pc.v_pages, pc.q_indptr, pc.page_table,
+                               pc.kv_lens_t, causal=pc.causal, sm_scale=pc.sm_scale, **kw)
+    torch.cuda.synchronize()
+    return o, lse
+
+
+def oracle_paged(pc, rows=None):
+    return oracle.paged_attention(pc.q, pc.q_indptr, pc.k_pages, pc.v_pages, pc.page_table,
+                                  pc.kv_lens_t, pc.num_qo_heads, pc.num_kv_heads, pc.causal,
+                                  pc.sm_scale, rows=rows)
+
+
+def full_check(api, pc, what):
+    o, lse = run_gpu(api, pc)
+    assert api.device_status() == 0
+    ro, rl = oracle_paged(pc)
+    return check_rows(o.reshape(-1, o.shape[-1]).float().cpu(), lse.reshape(-1).cpu(), ro, rl,
+                      what)
+
+
+SMALL = [
+    # qo_lens, kv_lens, Hq, Hk, d, causal, page_size
+    ([17, 64], [17, 64], 4, 2, 128, True, 16),
+    ([200, 77], [500, 1000], 8, 1, 128, True, 16),       # cached prefix
+    ([200, 77], [500, 1000], 8, 1, 128, False, 32),
+    ([90, 40], [30, 40], 4, 4, 128, True, 64),           # kv < qo: leading rows see no key
+    ([0, 33, 0, 70], [10, 33, 0, 0], 16, 1, 128, True, 16),  # empty q / empty kv requests
+    ([513], [700], 16, 16, 128, True, 128),              # G = 1, one page per K/V tile
+    ([260, 31], [300, 31], 32, 2, 128, True, 16),        # G = 16
+    ([129, 200], [129, 700], 8, 2, 256, True, 16),       # hd256
+    ([64, 300], [64, 333], 4, 1, 256, False, 64),
+    ([4] * 8, [1000, 17, 129, 4096, 5, 2048, 3000, 64], 32, 8, 128, True, 16),  # 4-token decode
+    ([1] * 5, [1, 16, 17, 300, 1029], 8, 2, 128, True, 32),  # one-token decode shape
+    ([3, 7], [2000, 131], 16, 4, 256, True, 32),         # hd256 multi-token decode
+]
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=[f"p{i}" for i in range(len(SMALL))])
+def test_small_shapes(cuda_lib, shape):
+    qo, kv, hq, hk, d, causal, ps = shape
+    pc = W.paged_case(kv, hq, hk, d, page_size=ps, qo_lens=qo, causal=causal,
+                      seed=len(qo) * 37 + hq + d + ps, device="cuda")
+    full_check(cuda_lib, pc, f"paged {shape}")
+
+
+@pytest.mark.parametrize("d,ps", [(128, 16), (128, 64), (256, 32)])
+def test_matches_ragged_prefill_bitwise(cuda_lib, d, ps):
+    """The paged kernel and the ragged kernel see the same keys in the same tiles, so
+    their results agree bit for bit."""
+    qo, kv = [300, 45, 1], [1000, 45, 777]
+    pc = W.paged_case(kv, 16, 4, d, page_size=ps, qo_lens=qo, seed=41 + d + ps, device="cuda")
+    o_p, l_p = run_gpu(cuda_lib, pc)
+    ks, vs = [], []
+    for b, n in enumerate(kv):
+        pages = pc.page_table[b, :(n + ps - 1) // ps].long()
+        ks.append(pc.k_pages[pages].reshape(-1, 4, d)[:n])
+        vs.append(pc.v_pages[pages].reshape(-1, 4, d)[:n])
+    k = torch.cat(ks).contiguous()
+    v = torch.cat(vs).contiguous()
+    kv_indptr = torch.tensor(np.concatenate([[0], np.cumsum(kv)]), dtype=torch.int32,
+                             device="cuda")
+    o_r, l_r = cuda_lib.ragged_prefill(pc.q, k, v, pc.q_indptr, kv_indptr, causal=True,
+                                       sm_scale=pc.sm_scale)
+    torch.cuda.synchronize()
+    assert cuda_lib.device_status() == 0
+    assert torch.equal(o_p, o_r) and torch.equal(l_p, l_r)
+
+
+@pytest.mark.parametrize("d", [128, 256])
+def test_nan_in_unused_tail_slots_is_invisible(cuda_lib, d):
+    ps = 16
+    kv = [20, 1030, 130]
+    pc = W.paged_case(kv, 8, 2, d, page_size=ps, qo_lens=[20, 70, 3], seed=43 + d,
+                      device="cuda")
+    o1, l1 = run_gpu(cuda_lib, pc)
+    for b, n in enumerate(kv):
+        last = int(pc.page_table[b, (n - 1) // ps])
+        pc.k_pages[last, n % ps:] = float("nan")
+        pc.v_pages[last, n % ps:] = float("nan")
+    o2, l2 = run_gpu(cuda_lib, pc)
+    assert cuda_lib.device_status() == 0
+    assert torch.isfinite(o2).all()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_page_table_padding_is_bitwise_invisible(cuda_lib):
+    outs = []
+    for pad in (-1, 0, 55):
+        pc = W.paged_case([40, 1500, 7], 16, 4, 128, page_size=32, qo_lens=[40, 100, 7],
+                          pad=pad, stride=70, seed=47, device="cuda")
+        outs.append(run_gpu(cuda_lib, pc))
+        assert cuda_lib.device_status() == 0
+    for o, l in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
+
+
+def test_prefix_hd256_shape_sampled(cuda_lib):
+    """The cached-prefix hd256 serving shape (8 requests, qo U{256..2048}, prefix
+    U{0..8192}, 16/4 heads) with its keys in a paged cache of 16-token pages."""
+    qo, kv = W.config_lengths("prefix_hd256")
+    pc = W.paged_case(kv, 16, 4, 256, page_size=16, qo_lens=qo, seed=0, device="cuda")
+    o, lse = run_gpu(cuda_lib, pc)
+    assert cuda_lib.device_status() == 0
+    rows = sample_prefill_rows(qo, 16, 4, seed=3, per_request_random=16)
+    og, lg = gather_rows(o, lse, rows, 16)
+    ro, rl = oracle_paged(pc, rows=rows)
+    check_rows(og, lg, ro, rl, "paged prefix_hd256")
+
+
+def test_multi_token_decode_sampled(cuda_lib):
+    """Four query tokens per request (speculative verification) over the first 48
+    requests of the paged decode workload's lengths, 32/8 heads, 16-token pages."""
+    kv = W.config_lengths("decode")[1][:48]
+    pc = W.paged_case(kv, 32, 8, 128, page_size=16, qo_lens=[4] * len(kv), seed=5,
+                      device="cuda")
+    o, lse = run_gpu(cuda_lib, pc)
+    assert cuda_lib.device_status() == 0
+    rng = np.random.default_rng(1)
+    rows = np.sort(rng.choice(4 * len(kv) * 32, 600, replace=False)).astype(np.int64)
+    og, lg = gather_rows(o, lse, rows, 32)
+    ro, rl = oracle_paged(pc, rows=rows)
+    check_rows(og, lg, ro, rl, "4-token decode")
+
+
+def test_bad_kv_len_reports_bounds_and_writes_nothing(cuda_lib):
+    pc = W.paged_case([40, 50], 8, 2, 128, page_size=16, qo_lens=[5, 6], seed=53,
+                      device="cuda")
+    pc.kv_lens_t[1] = pc.page_table.shape[1] * 16 + 1
+    o = torch.full_like(pc.q, 7.0)
+    run_gpu(cuda_lib, pc, out=o)
+    assert cuda_lib.device_status() == -6
+    assert torch.all(o == 7.0)
+
+
+def test_bad_page_id_reports_bounds_status(cuda_lib):
+    pc = W.paged_case([300], 8, 2, 128, page_size=16, qo_lens=[10], seed=59, device="cuda")
+    pc.page_table[0, 3] = pc.num_pages + 5
+    run_gpu(cuda_lib, pc)
+    assert cuda_lib.device_status() == -6
+    pc.page_table[0, 3] = 0
+    run_gpu(cuda_lib, pc)
+    assert cuda_lib.device_status() == 0
