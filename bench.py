@@ -350,6 +350,8 @@ def bench_gpu(args, ws, rank, local):
     d_e2e_ms = reduce_max(e0.elapsed_time(e1), dev)
     d_e2e_value = dc_bytes * ws * e2e_steps / (d_e2e_ms / 1e3) / 1e9
 
+    extra = None if args.no_extra else bench_extra(api, W, dev, stream, dc, peaks)
+
     if rank != 0:
         return 0
 
@@ -408,9 +410,83 @@ def bench_gpu(args, ws, rank, local):
         "clocks": clk,
         "device_status": status,
         "cpu_baseline": cpu,
+        "extra": extra,
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def time_calls(fn, stream, reps=20, warmup=3):
+    """Milliseconds per call of fn(): back-to-back launches between CUDA events on `stream`."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        fn()
+    e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def bench_extra(api, W, dev, stream, dc, peaks):
+    """The paged prefill (ragged queries over a paged KV cache) on the prefill_hd128 and
+    prefix_hd256 shapes with 16-token pages, the ragged prefix_hd256 beside it, and
+    4-token-per-request decode (speculative verification) over the resident 256-request
+    decode cache; each timed on its own (inputs resident in HBM)."""
+    out = {}
+
+    def tensor_line(flops, ms, what):
+        tf = flops / (ms / 1e3) / 1e12
+        return {"what": what, "ms_per_launch": ms, "value": tf, "unit": "TFLOP/s",
+                "roofline": {"bound": "tensor", "peak": peaks["bf16_tflops"],
+                             "frac": tf / peaks["bf16_tflops"]}}
+
+    for name in ("prefill_hd128", "prefix_hd256"):
+        qo, kv = W.config_lengths(name)
+        rc = W.config(name, device=dev)
+        pc = W.paged_case(kv, rc.num_qo_heads, rc.num_kv_heads, rc.head_dim, page_size=16,
+                          qo_lens=qo, seed=0, device=dev)
+        flops = prefill_flops(qo, kv, rc.num_qo_heads, rc.head_dim)
+        o = torch.empty_like(pc.q)
+        lse = torch.empty(pc.q.shape[:2], dtype=torch.float32, device=dev)
+        ms = time_calls(lambda: api.paged_prefill(pc.q, pc.k_pages, pc.v_pages, pc.q_indptr,
+                                                  pc.page_table, pc.kv_lens_t, causal=True,
+                                                  sm_scale=pc.sm_scale, out=o, lse=lse,
+                                                  stream=stream), stream)
+        out[f"paged_prefill_{name}"] = tensor_line(flops, ms, f"{name} shape, keys in 16-token "
+                                                   "pages (random page order)")
+        if name == "prefix_hd256":
+            o2 = torch.empty_like(rc.q)
+            l2 = torch.empty(rc.q.shape[:2], dtype=torch.float32, device=dev)
+            ms = time_calls(lambda: api.ragged_prefill(rc.q, rc.k, rc.v, rc.q_indptr,
+                                                       rc.kv_indptr, causal=True,
+                                                       sm_scale=rc.sm_scale, out=o2, lse=l2,
+                                                       stream=stream), stream)
+            out["ragged_prefill_prefix_hd256"] = tensor_line(flops, ms, "prefix_hd256, ragged K/V")
+        del pc, rc, o, lse
+    # 4 query tokens per request over the decode workload's paged cache
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    q4 = torch.randn((dc.batch * 4, dc.num_qo_heads, dc.head_dim), generator=g, device=dev,
+                     dtype=torch.float32).to(torch.bfloat16)
+    qi4 = torch.arange(0, 4 * dc.batch + 1, 4, dtype=torch.int32, device=dev)
+    o4 = torch.empty_like(q4)
+    l4 = torch.empty(q4.shape[:2], dtype=torch.float32, device=dev)
+    ms = time_calls(lambda: api.paged_prefill(q4, dc.k_pages, dc.v_pages, qi4, dc.page_table,
+                                              dc.kv_lens_t, causal=True, sm_scale=dc.sm_scale,
+                                              out=o4, lse=l4, stream=stream), stream, reps=10)
+    kv_bytes = decode_kv_bytes(dc.kv_lens, dc.num_kv_heads, dc.head_dim)
+    gbs = kv_bytes / (ms / 1e3) / 1e9
+    out["multi_token_decode_q4"] = {
+        "what": "256 requests x 4 query tokens (decode workload's cache, causal)",
+        "ms_per_launch": ms, "value": gbs, "unit": "GB/s",
+        "roofline": {"bound": "hbm", "peak": peaks["hbm_gbs"], "frac": gbs / peaks["hbm_gbs"]}}
+    out["device_status"] = api.device_status()
+    torch.cuda.empty_cache()
+    return out
 
 
 def profile_case(args):
@@ -425,6 +501,23 @@ def profile_case(args):
         for _ in range(args.reps):
             api.ragged_prefill(c.q, c.k, c.v, c.q_indptr, c.kv_indptr, causal=c.causal,
                                sm_scale=c.sm_scale, out=o, lse=lse)
+    elif args.profile in ("paged_prefill_hd128", "paged_prefix_hd256", "decode_q4"):
+        # paged prefill: the named shape in 16-token pages; decode_q4: 4 query tokens per
+        # request over the first --decode-batch requests of the decode workload
+        if args.profile == "decode_q4":
+            kv = W.config_lengths("decode")[1][:args.decode_batch]
+            c = W.paged_case(kv, 32, 8, 128, page_size=16, qo_lens=[4] * len(kv), seed=0,
+                             device=dev)
+        else:
+            name = args.profile[len("paged_"):]
+            qo, kv = W.config_lengths(name)
+            hq, hk, d = (32, 8, 128) if name == "prefill_hd128" else (16, 4, 256)
+            c = W.paged_case(kv, hq, hk, d, page_size=16, qo_lens=qo, seed=0, device=dev)
+        o = torch.empty_like(c.q)
+        lse = torch.empty(c.q.shape[:2], dtype=torch.float32, device=dev)
+        for _ in range(args.reps):
+            api.paged_prefill(c.q, c.k_pages, c.v_pages, c.q_indptr, c.page_table, c.kv_lens_t,
+                              causal=True, sm_scale=c.sm_scale, out=o, lse=lse)
     else:  # decode slice: the first --decode-batch requests of the decode workload
         kv = W.config_lengths("decode")[1][:args.decode_batch]
         c = W.paged_case(kv, 32, 8, 128, page_size=16, seed=0, device=dev)
@@ -452,8 +545,11 @@ def main(argv=None):
     ap.add_argument("--cpu-rows", type=int, default=800000,
                     help="oracle rows timed for the cpu_baseline object (about 10-30 s)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the paged-prefill and multi-token-decode measurements")
     ap.add_argument("--profile", choices=["prefill_hd128", "prefix_hd256", "long", "tiny",
-                                          "decode"], default=None,
+                                          "decode", "paged_prefill_hd128", "paged_prefix_hd256",
+                                          "decode_q4"], default=None,
                     help="run one bounded case --reps times and exit (ncu captures)")
     ap.add_argument("--reps", type=int, default=4)
     ap.add_argument("--decode-batch", type=int, default=32)

@@ -13,6 +13,12 @@ constexpr int PGQA_DEV_BOUNDS = 2;     // bad indptr / kv_len / page id
 constexpr int PGQA_DEV_CAPACITY = 4;   // work list larger than the workspace
 
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s per wait
+// Words status[kDiagFlag .. kDiagFlag + 4] after the status word: set once by the first
+// wait that times out (flag, block, thread, barrier shared-memory address, parity); then,
+// in that block, warp w (< 16) that leaves a wait on the abort flag writes the barrier
+// address and parity it was waiting for to status[kDiagFlag + 6 + 2w], [.. + 7 + 2w].
+// The status word lives in a header of at least 64 ints, so these words fit after it.
+constexpr int kDiagFlag = 4;
 
 // ------------------------------------------------------------------ workspace layout
 // [0, 256)      header: status word, counters

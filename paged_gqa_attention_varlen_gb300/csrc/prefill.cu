@@ -804,7 +804,7 @@ struct PairCfg {
     static constexpr int CHUNK_BYTES = BM * 128;
     static constexpr int TILE_BYTES = BM * D * 2;
     static constexpr int STAGES = 4;
-    static constexpr int NUM_BARS = 13;
+    static constexpr int NUM_BARS = 15;
     static constexpr int SMEM_BYTES = 1024 + TILE_BYTES * (2 + STAGES) + 8 * NUM_BARS + 16;
 };
 
@@ -832,13 +832,19 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
     // A step's stages are free again once its last MMA group has completed: that group's
     // commit is S_FULL of tile B (tile A for items without B) or, on an item's final step,
     // PV_DONE; the producer waits on those, so the MMA warp issues no extra commit.
+    // S_FULL[2x + c % 2]: Q.K^T of tile x's c-th K/V tile is in tensor memory.  Two
+    // barriers per tile, alternating: the producer waits for step t's completion only
+    // after it has issued step t + 1, so with one barrier per tile the completions of
+    // steps t and t + 1 could both land before it looks and its parity wait would miss
+    // them.  The next completion on the same barrier needs step t + 2's loads, which the
+    // producer issues only after that wait.
     // Paged K/V only: slots past kv_len in an item's last V tile hold whatever the cache
     // holds there (or stale data of an earlier tile), and P.V would turn a NaN there into
     // a NaN result even with P = 0.  The producer arrives on FIX_READY once it has issued
     // the loads of such a last step; warp 2 then waits for them, zeroes those V rows and
     // arrives on V_FIXED, which the MMA warp waits for instead of the step's STEP_FULL.
     constexpr int Q_FULL = 0, Q_EMPTY = 1, STEP_FULL = 2, S_FULL = 4,
-                  P_FULL = S_FULL + 2, PV_DONE = P_FULL + 2, MMA_DRAIN = PV_DONE + 2,
+                  P_FULL = S_FULL + 4, PV_DONE = P_FULL + 2, MMA_DRAIN = PV_DONE + 2,
                   FIX_READY = MMA_DRAIN + 1, V_FIXED = FIX_READY + 1;
     static_assert(V_FIXED + 1 == C::NUM_BARS, "barrier count");
 
@@ -849,7 +855,8 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
         mbar_init(BAR(Q_EMPTY), 1);
         for (int x = 0; x < 2; ++x) {
             mbar_init(BAR(STEP_FULL + x), 1);
-            mbar_init(BAR(S_FULL + x), 1);
+            mbar_init(BAR(S_FULL + 2 * x), 1);
+            mbar_init(BAR(S_FULL + 2 * x + 1), 1);
             mbar_init(BAR(P_FULL + x), 128);
             mbar_init(BAR(PV_DONE + x), 1);
         }
@@ -920,8 +927,9 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
                         if (!ok) break;
                     }
                     if (t < nmax) {
-                        done_bar[step & 1] = BAR(S_FULL + lx);
-                        done_par[step & 1] = (ctr[lx] + t) & 1;
+                        const uint32_t c = ctr[lx] + t;
+                        done_bar[step & 1] = BAR(S_FULL + 2 * lx + (c & 1));
+                        done_par[step & 1] = (c >> 1) & 1;
                     } else {
                         done_bar[step & 1] = BAR(PV_DONE + lx);
                         done_par[step & 1] = items_x[lx] & 1;
@@ -1043,7 +1051,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
                                 mma_ss(tmem_base + 128u * x, qdesc + off, kdesc + off, IDESC_QK,
                                        k > 0 ? 1u : 0u);
                             }
-                            mma_commit(BAR(S_FULL + x));
+                            mma_commit(BAR(S_FULL + 2 * x + ((ctr[x] + t) & 1)));
                         }
                     }
                     if (!ok) break;
@@ -1179,7 +1187,8 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
             float m_used = -INFINITY, l = 0.f;
             for (int j = 0; j < x.n_tiles; ++j) {
                 const uint32_t c = ctr + j;
-                ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(S_FULL + X), c & 1, abort_flag,
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(S_FULL + 2 * X + (c & 1)),
+                                                               (c >> 1) & 1, abort_flag,
                                                                p.status));
                 if (!ok) break;
                 tc_fence_after();

@@ -56,10 +56,29 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 63u) == 0) {
-            if (abort_flag != nullptr && *abort_flag) return false;
+            if (abort_flag != nullptr && *abort_flag) {
+                // in the block that timed out first, each warp notes where it was waiting
+                if (status != nullptr && status[kDiagFlag] == 1 &&
+                    status[kDiagFlag + 1] == (int)blockIdx.x && (threadIdx.x & 31) == 0 &&
+                    threadIdx.x / 32 < 16) {
+                    status[kDiagFlag + 6 + 2 * (threadIdx.x / 32)] = (int)bar;
+                    status[kDiagFlag + 7 + 2 * (threadIdx.x / 32)] = (int)parity;
+                }
+                return false;
+            }
             if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
                 if (abort_flag != nullptr) *abort_flag = 1;
-                if (status != nullptr) atomicOr(status, PGQA_DEV_TIMEOUT);
+                if (status != nullptr) {
+                    atomicOr(status, PGQA_DEV_TIMEOUT);
+                    // the first wait that gives up records where: block, thread, barrier
+                    // (shared-memory address) and the parity it waited for
+                    if (atomicCAS(status + kDiagFlag, 0, 1) == 0) {
+                        status[kDiagFlag + 1] = (int)blockIdx.x;
+                        status[kDiagFlag + 2] = (int)threadIdx.x;
+                        status[kDiagFlag + 3] = (int)bar;
+                        status[kDiagFlag + 4] = (int)parity;
+                    }
+                }
                 return false;
             }
         }

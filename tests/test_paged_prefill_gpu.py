@@ -130,6 +130,21 @@ def test_prefix_hd256_shape_sampled(cuda_lib):
     check_rows(og, lg, ro, rl, "paged prefix_hd256")
 
 
+def test_prefill_hd128_shape_many_items_per_cta(cuda_lib):
+    """The 16-request hd128 serving shape in 16-token pages: about 33 work items per CTA,
+    which exercises the K/V stage hand-off across many steps and item boundaries (a
+    stage-release race once timed out here); sampled rows against the oracle."""
+    qo, kv = W.config_lengths("prefill_hd128")
+    pc = W.paged_case(kv, 32, 8, 128, page_size=16, qo_lens=qo, seed=0, device="cuda")
+    for _ in range(3):
+        o, lse = run_gpu(cuda_lib, pc)
+        assert cuda_lib.device_status() == 0
+    rows = sample_prefill_rows(qo, 32, 4, seed=5, per_request_random=8)
+    og, lg = gather_rows(o, lse, rows, 32)
+    ro, rl = oracle_paged(pc, rows=rows)
+    check_rows(og, lg, ro, rl, "paged prefill_hd128")
+
+
 def test_multi_token_decode_sampled(cuda_lib):
     """Four query tokens per request (speculative verification) over the first 48
     requests of the paged decode workload's lengths, 32/8 heads, 16-token pages."""
