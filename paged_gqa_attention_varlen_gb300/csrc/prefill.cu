@@ -315,50 +315,45 @@ __global__ void __launch_bounds__(PLAN_THREADS)
 }
 
 // ------------------------------------------------------------------ paged K/V
-// Page ids of the pages of K/V tile j (keys j*BN .. j*BN+BN-1) that hold keys below
-// kv_len; pages past a request's last key are never read.  An id outside the page pool
-// is reported (PGQA_DEV_BOUNDS) and recorded as -1: that page is not loaded.  Returns the
-// number of pages in use (the tile's first n pages).
-__device__ __forceinline__ int tile_pages(int (&pid)[BN / 16], const Params& p, const int* pt_row,
-                                          int j, int kv_len) {
-    const int ps = p.page_size;
-    const int ppt = BN / ps;
-    const int first = j * ppt;
-    const int n = min(ppt, (kv_len + ps - 1) / ps - first);
-#pragma unroll
-    for (int i = 0; i < BN / 16; ++i) {
-        pid[i] = -1;
-        if (i < n) {
-            const int id = __ldg(pt_row + first + i);
-            if (id >= 0 && id < p.num_pages) pid[i] = id;
-            else atomicOr(p.status, PGQA_DEV_BOUNDS);
-        }
-    }
-    return n;
+// With paged K/V the producer is a whole warp: lane l owns page l of a K/V tile (a tile
+// of BN keys spans BN / page_size pages).  Pages past a request's last key are never read.
+// Page id of lane l for tile j (-1 if that page holds no key of the request).
+__device__ __forceinline__ int lane_page_id(const int* pt_row, int j, int ppt, int npg, int lane) {
+    const int pg = j * ppt + lane;
+    return lane < ppt && pg < npg ? __ldg(pt_row + pg) : -1;
 }
-
-// Bytes the TMA copies of tile_pages() will deliver.
-template <int CHUNKS>
-__device__ __forceinline__ uint32_t tile_page_bytes(const int (&pid)[BN / 16], int n, int ps) {
-    uint32_t b = 0;
-#pragma unroll
-    for (int i = 0; i < BN / 16; ++i)
-        if (i < n && pid[i] >= 0) b += (uint32_t)(CHUNKS * ps * 128);
-    return b;
+// Whether lane l's page of tile j is in use, reporting an id outside the page pool
+// (PGQA_DEV_BOUNDS; that page is then not loaded).
+__device__ __forceinline__ bool lane_page_ok(int id, int j, int ppt, int npg, int num_pages,
+                                             int lane, int* status) {
+    const bool in_use = lane < ppt && j * ppt + lane < npg;
+    const bool ok = in_use && id >= 0 && id < num_pages;
+    if (in_use && !ok) atomicOr(status, PGQA_DEV_BOUNDS);
+    return ok;
 }
-
-// One box per page and 64-column chunk: page i of the tile lands at rows i*ps.. of every
-// chunk of the stage, the layout a single 128-row box would have written.
+// Warp-collective: arm `bar` with the bytes of every valid page box of this load (lane 0),
+// then each lane issues the boxes of its own page(s): one box per 64-column chunk, landing
+// at rows lane * ps .. of every chunk of the stage, the layout a single 128-row box would
+// have written.
 template <int CHUNKS, int CHUNK_BYTES>
-__device__ __forceinline__ void load_tile_pages(uint32_t dst, const CUtensorMap* tm, uint32_t bar,
-                                                const int (&pid)[BN / 16], int n, int ps, int col0) {
+__device__ __forceinline__ void issue_page_boxes(uint32_t bar, int ps, int col0, int lane,
+                                                 bool v_ok, uint32_t v_dst, const CUtensorMap* tm_v,
+                                                 int v_id, bool k_ok, uint32_t k_dst,
+                                                 const CUtensorMap* tm_k, int k_id) {
+    const int n = __popc(__ballot_sync(0xffffffffu, v_ok)) +
+                  __popc(__ballot_sync(0xffffffffu, k_ok));
+    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(n * CHUNKS * ps * 128));
+    __syncwarp();
+    const uint32_t row_off = (uint32_t)(lane * ps * 128);
+    if (v_ok) {
 #pragma unroll
-    for (int i = 0; i < BN / 16; ++i) {
-        if (i < n && pid[i] >= 0) {
+        for (int c = 0; c < CHUNKS; ++c)
+            tma_load_2d(v_dst + c * CHUNK_BYTES + row_off, tm_v, bar, col0 + c * 64, v_id * ps);
+    }
+    if (k_ok) {
 #pragma unroll
-            for (int c = 0; c < CHUNKS; ++c)
-                tma_load_2d(dst + c * CHUNK_BYTES + i * ps * 128, tm, bar, col0 + c * 64, pid[i] * ps);
-        }
+        for (int c = 0; c < CHUNKS; ++c)
+            tma_load_2d(k_dst + c * CHUNK_BYTES + row_off, tm_k, bar, col0 + c * 64, k_id * ps);
     }
 }
 
@@ -464,10 +459,20 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
+        // Ragged K/V: lane 0 alone.  Paged K/V: the whole warp, lane l loading page l of
+        // each K/V tile (its id read one load ahead); lane 0 arms the barriers.
+        if (PAGED || lane == 0) {
+            auto wait = [&](uint32_t bar, uint32_t par) -> bool {
+                if constexpr (PAGED)
+                    return __all_sync(0xffffffffu, mbar_wait_bounded(bar, par, abort_flag, p.status));
+                else
+                    return mbar_wait_bounded(bar, par, abort_flag, p.status);
+            };
             tensormap_acquire(p.tm_q);
             tensormap_acquire(p.tm_k);
             tensormap_acquire(p.tm_v);
+            const int ps = p.page_size;
+            const int ppt = PAGED ? BN / ps : 0;
             uint32_t load_idx = 0, q_count = 0;
             bool ok = true;
             int rr = -1;
@@ -478,45 +483,52 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
                 if (it >= 0) prefetch_l1(p.items + it);
                 const Geo x = geo_of(w, 0, G, p.causal);
                 if (x.n_tiles == 0) continue;
-                ok = mbar_wait_bounded(BAR(Q_EMPTY), (q_count & 1) ^ 1, abort_flag, p.status);
+                ok = wait(BAR(Q_EMPTY), (q_count & 1) ^ 1);
                 if (!ok) break;
-                mbar_arrive_expect_tx(BAR(Q_FULL), C::TILE_BYTES);
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(BAR(Q_FULL), C::TILE_BYTES);
 #pragma unroll
-                for (int c = 0; c < C::CHUNKS; ++c)
-                    tma_load_3d(sQ + c * C::CHUNK_BYTES, p.tm_q, BAR(Q_FULL), c * 64, w.g * G,
-                                x.q_start + x.t0);
+                    for (int c = 0; c < C::CHUNKS; ++c)
+                        tma_load_3d(sQ + c * C::CHUNK_BYTES, p.tm_q, BAR(Q_FULL), c * 64, w.g * G,
+                                    x.q_start + x.t0);
+                }
                 ++q_count;
-                const int* pt_row = PAGED ? p.page_table + (size_t)w.b * p.page_table_stride : nullptr;
                 // consumption order of the MMA warp: K0, (K1, V0), (K2, V1), ..., V_{n-1}
                 const int nl = 2 * x.n_tiles;
-                for (int s = 0; s < nl; ++s) {
-                    int j;
-                    bool is_k;
+                auto tile_of = [&](int s, bool& is_k) -> int {
                     if (s == 0) {
-                        j = 0;
                         is_k = true;
-                    } else if (s == nl - 1) {
-                        j = x.n_tiles - 1;
-                        is_k = false;
-                    } else {
-                        const int pr = (s - 1) >> 1;
-                        is_k = ((s - 1) & 1) == 0;
-                        j = is_k ? pr + 1 : pr;
+                        return 0;
                     }
+                    if (s == nl - 1) {
+                        is_k = false;
+                        return x.n_tiles - 1;
+                    }
+                    const int pr = (s - 1) >> 1;
+                    is_k = ((s - 1) & 1) == 0;
+                    return is_k ? pr + 1 : pr;
+                };
+                const int* pt_row = PAGED ? p.page_table + (size_t)w.b * p.page_table_stride : nullptr;
+                const int npg = PAGED ? (x.kv_len + ps - 1) / ps : 0;
+                int pid = PAGED ? lane_page_id(pt_row, 0, ppt, npg, lane) : -1;  // load 0
+                for (int s = 0; s < nl; ++s) {
+                    bool is_k;
+                    const int j = tile_of(s, is_k);
                     const uint32_t st = load_idx % C::STAGES;
-                    ok = mbar_wait_bounded(BAR(KV_EMPTY + st), ((load_idx / C::STAGES) & 1) ^ 1,
-                                           abort_flag, p.status);
+                    ok = wait(BAR(KV_EMPTY + st), ((load_idx / C::STAGES) & 1) ^ 1);
                     if (!ok) break;
                     const CUtensorMap* tm = is_k ? p.tm_k : p.tm_v;
                     if constexpr (PAGED) {
-                        int pid[BN / 16];
-                        const int np = tile_pages(pid, p, pt_row, j, x.kv_len);
-                        mbar_arrive_expect_tx(BAR(KV_FULL + st),
-                                              tile_page_bytes<C::CHUNKS>(pid, np, p.page_size));
-                        load_tile_pages<C::CHUNKS, C::CHUNK_BYTES>(sKV + st * C::TILE_BYTES, tm,
-                                                                   BAR(KV_FULL + st), pid, np,
-                                                                   p.page_size, w.g * D);
-                        if (s == nl - 1 && x.n_tiles * BN > x.kv_len) mbar_arrive(BAR(FIX_READY));
+                        const bool pg_ok = lane_page_ok(pid, j, ppt, npg, p.num_pages, lane, p.status);
+                        issue_page_boxes<C::CHUNKS, C::CHUNK_BYTES>(
+                            BAR(KV_FULL + st), ps, w.g * D, lane, false, 0, tm, 0, pg_ok,
+                            sKV + st * C::TILE_BYTES, tm, pid);
+                        if (lane == 0 && s == nl - 1 && x.n_tiles * BN > x.kv_len)
+                            mbar_arrive(BAR(FIX_READY));
+                        if (s + 1 < nl) {
+                            bool kn;
+                            pid = lane_page_id(pt_row, tile_of(s + 1, kn), ppt, npg, lane);
+                        }
                     } else {
                         mbar_arrive_expect_tx(BAR(KV_FULL + st), C::TILE_BYTES);
 #pragma unroll
@@ -527,7 +539,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
                     ++load_idx;
                 }
             }
-            if (!ok) {
+            if (!ok && lane == 0) {
                 // let every copy already issued land before the CTA exits
                 const uint32_t first = load_idx > (uint32_t)C::STAGES ? load_idx - C::STAGES : 0;
                 for (uint32_t k = first; k < load_idx; ++k)
@@ -882,10 +894,20 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
         // ------------------------------------------------------------ TMA producer
         // An item of n K/V tiles is n + 1 MMA steps: step t consumes V_{t-1} and K_t.  The
         // loads of step t go out once step t - 2 is done, which frees both their stages.
-        if (lane == 0) {
+        // Ragged K/V: lane 0 alone.  Paged K/V: the whole warp, lane l loading page l of
+        // each K/V tile (its id read one step ahead); lane 0 arms the barriers.
+        if (PAGED || lane == 0) {
+            auto wait = [&](uint32_t bar, uint32_t par) -> bool {
+                if constexpr (PAGED)
+                    return __all_sync(0xffffffffu, mbar_wait_bounded(bar, par, abort_flag, p.status));
+                else
+                    return mbar_wait_bounded(bar, par, abort_flag, p.status);
+            };
             tensormap_acquire(p.tm_q);
             tensormap_acquire(p.tm_k);
             tensormap_acquire(p.tm_v);
+            const int ps = p.page_size;
+            const int ppt = PAGED ? BN / ps : 0;
             uint32_t load_idx = 0, q_count = 0, step = 0;
             uint32_t ctr[2] = {0, 0}, items_x[2] = {0, 0};
             uint32_t done_bar[2] = {0, 0}, done_par[2] = {0, 0};  // completion of steps t, t-1
@@ -903,27 +925,32 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
                 const int nmax = max(nA, nB);
                 if (nmax == 0) continue;
                 const int lx = nB > 0 ? 1 : 0;  // tile whose MMAs close every step
-                ok = mbar_wait_bounded(BAR(Q_EMPTY), (q_count & 1) ^ 1, abort_flag, p.status);
+                ok = wait(BAR(Q_EMPTY), (q_count & 1) ^ 1);
                 if (!ok) break;
-                mbar_arrive_expect_tx(BAR(Q_FULL), C::TILE_BYTES * (nB > 0 ? 2 : 1));
-#pragma unroll
-                for (int c = 0; c < C::CHUNKS; ++c)
-                    tma_load_3d(sQ + c * C::CHUNK_BYTES, p.tm_q, BAR(Q_FULL), c * 64, w.g * G,
-                                a.q_start + a.t0);
-                if (nB > 0) {
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(BAR(Q_FULL), C::TILE_BYTES * (nB > 0 ? 2 : 1));
 #pragma unroll
                     for (int c = 0; c < C::CHUNKS; ++c)
-                        tma_load_3d(sQ + C::TILE_BYTES + c * C::CHUNK_BYTES, p.tm_q, BAR(Q_FULL),
-                                    c * 64, w.g * G, bq.q_start + bq.t0);
+                        tma_load_3d(sQ + c * C::CHUNK_BYTES, p.tm_q, BAR(Q_FULL), c * 64, w.g * G,
+                                    a.q_start + a.t0);
+                    if (nB > 0) {
+#pragma unroll
+                        for (int c = 0; c < C::CHUNKS; ++c)
+                            tma_load_3d(sQ + C::TILE_BYTES + c * C::CHUNK_BYTES, p.tm_q,
+                                        BAR(Q_FULL), c * 64, w.g * G, bq.q_start + bq.t0);
+                    }
                 }
                 ++q_count;
                 const uint32_t L0 = load_idx;
                 const int* pt_row = PAGED ? p.page_table + (size_t)w.b * p.page_table_stride : nullptr;
-                int kp[BN / 16], nkp = 0;  // page ids of the K tile of the previous step
+                const int npg = PAGED ? (a.kv_len + ps - 1) / ps : 0;
+                // paged: this lane's page of K_t (read a step ahead) and of K_{t-1} (= V_{t-1})
+                int kid = PAGED ? lane_page_id(pt_row, 0, ppt, npg, lane) : -1;
+                int vid = -1;
+                bool v_ok = false;
                 for (int t = 0; t <= nmax; ++t, ++step) {
                     if (step >= 2) {
-                        ok = mbar_wait_bounded(done_bar[step & 1], done_par[step & 1], abort_flag,
-                                               p.status);
+                        ok = wait(done_bar[step & 1], done_par[step & 1]);
                         if (!ok) break;
                     }
                     if (t < nmax) {
@@ -938,19 +965,15 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
                     const uint32_t vst = (L0 + 2 * (t - 1) + 1) % C::STAGES;
                     const uint32_t kst = (L0 + 2 * t) % C::STAGES;
                     if constexpr (PAGED) {
-                        // V_{t-1} uses the page ids read for K_{t-1} one step earlier
-                        int vp[BN / 16];
-#pragma unroll
-                        for (int i = 0; i < BN / 16; ++i) vp[i] = kp[i];
-                        const int nv = t >= 1 ? nkp : 0;
-                        nkp = t < nmax ? tile_pages(kp, p, pt_row, t, a.kv_len) : 0;
-                        mbar_arrive_expect_tx(bar, tile_page_bytes<C::CHUNKS>(vp, nv, p.page_size) +
-                                                       tile_page_bytes<C::CHUNKS>(kp, nkp, p.page_size));
-                        load_tile_pages<C::CHUNKS, C::CHUNK_BYTES>(sKV + vst * C::TILE_BYTES, p.tm_v,
-                                                                   bar, vp, nv, p.page_size, w.g * D);
-                        load_tile_pages<C::CHUNKS, C::CHUNK_BYTES>(sKV + kst * C::TILE_BYTES, p.tm_k,
-                                                                   bar, kp, nkp, p.page_size, w.g * D);
-                        if (t == nmax && nmax * BN > a.kv_len) mbar_arrive(BAR(FIX_READY));
+                        const bool k_ok =
+                            t < nmax && lane_page_ok(kid, t, ppt, npg, p.num_pages, lane, p.status);
+                        issue_page_boxes<C::CHUNKS, C::CHUNK_BYTES>(
+                            bar, ps, w.g * D, lane, t >= 1 && v_ok, sKV + vst * C::TILE_BYTES, p.tm_v,
+                            vid, k_ok, sKV + kst * C::TILE_BYTES, p.tm_k, kid);
+                        if (lane == 0 && t == nmax && nmax * BN > a.kv_len) mbar_arrive(BAR(FIX_READY));
+                        vid = kid;
+                        v_ok = k_ok;
+                        if (t + 1 < nmax) kid = lane_page_id(pt_row, t + 1, ppt, npg, lane);
                     } else {
                         mbar_arrive_expect_tx(bar, C::TILE_BYTES * ((t >= 1) + (t < nmax)));
                         if (t >= 1) {  // V_{t-1}
@@ -973,7 +996,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
                 if (nA > 0) ++items_x[0];
                 if (nB > 0) ++items_x[1];
             }
-            if (!ok) {
+            if (!ok && lane == 0) {
                 // let every copy already issued land before the CTA exits
                 for (uint32_t s = step > 2 ? step - 2 : 0; s < step; ++s)
                     mbar_wait_bounded(BAR(STEP_FULL + (s & 1)), (s >> 1) & 1, nullptr, p.status);
