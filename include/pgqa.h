@@ -155,7 +155,8 @@ int pgqa_paged_prefill_bf16(const void* q, const void* k_pages, const void* v_pa
  *   Key slots past kv_lens[b] in a request's last page are never read, so whatever
  *   they hold (even NaN) cannot reach the output.
  *
- * Supported: head_dim 128; page_size 16; G = num_qo_heads / num_kv_heads in {1,2,4,8}.
+ * Supported: head_dim 128; page_size 16, 32, 64 or 128; G = num_qo_heads / num_kv_heads in
+ * {1,2,4,8}.
  * Errors as for pgqa_ragged_prefill_bf16; a page id outside 0..num_pages-1 or a
  * kv_len outside its range is reported as PGQA_ERR_DEVICE_BOUNDS by
  * pgqa_get_device_status(), and the affected request's keys are skipped.

@@ -21,7 +21,7 @@ namespace decode {
 cudaError_t launch_plan(const PlanParams&, cudaStream_t);
 cudaError_t launch_decode(const Params&, int group, int num_sms, cudaStream_t);
 cudaError_t launch_merge(const Params&, cudaStream_t);
-cudaError_t prepare_page_maps(Params&, const void*, const void*, int, int);
+cudaError_t prepare_page_maps(Params&, const void*, const void*, int, int, int);
 }  // namespace decode
 
 namespace {
@@ -477,7 +477,9 @@ int pgqa_paged_decode_bf16(const void* q, const void* k_pages, const void* v_pag
         (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(page_table) & 3u) ||
         (reinterpret_cast<uintptr_t>(kv_lens) & 3u))
         return PGQA_ERR_INVALID_ARG;
-    if (head_dim != decode::HEAD_DIM || page_size != decode::PAGE) return PGQA_ERR_UNSUPPORTED;
+    if (head_dim != decode::HEAD_DIM) return PGQA_ERR_UNSUPPORTED;
+    if (page_size != 16 && page_size != 32 && page_size != 64 && page_size != 128)
+        return PGQA_ERR_UNSUPPORTED;
     if (num_qo_heads % num_kv_heads != 0) return PGQA_ERR_UNSUPPORTED;
     const int group = num_qo_heads / num_kv_heads;
     if (group != 1 && group != 2 && group != 4 && group != 8) return PGQA_ERR_UNSUPPORTED;
@@ -531,12 +533,13 @@ int pgqa_paged_decode_bf16(const void* q, const void* k_pages, const void* v_pag
     p.status = &hdr->status;
     p.batch = batch;
     p.page_table_stride = page_table_stride;
+    p.page_size = page_size;
     p.num_pages = num_pages;
     p.num_qo_heads = num_qo_heads;
     p.num_kv_heads = num_kv_heads;
     p.scale_log2 = sm_scale * 1.4426950408889634f;
     p.chunk_capacity = chunks;
-    if (decode::prepare_page_maps(p, k_pages, v_pages, num_pages, num_kv_heads) != cudaSuccess)
+    if (decode::prepare_page_maps(p, k_pages, v_pages, num_pages, num_kv_heads, page_size) != cudaSuccess)
         return PGQA_ERR_INVALID_ARG;
     e = decode::launch_decode(p, group, st->num_sms, s);
     if (e != cudaSuccess) return PGQA_ERR_CUDA;

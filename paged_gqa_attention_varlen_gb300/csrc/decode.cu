@@ -2,7 +2,7 @@
 // merge, for sm_103a.
 //
 // What it computes: for request b and query head h, with kv_len keys stored in an NHD
-// page table (key j in slot j % 16 of page page_table[b][j / 16]),
+// page table (key j in slot j % page_size of page page_table[b][j / page_size]),
 //   o[b,h] = softmax_j(sm_scale * q[b,h] . k[j, h/G]) v[j, h/G],
 //   lse[b,h] = ln sum_j exp(sm_scale * q[b,h] . k[j, h/G]).
 // Sources: vllm-rlt pull request "feat: add FlashInfer attention backend for SM120
@@ -105,8 +105,9 @@ __device__ __forceinline__ void transpose_reduce(float* a, int lane) {
 }
 
 // ------------------------------------------------------------ TMA-staged decode
-// One warp per (chunk, kv head) item.  The warp streams its pages with TMA (one 4 KB box
-// per page for K and one for V) into a private two-stage ring in shared memory; lane 0
+// One warp per (chunk, kv head) item.  The warp streams its keys in units of 16 tokens
+// (one page of 16, or a 16-token slice of a larger page) with TMA (one 4 KB box per unit
+// for K and one for V) into a private two-stage ring in shared memory; lane 0
 // issues the copies and refills a stage as soon as the warp has finished reading it.
 // Lane (tp, ds) = (lane / 16, lane % 16) works on head-dim elements 8*ds .. 8*ds+7 of
 // the page's tokens with parity tp: 16-byte shared-memory reads of two whole K (V) rows
@@ -178,19 +179,28 @@ __global__ void __launch_bounds__(WARPS * 32, G >= 8 ? 2 : 3)
         const int kv_len = __ldg(p.kv_eff + b);
         const int tok0 = c * CHUNK;
         const int tok1 = min(kv_len, tok0 + CHUNK);
-        const int page0 = tok0 / PAGE;
+        const int page0 = tok0 / PAGE;  // first 16-token unit of the chunk
         const int np = (tok1 - tok0 + PAGE - 1) / PAGE;
         const int* pt_row = p.page_table + (size_t)b * p.page_table_stride;
+        const int page_size = p.page_size;
+        // pool row of 16-token unit u; false if its page id is outside the pool
+        auto unit_row = [&](int u, int& row) -> bool {
+            const int tok = u * PAGE;
+            const int pid = __ldg(pt_row + tok / page_size);
+            row = pid * page_size + tok % page_size;
+            return pid >= 0 && pid < p.num_pages;
+        };
 
         auto issue = [&](int page) {  // lane 0 only
-            const int pid = __ldg(pt_row + page);
+            int row;
+            const bool valid = unit_row(page, row);
             const uint32_t st = issued % STAGES;
             const uint32_t bar = full0 + 8 * st;
-            if (pid >= 0 && pid < p.num_pages) {
+            if (valid) {
                 mbar_arrive_expect_tx(bar, STAGE_BYTES);
                 const uint32_t dst = stage0 + st * STAGE_BYTES;
-                tma_load_2d(dst, &p.tm_kpages, bar, g * D, pid * PAGE);
-                tma_load_2d(dst + PAGE_HEAD_BYTES, &p.tm_vpages, bar, g * D, pid * PAGE);
+                tma_load_2d(dst, &p.tm_kpages, bar, g * D, row);
+                tma_load_2d(dst + PAGE_HEAD_BYTES, &p.tm_vpages, bar, g * D, row);
             } else {
                 atomicOr(p.status, PGQA_DEV_BOUNDS);
                 mbar_arrive(bar);  // the page is skipped; keep the ring in phase
@@ -233,8 +243,8 @@ __global__ void __launch_bounds__(WARPS * 32, G >= 8 ? 2 : 3)
             if (!ok) break;
             ++consumed;
             const int page = page0 + pi;
-            const int pid = __ldg(pt_row + page);
-            const int nvalid = (pid >= 0 && pid < p.num_pages) ? min(PAGE, tok1 - page * PAGE) : 0;
+            int row;
+            const int nvalid = unit_row(page, row) ? min(PAGE, tok1 - page * PAGE) : 0;
             const uint32_t kbase = stage0 + st * STAGE_BYTES + ds * 16;
             const uint32_t vbase = kbase + PAGE_HEAD_BYTES;
 
@@ -440,10 +450,10 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-// Tensor maps over the paged K and V caches viewed as [num_pages * PAGE, Hk * D] bf16;
-// one box is one page of one kv head (PAGE rows x D elements, 4 KB).
+// Tensor maps over the paged K and V caches viewed as [num_pages * page_size, Hk * D]
+// bf16; one box is 16 rows of one kv head (PAGE rows x D elements, 4 KB).
 cudaError_t prepare_page_maps(Params& p, const void* k_pages, const void* v_pages,
-                              int num_pages, int num_kv_heads) {
+                              int num_pages, int num_kv_heads, int page_size) {
     static EncodeTiledFn encode = nullptr;
     if (encode == nullptr) {
         void* fn = nullptr;
@@ -455,7 +465,7 @@ cudaError_t prepare_page_maps(Params& p, const void* k_pages, const void* v_page
         encode = reinterpret_cast<EncodeTiledFn>(fn);
     }
     const cuuint64_t dims[2] = {(cuuint64_t)num_kv_heads * HEAD_DIM,
-                                (cuuint64_t)(num_pages > 0 ? num_pages : 1) * PAGE};
+                                (cuuint64_t)(num_pages > 0 ? num_pages : 1) * page_size};
     const cuuint64_t strides[1] = {(cuuint64_t)num_kv_heads * HEAD_DIM * 2};
     const cuuint32_t box[2] = {HEAD_DIM, PAGE};
     const cuuint32_t estr[2] = {1, 1};

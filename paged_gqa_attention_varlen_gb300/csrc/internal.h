@@ -104,7 +104,7 @@ struct PlanParams {
 
 // ------------------------------------------------------------------ decode
 namespace decode {
-constexpr int PAGE = 16;           // tokens per page
+constexpr int PAGE = 16;           // tokens per TMA unit (one box); pages hold 1, 2, 4 or 8
 constexpr int CHUNK = 1024;        // tokens per split-KV chunk (fixed: depends on nothing
                                    // but the request, so results do not depend on the batch)
 constexpr int HEAD_DIM = 128;
@@ -117,7 +117,7 @@ constexpr int SMEM_BYTES = 1024 + WARPS * WARP_SMEM;
 constexpr int PLAN_THREADS = 1024;
 
 struct Params {
-    CUtensorMap tm_kpages;      // [num_pages * PAGE rows, Hk * D] bf16, box one page of one head
+    CUtensorMap tm_kpages;      // [num_pages * page_size rows, Hk * D] bf16, box 16 rows of one head
     CUtensorMap tm_vpages;
     const void* q;
     const void* k_pages;
@@ -132,6 +132,7 @@ struct Params {
     int* status;
     int batch;
     int page_table_stride;
+    int page_size;              // 16, 32, 64 or 128 tokens
     int num_pages;
     int num_qo_heads;
     int num_kv_heads;

@@ -128,7 +128,9 @@ def test_decode_host_validation(api):
     assert decode(api, batch=0) == 0
     assert decode(api, batch=-3) == -1
     assert decode(api, kl=0) == -1
-    assert decode(api, ps=32) == -2
+    assert decode(api, ps=8) == -2
+    assert decode(api, ps=48) == -2
+    assert decode(api, ps=256) == -2
     assert decode(api, d=256) == -2
     assert decode(api, hq=48, hk=8) == -2                   # group 6
     assert decode(api, hq=128, hk=8) == -2                  # group 16
@@ -141,6 +143,8 @@ def test_valid_calls_without_a_gpu_report_no_device(api):
         pytest.skip("a GPU is present")
     assert prefill(api) == -7
     assert decode(api) == -7
+    for ps in (32, 64, 128):
+        assert decode(api, ps=ps) == -7
     for ps in (16, 32, 64, 128):
         assert paged_prefill(api, ps=ps) == -7
     assert paged_prefill(api, d=256) == -7

@@ -36,6 +36,31 @@ def test_decode_lengths_and_groups(cuda_lib, G):
     check_rows(o.reshape(-1, 128).float().cpu(), lse.reshape(-1).cpu(), ro, rl, f"G={G}")
 
 
+@pytest.mark.parametrize("ps", [32, 64, 128])
+def test_decode_page_sizes(cuda_lib, ps):
+    """Larger pages: each is streamed as 16-token slices of the same page."""
+    pc = W.paged_case(LENS + [5000], 32, 8, 128, page_size=ps, seed=31 + ps, device="cuda")
+    o, lse = run_gpu(cuda_lib, pc)
+    assert cuda_lib.device_status() == 0
+    ro, rl = oracle_decode(pc)
+    check_rows(o.reshape(-1, 128).float().cpu(), lse.reshape(-1).cpu(), ro, rl, f"page {ps}")
+
+
+@pytest.mark.parametrize("ps", [16, 64])
+def test_decode_and_one_row_paged_prefill_agree(cuda_lib, ps):
+    """Decode (split-KV + merge on the CUDA cores) and the one-row paged prefill (tensor
+    cores, one pass) compute the same attention: they agree within the tolerance."""
+    pc = W.paged_case([1, 700, 3000], 16, 4, 128, page_size=ps, seed=37 + ps, device="cuda")
+    o_d, l_d = run_gpu(cuda_lib, pc)
+    o_p, l_p = cuda_lib.paged_prefill(pc.q, pc.k_pages, pc.v_pages, pc.q_indptr, pc.page_table,
+                                      pc.kv_lens_t, causal=True, sm_scale=pc.sm_scale)
+    torch.cuda.synchronize()
+    assert cuda_lib.device_status() == 0
+    ro, rl = oracle_decode(pc)
+    check_rows(o_d.reshape(-1, 128).float().cpu(), l_d.reshape(-1).cpu(), ro, rl, "decode")
+    check_rows(o_p.reshape(-1, 128).float().cpu(), l_p.reshape(-1).cpu(), ro, rl, "prefill q=1")
+
+
 def test_decode_single_request_long(cuda_lib):
     pc = W.paged_case([32768], 32, 8, 128, page_size=16, seed=11, device="cuda")
     o, lse = run_gpu(cuda_lib, pc)
