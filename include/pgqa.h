@@ -167,6 +167,41 @@ int pgqa_paged_decode_bf16(const void* q, const void* k_pages, const void* v_pag
                            int batch, int num_qo_heads, int num_kv_heads, int head_dim,
                            float sm_scale, pgqa_stream_t stream);
 
+/*
+ * The paged prefill and the paged decode over K/V pools of any layout whose head_dim
+ * elements are contiguous: element [page, slot, head, c] of k_pages (and v_pages, which
+ * must have the same layout) is at
+ *     page * page_stride + slot * slot_stride + head * head_stride + c      (elements).
+ * Covers the packed NHD layout of the calls above (page_stride = page_size * Hk * d,
+ * slot_stride = Hk * d, head_stride = d), the HND layout [num_pages, Hk, page_size, d]
+ * (page_stride = Hk * page_size * d, slot_stride = d, head_stride = page_size * d), and a
+ * per-layer slice of a larger cache such as [num_pages, num_layers, page_size, Hk, d]
+ * (page_stride = num_layers * page_size * Hk * d, others as for NHD).
+ *
+ * Defined by: the calls above (same arguments, results and supported shapes); the NHD /
+ * HND kv_layout choice is FlashInfer documentation, flashinfer_benchmark.py "Attention
+ * Flags" (--kv_layout), and non-contiguous per-layer slices of the cache are inputs the
+ * vllm-rlt pull request "feat: add FlashInfer attention backend for SM120 decode" tests
+ * its decode kernel on (its GPU test suite: oracle parity on non-contiguous layer slices).
+ *
+ * Strides are in elements: positive multiples of 8 (16 bytes) and below 2^36, else
+ * PGQA_ERR_INVALID_ARG.  k_pages / v_pages must be 16-byte aligned.
+ */
+int pgqa_paged_prefill_bf16_strided(const void* q, const void* k_pages, const void* v_pages,
+                                    void* o, float* lse, const int32_t* q_indptr,
+                                    const int32_t* page_table, int page_table_stride,
+                                    const int32_t* kv_lens, int page_size, int num_pages,
+                                    int64_t page_stride, int64_t slot_stride, int64_t head_stride,
+                                    int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                                    int causal, float sm_scale, pgqa_stream_t stream);
+int pgqa_paged_decode_bf16_strided(const void* q, const void* k_pages, const void* v_pages,
+                                   const int32_t* page_table, const int32_t* kv_lens,
+                                   int page_size, int page_table_stride, int num_pages,
+                                   int64_t page_stride, int64_t slot_stride, int64_t head_stride,
+                                   void* o, float* lse, int batch, int num_qo_heads,
+                                   int num_kv_heads, int head_dim, float sm_scale,
+                                   pgqa_stream_t stream);
+
 /* Same calls under the short names used by serving integrations. */
 int ragged_prefill_bf16(const void* q, const void* k, const void* v, void* o, float* lse,
                         const int32_t* q_indptr, const int32_t* kv_indptr, int batch,

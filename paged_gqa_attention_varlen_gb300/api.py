@@ -25,6 +25,7 @@ STATUS_NAMES = {
 
 ABI_FUNCTIONS = (
     "pgqa_ragged_prefill_bf16", "pgqa_paged_prefill_bf16", "pgqa_paged_decode_bf16",
+    "pgqa_paged_prefill_bf16_strided", "pgqa_paged_decode_bf16_strided",
     "ragged_prefill_bf16", "paged_prefill_bf16", "paged_decode_bf16", "pgqa_set_workspace", "pgqa_workspace_bytes_prefill",
     "pgqa_workspace_bytes_decode", "pgqa_get_device_status", "pgqa_status_string",
     "pgqa_version", "pgqa_paged_decode_bf16_noalloc",
@@ -57,6 +58,12 @@ def _load(path: Path):
     for name in ("pgqa_paged_prefill_bf16", "paged_prefill_bf16"):
         fn = getattr(lib, name)
         fn.argtypes, fn.restype = paged_prefill_args, i
+    lib.pgqa_paged_prefill_bf16_strided.argtypes = [p, p, p, p, p, p, p, i, p, i, i, i64, i64, i64,
+                                                    i, i, i, i, i, f, p]
+    lib.pgqa_paged_prefill_bf16_strided.restype = i
+    lib.pgqa_paged_decode_bf16_strided.argtypes = [p, p, p, p, p, i, i, i, i64, i64, i64, p, p, i,
+                                                   i, i, i, f, p]
+    lib.pgqa_paged_decode_bf16_strided.restype = i
     lib.pgqa_set_workspace.argtypes, lib.pgqa_set_workspace.restype = [p, sz], i
     lib.pgqa_workspace_bytes_prefill.argtypes = [i, i64, i, i]
     lib.pgqa_workspace_bytes_prefill.restype = sz
@@ -100,6 +107,35 @@ def _check(t, name, dtype, dim=None, device=None):
         raise ValueError(f"{name} is on {t.device}, expected {device}")
 
 
+def _page_pools(k_pages, v_pages, kv_layout, dev):
+    """Shape and element strides of the K/V page pools.
+
+    kv_layout "NHD": tensors [num_pages, page_size, Hk, d]; "HND": [num_pages, Hk,
+    page_size, d].  Any strides are accepted as long as d is contiguous and K and V share
+    them (for instance a per-layer slice of a larger cache).  Returns (num_pages,
+    page_size, Hk, d, (page_stride, slot_stride, head_stride), contiguous_nhd).
+    """
+    for t, name in ((k_pages, "k_pages"), (v_pages, "v_pages")):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16:
+            raise TypeError(f"{name} must be a bfloat16 torch.Tensor")
+        if not t.is_cuda or t.device != dev:
+            raise ValueError(f"{name} must be a CUDA tensor on {dev}")
+        if t.dim() != 4 or t.stride(-1) != 1:
+            raise ValueError(f"{name} must be 4-D with a contiguous last (head_dim) axis")
+    if k_pages.shape != v_pages.shape or k_pages.stride() != v_pages.stride():
+        raise ValueError("k_pages and v_pages must have the same shape and strides")
+    if kv_layout == "NHD":
+        num_pages, page_size, hk, d = k_pages.shape
+        page_s, slot_s, head_s, _ = k_pages.stride()
+    elif kv_layout == "HND":
+        num_pages, hk, page_size, d = k_pages.shape
+        page_s, head_s, slot_s, _ = k_pages.stride()
+    else:
+        raise ValueError(f"kv_layout must be 'NHD' or 'HND', got {kv_layout!r}")
+    contiguous_nhd = kv_layout == "NHD" and k_pages.is_contiguous() and v_pages.is_contiguous()
+    return num_pages, page_size, hk, d, (page_s, slot_s, head_s), contiguous_nhd
+
+
 def ragged_prefill(q, k, v, q_indptr, kv_indptr, causal=True, sm_scale=None, out=None,
                    lse=None, return_lse=True, stream=None):
     """Ragged batched prefill (pgqa_ragged_prefill_bf16).
@@ -137,26 +173,26 @@ def ragged_prefill(q, k, v, q_indptr, kv_indptr, causal=True, sm_scale=None, out
 
 
 def paged_prefill(q, k_pages, v_pages, q_indptr, page_table, kv_lens, causal=True, sm_scale=None,
-                  out=None, lse=None, return_lse=True, stream=None):
-    """Paged prefill / append (pgqa_paged_prefill_bf16).
+                  out=None, lse=None, return_lse=True, stream=None, kv_layout="NHD"):
+    """Paged prefill / append (pgqa_paged_prefill_bf16, or the _strided call for HND or
+    non-contiguous page pools).
 
     q [total_q, Hq, d] bf16 with q_indptr [batch + 1] int32; k_pages / v_pages
-    [num_pages, page_size, Hk, d] bf16; page_table [batch, stride] int32; kv_lens [batch]
-    int32 (keys per request, the cached prefix plus the new tokens); all on one CUDA device.
-    Returns (o [total_q, Hq, d] bf16, lse [total_q, Hq] fp32 or None).
+    [num_pages, page_size, Hk, d] (kv_layout "NHD") or [num_pages, Hk, page_size, d]
+    ("HND") bf16, any strides with d contiguous; page_table [batch, stride] int32; kv_lens
+    [batch] int32 (keys per request, the cached prefix plus the new tokens); all on one
+    CUDA device.  Returns (o [total_q, Hq, d] bf16, lse [total_q, Hq] fp32 or None).
     """
     dev = q.device
     _check(q, "q", torch.bfloat16, 3, dev)
-    _check(k_pages, "k_pages", torch.bfloat16, 4, dev)
-    _check(v_pages, "v_pages", torch.bfloat16, 4, dev)
     _check(q_indptr, "q_indptr", torch.int32, 1, dev)
     _check(page_table, "page_table", torch.int32, 2, dev)
     _check(kv_lens, "kv_lens", torch.int32, 1, dev)
     total_q, hq, d = q.shape
-    num_pages, page_size, hk, dk = k_pages.shape
+    num_pages, page_size, hk, dk, strides, packed = _page_pools(k_pages, v_pages, kv_layout, dev)
     batch = q_indptr.numel() - 1
-    if v_pages.shape != k_pages.shape or dk != d:
-        raise ValueError("k_pages / v_pages must be [num_pages, page_size, Hk, d]")
+    if dk != d:
+        raise ValueError("k_pages / v_pages must have q's head_dim")
     if page_table.shape[0] != batch or kv_lens.numel() != batch:
         raise ValueError("page_table / kv_lens must have one row per request")
     if sm_scale is None:
@@ -168,33 +204,40 @@ def paged_prefill(q, k_pages, v_pages, q_indptr, page_table, kv_lens, causal=Tru
         lse = torch.empty((total_q, hq), dtype=torch.float32, device=dev)
     if lse is not None:
         _check(lse, "lse", torch.float32, 2, dev)
-    rc = lib.pgqa_paged_prefill_bf16(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(out), _ptr(lse),
-                                     _ptr(q_indptr), _ptr(page_table), page_table.shape[1],
-                                     _ptr(kv_lens), page_size, num_pages, batch, hq, hk, d,
-                                     int(bool(causal)), float(sm_scale), _stream(stream))
+    if packed:
+        rc = lib.pgqa_paged_prefill_bf16(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(out),
+                                         _ptr(lse), _ptr(q_indptr), _ptr(page_table),
+                                         page_table.shape[1], _ptr(kv_lens), page_size, num_pages,
+                                         batch, hq, hk, d, int(bool(causal)), float(sm_scale),
+                                         _stream(stream))
+    else:
+        rc = lib.pgqa_paged_prefill_bf16_strided(
+            _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(out), _ptr(lse), _ptr(q_indptr),
+            _ptr(page_table), page_table.shape[1], _ptr(kv_lens), page_size, num_pages, *strides,
+            batch, hq, hk, d, int(bool(causal)), float(sm_scale), _stream(stream))
     if rc != PGQA_OK:
         raise PgqaError(rc, "pgqa_paged_prefill_bf16")
     return out, lse
 
 
 def paged_decode(q, k_pages, v_pages, page_table, kv_lens, sm_scale=None, out=None, lse=None,
-                 return_lse=True, stream=None):
-    """Paged decode (pgqa_paged_decode_bf16).
+                 return_lse=True, stream=None, kv_layout="NHD"):
+    """Paged decode (pgqa_paged_decode_bf16, or the _strided call for HND or non-contiguous
+    page pools).
 
-    q [batch, Hq, d]; k_pages / v_pages [num_pages, page_size, Hk, d] bf16;
-    page_table [batch, stride] int32; kv_lens [batch] int32; all on one CUDA device.
+    q [batch, Hq, d]; k_pages / v_pages [num_pages, page_size, Hk, d] ("NHD") or
+    [num_pages, Hk, page_size, d] ("HND") bf16, any strides with d contiguous; page_table
+    [batch, stride] int32; kv_lens [batch] int32; all on one CUDA device.
     Returns (o [batch, Hq, d] bf16, lse [batch, Hq] fp32 or None).
     """
     dev = q.device
     _check(q, "q", torch.bfloat16, 3, dev)
-    _check(k_pages, "k_pages", torch.bfloat16, 4, dev)
-    _check(v_pages, "v_pages", torch.bfloat16, 4, dev)
     _check(page_table, "page_table", torch.int32, 2, dev)
     _check(kv_lens, "kv_lens", torch.int32, 1, dev)
     batch, hq, d = q.shape
-    num_pages, page_size, hk, dk = k_pages.shape
-    if v_pages.shape != k_pages.shape or dk != d:
-        raise ValueError("k_pages / v_pages must be [num_pages, page_size, Hk, d]")
+    num_pages, page_size, hk, dk, strides, packed = _page_pools(k_pages, v_pages, kv_layout, dev)
+    if dk != d:
+        raise ValueError("k_pages / v_pages must have q's head_dim")
     if page_table.shape[0] != batch or kv_lens.numel() != batch:
         raise ValueError("page_table / kv_lens must have one row per request")
     if sm_scale is None:
@@ -206,10 +249,16 @@ def paged_decode(q, k_pages, v_pages, page_table, kv_lens, sm_scale=None, out=No
         lse = torch.empty((batch, hq), dtype=torch.float32, device=dev)
     if lse is not None:
         _check(lse, "lse", torch.float32, 2, dev)
-    rc = lib.pgqa_paged_decode_bf16(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table),
-                                    _ptr(kv_lens), page_size, page_table.shape[1], num_pages,
-                                    _ptr(out), _ptr(lse), batch, hq, hk, d, float(sm_scale),
-                                    _stream(stream))
+    if packed:
+        rc = lib.pgqa_paged_decode_bf16(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table),
+                                        _ptr(kv_lens), page_size, page_table.shape[1], num_pages,
+                                        _ptr(out), _ptr(lse), batch, hq, hk, d, float(sm_scale),
+                                        _stream(stream))
+    else:
+        rc = lib.pgqa_paged_decode_bf16_strided(
+            _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table), _ptr(kv_lens), page_size,
+            page_table.shape[1], num_pages, *strides, _ptr(out), _ptr(lse), batch, hq, hk, d,
+            float(sm_scale), _stream(stream))
     if rc != PGQA_OK:
         raise PgqaError(rc, "pgqa_paged_decode_bf16")
     return out, lse

@@ -21,7 +21,8 @@ namespace decode {
 cudaError_t launch_plan(const PlanParams&, cudaStream_t);
 cudaError_t launch_decode(const Params&, int group, int num_sms, cudaStream_t);
 cudaError_t launch_merge(const Params&, cudaStream_t);
-cudaError_t prepare_page_maps(Params&, const void*, const void*, int, int, int);
+cudaError_t prepare_page_maps(Params&, const void*, const void*, int, int, int, long long,
+                              long long, long long);
 }  // namespace decode
 
 namespace {
@@ -144,6 +145,33 @@ int encode_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? PGQA_OK : PGQA_ERR_INVALID_ARG;
+}
+
+// 4-D {d, slot, head, page} view of a page pool (element strides, d contiguous), box of
+// 64 columns x page_size slots of one head, 128-byte swizzle (the prefill's stage layout).
+int encode_pages_4d(CUtensorMap* map, const void* base, int d, int page_size, int heads,
+                    int num_pages, long long page_stride, long long slot_stride,
+                    long long head_stride) {
+    const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)page_size, (cuuint64_t)heads,
+                                (cuuint64_t)(num_pages > 0 ? num_pages : 1)};
+    const cuuint64_t strides[3] = {(cuuint64_t)slot_stride * 2, (cuuint64_t)head_stride * 2,
+                                   (cuuint64_t)page_stride * 2};
+    const cuuint32_t box[4] = {64, (cuuint32_t)page_size, 1, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PGQA_OK : PGQA_ERR_INVALID_ARG;
+}
+
+// Element strides of a page pool: positive multiples of 8 elements (16 bytes, the TMA
+// rule for global strides) and below 2^36 elements.
+bool kv_strides_ok(long long page_stride, long long slot_stride, long long head_stride) {
+    const long long lim = 1LL << 36;
+    for (long long x : {page_stride, slot_stride, head_stride})
+        if (x <= 0 || (x & 7) || x >= lim) return false;
+    return true;
 }
 
 size_t prefill_ws_bytes(int batch, long long max_items) {
@@ -356,8 +384,24 @@ int pgqa_paged_prefill_bf16(const void* q, const void* k_pages, const void* v_pa
                             int page_table_stride, const int32_t* kv_lens, int page_size,
                             int num_pages, int batch, int num_qo_heads, int num_kv_heads,
                             int head_dim, int causal, float sm_scale, pgqa_stream_t stream) {
+    const long long hd = (long long)num_kv_heads * head_dim;
+    return pgqa_paged_prefill_bf16_strided(q, k_pages, v_pages, o, lse, q_indptr, page_table,
+                                           page_table_stride, kv_lens, page_size, num_pages,
+                                           hd * page_size, hd, head_dim, batch, num_qo_heads,
+                                           num_kv_heads, head_dim, causal, sm_scale, stream);
+}
+
+int pgqa_paged_prefill_bf16_strided(const void* q, const void* k_pages, const void* v_pages,
+                                    void* o, float* lse, const int32_t* q_indptr,
+                                    const int32_t* page_table, int page_table_stride,
+                                    const int32_t* kv_lens, int page_size, int num_pages,
+                                    int64_t page_stride, int64_t slot_stride, int64_t head_stride,
+                                    int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                                    int causal, float sm_scale, pgqa_stream_t stream) {
     if (batch < 0 || num_qo_heads <= 0 || num_kv_heads <= 0 || page_table_stride < 0 ||
         num_pages < 0)
+        return PGQA_ERR_INVALID_ARG;
+    if (batch > 0 && !kv_strides_ok(page_stride, slot_stride, head_stride))
         return PGQA_ERR_INVALID_ARG;
     if (batch == 0) return PGQA_OK;
     if (!q || !k_pages || !v_pages || !o || !q_indptr || !kv_lens ||
@@ -376,9 +420,7 @@ int pgqa_paged_prefill_bf16(const void* q, const void* k_pages, const void* v_pa
     if (group > prefill::BM || prefill::BM % group != 0) return PGQA_ERR_UNSUPPORTED;
     if (!(sm_scale == sm_scale) || sm_scale > 3.0e38f || sm_scale < -3.0e38f)
         return PGQA_ERR_INVALID_ARG;
-    if ((long long)page_table_stride * page_size > 0x7fffffffLL ||
-        (long long)num_pages * page_size > 0x7fffffffLL)
-        return PGQA_ERR_UNSUPPORTED;
+    if ((long long)page_table_stride * page_size > 0x7fffffffLL) return PGQA_ERR_UNSUPPORTED;
 
     std::lock_guard<std::mutex> lock(g_mutex);
     int dev;
@@ -403,19 +445,18 @@ int pgqa_paged_prefill_bf16(const void* q, const void* k_pages, const void* v_pa
     const long long capacity =
         (long long)((st->ws_bytes - items_off) / sizeof(prefill::WorkItem));
 
-    // Q as for the ragged call (row extent patched on the device); K/V over the page pool
-    // [num_pages * page_size rows, Hk * d], one box = one page of one 64-column chunk.
+    // Q as for the ragged call (row extent patched on the device); K/V as 4-D page pools
+    // {d, slot, head, page}, one box = one page of one head and one 64-column chunk.
     CUtensorMap tq, tk, tv;
     const uint32_t tpt = prefill::BM / group;
-    const uint64_t pool_rows = (uint64_t)(num_pages > 0 ? num_pages : 1) * page_size;
     if ((rc = encode_3d(&tq, q, head_dim, num_qo_heads, tpt, (uint64_t)head_dim * 2,
                         (uint64_t)num_qo_heads * head_dim * 2, 64, group, tpt)) != PGQA_OK)
         return rc;
-    if ((rc = encode_2d(&tk, k_pages, (uint64_t)num_kv_heads * head_dim, pool_rows,
-                        (uint64_t)num_kv_heads * head_dim * 2, 64, page_size)) != PGQA_OK)
+    if ((rc = encode_pages_4d(&tk, k_pages, head_dim, page_size, num_kv_heads, num_pages,
+                              page_stride, slot_stride, head_stride)) != PGQA_OK)
         return rc;
-    if ((rc = encode_2d(&tv, v_pages, (uint64_t)num_kv_heads * head_dim, pool_rows,
-                        (uint64_t)num_kv_heads * head_dim * 2, 64, page_size)) != PGQA_OK)
+    if ((rc = encode_pages_4d(&tv, v_pages, head_dim, page_size, num_kv_heads, num_pages,
+                              page_stride, slot_stride, head_stride)) != PGQA_OK)
         return rc;
 
     prefill::PlanParams pp;
@@ -467,8 +508,24 @@ int pgqa_paged_decode_bf16(const void* q, const void* k_pages, const void* v_pag
                            int page_table_stride, int num_pages, void* o, float* lse,
                            int batch, int num_qo_heads, int num_kv_heads, int head_dim,
                            float sm_scale, pgqa_stream_t stream) {
+    const long long hd = (long long)num_kv_heads * head_dim;
+    return pgqa_paged_decode_bf16_strided(q, k_pages, v_pages, page_table, kv_lens, page_size,
+                                          page_table_stride, num_pages, hd * page_size, hd,
+                                          head_dim, o, lse, batch, num_qo_heads, num_kv_heads,
+                                          head_dim, sm_scale, stream);
+}
+
+int pgqa_paged_decode_bf16_strided(const void* q, const void* k_pages, const void* v_pages,
+                                   const int32_t* page_table, const int32_t* kv_lens,
+                                   int page_size, int page_table_stride, int num_pages,
+                                   int64_t page_stride, int64_t slot_stride, int64_t head_stride,
+                                   void* o, float* lse, int batch, int num_qo_heads,
+                                   int num_kv_heads, int head_dim, float sm_scale,
+                                   pgqa_stream_t stream) {
     if (batch < 0 || num_qo_heads <= 0 || num_kv_heads <= 0 || page_table_stride < 0 ||
         num_pages < 0)
+        return PGQA_ERR_INVALID_ARG;
+    if (batch > 0 && !kv_strides_ok(page_stride, slot_stride, head_stride))
         return PGQA_ERR_INVALID_ARG;
     if (batch == 0) return PGQA_OK;
     if (!q || !k_pages || !v_pages || !o || !kv_lens || (!page_table && page_table_stride > 0))
@@ -539,7 +596,8 @@ int pgqa_paged_decode_bf16(const void* q, const void* k_pages, const void* v_pag
     p.num_kv_heads = num_kv_heads;
     p.scale_log2 = sm_scale * 1.4426950408889634f;
     p.chunk_capacity = chunks;
-    if (decode::prepare_page_maps(p, k_pages, v_pages, num_pages, num_kv_heads, page_size) != cudaSuccess)
+    if (decode::prepare_page_maps(p, k_pages, v_pages, num_pages, num_kv_heads, page_size,
+                                  page_stride, slot_stride, head_stride) != cudaSuccess)
         return PGQA_ERR_INVALID_ARG;
     e = decode::launch_decode(p, group, st->num_sms, s);
     if (e != cudaSuccess) return PGQA_ERR_CUDA;

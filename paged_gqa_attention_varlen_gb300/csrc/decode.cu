@@ -183,24 +183,24 @@ __global__ void __launch_bounds__(WARPS * 32, G >= 8 ? 2 : 3)
         const int np = (tok1 - tok0 + PAGE - 1) / PAGE;
         const int* pt_row = p.page_table + (size_t)b * p.page_table_stride;
         const int page_size = p.page_size;
-        // pool row of 16-token unit u; false if its page id is outside the pool
-        auto unit_row = [&](int u, int& row) -> bool {
+        // page id and first slot of 16-token unit u; false if the id is outside the pool
+        auto unit_row = [&](int u, int& pid, int& slot) -> bool {
             const int tok = u * PAGE;
-            const int pid = __ldg(pt_row + tok / page_size);
-            row = pid * page_size + tok % page_size;
+            pid = __ldg(pt_row + tok / page_size);
+            slot = tok % page_size;
             return pid >= 0 && pid < p.num_pages;
         };
 
         auto issue = [&](int page) {  // lane 0 only
-            int row;
-            const bool valid = unit_row(page, row);
+            int pid, slot;
+            const bool valid = unit_row(page, pid, slot);
             const uint32_t st = issued % STAGES;
             const uint32_t bar = full0 + 8 * st;
             if (valid) {
                 mbar_arrive_expect_tx(bar, STAGE_BYTES);
                 const uint32_t dst = stage0 + st * STAGE_BYTES;
-                tma_load_2d(dst, &p.tm_kpages, bar, g * D, row);
-                tma_load_2d(dst + PAGE_HEAD_BYTES, &p.tm_vpages, bar, g * D, row);
+                tma_load_4d(dst, &p.tm_kpages, bar, 0, slot, g, pid);
+                tma_load_4d(dst + PAGE_HEAD_BYTES, &p.tm_vpages, bar, 0, slot, g, pid);
             } else {
                 atomicOr(p.status, PGQA_DEV_BOUNDS);
                 mbar_arrive(bar);  // the page is skipped; keep the ring in phase
@@ -243,8 +243,8 @@ __global__ void __launch_bounds__(WARPS * 32, G >= 8 ? 2 : 3)
             if (!ok) break;
             ++consumed;
             const int page = page0 + pi;
-            int row;
-            const int nvalid = unit_row(page, row) ? min(PAGE, tok1 - page * PAGE) : 0;
+            int pid, slot;
+            const int nvalid = unit_row(page, pid, slot) ? min(PAGE, tok1 - page * PAGE) : 0;
             const uint32_t kbase = stage0 + st * STAGE_BYTES + ds * 16;
             const uint32_t vbase = kbase + PAGE_HEAD_BYTES;
 
@@ -450,10 +450,13 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-// Tensor maps over the paged K and V caches viewed as [num_pages * page_size, Hk * D]
-// bf16; one box is 16 rows of one kv head (PAGE rows x D elements, 4 KB).
+// Tensor maps over the paged K and V caches as 4-D tensors {d, slot, head, page} with
+// element strides slot_stride / head_stride / page_stride (d contiguous); one box is 16
+// slots of one kv head (PAGE rows x D elements, 4 KB).
 cudaError_t prepare_page_maps(Params& p, const void* k_pages, const void* v_pages,
-                              int num_pages, int num_kv_heads, int page_size) {
+                              int num_pages, int num_kv_heads, int page_size,
+                              long long page_stride, long long slot_stride,
+                              long long head_stride) {
     static EncodeTiledFn encode = nullptr;
     if (encode == nullptr) {
         void* fn = nullptr;
@@ -464,15 +467,16 @@ cudaError_t prepare_page_maps(Params& p, const void* k_pages, const void* v_page
             return e != cudaSuccess ? e : cudaErrorNotSupported;
         encode = reinterpret_cast<EncodeTiledFn>(fn);
     }
-    const cuuint64_t dims[2] = {(cuuint64_t)num_kv_heads * HEAD_DIM,
-                                (cuuint64_t)(num_pages > 0 ? num_pages : 1) * page_size};
-    const cuuint64_t strides[1] = {(cuuint64_t)num_kv_heads * HEAD_DIM * 2};
-    const cuuint32_t box[2] = {HEAD_DIM, PAGE};
-    const cuuint32_t estr[2] = {1, 1};
+    const cuuint64_t dims[4] = {(cuuint64_t)HEAD_DIM, (cuuint64_t)page_size,
+                                (cuuint64_t)num_kv_heads, (cuuint64_t)(num_pages > 0 ? num_pages : 1)};
+    const cuuint64_t strides[3] = {(cuuint64_t)slot_stride * 2, (cuuint64_t)head_stride * 2,
+                                   (cuuint64_t)page_stride * 2};
+    const cuuint32_t box[4] = {HEAD_DIM, PAGE, 1, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
     CUtensorMap* maps[2] = {&p.tm_kpages, &p.tm_vpages};
     const void* bases[2] = {k_pages, v_pages};
     for (int i = 0; i < 2; ++i) {
-        CUresult r = encode(maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(bases[i]),
+        CUresult r = encode(maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(bases[i]),
                             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

@@ -75,8 +75,9 @@ struct Params {
     int causal;
     float scale_log2;          // sm_scale * log2(e)
     // paged K/V (paged kernels only): key j of request b is slot j % page_size of page
-    // page_table[b * page_table_stride + j / page_size]; the K/V maps view the page pool
-    // as [num_pages * page_size rows, Hk * D] with a box of one page (page_size rows)
+    // page_table[b * page_table_stride + j / page_size]; the K/V maps view each page pool
+    // as a 4-D tensor {d, slot, head, page} (caller strides) with a box of one page of
+    // one head and 64 columns (page_size rows)
     const int* page_table;
     int page_table_stride;
     int page_size;             // 16, 32, 64 or 128
@@ -117,7 +118,9 @@ constexpr int SMEM_BYTES = 1024 + WARPS * WARP_SMEM;
 constexpr int PLAN_THREADS = 1024;
 
 struct Params {
-    CUtensorMap tm_kpages;      // [num_pages * page_size rows, Hk * D] bf16, box 16 rows of one head
+    // K / V page pools as 4-D tensors {d, slot, head, page} with the caller's strides
+    // (NHD, HND or a slice of a larger cache); one box is 16 slots of one head (4 KB)
+    CUtensorMap tm_kpages;
     CUtensorMap tm_vpages;
     const void* q;
     const void* k_pages;

@@ -332,11 +332,11 @@ __device__ __forceinline__ bool lane_page_ok(int id, int j, int ppt, int npg, in
     return ok;
 }
 // Warp-collective: arm `bar` with the bytes of every valid page box of this load (lane 0),
-// then each lane issues the boxes of its own page(s): one box per 64-column chunk, landing
-// at rows lane * ps .. of every chunk of the stage, the layout a single 128-row box would
-// have written.
+// then each lane issues the boxes of its own page(s) of kv head g: one box per 64-column
+// chunk, landing at rows lane * ps .. of every chunk of the stage, the layout a single
+// 128-row box would have written.  The maps are 4-D {d, slot, head, page}.
 template <int CHUNKS, int CHUNK_BYTES>
-__device__ __forceinline__ void issue_page_boxes(uint32_t bar, int ps, int col0, int lane,
+__device__ __forceinline__ void issue_page_boxes(uint32_t bar, int ps, int g, int lane,
                                                  bool v_ok, uint32_t v_dst, const CUtensorMap* tm_v,
                                                  int v_id, bool k_ok, uint32_t k_dst,
                                                  const CUtensorMap* tm_k, int k_id) {
@@ -348,12 +348,12 @@ __device__ __forceinline__ void issue_page_boxes(uint32_t bar, int ps, int col0,
     if (v_ok) {
 #pragma unroll
         for (int c = 0; c < CHUNKS; ++c)
-            tma_load_2d(v_dst + c * CHUNK_BYTES + row_off, tm_v, bar, col0 + c * 64, v_id * ps);
+            tma_load_4d(v_dst + c * CHUNK_BYTES + row_off, tm_v, bar, c * 64, 0, g, v_id);
     }
     if (k_ok) {
 #pragma unroll
         for (int c = 0; c < CHUNKS; ++c)
-            tma_load_2d(k_dst + c * CHUNK_BYTES + row_off, tm_k, bar, col0 + c * 64, k_id * ps);
+            tma_load_4d(k_dst + c * CHUNK_BYTES + row_off, tm_k, bar, c * 64, 0, g, k_id);
     }
 }
 
@@ -521,7 +521,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
                     if constexpr (PAGED) {
                         const bool pg_ok = lane_page_ok(pid, j, ppt, npg, p.num_pages, lane, p.status);
                         issue_page_boxes<C::CHUNKS, C::CHUNK_BYTES>(
-                            BAR(KV_FULL + st), ps, w.g * D, lane, false, 0, tm, 0, pg_ok,
+                            BAR(KV_FULL + st), ps, w.g, lane, false, 0, tm, 0, pg_ok,
                             sKV + st * C::TILE_BYTES, tm, pid);
                         if (lane == 0 && s == nl - 1 && x.n_tiles * BN > x.kv_len)
                             mbar_arrive(BAR(FIX_READY));
@@ -968,7 +968,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
                         const bool k_ok =
                             t < nmax && lane_page_ok(kid, t, ppt, npg, p.num_pages, lane, p.status);
                         issue_page_boxes<C::CHUNKS, C::CHUNK_BYTES>(
-                            bar, ps, w.g * D, lane, t >= 1 && v_ok, sKV + vst * C::TILE_BYTES, p.tm_v,
+                            bar, ps, w.g, lane, t >= 1 && v_ok, sKV + vst * C::TILE_BYTES, p.tm_v,
                             vid, k_ok, sKV + kst * C::TILE_BYTES, p.tm_k, kid);
                         if (lane == 0 && t == nmax && nmax * BN > a.kv_len) mbar_arrive(BAR(FIX_READY));
                         vid = kid;

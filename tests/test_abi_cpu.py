@@ -112,6 +112,34 @@ def test_paged_prefill_host_validation(api):
     assert paged_prefill(api, stride=1 << 28, ps=128) == -2  # keys per request overflow int32
 
 
+def test_strided_page_pool_validation(api):
+    p = ctypes.c_void_p
+    lib = api.lib
+
+    def pf(page_s, slot_s, head_s, batch=2):
+        return lib.pgqa_paged_prefill_bf16_strided(p(A), p(A), p(A), p(A), p(A), p(A), p(A), 8,
+                                                   p(A), 16, 100, page_s, slot_s, head_s, batch,
+                                                   8, 2, 128, 1, 0.1, None)
+
+    def dc(page_s, slot_s, head_s, batch=2):
+        return lib.pgqa_paged_decode_bf16_strided(p(A), p(A), p(A), p(A), p(A), 16, 8, 100,
+                                                  page_s, slot_s, head_s, p(A), p(A), batch, 8, 2,
+                                                  128, 0.1, None)
+
+    nhd = (16 * 2 * 128, 2 * 128, 128)
+    hnd = (2 * 16 * 128, 128, 16 * 128)
+    for fn in (pf, dc):
+        assert fn(*nhd, batch=0) == 0
+        assert fn(0, 256, 128) == -1                # zero stride
+        assert fn(4096, 256, 4) == -1               # not a multiple of 8 elements
+        assert fn(-4096, 256, 128) == -1
+        assert fn(1 << 36, 256, 128) == -1
+    import torch
+    if not torch.cuda.is_available():
+        for fn in (pf, dc):
+            assert fn(*nhd) == -7 and fn(*hnd) == -7
+
+
 def test_prefill_host_validation(api):
     assert prefill(api, batch=0) == 0                       # empty batch: early return
     assert prefill(api, batch=-1) == -1
