@@ -17,6 +17,10 @@ Functions
                        backend for SM120 decode", Design notes).
   merge_states      -- merge of partial (V, LSE) states (FlashInfer documentation,
                        flashinfer.cascade, "Merge Attention States").
+  paged_attention_e4m3 -- paged attention over a KV cache stored as FP8 E4M3 with one
+                       scale per tensor (FlashInfer documentation, flashinfer_benchmark.py
+                       "Attention Flags", --kv_dtype fp8_e4m3).
+  e4m3_decode       -- the E4M3 byte decoder the previous function uses.
 """
 from __future__ import annotations
 
@@ -67,6 +71,11 @@ def _load():
         lib.pgqa_oracle_paged.restype = i
         lib.pgqa_oracle_merge_states.argtypes = [p, p, i, lng, i, p, p]
         lib.pgqa_oracle_merge_states.restype = None
+        lib.pgqa_oracle_paged_e4m3.argtypes = [p, p, p, p, d, d, p, i, p, i, lng, i, i, i, i, i,
+                                               d, p, lng, p, p, i]
+        lib.pgqa_oracle_paged_e4m3.restype = i
+        lib.pgqa_oracle_e4m3_decode.argtypes = [p, lng, p]
+        lib.pgqa_oracle_e4m3_decode.restype = None
         lib.pgqa_oracle_threads.argtypes = []
         lib.pgqa_oracle_threads.restype = i
         _LIB = lib
@@ -143,6 +152,52 @@ def paged_attention(q, q_indptr, k_pages, v_pages, page_table, kv_lens, num_qo_h
                                    _ptr(kl), page_size, num_pages, batch, num_qo_heads,
                                    num_kv_heads, d, int(bool(causal)), float(sm_scale),
                                    _ptr(rows), len(rows), _ptr(o), _ptr(lse), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return o, lse
+
+
+def _u8(x) -> np.ndarray:
+    """Raw bytes of a uint8 / float8 torch tensor (any device) or a uint8 array."""
+    if isinstance(x, np.ndarray):
+        if x.dtype != np.uint8:
+            raise TypeError("numpy inputs must be uint8 bytes")
+        return np.ascontiguousarray(x)
+    import torch
+    if x.element_size() != 1:
+        raise TypeError(f"expected a one-byte dtype, got {x.dtype}")
+    return np.ascontiguousarray(x.detach().cpu().contiguous().view(torch.uint8).numpy())
+
+
+def e4m3_decode(x) -> np.ndarray:
+    """Values (float64) of E4M3 bytes."""
+    b = _u8(x)
+    out = np.empty(b.shape, dtype=np.float64)
+    _load().pgqa_oracle_e4m3_decode(_ptr(b), b.size, _ptr(out))
+    return out
+
+
+def paged_attention_e4m3(q, q_indptr, k_pages, v_pages, k_scale, v_scale, page_table, kv_lens,
+                         num_qo_heads, num_kv_heads, causal, sm_scale, rows=None,
+                         nthreads: int = 0):
+    """Float64 attention through a page table over E4M3 K/V bytes (element = e4m3 value x
+    k_scale / v_scale); returns (o [n, d], lse [n])."""
+    qb, kb, vb = _bf16_bits(q), _u8(k_pages), _u8(v_pages)
+    qi, pt, kl = _i32(q_indptr), _i32(page_table), _i32(kv_lens)
+    batch = len(kl)
+    num_pages, page_size = kb.shape[0], kb.shape[1]
+    d = kb.shape[-1]
+    stride = pt.shape[1] if pt.ndim == 2 else 0
+    if rows is None:
+        rows = all_rows(qb.shape[0], num_qo_heads)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    o = np.empty((len(rows), d), dtype=np.float64)
+    lse = np.empty(len(rows), dtype=np.float64)
+    rc = _load().pgqa_oracle_paged_e4m3(_ptr(qb), _ptr(qi), _ptr(kb), _ptr(vb), float(k_scale),
+                                        float(v_scale), _ptr(pt), stride, _ptr(kl), page_size,
+                                        num_pages, batch, num_qo_heads, num_kv_heads, d,
+                                        int(bool(causal)), float(sm_scale), _ptr(rows), len(rows),
+                                        _ptr(o), _ptr(lse), int(nthreads))
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
     return o, lse

@@ -233,6 +233,123 @@ int pgqa_oracle_paged(const uint16_t* q, const int32_t* q_indptr, const uint16_t
 }
 
 /*
+ * OCP 8-bit floating point E4M3 in its "fn" form (no infinities), decoded from the
+ * format's definition: 1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits.
+ *   exponent 1..15: (-1)^s * 2^(e-7) * (1 + m/8)      (largest finite: 2^8 * 1.75 = 448)
+ *   exponent 0:     (-1)^s * 2^(1-7) * (m/8)           (subnormals; m = 0 is a signed zero)
+ *   S.1111.111:     NaN
+ * The KV-cache dtype fp8_e4m3 is listed by FlashInfer documentation,
+ * flashinfer_benchmark.py "Attention Flags" (--kv_dtype).
+ */
+static double e4m3_to_double(uint8_t bits) {
+    const int sign = bits >> 7;
+    const int e = (bits >> 3) & 15;
+    const int m = bits & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m / 8.0, 1 - 7);
+    else v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* decode n E4M3 bytes */
+void pgqa_oracle_e4m3_decode(const uint8_t* in, long n, double* out) {
+    for (long i = 0; i < n; ++i) out[i] = e4m3_to_double(in[i]);
+}
+
+/*
+ * Softmax attention of one query row over n keys stored as E4M3 bytes with one scale for
+ * all keys and one for all values: key element = e4m3 * k_scale, value element =
+ * e4m3 * v_scale.  krows[j] / vrows[j] point at the d bytes of key / value j.
+ */
+static void attend_row_e4m3(const uint16_t* qrow, const uint8_t* const* krows,
+                            const uint8_t* const* vrows, long n, int d, double k_scale,
+                            double v_scale, double sm_scale, double* s, double* o, double* lse) {
+    int c;
+    long j;
+    if (n <= 0) {
+        for (c = 0; c < d; ++c) o[c] = 0.0;
+        *lse = -INFINITY;
+        return;
+    }
+    double m = -INFINITY;
+    for (j = 0; j < n; ++j) {
+        double dot = 0.0;
+        for (c = 0; c < d; ++c)
+            dot += bf16_to_double(qrow[c]) * (e4m3_to_double(krows[j][c]) * k_scale);
+        s[j] = sm_scale * dot;
+        if (s[j] > m) m = s[j];
+    }
+    double z = 0.0;
+    for (j = 0; j < n; ++j) {
+        s[j] = exp(s[j] - m);
+        z += s[j];
+    }
+    for (c = 0; c < d; ++c) o[c] = 0.0;
+    for (j = 0; j < n; ++j) {
+        double w = s[j] / z;
+        for (c = 0; c < d; ++c) o[c] += w * (e4m3_to_double(vrows[j][c]) * v_scale);
+    }
+    *lse = m + log(z);
+}
+
+/*
+ * Attention over a paged NHD KV cache held as E4M3 bytes with per-tensor scales
+ * (k_scale for every key element, v_scale for every value element).  Arguments as for
+ * pgqa_oracle_paged, with k_pages / v_pages holding one byte per element.
+ */
+int pgqa_oracle_paged_e4m3(const uint16_t* q, const int32_t* q_indptr, const uint8_t* k_pages,
+                           const uint8_t* v_pages, double k_scale, double v_scale,
+                           const int32_t* page_table, int page_table_stride,
+                           const int32_t* kv_lens, int page_size, long num_pages, int batch,
+                           int num_qo_heads, int num_kv_heads, int head_dim, int causal,
+                           double sm_scale, const int64_t* rows, long n_rows, double* o,
+                           double* lse, int nthreads) {
+    if (batch <= 0 || num_kv_heads <= 0 || num_qo_heads % num_kv_heads != 0 || head_dim <= 0 ||
+        page_size <= 0)
+        return -1;
+    const int group = num_qo_heads / num_kv_heads;
+    long max_kv = 0;
+    for (int b = 0; b < batch; ++b)
+        if (kv_lens[b] > max_kv) max_kv = kv_lens[b];
+    int bad = 0;
+#pragma omp parallel num_threads(pick_threads(nthreads)) reduction(| : bad)
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)(max_kv > 0 ? max_kv : 1));
+        const uint8_t** kr = (const uint8_t**)malloc(sizeof(void*) * (size_t)(max_kv > 0 ? max_kv : 1));
+        const uint8_t** vr = (const uint8_t**)malloc(sizeof(void*) * (size_t)(max_kv > 0 ? max_kv : 1));
+        long r;
+#pragma omp for schedule(dynamic, 4)
+        for (r = 0; r < n_rows; ++r) {
+            long t = (long)(rows[r] / num_qo_heads);
+            int h = (int)(rows[r] % num_qo_heads);
+            int b = find_request(q_indptr, batch, t);
+            if (b < 0) { bad = 1; continue; }
+            long i = t - q_indptr[b];
+            long qo_len = (long)q_indptr[b + 1] - q_indptr[b];
+            long kv_len = kv_lens[b];
+            int g = h / group;
+            long n = allowed_keys(i, qo_len, kv_len, causal);
+            int row_bad = 0;
+            for (long j = 0; j < n; ++j) {
+                long page = page_table[(size_t)b * page_table_stride + j / page_size];
+                if (page < 0 || page >= num_pages) { row_bad = 1; break; }
+                size_t off = (((size_t)page * page_size + (size_t)(j % page_size)) * num_kv_heads + g) * head_dim;
+                kr[j] = k_pages + off;
+                vr[j] = v_pages + off;
+            }
+            if (row_bad) { bad = 1; continue; }
+            attend_row_e4m3(q + ((size_t)t * num_qo_heads + h) * head_dim, kr, vr, n, head_dim,
+                            k_scale, v_scale, sm_scale, s, o + (size_t)r * head_dim, lse + r);
+        }
+        free(s);
+        free(kr);
+        free(vr);
+    }
+    return bad ? -1 : 0;
+}
+
+/*
  * Merge of attention states (FlashInfer documentation, flashinfer.cascade,
  * "Merge Attention States"): given n_states partial results of the same rows over
  * disjoint key sets, v [n_states, n_rows, d] (each normalised over its own keys) and

@@ -332,3 +332,108 @@ def test_bf16_widening_matches_torch():
     case.v[0, 0] = x
     o, _ = run_oracle(case)
     assert np.array_equal(o[0], x.to(torch.float64).numpy())
+
+
+# ---------------------------------------------------------------- FP8 E4M3 KV cache
+def test_e4m3_decoder_matches_torch_float8_for_every_byte():
+    b = np.arange(256, dtype=np.uint8)
+    ours = oracle.e4m3_decode(b)
+    ref = torch.from_numpy(b).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(ours), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(ours[ok], ref[ok])
+    assert np.array_equal(np.signbit(ours[ok]), np.signbit(ref[ok]))
+
+
+def test_e4m3_closed_forms():
+    vals = oracle.e4m3_decode(np.array([0x38, 0x7E, 0x01, 0x08, 0x07, 0xB8, 0x00, 0x80, 0x7F],
+                                       dtype=np.uint8))
+    assert vals[0] == 1.0                      # exponent 7 (= bias), mantissa 0
+    assert vals[1] == 448.0                    # largest finite: 2^8 * 1.75
+    assert vals[2] == 2.0 ** -9                # smallest subnormal: 1/8 * 2^-6
+    assert vals[3] == 2.0 ** -6                # smallest normal
+    assert vals[4] == 7 / 8 * 2.0 ** -6        # largest subnormal
+    assert vals[5] == -1.0
+    assert vals[6] == 0.0 and not np.signbit(vals[6])
+    assert vals[7] == 0.0 and np.signbit(vals[7])
+    assert np.isnan(vals[8])
+
+
+def _dense_paged(q, k, v, qo, kv, G, causal, scale):
+    """Dense numpy attention over contiguous per-request K/V (float64 inputs)."""
+    qi = np.concatenate([[0], np.cumsum(qo)])
+    ki = np.concatenate([[0], np.cumsum(kv)])
+    k = np.repeat(k, G, axis=1)
+    v = np.repeat(v, G, axis=1)
+    o_all = np.zeros(q.shape)
+    lse_all = np.full(q.shape[:2], -np.inf)
+    for b in range(len(qo)):
+        Q, K, V = q[qi[b]:qi[b + 1]], k[ki[b]:ki[b + 1]], v[ki[b]:ki[b + 1]]
+        if len(Q) == 0 or len(K) == 0:
+            continue
+        S = np.einsum("ihd,jhd->hij", Q, K) * scale
+        ii = np.arange(len(Q))[:, None]
+        jj = np.arange(len(K))[None, :]
+        mask = (jj <= ii + len(K) - len(Q)) if causal else np.ones((len(Q), len(K)), bool)
+        S = np.where(mask[None], S, -np.inf)
+        lse = logsumexp(S, axis=-1)
+        with np.errstate(invalid="ignore"):
+            P = np.nan_to_num(np.exp(S - lse[..., None]), nan=0.0)
+        o_all[qi[b]:qi[b + 1]] = np.einsum("hij,jhd->ihd", P, V)
+        lse_all[qi[b]:qi[b + 1]] = lse.T
+    return o_all.reshape(-1, q.shape[-1]), lse_all.reshape(-1)
+
+
+def _contiguous_kv(pc, pages_f64):
+    out = []
+    for b, n in enumerate(pc.kv_lens):
+        npg = (n + pc.page_size - 1) // pc.page_size
+        rows = pages_f64[pc.page_table[b, :npg].numpy()].reshape(-1, pc.num_kv_heads, pc.head_dim)
+        out.append(rows[:n])
+    return np.concatenate(out)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("qo,kv,hq,hk,d,ps", [
+    ([1, 1, 1], [5, 40, 17], 4, 1, 16, 16),
+    ([3, 9], [30, 9], 8, 2, 32, 16),
+    ([4], [100], 4, 4, 128, 32),
+])
+def test_e4m3_oracle_matches_dense_brute_force(causal, qo, kv, hq, hk, d, ps):
+    pc = W.paged_case_e4m3(kv, hq, hk, d, page_size=ps, qo_lens=qo, causal=causal, seed=d + ps)
+    ks, vs = pc.meta["k_scale"], pc.meta["v_scale"]
+    o, lse = oracle.paged_attention_e4m3(pc.q, pc.q_indptr, pc.k_pages, pc.v_pages, ks, vs,
+                                         pc.page_table, pc.kv_lens_t, hq, hk, causal, pc.sm_scale)
+    kf = pc.k_pages.view(torch.float8_e4m3fn).to(torch.float64).numpy() * ks
+    vf = pc.v_pages.view(torch.float8_e4m3fn).to(torch.float64).numpy() * vs
+    bo, blse = _dense_paged(f64(pc.q), _contiguous_kv(pc, kf), _contiguous_kv(pc, vf), qo, kv,
+                            hq // hk, causal, pc.sm_scale)
+    assert np.max(np.abs(o - bo)) <= 1e-12
+    assert_lse_close(lse, blse, 1e-12)
+
+
+def test_e4m3_oracle_equals_bf16_oracle_on_representable_values():
+    """E4M3 values times a power-of-two scale are exact in bf16, so the bf16 oracle over
+    those values must give the very same float64 results."""
+    pc = W.paged_case_e4m3([70, 3, 129], 8, 2, 64, page_size=16, qo_lens=[5, 3, 2], seed=3,
+                           k_scale=0.25, v_scale=4.0)
+    kb = (pc.k_pages.view(torch.float8_e4m3fn).float() * 0.25).to(torch.bfloat16)
+    vb = (pc.v_pages.view(torch.float8_e4m3fn).float() * 4.0).to(torch.bfloat16)
+    o8, l8 = oracle.paged_attention_e4m3(pc.q, pc.q_indptr, pc.k_pages, pc.v_pages, 0.25, 4.0,
+                                         pc.page_table, pc.kv_lens_t, 8, 2, True, pc.sm_scale)
+    o16, l16 = oracle.paged_attention(pc.q, pc.q_indptr, kb, vb, pc.page_table, pc.kv_lens_t, 8,
+                                      2, True, pc.sm_scale)
+    assert np.array_equal(o8, o16) and np.array_equal(l8, l16)
+
+
+def test_e4m3_scales_fold_into_score_scale_and_output():
+    pc = W.paged_case_e4m3([50, 200], 4, 2, 32, page_size=16, qo_lens=[1, 1], seed=5)
+    base_o, base_l = oracle.paged_attention_e4m3(pc.q, pc.q_indptr, pc.k_pages, pc.v_pages, 1.0,
+                                                 1.0, pc.page_table, pc.kv_lens_t, 4, 2, True,
+                                                 pc.sm_scale)
+    o, l = oracle.paged_attention_e4m3(pc.q, pc.q_indptr, pc.k_pages, pc.v_pages, 3.0, 1.0,
+                                       pc.page_table, pc.kv_lens_t, 4, 2, True, pc.sm_scale / 3.0)
+    assert np.max(np.abs(o - base_o)) <= 1e-12 and np.max(np.abs(l - base_l)) <= 1e-12
+    o, l = oracle.paged_attention_e4m3(pc.q, pc.q_indptr, pc.k_pages, pc.v_pages, 1.0, 2.5,
+                                       pc.page_table, pc.kv_lens_t, 4, 2, True, pc.sm_scale)
+    assert np.max(np.abs(o - 2.5 * base_o)) <= 1e-12 and np.array_equal(l, base_l)
