@@ -433,9 +433,10 @@ def time_calls(fn, stream, reps=20, warmup=3):
 
 def bench_extra(api, W, dev, stream, dc, peaks):
     """The paged prefill (ragged queries over a paged KV cache) on the prefill_hd128 and
-    prefix_hd256 shapes with 16-token pages, the ragged prefix_hd256 beside it, and
+    prefix_hd256 shapes with 16-token pages, the ragged prefix_hd256 beside it,
     4-token-per-request decode (speculative verification) over the resident 256-request
-    decode cache; each timed on its own (inputs resident in HBM)."""
+    decode cache, and the decode over that cache stored as FP8 E4M3; each timed on its own
+    (inputs resident in HBM)."""
     out = {}
 
     def tensor_line(flops, ms, what):
@@ -484,6 +485,20 @@ def bench_extra(api, W, dev, stream, dc, peaks):
         "what": "256 requests x 4 query tokens (decode workload's cache, causal)",
         "ms_per_launch": ms, "value": gbs, "unit": "GB/s",
         "roofline": {"bound": "hbm", "peak": peaks["hbm_gbs"], "frac": gbs / peaks["hbm_gbs"]}}
+    # the decode workload's cache as FP8 E4M3 (per-tensor scales), same requests
+    k8 = dc.k_pages.to(torch.float8_e4m3fn)
+    v8 = dc.v_pages.to(torch.float8_e4m3fn)
+    o8 = torch.empty_like(dc.q)
+    l8 = torch.empty(dc.q.shape[:2], dtype=torch.float32, device=dev)
+    ms = time_calls(lambda: api.paged_decode(dc.q, k8, v8, dc.page_table, dc.kv_lens_t,
+                                             sm_scale=dc.sm_scale, k_scale=1.0, v_scale=1.0,
+                                             out=o8, lse=l8, stream=stream), stream, reps=20)
+    gbs8 = kv_bytes / 2 / (ms / 1e3) / 1e9
+    out["decode_e4m3"] = {
+        "what": "decode workload (256 requests) with an FP8 E4M3 KV cache; GB/s of E4M3 K/V",
+        "ms_per_launch": ms, "value": gbs8, "unit": "GB/s",
+        "roofline": {"bound": "hbm", "peak": peaks["hbm_gbs"], "frac": gbs8 / peaks["hbm_gbs"]}}
+    del k8, v8
     out["device_status"] = api.device_status()
     torch.cuda.empty_cache()
     return out

@@ -202,6 +202,29 @@ int pgqa_paged_decode_bf16_strided(const void* q, const void* k_pages, const voi
                                    int num_kv_heads, int head_dim, float sm_scale,
                                    pgqa_stream_t stream);
 
+/*
+ * Paged decode over an FP8 E4M3 KV cache: k_pages / v_pages hold one byte per element
+ * (OCP E4M3, "fn": no infinities, S.1111.111 is NaN) and the element values are
+ * e4m3 * k_scale (keys) and e4m3 * v_scale (values), one scale per tensor.  q, o and lse
+ * stay bf16 / bf16 / fp32; everything else is as for pgqa_paged_decode_bf16_strided, with
+ * strides in elements (= bytes) that must be positive multiples of 16.  For packed NHD
+ * pools pass page_stride = page_size * Hk * d, slot_stride = Hk * d, head_stride = d.
+ *
+ * Defined by: FlashInfer documentation, flashinfer_benchmark.py "Attention Flags"
+ * (--kv_dtype fp8_e4m3: E4M3 key and value tensors); the pages give no scale convention,
+ * so one float scale per tensor is taken (flashinfer "FP8 GEMM: Per-tensor and groupwise
+ * scaling" lists per-tensor scaling as one of its FP8 modes).
+ *
+ * Supported: head_dim 128; page_size 16, 32, 64 or 128; G in {1,2,4,8}.  Errors as for
+ * pgqa_paged_decode_bf16; a NaN or infinite scale is PGQA_ERR_INVALID_ARG.
+ */
+int pgqa_paged_decode_e4m3(const void* q, const void* k_pages, const void* v_pages,
+                           const int32_t* page_table, const int32_t* kv_lens, int page_size,
+                           int page_table_stride, int num_pages, int64_t page_stride,
+                           int64_t slot_stride, int64_t head_stride, float k_scale, float v_scale,
+                           void* o, float* lse, int batch, int num_qo_heads, int num_kv_heads,
+                           int head_dim, float sm_scale, pgqa_stream_t stream);
+
 /* Same calls under the short names used by serving integrations. */
 int ragged_prefill_bf16(const void* q, const void* k, const void* v, void* o, float* lse,
                         const int32_t* q_indptr, const int32_t* kv_indptr, int batch,

@@ -26,6 +26,7 @@ STATUS_NAMES = {
 ABI_FUNCTIONS = (
     "pgqa_ragged_prefill_bf16", "pgqa_paged_prefill_bf16", "pgqa_paged_decode_bf16",
     "pgqa_paged_prefill_bf16_strided", "pgqa_paged_decode_bf16_strided",
+    "pgqa_paged_decode_e4m3",
     "ragged_prefill_bf16", "paged_prefill_bf16", "paged_decode_bf16", "pgqa_set_workspace", "pgqa_workspace_bytes_prefill",
     "pgqa_workspace_bytes_decode", "pgqa_get_device_status", "pgqa_status_string",
     "pgqa_version", "pgqa_paged_decode_bf16_noalloc",
@@ -64,6 +65,9 @@ def _load(path: Path):
     lib.pgqa_paged_decode_bf16_strided.argtypes = [p, p, p, p, p, i, i, i, i64, i64, i64, p, p, i,
                                                    i, i, i, f, p]
     lib.pgqa_paged_decode_bf16_strided.restype = i
+    lib.pgqa_paged_decode_e4m3.argtypes = [p, p, p, p, p, i, i, i, i64, i64, i64, f, f, p, p, i, i,
+                                           i, i, f, p]
+    lib.pgqa_paged_decode_e4m3.restype = i
     lib.pgqa_set_workspace.argtypes, lib.pgqa_set_workspace.restype = [p, sz], i
     lib.pgqa_workspace_bytes_prefill.argtypes = [i, i64, i, i]
     lib.pgqa_workspace_bytes_prefill.restype = sz
@@ -107,23 +111,29 @@ def _check(t, name, dtype, dim=None, device=None):
         raise ValueError(f"{name} is on {t.device}, expected {device}")
 
 
-def _page_pools(k_pages, v_pages, kv_layout, dev):
+_E4M3_DTYPES = (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8))
+
+
+def _page_pools(k_pages, v_pages, kv_layout, dev, allow_e4m3=False):
     """Shape and element strides of the K/V page pools.
 
     kv_layout "NHD": tensors [num_pages, page_size, Hk, d]; "HND": [num_pages, Hk,
     page_size, d].  Any strides are accepted as long as d is contiguous and K and V share
-    them (for instance a per-layer slice of a larger cache).  Returns (num_pages,
+    them (for instance a per-layer slice of a larger cache).  bf16 pools, or with
+    allow_e4m3 one-byte E4M3 pools (uint8 or float8_e4m3fn).  Returns (num_pages,
     page_size, Hk, d, (page_stride, slot_stride, head_stride), contiguous_nhd).
     """
+    ok_types = (torch.bfloat16,) + (_E4M3_DTYPES if allow_e4m3 else ())
     for t, name in ((k_pages, "k_pages"), (v_pages, "v_pages")):
-        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16:
-            raise TypeError(f"{name} must be a bfloat16 torch.Tensor")
+        if not isinstance(t, torch.Tensor) or t.dtype not in ok_types:
+            raise TypeError(f"{name} must be a torch.Tensor of dtype {ok_types}")
         if not t.is_cuda or t.device != dev:
             raise ValueError(f"{name} must be a CUDA tensor on {dev}")
         if t.dim() != 4 or t.stride(-1) != 1:
             raise ValueError(f"{name} must be 4-D with a contiguous last (head_dim) axis")
-    if k_pages.shape != v_pages.shape or k_pages.stride() != v_pages.stride():
-        raise ValueError("k_pages and v_pages must have the same shape and strides")
+    if (k_pages.shape != v_pages.shape or k_pages.stride() != v_pages.stride() or
+            k_pages.element_size() != v_pages.element_size()):
+        raise ValueError("k_pages and v_pages must have the same dtype size, shape and strides")
     if kv_layout == "NHD":
         num_pages, page_size, hk, d = k_pages.shape
         page_s, slot_s, head_s, _ = k_pages.stride()
@@ -221,12 +231,13 @@ def paged_prefill(q, k_pages, v_pages, q_indptr, page_table, kv_lens, causal=Tru
 
 
 def paged_decode(q, k_pages, v_pages, page_table, kv_lens, sm_scale=None, out=None, lse=None,
-                 return_lse=True, stream=None, kv_layout="NHD"):
-    """Paged decode (pgqa_paged_decode_bf16, or the _strided call for HND or non-contiguous
-    page pools).
+                 return_lse=True, stream=None, kv_layout="NHD", k_scale=1.0, v_scale=1.0):
+    """Paged decode (pgqa_paged_decode_bf16; the _strided call for HND or non-contiguous
+    bf16 pools; pgqa_paged_decode_e4m3 for FP8 E4M3 pools).
 
-    q [batch, Hq, d]; k_pages / v_pages [num_pages, page_size, Hk, d] ("NHD") or
-    [num_pages, Hk, page_size, d] ("HND") bf16, any strides with d contiguous; page_table
+    q [batch, Hq, d] bf16; k_pages / v_pages [num_pages, page_size, Hk, d] ("NHD") or
+    [num_pages, Hk, page_size, d] ("HND"), any strides with d contiguous, either bf16 or
+    E4M3 bytes (uint8 / float8_e4m3fn, element = e4m3 x k_scale / v_scale); page_table
     [batch, stride] int32; kv_lens [batch] int32; all on one CUDA device.
     Returns (o [batch, Hq, d] bf16, lse [batch, Hq] fp32 or None).
     """
@@ -235,7 +246,9 @@ def paged_decode(q, k_pages, v_pages, page_table, kv_lens, sm_scale=None, out=No
     _check(page_table, "page_table", torch.int32, 2, dev)
     _check(kv_lens, "kv_lens", torch.int32, 1, dev)
     batch, hq, d = q.shape
-    num_pages, page_size, hk, dk, strides, packed = _page_pools(k_pages, v_pages, kv_layout, dev)
+    num_pages, page_size, hk, dk, strides, packed = _page_pools(k_pages, v_pages, kv_layout, dev,
+                                                                allow_e4m3=True)
+    e4m3 = k_pages.element_size() == 1
     if dk != d:
         raise ValueError("k_pages / v_pages must have q's head_dim")
     if page_table.shape[0] != batch or kv_lens.numel() != batch:
@@ -249,7 +262,12 @@ def paged_decode(q, k_pages, v_pages, page_table, kv_lens, sm_scale=None, out=No
         lse = torch.empty((batch, hq), dtype=torch.float32, device=dev)
     if lse is not None:
         _check(lse, "lse", torch.float32, 2, dev)
-    if packed:
+    if e4m3:
+        rc = lib.pgqa_paged_decode_e4m3(
+            _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table), _ptr(kv_lens), page_size,
+            page_table.shape[1], num_pages, *strides, float(k_scale), float(v_scale), _ptr(out),
+            _ptr(lse), batch, hq, hk, d, float(sm_scale), _stream(stream))
+    elif packed:
         rc = lib.pgqa_paged_decode_bf16(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table),
                                         _ptr(kv_lens), page_size, page_table.shape[1], num_pages,
                                         _ptr(out), _ptr(lse), batch, hq, hk, d, float(sm_scale),

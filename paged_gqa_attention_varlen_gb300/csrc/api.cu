@@ -19,10 +19,10 @@ cudaError_t launch_attention_pair(const Params&, int, cudaStream_t);
 }  // namespace prefill
 namespace decode {
 cudaError_t launch_plan(const PlanParams&, cudaStream_t);
-cudaError_t launch_decode(const Params&, int group, int num_sms, cudaStream_t);
+cudaError_t launch_decode(const Params&, int group, bool kv8, int num_sms, cudaStream_t);
 cudaError_t launch_merge(const Params&, cudaStream_t);
 cudaError_t prepare_page_maps(Params&, const void*, const void*, int, int, int, long long,
-                              long long, long long);
+                              long long, long long, bool);
 }  // namespace decode
 
 namespace {
@@ -165,12 +165,13 @@ int encode_pages_4d(CUtensorMap* map, const void* base, int d, int page_size, in
     return r == CUDA_SUCCESS ? PGQA_OK : PGQA_ERR_INVALID_ARG;
 }
 
-// Element strides of a page pool: positive multiples of 8 elements (16 bytes, the TMA
-// rule for global strides) and below 2^36 elements.
-bool kv_strides_ok(long long page_stride, long long slot_stride, long long head_stride) {
+// Element strides of a page pool: positive multiples of 16 bytes (the TMA rule for
+// global strides) and below 2^36 elements; elem_bytes is 2 (bf16) or 1 (E4M3).
+bool kv_strides_ok(long long page_stride, long long slot_stride, long long head_stride,
+                   int elem_bytes = 2) {
     const long long lim = 1LL << 36;
     for (long long x : {page_stride, slot_stride, head_stride})
-        if (x <= 0 || (x & 7) || x >= lim) return false;
+        if (x <= 0 || ((x * elem_bytes) & 15) || x >= lim) return false;
     return true;
 }
 
@@ -193,6 +194,15 @@ size_t decode_ws_bytes(int batch, int stride, int page_size, int hq, int d) {
 }  // namespace pgqa
 
 using namespace pgqa;
+
+namespace {
+int paged_decode_impl(const void* q, const void* k_pages, const void* v_pages,
+                      const int32_t* page_table, const int32_t* kv_lens, int page_size,
+                      int page_table_stride, int num_pages, int64_t page_stride,
+                      int64_t slot_stride, int64_t head_stride, void* o, float* lse, int batch,
+                      int num_qo_heads, int num_kv_heads, int head_dim, float sm_scale, bool kv8,
+                      float k_scale, float v_scale, pgqa_stream_t stream);
+}  // namespace
 
 extern "C" {
 
@@ -522,10 +532,42 @@ int pgqa_paged_decode_bf16_strided(const void* q, const void* k_pages, const voi
                                    void* o, float* lse, int batch, int num_qo_heads,
                                    int num_kv_heads, int head_dim, float sm_scale,
                                    pgqa_stream_t stream) {
+    return paged_decode_impl(q, k_pages, v_pages, page_table, kv_lens, page_size,
+                             page_table_stride, num_pages, page_stride, slot_stride, head_stride,
+                             o, lse, batch, num_qo_heads, num_kv_heads, head_dim, sm_scale, false,
+                             1.f, 1.f, stream);
+}
+
+int pgqa_paged_decode_e4m3(const void* q, const void* k_pages, const void* v_pages,
+                           const int32_t* page_table, const int32_t* kv_lens, int page_size,
+                           int page_table_stride, int num_pages, int64_t page_stride,
+                           int64_t slot_stride, int64_t head_stride, float k_scale, float v_scale,
+                           void* o, float* lse, int batch, int num_qo_heads, int num_kv_heads,
+                           int head_dim, float sm_scale, pgqa_stream_t stream) {
+    if (!(k_scale == k_scale) || !(v_scale == v_scale) || k_scale > 3.0e38f ||
+        k_scale < -3.0e38f || v_scale > 3.0e38f || v_scale < -3.0e38f)
+        return PGQA_ERR_INVALID_ARG;
+    return paged_decode_impl(q, k_pages, v_pages, page_table, kv_lens, page_size,
+                             page_table_stride, num_pages, page_stride, slot_stride, head_stride,
+                             o, lse, batch, num_qo_heads, num_kv_heads, head_dim, sm_scale, true,
+                             k_scale, v_scale, stream);
+}
+
+}  // extern "C"
+
+namespace {
+// The paged decode for bf16 (kv8 = false) or E4M3 (kv8 = true, with per-tensor scales)
+// K/V pools of the given element strides.
+int paged_decode_impl(const void* q, const void* k_pages, const void* v_pages,
+                      const int32_t* page_table, const int32_t* kv_lens, int page_size,
+                      int page_table_stride, int num_pages, int64_t page_stride,
+                      int64_t slot_stride, int64_t head_stride, void* o, float* lse, int batch,
+                      int num_qo_heads, int num_kv_heads, int head_dim, float sm_scale, bool kv8,
+                      float k_scale, float v_scale, pgqa_stream_t stream) {
     if (batch < 0 || num_qo_heads <= 0 || num_kv_heads <= 0 || page_table_stride < 0 ||
         num_pages < 0)
         return PGQA_ERR_INVALID_ARG;
-    if (batch > 0 && !kv_strides_ok(page_stride, slot_stride, head_stride))
+    if (batch > 0 && !kv_strides_ok(page_stride, slot_stride, head_stride, kv8 ? 1 : 2))
         return PGQA_ERR_INVALID_ARG;
     if (batch == 0) return PGQA_OK;
     if (!q || !k_pages || !v_pages || !o || !kv_lens || (!page_table && page_table_stride > 0))
@@ -594,15 +636,19 @@ int pgqa_paged_decode_bf16_strided(const void* q, const void* k_pages, const voi
     p.num_pages = num_pages;
     p.num_qo_heads = num_qo_heads;
     p.num_kv_heads = num_kv_heads;
-    p.scale_log2 = sm_scale * 1.4426950408889634f;
+    p.scale_log2 = sm_scale * 1.4426950408889634f * k_scale;
+    p.v_scale = v_scale;
     p.chunk_capacity = chunks;
     if (decode::prepare_page_maps(p, k_pages, v_pages, num_pages, num_kv_heads, page_size,
-                                  page_stride, slot_stride, head_stride) != cudaSuccess)
+                                  page_stride, slot_stride, head_stride, kv8) != cudaSuccess)
         return PGQA_ERR_INVALID_ARG;
-    e = decode::launch_decode(p, group, st->num_sms, s);
+    e = decode::launch_decode(p, group, kv8, st->num_sms, s);
     if (e != cudaSuccess) return PGQA_ERR_CUDA;
     return map_cuda(decode::launch_merge(p, s));
 }
+}  // namespace
+
+extern "C" {
 
 int ragged_prefill_bf16(const void* q, const void* k, const void* v, void* o, float* lse,
                         const int32_t* q_indptr, const int32_t* kv_indptr, int batch,

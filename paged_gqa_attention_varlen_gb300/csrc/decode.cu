@@ -121,6 +121,38 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     return v;
 }
 
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+    uint2 v;
+    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
+}
+
+// Two E4M3 values (low byte = element 0) -> one packed fp32 pair, exactly: E4M3 -> f16 is
+// exact (f16 has the range and the mantissa bits, NaN stays NaN), and f16 -> f32 is exact.
+// (An integer-ALU decoding, bits shifted into place and the exponent bias folded into q
+// and P, measured 14 % slower: the decode's issue slots, not the conversion pipe, bound
+// it.)
+__device__ __forceinline__ uint64_t e4m3x2_to_pair(uint32_t two_bytes) {
+    uint32_t h;
+    asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
+        : "=r"(h)
+        : "r"(two_bytes));
+    float lo, hi;
+    asm("{\n\t.reg .f16 l, u;\n\tmov.b32 {l, u}, %2;\n\tcvt.f32.f16 %0, l;\n\t"
+        "cvt.f32.f16 %1, u;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(h));
+    return f2_pack(lo, hi);
+}
+
+// 8 E4M3 bytes -> 4 packed fp32 pairs (element 2k in the low half of pair k)
+__device__ __forceinline__ void e4m3x8_to_pairs(const uint2& r, uint64_t (&o)[4]) {
+    o[0] = e4m3x2_to_pair(r.x & 0xffffu);
+    o[1] = e4m3x2_to_pair(r.x >> 16);
+    o[2] = e4m3x2_to_pair(r.y & 0xffffu);
+    o[3] = e4m3x2_to_pair(r.y >> 16);
+}
+
 // 8 bf16 -> 4 packed fp32 pairs (element 2k in the low half of pair k)
 __device__ __forceinline__ void bf16x8_to_pairs(const uint4& r, uint64_t (&o)[4]) {
     o[0] = f2_pack(bf_lo(r.x), bf_hi(r.x));
@@ -129,10 +161,17 @@ __device__ __forceinline__ void bf16x8_to_pairs(const uint4& r, uint64_t (&o)[4]
     o[3] = f2_pack(bf_lo(r.w), bf_hi(r.w));
 }
 
-template <int G>
+template <int G, bool KV8>
 __global__ void __launch_bounds__(WARPS * 32, G >= 8 ? 2 : 3)
     decode_tma_kernel(const __grid_constant__ Params p) {
     constexpr int D = HEAD_DIM;
+    // KV8: K/V are FP8 E4M3 bytes; a unit is then half the bytes and the ring has twice
+    // the stages, so the shared memory and the bytes in flight per warp stay the same
+    constexpr int EB = KV8 ? 1 : 2;              // bytes per K/V element
+    constexpr int UNIT = PAGE * D * EB;          // one 16-token unit of one head
+    constexpr int NST = KV8 ? 2 * STAGES : STAGES;
+    constexpr int SB = 2 * UNIT;                 // K + V of a unit
+    static_assert(NST * SB == STAGES * STAGE_BYTES, "ring size");
     constexpr int NV = 8 * G;                     // partial dot products per lane per page
     constexpr int VPL = NV >= 16 ? NV / 16 : 1;   // full scores per lane after the reduction
     constexpr int GS = 16 / G;                    // d-slices per head among the score lanes
@@ -144,10 +183,10 @@ __global__ void __launch_bounds__(WARPS * 32, G >= 8 ? 2 : 3)
     const int tp = lane >> 4, ds = lane & 15;
     uint8_t* wsm = smem + wib * WARP_SMEM;
     const uint32_t stage0 = smem_u32(wsm);
-    float* ps = reinterpret_cast<float*>(wsm + STAGES * STAGE_BYTES);  // [16 tokens][G]
-    const uint32_t full0 = smem_u32(wsm + STAGES * STAGE_BYTES + 512);
+    float* ps = reinterpret_cast<float*>(wsm + NST * SB);  // [16 tokens][G]
+    const uint32_t full0 = smem_u32(wsm + NST * SB + 512);
     if (lane == 0) {
-        for (int s = 0; s < STAGES; ++s) mbar_init(full0 + 8 * s, 1);
+        for (int s = 0; s < NST; ++s) mbar_init(full0 + 8 * s, 1);
         fence_barrier_init();
     }
     __syncwarp();
@@ -194,19 +233,19 @@ __global__ void __launch_bounds__(WARPS * 32, G >= 8 ? 2 : 3)
         auto issue = [&](int page) {  // lane 0 only
             int pid, slot;
             const bool valid = unit_row(page, pid, slot);
-            const uint32_t st = issued % STAGES;
+            const uint32_t st = issued % NST;
             const uint32_t bar = full0 + 8 * st;
             if (valid) {
-                mbar_arrive_expect_tx(bar, STAGE_BYTES);
-                const uint32_t dst = stage0 + st * STAGE_BYTES;
+                mbar_arrive_expect_tx(bar, SB);
+                const uint32_t dst = stage0 + st * SB;
                 tma_load_4d(dst, &p.tm_kpages, bar, 0, slot, g, pid);
-                tma_load_4d(dst + PAGE_HEAD_BYTES, &p.tm_vpages, bar, 0, slot, g, pid);
+                tma_load_4d(dst + UNIT, &p.tm_vpages, bar, 0, slot, g, pid);
             } else {
                 atomicOr(p.status, PGQA_DEV_BOUNDS);
                 mbar_arrive(bar);  // the page is skipped; keep the ring in phase
             }
         };
-        const int prime = min(np, STAGES);
+        const int prime = min(np, NST);
         for (int k = 0; k < prime; ++k) {
             if (lane == 0) issue(page0 + k);
             ++issued;
@@ -237,22 +276,23 @@ __global__ void __launch_bounds__(WARPS * 32, G >= 8 ? 2 : 3)
         float lp = 0.f;
 
         for (int pi = 0; pi < np; ++pi) {
-            const uint32_t st = consumed % STAGES;
-            ok = __all_sync(0xffffffffu, mbar_wait_bounded(full0 + 8 * st, (consumed / STAGES) & 1,
+            const uint32_t st = consumed % NST;
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(full0 + 8 * st, (consumed / NST) & 1,
                                                            nullptr, p.status));
             if (!ok) break;
             ++consumed;
             const int page = page0 + pi;
             int pid, slot;
             const int nvalid = unit_row(page, pid, slot) ? min(PAGE, tok1 - page * PAGE) : 0;
-            const uint32_t kbase = stage0 + st * STAGE_BYTES + ds * 16;
-            const uint32_t vbase = kbase + PAGE_HEAD_BYTES;
+            const uint32_t kbase = stage0 + st * SB + ds * (8 * EB);
+            const uint32_t vbase = kbase + UNIT;
 
             float part[NV];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 uint64_t k2[4];
-                bf16x8_to_pairs(lds128(kbase + (2 * i + tp) * (D * 2)), k2);
+                if constexpr (KV8) e4m3x8_to_pairs(lds64(kbase + (2 * i + tp) * D), k2);
+                else bf16x8_to_pairs(lds128(kbase + (2 * i + tp) * (D * 2)), k2);
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
                     uint64_t acc = f2_mul(q2[h][0], k2[0]);
@@ -313,7 +353,8 @@ __global__ void __launch_bounds__(WARPS * 32, G >= 8 ? 2 : 3)
             for (int i = 0; i < 8; ++i) {
                 const int t = 2 * i + tp;
                 uint64_t v2[4];
-                bf16x8_to_pairs(lds128(vbase + t * (D * 2)), v2);
+                if constexpr (KV8) e4m3x8_to_pairs(lds64(vbase + t * D), v2);
+                else bf16x8_to_pairs(lds128(vbase + t * (D * 2)), v2);
                 if (nvalid < PAGE && t >= nvalid) {  // slots past kv_len may hold anything
 #pragma unroll
                     for (int e = 0; e < 4; ++e) v2[e] = zero2;
@@ -340,10 +381,10 @@ __global__ void __launch_bounds__(WARPS * 32, G >= 8 ? 2 : 3)
                 }
             }
             __syncwarp();  // every lane is done with this stage and with ps
-            if (pi + STAGES < np) {
+            if (pi + NST < np) {
                 if (lane == 0) {
                     fence_async_smem();
-                    issue(page0 + pi + STAGES);
+                    issue(page0 + pi + NST);
                 }
                 ++issued;
             }
@@ -363,7 +404,7 @@ __global__ void __launch_bounds__(WARPS * 32, G >= 8 ? 2 : 3)
 #pragma unroll
         for (int h = 0; h < G; ++h) {
             const float l = __shfl_sync(0xffffffffu, lsum, h * GS);
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const float inv = l > 0.f ? p.v_scale / l : 0.f;  // v_scale = 1 for bf16 K/V
             const float lse_v = l > 0.f ? (m[h] + log2f(l)) * 0.69314718055994531f : -INFINITY;
             const int hq = g * G + h;
             float o[8];
@@ -395,7 +436,7 @@ __global__ void __launch_bounds__(WARPS * 32, G >= 8 ? 2 : 3)
     }
     // copies still in flight (an aborted item) land before the warp exits
     while (consumed < issued) {
-        mbar_wait_bounded(full0 + 8 * (consumed % STAGES), (consumed / STAGES) & 1, nullptr,
+        mbar_wait_bounded(full0 + 8 * (consumed % NST), (consumed / NST) & 1, nullptr,
                           p.status);
         ++consumed;
     }
@@ -456,7 +497,8 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 cudaError_t prepare_page_maps(Params& p, const void* k_pages, const void* v_pages,
                               int num_pages, int num_kv_heads, int page_size,
                               long long page_stride, long long slot_stride,
-                              long long head_stride) {
+                              long long head_stride, bool kv8) {
+    const int eb = kv8 ? 1 : 2;  // bytes per element
     static EncodeTiledFn encode = nullptr;
     if (encode == nullptr) {
         void* fn = nullptr;
@@ -469,14 +511,15 @@ cudaError_t prepare_page_maps(Params& p, const void* k_pages, const void* v_page
     }
     const cuuint64_t dims[4] = {(cuuint64_t)HEAD_DIM, (cuuint64_t)page_size,
                                 (cuuint64_t)num_kv_heads, (cuuint64_t)(num_pages > 0 ? num_pages : 1)};
-    const cuuint64_t strides[3] = {(cuuint64_t)slot_stride * 2, (cuuint64_t)head_stride * 2,
-                                   (cuuint64_t)page_stride * 2};
+    const cuuint64_t strides[3] = {(cuuint64_t)slot_stride * eb, (cuuint64_t)head_stride * eb,
+                                   (cuuint64_t)page_stride * eb};
     const cuuint32_t box[4] = {HEAD_DIM, PAGE, 1, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     CUtensorMap* maps[2] = {&p.tm_kpages, &p.tm_vpages};
     const void* bases[2] = {k_pages, v_pages};
+    const CUtensorMapDataType dt = kv8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     for (int i = 0; i < 2; ++i) {
-        CUresult r = encode(maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(bases[i]),
+        CUresult r = encode(maps[i], dt, 4, const_cast<void*>(bases[i]),
                             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -485,33 +528,39 @@ cudaError_t prepare_page_maps(Params& p, const void* k_pages, const void* v_page
     return cudaSuccess;
 }
 
-template <int G>
+template <int G, bool KV8>
 static cudaError_t launch_decode_g(const Params& p, int num_sms, cudaStream_t stream) {
     static int blocks_per_sm[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) dev = 0;
     if (blocks_per_sm[dev] == 0) {
-        cudaError_t e = cudaFuncSetAttribute(decode_tma_kernel<G>,
+        cudaError_t e = cudaFuncSetAttribute(decode_tma_kernel<G, KV8>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess) return e;
         int n = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_tma_kernel<G>, WARPS * 32,
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_tma_kernel<G, KV8>, WARPS * 32,
                                                           SMEM_BYTES);
         if (e != cudaSuccess) return e;
         blocks_per_sm[dev] = n > 0 ? n : 1;
     }
     const int grid = num_sms * blocks_per_sm[dev];
-    decode_tma_kernel<G><<<grid, WARPS * 32, SMEM_BYTES, stream>>>(p);
+    decode_tma_kernel<G, KV8><<<grid, WARPS * 32, SMEM_BYTES, stream>>>(p);
     return cudaGetLastError();
 }
 
-cudaError_t launch_decode(const Params& p, int group, int num_sms, cudaStream_t stream) {
-    switch (group) {
-        case 1: return launch_decode_g<1>(p, num_sms, stream);
-        case 2: return launch_decode_g<2>(p, num_sms, stream);
-        case 4: return launch_decode_g<4>(p, num_sms, stream);
-        case 8: return launch_decode_g<8>(p, num_sms, stream);
+// kv8: K/V pages are FP8 E4M3 bytes (p.scale_log2 already carries k_scale, p.v_scale
+// scales the outputs); else bf16 (p.v_scale = 1)
+cudaError_t launch_decode(const Params& p, int group, bool kv8, int num_sms, cudaStream_t stream) {
+    switch (group * 2 + (kv8 ? 1 : 0)) {
+        case 2: return launch_decode_g<1, false>(p, num_sms, stream);
+        case 3: return launch_decode_g<1, true>(p, num_sms, stream);
+        case 4: return launch_decode_g<2, false>(p, num_sms, stream);
+        case 5: return launch_decode_g<2, true>(p, num_sms, stream);
+        case 8: return launch_decode_g<4, false>(p, num_sms, stream);
+        case 9: return launch_decode_g<4, true>(p, num_sms, stream);
+        case 16: return launch_decode_g<8, false>(p, num_sms, stream);
+        case 17: return launch_decode_g<8, true>(p, num_sms, stream);
         default: return cudaErrorInvalidValue;
     }
 }

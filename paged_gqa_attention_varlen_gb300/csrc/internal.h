@@ -139,7 +139,8 @@ struct Params {
     int num_pages;
     int num_qo_heads;
     int num_kv_heads;
-    float scale_log2;
+    float scale_log2;           // sm_scale * log2(e) (* k_scale for E4M3 K/V)
+    float v_scale;              // output scale: 1 for bf16 K/V, v_scale for E4M3
     long long chunk_capacity;
 };
 

@@ -140,6 +140,25 @@ def test_strided_page_pool_validation(api):
             assert fn(*nhd) == -7 and fn(*hnd) == -7
 
 
+def test_e4m3_decode_validation(api):
+    p = ctypes.c_void_p
+    lib = api.lib
+
+    def dc(page_s=16 * 8 * 128, slot_s=8 * 128, head_s=128, ks=0.5, vs=2.0, batch=2, ps=16, d=128):
+        return lib.pgqa_paged_decode_e4m3(p(A), p(A), p(A), p(A), p(A), ps, 8, 100, page_s, slot_s,
+                                          head_s, ks, vs, p(A), p(A), batch, 32, 8, d, 0.1, None)
+
+    assert dc(batch=0) == 0
+    assert dc(head_s=8) == -1                      # 8 bytes: not a multiple of 16
+    assert dc(ks=float("nan")) == -1
+    assert dc(vs=float("inf")) == -1
+    assert dc(ps=24) == -2
+    assert dc(d=256) == -2
+    import torch
+    if not torch.cuda.is_available():
+        assert dc() == -7
+
+
 def test_prefill_host_validation(api):
     assert prefill(api, batch=0) == 0                       # empty batch: early return
     assert prefill(api, batch=-1) == -1
