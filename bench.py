@@ -406,7 +406,7 @@ def bench_gpu(args, ws, rank, local):
         "prefill_ms_per_launch": pf_launch_ms,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-        "gpu_launches": args.steps * (2 + 3),
+        "gpu_launches": args.steps * (3 + 3),
         "clocks": clk,
         "device_status": status,
         "cpu_baseline": cpu,

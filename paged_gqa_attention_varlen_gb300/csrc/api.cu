@@ -16,6 +16,7 @@ template <int D, bool PAGED>
 cudaError_t launch_attention(const Params&, int, cudaStream_t);
 template <bool PAGED>
 cudaError_t launch_attention_pair(const Params&, int, cudaStream_t);
+cudaError_t launch_merge(const Params&, int, cudaStream_t);
 }  // namespace prefill
 namespace decode {
 cudaError_t launch_plan(const PlanParams&, cudaStream_t);
@@ -175,9 +176,76 @@ bool kv_strides_ok(long long page_stride, long long slot_stride, long long head_
     return true;
 }
 
+// Prefill workspace: seven per-request int arrays, then the work list, then the split-KV
+// partial results (lse [rows] and O [rows, d] fp32) in what remains.
+constexpr int kPrefillArrays = 7;
+
 size_t prefill_ws_bytes(int batch, long long max_items) {
-    const size_t tile_off = align_up((size_t)(batch + 1) * sizeof(int), 256);
-    return kWsArrays + tile_off + (size_t)max_items * sizeof(prefill::WorkItem);
+    const size_t arr = align_up((size_t)(batch + 1) * sizeof(int), 256);
+    return kWsArrays + kPrefillArrays * arr + (size_t)max_items * sizeof(prefill::WorkItem);
+}
+
+struct PrefillWs {
+    WsHeader* hdr;
+    CUtensorMap* tmaps;
+    int *tile_off, *kv_off, *unit_off, *part_off, *merge_off, *nch, *kvl;
+    prefill::WorkItem* items;
+    long long item_capacity;
+    float *part_lse, *part_o;
+    long long part_capacity;
+};
+
+// Carve the workspace: a quarter of the space after the arrays holds the work list
+// (at least what 4096 items need), the rest the partial results.
+PrefillWs prefill_layout(const DeviceState& st, int batch, int head_dim) {
+    PrefillWs w;
+    uint8_t* ws = static_cast<uint8_t*>(st.ws);
+    w.hdr = reinterpret_cast<WsHeader*>(ws + kWsHeader);
+    w.tmaps = reinterpret_cast<CUtensorMap*>(ws + kWsTmapOffset);
+    const size_t arr = align_up((size_t)(batch + 1) * sizeof(int), 256);
+    int** arrays[kPrefillArrays] = {&w.tile_off, &w.kv_off, &w.unit_off, &w.part_off,
+                                    &w.merge_off, &w.nch, &w.kvl};
+    for (int i = 0; i < kPrefillArrays; ++i)
+        *arrays[i] = reinterpret_cast<int*>(ws + kWsArrays + i * arr);
+    const size_t items_off = kWsArrays + kPrefillArrays * arr;
+    const size_t rest = st.ws_bytes > items_off ? st.ws_bytes - items_off : 0;
+    size_t item_bytes = align_up(rest / 4, 256);
+    const size_t min_items = 4096 * sizeof(prefill::WorkItem);
+    if (item_bytes < min_items) item_bytes = rest < min_items ? rest : min_items;
+    w.items = reinterpret_cast<prefill::WorkItem*>(ws + items_off);
+    w.item_capacity = (long long)(item_bytes / sizeof(prefill::WorkItem));
+    const size_t part_off = items_off + item_bytes;
+    const size_t part_bytes = st.ws_bytes > part_off + 256 ? st.ws_bytes - part_off - 256 : 0;
+    const long long rows = (long long)(part_bytes / ((size_t)(head_dim + 1) * sizeof(float)));
+    w.part_capacity = rows;
+    w.part_lse = reinterpret_cast<float*>(ws + part_off);
+    w.part_o = reinterpret_cast<float*>(ws + part_off + align_up((size_t)rows * sizeof(float), 256));
+    if (rows > 0 && align_up((size_t)rows * sizeof(float), 256) + (size_t)rows * head_dim * 4 >
+                        part_bytes + 256)
+        w.part_capacity = rows - 64;  // keep the O block inside the workspace
+    if (w.part_capacity < 0) w.part_capacity = 0;
+    return w;
+}
+
+// Plan and attention parameters shared by the ragged and paged prefill
+void fill_split(prefill::PlanParams& pp, prefill::Params& p, const PrefillWs& w, int batch,
+                int head_dim, int num_qo_heads, int num_sms) {
+    pp.split_ok = head_dim == 128 ? 1 : 0;  // the hd256 kernel runs unsplit
+    pp.num_ctas = num_sms;
+    pp.num_qo_heads = num_qo_heads;
+    pp.part_capacity = w.part_capacity;
+    pp.unit_off = w.unit_off;
+    pp.part_off = w.part_off;
+    pp.merge_off = w.merge_off;
+    pp.nch = w.nch;
+    pp.kvl = w.kvl;
+    p.part_o = w.part_o;
+    p.part_lse = w.part_lse;
+    p.merge_off = w.merge_off;
+    p.part_off = w.part_off;
+    p.nch = w.nch;
+    p.kvl = w.kvl;
+    p.batch = batch;
 }
 
 size_t decode_ws_bytes(int batch, int stride, int page_size, int hq, int d) {
@@ -227,9 +295,7 @@ size_t pgqa_workspace_bytes_prefill(int batch, int64_t max_total_q, int num_qo_h
     if (batch < 0 || max_total_q < 0 || num_kv_heads <= 0 || num_qo_heads <= 0) return 0;
     const long long g = num_qo_heads / num_kv_heads;
     const long long tiles = (max_total_q * g + prefill::BM - 1) / prefill::BM + batch;
-    // + the per-request key offsets the paged prefill keeps
-    return prefill_ws_bytes(batch, tiles * num_kv_heads) +
-           align_up((size_t)(batch + 1) * sizeof(int), 256);
+    return prefill_ws_bytes(batch, tiles * num_kv_heads);
 }
 
 size_t pgqa_workspace_bytes_decode(int batch, int page_table_stride, int page_size,
@@ -320,14 +386,12 @@ int pgqa_ragged_prefill_bf16(const void* q, const void* k, const void* v, void* 
     rc = ensure_workspace(*st, prefill_ws_bytes(batch, 4096), s);
     if (rc != PGQA_OK) return rc;
 
-    uint8_t* ws = static_cast<uint8_t*>(st->ws);
-    WsHeader* hdr = reinterpret_cast<WsHeader*>(ws + kWsHeader);
-    CUtensorMap* tmaps = reinterpret_cast<CUtensorMap*>(ws + kWsTmapOffset);
-    int* tile_off = reinterpret_cast<int*>(ws + kWsArrays);
-    const size_t items_off = kWsArrays + align_up((size_t)(batch + 1) * sizeof(int), 256);
-    prefill::WorkItem* items = reinterpret_cast<prefill::WorkItem*>(ws + items_off);
-    const long long capacity =
-        (long long)((st->ws_bytes - items_off) / sizeof(prefill::WorkItem));
+    const PrefillWs lay = prefill_layout(*st, batch, head_dim);
+    WsHeader* hdr = lay.hdr;
+    CUtensorMap* tmaps = lay.tmaps;
+    int* tile_off = lay.tile_off;
+    prefill::WorkItem* items = lay.items;
+    const long long capacity = lay.item_capacity;
 
     // Tensor-map templates: row extents are placeholders (one box), patched on the
     // device from q_indptr[batch] / kv_indptr[batch] by the plan kernel.
@@ -361,8 +425,7 @@ int pgqa_ragged_prefill_bf16(const void* q, const void* k, const void* v, void* 
     pp.items = items;
     pp.item_capacity = capacity;
     pp.tm_out = tmaps;
-    cudaError_t e = prefill::launch_plan(pp, tq, tk, tv, s);
-    if (e != cudaSuccess) return PGQA_ERR_CUDA;
+    cudaError_t e;
 
     prefill::Params p;
     p.tm_q = tmaps + 0;
@@ -384,9 +447,13 @@ int pgqa_ragged_prefill_bf16(const void* q, const void* k, const void* v, void* 
     p.page_table_stride = 0;
     p.page_size = 0;
     p.num_pages = 0;
+    fill_split(pp, p, lay, batch, head_dim, num_qo_heads, st->num_sms);
+    e = prefill::launch_plan(pp, tq, tk, tv, s);
+    if (e != cudaSuccess) return PGQA_ERR_CUDA;
     e = head_dim == 128 ? prefill::launch_attention_pair<false>(p, st->num_sms, s)
                         : prefill::launch_attention<256, false>(p, st->num_sms, s);
-    return map_cuda(e);
+    if (e != cudaSuccess) return PGQA_ERR_CUDA;
+    return head_dim == 128 ? map_cuda(prefill::launch_merge(p, st->num_sms, s)) : PGQA_OK;
 }
 
 int pgqa_paged_prefill_bf16(const void* q, const void* k_pages, const void* v_pages, void* o,
@@ -439,21 +506,16 @@ int pgqa_paged_prefill_bf16_strided(const void* q, const void* k_pages, const vo
     if (rc != PGQA_OK) return rc;
     if ((rc = get_encoder()) != PGQA_OK) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const size_t kvoff_bytes = align_up((size_t)(batch + 1) * sizeof(int), 256);
-    rc = ensure_workspace(*st, prefill_ws_bytes(batch, 4096) + kvoff_bytes, s);
+    rc = ensure_workspace(*st, prefill_ws_bytes(batch, 4096), s);
     if (rc != PGQA_OK) return rc;
 
-    uint8_t* ws = static_cast<uint8_t*>(st->ws);
-    WsHeader* hdr = reinterpret_cast<WsHeader*>(ws + kWsHeader);
-    CUtensorMap* tmaps = reinterpret_cast<CUtensorMap*>(ws + kWsTmapOffset);
-    int* tile_off = reinterpret_cast<int*>(ws + kWsArrays);
-    int* kv_off = reinterpret_cast<int*>(ws + kWsArrays +
-                                         align_up((size_t)(batch + 1) * sizeof(int), 256));
-    const size_t items_off = kWsArrays + align_up((size_t)(batch + 1) * sizeof(int), 256) +
-                             kvoff_bytes;
-    prefill::WorkItem* items = reinterpret_cast<prefill::WorkItem*>(ws + items_off);
-    const long long capacity =
-        (long long)((st->ws_bytes - items_off) / sizeof(prefill::WorkItem));
+    const PrefillWs lay = prefill_layout(*st, batch, head_dim);
+    WsHeader* hdr = lay.hdr;
+    CUtensorMap* tmaps = lay.tmaps;
+    int* tile_off = lay.tile_off;
+    int* kv_off = lay.kv_off;
+    prefill::WorkItem* items = lay.items;
+    const long long capacity = lay.item_capacity;
 
     // Q as for the ragged call (row extent patched on the device); K/V as 4-D page pools
     // {d, slot, head, page}, one box = one page of one head and one 64-column chunk.
@@ -485,8 +547,7 @@ int pgqa_paged_prefill_bf16_strided(const void* q, const void* k_pages, const vo
     pp.items = items;
     pp.item_capacity = capacity;
     pp.tm_out = tmaps;
-    cudaError_t e = prefill::launch_plan(pp, tq, tk, tv, s);
-    if (e != cudaSuccess) return PGQA_ERR_CUDA;
+    cudaError_t e;
 
     prefill::Params p;
     p.tm_q = tmaps + 0;
@@ -508,9 +569,13 @@ int pgqa_paged_prefill_bf16_strided(const void* q, const void* k_pages, const vo
     p.page_table_stride = page_table_stride;
     p.page_size = page_size;
     p.num_pages = num_pages;
+    fill_split(pp, p, lay, batch, head_dim, num_qo_heads, st->num_sms);
+    e = prefill::launch_plan(pp, tq, tk, tv, s);
+    if (e != cudaSuccess) return PGQA_ERR_CUDA;
     e = head_dim == 128 ? prefill::launch_attention_pair<true>(p, st->num_sms, s)
                         : prefill::launch_attention<256, true>(p, st->num_sms, s);
-    return map_cuda(e);
+    if (e != cudaSuccess) return PGQA_ERR_CUDA;
+    return head_dim == 128 ? map_cuda(prefill::launch_merge(p, st->num_sms, s)) : PGQA_OK;
 }
 
 int pgqa_paged_decode_bf16(const void* q, const void* k_pages, const void* v_pages,

@@ -35,7 +35,8 @@ struct WsHeader {
     int n_items;      // prefill: number of work items written by the plan
     int total_q;
     int total_kv;
-    int pad[60];
+    int merge_rows;   // prefill: (token, head) rows the split-KV merge combines
+    int pad[59];
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -50,12 +51,17 @@ constexpr int PLAN_THREADS = 1024;
 constexpr int COST_BUCKETS = 4096;
 constexpr int PLAN_SMEM_BATCH = 2048;  // batches up to this size plan out of shared memory
 
-// One work item of the prefill: a (request, kv head, first q tile) triple plus the
+constexpr int SPLIT_TILES = 16;   // K/V tiles (2048 keys) per chunk of a split request
+
+// One work item of the prefill: a (request, kv head, first q tile, K/V chunk) plus the
 // request's offsets, written by the plan kernel so the attention roles need no further
-// global loads to place it.
+// global loads to place it.  An item covers K/V tiles [kt0, kt1) of its q tiles' range;
+// part < 0: it writes the outputs; part >= 0: it writes fp32 partial results to partial
+// rows part + t * Hq + h (t = token within the request), merged afterwards.
 struct alignas(16) WorkItem {
     int b, g, qt, cost;
     int q_start, qo_len, kv_start, kv_len;
+    int kt0, kt1, part, nch;
 };
 
 struct Params {
@@ -82,6 +88,15 @@ struct Params {
     int page_table_stride;
     int page_size;             // 16, 32, 64 or 128
     int num_pages;
+    // split-KV partial results: o [rows, D] fp32 normalised over the chunk's keys, lse
+    // [rows] fp32 (natural log); merge bookkeeping from the plan
+    float* part_o;
+    float* part_lse;
+    const int* merge_off;      // [batch + 1] first merge row of each request
+    const int* part_off;       // [batch] first partial row of each request (-1: not split)
+    const int* nch;            // [batch] chunks of each request
+    const int* kvl;            // [batch] keys of each request
+    int batch;
 };
 
 struct PlanParams {
@@ -100,6 +115,17 @@ struct PlanParams {
     WorkItem* items;
     long long item_capacity;
     CUtensorMap* tm_out;       // 3 maps: Q, K, V
+    // split-KV: allowed when split_ok; chosen when the work list would have fewer than
+    // 2 * num_ctas items and the partial results fit in part_capacity rows
+    int split_ok;
+    int num_ctas;
+    int num_qo_heads;
+    long long part_capacity;
+    int* unit_off;             // [batch + 1] (q item, chunk) units per request
+    int* part_off;             // [batch]
+    int* merge_off;            // [batch + 1]
+    int* nch;                  // [batch]
+    int* kvl;                  // [batch] keys per request (for the merge)
 };
 }  // namespace prefill
 

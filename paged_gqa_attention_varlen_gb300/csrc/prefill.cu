@@ -68,11 +68,18 @@ __device__ __forceinline__ Geo geo_of(const WorkItem& w, int dt, int group, int 
 
 __device__ __forceinline__ WorkItem load_item(const WorkItem* items, int i) {
     const int4* v = reinterpret_cast<const int4*>(items + i);
-    const int4 a = __ldg(v), c = __ldg(v + 1);
+    const int4 a = __ldg(v), c = __ldg(v + 1), e = __ldg(v + 2);
     WorkItem w;
     w.b = a.x; w.g = a.y; w.qt = a.z; w.cost = a.w;
     w.q_start = c.x; w.qo_len = c.y; w.kv_start = c.z; w.kv_len = c.w;
+    w.kt0 = e.x; w.kt1 = e.y; w.part = e.z; w.nch = e.w;
     return w;
+}
+
+// K/V chunks of a request of kv_len keys when its work is split
+__host__ __device__ __forceinline__ int split_chunks(int kv_len) {
+    const int tiles = (kv_len + BN - 1) / BN;
+    return tiles > SPLIT_TILES ? (tiles + SPLIT_TILES - 1) / SPLIT_TILES : 1;
 }
 
 __device__ __forceinline__ void prefetch_l1(const void* ptr) {
@@ -226,8 +233,63 @@ __global__ void __launch_bounds__(PLAN_THREADS)
         running += tot;
     }
     const int total_tiles = running;
-    const long long n_items = (long long)total_tiles * p.num_kv_heads;
     if (tid == 0) toff[p.batch] = total_tiles;
+
+    // Split-KV: a work list too short to fill the grid (decode-like calls: few requests,
+    // few query rows, long keys) has its requests cut into chunks of SPLIT_TILES K/V tiles.
+    // The cut depends on the request alone, so within this regime a request's results do
+    // not depend on the batch.  Units are (q item, chunk); chunked requests write fp32
+    // partial results that the merge kernel combines.  If the partial results would not
+    // fit in the workspace the work is not split.
+    bool split = p.split_ok && (long long)total_tiles * p.num_kv_heads < 2LL * p.num_ctas;
+    long long part_total = 0;
+    int merge_total = 0, unit_total = total_tiles;
+    if (split) {
+        int unit_run = 0, merge_run = 0;
+        for (int base = 0; base < p.batch; base += nthr) {
+            const int b = base + tid;
+            int units = 0, prow = 0, mrow = 0, nc = 1;
+            if (b < p.batch) {
+                const int qo = qi[b + 1] - qi[b];
+                const int tiles = (int)(((long long)qo * p.group + BM - 1) / BM);
+                const int qitems = (tiles + p.tiles_per_item - 1) / p.tiles_per_item;
+                nc = qo > 0 ? split_chunks(ki[b + 1] - ki[b]) : 1;
+                units = qitems * nc;
+                if (nc > 1) {
+                    prow = nc * qo * p.num_qo_heads;
+                    mrow = qo * p.num_qo_heads;
+                }
+            }
+            int tot_u, tot_p, tot_m;
+            const int inc_u = block_inclusive_scan(units, scan, &tot_u);
+            const int inc_p = block_inclusive_scan(prow, scan, &tot_p);
+            const int inc_m = block_inclusive_scan(mrow, scan, &tot_m);
+            if (b < p.batch) {
+                p.unit_off[b] = unit_run + inc_u - units;
+                p.part_off[b] = nc > 1 ? (int)(part_total + inc_p - prow) : -1;
+                p.merge_off[b] = merge_run + inc_m - mrow;
+                p.nch[b] = nc;
+                p.kvl[b] = ki[b + 1] - ki[b];
+            }
+            unit_run += tot_u;
+            part_total += tot_p;
+            merge_run += tot_m;
+        }
+        if (tid == 0) {
+            p.unit_off[p.batch] = unit_run;
+            p.merge_off[p.batch] = merge_run;
+        }
+        unit_total = unit_run;
+        merge_total = merge_run;
+        if (part_total > p.part_capacity) split = false;  // the same in every thread
+        __syncthreads();
+    }
+    if (!split) {
+        unit_total = total_tiles;
+        merge_total = 0;
+    }
+    const int* uoff = split ? p.unit_off : toff;
+    const long long n_items = (long long)unit_total * p.num_kv_heads;
     if (n_items > p.item_capacity) {
         if (tid == 0) {
             atomicOr(&p.hdr->status, PGQA_DEV_CAPACITY);
@@ -238,11 +300,22 @@ __global__ void __launch_bounds__(PLAN_THREADS)
     for (int i = tid; i < COST_BUCKETS; i += nthr) hist[i] = 0;
     __syncthreads();
 
-    // histogram of item costs (K/V tiles of the item's longest q tile)
-    for (int f = tid; f < total_tiles; f += nthr) {
-        const int b = find_segment(toff, p.batch, f);
-        const int qt = (f - toff[b]) * p.tiles_per_item;
-        atomicAdd(&hist[min(item_cost(p, qi, ki, b, qt), COST_BUCKETS - 1)], 1);
+    // a unit: request b, q item qt, chunk c (0 when not split) and its K/V-tile cost
+    auto unit_of = [&](int f, int& b, int& qt, int& c, int& cost) {
+        b = find_segment(uoff, p.batch, f);
+        const int local = f - uoff[b];
+        const int nc = split ? p.nch[b] : 1;
+        qt = (local / nc) * p.tiles_per_item;
+        c = local % nc;
+        const int full = item_cost(p, qi, ki, b, qt);
+        cost = nc > 1 ? max(0, min(full - c * SPLIT_TILES, SPLIT_TILES)) : full;
+    };
+
+    // histogram of unit costs (K/V tiles of the unit's longest q tile)
+    for (int f = tid; f < unit_total; f += nthr) {
+        int b, qt, c, cost;
+        unit_of(f, b, qt, c, cost);
+        atomicAdd(&hist[min(cost, COST_BUCKETS - 1)], 1);
     }
     __syncthreads();
 
@@ -269,13 +342,13 @@ __global__ void __launch_bounds__(PLAN_THREADS)
     }
     __syncthreads();
 
-    // scatter: the kv heads of one q tile take consecutive slots
-    for (int f = tid; f < total_tiles; f += nthr) {
-        const int b = find_segment(toff, p.batch, f);
-        const int qt = (f - toff[b]) * p.tiles_per_item;
-        const int cost = item_cost(p, qi, ki, b, qt);
+    // scatter: the kv heads of one unit take consecutive slots
+    for (int f = tid; f < unit_total; f += nthr) {
+        int b, qt, c, cost;
+        unit_of(f, b, qt, c, cost);
         const int slot = atomicAdd(&hist[min(cost, COST_BUCKETS - 1)], 1);
         const int q0 = qi[b], k0 = ki[b];
+        const int nc = split ? p.nch[b] : 1;
         WorkItem w;
         w.b = b;
         w.qt = qt;
@@ -284,6 +357,10 @@ __global__ void __launch_bounds__(PLAN_THREADS)
         w.qo_len = qi[b + 1] - q0;
         w.kv_start = k0;
         w.kv_len = ki[b + 1] - k0;
+        w.kt0 = nc > 1 ? c * SPLIT_TILES : 0;
+        w.kt1 = nc > 1 ? (c + 1) * SPLIT_TILES : 0x7fffffff;
+        w.part = nc > 1 ? p.part_off[b] + c * w.qo_len * p.num_qo_heads : -1;
+        w.nch = nc;
         for (int g = 0; g < p.num_kv_heads; ++g) {
             w.g = g;
             p.items[(long long)slot * p.num_kv_heads + g] = w;
@@ -306,6 +383,7 @@ __global__ void __launch_bounds__(PLAN_THREADS)
             p.hdr->n_items = (int)n_items;
             p.hdr->total_q = total_q;
             p.hdr->total_kv = total_kv;
+            p.hdr->merge_rows = merge_total;
         }
         __syncwarp();
         tensormap_publish(p.tm_out + 0, smem_u32(&smap[0]));
@@ -826,6 +904,11 @@ struct PairCfg {
 constexpr float kRescaleThreshold = 8.0f;
 
 
+// K/V tiles this item covers for a q tile of geometry x: [kt0, kt0 + n)
+__device__ __forceinline__ int item_tiles(const WorkItem& w, const Geo& x) {
+    return max(0, min(w.kt1, x.n_tiles) - w.kt0);
+}
+
 template <bool PAGED>
 __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const Params p) {
     using C = PairCfg;
@@ -920,11 +1003,12 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
                 if (it >= 0) prefetch_l1(p.items + it);
                 const Geo a = geo_of(w, 0, G, p.causal);
                 const Geo bq = geo_of(w, 1, G, p.causal);
-                const int nA = a.n_tiles;
-                const int nB = bq.t0 < bq.qo_len ? bq.n_tiles : 0;
+                const int nA = item_tiles(w, a);
+                const int nB = bq.t0 < bq.qo_len ? item_tiles(w, bq) : 0;
                 const int nmax = max(nA, nB);
                 if (nmax == 0) continue;
                 const int lx = nB > 0 ? 1 : 0;  // tile whose MMAs close every step
+                const int kt0 = w.kt0;          // first K/V tile of the item
                 ok = wait(BAR(Q_EMPTY), (q_count & 1) ^ 1);
                 if (!ok) break;
                 if (lane == 0) {
@@ -945,7 +1029,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
                 const int* pt_row = PAGED ? p.page_table + (size_t)w.b * p.page_table_stride : nullptr;
                 const int npg = PAGED ? (a.kv_len + ps - 1) / ps : 0;
                 // paged: this lane's page of K_t (read a step ahead) and of K_{t-1} (= V_{t-1})
-                int kid = PAGED ? lane_page_id(pt_row, 0, ppt, npg, lane) : -1;
+                int kid = PAGED ? lane_page_id(pt_row, kt0, ppt, npg, lane) : -1;
                 int vid = -1;
                 bool v_ok = false;
                 for (int t = 0; t <= nmax; ++t, ++step) {
@@ -965,28 +1049,29 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
                     const uint32_t vst = (L0 + 2 * (t - 1) + 1) % C::STAGES;
                     const uint32_t kst = (L0 + 2 * t) % C::STAGES;
                     if constexpr (PAGED) {
-                        const bool k_ok =
-                            t < nmax && lane_page_ok(kid, t, ppt, npg, p.num_pages, lane, p.status);
+                        const bool k_ok = t < nmax && lane_page_ok(kid, kt0 + t, ppt, npg,
+                                                                   p.num_pages, lane, p.status);
                         issue_page_boxes<C::CHUNKS, C::CHUNK_BYTES>(
                             bar, ps, w.g, lane, t >= 1 && v_ok, sKV + vst * C::TILE_BYTES, p.tm_v,
                             vid, k_ok, sKV + kst * C::TILE_BYTES, p.tm_k, kid);
-                        if (lane == 0 && t == nmax && nmax * BN > a.kv_len) mbar_arrive(BAR(FIX_READY));
+                        if (lane == 0 && t == nmax && (kt0 + nmax) * BN > a.kv_len)
+                            mbar_arrive(BAR(FIX_READY));
                         vid = kid;
                         v_ok = k_ok;
-                        if (t + 1 < nmax) kid = lane_page_id(pt_row, t + 1, ppt, npg, lane);
+                        if (t + 1 < nmax) kid = lane_page_id(pt_row, kt0 + t + 1, ppt, npg, lane);
                     } else {
                         mbar_arrive_expect_tx(bar, C::TILE_BYTES * ((t >= 1) + (t < nmax)));
                         if (t >= 1) {  // V_{t-1}
 #pragma unroll
                             for (int c = 0; c < C::CHUNKS; ++c)
                                 tma_load_2d(sKV + vst * C::TILE_BYTES + c * C::CHUNK_BYTES, p.tm_v,
-                                            bar, w.g * D + c * 64, a.kv_start + (t - 1) * BN);
+                                            bar, w.g * D + c * 64, a.kv_start + (kt0 + t - 1) * BN);
                         }
                         if (t < nmax) {  // K_t
 #pragma unroll
                             for (int c = 0; c < C::CHUNKS; ++c)
                                 tma_load_2d(sKV + kst * C::TILE_BYTES + c * C::CHUNK_BYTES, p.tm_k,
-                                            bar, w.g * D + c * 64, a.kv_start + t * BN);
+                                            bar, w.g * D + c * 64, a.kv_start + (kt0 + t) * BN);
                         }
                     }
                 }
@@ -1025,14 +1110,14 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
                 if (it >= 0) prefetch_l1(p.items + it);
                 const Geo a = geo_of(w, 0, G, p.causal);
                 const Geo bq = geo_of(w, 1, G, p.causal);
-                const int nx[2] = {a.n_tiles, bq.t0 < bq.qo_len ? bq.n_tiles : 0};
+                const int nx[2] = {item_tiles(w, a), bq.t0 < bq.qo_len ? item_tiles(w, bq) : 0};
                 const int nmax = max(nx[0], nx[1]);
                 if (nmax == 0) continue;
                 ok = mbar_wait_bounded(BAR(Q_FULL), q_count & 1, abort_flag, p.status);
                 ++q_count;
                 if (!ok) break;
                 const uint32_t L0 = load_idx;
-                const bool fix = PAGED && nmax * BN > a.kv_len;
+                const bool fix = PAGED && (w.kt0 + nmax) * BN > a.kv_len;
                 for (int t = 0; t <= nmax; ++t, ++step) {
                     if (fix && t == nmax) {  // the last V tile, its tail rows zeroed
                         ok = mbar_wait_bounded(BAR(V_FIXED), fixes & 1, abort_flag, p.status);
@@ -1103,13 +1188,14 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
             it = snake_next(rr, n_items);
             const Geo a = geo_of(w, 0, G, p.causal);
             const Geo bq = geo_of(w, 1, G, p.causal);
-            const int nmax = max(a.n_tiles, bq.t0 < bq.qo_len ? bq.n_tiles : 0);
+            const int nmax = max(item_tiles(w, a), bq.t0 < bq.qo_len ? item_tiles(w, bq) : 0);
             if (nmax == 0) continue;
             const uint32_t L0 = load_idx;
             const uint32_t fin = step + (uint32_t)nmax;  // the item's last step: V_{nmax-1}
             step += (uint32_t)nmax + 1;
             load_idx = L0 + 2 * (uint32_t)nmax;
-            if (nmax * BN <= a.kv_len) continue;
+            const int last = w.kt0 + nmax - 1;           // absolute index of that V tile
+            if ((last + 1) * BN <= a.kv_len) continue;
             ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(FIX_READY), fixes & 1, abort_flag,
                                                            p.status));
             if (ok)
@@ -1120,7 +1206,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
             ++fixes;
             const uint32_t st = (L0 + 2 * (uint32_t)(nmax - 1) + 1) % C::STAGES;
             zero_stage_rows<C::CHUNKS, C::CHUNK_BYTES>(sKV + st * C::TILE_BYTES,
-                                                       a.kv_len - (nmax - 1) * BN, lane);
+                                                       a.kv_len - last * BN, lane);
             mbar_arrive(BAR(V_FIXED));
         }
     } else if (warp >= 4) {
@@ -1139,10 +1225,11 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
         const bool fast_scale = p.scale_log2 > 0.f;
         const float c_eff = fast_scale ? p.scale_log2 : 1.f;
         uint32_t ctr = 0, items_done = 0;
-        // the item whose epilogue is pending
+        // the item whose epilogue is pending (pend_slot >= 0: a partial-result row)
         bool pend = false, pend_valid = false;
         float pend_l = 0.f, pend_m = 0.f;
         size_t pend_row = 0;
+        long long pend_slot = -1;
         // Wait for the pending item's last P.V and read its O row out of tensor memory.
         auto read_pending = [&](uint32_t (&u)[4][32]) -> bool {
             const bool okw = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(PV_DONE + X),
@@ -1160,6 +1247,20 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
         auto store_pending = [&](const uint32_t (&u)[4][32]) {
             if (!pend_valid) return;
             const float inv_l = pend_l > 0.f ? 1.f / pend_l : 0.f;
+            if (pend_slot >= 0) {  // split-KV partial: O / l in fp32 and the chunk's lse
+                float4* op = reinterpret_cast<float4*>(p.part_o + pend_slot * D);
+#pragma unroll
+                for (int cc = 0; cc < D / 32; ++cc)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        op[cc * 8 + e] = make_float4(__uint_as_float(u[cc][4 * e]) * inv_l,
+                                                     __uint_as_float(u[cc][4 * e + 1]) * inv_l,
+                                                     __uint_as_float(u[cc][4 * e + 2]) * inv_l,
+                                                     __uint_as_float(u[cc][4 * e + 3]) * inv_l);
+                p.part_lse[pend_slot] =
+                    pend_l > 0.f ? (pend_m + log2f(pend_l)) * 0.69314718055994531f : -INFINITY;
+                return;
+            }
             uint4* op = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + pend_row * D);
 #pragma unroll
             for (int cc = 0; cc < D / 32; ++cc) {
@@ -1195,8 +1296,11 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
             const int row_h = w.g * G + r % G;
             const bool valid = row_t < x.qo_len;
             const size_t out_row = (size_t)(x.q_start + row_t) * Hq + row_h;
-            if (x.n_tiles == 0) {
-                if (valid) {
+            const int nt = item_tiles(w, x);
+            if (nt == 0) {
+                // no visible key: zeros (a chunk of a split request without keys for this
+                // tile writes nothing; the merge leaves that chunk out)
+                if (valid && w.part < 0) {
                     uint4* op = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) +
                                                          out_row * D);
 #pragma unroll
@@ -1208,8 +1312,9 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
             const int klim = p.causal ? min(row_t + x.kv_len - x.qo_len, x.kv_len - 1)
                                       : x.kv_len - 1;
             float m_used = -INFINITY, l = 0.f;
-            for (int j = 0; j < x.n_tiles; ++j) {
-                const uint32_t c = ctr + j;
+            for (int jr = 0; jr < nt; ++jr) {
+                const int j = w.kt0 + jr;  // absolute K/V tile (masking); jr: within the item
+                const uint32_t c = ctr + jr;
                 ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(S_FULL + 2 * X + (c & 1)),
                                                                (c >> 1) & 1, abort_flag,
                                                                p.status));
@@ -1274,7 +1379,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
                 l = l * alpha + ((a0 + a1) + (a2 + a3));
                 // O may be rescaled now: S_FULL of this tile was committed after the previous
                 // P.V by the same issuing thread, so that P.V has completed
-                if (j > 0) {
+                if (jr > 0) {
                     if (__any_sync(0xffffffffu, grow)) {
 #pragma unroll 1
                         for (int cc = 0; cc < D / 32; ++cc) {
@@ -1312,12 +1417,13 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
                 m_used = m_new;
             }
             if (!ok) break;
-            ctr += x.n_tiles;
+            ctr += nt;
             pend = true;
             pend_valid = valid;
             pend_l = l;
             pend_m = m_used;
             pend_row = out_row;
+            pend_slot = w.part >= 0 ? (long long)w.part + (long long)row_t * Hq + row_h : -1;
         }
         if (ok && pend) {
             uint32_t u[4][32];
@@ -1331,6 +1437,60 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem_base, 512);
+    }
+}
+
+// ------------------------------------------------------------ split-KV merge
+// One warp per (token, query head) row of a split request: the chunks that hold keys
+// visible to the row are combined with weights exp(lse_c - max lse) (FlashInfer
+// documentation, flashinfer.cascade "Merge Attention States").  Rows without a visible key
+// get zeros and lse = -inf.
+__global__ void __launch_bounds__(256) merge_kernel(const Params p) {
+    constexpr int D = 128;
+    // launched as a dependent of the attention kernel: its partial results are read from here
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int rows = p.hdr->merge_rows;
+    const int Hq = p.num_qo_heads;
+    const int lane = threadIdx.x & 31;
+    for (long long m = (long long)blockIdx.x * 8 + (threadIdx.x >> 5); m < rows;
+         m += (long long)gridDim.x * 8) {
+        const int b = find_segment(p.merge_off, p.batch, (int)m);
+        const int local = (int)m - __ldg(p.merge_off + b);
+        const int t = local / Hq, h = local % Hq;
+        const int q0 = __ldg(p.q_indptr + b);
+        const int qo = __ldg(p.q_indptr + b + 1) - q0;
+        const int kv = __ldg(p.kvl + b);
+        const int nc = __ldg(p.nch + b);
+        const int nkeys = p.causal ? max(0, min(kv, t + kv - qo + 1)) : kv;
+        const int nvis = min(nc, (nkeys + SPLIT_TILES * BN - 1) / (SPLIT_TILES * BN));
+        const long long base = __ldg(p.part_off + b);
+        auto slot = [&](int c) { return base + ((long long)c * qo + t) * Hq + h; };
+        float mx = -INFINITY;
+        for (int c = lane; c < nvis; c += 32) mx = fmaxf(mx, p.part_lse[slot(c)]);
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float wsum = 0.f;
+        if (mx != -INFINITY) {
+            for (int c = 0; c < nvis; ++c) {
+                const long long sl = slot(c);
+                const float wgt = __expf(p.part_lse[sl] - mx);
+                const float4 v = *reinterpret_cast<const float4*>(p.part_o + sl * D + lane * 4);
+                wsum += wgt;
+                acc.x = fmaf(wgt, v.x, acc.x);
+                acc.y = fmaf(wgt, v.y, acc.y);
+                acc.z = fmaf(wgt, v.z, acc.z);
+                acc.w = fmaf(wgt, v.w, acc.w);
+            }
+        }
+        const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+        __nv_bfloat16* op = reinterpret_cast<__nv_bfloat16*>(p.o) + ((size_t)(q0 + t) * Hq + h) * D;
+        uint2 u;
+        u.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+        u.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+        *reinterpret_cast<uint2*>(op + lane * 4) = u;
+        if (lane == 0 && p.lse)
+            p.lse[(size_t)(q0 + t) * Hq + h] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
     }
 }
 
@@ -1383,6 +1543,10 @@ cudaError_t launch_attention_pair(const Params& p, int grid, cudaStream_t stream
     }
     return launch_dependent(attention_pair_kernel<PAGED>, grid, PAIR_THREADS, PairCfg::SMEM_BYTES,
                             stream, p);
+}
+
+cudaError_t launch_merge(const Params& p, int num_sms, cudaStream_t stream) {
+    return launch_dependent(merge_kernel, num_sms * 2, 256, 0, stream, p);
 }
 
 cudaError_t launch_plan(const PlanParams& pp, const CUtensorMap& tq, const CUtensorMap& tk,

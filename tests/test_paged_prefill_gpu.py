@@ -178,3 +178,43 @@ def test_bad_page_id_reports_bounds_status(cuda_lib):
     pc.page_table[0, 3] = 0
     run_gpu(cuda_lib, pc)
     assert cuda_lib.device_status() == 0
+
+
+# ---------------------------------------------------------------- split-KV (short work lists)
+# A work list shorter than two items per SM has its requests cut into chunks of 2048 keys;
+# the chunks' partial results are merged by their LSE weights (FlashInfer documentation,
+# flashinfer.cascade "Merge Attention States").
+
+@pytest.mark.parametrize("batch", [1, 4])
+def test_split_kv_multi_token_decode_long_context(cuda_lib, batch):
+    kv = [32768 - 77 * b for b in range(batch)]
+    pc = W.paged_case(kv, 32, 8, 128, page_size=16, qo_lens=[4] * batch, seed=101 + batch,
+                      device="cuda")
+    full_check(cuda_lib, pc, f"split-KV 4-token decode, batch {batch}")
+
+
+def test_split_kv_ragged_long_prefix_prefill(cuda_lib):
+    """One request, 300 query rows over 20000 keys, 8 query heads on one kv head: 10
+    q-tile items cut into 10 chunks each; causal masking across chunk boundaries."""
+    case = W.ragged_case([300], [20000], 8, 1, 128, causal=True, seed=103, device="cuda")
+    o, lse = cuda_lib.ragged_prefill(case.q, case.k, case.v, case.q_indptr, case.kv_indptr)
+    torch.cuda.synchronize()
+    assert cuda_lib.device_status() == 0
+    rows = sample_prefill_rows([300], 8, 8, seed=7, per_request_random=40)
+    og, lg = gather_rows(o, lse, rows, 8)
+    ro, rl = oracle.ragged_attention(case.q, case.k, case.v, case.q_indptr, case.kv_indptr, 8, 1,
+                                     True, case.sm_scale, rows=rows)
+    check_rows(og, lg, ro, rl, "split-KV ragged prefill")
+
+
+def test_split_kv_non_causal_and_short_requests(cuda_lib):
+    """Split regime with a mix: non-causal long request, requests shorter than a chunk, an
+    empty request, and a request with fewer keys than queries."""
+    qo = [7, 3, 0, 40, 1]
+    kv = [9000, 100, 500, 20, 4100]
+    pc = W.paged_case(kv, 16, 4, 128, page_size=32, qo_lens=qo, causal=False, seed=107,
+                      device="cuda")
+    full_check(cuda_lib, pc, "split-KV non-causal mix")
+    pc2 = W.paged_case(kv, 16, 4, 128, page_size=32, qo_lens=qo, causal=True, seed=107,
+                       device="cuda")
+    full_check(cuda_lib, pc2, "split-KV causal mix")
