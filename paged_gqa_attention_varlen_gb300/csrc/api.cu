@@ -248,11 +248,10 @@ void fill_split(prefill::PlanParams& pp, prefill::Params& p, const PrefillWs& w,
     p.batch = batch;
 }
 
-size_t decode_ws_bytes(int batch, int stride, int page_size, int hq, int d) {
+size_t decode_ws_bytes(int batch, int stride, int page_size, int hq, int d, int hk) {
     const long long max_kv = (long long)stride * page_size;
-    const long long chunks_per_req =
-        max_kv > 0 ? (max_kv + decode::CHUNK - 1) / decode::CHUNK : 1;
-    const long long chunks = (long long)batch * chunks_per_req;
+    const long long chunks =
+        decode::total_chunks(batch, max_kv, decode::chunk_keys(batch, max_kv, hk));
     const size_t ints = align_up((size_t)(2 * batch + 1) * sizeof(int), 256);
     return kWsArrays + ints + align_up((size_t)chunks * hq * sizeof(float), 256) +
            (size_t)chunks * hq * d * sizeof(float);
@@ -303,7 +302,8 @@ size_t pgqa_workspace_bytes_decode(int batch, int page_table_stride, int page_si
     if (batch < 0 || page_table_stride < 0 || page_size <= 0 || num_qo_heads <= 0 ||
         head_dim <= 0)
         return 0;
-    return decode_ws_bytes(batch, page_table_stride, page_size, num_qo_heads, head_dim);
+    // an upper bound for any number of kv heads (one kv head gives the most chunks)
+    return decode_ws_bytes(batch, page_table_stride, page_size, num_qo_heads, head_dim, 1);
 }
 
 int pgqa_set_workspace(void* ptr, size_t bytes) {
@@ -657,7 +657,8 @@ int paged_decode_impl(const void* q, const void* k_pages, const void* v_pages,
     int rc = current_device(&dev, &st);
     if (rc != PGQA_OK) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const size_t need = decode_ws_bytes(batch, page_table_stride, page_size, num_qo_heads, head_dim);
+    const size_t need = decode_ws_bytes(batch, page_table_stride, page_size, num_qo_heads, head_dim,
+                                        num_kv_heads);
     rc = ensure_workspace(*st, need, s);
     if (rc != PGQA_OK) return rc;
 
@@ -667,8 +668,8 @@ int paged_decode_impl(const void* q, const void* k_pages, const void* v_pages,
     int* kv_eff = chunk_off + (batch + 1);
     const size_t lse_off = kWsArrays + align_up((size_t)(2 * batch + 1) * sizeof(int), 256);
     const long long max_kv = (long long)page_table_stride * page_size;
-    const long long chunks =
-        (long long)batch * (max_kv > 0 ? (max_kv + decode::CHUNK - 1) / decode::CHUNK : 1);
+    const int chunk = decode::chunk_keys(batch, max_kv, num_kv_heads);
+    const long long chunks = decode::total_chunks(batch, max_kv, chunk);
     float* part_lse = reinterpret_cast<float*>(ws + lse_off);
     float* part_o = reinterpret_cast<float*>(
         ws + lse_off + align_up((size_t)chunks * num_qo_heads * sizeof(float), 256));
@@ -680,6 +681,7 @@ int paged_decode_impl(const void* q, const void* k_pages, const void* v_pages,
     pp.status = &hdr->status;
     pp.batch = batch;
     pp.max_kv = (int)max_kv;
+    pp.chunk = chunk;
     cudaError_t e = decode::launch_plan(pp, s);
     if (e != cudaSuccess) return PGQA_ERR_CUDA;
 
@@ -704,6 +706,7 @@ int paged_decode_impl(const void* q, const void* k_pages, const void* v_pages,
     p.scale_log2 = sm_scale * 1.4426950408889634f * k_scale;
     p.v_scale = v_scale;
     p.chunk_capacity = chunks;
+    p.chunk = chunk;
     if (decode::prepare_page_maps(p, k_pages, v_pages, num_pages, num_kv_heads, page_size,
                                   page_stride, slot_stride, head_stride, kv8) != cudaSuccess)
         return PGQA_ERR_INVALID_ARG;

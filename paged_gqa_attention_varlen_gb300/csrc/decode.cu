@@ -13,9 +13,10 @@
 //
 // Design: the path is bound by HBM bandwidth (about 4 flops per KV byte), so it runs on
 // the CUDA cores, not the tensor cores.
-//  * plan_kernel: sanitises kv_lens and cuts each request into chunks of CHUNK keys.
-//    The cut depends on the request alone, so a request's result does not depend on
-//    what else is in the batch.
+//  * plan_kernel: sanitises kv_lens and cuts each request into chunks of `chunk` keys
+//    (1024, or 256 for calls with little work; chosen from the call's shape).  Within a
+//    regime the cut depends on the request alone, so a request's result does not depend
+//    on what else is in the batch.
 //  * decode_tma_kernel: one warp per (chunk, kv head).  Pages stream through a per-warp
 //    TMA ring in shared memory; the online softmax keeps a running max and sum per
 //    head.  A request with a single chunk writes its bf16 output directly; otherwise
@@ -42,7 +43,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(PlanParams p) {
                 n = 0;
             }
             p.kv_eff[b] = n;
-            cnt = n > 0 ? (n + CHUNK - 1) / CHUNK : 1;
+            cnt = n > 0 ? (n + p.chunk - 1) / p.chunk : 1;
         }
         scan[tid] = cnt;
         __syncthreads();
@@ -216,8 +217,8 @@ __global__ void __launch_bounds__(WARPS * 32, G >= 8 ? 2 : 3)
         const int c = f - __ldg(p.chunk_off + b);
         const int nch = __ldg(p.chunk_off + b + 1) - __ldg(p.chunk_off + b);
         const int kv_len = __ldg(p.kv_eff + b);
-        const int tok0 = c * CHUNK;
-        const int tok1 = min(kv_len, tok0 + CHUNK);
+        const int tok0 = c * p.chunk;
+        const int tok1 = min(kv_len, tok0 + p.chunk);
         const int page0 = tok0 / PAGE;  // first 16-token unit of the chunk
         const int np = (tok1 - tok0 + PAGE - 1) / PAGE;
         const int* pt_row = p.page_table + (size_t)b * p.page_table_stride;

@@ -132,8 +132,21 @@ struct PlanParams {
 // ------------------------------------------------------------------ decode
 namespace decode {
 constexpr int PAGE = 16;           // tokens per TMA unit (one box); pages hold 1, 2, 4 or 8
-constexpr int CHUNK = 1024;        // tokens per split-KV chunk (fixed: depends on nothing
-                                   // but the request, so results do not depend on the batch)
+constexpr int CHUNK = 1024;        // tokens per split-KV chunk
+constexpr int CHUNK_SMALL = 256;   // tokens per chunk when the work is short
+constexpr int SMALL_WORK = 512;    // (request, chunk, kv head) items below which it is
+
+// Keys per split-KV chunk.  Decided from the call's shape alone (batch, the page table's
+// key capacity, kv heads): calls with less work than about one wave of warps use shorter
+// chunks to spread over the GPU.  Within either regime a request's chunks depend on the
+// request alone, so its results do not depend on the other requests of the batch.
+inline int chunk_keys(int batch, long long max_kv, int num_kv_heads) {
+    const long long per_req = max_kv > 0 ? (max_kv + CHUNK - 1) / CHUNK : 1;
+    return (long long)batch * per_req * num_kv_heads < SMALL_WORK ? CHUNK_SMALL : CHUNK;
+}
+inline long long total_chunks(int batch, long long max_kv, int chunk) {
+    return (long long)batch * (max_kv > 0 ? (max_kv + chunk - 1) / chunk : 1);
+}
 constexpr int HEAD_DIM = 128;
 constexpr int WARPS = 4;           // warps per CTA, one work item per warp
 constexpr int STAGES = 2;          // pages in flight per warp (TMA ring in shared memory)
@@ -168,6 +181,7 @@ struct Params {
     float scale_log2;           // sm_scale * log2(e) (* k_scale for E4M3 K/V)
     float v_scale;              // output scale: 1 for bf16 K/V, v_scale for E4M3
     long long chunk_capacity;
+    int chunk;                  // keys per split-KV chunk (chunk_keys)
 };
 
 struct PlanParams {
@@ -177,6 +191,7 @@ struct PlanParams {
     int* status;
     int batch;
     int max_kv;                 // page_table_stride * page_size
+    int chunk;                  // keys per split-KV chunk
 };
 }  // namespace decode
 

@@ -52,10 +52,11 @@ Slot g_slots[kMaxDev];
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
 // Bytes of scratch a call with these sizes needs (same carving as the kernels use below).
-size_t scratch_needed(int batch, int stride, int page_size, int hq, int d, long long* chunks) {
+size_t scratch_needed(int batch, int stride, int page_size, int hq, int d, int hk,
+                      long long* chunks, int* chunk) {
     const long long max_kv = (long long)stride * page_size;
-    const long long per_req = max_kv > 0 ? (max_kv + decode::CHUNK - 1) / decode::CHUNK : 1;
-    *chunks = (long long)batch * per_req;
+    *chunk = decode::chunk_keys(batch, max_kv, hk);
+    *chunks = decode::total_chunks(batch, max_kv, *chunk);
     return kScratchHeader + round256((size_t)(2 * batch + 1) * sizeof(int)) +
            round256((size_t)*chunks * hq * sizeof(float)) + (size_t)*chunks * hq * d * sizeof(float);
 }
@@ -93,8 +94,9 @@ extern "C" int pgqa_paged_decode_bf16_noalloc(
 
     // Sizes beyond the fixed scratch are rejected before anything is enqueued.
     long long chunks = 0;
-    const size_t need =
-        scratch_needed(batch, page_table_stride, page_size, num_qo_heads, head_dim, &chunks);
+    int chunk = decode::CHUNK;
+    const size_t need = scratch_needed(batch, page_table_stride, page_size, num_qo_heads, head_dim,
+                                       num_kv_heads, &chunks, &chunk);
     if (need > kNoAllocScratchBytes) return PGQA_ERR_WORKSPACE;
 
     std::lock_guard<std::mutex> guard(g_lock);
@@ -146,6 +148,7 @@ extern "C" int pgqa_paged_decode_bf16_noalloc(
     pp.status = status;
     pp.batch = batch;
     pp.max_kv = page_table_stride * page_size;
+    pp.chunk = chunk;
     if (decode::launch_plan(pp, st) != cudaSuccess) return PGQA_ERR_CUDA;
 
     decode::Params p;
@@ -169,6 +172,7 @@ extern "C" int pgqa_paged_decode_bf16_noalloc(
     p.scale_log2 = sm_scale * 1.4426950408889634f;
     p.v_scale = 1.f;
     p.chunk_capacity = chunks;
+    p.chunk = chunk;
     if (decode::prepare_page_maps(p, k_pages, v_pages, num_pages, num_kv_heads, page_size,
                                   (long long)page_size * num_kv_heads * head_dim,
                                   (long long)num_kv_heads * head_dim, head_dim, false) != cudaSuccess)
