@@ -894,7 +894,7 @@ struct PairCfg {
     static constexpr int CHUNK_BYTES = BM * 128;
     static constexpr int TILE_BYTES = BM * D * 2;
     static constexpr int STAGES = 4;
-    static constexpr int NUM_BARS = 15;
+    static constexpr int NUM_BARS = 17;
     static constexpr int SMEM_BYTES = 1024 + TILE_BYTES * (2 + STAGES) + 8 * NUM_BARS + 16;
 };
 
@@ -938,10 +938,12 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
     // a NaN result even with P = 0.  The producer arrives on FIX_READY once it has issued
     // the loads of such a last step; warp 2 then waits for them, zeroes those V rows and
     // arrives on V_FIXED, which the MMA warp waits for instead of the step's STEP_FULL.
+    // P_LO[x]: the first half of tile x's P (keys 0..63) is in tensor memory; P_FULL[x]:
+    // all of it.  The MMA warp issues the P.V of each half as soon as that half is there.
     constexpr int Q_FULL = 0, Q_EMPTY = 1, STEP_FULL = 2, S_FULL = 4,
                   P_FULL = S_FULL + 4, PV_DONE = P_FULL + 2, MMA_DRAIN = PV_DONE + 2,
-                  FIX_READY = MMA_DRAIN + 1, V_FIXED = FIX_READY + 1;
-    static_assert(V_FIXED + 1 == C::NUM_BARS, "barrier count");
+                  FIX_READY = MMA_DRAIN + 1, V_FIXED = FIX_READY + 1, P_LO = V_FIXED + 1;
+    static_assert(P_LO + 2 == C::NUM_BARS, "barrier count");
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -953,6 +955,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
             mbar_init(BAR(S_FULL + 2 * x), 1);
             mbar_init(BAR(S_FULL + 2 * x + 1), 1);
             mbar_init(BAR(P_FULL + x), 128);
+            mbar_init(BAR(P_LO + x), 128);
             mbar_init(BAR(PV_DONE + x), 1);
         }
         mbar_init(BAR(MMA_DRAIN), 1);
@@ -1093,8 +1096,9 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
         // ------------------------------------------------------------ MMA issuer
         // Step t of an item: P.V of A's tile t-1, Q.K^T of A's tile t, then the same for B.
         // tcgen05.mma issue paces the tensor core, so this thread keeps its own waits and
-        // commits per step to a minimum: one wait for the step's K/V, one per P tile, and
-        // commits for S_A, S_B and the step (PV_DONE only after an item's last P.V).
+        // commits per step to a minimum: one wait for the step's K/V, two per P tile (one
+        // per half), and commits for S_A, S_B and the step (PV_DONE only after an item's
+        // last P.V).
         if (lane == 0) {
             constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, false);
             constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, true);
@@ -1134,20 +1138,25 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
                     for (int x = 0; x < 2; ++x) {
                         if (t >= 1 && t - 1 < nx[x]) {
                             const int jj = t - 1;
-                            // P_FULL of an item's first tile also says that the previous
+                            // P_LO of an item's first tile also says that the previous
                             // item's O has been read out, so this P.V may overwrite it
-                            ok = mbar_wait_bounded(BAR(P_FULL + x), (ctr[x] + jj) & 1, abort_flag,
-                                                   p.status);
-                            if (!ok) break;
-                            tc_fence_after();
                             // descriptor of a 16-key slice = base + byte offset / 16
                             const uint64_t vdesc =
                                 sdesc_sw128(sKV + vst * C::TILE_BYTES, C::CHUNK_BYTES, 1024);
+                            // P in two halves: keys 0..63 (P_LO), then 64..127 (P_FULL)
 #pragma unroll
-                            for (int k = 0; k < BN / 16; ++k)
-                                mma_ts(tmem_base + 256u + 128u * x, tmem_base + 128u * x + k * 8,
-                                       vdesc + (uint64_t)(k * 2048 / 16), IDESC_PV,
-                                       (jj > 0 || k > 0) ? 1u : 0u);
+                            for (int hf = 0; hf < 2; ++hf) {
+                                ok = mbar_wait_bounded(BAR((hf ? P_FULL : P_LO) + x),
+                                                       (ctr[x] + jj) & 1, abort_flag, p.status);
+                                if (!ok) break;
+                                tc_fence_after();
+#pragma unroll
+                                for (int k = hf * BN / 32; k < (hf + 1) * BN / 32; ++k)
+                                    mma_ts(tmem_base + 256u + 128u * x, tmem_base + 128u * x + k * 8,
+                                           vdesc + (uint64_t)(k * 2048 / 16), IDESC_PV,
+                                           (jj > 0 || k > 0) ? 1u : 0u);
+                            }
+                            if (!ok) break;
                             if (jj == nx[x] - 1) mma_commit(BAR(PV_DONE + x));
                         }
                         if (t < nx[x]) {
@@ -1358,6 +1367,11 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
                 const float neg = m_new == -INFINITY ? 0.f : -m_new;
                 const uint64_t c2 = f2_pack(c_eff, c_eff), n2 = f2_pack(neg, neg);
                 uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
+                // P leaves in two halves (P_LO: keys 0..63) so that the tensor core starts
+                // this tile's P.V while the second half is computed.  The first tile of an
+                // item with an epilogue pending releases both halves only after the
+                // previous O has been read out.
+                const bool early = jr > 0 || !pend;
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
                     uint32_t pk[32];
@@ -1372,47 +1386,49 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
                         pk[i] = pack_bf16x2(p0, p1);
                     }
                     tmem_st32(s_addr + cc * 32, pk);
+                    if (cc == 0 && early) {
+                        // O may be rescaled now: S_FULL of this tile was committed after the
+                        // previous P.V by the same issuing thread, so that P.V has completed
+                        if (jr > 0 && __any_sync(0xffffffffu, grow)) {
+#pragma unroll 1
+                            for (int oc = 0; oc < D / 32; ++oc) {
+                                uint32_t v[32];
+                                tmem_ld32(o_addr + oc * 32, v);
+                                tmem_wait_ld_regs(v);
+                                const uint64_t al2 = f2_pack(alpha, alpha);
+#pragma unroll
+                                for (int i = 0; i < 32; i += 2) {
+                                    float o0, o1;
+                                    f2_unpack(f2_mul(f2_pack(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), al2), o0, o1);
+                                    v[i] = __float_as_uint(o0);
+                                    v[i + 1] = __float_as_uint(o1);
+                                }
+                                tmem_st32(o_addr + oc * 32, v);
+                            }
+                        }
+                        tmem_wait_st();
+                        tc_fence_before();
+                        mbar_arrive(BAR(P_LO + X));
+                    }
                 }
                 float a0, a1, a2, a3;
                 f2_unpack(acc0, a0, a1);
                 f2_unpack(acc1, a2, a3);
                 l = l * alpha + ((a0 + a1) + (a2 + a3));
-                // O may be rescaled now: S_FULL of this tile was committed after the previous
-                // P.V by the same issuing thread, so that P.V has completed
-                if (jr > 0) {
-                    if (__any_sync(0xffffffffu, grow)) {
-#pragma unroll 1
-                        for (int cc = 0; cc < D / 32; ++cc) {
-                            uint32_t v[32];
-                            tmem_ld32(o_addr + cc * 32, v);
-                            tmem_wait_ld_regs(v);
-                            const uint64_t al2 = f2_pack(alpha, alpha);
-#pragma unroll
-                            for (int i = 0; i < 32; i += 2) {
-                                float o0, o1;
-                                f2_unpack(f2_mul(f2_pack(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), al2), o0, o1);
-                                v[i] = __float_as_uint(o0);
-                                v[i + 1] = __float_as_uint(o1);
-                            }
-                            tmem_st32(o_addr + cc * 32, v);
-                        }
-                    }
+                if (early) {
                     tmem_wait_st();
                     tc_fence_before();
                     mbar_arrive(BAR(P_FULL + X));
-                } else if (pend) {
+                } else {
                     // first tile of an item with an epilogue pending: read the previous O
                     // (its last P.V is done), release O and this tile's P, then store
                     ok = read_pending(u);
                     if (!ok) break;
                     tmem_wait_st();
                     tc_fence_before();
+                    mbar_arrive(BAR(P_LO + X));
                     mbar_arrive(BAR(P_FULL + X));
                     store_pending(u);
-                } else {
-                    tmem_wait_st();
-                    tc_fence_before();
-                    mbar_arrive(BAR(P_FULL + X));
                 }
                 m_used = m_new;
             }

@@ -118,8 +118,13 @@ def test_zero_length_rows_are_exact_zeros(cuda_lib):
     assert torch.all(torch.isneginf(l[0])) and torch.all(torch.isneginf(l[2]))
 
 
-def test_batch_composition_is_bitwise_invariant(cuda_lib):
-    pc = W.paged_case([3000, 64, 1025], 32, 8, 128, page_size=16, seed=23, device="cuda")
+@pytest.mark.parametrize("stride", [None, 4096])
+def test_batch_composition_is_bitwise_invariant(cuda_lib, stride):
+    """A 188-page table puts the batch and each single request under the 256-key chunking
+    (few work items); a 4096-page table (64k keys of capacity) puts both under the
+    1024-key chunking.  Within a regime a request's result does not depend on the batch."""
+    pc = W.paged_case([3000, 64, 1025], 32, 8, 128, page_size=16, seed=23, stride=stride,
+                      device="cuda")
     o, l = run_gpu(cuda_lib, pc)
     for b in range(3):
         sub_o, sub_l = cuda_lib.paged_decode(pc.q[b:b + 1].contiguous(), pc.k_pages, pc.v_pages,
