@@ -11,6 +11,8 @@ Printed (rank 0, one JSON line): value = prefill TFLOP/s (causal-visible pairs o
 carries its roofline against MEASURED_PEAKS.json.  `e2e` repeats the measurement with
 host-resident inputs copied in (pinned memory) and outputs copied out every step.
 `cpu_baseline` times the float64 oracle on a bounded row sample on the host cores.
+`median_ms_per_launch` gives the median over the timed steps; `cuda_graph` times the same
+two calls captured in CUDA graphs and replayed back to back (after the timed region).
 
 --impl reference times that oracle as the reference arm on the same workload and metric.
 Multi-GPU (torchrun): every rank runs the same per-GPU workload (requests are
@@ -255,13 +257,13 @@ def bench_gpu(args, ws, rank, local):
     l_dc = torch.empty(dc.q.shape[:2], dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def prefill():
+    def prefill(st=stream):
         api.ragged_prefill(pf.q, pf.k, pf.v, pf.q_indptr, pf.kv_indptr, causal=True,
-                           sm_scale=pf.sm_scale, out=o_pf, lse=l_pf, stream=stream)
+                           sm_scale=pf.sm_scale, out=o_pf, lse=l_pf, stream=st)
 
-    def decode():
+    def decode(st=stream):
         api.paged_decode(dc.q, dc.k_pages, dc.v_pages, dc.page_table, dc.kv_lens_t,
-                         sm_scale=dc.sm_scale, out=o_dc, lse=l_dc, stream=stream)
+                         sm_scale=dc.sm_scale, out=o_dc, lse=l_dc, stream=st)
 
     for _ in range(max(args.warmup, 3)):
         prefill()
@@ -350,6 +352,17 @@ def bench_gpu(args, ws, rank, local):
     d_e2e_ms = reduce_max(e0.elapsed_time(e1), dev)
     d_e2e_value = dc_bytes * ws * e2e_steps / (d_e2e_ms / 1e3) / 1e9
 
+    # the same calls replayed from CUDA graphs (after the timed region; reported beside it)
+    graph = None
+    if args.graph_reps > 0:
+        graph = {"prefill_ms_per_launch": graph_ms(prefill, dev, args.graph_reps),
+                 "decode_ms_per_launch": graph_ms(decode, dev, args.graph_reps),
+                 "reps": args.graph_reps}
+        graph["prefill_tflops"] = pf_flops / (graph["prefill_ms_per_launch"] / 1e3) / 1e12
+        graph["decode_gbs"] = dc_bytes / (graph["decode_ms_per_launch"] / 1e3) / 1e9
+        if api.device_status() != 0:
+            raise RuntimeError("device status after the graph replays is not ok")
+
     extra = None if args.no_extra else bench_extra(api, W, dev, stream, dc, peaks)
 
     if rank != 0:
@@ -404,6 +417,9 @@ def bench_gpu(args, ws, rank, local):
                     "d2h_bytes_per_step": d_d2h,
                     "note": "KV cache resident (serving state); q, page table, lengths in"}},
         "prefill_ms_per_launch": pf_launch_ms,
+        "median_ms_per_launch": {"prefill": statistics.median(pf_ms),
+                                 "decode": statistics.median(dc_ms)},
+        "cuda_graph": graph,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": args.steps * (3 + 3),
@@ -414,6 +430,31 @@ def bench_gpu(args, ws, rank, local):
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def graph_ms(fn, dev, reps):
+    """Milliseconds per call of fn(stream) captured once in a CUDA graph and replayed
+    `reps` times back to back between CUDA events."""
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        fn(side)  # a call on the capture stream first, as graph capture wants
+    torch.cuda.current_stream(dev).wait_stream(side)
+    with torch.cuda.graph(g):
+        fn(torch.cuda.current_stream(dev))
+    for _ in range(3):
+        g.replay()
+    st = torch.cuda.current_stream(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(st)
+    for _ in range(reps):
+        g.replay()
+    e1.record(st)
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) / reps
 
 
 def time_calls(fn, stream, reps=20, warmup=3):
@@ -535,12 +576,17 @@ def profile_case(args):
                               causal=True, sm_scale=c.sm_scale, out=o, lse=lse)
     else:  # decode slice: the first --decode-batch requests of the decode workload
         kv = W.config_lengths("decode")[1][:args.decode_batch]
-        c = W.paged_case(kv, 32, 8, 128, page_size=16, seed=0, device=dev)
+        if args.profile == "decode_e4m3":
+            c = W.paged_case_e4m3(kv, 32, 8, 128, page_size=16, seed=0, device=dev)
+            scales = dict(k_scale=c.meta["k_scale"], v_scale=c.meta["v_scale"])
+        else:
+            c = W.paged_case(kv, 32, 8, 128, page_size=16, seed=0, device=dev)
+            scales = {}
         o = torch.empty_like(c.q)
         lse = torch.empty(c.q.shape[:2], dtype=torch.float32, device=dev)
         for _ in range(args.reps):
             api.paged_decode(c.q, c.k_pages, c.v_pages, c.page_table, c.kv_lens_t,
-                             sm_scale=c.sm_scale, out=o, lse=lse)
+                             sm_scale=c.sm_scale, out=o, lse=lse, **scales)
     torch.cuda.synchronize(dev)
     st = api.device_status()
     print(json.dumps({"profile": args.profile, "reps": args.reps, "status": st,
@@ -560,11 +606,13 @@ def main(argv=None):
     ap.add_argument("--cpu-rows", type=int, default=800000,
                     help="oracle rows timed for the cpu_baseline object (about 10-30 s)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph-reps", type=int, default=20,
+                    help="CUDA-graph replays per kernel timed after the main region (0: skip)")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the paged-prefill and multi-token-decode measurements")
     ap.add_argument("--profile", choices=["prefill_hd128", "prefix_hd256", "long", "tiny",
                                           "decode", "paged_prefill_hd128", "paged_prefix_hd256",
-                                          "decode_q4"], default=None,
+                                          "decode_q4", "decode_e4m3"], default=None,
                     help="run one bounded case --reps times and exit (ncu captures)")
     ap.add_argument("--reps", type=int, default=4)
     ap.add_argument("--decode-batch", type=int, default=32)
