@@ -588,7 +588,11 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
                 };
                 const int* pt_row = PAGED ? p.page_table + (size_t)w.b * p.page_table_stride : nullptr;
                 const int npg = PAGED ? (x.kv_len + ps - 1) / ps : 0;
-                int pid = PAGED ? lane_page_id(pt_row, 0, ppt, npg, lane) : -1;  // load 0
+                // paged: K_j and V_j share tile j's pages.  This lane's page ids of the
+                // last two K tiles issued (V loads reuse them) and of the next K tile,
+                // whose read is started one K load ahead.
+                int id_next = PAGED ? lane_page_id(pt_row, 0, ppt, npg, lane) : -1;
+                int id_last = -1, id_prev = -1, k_last = -1;
                 for (int s = 0; s < nl; ++s) {
                     bool is_k;
                     const int j = tile_of(s, is_k);
@@ -597,16 +601,22 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
                     if (!ok) break;
                     const CUtensorMap* tm = is_k ? p.tm_k : p.tm_v;
                     if constexpr (PAGED) {
+                        int pid;
+                        if (is_k) {
+                            pid = id_next;
+                            id_prev = id_last;
+                            id_last = id_next;
+                            k_last = j;
+                            if (j + 1 < x.n_tiles) id_next = lane_page_id(pt_row, j + 1, ppt, npg, lane);
+                        } else {
+                            pid = j == k_last ? id_last : id_prev;
+                        }
                         const bool pg_ok = lane_page_ok(pid, j, ppt, npg, p.num_pages, lane, p.status);
                         issue_page_boxes<C::CHUNKS, C::CHUNK_BYTES>(
                             BAR(KV_FULL + st), ps, w.g, lane, false, 0, tm, 0, pg_ok,
                             sKV + st * C::TILE_BYTES, tm, pid);
                         if (lane == 0 && s == nl - 1 && x.n_tiles * BN > x.kv_len)
                             mbar_arrive(BAR(FIX_READY));
-                        if (s + 1 < nl) {
-                            bool kn;
-                            pid = lane_page_id(pt_row, tile_of(s + 1, kn), ppt, npg, lane);
-                        }
                     } else {
                         mbar_arrive_expect_tx(BAR(KV_FULL + st), C::TILE_BYTES);
 #pragma unroll
