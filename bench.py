@@ -510,7 +510,8 @@ def time_calls(fn, stream, reps=20, warmup=3):
 
 def bench_extra(api, W, dev, stream, dc, peaks):
     """The paged prefill (ragged queries over a paged KV cache) on the prefill_hd128 and
-    prefix_hd256 shapes with 16-token pages, the ragged prefix_hd256 beside it,
+    prefix_hd256 shapes with 16-token pages, the ragged prefix_hd256 beside it, the ragged
+    prefill of one 32k-token request,
     4-token-per-request decode (speculative verification) over the resident 256-request
     decode cache, and the decode over that cache stored as FP8 E4M3; each timed on its own
     (inputs resident in HBM)."""
@@ -545,6 +546,17 @@ def bench_extra(api, W, dev, stream, dc, peaks):
                                                        stream=stream), stream)
             out["ragged_prefill_prefix_hd256"] = tensor_line(flops, ms, "prefix_hd256, ragged K/V")
         del pc, rc, o, lse
+    # one 32k-token request, 64 / 8 heads (G = 8), K scaled by 3: long items, few boundaries
+    lc = W.config("long", device=dev)
+    lo = torch.empty_like(lc.q)
+    ll = torch.empty(lc.q.shape[:2], dtype=torch.float32, device=dev)
+    ms = time_calls(lambda: api.ragged_prefill(lc.q, lc.k, lc.v, lc.q_indptr, lc.kv_indptr,
+                                               causal=True, sm_scale=lc.sm_scale, out=lo, lse=ll,
+                                               stream=stream), stream, reps=5)
+    out["ragged_prefill_long"] = tensor_line(
+        prefill_flops(lc.qo_lens, lc.kv_lens, lc.num_qo_heads, lc.head_dim), ms,
+        "one 32768-token request, 64/8 heads, d 128, causal, K x 3")
+    del lc, lo, ll
     # 4 query tokens per request over the decode workload's paged cache
     g = torch.Generator(device=dev)
     g.manual_seed(7)
