@@ -209,6 +209,27 @@ def host_copies(case):
 
 
 # ------------------------------------------------------------------ main arms
+def bench_config():
+    """The `config` object of the bench line, from the workloads' lengths and shapes alone
+    (no tensor is drawn), so that both arms report the same one."""
+    from paged_gqa_attention_varlen_gb300 import workloads as W
+    qo, kv = W.config_lengths(PREFILL_WORKLOAD)
+    ps = W.CONFIG_SHAPES[PREFILL_WORKLOAD]
+    _, dkv = W.config_lengths(DECODE_WORKLOAD)
+    ds = W.CONFIG_SHAPES[DECODE_WORKLOAD]
+    return {"workload": f"{PREFILL_WORKLOAD} + {DECODE_WORKLOAD}",
+            "prefill": {"batch": len(qo), "total_q": int(sum(qo)),
+                        "num_qo_heads": ps["num_qo_heads"], "num_kv_heads": ps["num_kv_heads"],
+                        "head_dim": ps["head_dim"], "causal": ps["causal"],
+                        "flops": prefill_flops(qo, kv, ps["num_qo_heads"], ps["head_dim"],
+                                               ps["causal"])},
+            "decode": {"batch": len(dkv), "sum_kv": int(sum(dkv)), "page_size": ds["page_size"],
+                       "num_qo_heads": ds["num_qo_heads"], "num_kv_heads": ds["num_kv_heads"],
+                       "head_dim": ds["head_dim"],
+                       "kv_bytes": decode_kv_bytes(dkv, ds["num_kv_heads"], ds["head_dim"])},
+            "l2": "inputs larger than L2 (0.42 GB prefill, 17.4 GB decode), no flush"}
+
+
 def bench_reference(args, ws, rank):
     """The float64 oracle, timed on the host cores, on a row sample per step."""
     if rank != 0:
@@ -230,7 +251,7 @@ def bench_reference(args, ws, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "impl": "reference",
-        "config": {"workload": PREFILL_WORKLOAD, "sample": sample},
+        "config": dict(bench_config(), sample=sample),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.threads(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -423,16 +444,7 @@ def bench_gpu(args, ws, rank, local):
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": total_ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": f"{PREFILL_WORKLOAD} + {DECODE_WORKLOAD}",
-                   "prefill": {"batch": pf.batch, "total_q": pf.total_q,
-                               "num_qo_heads": pf.num_qo_heads, "num_kv_heads": pf.num_kv_heads,
-                               "head_dim": pf.head_dim, "causal": True,
-                               "flops": pf_flops},
-                   "decode": {"batch": dc.batch, "sum_kv": int(sum(dc.kv_lens)),
-                              "page_size": dc.page_size, "num_qo_heads": dc.num_qo_heads,
-                              "num_kv_heads": dc.num_kv_heads, "head_dim": dc.head_dim,
-                              "kv_bytes": dc_bytes},
-                   "l2": "inputs larger than L2 (0.42 GB prefill, 17.4 GB decode), no flush"},
+        "config": bench_config(),
         "roofline": {"bound": "tensor", "kernel": "prefill (plan + attention launch pair)",
                      "achieved": pf_achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": pf_achieved / peaks["bf16_tflops"],

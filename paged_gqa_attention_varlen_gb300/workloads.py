@@ -204,6 +204,15 @@ def config(name: str, device="cpu", seed=0):
 CONFIG_NAMES = ("tiny", "prefill_hd128", "prefix_hd256", "decode", "long")
 
 
+CONFIG_SHAPES = {  # heads, head_dim, page size (0: ragged K/V) and causality of each workload
+    "tiny": dict(num_qo_heads=4, num_kv_heads=2, head_dim=128, page_size=0, causal=True),
+    "prefill_hd128": dict(num_qo_heads=32, num_kv_heads=8, head_dim=128, page_size=0, causal=True),
+    "prefix_hd256": dict(num_qo_heads=16, num_kv_heads=4, head_dim=256, page_size=0, causal=True),
+    "decode": dict(num_qo_heads=32, num_kv_heads=8, head_dim=128, page_size=16, causal=True),
+    "long": dict(num_qo_heads=64, num_kv_heads=8, head_dim=128, page_size=0, causal=True),
+}
+
+
 def config_lengths(name: str, seed=0):
     """Per-request (qo_lens, kv_lens) of a named workload without drawing any tensor."""
     cg = torch.Generator()

@@ -78,3 +78,20 @@ def test_reference_arm_prints_one_line(capsys):
     assert line["impl"] == "reference" and line["unit"] == "TFLOP/s"
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
     assert line["value"] > 0
+    # the same workload description as the GPU arm's line, plus the sample
+    cfg = dict(line["config"])
+    assert cfg.pop("sample")
+    assert cfg == bench.bench_config()
+    assert line["metric"] == bench.METRIC and line["higher_is_better"] is True
+
+
+def test_config_shapes_match_the_workload_generator():
+    from paged_gqa_attention_varlen_gb300 import workloads as W
+    c = W.config("tiny")
+    shape = W.CONFIG_SHAPES["tiny"]
+    assert (c.num_qo_heads, c.num_kv_heads, c.head_dim, c.causal) == (
+        shape["num_qo_heads"], shape["num_kv_heads"], shape["head_dim"], shape["causal"])
+    cfg = bench.bench_config()
+    qo, kv = W.config_lengths("prefill_hd128")
+    assert cfg["prefill"]["total_q"] == sum(qo) == 39332
+    assert cfg["decode"]["kv_bytes"] == sum(W.config_lengths("decode")[1]) * 8 * 128 * 2 * 2
