@@ -176,34 +176,6 @@ def _lens(gen, n, lo, hi):
     return [int(x) for x in torch.randint(lo, hi + 1, (n,), generator=gen)]
 
 
-def config(name: str, device="cpu", seed=0):
-    """One of the named serving workloads (see the module docstring)."""
-    cg = torch.Generator()
-    cg.manual_seed(seed)
-    if name == "tiny":
-        c = ragged_case([17, 64], [17, 64], 4, 2, 128, True, seed=seed, device=device, name=name)
-    elif name == "prefill_hd128":
-        lens = _lens(cg, 16, 128, 4096)
-        c = ragged_case(lens, lens, 32, 8, 128, True, seed=seed, device=device, name=name)
-    elif name == "prefix_hd256":
-        qo = _lens(cg, 8, 256, 2048)
-        prefix = _lens(cg, 8, 0, 8192)
-        kv = [a + b for a, b in zip(qo, prefix)]
-        c = ragged_case(qo, kv, 16, 4, 256, True, seed=seed, device=device, name=name)
-    elif name == "decode":
-        kv = _lens(cg, 256, 512, 32768)
-        c = paged_case(kv, 32, 8, 128, page_size=16, seed=seed, device=device, name=name)
-    elif name == "long":
-        c = ragged_case([32768], [32768], 64, 8, 128, True, seed=seed, device=device,
-                        k_scale=3.0, name=name)
-    else:
-        raise KeyError(name)
-    return c
-
-
-CONFIG_NAMES = ("tiny", "prefill_hd128", "prefix_hd256", "decode", "long")
-
-
 CONFIG_SHAPES = {  # heads, head_dim, page size (0: ragged K/V) and causality of each workload
     "tiny": dict(num_qo_heads=4, num_kv_heads=2, head_dim=128, page_size=0, causal=True),
     "prefill_hd128": dict(num_qo_heads=32, num_kv_heads=8, head_dim=128, page_size=0, causal=True),
@@ -211,6 +183,21 @@ CONFIG_SHAPES = {  # heads, head_dim, page size (0: ragged K/V) and causality of
     "decode": dict(num_qo_heads=32, num_kv_heads=8, head_dim=128, page_size=16, causal=True),
     "long": dict(num_qo_heads=64, num_kv_heads=8, head_dim=128, page_size=0, causal=True),
 }
+
+
+def config(name: str, device="cpu", seed=0):
+    """One of the named serving workloads (see the module docstring)."""
+    shape = CONFIG_SHAPES[name]
+    hq, hk, d = shape["num_qo_heads"], shape["num_kv_heads"], shape["head_dim"]
+    qo, kv = config_lengths(name, seed)
+    if name == "decode":
+        return paged_case(kv, hq, hk, d, page_size=shape["page_size"], seed=seed, device=device,
+                          name=name)
+    return ragged_case(qo, kv, hq, hk, d, shape["causal"], seed=seed, device=device,
+                       k_scale=3.0 if name == "long" else 1.0, name=name)
+
+
+CONFIG_NAMES = ("tiny", "prefill_hd128", "prefix_hd256", "decode", "long")
 
 
 def config_lengths(name: str, seed=0):
