@@ -90,9 +90,12 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _stream(stream):
+def _stream(stream, dev=None):
+    """The stream handle for a call on device `dev` (default: its current stream)."""
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(dev)
+    elif dev is not None and stream.device != dev:
+        raise ValueError(f"stream is on {stream.device}, the tensors on {dev}")
     return ctypes.c_void_p(stream.cuda_stream)
 
 
@@ -174,9 +177,11 @@ def ragged_prefill(q, k, v, q_indptr, kv_indptr, causal=True, sm_scale=None, out
     if lse is not None:
         _check(lse, "lse", torch.float32, 2, dev)
     batch = q_indptr.numel() - 1
-    rc = lib.pgqa_ragged_prefill_bf16(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
-                                      _ptr(q_indptr), _ptr(kv_indptr), batch, hq, hk, d,
-                                      int(bool(causal)), float(sm_scale), _stream(stream))
+    with torch.cuda.device(dev):  # the library works on the current device
+        rc = lib.pgqa_ragged_prefill_bf16(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                                          _ptr(q_indptr), _ptr(kv_indptr), batch, hq, hk, d,
+                                          int(bool(causal)), float(sm_scale),
+                                          _stream(stream, dev))
     if rc != PGQA_OK:
         raise PgqaError(rc, "pgqa_ragged_prefill_bf16")
     return out, lse
@@ -214,19 +219,22 @@ def paged_prefill(q, k_pages, v_pages, q_indptr, page_table, kv_lens, causal=Tru
         lse = torch.empty((total_q, hq), dtype=torch.float32, device=dev)
     if lse is not None:
         _check(lse, "lse", torch.float32, 2, dev)
-    if packed:
-        rc = lib.pgqa_paged_prefill_bf16(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(out),
-                                         _ptr(lse), _ptr(q_indptr), _ptr(page_table),
-                                         page_table.shape[1], _ptr(kv_lens), page_size, num_pages,
-                                         batch, hq, hk, d, int(bool(causal)), float(sm_scale),
-                                         _stream(stream))
-    else:
-        rc = lib.pgqa_paged_prefill_bf16_strided(
-            _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(out), _ptr(lse), _ptr(q_indptr),
-            _ptr(page_table), page_table.shape[1], _ptr(kv_lens), page_size, num_pages, *strides,
-            batch, hq, hk, d, int(bool(causal)), float(sm_scale), _stream(stream))
+    name = "pgqa_paged_prefill_bf16" if packed else "pgqa_paged_prefill_bf16_strided"
+    with torch.cuda.device(dev):  # the library works on the current device
+        st = _stream(stream, dev)
+        if packed:
+            rc = lib.pgqa_paged_prefill_bf16(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(out),
+                                             _ptr(lse), _ptr(q_indptr), _ptr(page_table),
+                                             page_table.shape[1], _ptr(kv_lens), page_size,
+                                             num_pages, batch, hq, hk, d, int(bool(causal)),
+                                             float(sm_scale), st)
+        else:
+            rc = lib.pgqa_paged_prefill_bf16_strided(
+                _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(out), _ptr(lse), _ptr(q_indptr),
+                _ptr(page_table), page_table.shape[1], _ptr(kv_lens), page_size, num_pages,
+                *strides, batch, hq, hk, d, int(bool(causal)), float(sm_scale), st)
     if rc != PGQA_OK:
-        raise PgqaError(rc, "pgqa_paged_prefill_bf16")
+        raise PgqaError(rc, name)
     return out, lse
 
 
@@ -262,39 +270,51 @@ def paged_decode(q, k_pages, v_pages, page_table, kv_lens, sm_scale=None, out=No
         lse = torch.empty((batch, hq), dtype=torch.float32, device=dev)
     if lse is not None:
         _check(lse, "lse", torch.float32, 2, dev)
-    if e4m3:
-        rc = lib.pgqa_paged_decode_e4m3(
-            _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table), _ptr(kv_lens), page_size,
-            page_table.shape[1], num_pages, *strides, float(k_scale), float(v_scale), _ptr(out),
-            _ptr(lse), batch, hq, hk, d, float(sm_scale), _stream(stream))
-    elif packed:
-        rc = lib.pgqa_paged_decode_bf16(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table),
-                                        _ptr(kv_lens), page_size, page_table.shape[1], num_pages,
-                                        _ptr(out), _ptr(lse), batch, hq, hk, d, float(sm_scale),
-                                        _stream(stream))
-    else:
-        rc = lib.pgqa_paged_decode_bf16_strided(
-            _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table), _ptr(kv_lens), page_size,
-            page_table.shape[1], num_pages, *strides, _ptr(out), _ptr(lse), batch, hq, hk, d,
-            float(sm_scale), _stream(stream))
+    name = ("pgqa_paged_decode_e4m3" if e4m3 else
+            "pgqa_paged_decode_bf16" if packed else "pgqa_paged_decode_bf16_strided")
+    with torch.cuda.device(dev):  # the library works on the current device
+        st = _stream(stream, dev)
+        if e4m3:
+            rc = lib.pgqa_paged_decode_e4m3(
+                _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table), _ptr(kv_lens),
+                page_size, page_table.shape[1], num_pages, *strides, float(k_scale),
+                float(v_scale), _ptr(out), _ptr(lse), batch, hq, hk, d, float(sm_scale), st)
+        elif packed:
+            rc = lib.pgqa_paged_decode_bf16(_ptr(q), _ptr(k_pages), _ptr(v_pages),
+                                            _ptr(page_table), _ptr(kv_lens), page_size,
+                                            page_table.shape[1], num_pages, _ptr(out), _ptr(lse),
+                                            batch, hq, hk, d, float(sm_scale), st)
+        else:
+            rc = lib.pgqa_paged_decode_bf16_strided(
+                _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table), _ptr(kv_lens),
+                page_size, page_table.shape[1], num_pages, *strides, _ptr(out), _ptr(lse), batch,
+                hq, hk, d, float(sm_scale), st)
     if rc != PGQA_OK:
-        raise PgqaError(rc, "pgqa_paged_decode_bf16")
+        raise PgqaError(rc, name)
     return out, lse
 
 
-def device_status(stream=None) -> int:
-    """Synchronise the stream and return (and clear) the device status code."""
-    return lib.pgqa_get_device_status(_stream(stream))
+def device_status(stream=None, device=None) -> int:
+    """Synchronise the stream and return (and clear) the device status code of `device`
+    (default: the current device, or the stream's)."""
+    if device is None:
+        device = stream.device if stream is not None else torch.device(
+            "cuda", torch.cuda.current_device())
+    with torch.cuda.device(device):
+        return lib.pgqa_get_device_status(_stream(stream, device))
 
 
-def set_workspace(buf: torch.Tensor | None):
-    """Use a caller-owned uint8 CUDA tensor as the workspace (None: back to lazy)."""
+def set_workspace(buf: torch.Tensor | None, device=None):
+    """Use a caller-owned uint8 CUDA tensor as the workspace of its device (None: back to
+    lazy allocation on `device`, default the current device)."""
     if buf is None:
-        rc = lib.pgqa_set_workspace(None, 0)
+        with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+            rc = lib.pgqa_set_workspace(None, 0)
     else:
         if buf.dtype != torch.uint8 or not buf.is_cuda or not buf.is_contiguous():
             raise ValueError("workspace must be a contiguous uint8 CUDA tensor")
-        rc = lib.pgqa_set_workspace(_ptr(buf), buf.numel())
+        with torch.cuda.device(buf.device):
+            rc = lib.pgqa_set_workspace(_ptr(buf), buf.numel())
     if rc != PGQA_OK:
         raise PgqaError(rc, "pgqa_set_workspace")
 

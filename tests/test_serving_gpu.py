@@ -162,3 +162,30 @@ def test_cuda_graph_replay_with_rewritten_inputs(cuda_lib):
         assert torch.equal(o[:nq], ref[0][:nq]) and torch.equal(lse[:nq], ref[1][:nq]), idx
         for got, want in zip((do, dl, po, pl), ref[2:]):
             assert torch.equal(got, want), idx
+
+
+def test_calls_on_a_side_stream_match_the_default_stream(cuda_lib):
+    """Every entry point enqueues on the stream it is given (here a second stream of the
+    tensors' device) and gives the same bits as on the current stream."""
+    case = W.ragged_case([300, 77], [300, 900], 16, 4, 128, seed=77, device="cuda")
+    pc = W.paged_case([1000, 20], 32, 8, 128, page_size=16, qo_lens=[4, 3], seed=78,
+                      device="cuda")
+    dc = W.paged_case([1000, 20, 4000], 32, 8, 128, page_size=16, seed=79, device="cuda")
+
+    def run(stream):
+        return (cuda_lib.ragged_prefill(case.q, case.k, case.v, case.q_indptr, case.kv_indptr,
+                                        stream=stream),
+                cuda_lib.paged_prefill(pc.q, pc.k_pages, pc.v_pages, pc.q_indptr, pc.page_table,
+                                       pc.kv_lens_t, stream=stream),
+                cuda_lib.paged_decode(dc.q, dc.k_pages, dc.v_pages, dc.page_table, dc.kv_lens_t,
+                                      stream=stream))
+
+    ref = run(None)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    got = run(side)
+    side.synchronize()
+    assert cuda_lib.device_status(side) == 0
+    for (o1, l1), (o2, l2) in zip(ref, got):
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
