@@ -21,8 +21,9 @@
 //    TMA ring in shared memory; the online softmax keeps a running max and sum per
 //    head.  A request with a single chunk writes its bf16 output directly; otherwise
 //    each chunk writes a normalised fp32 partial output and its lse.
-//  * merge_kernel: one warp per (request, head) with more than one chunk combines the
-//    partials with weights exp(lse_c - max lse).
+//  * merge_kernel: each (request, head) with more than one chunk combines the partials
+//    with weights exp(lse_c - max lse), in groups of 8 chunks; a warp per row, or a CTA
+//    per row when there are few rows (same arithmetic, same order).
 #include "ptx.cuh"
 
 namespace pgqa {
@@ -444,41 +445,139 @@ __global__ void __launch_bounds__(WARPS * 32, G >= 8 ? 2 : 3)
 }
 
 // One warp per (request, head) row whose request was split into several chunks.
-__global__ void __launch_bounds__(256) merge_kernel(const Params p) {
+// Merge of one (request, head) row's chunk partials, in a fixed order: chunks are summed
+// in groups of MERGE_GROUP consecutive chunks (weights exp(lse_c - max lse)), and the group
+// sums are added in group order.  With few rows a whole CTA works on one row (warp w
+// computes groups w, w + 8, ...); with many rows one warp computes every group of its row.
+// Both do the same floating-point operations in the same order, so the result does not
+// depend on which one ran, and so not on the rest of the batch.
+constexpr int MERGE_GROUP = 8;
+constexpr int MERGE_WARPS = 8;
+
+struct MergeRow {
+    int b, h, f0, nch;
+};
+
+// one group's weighted sum (lane: 4 of the D columns) and weight sum
+__device__ __forceinline__ void merge_group(const Params& p, const MergeRow& r, int g, float mx,
+                                            int lane, float4& acc, float& wsum) {
     constexpr int D = HEAD_DIM;
-    const int lane = threadIdx.x & 31;
-    const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int Hq = p.num_qo_heads;
-    if (row >= (long long)p.batch * Hq) return;
-    const int b = (int)(row / Hq), h = (int)(row % Hq);
-    const int f0 = __ldg(p.chunk_off + b);
-    const int nch = __ldg(p.chunk_off + b + 1) - f0;
-    if (nch <= 1) return;
-    float mx = -INFINITY;
-    for (int c = lane; c < nch; c += 32) mx = fmaxf(mx, p.part_lse[(size_t)(f0 + c) * Hq + h]);
+    const int c0 = g * MERGE_GROUP;
+    const int n = min(MERGE_GROUP, r.nch - c0);
+    const float* lp = p.part_lse + (size_t)(r.f0 + c0) * Hq + r.h;
+    const float4* vp =
+        reinterpret_cast<const float4*>(p.part_o + ((size_t)(r.f0 + c0) * Hq + r.h) * D) + lane;
+    const size_t vstride = (size_t)Hq * D / 4;  // float4s from one chunk's row to the next
+    float l[MERGE_GROUP];
+    float4 v[MERGE_GROUP];
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float wsum = 0.f;
-    if (mx != -INFINITY) {
-        for (int c = 0; c < nch; ++c) {
-            const float w = __expf(p.part_lse[(size_t)(f0 + c) * Hq + h] - mx);
-            const float4 v = *reinterpret_cast<const float4*>(
-                p.part_o + ((size_t)(f0 + c) * Hq + h) * D + lane * 4);
-            wsum += w;
-            acc.x = fmaf(w, v.x, acc.x);
-            acc.y = fmaf(w, v.y, acc.y);
-            acc.z = fmaf(w, v.z, acc.z);
-            acc.w = fmaf(w, v.w, acc.w);
+    for (int u = 0; u < MERGE_GROUP; ++u) {  // every load of the group before any arithmetic
+        if (u < n) {
+            l[u] = lp[(size_t)u * Hq];
+            v[u] = vp[(size_t)u * vstride];
         }
     }
+    acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    wsum = 0.f;
+#pragma unroll
+    for (int u = 0; u < MERGE_GROUP; ++u) {
+        if (u < n) {
+            const float w = __expf(l[u] - mx);
+            wsum += w;
+            acc.x = fmaf(w, v[u].x, acc.x);
+            acc.y = fmaf(w, v[u].y, acc.y);
+            acc.z = fmaf(w, v[u].z, acc.z);
+            acc.w = fmaf(w, v[u].w, acc.w);
+        }
+    }
+}
+
+__device__ __forceinline__ void merge_store(const Params& p, const MergeRow& r, int lane,
+                                            float mx, const float4& acc, float wsum) {
+    constexpr int D = HEAD_DIM;
+    const int Hq = p.num_qo_heads;
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    __nv_bfloat16* op = reinterpret_cast<__nv_bfloat16*>(p.o) + ((size_t)b * Hq + h) * D;
+    __nv_bfloat16* op = reinterpret_cast<__nv_bfloat16*>(p.o) + ((size_t)r.b * Hq + r.h) * D;
     uint2 u;
     u.x = pack_bf16x2(acc.x * inv, acc.y * inv);
     u.y = pack_bf16x2(acc.z * inv, acc.w * inv);
     *reinterpret_cast<uint2*>(op + lane * 4) = u;
-    if (lane == 0 && p.lse) p.lse[(size_t)b * Hq + h] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
+    if (lane == 0 && p.lse) p.lse[(size_t)r.b * Hq + r.h] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
+}
+
+__device__ __forceinline__ float4 f4_add(const float4& a, const float4& b) {
+    return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+}
+
+// SPLIT = false: one warp per row, 8 rows per CTA.  SPLIT = true: one CTA per row.
+template <bool SPLIT>
+__global__ void __launch_bounds__(MERGE_WARPS * 32) merge_kernel(const Params p) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int Hq = p.num_qo_heads;
+    const long long row = SPLIT ? (long long)blockIdx.x : (long long)blockIdx.x * MERGE_WARPS + warp;
+    if (row >= (long long)p.batch * Hq) return;  // uniform per CTA when SPLIT
+    MergeRow r;
+    r.b = (int)(row / Hq);
+    r.h = (int)(row % Hq);
+    r.f0 = __ldg(p.chunk_off + r.b);
+    r.nch = __ldg(p.chunk_off + r.b + 1) - r.f0;
+    if (r.nch <= 1) return;  // written by the decode kernel
+    const int ngroups = (r.nch + MERGE_GROUP - 1) / MERGE_GROUP;
+    // the largest chunk lse
+    const int t0 = SPLIT ? warp * 32 + lane : lane, tstep = SPLIT ? MERGE_WARPS * 32 : 32;
+    float mx = -INFINITY;
+    for (int c = t0; c < r.nch; c += tstep)
+        mx = fmaxf(mx, p.part_lse[(size_t)(r.f0 + c) * Hq + r.h]);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if constexpr (SPLIT) {
+        __shared__ float s_mx[MERGE_WARPS];
+        __shared__ float4 s_acc[MERGE_WARPS][32];
+        __shared__ float s_w[MERGE_WARPS];
+        if (lane == 0) s_mx[warp] = mx;
+        __syncthreads();
+        mx = s_mx[0];
+#pragma unroll
+        for (int w = 1; w < MERGE_WARPS; ++w) mx = fmaxf(mx, s_mx[w]);
+        float4 tot = make_float4(0.f, 0.f, 0.f, 0.f);
+        float wtot = 0.f;
+        if (mx != -INFINITY) {
+            for (int g0 = 0; g0 < ngroups; g0 += MERGE_WARPS) {
+                const int g = g0 + warp;
+                if (g < ngroups) {
+                    float4 acc;
+                    float ws;
+                    merge_group(p, r, g, mx, lane, acc, ws);
+                    s_acc[warp][lane] = acc;
+                    if (lane == 0) s_w[warp] = ws;
+                }
+                __syncthreads();
+                if (warp == 0) {  // group sums in group order
+                    const int n = min(MERGE_WARPS, ngroups - g0);
+                    for (int w = 0; w < n; ++w) {
+                        tot = f4_add(tot, s_acc[w][lane]);
+                        wtot += s_w[w];
+                    }
+                }
+                __syncthreads();
+            }
+        }
+        if (warp == 0) merge_store(p, r, lane, mx, tot, wtot);
+    } else {
+        float4 tot = make_float4(0.f, 0.f, 0.f, 0.f);
+        float wtot = 0.f;
+        if (mx != -INFINITY) {
+            for (int g = 0; g < ngroups; ++g) {
+                float4 acc;
+                float ws;
+                merge_group(p, r, g, mx, lane, acc, ws);
+                tot = f4_add(tot, acc);
+                wtot += ws;
+            }
+        }
+        merge_store(p, r, lane, mx, tot, wtot);
+    }
 }
 
 // ------------------------------------------------------------------ host launchers
@@ -568,8 +667,14 @@ cudaError_t launch_decode(const Params& p, int group, bool kv8, int num_sms, cud
 
 cudaError_t launch_merge(const Params& p, cudaStream_t stream) {
     const long long rows = (long long)p.batch * p.num_qo_heads;
-    const int grid = (int)((rows + 7) / 8);
-    if (grid > 0) merge_kernel<<<grid, 256, 0, stream>>>(p);
+    if (rows <= 0) return cudaSuccess;
+    // too few rows to fill the GPU with one warp per row: a CTA per row (the result is
+    // the same bits either way)
+    if (rows < 1024)
+        merge_kernel<true><<<(unsigned)rows, MERGE_WARPS * 32, 0, stream>>>(p);
+    else
+        merge_kernel<false><<<(unsigned)((rows + MERGE_WARPS - 1) / MERGE_WARPS),
+                              MERGE_WARPS * 32, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -1498,16 +1498,32 @@ __global__ void __launch_bounds__(256) merge_kernel(const Params p) {
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         float wsum = 0.f;
         if (mx != -INFINITY) {
-            for (int c = 0; c < nvis; ++c) {
-                const long long sl = slot(c);
-                const float wgt = __expf(p.part_lse[sl] - mx);
-                const float4 v = *reinterpret_cast<const float4*>(p.part_o + sl * D + lane * 4);
+            // chunks in index order, the loads of MU chunks issued before their arithmetic
+            constexpr int MU = 4;
+            auto add = [&](float l, const float4& v) {
+                const float wgt = __expf(l - mx);
                 wsum += wgt;
                 acc.x = fmaf(wgt, v.x, acc.x);
                 acc.y = fmaf(wgt, v.y, acc.y);
                 acc.z = fmaf(wgt, v.z, acc.z);
                 acc.w = fmaf(wgt, v.w, acc.w);
+            };
+            auto row = [&](int c) {
+                return *reinterpret_cast<const float4*>(p.part_o + slot(c) * D + lane * 4);
+            };
+            int c = 0;
+            for (; c + MU <= nvis; c += MU) {
+                float l[MU];
+                float4 v[MU];
+#pragma unroll
+                for (int u = 0; u < MU; ++u) {
+                    l[u] = p.part_lse[slot(c + u)];
+                    v[u] = row(c + u);
+                }
+#pragma unroll
+                for (int u = 0; u < MU; ++u) add(l[u], v[u]);
             }
+            for (; c < nvis; ++c) add(p.part_lse[slot(c)], row(c));
         }
         const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
         __nv_bfloat16* op = reinterpret_cast<__nv_bfloat16*>(p.o) + ((size_t)(q0 + t) * Hq + h) * D;

@@ -143,3 +143,24 @@ def test_bad_page_id_reports_bounds_status(cuda_lib):
     pc.page_table[0, 1] = 0
     run_gpu(cuda_lib, pc)
     assert cuda_lib.device_status() == 0
+
+
+def test_merge_modes_give_the_same_bits(cuda_lib):
+    """The chunk merge runs one CTA per (request, head) when a call has few rows and one
+    warp per row otherwise, with the same arithmetic in the same order.  A request's
+    result must not depend on which mode its batch size picked.  A 4096-page table
+    (64k keys of capacity) keeps both calls under the 1024-key chunking."""
+    kv = [5000] + [int(x) for x in np.random.default_rng(7).integers(1, 9000, 39)]
+    pc = W.paged_case(kv, 32, 8, 128, page_size=16, seed=31, stride=4096, device="cuda")
+    o, l = run_gpu(cuda_lib, pc)  # 40 x 32 = 1280 rows: a warp per row
+    o1, l1 = cuda_lib.paged_decode(pc.q[:1].contiguous(), pc.k_pages, pc.v_pages,
+                                   pc.page_table[:1].contiguous(), pc.kv_lens_t[:1].contiguous(),
+                                   sm_scale=pc.sm_scale)  # 32 rows: a CTA per row
+    torch.cuda.synchronize()
+    assert cuda_lib.device_status() == 0
+    assert torch.equal(o1[0], o[0]) and torch.equal(l1[0], l[0])
+    ro, rl = oracle_decode(W.PagedCase("r0", pc.q[:1], torch.tensor([0, 1], dtype=torch.int32),
+                                       pc.k_pages, pc.v_pages, pc.page_table[:1],
+                                       pc.kv_lens_t[:1], kv[:1], [1], 16, 32, 8, 128, True,
+                                       pc.sm_scale))
+    check_rows(o1[0].float().cpu(), l1[0].cpu(), ro, rl, "request 0")
