@@ -155,10 +155,10 @@ int pgqa_paged_prefill_bf16(const void* q, const void* k_pages, const void* v_pa
  *   Key slots past kv_lens[b] in a request's last page are never read, so whatever
  *   they hold (even NaN) cannot reach the output.
  *
- * Split: each request's keys are cut into chunks of 1024 keys, or of 256 keys when the
- * call is small (batch * ceil(page_table_stride * page_size / 1024) * num_kv_heads < 512),
- * a choice made from these sizes alone.  Within either regime a request's result does not
- * depend on the other requests of the batch, bit for bit.
+ * Split: each request's keys are cut into chunks of C keys, C the longest of 1024, 512,
+ * 256, 128 for which batch * ceil(page_table_stride * page_size / C) * num_kv_heads >= 2048
+ * (128 if none is), a choice made from these sizes alone.  For a given C a request's
+ * result does not depend on the other requests of the batch, bit for bit.
  *
  * Supported: head_dim 128; page_size 16, 32, 64 or 128; G = num_qo_heads / num_kv_heads in
  * {1,2,4,8}.
@@ -264,9 +264,9 @@ int paged_decode_bf16(const void* q, const void* k_pages, const void* v_pages,
  *     stream capture.
  *   - Limit: returns PGQA_ERR_WORKSPACE, enqueueing nothing, when
  *       1024 + 256-rounded (2*batch+1)*4 + 256-rounded C*Hq*4 + C*Hq*head_dim*4 > 16 MiB,
- *     with C = batch * ceil(page_table_stride * page_size / K) partial chunks, K = 256
- *     keys when batch * ceil(page_table_stride * page_size / 1024) * num_kv_heads < 512,
- *     else 1024 (e.g. batch 32 with 32k-key tables at 32 query heads fits).
+ *     with C = batch * ceil(page_table_stride * page_size / K) partial chunks and K the
+ *     chunk length chosen as for pgqa_paged_decode_bf16 (e.g. batch 16 with 32k-key
+ *     tables at 32 query heads fits; batch 32 does not).
  *   - Sharing: every call on a device uses the same array and leaves its contents
  *     behind; calls that overlap on the GPU (different streams without ordering) race
  *     and corrupt each other's results.  Order them.

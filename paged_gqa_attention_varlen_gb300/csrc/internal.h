@@ -132,17 +132,23 @@ struct PlanParams {
 // ------------------------------------------------------------------ decode
 namespace decode {
 constexpr int PAGE = 16;           // tokens per TMA unit (one box); pages hold 1, 2, 4 or 8
-constexpr int CHUNK = 1024;        // tokens per split-KV chunk
-constexpr int CHUNK_SMALL = 256;   // tokens per chunk when the work is short
-constexpr int SMALL_WORK = 512;    // (request, chunk, kv head) items below which it is
+constexpr int CHUNK = 1024;        // tokens per split-KV chunk (calls with a lot of work)
+constexpr int CHUNK_MIN = 128;     // the shortest chunk
+constexpr int WAVE_ITEMS = 2048;   // (request, chunk, kv head) items of about one wave of warps
 
-// Keys per split-KV chunk.  Decided from the call's shape alone (batch, the page table's
-// key capacity, kv heads): calls with less work than about one wave of warps use shorter
-// chunks to spread over the GPU.  Within either regime a request's chunks depend on the
-// request alone, so its results do not depend on the other requests of the batch.
+// Keys per split-KV chunk, decided from the call's shape alone (batch, the page table's key
+// capacity, kv heads): the longest of 1024, 512, 256, 128 keys that still gives about a
+// wave of (chunk, kv head) warps, so that calls with little work spread over the GPU.  For
+// a given chunk length a request's chunks depend on the request alone, so its results do
+// not depend on the other requests of the batch.
 inline int chunk_keys(int batch, long long max_kv, int num_kv_heads) {
-    const long long per_req = max_kv > 0 ? (max_kv + CHUNK - 1) / CHUNK : 1;
-    return (long long)batch * per_req * num_kv_heads < SMALL_WORK ? CHUNK_SMALL : CHUNK;
+    int chunk = CHUNK;
+    while (chunk > CHUNK_MIN) {
+        const long long per_req = max_kv > 0 ? (max_kv + chunk - 1) / chunk : 1;
+        if ((long long)batch * per_req * num_kv_heads >= WAVE_ITEMS) break;
+        chunk /= 2;
+    }
+    return chunk;
 }
 inline long long total_chunks(int batch, long long max_kv, int chunk) {
     return (long long)batch * (max_kv > 0 ? (max_kv + chunk - 1) / chunk : 1);

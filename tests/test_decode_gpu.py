@@ -118,11 +118,11 @@ def test_zero_length_rows_are_exact_zeros(cuda_lib):
     assert torch.all(torch.isneginf(l[0])) and torch.all(torch.isneginf(l[2]))
 
 
-@pytest.mark.parametrize("stride", [None, 4096])
+@pytest.mark.parametrize("stride", [None, 16384])
 def test_batch_composition_is_bitwise_invariant(cuda_lib, stride):
-    """A 188-page table puts the batch and each single request under the 256-key chunking
-    (few work items); a 4096-page table (64k keys of capacity) puts both under the
-    1024-key chunking.  Within a regime a request's result does not depend on the batch."""
+    """A 188-page table puts the batch and each single request under 128-key chunks (few
+    work items); a 16384-page table (256k keys of capacity) puts both under 1024-key
+    chunks.  For a given chunk length a request's result does not depend on the batch."""
     pc = W.paged_case([3000, 64, 1025], 32, 8, 128, page_size=16, seed=23, stride=stride,
                       device="cuda")
     o, l = run_gpu(cuda_lib, pc)
@@ -148,10 +148,10 @@ def test_bad_page_id_reports_bounds_status(cuda_lib):
 def test_merge_modes_give_the_same_bits(cuda_lib):
     """The chunk merge runs one CTA per (request, head) when a call has few rows and one
     warp per row otherwise, with the same arithmetic in the same order.  A request's
-    result must not depend on which mode its batch size picked.  A 4096-page table
-    (64k keys of capacity) keeps both calls under the 1024-key chunking."""
+    result must not depend on which mode its batch size picked.  A 16384-page table
+    (256k keys of capacity) keeps both calls under 1024-key chunks."""
     kv = [5000] + [int(x) for x in np.random.default_rng(7).integers(1, 9000, 39)]
-    pc = W.paged_case(kv, 32, 8, 128, page_size=16, seed=31, stride=4096, device="cuda")
+    pc = W.paged_case(kv, 32, 8, 128, page_size=16, seed=31, stride=16384, device="cuda")
     o, l = run_gpu(cuda_lib, pc)  # 40 x 32 = 1280 rows: a warp per row
     o1, l1 = cuda_lib.paged_decode(pc.q[:1].contiguous(), pc.k_pages, pc.v_pages,
                                    pc.page_table[:1].contiguous(), pc.kv_lens_t[:1].contiguous(),

@@ -106,7 +106,8 @@ def test_paged_decode_sweep(cuda_lib, case):
     ps = int(rng.choice([16, 32, 64, 128]))
     layout = str(rng.choice(["NHD", "HND"]))
     kv = _lens(rng, batch, 1, 5000)
-    # a wide page table puts small batches under the 1024-key chunking as well
+    # a wide page table gives small batches longer chunks (the chunk length follows the
+    # table's key capacity)
     stride = None if rng.random() < 0.5 else 70000 // ps
     pc = W.paged_case(kv, hq, hk, 128, page_size=ps, sm_scale=_scale(rng, 128), stride=stride,
                       seed=10000 + case, device="cuda")

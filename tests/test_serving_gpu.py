@@ -4,9 +4,9 @@
   requests share the launch or on their order, bit for bit, among launches that take the
   same chunking regime.  The work list cuts every request into (kv head, q tile) items
   with a fixed K/V tiling, and split-KV chunks are request-local (2048 keys in the
-  prefill; 1024 or 256 keys in the decode), so each row's arithmetic is the same in any
-  such batch (the vllm-rlt pull request "feat: add FlashInfer attention backend for SM120
-  decode" asks the same of its decode kernel, Design notes).
+  prefill; 1024, 512, 256 or 128 keys in the decode), so each row's arithmetic is the
+  same in any such batch (the vllm-rlt pull request "feat: add FlashInfer attention
+  backend for SM120 decode" asks the same of its decode kernel, Design notes).
 - CUDA-graph replay: once a call has run (so the workspace exists), the prefills and the
   decode can be captured into a CUDA graph; replaying it after rewriting the captured
   input buffers (new contents and new per-request lengths within the same buffer sizes)
