@@ -208,6 +208,36 @@ def test_workspace_size_queries(api):
     assert lib.pgqa_workspace_bytes_prefill(1, -5, 32, 8) == 0
 
 
+def _chunk_keys(batch, max_kv, hk):
+    """The decode's chunk rule restated: the longest of 1024, 512, 256, 128 keys for which
+    batch * ceil(max_kv / chunk) * hk >= 2048, else 128."""
+    chunk = 1024
+    while chunk > 128 and batch * max(1, -(-max_kv // chunk)) * hk < 2048:
+        chunk //= 2
+    return chunk
+
+
+def test_decode_chunk_rule_through_the_workspace_query(api):
+    """pgqa_workspace_bytes_decode sizes the partial results for one kv head, the case with
+    the most chunks; its growth with the table's key capacity follows the chunk rule."""
+    lib = api.lib
+    hq, d = 32, 128
+
+    def partial_bytes(batch, stride, ps):
+        chunks = batch * -(-(stride * ps) // _chunk_keys(batch, stride * ps, 1))
+        return chunks * hq * d * 4
+
+    assert _chunk_keys(1, 32768, 8) == 128 and _chunk_keys(4, 32768, 8) == 512
+    assert _chunk_keys(16, 32768, 8) == 1024 and _chunk_keys(256, 512, 8) == 1024
+    for batch, stride, ps in ((1, 2048, 16), (3, 188, 16), (4, 2048, 16), (40, 16384, 16),
+                              (256, 2048, 16), (2, 100, 128)):
+        n = lib.pgqa_workspace_bytes_decode(batch, stride, ps, hq, d)
+        want = partial_bytes(batch, stride, ps)
+        # the fp32 partial rows plus lse, int arrays and headers of at most a few KB per
+        # request and 1 MiB of fixed arrays
+        assert want <= n <= want * 1.01 + (1 << 20) + 4096 * batch, (batch, stride, ps, n, want)
+
+
 def test_binding_refuses_cpu_tensors(api):
     import torch
     q = torch.zeros(4, 2, 128, dtype=torch.bfloat16)
