@@ -347,9 +347,10 @@ int pgqa_get_device_status(pgqa_stream_t stream) {
         cudaGetLastError();
         return PGQA_ERR_CUDA;
     }
-    if (word != 0) {
+    if (word != 0) {  // clear the status word and the timeout diagnostic words
         const int zero = 0;
         cudaMemcpy(st.ws, &zero, sizeof(int), cudaMemcpyHostToDevice);
+        cudaMemset(static_cast<int*>(st.ws) + kDiagFlag, 0, kDiagWords * sizeof(int));
     }
     if (word & PGQA_DEV_TIMEOUT) return PGQA_ERR_DEVICE_TIMEOUT;
     if (word & (PGQA_DEV_BOUNDS | PGQA_DEV_CAPACITY)) return PGQA_ERR_DEVICE_BOUNDS;

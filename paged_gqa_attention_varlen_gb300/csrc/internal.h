@@ -17,8 +17,9 @@ constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s per wait
 // wait that times out (flag, block, thread, barrier shared-memory address, parity); then,
 // in that block, warp w (< 16) that leaves a wait on the abort flag writes the barrier
 // address and parity it was waiting for to status[kDiagFlag + 6 + 2w], [.. + 7 + 2w].
-// The status word lives in a header of at least 64 ints, so these words fit after it.
-constexpr int kDiagFlag = 4;
+// The status word starts a header of 64 ints; these words sit after its counters.
+constexpr int kDiagFlag = 8;
+constexpr int kDiagWords = 6 + 2 * 16;  // flag .. the last warp's record
 
 // ------------------------------------------------------------------ workspace layout
 // [0, 256)      header: status word, counters
@@ -36,8 +37,12 @@ struct WsHeader {
     int total_q;
     int total_kv;
     int merge_rows;   // prefill: (token, head) rows the split-KV merge combines
-    int pad[59];
+    int pad[59];      // from word kDiagFlag on: the timeout diagnostic words
 };
+static_assert(sizeof(WsHeader) == 256, "workspace header size");
+static_assert(kDiagFlag * sizeof(int) >= offsetof(WsHeader, pad) &&
+                  (kDiagFlag + kDiagWords) * sizeof(int) <= sizeof(WsHeader),
+              "the diagnostic words must not overlap the header's counters");
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -50,6 +55,7 @@ constexpr int PAIR_THREADS = 384;  // + warps 8-11: softmax of the second q tile
 constexpr int PLAN_THREADS = 1024;
 constexpr int COST_BUCKETS = 4096;
 constexpr int PLAN_SMEM_BATCH = 2048;  // batches up to this size plan out of shared memory
+constexpr int PLAN_STAGE_UNITS = 2048; // work lists up to this many units are staged in smem
 
 constexpr int SPLIT_TILES = 16;   // K/V tiles (2048 keys) per chunk of a split request
 
