@@ -342,7 +342,13 @@ __global__ void __launch_bounds__(PLAN_THREADS)
     }
     __syncthreads();
 
-    // scatter: the kv heads of one unit take consecutive slots
+    // scatter: the kv heads of one unit take consecutive slots.  With up to
+    // PLAN_STAGE_UNITS units each unit's record goes to shared memory at its sorted slot,
+    // and the whole list is then written out in consecutive 16-byte pieces; longer lists
+    // write each unit's kv-head items directly.
+    extern __shared__ __align__(16) uint8_t plan_dyn[];
+    WorkItem* staged = reinterpret_cast<WorkItem*>(plan_dyn);
+    const bool stage = unit_total <= PLAN_STAGE_UNITS;
     for (int f = tid; f < unit_total; f += nthr) {
         int b, qt, c, cost;
         unit_of(f, b, qt, c, cost);
@@ -361,9 +367,28 @@ __global__ void __launch_bounds__(PLAN_THREADS)
         w.kt1 = nc > 1 ? (c + 1) * SPLIT_TILES : 0x7fffffff;
         w.part = nc > 1 ? p.part_off[b] + c * w.qo_len * p.num_qo_heads : -1;
         w.nch = nc;
-        for (int g = 0; g < p.num_kv_heads; ++g) {
-            w.g = g;
-            p.items[(long long)slot * p.num_kv_heads + g] = w;
+        if (stage) {
+            w.g = 0;
+            staged[slot] = w;
+        } else {
+            for (int g = 0; g < p.num_kv_heads; ++g) {
+                w.g = g;
+                p.items[(long long)slot * p.num_kv_heads + g] = w;
+            }
+        }
+    }
+    if (stage) {
+        __syncthreads();
+        constexpr int PIECES = (int)(sizeof(WorkItem) / sizeof(int4));  // 16-byte pieces
+        const int hk = p.num_kv_heads;
+        const int4* src = reinterpret_cast<const int4*>(staged);
+        int4* dst = reinterpret_cast<int4*>(p.items);
+        for (int i = tid; i < (int)n_items * PIECES; i += nthr) {
+            const int item = i / PIECES, piece = i - item * PIECES;
+            const int u = item / hk;
+            int4 v = src[u * PIECES + piece];
+            if (piece == 0) v.y = item - u * hk;  // WorkItem::g
+            dst[i] = v;
         }
     }
 
@@ -1593,7 +1618,17 @@ cudaError_t launch_merge(const Params& p, int num_sms, cudaStream_t stream) {
 
 cudaError_t launch_plan(const PlanParams& pp, const CUtensorMap& tq, const CUtensorMap& tk,
                         const CUtensorMap& tv, cudaStream_t stream) {
-    plan_kernel<<<1, PLAN_THREADS, 0, stream>>>(pp, tq, tk, tv);
+    constexpr int kDyn = PLAN_STAGE_UNITS * (int)sizeof(WorkItem);
+    static bool attr_set[64] = {};  // per device (callers hold the library lock)
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDyn);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    plan_kernel<<<1, PLAN_THREADS, kDyn, stream>>>(pp, tq, tk, tv);
     return cudaGetLastError();
 }
 
