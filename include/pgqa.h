@@ -312,6 +312,17 @@ size_t pgqa_workspace_bytes_decode(int batch, int page_table_stride, int page_si
  */
 int pgqa_get_device_status(pgqa_stream_t stream);
 
+/*
+ * Self-test of the device-side failure path.  Enqueues on `stream` one warp that waits,
+ * with the same bounded mbarrier wait as every kernel of this library, on a barrier that
+ * nothing arrives at.  After the wait limit (2 s) the kernel records PGQA_DEV_TIMEOUT in
+ * this device's status word, plus where it gave up, and returns; the next
+ * pgqa_get_device_status() reports PGQA_ERR_DEVICE_TIMEOUT and clears both.  Nothing
+ * else is touched, and the context stays usable.  Creates the workspace if there is
+ * none.  Returns PGQA_OK once enqueued, or PGQA_ERR_NO_DEVICE / PGQA_ERR_CUDA.
+ */
+int pgqa_selftest_expired_wait(pgqa_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char* pgqa_status_string(int status);
 

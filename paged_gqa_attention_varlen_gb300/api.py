@@ -29,7 +29,7 @@ ABI_FUNCTIONS = (
     "pgqa_paged_decode_e4m3",
     "ragged_prefill_bf16", "paged_prefill_bf16", "paged_decode_bf16", "pgqa_set_workspace", "pgqa_workspace_bytes_prefill",
     "pgqa_workspace_bytes_decode", "pgqa_get_device_status", "pgqa_status_string",
-    "pgqa_version", "pgqa_paged_decode_bf16_noalloc",
+    "pgqa_version", "pgqa_paged_decode_bf16_noalloc", "pgqa_selftest_expired_wait",
 )
 
 
@@ -76,6 +76,8 @@ def _load(path: Path):
     lib.pgqa_get_device_status.argtypes, lib.pgqa_get_device_status.restype = [p], i
     lib.pgqa_status_string.argtypes, lib.pgqa_status_string.restype = [i], ctypes.c_char_p
     lib.pgqa_version.argtypes, lib.pgqa_version.restype = [], i
+    lib.pgqa_selftest_expired_wait.argtypes = [p]
+    lib.pgqa_selftest_expired_wait.restype = i
     return lib
 
 
@@ -302,6 +304,18 @@ def device_status(stream=None, device=None) -> int:
             "cuda", torch.cuda.current_device())
     with torch.cuda.device(device):
         return lib.pgqa_get_device_status(_stream(stream, device))
+
+
+def selftest_expired_wait(stream=None, device=None):
+    """Enqueue the library's failure-path self-test (pgqa_selftest_expired_wait): a wait
+    that runs out after 2 s and leaves PGQA_ERR_DEVICE_TIMEOUT for device_status()."""
+    if device is None:
+        device = stream.device if stream is not None else torch.device(
+            "cuda", torch.cuda.current_device())
+    with torch.cuda.device(device):
+        rc = lib.pgqa_selftest_expired_wait(_stream(stream, device))
+    if rc != PGQA_OK:
+        raise PgqaError(rc, "pgqa_selftest_expired_wait")
 
 
 def set_workspace(buf: torch.Tensor | None, device=None):

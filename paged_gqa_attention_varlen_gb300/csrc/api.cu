@@ -25,6 +25,9 @@ cudaError_t launch_merge(const Params&, cudaStream_t);
 cudaError_t prepare_page_maps(Params&, const void*, const void*, int, int, int, long long,
                               long long, long long, bool);
 }  // namespace decode
+namespace selftest {
+cudaError_t launch_expired_wait(int* status, cudaStream_t stream);
+}  // namespace selftest
 
 namespace {
 
@@ -329,6 +332,17 @@ int pgqa_set_workspace(void* ptr, size_t bytes) {
         st.ws_bytes = bytes;
     }
     return PGQA_OK;
+}
+
+int pgqa_selftest_expired_wait(pgqa_stream_t stream) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    int dev;
+    DeviceState* st;
+    int rc = current_device(&dev, &st);
+    if (rc != PGQA_OK) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if ((rc = ensure_workspace(*st, kWsArrays + 4096, s)) != PGQA_OK) return rc;
+    return map_cuda(selftest::launch_expired_wait(static_cast<int*>(st->ws), s));
 }
 
 int pgqa_get_device_status(pgqa_stream_t stream) {
