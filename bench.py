@@ -77,11 +77,22 @@ KERNEL_SOURCES = {"prefill_attention": "paged_gqa_attention_varlen_gb300/csrc/pr
                   "decode": "paged_gqa_attention_varlen_gb300/csrc/decode.cu"}
 
 
+def source_code_md5(path):
+    """md5 of a CUDA source with its comments and whitespace removed: it changes when the
+    code changes, not when only a comment does."""
+    import hashlib
+    import re
+    with open(path) as f:
+        src = f.read()
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return hashlib.md5(" ".join(src.split()).encode()).hexdigest()
+
+
 def load_traffic():
     """Per-launch DRAM bytes (ncu dram__bytes_read.sum + dram__bytes_write.sum) of each
-    kernel from profiles/traffic.json -- None for a kernel whose source changed since the
-    counters were taken (the file records the source's md5)."""
-    import hashlib
+    kernel from profiles/traffic.json -- None for a kernel whose source code changed since
+    the counters were taken (the file records source_code_md5 of the source)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -92,8 +103,7 @@ def load_traffic():
     for key, src in KERNEL_SOURCES.items():
         r = rec.get(key)
         try:
-            with open(os.path.join(ROOT, src), "rb") as f:
-                md5 = hashlib.md5(f.read()).hexdigest()
+            md5 = source_code_md5(os.path.join(ROOT, src))
         except OSError:
             md5 = None
         out[key] = r["bytes_per_launch"] if r and r.get("source_md5") == md5 else None

@@ -11,18 +11,29 @@
 // Flags" (--causal, bottom-right masking).
 //
 // Design (GB300-first, not the SM80 mma.sync kernel the pages describe):
-//  * plan_kernel (1 CTA) validates the indptr arrays, turns them into a work list of
-//    (request, kv head, q tile) items sorted by their number of K/V tiles (longest
-//    first), and patches the global extents of the TMA tensor maps from
-//    q_indptr[batch] / kv_indptr[batch], so the host never reads device data.
-//  * attention_kernel is persistent (one CTA per SM) and warp-specialised:
-//      warp 0   TMA producer: Q tile once per item, then K/V tiles through a ring of
-//               shared-memory stages (mbarrier full/empty pairs);
-//      warp 1   tcgen05.mma issuer: S = Q K^T into tensor memory (two S buffers), then
-//               O += P V with P read straight from tensor memory;
-//      warps 4-7 softmax: one thread per packed query row (= TMEM lane): masking on the
-//               diagonal tiles only, online max / sum, P written back to TMEM as bf16,
-//               O rescaled in TMEM when the running max grows, then the epilogue.
+//  * plan_kernel (1 CTA) validates the indptr arrays (or kv_lens for paged K/V), turns
+//    them into a work list of (request, kv head, q tile(s), K/V chunk) items sorted by
+//    their number of K/V tiles (longest first; records staged in shared memory and
+//    written out in coalesced pieces), and patches the global extents of the TMA tensor
+//    maps from q_indptr[batch] / kv_indptr[batch], so the host never reads device data.
+//    Work lists too short to fill the GPU are split into request-local 2048-key chunks.
+//  * attention_pair_kernel (head_dim 128) is persistent (one CTA per SM) and
+//    warp-specialised, two 128-row q tiles (A, B) per CTA sharing one K/V stream:
+//      warp 0   TMA producer: Q tiles once per item, K/V tiles through a 4-stage ring;
+//      warp 1   tcgen05.mma issuer: S_x = Q_x K^T into tensor memory, O_x += P_x V with
+//               P read straight from tensor memory, alternating A and B so that one
+//               tile's softmax overlaps the other tile's MMAs;
+//      warps 4-11 softmax, a warpgroup per tile: one thread per packed query row (= TMEM
+//               lane), masking on diagonal tiles only, online max / sum, P written back
+//               as bf16 in two halves (the MMA warp starts P.V on the first), O rescaled
+//               in TMEM only when the running max grows by more than 2^8; an item's
+//               epilogue runs inside the next item's first tile.
+//  * attention_kernel<256> (head_dim 256): one q tile per CTA, two S buffers (O alone
+//    takes 256 TMEM columns), the same roles.
+//  * PAGED instances read K/V through a page table: lane l of the producer warp loads
+//    page l of each K/V tile as 4-D TMA boxes, and warp 2 zeroes an item's last V rows
+//    past kv_len before its final P.V.
+//  * merge_kernel combines split-KV partial results (fp32 O, lse) per (token, head).
 //  * GQA packing: a 128-row Q tile holds 128/G tokens x the G query heads that share a
 //    KV head (3-D TMA box), so each K/V tile is read once for all G heads.
 #include "ptx.cuh"

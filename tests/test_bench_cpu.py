@@ -95,3 +95,14 @@ def test_config_shapes_match_the_workload_generator():
     qo, kv = W.config_lengths("prefill_hd128")
     assert cfg["prefill"]["total_q"] == sum(qo) == 39332
     assert cfg["decode"]["kv_bytes"] == sum(W.config_lengths("decode")[1]) * 8 * 128 * 2 * 2
+
+
+def test_source_code_md5_ignores_comments_but_not_code(tmp_path):
+    a = tmp_path / "a.cu"
+    a.write_text("// header\nint f(int x) { return x + 1; }  // one\n/* block\n comment */\n")
+    b = tmp_path / "b.cu"
+    b.write_text("// other header\nint f(int x) {\n    return x + 1;\n}\n")
+    c = tmp_path / "c.cu"
+    c.write_text("int f(int x) { return x + 2; }\n")
+    assert bench.source_code_md5(a) == bench.source_code_md5(b)
+    assert bench.source_code_md5(a) != bench.source_code_md5(c)
