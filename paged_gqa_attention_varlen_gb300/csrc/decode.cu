@@ -14,9 +14,9 @@
 // Design: the path is bound by HBM bandwidth (about 4 flops per KV byte), so it runs on
 // the CUDA cores, not the tensor cores.
 //  * plan_kernel: sanitises kv_lens and cuts each request into chunks of `chunk` keys
-//    (1024, or 256 for calls with little work; chosen from the call's shape).  Within a
-//    regime the cut depends on the request alone, so a request's result does not depend
-//    on what else is in the batch.
+//    (1024, or 512 / 256 / 128 for calls with little work; chosen from the call's shape).
+//    For a given chunk length the cut depends on the request alone, so a request's
+//    result does not depend on what else is in the batch.
 //  * decode_tma_kernel: one warp per (chunk, kv head).  Pages stream through a per-warp
 //    TMA ring in shared memory; the online softmax keeps a running max and sum per
 //    head.  A request with a single chunk writes its bf16 output directly; otherwise
