@@ -189,3 +189,41 @@ def test_calls_on_a_side_stream_match_the_default_stream(cuda_lib):
     assert cuda_lib.device_status(side) == 0
     for (o1, l1), (o2, l2) in zip(ref, got):
         assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_batches_beyond_the_plans_shared_memory_path(cuda_lib):
+    """Batches of more than 2048 requests make the prefill plan keep its per-request
+    arrays in global memory instead of shared memory; 3000 short requests go through the
+    ragged prefill, the paged prefill and the decode, checked against the oracle on a
+    sample of requests."""
+    import oracle
+    from gpu_util import check_rows
+    rng = np.random.default_rng(91)
+    batch = 3000
+    qo = rng.integers(1, 4, batch).tolist()
+    kv = [q + int(x) for q, x in zip(qo, rng.integers(0, 60, batch))]
+    case = W.ragged_case(qo, kv, 8, 2, 128, causal=True, seed=92, device="cuda")
+    o, lse = cuda_lib.ragged_prefill(case.q, case.k, case.v, case.q_indptr, case.kv_indptr)
+    pc = W.paged_case(kv, 8, 2, 128, page_size=16, qo_lens=qo, seed=93, device="cuda")
+    po, pl = cuda_lib.paged_prefill(pc.q, pc.k_pages, pc.v_pages, pc.q_indptr, pc.page_table,
+                                    pc.kv_lens_t)
+    dc = W.paged_case(kv, 8, 2, 128, page_size=16, seed=94, device="cuda")
+    do, dl = cuda_lib.paged_decode(dc.q, dc.k_pages, dc.v_pages, dc.page_table, dc.kv_lens_t)
+    torch.cuda.synchronize()
+    assert cuda_lib.device_status() == 0
+    qi = case.q_indptr.tolist()
+    pick = sorted(set([0, batch - 1] + rng.choice(batch, 40, replace=False).tolist()))
+    rows = np.array([(t * 8 + h) for b in pick for t in range(qi[b], qi[b + 1])
+                     for h in range(8)], dtype=np.int64)
+    ro, rl = oracle.ragged_attention(case.q, case.k, case.v, case.q_indptr, case.kv_indptr,
+                                     8, 2, True, case.sm_scale, rows=rows)
+    idx = torch.as_tensor(rows, device="cuda")
+    check_rows(o.reshape(-1, 128)[idx], lse.reshape(-1)[idx], ro, rl, "ragged, 3000 requests")
+    ro, rl = oracle.paged_attention(pc.q, pc.q_indptr, pc.k_pages, pc.v_pages, pc.page_table,
+                                    pc.kv_lens_t, 8, 2, True, pc.sm_scale, rows=rows)
+    check_rows(po.reshape(-1, 128)[idx], pl.reshape(-1)[idx], ro, rl, "paged, 3000 requests")
+    drows = np.array([b * 8 + h for b in pick for h in range(8)], dtype=np.int64)
+    ro, rl = oracle.paged_attention(dc.q, dc.q_indptr, dc.k_pages, dc.v_pages, dc.page_table,
+                                    dc.kv_lens_t, 8, 2, True, dc.sm_scale, rows=drows)
+    didx = torch.as_tensor(drows, device="cuda")
+    check_rows(do.reshape(-1, 128)[didx], dl.reshape(-1)[didx], ro, rl, "decode, 3000 requests")
