@@ -105,7 +105,14 @@ int ensure_workspace(DeviceState& st, size_t need, cudaStream_t stream) {
     }
     if (cs != cudaStreamCaptureStatusNone) return PGQA_ERR_WORKSPACE;
     size_t bytes = need > kDefaultWorkspace ? align_up(need, 1u << 20) : kDefaultWorkspace;
+    // a status still pending from an earlier call (and its diagnostic words) moves to the
+    // new buffer rather than being lost with the old one
+    WsHeader keep{};
+    bool carry = false;
     if (st.ws != nullptr) {
+        carry = cudaMemcpy(&keep, st.ws, sizeof(WsHeader), cudaMemcpyDeviceToHost) == cudaSuccess &&
+                keep.status != 0;
+        cudaGetLastError();
         cudaFree(st.ws);  // synchronises the device: no kernel still uses the old buffer
         st.ws = nullptr;
         st.ws_bytes = 0;
@@ -118,6 +125,17 @@ int ensure_workspace(DeviceState& st, size_t need, cudaStream_t stream) {
     if (cudaMemset(p, 0, kWsArrays) != cudaSuccess) {
         cudaFree(p);
         return PGQA_ERR_CUDA;
+    }
+    if (carry) {
+        WsHeader h{};
+        const int* from = reinterpret_cast<const int*>(&keep);
+        int* to = reinterpret_cast<int*>(&h);
+        to[0] = from[0];  // the status word
+        for (int i = kDiagFlag; i < kDiagFlag + kDiagWords; ++i) to[i] = from[i];
+        if (cudaMemcpy(p, &h, sizeof(WsHeader), cudaMemcpyHostToDevice) != cudaSuccess) {
+            cudaFree(p);
+            return PGQA_ERR_CUDA;
+        }
     }
     st.ws = p;
     st.ws_bytes = bytes;

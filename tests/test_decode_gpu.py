@@ -164,3 +164,18 @@ def test_merge_modes_give_the_same_bits(cuda_lib):
                                        pc.kv_lens_t[:1], kv[:1], [1], 16, 32, 8, 128, True,
                                        pc.sm_scale))
     check_rows(o1[0].float().cpu(), l1[0].cpu(), ro, rl, "request 0")
+
+
+def test_pending_status_survives_workspace_growth(cuda_lib):
+    """A device error left unread by one call is still reported after a later call made
+    the library grow its workspace (the status word moves to the new buffer)."""
+    pc = W.paged_case([40], 8, 2, 128, page_size=16, seed=37, device="cuda")
+    pc.page_table[0, 1] = pc.num_pages + 5  # a page id outside the pool
+    run_gpu(cuda_lib, pc)  # leaves PGQA_DEV_BOUNDS pending
+    # 2048 requests with 32k-key tables: about 1 GB of split-KV partial results, more than
+    # the default workspace, so this call reallocates it
+    big = W.paged_case([1] * 2048, 32, 8, 128, page_size=16, stride=2048, seed=38,
+                       device="cuda")
+    run_gpu(cuda_lib, big)
+    assert cuda_lib.device_status() == -6
+    assert cuda_lib.device_status() == 0
