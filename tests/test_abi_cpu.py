@@ -244,3 +244,20 @@ def test_binding_refuses_cpu_tensors(api):
     ip = torch.tensor([0, 4], dtype=torch.int32)
     with pytest.raises((ValueError, TypeError, RuntimeError, AssertionError)):
         api.ragged_prefill(q, q[:, :1].contiguous(), q[:, :1].contiguous(), ip, ip)
+
+
+def test_the_product_package_never_imports_the_oracle():
+    """The oracle is test infrastructure: nothing in the package (binding, build, inputs)
+    may import it, so the product path has no CPU route to an answer."""
+    import ast
+    from pathlib import Path
+    pkg = Path(__file__).resolve().parents[1] / "paged_gqa_attention_varlen_gb300"
+    for path in pkg.rglob("*.py"):
+        tree = ast.parse(path.read_text())
+        for node in ast.walk(tree):
+            names = []
+            if isinstance(node, ast.Import):
+                names = [a.name for a in node.names]
+            elif isinstance(node, ast.ImportFrom):
+                names = [node.module or ""]
+            assert not any(n == "oracle" or n.startswith("oracle.") for n in names), path
