@@ -78,6 +78,13 @@ enum {
  *       j <= i + kv_len - qo_len  (bottom-right aligned); else every key of its request.
  *   sm_scale: scores are sm_scale * q.k (any finite value, 0 allowed).
  *
+ * Split: with head_dim 128, a call whose work list would have fewer than two items per
+ * SM cuts each request's keys into chunks of 2048 and merges the chunks' partial
+ * results by their log-sum-exp (when the partial rows fit in the workspace).  The choice
+ * is made on the device from the whole call, and the chunks of a request depend on that
+ * request alone, so among calls that take the same choice a request's results do not
+ * depend on the rest of the batch, bit for bit.
+ *
  * Supported: head_dim 128 or 256; num_qo_heads a multiple of num_kv_heads with group
  * size G = num_qo_heads / num_kv_heads dividing 128.  batch == 0 returns PGQA_OK at once.
  * Errors: PGQA_ERR_INVALID_ARG for NULL/misaligned pointers or bad counts,
@@ -119,6 +126,8 @@ int pgqa_ragged_prefill_bf16(const void* q, const void* k, const void* v, void* 
  *       j <= i + kv_len - qo_len; else every key of its request.
  *   Key slots past kv_lens[b] in a request's last page are never used, so whatever they
  *   hold (even NaN) cannot reach the output.
+ *   Split-KV for short work lists (a few requests with few query rows over long keys) as
+ *   for pgqa_ragged_prefill_bf16.
  *
  * Supported: head_dim 128 or 256; page_size 16, 32, 64 or 128; G = num_qo_heads /
  * num_kv_heads dividing 128.  batch == 0 returns PGQA_OK at once.  Errors as for
