@@ -24,6 +24,8 @@
 //  * merge_kernel: each (request, head) with more than one chunk combines the partials
 //    with weights exp(lse_c - max lse), in groups of 8 chunks; a warp per row, or a CTA
 //    per row when there are few rows (same arithmetic, same order).
+#include <atomic>
+
 #include "ptx.cuh"
 
 namespace pgqa {
@@ -599,16 +601,20 @@ cudaError_t prepare_page_maps(Params& p, const void* k_pages, const void* v_page
                               long long page_stride, long long slot_stride,
                               long long head_stride, bool kv8) {
     const int eb = kv8 ? 1 : 2;  // bytes per element
-    static EncodeTiledFn encode = nullptr;
-    if (encode == nullptr) {
+    // resolved once; a function-local static is initialised exactly once even when the
+    // main entry points and the allocation-free one (different locks) race to first use
+    static const EncodeTiledFn encode = []() -> EncodeTiledFn {
         void* fn = nullptr;
         cudaDriverEntryPointQueryResult q;
-        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                                         cudaEnableDefault, &q);
-        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
-            return e != cudaSuccess ? e : cudaErrorNotSupported;
-        encode = reinterpret_cast<EncodeTiledFn>(fn);
-    }
+        const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn,
+                                                               12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        return reinterpret_cast<EncodeTiledFn>(fn);
+    }();
+    if (encode == nullptr) return cudaErrorNotSupported;
     const cuuint64_t dims[4] = {(cuuint64_t)HEAD_DIM, (cuuint64_t)page_size,
                                 (cuuint64_t)num_kv_heads, (cuuint64_t)(num_pages > 0 ? num_pages : 1)};
     const cuuint64_t strides[3] = {(cuuint64_t)slot_stride * eb, (cuuint64_t)head_stride * eb,
@@ -630,11 +636,15 @@ cudaError_t prepare_page_maps(Params& p, const void* k_pages, const void* v_page
 
 template <int G, bool KV8>
 static cudaError_t launch_decode_g(const Params& p, int num_sms, cudaStream_t stream) {
-    static int blocks_per_sm[64] = {};
+    // per device, set up on first use; the entries are atomics because the main entry
+    // points and the allocation-free one hold different locks (a repeated set-up is
+    // harmless: it computes the same value)
+    static std::atomic<int> blocks_per_sm[64];
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) dev = 0;
-    if (blocks_per_sm[dev] == 0) {
+    int bps = blocks_per_sm[dev].load(std::memory_order_acquire);
+    if (bps == 0) {
         cudaError_t e = cudaFuncSetAttribute(decode_tma_kernel<G, KV8>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess) return e;
@@ -642,9 +652,10 @@ static cudaError_t launch_decode_g(const Params& p, int num_sms, cudaStream_t st
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_tma_kernel<G, KV8>, WARPS * 32,
                                                           SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        blocks_per_sm[dev] = n > 0 ? n : 1;
+        bps = n > 0 ? n : 1;
+        blocks_per_sm[dev].store(bps, std::memory_order_release);
     }
-    const int grid = num_sms * blocks_per_sm[dev];
+    const int grid = num_sms * bps;
     decode_tma_kernel<G, KV8><<<grid, WARPS * 32, SMEM_BYTES, stream>>>(p);
     return cudaGetLastError();
 }

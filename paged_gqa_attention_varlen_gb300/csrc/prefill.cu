@@ -36,6 +36,8 @@
 //  * merge_kernel combines split-KV partial results (fp32 O, lse) per (token, head).
 //  * GQA packing: a 128-row Q tile holds 128/G tokens x the G query heads that share a
 //    KV head (3-D TMA box), so each K/V tile is read once for all G heads.
+#include <atomic>
+
 #include "ptx.cuh"
 
 namespace pgqa {
@@ -1593,15 +1595,15 @@ static cudaError_t launch_dependent(Kernel kernel, int grid, int threads, int sm
 
 template <int D, bool PAGED>
 cudaError_t launch_attention(const Params& p, int grid, cudaStream_t stream) {
-    static bool configured[64] = {};
+    static std::atomic<bool> configured[64];  // per device, set once (repeats are harmless)
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !configured[dev]) {
+    if (dev >= 0 && dev < 64 && !configured[dev].load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(attention_kernel<D, PAGED>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              Cfg<D>::SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        configured[dev] = true;
+        configured[dev].store(true, std::memory_order_release);
     }
     return launch_dependent(attention_kernel<D, PAGED>, grid, THREADS, Cfg<D>::SMEM_BYTES, stream,
                             p);
@@ -1609,15 +1611,15 @@ cudaError_t launch_attention(const Params& p, int grid, cudaStream_t stream) {
 
 template <bool PAGED>
 cudaError_t launch_attention_pair(const Params& p, int grid, cudaStream_t stream) {
-    static bool configured[64] = {};
+    static std::atomic<bool> configured[64];  // per device, set once (repeats are harmless)
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !configured[dev]) {
+    if (dev >= 0 && dev < 64 && !configured[dev].load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(attention_pair_kernel<PAGED>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              PairCfg::SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        configured[dev] = true;
+        configured[dev].store(true, std::memory_order_release);
     }
     return launch_dependent(attention_pair_kernel<PAGED>, grid, PAIR_THREADS, PairCfg::SMEM_BYTES,
                             stream, p);
@@ -1630,14 +1632,14 @@ cudaError_t launch_merge(const Params& p, int num_sms, cudaStream_t stream) {
 cudaError_t launch_plan(const PlanParams& pp, const CUtensorMap& tq, const CUtensorMap& tk,
                         const CUtensorMap& tv, cudaStream_t stream) {
     constexpr int kDyn = PLAN_STAGE_UNITS * (int)sizeof(WorkItem);
-    static bool attr_set[64] = {};  // per device (callers hold the library lock)
+    static std::atomic<bool> attr_set[64];  // per device, set once (repeats are harmless)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!attr_set[dev]) {
+    if (!attr_set[dev].load(std::memory_order_acquire)) {
         const cudaError_t e =
             cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDyn);
         if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
+        attr_set[dev].store(true, std::memory_order_release);
     }
     plan_kernel<<<1, PLAN_THREADS, kDyn, stream>>>(pp, tq, tk, tv);
     return cudaGetLastError();
