@@ -3,12 +3,15 @@
 One step = one ragged prefill over the 16-request hd128 workload (16 requests, lengths
 U{128..4096}, 32 qo / 8 kv heads, causal) followed by one paged decode over the
 256-request workload (kv U{512..32768}, page 16, 32 / 8 heads, split-KV + merge), both
-through the C ABI (libpgqa) on inputs already resident in HBM.  Both inputs exceed the
-129 MB L2 (0.42 GB and 17.4 GB), so no flush is needed between steps.
+through the C ABI (libpgqa) on inputs already resident in HBM.  Both exceed the 129 MB
+L2 (the prefill moves 0.81 GB of Q, K, V, O and lse for the seed-0 draw of 39,332 query
+tokens; the decode reads 16.3 GB of K/V), so no flush is needed between steps.
 
 Printed (rank 0, one JSON line): value = prefill TFLOP/s (causal-visible pairs only,
-4 * d flops per pair and query head); the decode KV GB/s sits under "secondary".  Each
-carries its roofline against MEASURED_PEAKS.json.  `e2e` repeats the measurement with
+4 * d flops per pair and query head), with the prefill's tok/s (query tokens / s) beside
+it; the decode KV GB/s sits under "secondary".  Each carries its roofline against
+MEASURED_PEAKS.json, with the algorithmic bytes per launch next to the measured DRAM
+traffic.  `e2e` repeats the measurement with
 host-resident inputs copied in (pinned memory) and outputs copied out every step.
 `cpu_baseline` times the float64 oracle on a bounded row sample on the host cores.
 The e2e steps run pipelined, as a serving loop would: step s + 1's inputs are copied in on
@@ -58,6 +61,19 @@ def prefill_flops(qo_lens, kv_lens, hq, d, causal=True):
 
 def decode_kv_bytes(kv_lens, hk, d):
     return sum(kv_lens) * hk * d * 2 * 2
+
+
+def prefill_algorithmic_bytes(qo_lens, kv_lens, hq, hk, d):
+    """Bytes a prefill must move at least once: Q, K, V and O (bf16) and lse (fp32)."""
+    tq, tk = sum(qo_lens), sum(kv_lens)
+    return tq * hq * d * 2 * 2 + tk * hk * d * 2 * 2 + tq * hq * 4
+
+
+def decode_algorithmic_bytes(kv_lens, hq, hk, d, max_pages):
+    """K/V plus q, o (bf16), lse (fp32), the page table and the lengths (int32)."""
+    b = len(kv_lens)
+    return decode_kv_bytes(kv_lens, hk, d) + b * hq * d * 2 * 2 + b * hq * 4 + \
+        b * max_pages * 4 + b * 4
 
 
 def load_peaks():
@@ -237,7 +253,8 @@ def bench_config():
                        "num_qo_heads": ds["num_qo_heads"], "num_kv_heads": ds["num_kv_heads"],
                        "head_dim": ds["head_dim"],
                        "kv_bytes": decode_kv_bytes(dkv, ds["num_kv_heads"], ds["head_dim"])},
-            "l2": "inputs larger than L2 (0.42 GB prefill, 17.4 GB decode), no flush"}
+            "l2": "inputs larger than L2 (0.81 GB prefill Q/K/V/O/lse, 16.3 GB decode K/V), "
+                  "no flush"}
 
 
 def bench_reference(args, ws, rank):
@@ -283,7 +300,12 @@ def bench_gpu(args, ws, rank, local):
     pf = W.config(PREFILL_WORKLOAD, device=dev)
     dc = W.config(DECODE_WORKLOAD, device=dev)
     pf_flops = prefill_flops(pf.qo_lens, pf.kv_lens, pf.num_qo_heads, pf.head_dim)
+    pf_tokens = sum(pf.qo_lens)
+    pf_alg_bytes = prefill_algorithmic_bytes(pf.qo_lens, pf.kv_lens, pf.num_qo_heads,
+                                             pf.num_kv_heads, pf.head_dim)
     dc_bytes = decode_kv_bytes(dc.kv_lens, dc.num_kv_heads, dc.head_dim)
+    dc_alg_bytes = decode_algorithmic_bytes(dc.kv_lens, dc.num_qo_heads, dc.num_kv_heads,
+                                            dc.head_dim, dc.page_table.shape[1])
     o_pf = torch.empty_like(pf.q)
     l_pf = torch.empty(pf.q.shape[:2], dtype=torch.float32, device=dev)
     o_dc = torch.empty_like(dc.q)
@@ -423,6 +445,7 @@ def bench_gpu(args, ws, rank, local):
                  "decode_ms_per_launch": graph_ms(decode, dev, args.graph_reps),
                  "reps": args.graph_reps}
         graph["prefill_tflops"] = pf_flops / (graph["prefill_ms_per_launch"] / 1e3) / 1e12
+        graph["prefill_tok_s"] = pf_tokens / (graph["prefill_ms_per_launch"] / 1e3)
         graph["decode_gbs"] = dc_bytes / (graph["decode_ms_per_launch"] / 1e3) / 1e9
         if api.device_status() != 0:
             raise RuntimeError("device status after the graph replays is not ok")
@@ -455,11 +478,13 @@ def bench_gpu(args, ws, rank, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": bench_config(),
+        "tok_s": pf_tokens * ws * args.steps / (pf_total / 1e3),
         "roofline": {"bound": "tensor", "kernel": "prefill (plan + attention launch pair)",
                      "achieved": pf_achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": pf_achieved / peaks["bf16_tflops"],
                      "peak_source": peaks["source"] + " burst bf16",
-                     "traffic": pf_tr},
+                     "traffic": pf_tr, "algorithmic_bytes": pf_alg_bytes,
+                     "traffic_over_algorithmic": (pf_tr / pf_alg_bytes) if pf_tr else None},
         "secondary": {
             "metric": "paged decode KV GB/s", "value": dc_gbs, "unit": "GB/s",
             "ms_per_launch": dc_launch_ms,
@@ -467,7 +492,8 @@ def bench_gpu(args, ws, rank, local):
                          "achieved": dc_achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": dc_achieved / peaks["hbm_gbs"],
                          "peak_source": peaks["source"] + " copy bandwidth",
-                         "traffic": dc_tr},
+                         "traffic": dc_tr, "algorithmic_bytes": dc_alg_bytes,
+                         "traffic_over_algorithmic": (dc_tr / dc_alg_bytes) if dc_tr else None},
             "e2e": {"value": d_e2e_value, "unit": "GB/s", "h2d_bytes_per_step": d_h2d,
                     "d2h_bytes_per_step": d_d2h,
                     "note": "KV cache resident (serving state); q, page table, lengths in"}},
@@ -477,6 +503,7 @@ def bench_gpu(args, ws, rank, local):
         "cuda_graph": graph,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "tok_s": pf_tokens * ws * e2e_steps / (e2e_ms / 1e3),
                 "note": "pipelined: step s+1's inputs copied in on a second stream while step s "
                         "computes and copies out",
                 "serial_value": serial_value},

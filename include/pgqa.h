@@ -54,7 +54,9 @@ enum {
     PGQA_ERR_CUDA = -4,           /* a CUDA runtime/driver call failed */
     PGQA_ERR_DEVICE_TIMEOUT = -5, /* a kernel's bounded wait expired (device status) */
     PGQA_ERR_DEVICE_BOUNDS = -6,  /* bad indptr / page id seen on the device */
-    PGQA_ERR_NO_DEVICE = -7       /* no usable sm_103 GPU for this call */
+    PGQA_ERR_NO_DEVICE = -7,      /* no usable sm_103 GPU for this call */
+    PGQA_ERR_DEVICE_CAPACITY = -8 /* a prefill's work list outgrew the workspace (device
+                                     status); nothing was written */
 };
 
 /*
@@ -89,9 +91,14 @@ enum {
  * size G = num_qo_heads / num_kv_heads dividing 128.  batch == 0 returns PGQA_OK at once.
  * Errors: PGQA_ERR_INVALID_ARG for NULL/misaligned pointers or bad counts,
  * PGQA_ERR_UNSUPPORTED for other shapes, PGQA_ERR_WORKSPACE if the workspace is too
- * small while the stream is being captured, PGQA_ERR_CUDA on a launch failure.  A
+ * small while the stream is being captured (or a caller-supplied workspace cannot hold
+ * the per-request arrays plus 4096 work items), PGQA_ERR_CUDA on a launch failure.  A
  * decreasing or negative indptr is reported later as PGQA_ERR_DEVICE_BOUNDS by
- * pgqa_get_device_status() and nothing is written.
+ * pgqa_get_device_status() and nothing is written.  A work list (one item per kv head and
+ * pair of 128-row query tiles, or per such item and 2048-key chunk when split) longer than
+ * the workspace holds is reported as PGQA_ERR_DEVICE_CAPACITY and nothing is written:
+ * give the library a workspace of pgqa_workspace_bytes_prefill() bytes.  The lazily
+ * allocated 128 MiB workspace holds about 690,000 items.
  */
 int pgqa_ragged_prefill_bf16(const void* q, const void* k, const void* v, void* o, float* lse,
                              const int32_t* q_indptr, const int32_t* kv_indptr, int batch,
@@ -131,7 +138,8 @@ int pgqa_ragged_prefill_bf16(const void* q, const void* k, const void* v, void* 
  *
  * Supported: head_dim 128 or 256; page_size 16, 32, 64 or 128; G = num_qo_heads /
  * num_kv_heads dividing 128.  batch == 0 returns PGQA_OK at once.  Errors as for
- * pgqa_ragged_prefill_bf16; a kv_len outside its range or a decreasing q_indptr is
+ * pgqa_ragged_prefill_bf16 (including PGQA_ERR_DEVICE_CAPACITY for a work list longer
+ * than the workspace holds); a kv_len outside its range or a decreasing q_indptr is
  * reported as PGQA_ERR_DEVICE_BOUNDS by pgqa_get_device_status() and nothing is written;
  * a page id outside 0..num_pages-1 is reported the same way and that page is not read
  * (the rows that need it are then undefined).
@@ -256,32 +264,37 @@ int paged_decode_bf16(const void* q, const void* k_pages, const void* v_pages,
                       pgqa_stream_t stream);
 
 /*
- * Paged decode that allocates nothing (the source pages describe no such call; it is an
- * addition of this library).
+ * Paged decode that allocates nothing.  The source pages have no counterpart for this
+ * call: it is an addition of this library.
  *
- * Same arguments, results and supported shapes as pgqa_paged_decode_bf16, which lazily
- * cudaMalloc's a workspace for its split-KV partial results.  Callers that must not
- * allocate device memory use this one instead: work enqueued while a stream is being
- * captured into a CUDA graph, engines that give all device memory to their own pool at
- * start-up, and deployments that forbid allocation after initialisation.  Its scratch is a
- * fixed 16 MiB array in the library's own static device memory, which every GPU that
- * loads the library holds until the process exits.  The caller still passes (and owns)
- * every input and output.
+ * Same arguments, results and supported shapes as pgqa_paged_decode_bf16.  That call keeps
+ * its split-KV partial results in a workspace it cudaMalloc's on first use (and grows when
+ * a call needs more).  Some callers cannot let a library allocate device memory: serving
+ * engines that hand all free device memory to their own pool (KV cache, activations) at
+ * start-up, so a later cudaMalloc fails or fragments that pool; and deployments that
+ * forbid allocation once initialisation is over (real-time or certified systems, where
+ * every byte is budgeted up front).  This call keeps its scratch in a fixed 16 MiB array
+ * in the library's own static device memory instead, which every GPU that loads the
+ * library holds until the process exits.  The caller still passes (and owns) every input
+ * and output.
  *
  *   - Set-up: the first call on each device, with that device current, looks up the
- *     array's device address (cudaGetSymbolAddress).  Make that first call before any
- *     stream capture.
+ *     array's device address (cudaGetSymbolAddress) and keeps it.  Make that first call
+ *     before any stream capture.
  *   - Limit: returns PGQA_ERR_WORKSPACE, enqueueing nothing, when
  *       1024 + 256-rounded (2*batch+1)*4 + 256-rounded C*Hq*4 + C*Hq*head_dim*4 > 16 MiB,
  *     with C = batch * ceil(page_table_stride * page_size / K) partial chunks and K the
  *     chunk length chosen as for pgqa_paged_decode_bf16 (e.g. batch 16 with 32k-key
  *     tables at 32 query heads fits; batch 32 does not).
  *   - Sharing: every call on a device uses the same array and leaves its contents
- *     behind; calls that overlap on the GPU (different streams without ordering) race
- *     and corrupt each other's results.  Order them.
- *   - Device-side index errors (bad page id, bad kv_len) are handled as in
- *     pgqa_paged_decode_bf16 (the bad keys are skipped) but are not reported through
- *     pgqa_get_device_status.
+ *     behind (each call clears what it needs cleared); calls that overlap on the GPU
+ *     (different streams without ordering) race and corrupt each other's results.  Order
+ *     them.
+ *   - Device-side errors are not reported: pgqa_get_device_status() does not see this
+ *     call's status word.  Bad page ids and kv_lens are handled as in
+ *     pgqa_paged_decode_bf16 (the bad keys are skipped).  If a bounded wait expires (the
+ *     2 s device timeout), the warp gives up and the rows it was working on hold
+ *     undefined values; the call still returned PGQA_OK.
  * No cudaMalloc, cudaFree or other allocating call is made.
  */
 int pgqa_paged_decode_bf16_noalloc(const void* q, const void* k_pages, const void* v_pages,

@@ -21,6 +21,7 @@ PGQA_OK = 0
 STATUS_NAMES = {
     0: "ok", -1: "invalid argument", -2: "unsupported shape", -3: "workspace",
     -4: "CUDA error", -5: "device timeout", -6: "device bounds", -7: "no device",
+    -8: "device capacity (work list larger than the workspace)",
 }
 
 ABI_FUNCTIONS = (

@@ -110,10 +110,17 @@ int ensure_workspace(DeviceState& st, size_t need, cudaStream_t stream) {
     WsHeader keep{};
     bool carry = false;
     if (st.ws != nullptr) {
+        // Every kernel that may still set a status bit in the old buffer must finish before
+        // its header is read: a blocking copy orders itself only against the legacy default
+        // stream, not against the caller's non-blocking streams.
+        if (cudaDeviceSynchronize() != cudaSuccess) {
+            cudaGetLastError();
+            return PGQA_ERR_CUDA;
+        }
         carry = cudaMemcpy(&keep, st.ws, sizeof(WsHeader), cudaMemcpyDeviceToHost) == cudaSuccess &&
                 keep.status != 0;
         cudaGetLastError();
-        cudaFree(st.ws);  // synchronises the device: no kernel still uses the old buffer
+        cudaFree(st.ws);
         st.ws = nullptr;
         st.ws_bytes = 0;
     }
@@ -306,6 +313,7 @@ const char* pgqa_status_string(int s) {
         case PGQA_ERR_DEVICE_TIMEOUT: return "device wait timed out";
         case PGQA_ERR_DEVICE_BOUNDS: return "bad index data seen on the device";
         case PGQA_ERR_NO_DEVICE: return "no usable sm_103 device";
+        case PGQA_ERR_DEVICE_CAPACITY: return "work list larger than the workspace";
         default: return "unknown status";
     }
 }
@@ -385,7 +393,8 @@ int pgqa_get_device_status(pgqa_stream_t stream) {
         cudaMemset(static_cast<int*>(st.ws) + kDiagFlag, 0, kDiagWords * sizeof(int));
     }
     if (word & PGQA_DEV_TIMEOUT) return PGQA_ERR_DEVICE_TIMEOUT;
-    if (word & (PGQA_DEV_BOUNDS | PGQA_DEV_CAPACITY)) return PGQA_ERR_DEVICE_BOUNDS;
+    if (word & PGQA_DEV_BOUNDS) return PGQA_ERR_DEVICE_BOUNDS;
+    if (word & PGQA_DEV_CAPACITY) return PGQA_ERR_DEVICE_CAPACITY;
     return PGQA_OK;
 }
 

@@ -1,10 +1,10 @@
 // noalloc.cu -- a paged decode entry point that allocates nothing.
 //
 // pgqa_paged_decode_bf16 keeps its split-KV partial results in a library workspace that
-// it cudaMalloc's on first use.  Some callers cannot allow that: code running while a
-// stream is being captured into a CUDA graph, engines that hand every byte of device
-// memory to their own pool allocator at start-up, and hosts that forbid allocation after
-// initialisation (real-time or certified deployments).  This file gives them
+// it cudaMalloc's on first use.  Some callers cannot allow that: engines that hand every
+// byte of free device memory to their own pool allocator at start-up (a later cudaMalloc
+// fails or fragments the pool), and hosts that forbid allocation after initialisation
+// (real-time or certified deployments).  This file gives them
 // pgqa_paged_decode_bf16_noalloc, which runs the same plan / split-KV / merge kernels but
 // keeps their scratch in one fixed-size array in the library's own device memory.
 //
@@ -12,7 +12,9 @@
 // that loads the library holds it until the process exits.  In host code its name is
 // only a host-side stand-in, so the first call on each device resolves the device
 // address with cudaGetSymbolAddress (with that device current) and passes it to the
-// kernels.
+// kernels; that first call should come before any stream capture.  The status word the
+// kernels write lives in the array too, so device-side errors of this call (skipped bad
+// page ids, an expired bounded wait) are not reported to the caller.
 #include <cuda_runtime.h>
 
 #include <mutex>

@@ -226,6 +226,7 @@ __global__ void __launch_bounds__(PLAN_THREADS)
         if (tid == 0) {
             atomicOr(&p.hdr->status, PGQA_DEV_BOUNDS);
             p.hdr->n_items = 0;
+            p.hdr->merge_rows = 0;  // the merge kernel must not run on a stale count
         }
         return;
     }
@@ -294,7 +295,10 @@ __global__ void __launch_bounds__(PLAN_THREADS)
         }
         unit_total = unit_run;
         merge_total = merge_run;
-        if (part_total > p.part_capacity) split = false;  // the same in every thread
+        // the same in every thread: the split list must fit where the unsplit one would
+        if (part_total > p.part_capacity ||
+            (long long)unit_total * p.num_kv_heads > p.item_capacity)
+            split = false;
         __syncthreads();
     }
     if (!split) {
@@ -307,6 +311,7 @@ __global__ void __launch_bounds__(PLAN_THREADS)
         if (tid == 0) {
             atomicOr(&p.hdr->status, PGQA_DEV_CAPACITY);
             p.hdr->n_items = 0;
+            p.hdr->merge_rows = 0;
         }
         return;
     }

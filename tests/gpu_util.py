@@ -64,3 +64,43 @@ def gather_rows(o, lse, rows, num_qo_heads):
     o2 = o.reshape(-1, o.shape[-1]).index_select(0, idx)
     l2 = lse.reshape(-1).index_select(0, idx)
     return o2.float().cpu(), l2.float().cpu()
+
+
+def check_paged_decode_all_rows(pc, o, lse, oracle_fn, what="", requests_per_pass=32):
+    """Compare every output row of a one-row-per-request paged call with the oracle.
+
+    pc is a workloads.PagedCase on the GPU (bf16 or E4M3 pages), o [batch, Hq, d] and
+    lse [batch, Hq] the GPU results.  The requests' pages are gathered to the host
+    `requests_per_pass` requests at a time (a few GB of host memory at most), renumbered
+    0..n-1 with a page table of their own, and oracle_fn(sub_case) computes all of their
+    rows.
+    """
+    from paged_gqa_attention_varlen_gb300 import workloads as W
+    ps, d = pc.page_size, pc.head_dim
+    worst = 0.0
+    for b0 in range(0, pc.batch, requests_per_pass):
+        b1 = min(pc.batch, b0 + requests_per_pass)
+        lens = pc.kv_lens[b0:b1]
+        npg = [(n + ps - 1) // ps for n in lens]
+        ids = [pc.page_table[b, :n] for b, n in zip(range(b0, b1), npg) if n]
+        if ids:
+            idx = torch.cat(ids).long()
+            kp = pc.k_pages.index_select(0, idx).cpu()
+            vp = pc.v_pages.index_select(0, idx).cpu()
+        else:
+            kp = pc.k_pages[:1].cpu()
+            vp = pc.v_pages[:1].cpu()
+        table = torch.full((b1 - b0, max(1, max(npg))), -1, dtype=torch.int32)
+        off = 0
+        for i, n in enumerate(npg):
+            table[i, :n] = torch.arange(off, off + n, dtype=torch.int32)
+            off += n
+        sub = W.PagedCase(f"{pc.name}[{b0}:{b1}]", pc.q[b0:b1].cpu(),
+                          torch.arange(0, b1 - b0 + 1, dtype=torch.int32), kp, vp, table,
+                          torch.tensor(lens, dtype=torch.int32), list(lens), [1] * (b1 - b0), ps,
+                          pc.num_qo_heads, pc.num_kv_heads, d, True, pc.sm_scale, dict(pc.meta))
+        ro, rl = oracle_fn(sub)
+        err, _ = check_rows(o[b0:b1].reshape(-1, d).float().cpu(), lse[b0:b1].reshape(-1).cpu(),
+                            ro, rl, f"{what} requests {b0}..{b1 - 1}")
+        worst = max(worst, err)
+    return worst

@@ -54,8 +54,9 @@ def test_binding_lists_every_declared_function(api):
 
 def test_version_and_status_strings(api):
     assert api.lib.pgqa_version() >= 10000
-    for code in range(-7, 1):
-        assert api.lib.pgqa_status_string(code).decode()
+    for code in range(-8, 1):
+        assert api.lib.pgqa_status_string(code).decode() != "unknown status"
+        assert code in api.STATUS_NAMES
     assert api.lib.pgqa_status_string(123) == b"unknown status"
 
 
