@@ -94,7 +94,8 @@ def test_work_list_overflow_reports_capacity_and_writes_nothing(lazy_after):
     # 256 KiB buffer holds once the per-request arrays are carved out
     lens = [1] * 600
     case = W.ragged_case(lens, lens, 8, 8, 128, seed=207, device="cuda")
-    api.set_workspace(torch.empty(256 << 10, dtype=torch.uint8, device="cuda"))
+    buf = torch.empty(256 << 10, dtype=torch.uint8, device="cuda")  # kept alive while in use
+    api.set_workspace(buf)
     o = torch.full_like(case.q, 7.0)
     lse = torch.full(case.q.shape[:2], 9.0, dtype=torch.float32, device="cuda")
     _prefill(api, case, out=o, lse=lse)
