@@ -13,10 +13,10 @@ namespace prefill {
 cudaError_t launch_plan(const PlanParams&, const CUtensorMap&, const CUtensorMap&,
                         const CUtensorMap&, cudaStream_t);
 template <int D, bool PAGED>
-cudaError_t launch_attention(const Params&, int, cudaStream_t);
+cudaError_t launch_attention(const Params&, int, bool grouped, cudaStream_t);
 template <bool PAGED>
 cudaError_t launch_attention_pair(const Params&, int, cudaStream_t);
-cudaError_t launch_merge(const Params&, int, cudaStream_t);
+cudaError_t launch_merge(const Params&, int head_dim, int num_sms, cudaStream_t);
 }  // namespace prefill
 namespace decode {
 cudaError_t launch_plan(const PlanParams&, cudaStream_t);
@@ -194,6 +194,50 @@ int encode_pages_4d(CUtensorMap* map, const void* base, int d, int page_size, in
     return r == CUDA_SUCCESS ? PGQA_OK : PGQA_ERR_INVALID_ARG;
 }
 
+// 5-D views of a page pool for the grouped stage layout; a box lands as 8-row swizzle atoms
+// of each 64-column chunk 1 KB apart (the chunk dimension's stride is 128 bytes: the
+// head_dim row of a slot is contiguous), groups of 8 rows (d / 64) KB apart.
+//  - box_keys 16, when a page's (page, head) pairs are one dimension (page_stride a
+//    multiple of head_stride, page_heads = page_stride / head_stride >= heads):
+//    {64 columns, 8 slots, chunk, page_size / 8 halves, page * page_heads + head}, box
+//    {64, 8, d / 64, 2, 1} = 16 slots of one page and head;
+//  - box_keys 8 otherwise: {64 columns, slot, chunk, head, page}, box {64, 8, d / 64, 1, 1}.
+int encode_pages_grouped(CUtensorMap* map, const void* base, int d, int page_size, int heads,
+                         int num_pages, long long page_stride, long long slot_stride,
+                         long long head_stride, int* box_keys, int* page_heads) {
+    const long long np = num_pages > 0 ? num_pages : 1;
+    const long long ph = page_stride % head_stride == 0 ? page_stride / head_stride : 0;
+    const bool merged = ph >= heads && np * ph < (1LL << 31);
+    cuuint64_t dims[5];
+    cuuint64_t strides[4];
+    cuuint32_t box[5];
+    if (merged) {
+        const cuuint64_t dd[5] = {64, 8, (cuuint64_t)(d / 64), (cuuint64_t)(page_size / 8),
+                                  (cuuint64_t)(np * ph)};
+        const cuuint64_t ss[4] = {(cuuint64_t)slot_stride * 2, 128, (cuuint64_t)slot_stride * 16,
+                                  (cuuint64_t)head_stride * 2};
+        const cuuint32_t bb[5] = {64, 8, (cuuint32_t)(d / 64), 2, 1};
+        for (int i = 0; i < 5; ++i) dims[i] = dd[i], box[i] = bb[i];
+        for (int i = 0; i < 4; ++i) strides[i] = ss[i];
+    } else {
+        const cuuint64_t dd[5] = {64, (cuuint64_t)page_size, (cuuint64_t)(d / 64), (cuuint64_t)heads,
+                                  (cuuint64_t)np};
+        const cuuint64_t ss[4] = {(cuuint64_t)slot_stride * 2, 128, (cuuint64_t)head_stride * 2,
+                                  (cuuint64_t)page_stride * 2};
+        const cuuint32_t bb[5] = {64, 8, (cuuint32_t)(d / 64), 1, 1};
+        for (int i = 0; i < 5; ++i) dims[i] = dd[i], box[i] = bb[i];
+        for (int i = 0; i < 4; ++i) strides[i] = ss[i];
+    }
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    *box_keys = merged ? 16 : 8;
+    *page_heads = merged ? (int)ph : 0;
+    return r == CUDA_SUCCESS ? PGQA_OK : PGQA_ERR_INVALID_ARG;
+}
+
 // Element strides of a page pool: positive multiples of 16 bytes (the TMA rule for
 // global strides) and below 2^36 elements; elem_bytes is 2 (bf16) or 1 (E4M3).
 bool kv_strides_ok(long long page_stride, long long slot_stride, long long head_stride,
@@ -258,7 +302,7 @@ PrefillWs prefill_layout(const DeviceState& st, int batch, int head_dim) {
 // Plan and attention parameters shared by the ragged and paged prefill
 void fill_split(prefill::PlanParams& pp, prefill::Params& p, const PrefillWs& w, int batch,
                 int head_dim, int num_qo_heads, int num_sms) {
-    pp.split_ok = head_dim == 128 ? 1 : 0;  // the hd256 kernel runs unsplit
+    pp.split_ok = 1;
     pp.num_ctas = num_sms;
     pp.num_qo_heads = num_qo_heads;
     pp.part_capacity = w.part_capacity;
@@ -489,13 +533,15 @@ int pgqa_ragged_prefill_bf16(const void* q, const void* k, const void* v, void* 
     p.page_table_stride = 0;
     p.page_size = 0;
     p.num_pages = 0;
+    p.box_keys = 0;
+    p.page_heads = 0;
     fill_split(pp, p, lay, batch, head_dim, num_qo_heads, st->num_sms);
     e = prefill::launch_plan(pp, tq, tk, tv, s);
     if (e != cudaSuccess) return PGQA_ERR_CUDA;
     e = head_dim == 128 ? prefill::launch_attention_pair<false>(p, st->num_sms, s)
-                        : prefill::launch_attention<256, false>(p, st->num_sms, s);
+                        : prefill::launch_attention<256, false>(p, st->num_sms, false, s);
     if (e != cudaSuccess) return PGQA_ERR_CUDA;
-    return head_dim == 128 ? map_cuda(prefill::launch_merge(p, st->num_sms, s)) : PGQA_OK;
+    return map_cuda(prefill::launch_merge(p, head_dim, st->num_sms, s));
 }
 
 int pgqa_paged_prefill_bf16(const void* q, const void* k_pages, const void* v_pages, void* o,
@@ -566,12 +612,25 @@ int pgqa_paged_prefill_bf16_strided(const void* q, const void* k_pages, const vo
     if ((rc = encode_3d(&tq, q, head_dim, num_qo_heads, tpt, (uint64_t)head_dim * 2,
                         (uint64_t)num_qo_heads * head_dim * 2, 64, group, tpt)) != PGQA_OK)
         return rc;
-    if ((rc = encode_pages_4d(&tk, k_pages, head_dim, page_size, num_kv_heads, num_pages,
-                              page_stride, slot_stride, head_stride)) != PGQA_OK)
-        return rc;
-    if ((rc = encode_pages_4d(&tv, v_pages, head_dim, page_size, num_kv_heads, num_pages,
-                              page_stride, slot_stride, head_stride)) != PGQA_OK)
-        return rc;
+    // head_dim 256 with pages of up to 32 tokens: the grouped stage layout (a 64 KB K/V tile
+    // in 16 boxes of 4 KB rather than 4 * 128 / page_size boxes)
+    const bool grouped = head_dim == 256 && page_size <= 32;
+    int box_keys = 0, page_heads = 0;
+    if (grouped) {
+        if ((rc = encode_pages_grouped(&tk, k_pages, head_dim, page_size, num_kv_heads, num_pages,
+                                       page_stride, slot_stride, head_stride, &box_keys,
+                                       &page_heads)) != PGQA_OK ||
+            (rc = encode_pages_grouped(&tv, v_pages, head_dim, page_size, num_kv_heads, num_pages,
+                                       page_stride, slot_stride, head_stride, &box_keys,
+                                       &page_heads)) != PGQA_OK)
+            return rc;
+    } else {
+        if ((rc = encode_pages_4d(&tk, k_pages, head_dim, page_size, num_kv_heads, num_pages,
+                                  page_stride, slot_stride, head_stride)) != PGQA_OK ||
+            (rc = encode_pages_4d(&tv, v_pages, head_dim, page_size, num_kv_heads, num_pages,
+                                  page_stride, slot_stride, head_stride)) != PGQA_OK)
+            return rc;
+    }
 
     prefill::PlanParams pp;
     pp.q_indptr = q_indptr;
@@ -611,13 +670,15 @@ int pgqa_paged_prefill_bf16_strided(const void* q, const void* k_pages, const vo
     p.page_table_stride = page_table_stride;
     p.page_size = page_size;
     p.num_pages = num_pages;
+    p.box_keys = box_keys;
+    p.page_heads = page_heads;
     fill_split(pp, p, lay, batch, head_dim, num_qo_heads, st->num_sms);
     e = prefill::launch_plan(pp, tq, tk, tv, s);
     if (e != cudaSuccess) return PGQA_ERR_CUDA;
     e = head_dim == 128 ? prefill::launch_attention_pair<true>(p, st->num_sms, s)
-                        : prefill::launch_attention<256, true>(p, st->num_sms, s);
+                        : prefill::launch_attention<256, true>(p, st->num_sms, grouped, s);
     if (e != cudaSuccess) return PGQA_ERR_CUDA;
-    return head_dim == 128 ? map_cuda(prefill::launch_merge(p, st->num_sms, s)) : PGQA_OK;
+    return map_cuda(prefill::launch_merge(p, head_dim, st->num_sms, s));
 }
 
 int pgqa_paged_decode_bf16(const void* q, const void* k_pages, const void* v_pages,

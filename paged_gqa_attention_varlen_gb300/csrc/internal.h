@@ -94,6 +94,11 @@ struct Params {
     int page_table_stride;
     int page_size;             // 16, 32, 64 or 128
     int num_pages;
+    // grouped stage layout (head_dim 256, pages of up to 32 tokens): keys per TMA box (8,
+    // or 16 when a page's (page, head) pairs can be addressed as one tensor dimension) and
+    // that dimension's rows per page (page stride / head stride)
+    int box_keys;
+    int page_heads;
     // split-KV partial results: o [rows, D] fp32 normalised over the chunk's keys, lse
     // [rows] fp32 (natural log); merge bookkeeping from the plan
     float* part_o;

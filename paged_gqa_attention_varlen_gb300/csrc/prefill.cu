@@ -493,6 +493,61 @@ __device__ __forceinline__ void zero_stage_rows(uint32_t stage, int r0, int lane
     fence_async_smem();
 }
 
+// Grouped stage layout (paged K/V with small pages, head_dim 256): a 128-key stage is 16
+// groups of 8 keys, group i at i * (D / 64) KB, and within a group the 64-column chunks
+// (one 128-byte swizzle atom of 8 rows each) 1 KB apart.  A TMA box of a 5-D map fills
+// one or two consecutive groups, all chunks: with box_keys = 16 the map is {64 columns,
+// 8 slots, chunk, 8-slot half of a page, (page, head)} and a box is 16 slots of one page
+// and head; with box_keys = 8 (page and head kept as separate dimensions) it is
+// {64 columns, slot, chunk, head, page} and a box is 8 slots.  A 64 KB tile of 16-token
+// pages is then 8 (or 16) boxes instead of 32 boxes of 2 KB; the tensor core reads the
+// same swizzle atoms, with 8-row groups (D / 64) KB apart instead of 1 KB.
+// Lane l < 128 / box_keys of the producer warp loads box l of tile j: keys
+// box_keys * l .. + box_keys - 1 of the tile, in page (j * 128 + box_keys * l) / page_size.
+__device__ __forceinline__ int group_page_id(const int* pt_row, int j, int ps, int npg, int bk,
+                                             int lane) {
+    const int pg = (j * BN + bk * lane) / ps;
+    return lane < BN / bk && pg < npg ? __ldg(pt_row + pg) : -1;
+}
+__device__ __forceinline__ bool group_page_ok(int id, int j, int ps, int npg, int bk,
+                                              int num_pages, int lane, int* status) {
+    const bool in_use = lane < BN / bk && (j * BN + bk * lane) / ps < npg;
+    const bool ok = in_use && id >= 0 && id < num_pages;
+    if (in_use && !ok) atomicOr(status, PGQA_DEV_BOUNDS);
+    return ok;
+}
+// Warp-collective: lane 0 arms `bar` with the bytes of every valid box, then each lane with
+// a valid page loads its box of kv head g.
+template <int GROUP_BYTES>
+__device__ __forceinline__ void issue_group_boxes(uint32_t bar, int ps, int g, int bk,
+                                                  int page_heads, int lane, bool ok, uint32_t dst,
+                                                  const CUtensorMap* tm, int id) {
+    const int n = __popc(__ballot_sync(0xffffffffu, ok));
+    const int box_bytes = GROUP_BYTES * (bk / 8);
+    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(n * box_bytes));
+    __syncwarp();
+    if (ok) {
+        const int slot = (bk * lane) % ps;
+        if (bk == 16)
+            tma_load_5d(dst + lane * box_bytes, tm, bar, 0, 0, 0, slot / 8, id * page_heads + g);
+        else
+            tma_load_5d(dst + lane * box_bytes, tm, bar, 0, slot, 0, g, id);
+    }
+}
+// Zero rows r0..BN-1 of a grouped stage (warp-collective): whole 128-byte lines, fenced for
+// the tensor core's async-proxy reads.
+template <int CHUNKS>
+__device__ __forceinline__ void zero_group_rows(uint32_t stage, int r0, int lane) {
+    const int n16 = (BN - r0) * CHUNKS * 8;  // 16-byte units
+    for (int u = lane; u < n16; u += 32) {
+        const int r = r0 + u / (CHUNKS * 8), rest = u % (CHUNKS * 8);
+        const uint32_t a = stage + (r >> 3) * (CHUNKS * 1024) + (rest >> 3) * 1024 + (r & 7) * 128 +
+                           (rest & 7) * 16;
+        asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0) : "memory");
+    }
+    fence_async_smem();
+}
+
 // ---------------------------------------------------------------------- attention
 template <int D>
 struct Cfg {
@@ -502,9 +557,19 @@ struct Cfg {
     static constexpr int STAGES = D == 128 ? 4 : 2;
     static constexpr int TMEM_O = 256;                 // S buffers at columns 0 and 128
     static constexpr int TMEM_COLS = 512;
-    static constexpr int NUM_BARS = 2 + 2 * STAGES + 9;
+    static constexpr int NUM_BARS = 2 + 2 * STAGES + 10;
     static constexpr int SMEM_BYTES = 1024 + TILE_BYTES * (1 + STAGES) + 8 * NUM_BARS + 16;
 };
+
+// Growth of the running max (log2 units) below which O and l keep their old scale:
+// probabilities then stay below 2^8 and the fp32 accumulators are unaffected, while the
+// O rescale in tensor memory is skipped for most tiles.
+constexpr float kRescaleThreshold = 8.0f;
+
+// K/V tiles this item covers for a q tile of geometry x: [kt0, kt0 + n)
+__device__ __forceinline__ int item_tiles(const WorkItem& w, const Geo& x) {
+    return max(0, min(w.kt1, x.n_tiles) - w.kt0);
+}
 
 // The wait on tcgen05.ld results names the destination registers, so no use of them can
 // be scheduled before the wait.
@@ -521,9 +586,13 @@ __device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&r)[32]) {
         : "memory");
 }
 
-template <int D, bool PAGED>
+template <int D, bool PAGED, bool GROUPED>
 __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
     using C = Cfg<D>;
+    static_assert(!GROUPED || PAGED, "the grouped layout is for paged K/V");
+    // K/V stage layout: byte stride between 64-column chunks and between 8-row groups
+    constexpr uint32_t KV_CH = GROUPED ? 1024u : (uint32_t)C::CHUNK_BYTES;
+    constexpr uint32_t KV_SBO = GROUPED ? (uint32_t)C::CHUNKS * 1024u : 1024u;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -537,10 +606,16 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
     auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
     const int Q_FULL = 0, Q_EMPTY = 1, KV_FULL = 2, KV_EMPTY = 2 + C::STAGES;
     // FIX_READY / V_FIXED: paged K/V only, as in the two-tile kernel (warp 2 zeroes the
-    // rows past kv_len of an item's last V tile before its P.V)
+    // rows past kv_len of an item's last V tile before its P.V).
+    // PV_DONE completes after every P.V; the softmax waits on it only before rescaling O
+    // (when S_FULL of tile t has fired, the P.V of tile t - 2 is done and that of tile t
+    // cannot start, so PV_DONE is at most one phase from tile t - 1's: a parity wait is
+    // exact even though most tiles skip it).  PV_LAST completes once per item, after its
+    // last P.V: the epilogue waits on it.
     const int S_FULL = 2 + 2 * C::STAGES, P_FULL = S_FULL + 2, PV_DONE = P_FULL + 2,
               O_EMPTY = PV_DONE + 1, MMA_DRAIN = O_EMPTY + 1, FIX_READY = MMA_DRAIN + 1,
-              V_FIXED = FIX_READY + 1;
+              V_FIXED = FIX_READY + 1, PV_LAST = V_FIXED + 1;
+    static_assert(PV_LAST + 1 == C::NUM_BARS, "barrier count");
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -561,6 +636,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
         mbar_init(BAR(MMA_DRAIN), 1);
         mbar_init(BAR(FIX_READY), 1);
         mbar_init(BAR(V_FIXED), 32);
+        mbar_init(BAR(PV_LAST), 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -603,7 +679,9 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
                 it = snake_next(rr, n_items);
                 if (it >= 0) prefetch_l1(p.items + it);
                 const Geo x = geo_of(w, 0, G, p.causal);
-                if (x.n_tiles == 0) continue;
+                const int n = item_tiles(w, x);  // K/V tiles kt0 .. kt0 + n - 1
+                const int kt0 = w.kt0;
+                if (n == 0) continue;
                 ok = wait(BAR(Q_EMPTY), (q_count & 1) ^ 1);
                 if (!ok) break;
                 if (lane == 0) {
@@ -615,7 +693,8 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
                 }
                 ++q_count;
                 // consumption order of the MMA warp: K0, (K1, V0), (K2, V1), ..., V_{n-1}
-                const int nl = 2 * x.n_tiles;
+                // (tile indices relative to kt0)
+                const int nl = 2 * n;
                 auto tile_of = [&](int s, bool& is_k) -> int {
                     if (s == 0) {
                         is_k = true;
@@ -623,7 +702,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
                     }
                     if (s == nl - 1) {
                         is_k = false;
-                        return x.n_tiles - 1;
+                        return n - 1;
                     }
                     const int pr = (s - 1) >> 1;
                     is_k = ((s - 1) & 1) == 0;
@@ -634,11 +713,17 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
                 // paged: K_j and V_j share tile j's pages.  This lane's page ids of the
                 // last two K tiles issued (V loads reuse them) and of the next K tile,
                 // whose read is started one K load ahead.
-                int id_next = PAGED ? lane_page_id(pt_row, 0, ppt, npg, lane) : -1;
+                auto page_id = [&](int jj) -> int {
+                    if constexpr (GROUPED)
+                        return group_page_id(pt_row, jj, ps, npg, p.box_keys, lane);
+                    else return lane_page_id(pt_row, jj, ppt, npg, lane);
+                };
+                int id_next = PAGED ? page_id(kt0) : -1;
                 int id_last = -1, id_prev = -1, k_last = -1;
                 for (int s = 0; s < nl; ++s) {
                     bool is_k;
-                    const int j = tile_of(s, is_k);
+                    const int jr = tile_of(s, is_k);
+                    const int j = kt0 + jr;  // absolute K/V tile of the request
                     const uint32_t st = load_idx % C::STAGES;
                     ok = wait(BAR(KV_EMPTY + st), ((load_idx / C::STAGES) & 1) ^ 1);
                     if (!ok) break;
@@ -650,15 +735,24 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
                             id_prev = id_last;
                             id_last = id_next;
                             k_last = j;
-                            if (j + 1 < x.n_tiles) id_next = lane_page_id(pt_row, j + 1, ppt, npg, lane);
+                            if (jr + 1 < n) id_next = page_id(j + 1);
                         } else {
                             pid = j == k_last ? id_last : id_prev;
                         }
-                        const bool pg_ok = lane_page_ok(pid, j, ppt, npg, p.num_pages, lane, p.status);
-                        issue_page_boxes<C::CHUNKS, C::CHUNK_BYTES>(
-                            BAR(KV_FULL + st), ps, w.g, lane, false, 0, tm, 0, pg_ok,
-                            sKV + st * C::TILE_BYTES, tm, pid);
-                        if (lane == 0 && s == nl - 1 && x.n_tiles * BN > x.kv_len)
+                        if constexpr (GROUPED) {
+                            const bool pg_ok = group_page_ok(pid, j, ps, npg, p.box_keys,
+                                                             p.num_pages, lane, p.status);
+                            issue_group_boxes<(int)KV_SBO>(BAR(KV_FULL + st), ps, w.g, p.box_keys,
+                                                           p.page_heads, lane, pg_ok,
+                                                           sKV + st * C::TILE_BYTES, tm, pid);
+                        } else {
+                            const bool pg_ok = lane_page_ok(pid, j, ppt, npg, p.num_pages, lane,
+                                                            p.status);
+                            issue_page_boxes<C::CHUNKS, C::CHUNK_BYTES>(
+                                BAR(KV_FULL + st), ps, w.g, lane, false, 0, tm, 0, pg_ok,
+                                sKV + st * C::TILE_BYTES, tm, pid);
+                        }
+                        if (lane == 0 && s == nl - 1 && (kt0 + n) * BN > x.kv_len)
                             mbar_arrive(BAR(FIX_READY));
                     } else {
                         mbar_arrive_expect_tx(BAR(KV_FULL + st), C::TILE_BYTES);
@@ -707,16 +801,18 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
                     return false;
                 tc_fence_after();
                 const uint32_t p_col = (ctr & 1) ? 128u : 0u;
-                // V tile, MN-major: 16 keys = two 8-row swizzle groups (2048 bytes);
-                // consecutive 64-column chunks of the head dim are CHUNK_BYTES apart.
+                // V tile, MN-major: 16 keys = two 8-row swizzle groups (KV_SBO apart);
+                // consecutive 64-column chunks of the head dim are KV_CH apart.
                 // A descriptor's address field is addr / 16, so offsets add to it directly.
-                const uint64_t vdesc = sdesc_sw128(sKV + st * C::TILE_BYTES, C::CHUNK_BYTES, 1024);
+                const uint64_t vdesc = sdesc_sw128(sKV + st * C::TILE_BYTES, KV_CH, KV_SBO);
 #pragma unroll
                 for (int k = 0; k < BN / 16; ++k)
                     mma_ts(tmem_base + C::TMEM_O, tmem_base + p_col + k * 8,
-                           vdesc + (uint64_t)(k * 2048 / 16), IDESC_PV, (jj > 0 || k > 0) ? 1u : 0u);
+                           vdesc + (uint64_t)(k * 2 * KV_SBO / 16), IDESC_PV,
+                           (jj > 0 || k > 0) ? 1u : 0u);
                 mma_commit(BAR(KV_EMPTY + st));
                 mma_commit(BAR(PV_DONE));
+                if (jj == n - 1) mma_commit(BAR(PV_LAST));
                 return true;
             };
             int rr = -1;
@@ -726,9 +822,9 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
                 it = snake_next(rr, n_items);
                 if (it >= 0) prefetch_l1(p.items + it);
                 const Geo x = geo_of(w, 0, G, p.causal);
-                const int n = x.n_tiles;
+                const int n = item_tiles(w, x);
                 if (n == 0) continue;
-                const bool fix = PAGED && n * BN > x.kv_len;
+                const bool fix = PAGED && (w.kt0 + n) * BN > x.kv_len;
                 ok = mbar_wait_bounded(BAR(Q_FULL), q_count & 1, abort_flag, p.status);
                 ++q_count;
                 if (!ok) break;
@@ -742,12 +838,14 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
                     tc_fence_after();
                     const uint32_t ctr = tile_ctr + j;
                     const uint32_t s_col = (ctr & 1) ? 128u : 0u;
-                    const uint64_t kdesc = sdesc_sw128(sKV + st * C::TILE_BYTES, 16, 1024);
+                    const uint64_t kdesc = sdesc_sw128(sKV + st * C::TILE_BYTES, 16, KV_SBO);
                     const uint64_t qdesc = sdesc_sw128(sQ, 16, 1024);
 #pragma unroll
                     for (int k = 0; k < D / 16; ++k) {
-                        const uint64_t off = ((k >> 2) * C::CHUNK_BYTES + (k & 3) * 32) / 16;
-                        mma_ss(tmem_base + s_col, qdesc + off, kdesc + off, IDESC_QK, k > 0 ? 1u : 0u);
+                        const uint64_t qoff = ((k >> 2) * C::CHUNK_BYTES + (k & 3) * 32) / 16;
+                        const uint64_t koff = ((k >> 2) * KV_CH + (k & 3) * 32) / 16;
+                        mma_ss(tmem_base + s_col, qdesc + qoff, kdesc + koff, IDESC_QK,
+                               k > 0 ? 1u : 0u);
                     }
                     mma_commit(BAR(KV_EMPTY + st));
                     mma_commit(BAR(S_FULL + (ctr & 1)));
@@ -775,10 +873,12 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
             const WorkItem w = load_item(p.items, it);
             it = snake_next(rr, n_items);
             const Geo x = geo_of(w, 0, G, p.causal);
-            if (x.n_tiles == 0) continue;
-            const uint32_t last = load_idx + 2 * (uint32_t)x.n_tiles - 1;  // V_{n-1}
-            load_idx += 2 * (uint32_t)x.n_tiles;
-            if (x.n_tiles * BN <= x.kv_len) continue;
+            const int n = item_tiles(w, x);
+            if (n == 0) continue;
+            const uint32_t last = load_idx + 2 * (uint32_t)n - 1;  // V_{n-1}
+            load_idx += 2 * (uint32_t)n;
+            const int r0 = x.kv_len - (w.kt0 + n - 1) * BN;  // first row past kv_len
+            if (r0 >= BN) continue;
             ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(FIX_READY), fixes & 1, abort_flag,
                                                            p.status));
             if (ok)
@@ -787,16 +887,26 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
                                                   (last / C::STAGES) & 1, abort_flag, p.status));
             if (!ok) break;
             ++fixes;
-            zero_stage_rows<C::CHUNKS, C::CHUNK_BYTES>(sKV + (last % C::STAGES) * C::TILE_BYTES,
-                                                       x.kv_len - (x.n_tiles - 1) * BN, lane);
+            if constexpr (GROUPED)
+                zero_group_rows<C::CHUNKS>(sKV + (last % C::STAGES) * C::TILE_BYTES, r0, lane);
+            else
+                zero_stage_rows<C::CHUNKS, C::CHUNK_BYTES>(sKV + (last % C::STAGES) * C::TILE_BYTES,
+                                                           r0, lane);
             mbar_arrive(BAR(V_FIXED));
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------------ softmax / epilogue
+        // One thread per packed row.  The running max is kept in log2 units and O, l keep
+        // their scale until the max grows by more than kRescaleThreshold, so most tiles
+        // neither touch O in tensor memory nor wait for the previous P.V.  A split item
+        // (part >= 0) writes its O / l and lse in fp32 for the merge kernel.
         const int r = threadIdx.x - 128;                       // packed row = TMEM lane
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        const uint32_t o_addr = tmem_base + lane_base + C::TMEM_O;
         const int Hq = p.num_qo_heads;
-        uint32_t tile_ctr = 0;
+        const bool fast_scale = p.scale_log2 > 0.f;
+        const float c_eff = fast_scale ? p.scale_log2 : 1.f;
+        uint32_t tile_ctr = 0, items_done = 0;
         bool ok = true;
         int rr = -1;
         int it = snake_next(rr, n_items);
@@ -809,8 +919,11 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
             const int row_h = w.g * G + r % G;
             const bool valid = row_t < x.qo_len;
             const size_t out_row = (size_t)(x.q_start + row_t) * Hq + row_h;
-            if (x.n_tiles == 0) {
-                if (valid) {
+            const int n = item_tiles(w, x);
+            if (n == 0) {
+                // no visible key: zeros (a chunk of a split request without keys for this
+                // tile writes nothing; the merge leaves that chunk out)
+                if (valid && w.part < 0) {
                     uint4* op = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) +
                                                          out_row * D);
 #pragma unroll
@@ -821,23 +934,31 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
             }
             const int klim = p.causal ? min(row_t + x.kv_len - x.qo_len, x.kv_len - 1)
                                       : x.kv_len - 1;
-            float m = -INFINITY, l = 0.f;
-            for (int j = 0; j < x.n_tiles; ++j) {
-                const uint32_t ctr = tile_ctr + j;
+            float m_used = -INFINITY, l = 0.f;
+            for (int jr = 0; jr < n; ++jr) {
+                const int j = w.kt0 + jr;  // absolute K/V tile (masking)
+                const uint32_t ctr = tile_ctr + jr;
                 const uint32_t buf = ctr & 1;
                 ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(S_FULL + buf), (ctr >> 1) & 1,
                                                                abort_flag, p.status));
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t s_addr = tmem_base + lane_base + (buf ? 128u : 0u);
+                uint32_t u[4][32];
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) tmem_ld32(s_addr + cc * 32, u[cc]);
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) tmem_wait_ld_regs(u[cc]);
                 float s[BN];
 #pragma unroll
-                for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t u[32];
-                    tmem_ld32(s_addr + c * 32, u);
-                    tmem_wait_ld_regs(u);
+                for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(u[i]) * p.scale_log2;
+                    for (int i = 0; i < 32; ++i) s[cc * 32 + i] = __uint_as_float(u[cc][i]);
+                if (!fast_scale) {
+                    const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2);
+#pragma unroll
+                    for (int i = 0; i < BN; i += 2)
+                        f2_unpack(f2_mul(f2_pack(s[i], s[i + 1]), c2), s[i], s[i + 1]);
                 }
                 if (j >= x.n_unmasked) {
                     const int key0 = j * BN;
@@ -845,82 +966,122 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
                     for (int i = 0; i < BN; ++i)
                         if (key0 + i > klim) s[i] = -INFINITY;
                 }
-                float mt = s[0];
+                float mx[8];
 #pragma unroll
-                for (int i = 1; i < BN; ++i) mt = fmaxf(mt, s[i]);
-                const float m_new = fmaxf(m, mt);
-                const float m_use = m_new == -INFINITY ? 0.f : m_new;
-                const float alpha = ex2_approx(m - m_use);
-                float rs = 0.f;
+                for (int q = 0; q < 8; ++q) mx[q] = fmaxf(s[q], s[8 + q]);
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
+                for (int i = 16; i < BN; i += 16)
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) mx[q] = fmax3(mx[q], s[i + q], s[i + 8 + q]);
+                const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                                       fmaxf(mx[6], mx[7])) * c_eff;
+                const bool grow = mt > m_used + kRescaleThreshold;
+                const float m_new = grow ? mt : m_used;
+                const float alpha = grow ? ex2_approx(m_used - m_new) : 1.f;
+                const float neg = m_new == -INFINITY ? 0.f : -m_new;
+                const uint64_t c2 = f2_pack(c_eff, c_eff), n2 = f2_pack(neg, neg);
+                uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
                     uint32_t pk[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        const float p0 = ex2_approx(s[c * 64 + 2 * i] - m_use);
-                        const float p1 = ex2_approx(s[c * 64 + 2 * i + 1] - m_use);
-                        rs += p0 + p1;
+                        const int e = cc * 64 + 2 * i;
+                        float t0, t1;
+                        f2_unpack(f2_fma(f2_pack(s[e], s[e + 1]), c2, n2), t0, t1);
+                        const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
+                        if (i & 1) acc1 = f2_add(acc1, f2_pack(p0, p1));
+                        else acc0 = f2_add(acc0, f2_pack(p0, p1));
                         pk[i] = pack_bf16x2(p0, p1);
                     }
-                    tmem_st32(s_addr + c * 32, pk);
+                    tmem_st32(s_addr + cc * 32, pk);
                 }
-                l = l * alpha + rs;
-                if (j > 0) {
+                float a0, a1, a2, a3;
+                f2_unpack(acc0, a0, a1);
+                f2_unpack(acc1, a2, a3);
+                l = l * alpha + ((a0 + a1) + (a2 + a3));
+                if (jr > 0 && __any_sync(0xffffffffu, grow)) {
+                    // the previous tile's P.V must be done before O is rescaled
                     ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(PV_DONE), (ctr - 1) & 1,
                                                                    abort_flag, p.status));
                     if (!ok) break;
                     tc_fence_after();
-                    if (__any_sync(0xffffffffu, alpha < 1.f)) {
-                        const uint32_t o_addr = tmem_base + lane_base + C::TMEM_O;
+                    const uint64_t al2 = f2_pack(alpha, alpha);
 #pragma unroll 1
-                        for (int c = 0; c < D / 32; ++c) {
-                            uint32_t u[32];
-                            tmem_ld32(o_addr + c * 32, u);
-                            tmem_wait_ld_regs(u);
+                    for (int oc = 0; oc < D / 32; ++oc) {
+                        uint32_t v[32];
+                        tmem_ld32(o_addr + oc * 32, v);
+                        tmem_wait_ld_regs(v);
 #pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
-                            tmem_st32(o_addr + c * 32, u);
+                        for (int i = 0; i < 32; i += 2) {
+                            float o0, o1;
+                            f2_unpack(f2_mul(f2_pack(__uint_as_float(v[i]), __uint_as_float(v[i + 1])),
+                                             al2), o0, o1);
+                            v[i] = __float_as_uint(o0);
+                            v[i + 1] = __float_as_uint(o1);
                         }
+                        tmem_st32(o_addr + oc * 32, v);
                     }
                 }
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(BAR(P_FULL + buf));
-                m = m_new;
+                m_used = m_new;
             }
             if (!ok) break;
-            tile_ctr += x.n_tiles;
-            ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(PV_DONE), (tile_ctr - 1) & 1,
+            tile_ctr += n;
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(PV_LAST), items_done & 1,
                                                            abort_flag, p.status));
+            ++items_done;
             if (!ok) break;
             tc_fence_after();
             const float inv_l = l > 0.f ? 1.f / l : 0.f;
-            const uint32_t o_addr = tmem_base + lane_base + C::TMEM_O;
-            uint4* op = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + out_row * D);
+            const float lse_v = l > 0.f ? (m_used + log2f(l)) * 0.69314718055994531f : -INFINITY;
+            if (w.part >= 0) {
+                // split-KV partial: O / l in fp32 and the chunk's lse
+                const long long slot = (long long)w.part + (long long)row_t * Hq + row_h;
+                float4* op = reinterpret_cast<float4*>(p.part_o + slot * D);
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t u[32];
-                tmem_ld32(o_addr + c * 32, u);
-                tmem_wait_ld_regs(u);
-                if (valid) {
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(o_addr + c * 32, v);
+                    tmem_wait_ld_regs(v);
+                    if (valid) {
 #pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4) {
-                        uint4 q;
-                        q.x = pack_bf16x2(__uint_as_float(u[v4 * 8 + 0]) * inv_l,
-                                          __uint_as_float(u[v4 * 8 + 1]) * inv_l);
-                        q.y = pack_bf16x2(__uint_as_float(u[v4 * 8 + 2]) * inv_l,
-                                          __uint_as_float(u[v4 * 8 + 3]) * inv_l);
-                        q.z = pack_bf16x2(__uint_as_float(u[v4 * 8 + 4]) * inv_l,
-                                          __uint_as_float(u[v4 * 8 + 5]) * inv_l);
-                        q.w = pack_bf16x2(__uint_as_float(u[v4 * 8 + 6]) * inv_l,
-                                          __uint_as_float(u[v4 * 8 + 7]) * inv_l);
-                        op[c * 4 + v4] = q;
+                        for (int e = 0; e < 8; ++e)
+                            op[c * 8 + e] = make_float4(__uint_as_float(v[4 * e]) * inv_l,
+                                                        __uint_as_float(v[4 * e + 1]) * inv_l,
+                                                        __uint_as_float(v[4 * e + 2]) * inv_l,
+                                                        __uint_as_float(v[4 * e + 3]) * inv_l);
                     }
                 }
+                if (valid) p.part_lse[slot] = lse_v;
+            } else {
+                uint4* op = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) +
+                                                     out_row * D);
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(o_addr + c * 32, v);
+                    tmem_wait_ld_regs(v);
+                    if (valid) {
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4) {
+                            uint4 q;
+                            q.x = pack_bf16x2(__uint_as_float(v[v4 * 8 + 0]) * inv_l,
+                                              __uint_as_float(v[v4 * 8 + 1]) * inv_l);
+                            q.y = pack_bf16x2(__uint_as_float(v[v4 * 8 + 2]) * inv_l,
+                                              __uint_as_float(v[v4 * 8 + 3]) * inv_l);
+                            q.z = pack_bf16x2(__uint_as_float(v[v4 * 8 + 4]) * inv_l,
+                                              __uint_as_float(v[v4 * 8 + 5]) * inv_l);
+                            q.w = pack_bf16x2(__uint_as_float(v[v4 * 8 + 6]) * inv_l,
+                                              __uint_as_float(v[v4 * 8 + 7]) * inv_l);
+                            op[c * 4 + v4] = q;
+                        }
+                    }
+                }
+                if (valid && p.lse) p.lse[out_row] = lse_v;
             }
-            if (valid && p.lse)
-                p.lse[out_row] = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
             tc_fence_before();
             mbar_arrive(BAR(O_EMPTY));
         }
@@ -951,16 +1112,6 @@ struct PairCfg {
     static constexpr int SMEM_BYTES = 1024 + TILE_BYTES * (2 + STAGES) + 8 * NUM_BARS + 16;
 };
 
-// Growth of the running max (log2 units) below which O and l keep their old scale:
-// probabilities then stay below 2^8 and the fp32 accumulators are unaffected, while the
-// O rescale in tensor memory is skipped for most tiles.
-constexpr float kRescaleThreshold = 8.0f;
-
-
-// K/V tiles this item covers for a q tile of geometry x: [kt0, kt0 + n)
-__device__ __forceinline__ int item_tiles(const WorkItem& w, const Geo& x) {
-    return max(0, min(w.kt1, x.n_tiles) - w.kt0);
-}
 
 template <bool PAGED>
 __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const Params p) {
@@ -1513,9 +1664,10 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
 // One warp per (token, query head) row of a split request: the chunks that hold keys
 // visible to the row are combined with weights exp(lse_c - max lse) (FlashInfer
 // documentation, flashinfer.cascade "Merge Attention States").  Rows without a visible key
-// get zeros and lse = -inf.
+// get zeros and lse = -inf.  Lane l combines columns 4l .. 4l + 3 of each 128-column half.
+template <int D>
 __global__ void __launch_bounds__(256) merge_kernel(const Params p) {
-    constexpr int D = 128;
+    constexpr int NV = D / 128;  // float4s per lane
     // launched as a dependent of the attention kernel: its partial results are read from here
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int rows = p.hdr->merge_rows;
@@ -1538,42 +1690,56 @@ __global__ void __launch_bounds__(256) merge_kernel(const Params p) {
         for (int c = lane; c < nvis; c += 32) mx = fmaxf(mx, p.part_lse[slot(c)]);
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 acc[NV];
+#pragma unroll
+        for (int e = 0; e < NV; ++e) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
         float wsum = 0.f;
         if (mx != -INFINITY) {
             // chunks in index order, the loads of MU chunks issued before their arithmetic
             constexpr int MU = 4;
-            auto add = [&](float l, const float4& v) {
+            auto add = [&](float l, const float4 (&v)[NV]) {
                 const float wgt = __expf(l - mx);
                 wsum += wgt;
-                acc.x = fmaf(wgt, v.x, acc.x);
-                acc.y = fmaf(wgt, v.y, acc.y);
-                acc.z = fmaf(wgt, v.z, acc.z);
-                acc.w = fmaf(wgt, v.w, acc.w);
+#pragma unroll
+                for (int e = 0; e < NV; ++e) {
+                    acc[e].x = fmaf(wgt, v[e].x, acc[e].x);
+                    acc[e].y = fmaf(wgt, v[e].y, acc[e].y);
+                    acc[e].z = fmaf(wgt, v[e].z, acc[e].z);
+                    acc[e].w = fmaf(wgt, v[e].w, acc[e].w);
+                }
             };
-            auto row = [&](int c) {
-                return *reinterpret_cast<const float4*>(p.part_o + slot(c) * D + lane * 4);
+            auto row = [&](int c, float4 (&v)[NV]) {
+                const float4* r = reinterpret_cast<const float4*>(p.part_o + slot(c) * D);
+#pragma unroll
+                for (int e = 0; e < NV; ++e) v[e] = r[e * 32 + lane];
             };
             int c = 0;
             for (; c + MU <= nvis; c += MU) {
                 float l[MU];
-                float4 v[MU];
+                float4 v[MU][NV];
 #pragma unroll
                 for (int u = 0; u < MU; ++u) {
                     l[u] = p.part_lse[slot(c + u)];
-                    v[u] = row(c + u);
+                    row(c + u, v[u]);
                 }
 #pragma unroll
                 for (int u = 0; u < MU; ++u) add(l[u], v[u]);
             }
-            for (; c < nvis; ++c) add(p.part_lse[slot(c)], row(c));
+            for (; c < nvis; ++c) {
+                float4 v[NV];
+                row(c, v);
+                add(p.part_lse[slot(c)], v);
+            }
         }
         const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
         __nv_bfloat16* op = reinterpret_cast<__nv_bfloat16*>(p.o) + ((size_t)(q0 + t) * Hq + h) * D;
-        uint2 u;
-        u.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-        u.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-        *reinterpret_cast<uint2*>(op + lane * 4) = u;
+#pragma unroll
+        for (int e = 0; e < NV; ++e) {
+            uint2 u;
+            u.x = pack_bf16x2(acc[e].x * inv, acc[e].y * inv);
+            u.y = pack_bf16x2(acc[e].z * inv, acc[e].w * inv);
+            *reinterpret_cast<uint2*>(op + e * 128 + lane * 4) = u;
+        }
         if (lane == 0 && p.lse)
             p.lse[(size_t)(q0 + t) * Hq + h] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
     }
@@ -1598,20 +1764,29 @@ static cudaError_t launch_dependent(Kernel kernel, int grid, int threads, int sm
     return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
-template <int D, bool PAGED>
-cudaError_t launch_attention(const Params& p, int grid, cudaStream_t stream) {
+template <int D, bool PAGED, bool GROUPED>
+static cudaError_t launch_attention_t(const Params& p, int grid, cudaStream_t stream) {
     static std::atomic<bool> configured[64];  // per device, set once (repeats are harmless)
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !configured[dev].load(std::memory_order_acquire)) {
-        cudaError_t e = cudaFuncSetAttribute(attention_kernel<D, PAGED>,
+        cudaError_t e = cudaFuncSetAttribute(attention_kernel<D, PAGED, GROUPED>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              Cfg<D>::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         configured[dev].store(true, std::memory_order_release);
     }
-    return launch_dependent(attention_kernel<D, PAGED>, grid, THREADS, Cfg<D>::SMEM_BYTES, stream,
-                            p);
+    return launch_dependent(attention_kernel<D, PAGED, GROUPED>, grid, THREADS,
+                            Cfg<D>::SMEM_BYTES, stream, p);
+}
+
+// grouped: paged K/V through 5-D tensor maps filling the grouped stage layout
+template <int D, bool PAGED>
+cudaError_t launch_attention(const Params& p, int grid, bool grouped, cudaStream_t stream) {
+    if constexpr (PAGED) {
+        if (grouped) return launch_attention_t<D, true, true>(p, grid, stream);
+    }
+    return launch_attention_t<D, PAGED, false>(p, grid, stream);
 }
 
 template <bool PAGED>
@@ -1630,8 +1805,9 @@ cudaError_t launch_attention_pair(const Params& p, int grid, cudaStream_t stream
                             stream, p);
 }
 
-cudaError_t launch_merge(const Params& p, int num_sms, cudaStream_t stream) {
-    return launch_dependent(merge_kernel, num_sms * 2, 256, 0, stream, p);
+cudaError_t launch_merge(const Params& p, int head_dim, int num_sms, cudaStream_t stream) {
+    return head_dim == 256 ? launch_dependent(merge_kernel<256>, num_sms * 2, 256, 0, stream, p)
+                           : launch_dependent(merge_kernel<128>, num_sms * 2, 256, 0, stream, p);
 }
 
 cudaError_t launch_plan(const PlanParams& pp, const CUtensorMap& tq, const CUtensorMap& tk,
@@ -1650,8 +1826,8 @@ cudaError_t launch_plan(const PlanParams& pp, const CUtensorMap& tq, const CUten
     return cudaGetLastError();
 }
 
-template cudaError_t launch_attention<256, false>(const Params&, int, cudaStream_t);
-template cudaError_t launch_attention<256, true>(const Params&, int, cudaStream_t);
+template cudaError_t launch_attention<256, false>(const Params&, int, bool, cudaStream_t);
+template cudaError_t launch_attention<256, true>(const Params&, int, bool, cudaStream_t);
 template cudaError_t launch_attention_pair<false>(const Params&, int, cudaStream_t);
 template cudaError_t launch_attention_pair<true>(const Params&, int, cudaStream_t);
 

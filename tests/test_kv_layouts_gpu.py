@@ -28,10 +28,19 @@ def layouts(pc, layers=3, layer=1):
     out.append(("layer-slice", "NHD", stk[:, layer], stv[:, layer]))
     # an HND view of a permuted (non-contiguous) tensor: strides differ from a packed HND
     out.append(("hnd-view", "HND", pc.k_pages.permute(0, 2, 1, 3), pc.v_pages.permute(0, 2, 1, 3)))
+    # pages padded by 8 elements: the page stride is not a multiple of the head stride
+    n, ps, hk, d = pc.k_pages.shape
+    padded = []
+    for src in (pc.k_pages, pc.v_pages):
+        flat = torch.zeros((n, ps * hk * d + 8), device="cuda", dtype=torch.bfloat16)
+        view = flat.as_strided((n, ps, hk, d), (ps * hk * d + 8, hk * d, d, 1))
+        view.copy_(src)
+        padded.append(view)
+    out.append(("padded-pages", "NHD", padded[0], padded[1]))
     return out
 
 
-@pytest.mark.parametrize("d,ps", [(128, 16), (128, 64), (256, 32)])
+@pytest.mark.parametrize("d,ps", [(128, 16), (128, 64), (256, 16), (256, 32)])
 def test_paged_prefill_layouts_match_nhd_bitwise(cuda_lib, d, ps):
     pc = W.paged_case([500, 45, 1300], 16, 4, d, page_size=ps, qo_lens=[200, 45, 7],
                       seed=81 + d + ps, device="cuda")

@@ -66,7 +66,7 @@ def test_small_shapes(cuda_lib, shape):
     full_check(cuda_lib, pc, f"paged {shape}")
 
 
-@pytest.mark.parametrize("d,ps", [(128, 16), (128, 64), (256, 32)])
+@pytest.mark.parametrize("d,ps", [(128, 16), (128, 64), (256, 16), (256, 32), (256, 128)])
 def test_matches_ragged_prefill_bitwise(cuda_lib, d, ps):
     """The paged kernel and the ragged kernel see the same keys in the same tiles, so
     their results agree bit for bit."""
@@ -218,3 +218,38 @@ def test_split_kv_non_causal_and_short_requests(cuda_lib):
     pc2 = W.paged_case(kv, 16, 4, 128, page_size=32, qo_lens=qo, causal=True, seed=107,
                        device="cuda")
     full_check(cuda_lib, pc2, "split-KV causal mix")
+
+
+# head_dim 256 in the split regime: the hd256 kernel processes each chunk's tile range and
+# writes fp32 partial rows; the merge kernel combines 256-column rows.
+
+@pytest.mark.parametrize("ps", [16, 64])
+def test_split_kv_hd256_paged_short_list(cuda_lib, ps):
+    """Two requests with long cached prefixes (qo 200 / 37 over 9000 / 4100 keys), 16/4
+    heads: 12 q-tile items per kv head, cut into 2048-key chunks; all rows checked."""
+    pc = W.paged_case([9000, 4100], 16, 4, 256, page_size=ps, qo_lens=[200, 37], seed=111 + ps,
+                      device="cuda")
+    full_check(cuda_lib, pc, f"split-KV hd256 paged, page {ps}")
+
+
+def test_split_kv_hd256_ragged_and_paged_agree_bitwise(cuda_lib):
+    """The same split work in the ragged and the paged kernel: same chunks, tiles and
+    merge, so the same bits; plus a multi-token decode mix and the oracle."""
+    qo, kv = [4, 4, 1, 0, 9], [20000, 5000, 300, 700, 30]
+    pc = W.paged_case(kv, 16, 4, 256, page_size=16, qo_lens=qo, seed=117, device="cuda")
+    o_p, l_p = run_gpu(cuda_lib, pc)
+    ks, vs = [], []
+    for b, n in enumerate(kv):
+        pages = pc.page_table[b, :(n + 15) // 16].long()
+        ks.append(pc.k_pages[pages].reshape(-1, 4, 256)[:n])
+        vs.append(pc.v_pages[pages].reshape(-1, 4, 256)[:n])
+    kv_indptr = torch.tensor(np.concatenate([[0], np.cumsum(kv)]), dtype=torch.int32,
+                             device="cuda")
+    o_r, l_r = cuda_lib.ragged_prefill(pc.q, torch.cat(ks).contiguous(), torch.cat(vs).contiguous(),
+                                       pc.q_indptr, kv_indptr, causal=True, sm_scale=pc.sm_scale)
+    torch.cuda.synchronize()
+    assert cuda_lib.device_status() == 0
+    assert torch.equal(o_p, o_r) and torch.equal(l_p, l_r)
+    ro, rl = oracle_paged(pc)
+    check_rows(o_p.reshape(-1, 256).float().cpu(), l_p.reshape(-1).cpu(), ro, rl,
+               "split-KV hd256 decode mix")
