@@ -595,6 +595,19 @@ def bench_extra(api, W, dev, stream, dc, peaks):
                                                        stream=stream), stream)
             out["ragged_prefill_prefix_hd256"] = tensor_line(flops, ms, "prefix_hd256, ragged K/V")
         del pc, rc, o, lse
+    # head_dim 256 with a short work list: 2 requests of 256 query rows over 16k-key cached
+    # prefixes (16 / 4 heads): 16 q-tile items per kv head, split into 2048-key chunks
+    sqo, skv = [256, 256], [256 + 16384, 256 + 16384]
+    sc = W.ragged_case(sqo, skv, 16, 4, 256, causal=True, seed=5, device=dev)
+    so = torch.empty_like(sc.q)
+    sl = torch.empty(sc.q.shape[:2], dtype=torch.float32, device=dev)
+    ms = time_calls(lambda: api.ragged_prefill(sc.q, sc.k, sc.v, sc.q_indptr, sc.kv_indptr,
+                                               causal=True, sm_scale=sc.sm_scale, out=so, lse=sl,
+                                               stream=stream), stream, reps=20)
+    out["ragged_prefill_hd256_short_list"] = tensor_line(
+        prefill_flops(sqo, skv, 16, 256), ms,
+        "batch 2, qo 256 over 16k-key prefixes, 16/4 heads, d 256 (split-KV regime)")
+    del sc, so, sl
     # one 32k-token request, 64 / 8 heads (G = 8), K scaled by 3: long items, few boundaries
     lc = W.config("long", device=dev)
     lo = torch.empty_like(lc.q)
