@@ -20,8 +20,9 @@ cudaError_t launch_merge(const Params&, int head_dim, int num_sms, cudaStream_t)
 }  // namespace prefill
 namespace decode {
 cudaError_t launch_plan(const PlanParams&, cudaStream_t);
-cudaError_t launch_decode(const Params&, int group, bool kv8, int num_sms, cudaStream_t);
+cudaError_t launch_decode(const Params&, int group, int num_sms, cudaStream_t);
 cudaError_t launch_merge(const Params&, cudaStream_t);
+cudaError_t launch_decode_mma(const Params&, int group, int num_sms, cudaStream_t);
 cudaError_t prepare_page_maps(Params&, const void*, const void*, int, int, int, long long,
                               long long, long long, bool);
 }  // namespace decode
@@ -813,7 +814,9 @@ int paged_decode_impl(const void* q, const void* k_pages, const void* v_pages,
     if (decode::prepare_page_maps(p, k_pages, v_pages, num_pages, num_kv_heads, page_size,
                                   page_stride, slot_stride, head_stride, kv8) != cudaSuccess)
         return PGQA_ERR_INVALID_ARG;
-    e = decode::launch_decode(p, group, kv8, st->num_sms, s);
+    // E4M3 K/V: the dot products on the tensor cores (the CUDA cores convert bytes)
+    e = kv8 ? decode::launch_decode_mma(p, group, st->num_sms, s)
+            : decode::launch_decode(p, group, st->num_sms, s);
     if (e != cudaSuccess) return PGQA_ERR_CUDA;
     return map_cuda(decode::launch_merge(p, s));
 }

@@ -11,8 +11,9 @@
 // FlashInfer documentation, flashinfer.cascade "Merge Attention States" (how partial
 // results over disjoint key sets combine).
 //
-// Design: the path is bound by HBM bandwidth (about 4 flops per KV byte), so it runs on
-// the CUDA cores, not the tensor cores.
+// Design: with bf16 K/V the path is bound by HBM bandwidth (about 4 flops per KV byte), so
+// it runs on the CUDA cores, not the tensor cores.  (An E4M3 cache takes the tensor-core
+// decode of decode_mma.cu, which shares this file's plan and merge kernels.)
 //  * plan_kernel: sanitises kv_lens and cuts each request into chunks of `chunk` keys
 //    (1024, or 512 / 256 / 128 for calls with little work; chosen from the call's shape).
 //    For a given chunk length the cut depends on the request alone, so a request's
@@ -125,38 +126,6 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     return v;
 }
 
-__device__ __forceinline__ uint2 lds64(uint32_t addr) {
-    uint2 v;
-    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
-    return v;
-}
-
-// Two E4M3 values (low byte = element 0) -> one packed fp32 pair, exactly: E4M3 -> f16 is
-// exact (f16 has the range and the mantissa bits, NaN stays NaN), and f16 -> f32 is exact.
-// (An integer-ALU decoding, bits shifted into place and the exponent bias folded into q
-// and P, measured 14 % slower: the decode's issue slots, not the conversion pipe, bound
-// it.)
-__device__ __forceinline__ uint64_t e4m3x2_to_pair(uint32_t two_bytes) {
-    uint32_t h;
-    asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
-        : "=r"(h)
-        : "r"(two_bytes));
-    float lo, hi;
-    asm("{\n\t.reg .f16 l, u;\n\tmov.b32 {l, u}, %2;\n\tcvt.f32.f16 %0, l;\n\t"
-        "cvt.f32.f16 %1, u;\n\t}"
-        : "=f"(lo), "=f"(hi)
-        : "r"(h));
-    return f2_pack(lo, hi);
-}
-
-// 8 E4M3 bytes -> 4 packed fp32 pairs (element 2k in the low half of pair k)
-__device__ __forceinline__ void e4m3x8_to_pairs(const uint2& r, uint64_t (&o)[4]) {
-    o[0] = e4m3x2_to_pair(r.x & 0xffffu);
-    o[1] = e4m3x2_to_pair(r.x >> 16);
-    o[2] = e4m3x2_to_pair(r.y & 0xffffu);
-    o[3] = e4m3x2_to_pair(r.y >> 16);
-}
-
 // 8 bf16 -> 4 packed fp32 pairs (element 2k in the low half of pair k)
 __device__ __forceinline__ void bf16x8_to_pairs(const uint4& r, uint64_t (&o)[4]) {
     o[0] = f2_pack(bf_lo(r.x), bf_hi(r.x));
@@ -165,15 +134,12 @@ __device__ __forceinline__ void bf16x8_to_pairs(const uint4& r, uint64_t (&o)[4]
     o[3] = f2_pack(bf_lo(r.w), bf_hi(r.w));
 }
 
-template <int G, bool KV8>
+template <int G>
 __global__ void __launch_bounds__(WARPS * 32, G >= 8 ? 2 : 3)
     decode_tma_kernel(const __grid_constant__ Params p) {
     constexpr int D = HEAD_DIM;
-    // KV8: K/V are FP8 E4M3 bytes; a unit is then half the bytes and the ring has twice
-    // the stages, so the shared memory and the bytes in flight per warp stay the same
-    constexpr int EB = KV8 ? 1 : 2;              // bytes per K/V element
-    constexpr int UNIT = PAGE * D * EB;          // one 16-token unit of one head
-    constexpr int NST = KV8 ? 2 * STAGES : STAGES;
+    constexpr int UNIT = PAGE * D * 2;           // one 16-token unit of one head (bf16)
+    constexpr int NST = STAGES;
     constexpr int SB = 2 * UNIT;                 // K + V of a unit
     static_assert(NST * SB == STAGES * STAGE_BYTES, "ring size");
     constexpr int NV = 8 * G;                     // partial dot products per lane per page
@@ -288,15 +254,14 @@ __global__ void __launch_bounds__(WARPS * 32, G >= 8 ? 2 : 3)
             const int page = page0 + pi;
             int pid, slot;
             const int nvalid = unit_row(page, pid, slot) ? min(PAGE, tok1 - page * PAGE) : 0;
-            const uint32_t kbase = stage0 + st * SB + ds * (8 * EB);
+            const uint32_t kbase = stage0 + st * SB + ds * 16;
             const uint32_t vbase = kbase + UNIT;
 
             float part[NV];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 uint64_t k2[4];
-                if constexpr (KV8) e4m3x8_to_pairs(lds64(kbase + (2 * i + tp) * D), k2);
-                else bf16x8_to_pairs(lds128(kbase + (2 * i + tp) * (D * 2)), k2);
+                bf16x8_to_pairs(lds128(kbase + (2 * i + tp) * (D * 2)), k2);
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
                     uint64_t acc = f2_mul(q2[h][0], k2[0]);
@@ -357,8 +322,7 @@ __global__ void __launch_bounds__(WARPS * 32, G >= 8 ? 2 : 3)
             for (int i = 0; i < 8; ++i) {
                 const int t = 2 * i + tp;
                 uint64_t v2[4];
-                if constexpr (KV8) e4m3x8_to_pairs(lds64(vbase + t * D), v2);
-                else bf16x8_to_pairs(lds128(vbase + t * (D * 2)), v2);
+                bf16x8_to_pairs(lds128(vbase + t * (D * 2)), v2);
                 if (nvalid < PAGE && t >= nvalid) {  // slots past kv_len may hold anything
 #pragma unroll
                     for (int e = 0; e < 4; ++e) v2[e] = zero2;
@@ -624,17 +588,19 @@ cudaError_t prepare_page_maps(Params& p, const void* k_pages, const void* v_page
     CUtensorMap* maps[2] = {&p.tm_kpages, &p.tm_vpages};
     const void* bases[2] = {k_pages, v_pages};
     const CUtensorMapDataType dt = kv8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    // E4M3 tiles feed the tensor-core decode, whose converters read them 128-byte swizzled
+    const CUtensorMapSwizzle sw = kv8 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
     for (int i = 0; i < 2; ++i) {
         CUresult r = encode(maps[i], dt, 4, const_cast<void*>(bases[i]),
                             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
     return cudaSuccess;
 }
 
-template <int G, bool KV8>
+template <int G>
 static cudaError_t launch_decode_g(const Params& p, int num_sms, cudaStream_t stream) {
     // per device, set up on first use; the entries are atomics because the main entry
     // points and the allocation-free one hold different locks (a repeated set-up is
@@ -645,33 +611,28 @@ static cudaError_t launch_decode_g(const Params& p, int num_sms, cudaStream_t st
     if (dev < 0 || dev >= 64) dev = 0;
     int bps = blocks_per_sm[dev].load(std::memory_order_acquire);
     if (bps == 0) {
-        cudaError_t e = cudaFuncSetAttribute(decode_tma_kernel<G, KV8>,
+        cudaError_t e = cudaFuncSetAttribute(decode_tma_kernel<G>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess) return e;
         int n = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_tma_kernel<G, KV8>, WARPS * 32,
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_tma_kernel<G>, WARPS * 32,
                                                           SMEM_BYTES);
         if (e != cudaSuccess) return e;
         bps = n > 0 ? n : 1;
         blocks_per_sm[dev].store(bps, std::memory_order_release);
     }
     const int grid = num_sms * bps;
-    decode_tma_kernel<G, KV8><<<grid, WARPS * 32, SMEM_BYTES, stream>>>(p);
+    decode_tma_kernel<G><<<grid, WARPS * 32, SMEM_BYTES, stream>>>(p);
     return cudaGetLastError();
 }
 
-// kv8: K/V pages are FP8 E4M3 bytes (p.scale_log2 already carries k_scale, p.v_scale
-// scales the outputs); else bf16 (p.v_scale = 1)
-cudaError_t launch_decode(const Params& p, int group, bool kv8, int num_sms, cudaStream_t stream) {
-    switch (group * 2 + (kv8 ? 1 : 0)) {
-        case 2: return launch_decode_g<1, false>(p, num_sms, stream);
-        case 3: return launch_decode_g<1, true>(p, num_sms, stream);
-        case 4: return launch_decode_g<2, false>(p, num_sms, stream);
-        case 5: return launch_decode_g<2, true>(p, num_sms, stream);
-        case 8: return launch_decode_g<4, false>(p, num_sms, stream);
-        case 9: return launch_decode_g<4, true>(p, num_sms, stream);
-        case 16: return launch_decode_g<8, false>(p, num_sms, stream);
-        case 17: return launch_decode_g<8, true>(p, num_sms, stream);
+// bf16 K/V pages (the E4M3 decode runs on the tensor cores: decode_mma.cu)
+cudaError_t launch_decode(const Params& p, int group, int num_sms, cudaStream_t stream) {
+    switch (group) {
+        case 1: return launch_decode_g<1>(p, num_sms, stream);
+        case 2: return launch_decode_g<2>(p, num_sms, stream);
+        case 4: return launch_decode_g<4>(p, num_sms, stream);
+        case 8: return launch_decode_g<8>(p, num_sms, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -1,0 +1,795 @@
+// decode_mma.cu -- paged GQA decode over an FP8 E4M3 KV cache on the tensor cores.
+//
+// What it computes is the decode of decode.cu (one query row per request; split-KV over
+// request-local chunks; partial results merged by log-sum-exp weights) with K/V stored as
+// OCP E4M3 bytes and one scale per tensor:
+//   o[b,h] = v_scale * softmax_j(sm_scale * k_scale * q[b,h] . k8[j, h/G]) v8[j, h/G]
+// Sources: FlashInfer documentation, flashinfer_benchmark.py "Attention Flags"
+// (--kv_dtype fp8_e4m3); vllm-rlt pull request "feat: add FlashInfer attention backend for
+// SM120 decode" (paged decode over a block table, padding never visible); FlashInfer
+// documentation, flashinfer.cascade "Merge Attention States" (the chunk merge).
+//
+// Why tensor cores: on the CUDA cores every E4M3 byte costs a conversion plus G fused
+// multiply-adds per K and V element, so the E4M3 decode ran into the issue rate at about
+// half of HBM speed.  Here the dot products run on tcgen05.mma and the CUDA cores only
+// convert bytes, which leaves HBM as the bound.
+//
+// Design (one persistent CTA per SM, 448 threads; work item = one (chunk, kv head) of up
+// to 8 tiles of 128 keys; the items of a CTA run as a software pipeline in which step s
+// handles the K tiles of item s and the V tiles of item s - 1):
+//  * warps 0 and 14, producers: stream 128-key tiles of raw E4M3 bytes in step order (K
+//    tiles of item s, then V tiles of item s - 1) through a 5-stage TMA ring, taking
+//    alternate tiles; lane u < 8 loads the 16-key unit u of a tile (a 16-token page, or a
+//    slice of a larger page) as one 2 KB box, 128-byte swizzled.  Page ids are read one
+//    item ahead.
+//  * warps 2-9, two converter warpgroups, both on every raw tile: E4M3 -> f16 is exact.
+//    A K tile goes into tensor memory (lanes = keys, two dims per column), where the MMA
+//    reads its A operand; a V tile goes to shared memory in the 128-byte-swizzled MN-major
+//    layout.  Keys past the chunk or in a page that was not loaded become zeros.  At each
+//    item start warpgroup 0 writes the G query rows as f16, scaled by a power of two 2^e
+//    chosen from max|q| so that they sit well inside f16's range (exact for bf16 inputs).
+//  * warp 1, MMA issuer (swap-AB, keys as M = 128, query heads padded to N = 16):
+//      S^T_t  = K_t . (2^e Q)^T        A = K tile (K-major), B = Q (K-major)
+//      O^T   += V_t^T . P_t^T          A = V tile (MN-major), B = P^T (K-major, smem)
+//    Every S^T tile of an item stays in tensor memory (two item regions of 8 x 16 columns)
+//    so the softmax sees the whole item at once; O^T takes 16 more columns and three K
+//    tiles 3 x 64.
+//  * warps 10-13, softmax: thread r owns key r of every tile (TMEM lane r).  Per item: one
+//    pass over all its S^T tiles gives the exact max per head (a warp butterfly and one
+//    exchange among the four warps), so no running rescale is needed; then each tile's
+//    P^T = exp2(s - max) goes to shared memory as f16 while the row sums accumulate; at
+//    the item's end thread r holds column r of O^T: divided by l, scaled by v_scale, it
+//    becomes the bf16 output (single-chunk request) or the fp32 partial and its lse.
+//  While the softmax works on item s - 1, the converter and the tensor core are already on
+//  the K tiles of item s.
+#include <atomic>
+
+#include "ptx.cuh"
+
+namespace pgqa {
+namespace decode {
+namespace mmad {
+
+constexpr int D = HEAD_DIM;                 // 128
+constexpr int TK = 128;                     // keys per tile = the MMA's M
+constexpr int NH = 16;                      // query heads per kv head, padded = the MMA's N
+constexpr int UNITS = TK / PAGE;            // 16-key units per tile (8)
+constexpr int RAW_STAGES = 5;
+constexpr int NKB = 3;                      // K tiles in tensor memory
+constexpr int NVB = 3;                      // converted V tiles in shared memory
+constexpr int NPB = 8;                      // P^T tiles in shared memory (a whole item)
+constexpr int MAX_TILES = 8;                // tiles per item (chunks of at most 1024 keys)
+constexpr int RAW_BYTES = TK * D;           // 16 KB of E4M3 per K or V tile
+constexpr int CVT_BYTES = TK * D * 2;       // 32 KB of f16
+constexpr int CVT_CHUNK = TK * 128;         // one 64-column chunk of a converted tile
+constexpr int QP_BYTES = NH * D * 2;        // 4 KB: Q (16 x 128 dims) or P^T (16 x 128 keys)
+constexpr int QP_CHUNK = NH * 128;          // one 64-column chunk of Q or P^T
+constexpr int PRODUCERS = 2;                // TMA producer warps (0 and 14)
+constexpr int THREADS = 448 + 32 * (PRODUCERS - 1);
+constexpr int CVT_THREADS = 256;            // two converter warpgroups share every tile
+// tensor memory: S^T regions of two items (8 tiles x 16 columns each) at 0 and 128, O^T at
+// 256, and NKB K tiles as f16 (128 lanes = keys, 64 columns = 128 dims) from 288 on
+constexpr int TMEM_COLS = 512;
+constexpr int TMEM_O = 256;
+constexpr int TMEM_K = 288;
+static_assert(TMEM_K + 64 * NKB <= TMEM_COLS, "tensor memory columns");
+
+constexpr int OFF_RAW = 0;
+constexpr int OFF_VC = OFF_RAW + RAW_STAGES * RAW_BYTES;  // NVB buffers
+constexpr int OFF_Q = OFF_VC + NVB * CVT_BYTES;           // two buffers
+constexpr int OFF_P = OFF_Q + 2 * QP_BYTES;               // NPB buffers
+constexpr int OFF_RED = OFF_P + NPB * QP_BYTES;           // exchange areas (1 KB)
+constexpr int OFF_MASK = OFF_RED + 1024;  // loaded-unit bits per raw stage (<= 10 words), the
+                                          // q exponents (2 words at +40) and the per-item
+                                          // unit masks (2 x 64 bits at +48)
+constexpr int OFF_BAR = OFF_MASK + 64;
+
+// barrier indices
+constexpr int RAW_FULL = 0, RAW_EMPTY = RAW_FULL + RAW_STAGES, KC_FULL = RAW_EMPTY + RAW_STAGES,
+              KC_EMPTY = KC_FULL + NKB, VC_FULL = KC_EMPTY + NKB, VC_EMPTY = VC_FULL + NVB,
+              Q_FULL = VC_EMPTY + NVB, Q_EMPTY = Q_FULL + 2, S_FULL = Q_EMPTY + 2,
+              S_EMPTY = S_FULL + 2, P_FULL = S_EMPTY + 2, P_EMPTY = P_FULL + NPB,
+              PV_LAST = P_EMPTY + NPB, O_EMPTY = PV_LAST + 1, MMA_DRAIN = O_EMPTY + 1,
+              XCH_CVT = MMA_DRAIN + 1, XCH_SMX = XCH_CVT + 1, MASK_FULL = XCH_SMX + 1,
+              NUM_BARS = MASK_FULL + 2;
+constexpr int SMEM_BYTES = 1024 + OFF_BAR + 8 * NUM_BARS + 16;
+static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+static_assert(RAW_STAGES <= 10, "unit-mask words");
+
+// Byte offset of element (row, col) of a 128-byte-swizzled K-major tile whose 64-column
+// chunks are chunk_bytes apart (rows of 128 bytes, 16-byte units XORed with row % 8).
+__device__ __forceinline__ uint32_t sw128_off(int row, int col, int chunk_bytes) {
+    const int unit = (col & 63) >> 3;
+    return (uint32_t)((col >> 6) * chunk_bytes + row * 128 + ((unit ^ (row & 7)) << 4) +
+                      ((col & 7) << 1));
+}
+
+// Geometry of work item `item`: request b, kv head g, chunk c of nch, keys [tok0, tok1).
+struct Item {
+    int b, g, f, nch, tok0, tok1, ntiles;
+};
+__device__ __forceinline__ Item item_of(const Params& p, long long item) {
+    Item it;
+    const int Hk = p.num_kv_heads;
+    it.f = (int)(item / Hk);
+    it.g = (int)(item % Hk);
+    int lo = 0, hi = p.batch - 1;  // the request whose chunks contain f
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(p.chunk_off + mid) <= it.f) lo = mid;
+        else hi = mid - 1;
+    }
+    it.b = lo;
+    const int c0 = __ldg(p.chunk_off + lo);
+    it.nch = __ldg(p.chunk_off + lo + 1) - c0;
+    const int kv = __ldg(p.kv_eff + lo);
+    it.tok0 = (it.f - c0) * p.chunk;
+    it.tok1 = min(kv, it.tok0 + p.chunk);
+    it.ntiles = it.tok1 > it.tok0 ? (it.tok1 - it.tok0 + TK - 1) / TK : 0;
+    return it;
+}
+
+// Exchange of per-warp values among the four warps of a warpgroup through shared memory
+// and an mbarrier of count 4 (lane 0 of each warp writes its warp's values, then arrives),
+// with a bounded wait: a warp that has given up never leaves the others waiting forever.
+// Two areas of 4 x 8 floats alternate by use, so a warp may write the next exchange while
+// a slower one still reads this one (it cannot get two exchanges ahead).
+struct WgExchange {
+    uint32_t bar;
+    float* area;   // 2 x 32 floats
+    uint32_t use;
+};
+template <int N>
+__device__ __forceinline__ bool wg_exchange(WgExchange& x, const float (&vals)[N], int warp4,
+                                            int lane, volatile int* abort_flag, int* status,
+                                            const float*& out) {
+    float* a = x.area + (x.use & 1) * 32;
+    if (lane == 0) {
+#pragma unroll
+        for (int i = 0; i < N; ++i) a[warp4 * 8 + i] = vals[i];
+        mbar_arrive(x.bar);
+    }
+    const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(x.bar, x.use & 1, abort_flag, status));
+    ++x.use;
+    out = a;
+    return ok;
+}
+
+// The G query rows of item (b, g), column d (thread d of a warpgroup), as floats.
+template <int G>
+__device__ __forceinline__ void load_q(const Params& p, int b, int g, int d, float (&qv)[G]) {
+    const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(p.q) +
+                             ((size_t)b * p.num_qo_heads + (size_t)g * G) * D + d;
+#pragma unroll
+    for (int h = 0; h < G; ++h) qv[h] = __bfloat162float(q[h * D]);
+}
+
+// Power-of-two exponent e for the query rows of an item: 2^e * max|q| lies in
+// [2^14, 2^15), so the scaled rows fit f16 with bf16's precision intact.  Warpgroup-wide
+// (thread d holds column d of the G rows).
+template <int G>
+__device__ __forceinline__ bool q_exponent(const float (&qv)[G], int d, WgExchange& x,
+                                           volatile int* abort_flag, int* status, int& e) {
+    float m[1] = {0.f};
+#pragma unroll
+    for (int h = 0; h < G; ++h) m[0] = fmaxf(m[0], fabsf(qv[h]));
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1)
+        m[0] = fmaxf(m[0], __shfl_xor_sync(0xffffffffu, m[0], off));
+    const float* a;
+    if (!wg_exchange<1>(x, m, d >> 5, d & 31, abort_flag, status, a)) return false;
+    const float mm = fmaxf(fmaxf(a[0], a[8]), fmaxf(a[16], a[24]));
+    e = 0;
+    if (mm > 0.f && mm < INFINITY) {
+        const int ex = ((__float_as_int(mm) >> 23) & 0xff) - 127;  // floor(log2 mm), normal
+        e = max(-100, min(100, 14 - max(ex, -126)));
+    }
+    return true;
+}
+
+__device__ __forceinline__ float exp2i(int e) { return __int_as_float((e + 127) << 23); }
+
+// 16 E4M3 bytes -> 16 f16 (exact), as two 16-byte units
+__device__ __forceinline__ void e4m3x16_to_f16(const uint4& raw, uint4& lo, uint4& hi) {
+    uint32_t h[8];
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+            "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+            : "=r"(h[2 * i]), "=r"(h[2 * i + 1])
+            : "r"(w[i]));
+    }
+    lo = make_uint4(h[0], h[1], h[2], h[3]);
+    hi = make_uint4(h[4], h[5], h[6], h[7]);
+}
+
+template <int G>
+__global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_constant__ Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    const uint32_t s0 = smem_u32(smem);
+    float* red = reinterpret_cast<float*>(smem + OFF_RED);
+    uint32_t* unit_mask = reinterpret_cast<uint32_t*>(smem + OFF_MASK);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const uint32_t bar0 = smem_u32(bars);
+    auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < RAW_STAGES; ++s) {
+            mbar_init(BAR(RAW_FULL + s), 1);
+            mbar_init(BAR(RAW_EMPTY + s), CVT_THREADS);
+        }
+        for (int x = 0; x < NKB; ++x) {
+            mbar_init(BAR(KC_FULL + x), CVT_THREADS);
+            mbar_init(BAR(KC_EMPTY + x), 1);
+        }
+        for (int x = 0; x < NVB; ++x) {
+            mbar_init(BAR(VC_FULL + x), CVT_THREADS);
+            mbar_init(BAR(VC_EMPTY + x), 1);
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(BAR(Q_FULL + x), 128);
+            mbar_init(BAR(Q_EMPTY + x), 1);
+            mbar_init(BAR(S_FULL + x), 1);
+            mbar_init(BAR(S_EMPTY + x), 128);
+        }
+        for (int x = 0; x < NPB; ++x) {
+            mbar_init(BAR(P_FULL + x), 128);
+            mbar_init(BAR(P_EMPTY + x), 1);
+        }
+        mbar_init(BAR(PV_LAST), 1);
+        mbar_init(BAR(O_EMPTY), 128);
+        mbar_init(BAR(MMA_DRAIN), 1);
+        mbar_init(BAR(XCH_CVT), 4);
+        mbar_init(BAR(XCH_SMX), 4);
+        mbar_init(BAR(MASK_FULL), 1);
+        mbar_init(BAR(MASK_FULL + 1), 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    // Q and P^T rows G..15 stay zero: clear every buffer of both once
+    for (int i = threadIdx.x; i < (2 + NPB) * QP_BYTES / 16; i += THREADS)
+        reinterpret_cast<uint4*>(smem + OFF_Q)[i] = make_uint4(0, 0, 0, 0);
+    fence_async_smem();
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int Hq = p.num_qo_heads;
+    const long long n_items = (long long)__ldg(p.chunk_off + p.batch) * p.num_kv_heads;
+    const long long stride = gridDim.x;
+
+    if (warp == 0 || warp >= 14) {
+        // ------------------------------------------------------------ TMA producers
+        // Producer w takes ring positions ld with ld % PRODUCERS == w: a warp issues its
+        // boxes one lane after another, so several warps keep more boxes in flight.
+        const uint32_t pw = warp == 0 ? 0u : (uint32_t)(warp - 13);
+        // step order: the K tiles of item s, then the V tiles of item s - 1.  The page ids of
+        // an item (at most 64 units of 16 keys: lane l holds units l and l + 32) are read one
+        // item ahead, so no page-table read waits in front of a tile's loads.
+        uint32_t ld = 0;  // raw tiles issued (ring position)
+        bool ok = true;
+        auto read_ids = [&](const Item& it, int (&ids)[2]) {
+            const int* pt_row = p.page_table + (size_t)it.b * p.page_table_stride;
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int key = it.tok0 + (lane + 32 * k) * PAGE;
+                ids[k] = key < it.tok1 ? __ldg(pt_row + key / p.page_size) : -1;
+            }
+        };
+        auto load_tiles = [&](const Item& it, const int (&ids)[2], bool v) {
+            for (int t = 0; ok && t < it.ntiles; ++t, ++ld) {
+                if (ld % PRODUCERS != pw) continue;
+                const int u = t * UNITS + lane;  // this lane's 16-key unit within the item
+                const int key = it.tok0 + u * PAGE;
+                const int pid = __shfl_sync(0xffffffffu, ids[t >> 2], u & 31);
+                const bool in_use = lane < UNITS && key < it.tok1;
+                const bool valid = in_use && pid >= 0 && pid < p.num_pages;
+                if (!v && in_use && !valid) atomicOr(p.status, PGQA_DEV_BOUNDS);
+                const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
+                const uint32_t st = ld % RAW_STAGES;
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait_bounded(BAR(RAW_EMPTY + st), ((ld / RAW_STAGES) & 1) ^ 1,
+                                                  abort_flag, p.status));
+                if (!ok) break;
+                if (lane == 0) {
+                    unit_mask[st] = vmask;
+                    mbar_arrive_expect_tx(BAR(RAW_FULL + st), (uint32_t)(__popc(vmask) * PAGE * D));
+                }
+                __syncwarp();
+                if (valid)
+                    tma_load_4d(s0 + OFF_RAW + st * RAW_BYTES + lane * PAGE * D,
+                                v ? &p.tm_vpages : &p.tm_kpages, BAR(RAW_FULL + st), 0,
+                                key % p.page_size, it.g, pid);
+            }
+        };
+        auto next_item = [&](long long from) -> long long {
+            for (long long k = from; k < n_items; k += stride)
+                if (item_of(p, k).ntiles > 0) return k;
+            return -1;
+        };
+        long long cur = next_item(blockIdx.x);
+        Item prev, it;
+        prev.ntiles = 0;
+        it.ntiles = 0;
+        int ids_prev[2] = {-1, -1}, ids[2] = {-1, -1};
+        if (cur >= 0) {
+            it = item_of(p, cur);
+            read_ids(it, ids);
+        }
+        while (ok && cur >= 0) {
+            const long long nxt = next_item(cur + stride);
+            Item ni;
+            ni.ntiles = 0;
+            int ids_next[2] = {-1, -1};
+            if (nxt >= 0) {  // read ahead: used by the next step
+                ni = item_of(p, nxt);
+                read_ids(ni, ids_next);
+            }
+            load_tiles(it, ids, false);
+            if (ok && prev.ntiles > 0) load_tiles(prev, ids_prev, true);
+            prev = it;
+            ids_prev[0] = ids[0];
+            ids_prev[1] = ids[1];
+            it = ni;
+            ids[0] = ids_next[0];
+            ids[1] = ids_next[1];
+            cur = nxt;
+        }
+        if (ok && prev.ntiles > 0) load_tiles(prev, ids_prev, true);
+        if (lane == 0) {
+            // copies still in flight (an aborted walk) land before the CTA exits
+            const uint32_t first = ld > (uint32_t)RAW_STAGES ? ld - RAW_STAGES : 0;
+            for (uint32_t k = first; k < ld; ++k)
+                if (k % PRODUCERS == pw)
+                    mbar_wait_bounded(BAR(RAW_FULL + k % RAW_STAGES), (k / RAW_STAGES) & 1,
+                                      nullptr, p.status);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t IDESC_S = idesc_f16_f32(TK, NH, false, false);
+            constexpr uint32_t IDESC_O = idesc_f16_f32(D, NH, true, false);
+            uint32_t kt = 0, vt = 0, s = 0;  // K tiles, V tiles and items so far
+            bool ok = true;
+            auto qk_tiles = [&](const Item& it) {
+                const uint32_t x = s & 1;  // Q buffer and S^T region of item s
+                ok = mbar_wait_bounded(BAR(Q_FULL + x), (s >> 1) & 1, abort_flag, p.status) &&
+                     mbar_wait_bounded(BAR(S_EMPTY + x), ((s >> 1) & 1) ^ 1, abort_flag, p.status);
+                for (int t = 0; ok && t < it.ntiles; ++t, ++kt) {
+                    const uint32_t kb = kt % NKB;
+                    ok = mbar_wait_bounded(BAR(KC_FULL + kb), (kt / NKB) & 1, abort_flag, p.status);
+                    if (!ok) break;
+                    tc_fence_after();
+                    // A = the K tile in tensor memory (lanes = keys, 2 dims per column)
+                    const uint64_t qdesc = sdesc_sw128(s0 + OFF_Q + x * QP_BYTES, 16, 1024);
+#pragma unroll
+                    for (int k = 0; k < D / 16; ++k)
+                        mma_ts(tmem_base + 128u * x + 16u * t, tmem_base + TMEM_K + 64u * kb + 8u * k,
+                               qdesc + (uint64_t)(((k >> 2) * QP_CHUNK + (k & 3) * 32) / 16),
+                               IDESC_S, k > 0 ? 1u : 0u);
+                    mma_commit(BAR(KC_EMPTY + kb));
+                }
+                if (ok) {
+                    mma_commit(BAR(S_FULL + x));
+                    mma_commit(BAR(Q_EMPTY + x));
+                }
+            };
+            auto pv_tiles = [&](const Item& it, uint32_t sp) {  // sp: the item's index
+                if (sp > 0)
+                    ok = mbar_wait_bounded(BAR(O_EMPTY), (sp - 1) & 1, abort_flag, p.status);
+                for (int t = 0; ok && t < it.ntiles; ++t, ++vt) {
+                    const uint32_t x = vt % NPB, xv = vt % NVB;
+                    ok = mbar_wait_bounded(BAR(P_FULL + x), (vt / NPB) & 1, abort_flag, p.status) &&
+                         mbar_wait_bounded(BAR(VC_FULL + xv), (vt / NVB) & 1, abort_flag, p.status);
+                    if (!ok) break;
+                    tc_fence_after();
+                    // A = V^T: MN-major, 64-dim chunks CVT_CHUNK apart, 8-key groups 1 KB
+                    // apart; B = P^T: K-major, 16 rows, 64-key chunks QP_CHUNK apart
+                    const uint64_t vdesc = sdesc_sw128(s0 + OFF_VC + xv * CVT_BYTES, CVT_CHUNK, 1024);
+                    const uint64_t pdesc = sdesc_sw128(s0 + OFF_P + x * QP_BYTES, 16, 1024);
+#pragma unroll
+                    for (int k = 0; k < TK / 16; ++k)
+                        mma_ss(tmem_base + TMEM_O, vdesc + (uint64_t)(k * 2048 / 16),
+                               pdesc + (uint64_t)(((k >> 2) * QP_CHUNK + (k & 3) * 32) / 16),
+                               IDESC_O, (t > 0 || k > 0) ? 1u : 0u);
+                    mma_commit(BAR(VC_EMPTY + xv));
+                    mma_commit(BAR(P_EMPTY + x));
+                }
+                if (ok) mma_commit(BAR(PV_LAST));
+            };
+            Item prev;
+            prev.ntiles = 0;
+            for (long long item = blockIdx.x; ok && item < n_items; item += stride) {
+                const Item it = item_of(p, item);
+                if (it.ntiles == 0) continue;
+                qk_tiles(it);
+                if (ok && prev.ntiles > 0) pv_tiles(prev, s - 1);
+                prev = it;
+                ++s;
+            }
+            if (ok && prev.ntiles > 0) pv_tiles(prev, s - 1);
+            // every MMA issued has completed before tensor memory is released
+            mma_commit(BAR(MMA_DRAIN));
+            mbar_wait_bounded(BAR(MMA_DRAIN), 0, nullptr, p.status);
+        }
+    } else if (warp >= 2 && warp < 10) {
+        // ------------------------------------------------------------ converters
+        // Both warpgroups work on every raw tile.  A K tile goes to tensor memory: the warp
+        // of lane quarter q (warp % 4) and half c (its warpgroup) converts keys 32q .. 32q+31,
+        // dims 64c .. 64c+63 (thread = key = TMEM lane).  A V tile goes to shared memory in
+        // the swizzled MN-major layout, 4 of its 1024 16-byte segments per thread.
+        // Warpgroup 0 also writes each item's Q and records its loaded units.
+        const int cid = (warp - 2) >> 2;
+        const int j = threadIdx.x - 64;          // 0..255 over both warpgroups
+        const int i = j - 128 * cid;             // 0..127 within the warpgroup
+        const int q4 = warp & 3;                 // TMEM lane quarter of this warp
+        const int krow = 32 * q4 + lane;         // key row this thread converts in K tiles
+        WgExchange xch{BAR(XCH_CVT), red, 0};
+        int* qe = reinterpret_cast<int*>(smem + OFF_MASK + 40);
+        unsigned long long* kmask = reinterpret_cast<unsigned long long*>(smem + OFF_MASK + 48);
+        uint32_t cv = 0, kt = 0, vt = 0, s = 0;
+        bool ok = true;
+        // raw tiles arrive with the 128-byte swizzle: 16-byte unit u of row r sits at unit
+        // u ^ (r % 8); rows past nvalid and rows of units that were not loaded become zeros
+        auto raw_unit = [&](uint32_t raw, int row, int u, bool use) -> uint4 {
+            uint4 r = make_uint4(0, 0, 0, 0);
+            if (use)
+                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                             : "r"(raw + row * 128 + ((u ^ (row & 7)) << 4)));
+            return r;
+        };
+        auto wait_raw = [&]() -> uint32_t {
+            const uint32_t st = cv % RAW_STAGES;
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(RAW_FULL + st), (cv / RAW_STAGES) & 1,
+                                                           abort_flag, p.status));
+            return st;
+        };
+        // Q of item s (from query rows already in registers), then its K tiles
+        auto k_tiles = [&](const Item& it, const float (&qv)[G]) {
+            const uint32_t qb = s & 1;
+            if (cid == 0) {
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(Q_EMPTY + qb),
+                                                               ((s >> 1) & 1) ^ 1, abort_flag,
+                                                               p.status));
+                if (!ok) return;
+                int e;
+                ok = q_exponent<G>(qv, i, xch, abort_flag, p.status, e);
+                if (!ok) return;
+                const float sc = exp2i(e);
+                uint8_t* qs = smem + OFF_Q + qb * QP_BYTES;
+#pragma unroll
+                for (int h = 0; h < G; ++h)
+                    *reinterpret_cast<__half*>(qs + sw128_off(h, i, QP_CHUNK)) =
+                        __float2half_rn(qv[h] * sc);
+                if (i == 0) qe[qb] = e;
+                fence_async_smem();
+                mbar_arrive(BAR(Q_FULL + qb));
+            }
+            unsigned long long bits = 0;  // loaded units of every tile (8 bits per tile)
+            for (int t = 0; ok && t < it.ntiles; ++t, ++kt, ++cv) {
+                const uint32_t st = wait_raw();
+                const uint32_t kb = kt % NKB;
+                if (ok)
+                    ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(KC_EMPTY + kb),
+                                                                   ((kt / NKB) & 1) ^ 1, abort_flag,
+                                                                   p.status));
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t um = unit_mask[st];
+                bits |= (unsigned long long)(um & 0xffu) << (8 * t);
+                const int nvalid = min(TK, it.tok1 - (it.tok0 + t * TK));
+                const bool use = krow < nvalid && ((um >> (krow >> 4)) & 1u);
+                const uint32_t raw = s0 + OFF_RAW + st * RAW_BYTES;
+                uint4 rv[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) rv[u] = raw_unit(raw, krow, 4 * cid + u, use);
+                uint32_t f[32];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    uint4 lo, hi;
+                    e4m3x16_to_f16(rv[u], lo, hi);
+                    f[8 * u + 0] = lo.x; f[8 * u + 1] = lo.y; f[8 * u + 2] = lo.z; f[8 * u + 3] = lo.w;
+                    f[8 * u + 4] = hi.x; f[8 * u + 5] = hi.y; f[8 * u + 6] = hi.z; f[8 * u + 7] = hi.w;
+                }
+                tmem_st32(tmem_base + ((uint32_t)(32 * q4) << 16) + TMEM_K + 64u * kb + 32u * cid, f);
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(BAR(KC_FULL + kb));
+                mbar_arrive(BAR(RAW_EMPTY + st));
+            }
+            if (ok && j == 0) {
+                kmask[qb] = bits;
+                mbar_arrive(BAR(MASK_FULL + qb));
+            }
+        };
+        auto v_tiles = [&](const Item& it) {
+            for (int t = 0; ok && t < it.ntiles; ++t, ++vt, ++cv) {
+                const uint32_t st = wait_raw();
+                const uint32_t x = vt % NVB;
+                if (ok)
+                    ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(VC_EMPTY + x),
+                                                                   ((vt / NVB) & 1) ^ 1, abort_flag,
+                                                                   p.status));
+                if (!ok) break;
+                const uint32_t um = unit_mask[st];
+                const int nvalid = min(TK, it.tok1 - (it.tok0 + t * TK));
+                const uint32_t raw = s0 + OFF_RAW + st * RAW_BYTES;
+                const uint32_t dst = s0 + OFF_VC + x * CVT_BYTES;
+                uint4 rv[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {  // all loads first
+                    const int lin = k * CVT_THREADS + j;
+                    const int row = lin >> 3, seg = lin & 7;  // 16 bytes = 16 dims of one key
+                    rv[k] = raw_unit(raw, row, seg, row < nvalid && ((um >> (row >> 4)) & 1u));
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int lin = k * CVT_THREADS + j;
+                    const int row = lin >> 3, seg = lin & 7;
+                    uint4 lo, hi;
+                    e4m3x16_to_f16(rv[k], lo, hi);
+                    const uint32_t a0 = dst + sw128_off(row, seg * 16, CVT_CHUNK);
+                    const uint32_t a1 = dst + sw128_off(row, seg * 16 + 8, CVT_CHUNK);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a0), "r"(lo.x),
+                                 "r"(lo.y), "r"(lo.z), "r"(lo.w)
+                                 : "memory");
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a1), "r"(hi.x),
+                                 "r"(hi.y), "r"(hi.z), "r"(hi.w)
+                                 : "memory");
+                }
+                fence_async_smem();
+                mbar_arrive(BAR(VC_FULL + x));
+                mbar_arrive(BAR(RAW_EMPTY + st));
+            }
+        };
+        auto next_item = [&](long long from) -> long long {
+            for (long long k = from; k < n_items; k += stride)
+                if (item_of(p, k).ntiles > 0) return k;
+            return -1;
+        };
+        long long cur = next_item(blockIdx.x);
+        float qv[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) qv[h] = 0.f;
+        if (cur >= 0 && cid == 0) {
+            const Item it = item_of(p, cur);
+            load_q<G>(p, it.b, it.g, i, qv);
+        }
+        Item prev;
+        prev.ntiles = 0;
+        while (ok && cur >= 0) {
+            const Item it = item_of(p, cur);
+            const long long nxt = next_item(cur + stride);
+            float qn[G];  // the next item's query rows, loaded while this one converts
+#pragma unroll
+            for (int h = 0; h < G; ++h) qn[h] = 0.f;
+            if (nxt >= 0 && cid == 0) {
+                const Item ni = item_of(p, nxt);
+                load_q<G>(p, ni.b, ni.g, i, qn);
+            }
+            k_tiles(it, qv);
+            if (ok && prev.ntiles > 0) v_tiles(prev);
+            prev = it;
+            ++s;
+            cur = nxt;
+#pragma unroll
+            for (int h = 0; h < G; ++h) qv[h] = qn[h];
+        }
+        if (ok && prev.ntiles > 0) v_tiles(prev);
+    } else if (warp >= 10) {
+        // ------------------------------------------------------------ softmax / epilogue
+        // Per item s: (A) its S^T tiles and exact max; (B) the epilogue of item s - 1, whose
+        // last P.V completes while (A) runs; (C) its P^T tiles and row sums.
+        const int w4 = warp & 3;                                // TMEM lane quarter
+        const int r = 32 * w4 + lane;                           // key of a tile = TMEM lane
+        const uint32_t lane_base = (uint32_t)(32 * w4) << 16;
+        WgExchange xch{BAR(XCH_SMX), red + 64, 0};
+        const int* qe = reinterpret_cast<const int*>(smem + OFF_MASK + 40);
+        const unsigned long long* kmask =
+            reinterpret_cast<const unsigned long long*>(smem + OFF_MASK + 48);
+        uint32_t pt = 0, s = 0;  // P^T tiles written, items
+        bool ok = true;
+        Item prev;
+        prev.ntiles = 0;
+        float prev_m[G], prev_l[G];
+        // (B): wait for item j's last P.V, release O^T, write its outputs
+        auto epilogue = [&](const Item& it, uint32_t j, const float (&m)[G], const float (&l)[G]) {
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(PV_LAST), j & 1, abort_flag,
+                                                           p.status));
+            if (!ok) return;
+            tc_fence_after();
+            uint32_t v[8];
+            tmem_ld8(tmem_base + lane_base + TMEM_O, v);  // thread r: column r of O, all heads
+            tmem_wait_ld8(v);
+            tc_fence_before();
+            mbar_arrive(BAR(O_EMPTY));
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float inv = l[h] > 0.f ? p.v_scale / l[h] : 0.f;
+                const float lse_v = l[h] > 0.f ? (m[h] + log2f(l[h])) * 0.69314718055994531f
+                                               : -INFINITY;
+                const int hq = it.g * G + h;
+                const float o = __uint_as_float(v[h]) * inv;
+                if (it.nch == 1) {
+                    reinterpret_cast<__nv_bfloat16*>(p.o)[((size_t)it.b * Hq + hq) * D + r] =
+                        __float2bfloat16_rn(o);
+                    if (r == 0 && p.lse) p.lse[(size_t)it.b * Hq + hq] = lse_v;
+                } else {
+                    p.part_o[((size_t)it.f * Hq + hq) * D + r] = o;
+                    if (r == 0) p.part_lse[(size_t)it.f * Hq + hq] = lse_v;
+                }
+            }
+        };
+        for (long long item = blockIdx.x; ok && item < n_items; item += stride) {
+            const Item it = item_of(p, item);
+            if (it.ntiles == 0) {
+                // no keys: zeros and lse = -inf (a request of a single empty chunk)
+                if (r < G * D / 8) {
+                    const int h = r / (D / 8), c = r % (D / 8);
+                    reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) +
+                                             ((size_t)it.b * Hq + it.g * G + h) * D)[c] =
+                        make_uint4(0, 0, 0, 0);
+                    if (c == 0 && p.lse) p.lse[(size_t)it.b * Hq + it.g * G + h] = -INFINITY;
+                }
+                continue;
+            }
+            // (A) the scale of the item's query rows and its loaded units, then its scores
+            const uint32_t x = s & 1;
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(Q_FULL + x), (s >> 1) & 1,
+                                                           abort_flag, p.status));
+            if (ok)
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(MASK_FULL + x), (s >> 1) & 1,
+                                                               abort_flag, p.status));
+            if (ok)
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(S_FULL + x), (s >> 1) & 1,
+                                                               abort_flag, p.status));
+            if (!ok) break;
+            const float c_eff = p.scale_log2 * exp2i(-qe[x]);  // score units: log2, all scales
+            const unsigned long long km = kmask[x];
+            tc_fence_after();
+            float sv[MAX_TILES][G];
+#pragma unroll
+            for (int t = 0; t < MAX_TILES; ++t) {
+                // key r of tile t counts if it is inside the chunk and its unit was loaded
+                const bool valid = t < it.ntiles && it.tok0 + t * TK + r < it.tok1 &&
+                                   ((km >> (8 * t + (r >> 4))) & 1ull);
+                if (t < it.ntiles) {
+                    uint32_t u[8];
+                    tmem_ld8(tmem_base + lane_base + 128u * x + 16u * t, u);
+                    tmem_wait_ld8(u);
+#pragma unroll
+                    for (int h = 0; h < G; ++h)
+                        sv[t][h] = valid ? __uint_as_float(u[h]) * c_eff : -INFINITY;
+                } else {
+#pragma unroll
+                    for (int h = 0; h < G; ++h) sv[t][h] = -INFINITY;
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(BAR(S_EMPTY + x));
+            // exact max per head over the item's keys
+            float mx[G];
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                float m = sv[0][h];
+#pragma unroll
+                for (int t = 1; t < MAX_TILES; ++t) m = fmaxf(m, sv[t][h]);
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+                mx[h] = m;
+            }
+            const float* rt;  // [warp][head]
+            ok = wg_exchange<G>(xch, mx, w4, lane, abort_flag, p.status, rt);
+            if (!ok) break;
+            float neg[G], l[G];
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float m = fmaxf(fmaxf(rt[h], rt[8 + h]), fmaxf(rt[16 + h], rt[24 + h]));
+                mx[h] = m;
+                neg[h] = m == -INFINITY ? 0.f : -m;
+                l[h] = 0.f;
+            }
+            // (B) the previous item's epilogue
+            if (prev.ntiles > 0) {
+                epilogue(prev, s - 1, prev_m, prev_l);
+                if (!ok) break;
+            }
+            // (C) P^T tiles, f16, into the ring of NPB buffers the P.V MMAs read
+            for (int t = 0; t < it.ntiles; ++t, ++pt) {
+                const uint32_t pb = pt % NPB;
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(P_EMPTY + pb),
+                                                               ((pt / NPB) & 1) ^ 1, abort_flag,
+                                                               p.status));
+                if (!ok) break;
+                uint8_t* pp = smem + OFF_P + pb * QP_BYTES;
+#pragma unroll
+                for (int tt = 0; tt < MAX_TILES; ++tt) {
+                    if (tt == t) {
+#pragma unroll
+                        for (int h = 0; h < G; ++h) {
+                            const float pv = ex2_approx(sv[tt][h] + neg[h]);
+                            l[h] += pv;
+                            *reinterpret_cast<__half*>(pp + sw128_off(h, r, QP_CHUNK)) =
+                                __float2half_rn(pv);
+                        }
+                    }
+                }
+                fence_async_smem();
+                mbar_arrive(BAR(P_FULL + pb));
+            }
+            if (!ok) break;
+            // l over the item's keys: a warp sum, then the four warps (read out at once: the
+            // exchange area is reused two exchanges later)
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1) l[h] += __shfl_xor_sync(0xffffffffu, l[h], off);
+            }
+            const float* rl;
+            ok = wg_exchange<G>(xch, l, w4, lane, abort_flag, p.status, rl);
+            if (!ok) break;
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                prev_l[h] = (rl[h] + rl[8 + h]) + (rl[16 + h] + rl[24 + h]);
+                prev_m[h] = mx[h];
+            }
+            prev = it;
+            ++s;
+        }
+        if (ok && prev.ntiles > 0) epilogue(prev, s - 1, prev_m, prev_l);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+template <int G>
+static cudaError_t launch_g(const Params& p, int num_sms, cudaStream_t stream) {
+    static std::atomic<bool> configured[64];  // per device, set once (repeats are harmless)
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !configured[dev].load(std::memory_order_acquire)) {
+        const cudaError_t e = cudaFuncSetAttribute(
+            decode_mma_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        configured[dev].store(true, std::memory_order_release);
+    }
+    decode_mma_kernel<G><<<num_sms, THREADS, SMEM_BYTES, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace mmad
+
+// The E4M3 decode on the tensor cores (p.tm_kpages / p.tm_vpages: one-byte 4-D page maps
+// with a box of 16 slots of one head; p.scale_log2 carries sm_scale * k_scale * log2 e,
+// p.v_scale the value scale).
+cudaError_t launch_decode_mma(const Params& p, int group, int num_sms, cudaStream_t stream) {
+    switch (group) {
+        case 1: return mmad::launch_g<1>(p, num_sms, stream);
+        case 2: return mmad::launch_g<2>(p, num_sms, stream);
+        case 4: return mmad::launch_g<4>(p, num_sms, stream);
+        case 8: return mmad::launch_g<8>(p, num_sms, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace decode
+}  // namespace pgqa

@@ -25,7 +25,7 @@
 namespace pgqa {
 namespace decode {
 cudaError_t launch_plan(const PlanParams&, cudaStream_t);
-cudaError_t launch_decode(const Params&, int group, bool kv8, int num_sms, cudaStream_t);
+cudaError_t launch_decode(const Params&, int group, int num_sms, cudaStream_t);
 cudaError_t launch_merge(const Params&, cudaStream_t);
 cudaError_t prepare_page_maps(Params&, const void*, const void*, int, int, int, long long,
                               long long, long long, bool);
@@ -179,6 +179,6 @@ extern "C" int pgqa_paged_decode_bf16_noalloc(
                                   (long long)page_size * num_kv_heads * head_dim,
                                   (long long)num_kv_heads * head_dim, head_dim, false) != cudaSuccess)
         return PGQA_ERR_INVALID_ARG;
-    if (decode::launch_decode(p, group, false, s.num_sms, st) != cudaSuccess) return PGQA_ERR_CUDA;
+    if (decode::launch_decode(p, group, s.num_sms, st) != cudaSuccess) return PGQA_ERR_CUDA;
     return decode::launch_merge(p, st) == cudaSuccess ? PGQA_OK : PGQA_ERR_CUDA;
 }
