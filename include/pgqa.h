@@ -247,6 +247,43 @@ int pgqa_paged_decode_e4m3(const void* q, const void* k_pages, const void* v_pag
                            void* o, float* lse, int batch, int num_qo_heads, int num_kv_heads,
                            int head_dim, float sm_scale, pgqa_stream_t stream);
 
+/*
+ * Paged prefill with few query rows per request (multi-token decode, speculative
+ * verification) over an FP8 E4M3 KV cache: the computation of pgqa_paged_prefill_bf16 with
+ * K/V stored as in pgqa_paged_decode_e4m3 (one byte per element, values e4m3 * k_scale and
+ * e4m3 * v_scale, strides in elements = bytes, positive multiples of 16).
+ *
+ * Defined by: FlashInfer documentation, flashinfer.prefill
+ * (BatchPrefillWithPagedKVCacheWrapper: ragged queries over a paged KV cache, causal
+ * masking aligned to the bottom right) with flashinfer_benchmark.py "Attention Flags"
+ * (--kv_dtype fp8_e4m3 for the prefill and decode routines); scale convention as for
+ * pgqa_paged_decode_e4m3.
+ *
+ *   q [total_q, num_qo_heads, 128] bf16 and q_indptr [batch + 1] int32 (device) as for
+ *       pgqa_paged_prefill_bf16; every request has at most max_qo_len rows.
+ *   page_table, kv_lens, page_size, num_pages: as for pgqa_paged_prefill_bf16.
+ *   o [total_q, num_qo_heads, 128] bf16, lse [total_q, num_qo_heads] fp32 or NULL.
+ *   causal != 0: query row i of a request with qo_len rows and kv_len keys sees key j iff
+ *       j <= i + kv_len - qo_len (a row that sees no key gets zeros and lse = -inf).
+ * The keys stream once per (request, kv head) for all of its query rows and heads, on the
+ * tensor-core E4M3 decode path, with split-KV as for the decode.
+ *
+ * Supported: head_dim 128; page_size 16, 32, 64 or 128; G = num_qo_heads / num_kv_heads
+ * in {1,2,4,8}; max_qo_len * G <= 16, else PGQA_ERR_UNSUPPORTED.  max_qo_len < 1 (with
+ * batch > 0), a NULL q_indptr or a NaN / infinite scale is PGQA_ERR_INVALID_ARG; other
+ * errors as for pgqa_paged_decode_e4m3.  A request whose q_indptr range is negative or
+ * longer than max_qo_len, or whose kv_len is out of range, is reported as
+ * PGQA_ERR_DEVICE_BOUNDS by pgqa_get_device_status() and none of its rows is written; a
+ * page id outside 0..num_pages-1 is reported the same way and that page is not read.
+ */
+int pgqa_paged_prefill_e4m3(const void* q, const void* k_pages, const void* v_pages, void* o,
+                            float* lse, const int32_t* q_indptr, const int32_t* page_table,
+                            int page_table_stride, const int32_t* kv_lens, int page_size,
+                            int num_pages, int64_t page_stride, int64_t slot_stride,
+                            int64_t head_stride, float k_scale, float v_scale, int batch,
+                            int max_qo_len, int num_qo_heads, int num_kv_heads, int head_dim,
+                            int causal, float sm_scale, pgqa_stream_t stream);
+
 /* Same calls under the short names used by serving integrations. */
 int ragged_prefill_bf16(const void* q, const void* k, const void* v, void* o, float* lse,
                         const int32_t* q_indptr, const int32_t* kv_indptr, int batch,

@@ -27,7 +27,7 @@ STATUS_NAMES = {
 ABI_FUNCTIONS = (
     "pgqa_ragged_prefill_bf16", "pgqa_paged_prefill_bf16", "pgqa_paged_decode_bf16",
     "pgqa_paged_prefill_bf16_strided", "pgqa_paged_decode_bf16_strided",
-    "pgqa_paged_decode_e4m3",
+    "pgqa_paged_decode_e4m3", "pgqa_paged_prefill_e4m3",
     "ragged_prefill_bf16", "paged_prefill_bf16", "paged_decode_bf16", "pgqa_set_workspace", "pgqa_workspace_bytes_prefill",
     "pgqa_workspace_bytes_decode", "pgqa_get_device_status", "pgqa_status_string",
     "pgqa_version", "pgqa_paged_decode_bf16_noalloc", "pgqa_selftest_expired_wait",
@@ -69,6 +69,9 @@ def _load(path: Path):
     lib.pgqa_paged_decode_e4m3.argtypes = [p, p, p, p, p, i, i, i, i64, i64, i64, f, f, p, p, i, i,
                                            i, i, f, p]
     lib.pgqa_paged_decode_e4m3.restype = i
+    lib.pgqa_paged_prefill_e4m3.argtypes = [p, p, p, p, p, p, p, i, p, i, i, i64, i64, i64, f, f,
+                                            i, i, i, i, i, i, f, p]
+    lib.pgqa_paged_prefill_e4m3.restype = i
     lib.pgqa_set_workspace.argtypes, lib.pgqa_set_workspace.restype = [p, sz], i
     lib.pgqa_workspace_bytes_prefill.argtypes = [i, i64, i, i]
     lib.pgqa_workspace_bytes_prefill.restype = sz
@@ -191,15 +194,18 @@ def ragged_prefill(q, k, v, q_indptr, kv_indptr, causal=True, sm_scale=None, out
 
 
 def paged_prefill(q, k_pages, v_pages, q_indptr, page_table, kv_lens, causal=True, sm_scale=None,
-                  out=None, lse=None, return_lse=True, stream=None, kv_layout="NHD"):
+                  out=None, lse=None, return_lse=True, stream=None, kv_layout="NHD",
+                  k_scale=1.0, v_scale=1.0, max_qo_len=None):
     """Paged prefill / append (pgqa_paged_prefill_bf16, or the _strided call for HND or
-    non-contiguous page pools).
+    non-contiguous page pools; pgqa_paged_prefill_e4m3 for FP8 E4M3 pools).
 
     q [total_q, Hq, d] bf16 with q_indptr [batch + 1] int32; k_pages / v_pages
     [num_pages, page_size, Hk, d] (kv_layout "NHD") or [num_pages, Hk, page_size, d]
-    ("HND") bf16, any strides with d contiguous; page_table [batch, stride] int32; kv_lens
-    [batch] int32 (keys per request, the cached prefix plus the new tokens); all on one
-    CUDA device.  Returns (o [total_q, Hq, d] bf16, lse [total_q, Hq] fp32 or None).
+    ("HND"), any strides with d contiguous, bf16 or E4M3 bytes (uint8 / float8_e4m3fn,
+    element = e4m3 x k_scale / v_scale); page_table [batch, stride] int32; kv_lens [batch]
+    int32 (keys per request, the cached prefix plus the new tokens); all on one CUDA device.
+    E4M3 pools need max_qo_len, the most query rows any request has (q_indptr stays on the
+    device).  Returns (o [total_q, Hq, d] bf16, lse [total_q, Hq] fp32 or None).
     """
     dev = q.device
     _check(q, "q", torch.bfloat16, 3, dev)
@@ -207,8 +213,12 @@ def paged_prefill(q, k_pages, v_pages, q_indptr, page_table, kv_lens, causal=Tru
     _check(page_table, "page_table", torch.int32, 2, dev)
     _check(kv_lens, "kv_lens", torch.int32, 1, dev)
     total_q, hq, d = q.shape
-    num_pages, page_size, hk, dk, strides, packed = _page_pools(k_pages, v_pages, kv_layout, dev)
+    num_pages, page_size, hk, dk, strides, packed = _page_pools(k_pages, v_pages, kv_layout, dev,
+                                                                allow_e4m3=True)
+    e4m3 = k_pages.element_size() == 1
     batch = q_indptr.numel() - 1
+    if e4m3 and max_qo_len is None:
+        raise ValueError("an E4M3 paged prefill needs max_qo_len")
     if dk != d:
         raise ValueError("k_pages / v_pages must have q's head_dim")
     if page_table.shape[0] != batch or kv_lens.numel() != batch:
@@ -222,10 +232,17 @@ def paged_prefill(q, k_pages, v_pages, q_indptr, page_table, kv_lens, causal=Tru
         lse = torch.empty((total_q, hq), dtype=torch.float32, device=dev)
     if lse is not None:
         _check(lse, "lse", torch.float32, 2, dev)
-    name = "pgqa_paged_prefill_bf16" if packed else "pgqa_paged_prefill_bf16_strided"
+    name = ("pgqa_paged_prefill_e4m3" if e4m3 else
+            "pgqa_paged_prefill_bf16" if packed else "pgqa_paged_prefill_bf16_strided")
     with torch.cuda.device(dev):  # the library works on the current device
         st = _stream(stream, dev)
-        if packed:
+        if e4m3:
+            rc = lib.pgqa_paged_prefill_e4m3(
+                _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(out), _ptr(lse), _ptr(q_indptr),
+                _ptr(page_table), page_table.shape[1], _ptr(kv_lens), page_size, num_pages,
+                *strides, float(k_scale), float(v_scale), batch, int(max_qo_len), hq, hk, d,
+                int(bool(causal)), float(sm_scale), st)
+        elif packed:
             rc = lib.pgqa_paged_prefill_bf16(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(out),
                                              _ptr(lse), _ptr(q_indptr), _ptr(page_table),
                                              page_table.shape[1], _ptr(kv_lens), page_size,

@@ -321,13 +321,18 @@ void fill_split(prefill::PlanParams& pp, prefill::Params& p, const PrefillWs& w,
     p.batch = batch;
 }
 
-size_t decode_ws_bytes(int batch, int stride, int page_size, int hq, int d, int hk) {
+// Decode workspace: chunk offsets and kv lengths (plus query offsets and lengths when the
+// requests have several query rows), then the partial lse and outputs of every chunk with
+// room for max_qo query rows each.
+size_t decode_ints(int batch, bool rows) { return (size_t)((rows ? 4 : 2) * (size_t)batch + 1); }
+size_t decode_ws_bytes(int batch, int stride, int page_size, int hq, int d, int hk, bool rows,
+                       int max_qo) {
     const long long max_kv = (long long)stride * page_size;
     const long long chunks =
         decode::total_chunks(batch, max_kv, decode::chunk_keys(batch, max_kv, hk));
-    const size_t ints = align_up((size_t)(2 * batch + 1) * sizeof(int), 256);
-    return kWsArrays + ints + align_up((size_t)chunks * hq * sizeof(float), 256) +
-           (size_t)chunks * hq * d * sizeof(float);
+    const size_t slots = (size_t)chunks * max_qo * hq;
+    const size_t ints = align_up(decode_ints(batch, rows) * sizeof(int), 256);
+    return kWsArrays + ints + align_up(slots * sizeof(float), 256) + slots * d * sizeof(float);
 }
 
 }  // namespace
@@ -341,7 +346,8 @@ int paged_decode_impl(const void* q, const void* k_pages, const void* v_pages,
                       int page_table_stride, int num_pages, int64_t page_stride,
                       int64_t slot_stride, int64_t head_stride, void* o, float* lse, int batch,
                       int num_qo_heads, int num_kv_heads, int head_dim, float sm_scale, bool kv8,
-                      float k_scale, float v_scale, pgqa_stream_t stream);
+                      float k_scale, float v_scale, const int32_t* q_indptr, int max_qo,
+                      int causal, pgqa_stream_t stream);
 }  // namespace
 
 extern "C" {
@@ -377,7 +383,8 @@ size_t pgqa_workspace_bytes_decode(int batch, int page_table_stride, int page_si
         head_dim <= 0)
         return 0;
     // an upper bound for any number of kv heads (one kv head gives the most chunks)
-    return decode_ws_bytes(batch, page_table_stride, page_size, num_qo_heads, head_dim, 1);
+    return decode_ws_bytes(batch, page_table_stride, page_size, num_qo_heads, head_dim, 1, false,
+                           1);
 }
 
 int pgqa_set_workspace(void* ptr, size_t bytes) {
@@ -704,8 +711,10 @@ int pgqa_paged_decode_bf16_strided(const void* q, const void* k_pages, const voi
     return paged_decode_impl(q, k_pages, v_pages, page_table, kv_lens, page_size,
                              page_table_stride, num_pages, page_stride, slot_stride, head_stride,
                              o, lse, batch, num_qo_heads, num_kv_heads, head_dim, sm_scale, false,
-                             1.f, 1.f, stream);
+                             1.f, 1.f, nullptr, 1, 1, stream);
 }
+
+static bool finite_scale(float x) { return x == x && x <= 3.0e38f && x >= -3.0e38f; }
 
 int pgqa_paged_decode_e4m3(const void* q, const void* k_pages, const void* v_pages,
                            const int32_t* page_table, const int32_t* kv_lens, int page_size,
@@ -713,13 +722,30 @@ int pgqa_paged_decode_e4m3(const void* q, const void* k_pages, const void* v_pag
                            int64_t slot_stride, int64_t head_stride, float k_scale, float v_scale,
                            void* o, float* lse, int batch, int num_qo_heads, int num_kv_heads,
                            int head_dim, float sm_scale, pgqa_stream_t stream) {
-    if (!(k_scale == k_scale) || !(v_scale == v_scale) || k_scale > 3.0e38f ||
-        k_scale < -3.0e38f || v_scale > 3.0e38f || v_scale < -3.0e38f)
-        return PGQA_ERR_INVALID_ARG;
+    if (!finite_scale(k_scale) || !finite_scale(v_scale)) return PGQA_ERR_INVALID_ARG;
     return paged_decode_impl(q, k_pages, v_pages, page_table, kv_lens, page_size,
                              page_table_stride, num_pages, page_stride, slot_stride, head_stride,
                              o, lse, batch, num_qo_heads, num_kv_heads, head_dim, sm_scale, true,
-                             k_scale, v_scale, stream);
+                             k_scale, v_scale, nullptr, 1, 1, stream);
+}
+
+int pgqa_paged_prefill_e4m3(const void* q, const void* k_pages, const void* v_pages, void* o,
+                            float* lse, const int32_t* q_indptr, const int32_t* page_table,
+                            int page_table_stride, const int32_t* kv_lens, int page_size,
+                            int num_pages, int64_t page_stride, int64_t slot_stride,
+                            int64_t head_stride, float k_scale, float v_scale, int batch,
+                            int max_qo_len, int num_qo_heads, int num_kv_heads, int head_dim,
+                            int causal, float sm_scale, pgqa_stream_t stream) {
+    if (!finite_scale(k_scale) || !finite_scale(v_scale)) return PGQA_ERR_INVALID_ARG;
+    if (batch > 0 && (max_qo_len < 1 || !q_indptr)) return PGQA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(q_indptr) & 3u) return PGQA_ERR_INVALID_ARG;
+    if (num_kv_heads > 0 && num_qo_heads % num_kv_heads == 0 && batch > 0 &&
+        (long long)max_qo_len * (num_qo_heads / num_kv_heads) > 16)
+        return PGQA_ERR_UNSUPPORTED;
+    return paged_decode_impl(q, k_pages, v_pages, page_table, kv_lens, page_size,
+                             page_table_stride, num_pages, page_stride, slot_stride, head_stride,
+                             o, lse, batch, num_qo_heads, num_kv_heads, head_dim, sm_scale, true,
+                             k_scale, v_scale, q_indptr, max_qo_len, causal ? 1 : 0, stream);
 }
 
 }  // extern "C"
@@ -732,7 +758,8 @@ int paged_decode_impl(const void* q, const void* k_pages, const void* v_pages,
                       int page_table_stride, int num_pages, int64_t page_stride,
                       int64_t slot_stride, int64_t head_stride, void* o, float* lse, int batch,
                       int num_qo_heads, int num_kv_heads, int head_dim, float sm_scale, bool kv8,
-                      float k_scale, float v_scale, pgqa_stream_t stream) {
+                      float k_scale, float v_scale, const int32_t* q_indptr, int max_qo,
+                      int causal, pgqa_stream_t stream) {
     if (batch < 0 || num_qo_heads <= 0 || num_kv_heads <= 0 || page_table_stride < 0 ||
         num_pages < 0)
         return PGQA_ERR_INVALID_ARG;
@@ -761,8 +788,9 @@ int paged_decode_impl(const void* q, const void* k_pages, const void* v_pages,
     int rc = current_device(&dev, &st);
     if (rc != PGQA_OK) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const bool rows = q_indptr != nullptr;
     const size_t need = decode_ws_bytes(batch, page_table_stride, page_size, num_qo_heads, head_dim,
-                                        num_kv_heads);
+                                        num_kv_heads, rows, max_qo);
     rc = ensure_workspace(*st, need, s);
     if (rc != PGQA_OK) return rc;
 
@@ -770,13 +798,15 @@ int paged_decode_impl(const void* q, const void* k_pages, const void* v_pages,
     WsHeader* hdr = reinterpret_cast<WsHeader*>(ws + kWsHeader);
     int* chunk_off = reinterpret_cast<int*>(ws + kWsArrays);
     int* kv_eff = chunk_off + (batch + 1);
-    const size_t lse_off = kWsArrays + align_up((size_t)(2 * batch + 1) * sizeof(int), 256);
+    int* q_off = rows ? kv_eff + batch : nullptr;
+    int* q_len = rows ? q_off + batch : nullptr;
+    const size_t lse_off = kWsArrays + align_up(decode_ints(batch, rows) * sizeof(int), 256);
     const long long max_kv = (long long)page_table_stride * page_size;
     const int chunk = decode::chunk_keys(batch, max_kv, num_kv_heads);
     const long long chunks = decode::total_chunks(batch, max_kv, chunk);
     float* part_lse = reinterpret_cast<float*>(ws + lse_off);
     float* part_o = reinterpret_cast<float*>(
-        ws + lse_off + align_up((size_t)chunks * num_qo_heads * sizeof(float), 256));
+        ws + lse_off + align_up((size_t)chunks * max_qo * num_qo_heads * sizeof(float), 256));
 
     decode::PlanParams pp;
     pp.kv_lens = kv_lens;
@@ -786,6 +816,10 @@ int paged_decode_impl(const void* q, const void* k_pages, const void* v_pages,
     pp.batch = batch;
     pp.max_kv = (int)max_kv;
     pp.chunk = chunk;
+    pp.q_indptr = q_indptr;
+    pp.q_off = q_off;
+    pp.q_len = q_len;
+    pp.max_qo = max_qo;
     cudaError_t e = decode::launch_plan(pp, s);
     if (e != cudaSuccess) return PGQA_ERR_CUDA;
 
@@ -809,6 +843,10 @@ int paged_decode_impl(const void* q, const void* k_pages, const void* v_pages,
     p.num_kv_heads = num_kv_heads;
     p.scale_log2 = sm_scale * 1.4426950408889634f * k_scale;
     p.v_scale = v_scale;
+    p.q_off = q_off;
+    p.q_len = q_len;
+    p.max_qo = max_qo;
+    p.causal = causal;
     p.chunk_capacity = chunks;
     p.chunk = chunk;
     if (decode::prepare_page_maps(p, k_pages, v_pages, num_pages, num_kv_heads, page_size,

@@ -46,6 +46,18 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(PlanParams p) {
                 atomicOr(p.status, PGQA_DEV_BOUNDS);
                 n = 0;
             }
+            if (p.q_indptr != nullptr) {
+                // a request with a bad query range keeps no keys and no rows: nothing of it
+                // is computed or written
+                const int q0 = p.q_indptr[b], qo = p.q_indptr[b + 1] - q0;
+                const bool q_ok = q0 >= 0 && qo >= 0 && qo <= p.max_qo;
+                if (!q_ok) {
+                    atomicOr(p.status, PGQA_DEV_BOUNDS);
+                    n = 0;
+                }
+                p.q_off[b] = q_ok ? q0 : 0;
+                p.q_len[b] = q_ok ? qo : 0;
+            }
             p.kv_eff[b] = n;
             cnt = n > 0 ? (n + p.chunk - 1) / p.chunk : 1;
         }
@@ -421,7 +433,8 @@ constexpr int MERGE_GROUP = 8;
 constexpr int MERGE_WARPS = 8;
 
 struct MergeRow {
-    int b, h, f0, nch;
+    int b, i, h, f0, nch;  // request, its query row i, head, first chunk, chunks
+    int orow;              // output row
 };
 
 // one group's weighted sum (lane: 4 of the D columns) and weight sum
@@ -431,16 +444,17 @@ __device__ __forceinline__ void merge_group(const Params& p, const MergeRow& r, 
     const int Hq = p.num_qo_heads;
     const int c0 = g * MERGE_GROUP;
     const int n = min(MERGE_GROUP, r.nch - c0);
-    const float* lp = p.part_lse + (size_t)(r.f0 + c0) * Hq + r.h;
-    const float4* vp =
-        reinterpret_cast<const float4*>(p.part_o + ((size_t)(r.f0 + c0) * Hq + r.h) * D) + lane;
-    const size_t vstride = (size_t)Hq * D / 4;  // float4s from one chunk's row to the next
+    const size_t qh = (size_t)p.max_qo * Hq;   // partial slots per chunk
+    const size_t s0 = (size_t)(r.f0 + c0) * qh + (size_t)r.i * Hq + r.h;
+    const float* lp = p.part_lse + s0;
+    const float4* vp = reinterpret_cast<const float4*>(p.part_o + s0 * D) + lane;
+    const size_t vstride = qh * D / 4;  // float4s from one chunk's row to the next
     float l[MERGE_GROUP];
     float4 v[MERGE_GROUP];
 #pragma unroll
     for (int u = 0; u < MERGE_GROUP; ++u) {  // every load of the group before any arithmetic
         if (u < n) {
-            l[u] = lp[(size_t)u * Hq];
+            l[u] = lp[(size_t)u * qh];
             v[u] = vp[(size_t)u * vstride];
         }
     }
@@ -464,12 +478,13 @@ __device__ __forceinline__ void merge_store(const Params& p, const MergeRow& r, 
     constexpr int D = HEAD_DIM;
     const int Hq = p.num_qo_heads;
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    __nv_bfloat16* op = reinterpret_cast<__nv_bfloat16*>(p.o) + ((size_t)r.b * Hq + r.h) * D;
+    __nv_bfloat16* op = reinterpret_cast<__nv_bfloat16*>(p.o) + ((size_t)r.orow * Hq + r.h) * D;
     uint2 u;
     u.x = pack_bf16x2(acc.x * inv, acc.y * inv);
     u.y = pack_bf16x2(acc.z * inv, acc.w * inv);
     *reinterpret_cast<uint2*>(op + lane * 4) = u;
-    if (lane == 0 && p.lse) p.lse[(size_t)r.b * Hq + r.h] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
+    if (lane == 0 && p.lse)
+        p.lse[(size_t)r.orow * Hq + r.h] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
 }
 
 __device__ __forceinline__ float4 f4_add(const float4& a, const float4& b) {
@@ -482,10 +497,14 @@ __global__ void __launch_bounds__(MERGE_WARPS * 32) merge_kernel(const Params p)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int Hq = p.num_qo_heads;
     const long long row = SPLIT ? (long long)blockIdx.x : (long long)blockIdx.x * MERGE_WARPS + warp;
-    if (row >= (long long)p.batch * Hq) return;  // uniform per CTA when SPLIT
+    const long long qh = (long long)p.max_qo * Hq;
+    if (row >= (long long)p.batch * qh) return;  // uniform per CTA when SPLIT
     MergeRow r;
-    r.b = (int)(row / Hq);
+    r.b = (int)(row / qh);
+    r.i = (int)((row % qh) / Hq);
     r.h = (int)(row % Hq);
+    if (p.q_off != nullptr && r.i >= __ldg(p.q_len + r.b)) return;  // no such query row
+    r.orow = p.q_off != nullptr ? __ldg(p.q_off + r.b) + r.i : r.b;
     r.f0 = __ldg(p.chunk_off + r.b);
     r.nch = __ldg(p.chunk_off + r.b + 1) - r.f0;
     if (r.nch <= 1) return;  // written by the decode kernel
@@ -494,7 +513,7 @@ __global__ void __launch_bounds__(MERGE_WARPS * 32) merge_kernel(const Params p)
     const int t0 = SPLIT ? warp * 32 + lane : lane, tstep = SPLIT ? MERGE_WARPS * 32 : 32;
     float mx = -INFINITY;
     for (int c = t0; c < r.nch; c += tstep)
-        mx = fmaxf(mx, p.part_lse[(size_t)(r.f0 + c) * Hq + r.h]);
+        mx = fmaxf(mx, p.part_lse[(size_t)(r.f0 + c) * qh + (size_t)r.i * Hq + r.h]);
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
     if constexpr (SPLIT) {
@@ -638,7 +657,7 @@ cudaError_t launch_decode(const Params& p, int group, int num_sms, cudaStream_t 
 }
 
 cudaError_t launch_merge(const Params& p, cudaStream_t stream) {
-    const long long rows = (long long)p.batch * p.num_qo_heads;
+    const long long rows = (long long)p.batch * p.max_qo * p.num_qo_heads;
     if (rows <= 0) return cudaSuccess;
     // too few rows to fill the GPU with one warp per row: a CTA per row (the result is
     // the same bits either way)

@@ -4,10 +4,14 @@
 // request-local chunks; partial results merged by log-sum-exp weights) with K/V stored as
 // OCP E4M3 bytes and one scale per tensor:
 //   o[b,h] = v_scale * softmax_j(sm_scale * k_scale * q[b,h] . k8[j, h/G]) v8[j, h/G]
+// and the same for a few query rows per request (a paged prefill of at most 16 / G rows per
+// request, as in multi-token decode): row i of a request with qo rows and kv keys sees the
+// keys j <= i + kv - qo when causal, all kv keys otherwise.
 // Sources: FlashInfer documentation, flashinfer_benchmark.py "Attention Flags"
-// (--kv_dtype fp8_e4m3); vllm-rlt pull request "feat: add FlashInfer attention backend for
-// SM120 decode" (paged decode over a block table, padding never visible); FlashInfer
-// documentation, flashinfer.cascade "Merge Attention States" (the chunk merge).
+// (--kv_dtype fp8_e4m3; --causal for the prefill routines); vllm-rlt pull request "feat: add
+// FlashInfer attention backend for SM120 decode" (paged decode over a block table, padding
+// never visible); FlashInfer documentation, flashinfer.cascade "Merge Attention States"
+// (the chunk merge).
 //
 // Why tensor cores: on the CUDA cores every E4M3 byte costs a conversion plus G fused
 // multiply-adds per K and V element, so the E4M3 decode ran into the issue rate at about
@@ -28,21 +32,24 @@
 //    layout.  Keys past the chunk or in a page that was not loaded become zeros.  At each
 //    item start warpgroup 0 writes the G query rows as f16, scaled by a power of two 2^e
 //    chosen from max|q| so that they sit well inside f16's range (exact for bf16 inputs).
-//  * warp 1, MMA issuer (swap-AB, keys as M = 128, query heads padded to N = 16):
+//  * warp 1, MMA issuer (swap-AB, keys as M = 128, query heads padded to N = 16; with
+//    several query rows per request, column n is row n / G, head n % G):
 //      S^T_t  = K_t . (2^e Q)^T        A = K tile (K-major), B = Q (K-major)
-//      O^T   += V_t^T . P_t^T          A = V tile (MN-major), B = P^T (K-major, smem)
+//      O^T   += V_t^T . P_t^T          A = V tile (MN-major), B = P^T (MN-major, smem)
 //    Every S^T tile of an item stays in tensor memory (two item regions of 8 x 16 columns)
 //    so the softmax sees the whole item at once; O^T takes 16 more columns and three K
 //    tiles 3 x 64.
 //  * warps 10-13, softmax: thread r owns key r of every tile (TMEM lane r).  Per item: one
-//    pass over all its S^T tiles gives the exact max per head (a warp butterfly and one
-//    exchange among the four warps), so no running rescale is needed; then each tile's
-//    P^T = exp2(s - max) goes to shared memory as f16 while the row sums accumulate; at
-//    the item's end thread r holds column r of O^T: divided by l, scaled by v_scale, it
-//    becomes the bf16 output (single-chunk request) or the fp32 partial and its lse.
+//    pass over all its S^T tiles gives the exact max per column (a transposing warp
+//    butterfly and one exchange among the four warps), so no running rescale is needed;
+//    then each tile's P^T = exp2(s - max) goes to shared memory as f16 (key r's columns
+//    in one 32-byte row: the MN-major B operand) while the column sums accumulate; at the
+//    item's end thread r holds row r of O^T: divided by l, scaled by v_scale, it becomes
+//    the bf16 output (single-chunk request) or the fp32 partial and its lse.
 //  While the softmax works on item s - 1, the converter and the tensor core are already on
 //  the K tiles of item s.
 #include <atomic>
+#include <climits>
 
 #include "ptx.cuh"
 
@@ -62,8 +69,8 @@ constexpr int MAX_TILES = 8;                // tiles per item (chunks of at most
 constexpr int RAW_BYTES = TK * D;           // 16 KB of E4M3 per K or V tile
 constexpr int CVT_BYTES = TK * D * 2;       // 32 KB of f16
 constexpr int CVT_CHUNK = TK * 128;         // one 64-column chunk of a converted tile
-constexpr int QP_BYTES = NH * D * 2;        // 4 KB: Q (16 x 128 dims) or P^T (16 x 128 keys)
-constexpr int QP_CHUNK = NH * 128;          // one 64-column chunk of Q or P^T
+constexpr int QP_BYTES = NH * D * 2;        // 4 KB: Q (16 x 128 dims) or P^T (128 keys x 16)
+constexpr int QP_CHUNK = NH * 128;          // one 64-column chunk of Q
 constexpr int PRODUCERS = 2;                // TMA producer warps (0 and 14)
 constexpr int THREADS = 448 + 32 * (PRODUCERS - 1);
 constexpr int CVT_THREADS = 256;            // two converter warpgroups share every tile
@@ -104,9 +111,11 @@ __device__ __forceinline__ uint32_t sw128_off(int row, int col, int chunk_bytes)
                       ((col & 7) << 1));
 }
 
-// Geometry of work item `item`: request b, kv head g, chunk c of nch, keys [tok0, tok1).
+// Geometry of work item `item`: request b, kv head g, chunk f (of the request's nch),
+// keys [tok0, tok1) of the request's kv; its query rows q0 .. q0 + qo - 1.  An item with
+// no query rows has no tiles.
 struct Item {
-    int b, g, f, nch, tok0, tok1, ntiles;
+    int b, g, f, nch, tok0, tok1, ntiles, kv, q0, qo;
 };
 __device__ __forceinline__ Item item_of(const Params& p, long long item) {
     Item it;
@@ -123,30 +132,35 @@ __device__ __forceinline__ Item item_of(const Params& p, long long item) {
     const int c0 = __ldg(p.chunk_off + lo);
     it.nch = __ldg(p.chunk_off + lo + 1) - c0;
     const int kv = __ldg(p.kv_eff + lo);
+    it.kv = kv;
+    it.q0 = p.q_off != nullptr ? __ldg(p.q_off + lo) : lo;
+    it.qo = p.q_off != nullptr ? __ldg(p.q_len + lo) : 1;
     it.tok0 = (it.f - c0) * p.chunk;
     it.tok1 = min(kv, it.tok0 + p.chunk);
-    it.ntiles = it.tok1 > it.tok0 ? (it.tok1 - it.tok0 + TK - 1) / TK : 0;
+    it.ntiles = it.tok1 > it.tok0 && it.qo > 0 ? (it.tok1 - it.tok0 + TK - 1) / TK : 0;
     return it;
 }
 
 // Exchange of per-warp values among the four warps of a warpgroup through shared memory
 // and an mbarrier of count 4 (lane 0 of each warp writes its warp's values, then arrives),
 // with a bounded wait: a warp that has given up never leaves the others waiting forever.
-// Two areas of 4 x 8 floats alternate by use, so a warp may write the next exchange while
-// a slower one still reads this one (it cannot get two exchanges ahead).
+// Two areas of 4 x W floats alternate by use, so a warp may write the next exchange while
+// a slower one still reads this one (it cannot get two exchanges ahead).  Warp w's values
+// come back at out[w * W + i].
 struct WgExchange {
     uint32_t bar;
-    float* area;   // 2 x 32 floats
+    float* area;   // 2 x 4 x W floats
     uint32_t use;
 };
-template <int N>
+template <int N, int W = 8>
 __device__ __forceinline__ bool wg_exchange(WgExchange& x, const float (&vals)[N], int warp4,
                                             int lane, volatile int* abort_flag, int* status,
                                             const float*& out) {
-    float* a = x.area + (x.use & 1) * 32;
+    static_assert(N <= W, "exchange width");
+    float* a = x.area + (x.use & 1) * 4 * W;
     if (lane == 0) {
 #pragma unroll
-        for (int i = 0; i < N; ++i) a[warp4 * 8 + i] = vals[i];
+        for (int i = 0; i < N; ++i) a[warp4 * W + i] = vals[i];
         mbar_arrive(x.bar);
     }
     const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(x.bar, x.use & 1, abort_flag, status));
@@ -155,24 +169,29 @@ __device__ __forceinline__ bool wg_exchange(WgExchange& x, const float (&vals)[N
     return ok;
 }
 
-// The G query rows of item (b, g), column d (thread d of a warpgroup), as floats.
-template <int G>
-__device__ __forceinline__ void load_q(const Params& p, int b, int g, int d, float (&qv)[G]) {
+// The query rows of an item as the MMA's N = NR columns, column d (thread d of a
+// warpgroup), as floats: column n is query row n / G of the item, head g * G + n % G.
+// Columns past the item's qo * G rows are zero.
+template <int G, int NR>
+__device__ __forceinline__ void load_q(const Params& p, const Item& it, int d, float (&qv)[NR]) {
+    const int Hq = p.num_qo_heads;
     const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(p.q) +
-                             ((size_t)b * p.num_qo_heads + (size_t)g * G) * D + d;
+                             ((size_t)it.q0 * Hq + (size_t)it.g * G) * D + d;
+    const int nrows = it.qo * G;
 #pragma unroll
-    for (int h = 0; h < G; ++h) qv[h] = __bfloat162float(q[h * D]);
+    for (int n = 0; n < NR; ++n)
+        qv[n] = n < nrows ? __bfloat162float(q[((size_t)(n / G) * Hq + n % G) * D]) : 0.f;
 }
 
 // Power-of-two exponent e for the query rows of an item: 2^e * max|q| lies in
 // [2^14, 2^15), so the scaled rows fit f16 with bf16's precision intact.  Warpgroup-wide
-// (thread d holds column d of the G rows).
-template <int G>
-__device__ __forceinline__ bool q_exponent(const float (&qv)[G], int d, WgExchange& x,
+// (thread d holds column d of the NR rows).
+template <int NR>
+__device__ __forceinline__ bool q_exponent(const float (&qv)[NR], int d, WgExchange& x,
                                            volatile int* abort_flag, int* status, int& e) {
     float m[1] = {0.f};
 #pragma unroll
-    for (int h = 0; h < G; ++h) m[0] = fmaxf(m[0], fabsf(qv[h]));
+    for (int h = 0; h < NR; ++h) m[0] = fmaxf(m[0], fabsf(qv[h]));
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1)
         m[0] = fmaxf(m[0], __shfl_xor_sync(0xffffffffu, m[0], off));
@@ -189,6 +208,60 @@ __device__ __forceinline__ bool q_exponent(const float (&qv)[G], int d, WgExchan
 
 __device__ __forceinline__ float exp2i(int e) { return __int_as_float((e + 127) << 23); }
 
+__device__ __forceinline__ uint32_t half2_bits(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// One step of a transposing butterfly over the lanes: N values per lane become N / 2, each
+// combined (max or sum) over the lane pair (lane, lane ^ OFF); the lane with bit OFF set
+// keeps the upper half.  With N == 1 it is a plain butterfly step.
+template <int N, int OFF, bool MAX>
+__device__ __forceinline__ void tr_step(float* a, int lane) {
+    if constexpr (N >= 2) {
+        const bool up = (lane & OFF) != 0;
+#pragma unroll
+        for (int i = 0; i < N / 2; ++i) {
+            const float keep = up ? a[i + N / 2] : a[i];
+            const float send = up ? a[i] : a[i + N / 2];
+            const float other = __shfl_xor_sync(0xffffffffu, send, OFF);
+            a[i] = MAX ? fmaxf(keep, other) : keep + other;
+        }
+    } else {
+        const float other = __shfl_xor_sync(0xffffffffu, a[0], OFF);
+        a[0] = MAX ? fmaxf(a[0], other) : a[0] + other;
+    }
+}
+__host__ __device__ constexpr int at_least_1(int n) { return n > 1 ? n : 1; }
+// Max or sum of each of N per-lane values over the warp; afterwards a[0] of lane L holds
+// the result for value L / (32 / N).  Every value is summed over the same tree of lane
+// pairs whatever N is, so a column's sum does not depend on how many columns there are.
+template <int N, bool MAX>
+__device__ __forceinline__ void tr_reduce(float (&a)[N], int lane) {
+    tr_step<N, 16, MAX>(a, lane);
+    tr_step<at_least_1(N / 2), 8, MAX>(a, lane);
+    tr_step<at_least_1(N / 4), 4, MAX>(a, lane);
+    tr_step<at_least_1(N / 8), 2, MAX>(a, lane);
+    tr_step<at_least_1(N / 16), 1, MAX>(a, lane);
+}
+
+// wg_exchange for values spread over the lanes as tr_reduce leaves them: lane L holds
+// value L / (32 / N) of its warp; warp w's values come back at out[w * W + i].
+template <int N, int W>
+__device__ __forceinline__ bool wg_exchange_cols(WgExchange& x, float val, int warp4, int lane,
+                                                 volatile int* abort_flag, int* status,
+                                                 const float*& out) {
+    static_assert(N <= W && 32 % N == 0, "exchange width");
+    float* a = x.area + (x.use & 1) * 4 * W;
+    if (lane % (32 / N) == 0) a[warp4 * W + lane / (32 / N)] = val;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(x.bar);
+    const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(x.bar, x.use & 1, abort_flag, status));
+    ++x.use;
+    out = a;
+    return ok;
+}
+
 // 16 E4M3 bytes -> 16 f16 (exact), as two 16-byte units
 __device__ __forceinline__ void e4m3x16_to_f16(const uint4& raw, uint4& lo, uint4& hi) {
     uint32_t h[8];
@@ -204,8 +277,12 @@ __device__ __forceinline__ void e4m3x16_to_f16(const uint4& raw, uint4& lo, uint
     hi = make_uint4(h[4], h[5], h[6], h[7]);
 }
 
-template <int G>
+// G query heads per kv head; NR = the MMA's used N columns: G (one query row per request)
+// or 16 (up to 16 / G query rows per request)
+template <int G, int NR>
 __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_constant__ Params p) {
+    static_assert(NR == G || NR == NH, "query columns");
+    constexpr int XW = NR <= 8 ? 8 : 16;  // width of the softmax exchanges
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -235,7 +312,9 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(BAR(Q_FULL + x), 128);
-            mbar_init(BAR(Q_EMPTY + x), 1);
+            // released by the QK MMAs' commit and by the four softmax warps once they have
+            // read the item's q exponent and unit mask (which the converter writes with Q)
+            mbar_init(BAR(Q_EMPTY + x), 1 + 4);
             mbar_init(BAR(S_FULL + x), 1);
             mbar_init(BAR(S_EMPTY + x), 128);
         }
@@ -253,7 +332,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
         *abort_flag = 0;
         fence_barrier_init();
     }
-    // Q and P^T rows G..15 stay zero: clear every buffer of both once
+    // Q rows and P^T columns NR..15 stay zero: clear every buffer of both once
     for (int i = threadIdx.x; i < (2 + NPB) * QP_BYTES / 16; i += THREADS)
         reinterpret_cast<uint4*>(smem + OFF_Q)[i] = make_uint4(0, 0, 0, 0);
     fence_async_smem();
@@ -360,7 +439,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t IDESC_S = idesc_f16_f32(TK, NH, false, false);
-            constexpr uint32_t IDESC_O = idesc_f16_f32(D, NH, true, false);
+            constexpr uint32_t IDESC_O = idesc_f16_f32(D, NH, true, true);
             uint32_t kt = 0, vt = 0, s = 0;  // K tiles, V tiles and items so far
             bool ok = true;
             auto qk_tiles = [&](const Item& it) {
@@ -396,14 +475,14 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
                     if (!ok) break;
                     tc_fence_after();
                     // A = V^T: MN-major, 64-dim chunks CVT_CHUNK apart, 8-key groups 1 KB
-                    // apart; B = P^T: K-major, 16 rows, 64-key chunks QP_CHUNK apart
+                    // apart; B = P^T: MN-major with the 32-byte swizzle (the 16 columns of
+                    // a key in one 32-byte row), 8-key groups 256 bytes apart
                     const uint64_t vdesc = sdesc_sw128(s0 + OFF_VC + xv * CVT_BYTES, CVT_CHUNK, 1024);
-                    const uint64_t pdesc = sdesc_sw128(s0 + OFF_P + x * QP_BYTES, 16, 1024);
+                    const uint64_t pdesc = sdesc_sw32(s0 + OFF_P + x * QP_BYTES, 256, 256);
 #pragma unroll
                     for (int k = 0; k < TK / 16; ++k)
                         mma_ss(tmem_base + TMEM_O, vdesc + (uint64_t)(k * 2048 / 16),
-                               pdesc + (uint64_t)(((k >> 2) * QP_CHUNK + (k & 3) * 32) / 16),
-                               IDESC_O, (t > 0 || k > 0) ? 1u : 0u);
+                               pdesc + (uint64_t)(k * 512 / 16), IDESC_O, (t > 0 || k > 0) ? 1u : 0u);
                     mma_commit(BAR(VC_EMPTY + xv));
                     mma_commit(BAR(P_EMPTY + x));
                 }
@@ -458,7 +537,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
             return st;
         };
         // Q of item s (from query rows already in registers), then its K tiles
-        auto k_tiles = [&](const Item& it, const float (&qv)[G]) {
+        auto k_tiles = [&](const Item& it, const float (&qv)[NR]) {
             const uint32_t qb = s & 1;
             if (cid == 0) {
                 ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(Q_EMPTY + qb),
@@ -466,14 +545,14 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
                                                                p.status));
                 if (!ok) return;
                 int e;
-                ok = q_exponent<G>(qv, i, xch, abort_flag, p.status, e);
+                ok = q_exponent<NR>(qv, i, xch, abort_flag, p.status, e);
                 if (!ok) return;
                 const float sc = exp2i(e);
                 uint8_t* qs = smem + OFF_Q + qb * QP_BYTES;
 #pragma unroll
-                for (int h = 0; h < G; ++h)
-                    *reinterpret_cast<__half*>(qs + sw128_off(h, i, QP_CHUNK)) =
-                        __float2half_rn(qv[h] * sc);
+                for (int n = 0; n < NR; ++n)
+                    *reinterpret_cast<__half*>(qs + sw128_off(n, i, QP_CHUNK)) =
+                        __float2half_rn(qv[n] * sc);
                 if (i == 0) qe[qb] = e;
                 fence_async_smem();
                 mbar_arrive(BAR(Q_FULL + qb));
@@ -561,38 +640,37 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
             return -1;
         };
         long long cur = next_item(blockIdx.x);
-        float qv[G];
+        float qv[NR];
 #pragma unroll
-        for (int h = 0; h < G; ++h) qv[h] = 0.f;
-        if (cur >= 0 && cid == 0) {
-            const Item it = item_of(p, cur);
-            load_q<G>(p, it.b, it.g, i, qv);
-        }
+        for (int n = 0; n < NR; ++n) qv[n] = 0.f;
+        if (cur >= 0 && cid == 0) load_q<G, NR>(p, item_of(p, cur), i, qv);
         Item prev;
         prev.ntiles = 0;
         while (ok && cur >= 0) {
             const Item it = item_of(p, cur);
             const long long nxt = next_item(cur + stride);
-            float qn[G];  // the next item's query rows, loaded while this one converts
+            float qn[NR];  // the next item's query rows, loaded while this one converts
 #pragma unroll
-            for (int h = 0; h < G; ++h) qn[h] = 0.f;
-            if (nxt >= 0 && cid == 0) {
-                const Item ni = item_of(p, nxt);
-                load_q<G>(p, ni.b, ni.g, i, qn);
-            }
+            for (int n = 0; n < NR; ++n) qn[n] = 0.f;
+            if (nxt >= 0 && cid == 0) load_q<G, NR>(p, item_of(p, nxt), i, qn);
             k_tiles(it, qv);
             if (ok && prev.ntiles > 0) v_tiles(prev);
             prev = it;
             ++s;
             cur = nxt;
 #pragma unroll
-            for (int h = 0; h < G; ++h) qv[h] = qn[h];
+            for (int n = 0; n < NR; ++n) qv[n] = qn[n];
         }
         if (ok && prev.ntiles > 0) v_tiles(prev);
     } else if (warp >= 10) {
         // ------------------------------------------------------------ softmax / epilogue
         // Per item s: (A) its S^T tiles and exact max; (B) the epilogue of item s - 1, whose
-        // last P.V completes while (A) runs; (C) its P^T tiles and row sums.
+        // last P.V completes while (A) runs; (C) its P^T tiles and column sums.  Column n
+        // of an S^T tile is query row n / G of the item, head n % G.  With NR = G columns
+        // the item's scores stay in registers between (A) and (C); with 16 columns (several
+        // query rows) (C) reads them from tensor memory a second time.  Column maxima and
+        // sums are reduced over a warp by a transposing butterfly and over the four warps
+        // through shared memory; lane n < NR then keeps column n's max and sum.
         const int w4 = warp & 3;                                // TMEM lane quarter
         const int r = 32 * w4 + lane;                           // key of a tile = TMEM lane
         const uint32_t lane_base = (uint32_t)(32 * w4) << 16;
@@ -600,49 +678,97 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
         const int* qe = reinterpret_cast<const int*>(smem + OFF_MASK + 40);
         const unsigned long long* kmask =
             reinterpret_cast<const unsigned long long*>(smem + OFF_MASK + 48);
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.o);
+        // key r's 16 columns in a P^T buffer (MN-major, 32-byte swizzle): 8-key atoms of
+        // 256 bytes, 32 bytes per key, 16-byte unit u at u ^ ((r >> 2) & 1)
+        const uint32_t p_row = (uint32_t)((r >> 3) * 256 + (r & 7) * 32);
+        const uint32_t p_sw = (uint32_t)(((r >> 2) & 1) << 4);
+        const int cl = lane < NR ? lane : 0;                    // this lane's column
         uint32_t pt = 0, s = 0;  // P^T tiles written, items
         bool ok = true;
         Item prev;
         prev.ntiles = 0;
-        float prev_m[G], prev_l[G];
+        float prev_m = 0.f, prev_l = 0.f;  // the previous item's max and sum of column cl
         // (B): wait for item j's last P.V, release O^T, write its outputs
-        auto epilogue = [&](const Item& it, uint32_t j, const float (&m)[G], const float (&l)[G]) {
+        auto epilogue = [&](const Item& it, uint32_t j, float m_c, float l_c) {
             ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(PV_LAST), j & 1, abort_flag,
                                                            p.status));
             if (!ok) return;
             tc_fence_after();
-            uint32_t v[8];
-            tmem_ld8(tmem_base + lane_base + TMEM_O, v);  // thread r: column r of O, all heads
-            tmem_wait_ld8(v);
+            float ov[NR];  // thread r: column r of O, every query column
+            if constexpr (NR <= 8) {
+                uint32_t v[8];
+                tmem_ld8(tmem_base + lane_base + TMEM_O, v);
+                tmem_wait_ld8(v);
+#pragma unroll
+                for (int n = 0; n < NR; ++n) ov[n] = __uint_as_float(v[n]);
+            } else {
+                uint32_t v[16];
+                tmem_ld16(tmem_base + lane_base + TMEM_O, v);
+                tmem_wait_ld16(v);
+#pragma unroll
+                for (int n = 0; n < NR; ++n) ov[n] = __uint_as_float(v[n]);
+            }
             tc_fence_before();
             mbar_arrive(BAR(O_EMPTY));
+            // lane n < NR: column n's output scale and lse
+            const float inv_c = l_c > 0.f ? p.v_scale / l_c : 0.f;
+            const float lse_c = l_c > 0.f ? (m_c + log2f(l_c)) * 0.69314718055994531f : -INFINITY;
+            const int nrows = it.qo * G;
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const float inv = l[h] > 0.f ? p.v_scale / l[h] : 0.f;
-                const float lse_v = l[h] > 0.f ? (m[h] + log2f(l[h])) * 0.69314718055994531f
-                                               : -INFINITY;
-                const int hq = it.g * G + h;
-                const float o = __uint_as_float(v[h]) * inv;
+            for (int n = 0; n < NR; ++n) {
+                const float inv = __shfl_sync(0xffffffffu, inv_c, n);
+                if (n < nrows) {
+                    const int qi = n / G, hq = it.g * G + n % G;
+                    const float o = ov[n] * inv;
+                    if (it.nch == 1)
+                        out[((size_t)(it.q0 + qi) * Hq + hq) * D + r] = __float2bfloat16_rn(o);
+                    else
+                        p.part_o[(((size_t)it.f * p.max_qo + qi) * Hq + hq) * D + r] = o;
+                }
+            }
+            if (w4 == 0 && lane < NR && lane < nrows) {
+                const int qi = lane / G, hq = it.g * G + lane % G;
                 if (it.nch == 1) {
-                    reinterpret_cast<__nv_bfloat16*>(p.o)[((size_t)it.b * Hq + hq) * D + r] =
-                        __float2bfloat16_rn(o);
-                    if (r == 0 && p.lse) p.lse[(size_t)it.b * Hq + hq] = lse_v;
+                    if (p.lse) p.lse[(size_t)(it.q0 + qi) * Hq + hq] = lse_c;
                 } else {
-                    p.part_o[((size_t)it.f * Hq + hq) * D + r] = o;
-                    if (r == 0) p.part_lse[(size_t)it.f * Hq + hq] = lse_v;
+                    p.part_lse[((size_t)it.f * p.max_qo + qi) * Hq + hq] = lse_c;
+                }
+            }
+        };
+        // P^T values of key r for the NR columns, as f16, into P^T buffer pp (columns past
+        // NR keep the zeros written at start-up)
+        auto store_p = [&](uint8_t* pp, const float (&pv)[NR]) {
+            uint8_t* row = pp + p_row;
+            if constexpr (NR == 1) {
+                *reinterpret_cast<__half*>(row + p_sw) = __float2half_rn(pv[0]);
+            } else {
+                uint32_t h[NR / 2];
+#pragma unroll
+                for (int i = 0; i < NR / 2; ++i) h[i] = half2_bits(pv[2 * i], pv[2 * i + 1]);
+                if constexpr (NR == 2) {
+                    *reinterpret_cast<uint32_t*>(row + p_sw) = h[0];
+                } else if constexpr (NR == 4) {
+                    *reinterpret_cast<uint2*>(row + p_sw) = make_uint2(h[0], h[1]);
+                } else {
+                    *reinterpret_cast<uint4*>(row + p_sw) = make_uint4(h[0], h[1], h[2], h[3]);
+                    if constexpr (NR == 16)
+                        *reinterpret_cast<uint4*>(row + (p_sw ^ 16u)) =
+                            make_uint4(h[4], h[5], h[6], h[7]);
                 }
             }
         };
         for (long long item = blockIdx.x; ok && item < n_items; item += stride) {
             const Item it = item_of(p, item);
             if (it.ntiles == 0) {
-                // no keys: zeros and lse = -inf (a request of a single empty chunk)
-                if (r < G * D / 8) {
-                    const int h = r / (D / 8), c = r % (D / 8);
-                    reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) +
-                                             ((size_t)it.b * Hq + it.g * G + h) * D)[c] =
-                        make_uint4(0, 0, 0, 0);
-                    if (c == 0 && p.lse) p.lse[(size_t)it.b * Hq + it.g * G + h] = -INFINITY;
+                // no keys: zeros and lse = -inf (a request of a single empty chunk); an item
+                // without query rows writes nothing
+                const int nrows = it.nch == 1 ? it.qo * G : 0;
+                for (int k = r; k < nrows * (D / 8); k += 128) {
+                    const int n = k / (D / 8), c = k % (D / 8);
+                    const size_t row = (size_t)(it.q0 + n / G) * Hq + it.g * G + n % G;
+                    reinterpret_cast<uint4*>(out + row * D)[c] = make_uint4(0, 0, 0, 0);
+                    if (c == 0 && p.lse) p.lse[row] = -INFINITY;
                 }
                 continue;
             }
@@ -659,99 +785,139 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
             if (!ok) break;
             const float c_eff = p.scale_log2 * exp2i(-qe[x]);  // score units: log2, all scales
             const unsigned long long km = kmask[x];
+            // the converter may now write the next item of this Q buffer: without this
+            // arrival it could complete Q_FULL / MASK_FULL twice before a slow softmax waits
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(Q_EMPTY + x));
+            const uint32_t s_base = tmem_base + lane_base + 128u * x;
             tc_fence_after();
-            float sv[MAX_TILES][G];
+            // bit n set: key r of tile t counts for column n (inside the chunk, its unit
+            // loaded, and, causal with several query rows, row n / G >= key - (kv - qo))
+            auto vis_mask = [&](int t) -> uint32_t {
+                const int key = it.tok0 + t * TK + r;
+                if (!(key < it.tok1 && ((km >> (8 * t + (r >> 4))) & 1ull))) return 0u;
+                if (!p.causal) return 0xFFFFu;
+                const int dk = key - (it.kv - it.qo);
+                if (dk <= 0) return 0xFFFFu;
+                return dk * G >= 16 ? 0u : (0xFFFFu << (dk * G)) & 0xFFFFu;
+            };
+            float mx[NR];
+            float sv[NR == G ? MAX_TILES : 1][NR];  // the item's scores (NR == G only)
+            if constexpr (NR == G) {
+                // one query row (qo == 1): every score of the item in registers
 #pragma unroll
-            for (int t = 0; t < MAX_TILES; ++t) {
-                // key r of tile t counts if it is inside the chunk and its unit was loaded
-                const bool valid = t < it.ntiles && it.tok0 + t * TK + r < it.tok1 &&
-                                   ((km >> (8 * t + (r >> 4))) & 1ull);
-                if (t < it.ntiles) {
-                    uint32_t u[8];
-                    tmem_ld8(tmem_base + lane_base + 128u * x + 16u * t, u);
-                    tmem_wait_ld8(u);
+                for (int t = 0; t < MAX_TILES; ++t) {
+                    const bool valid = t < it.ntiles && vis_mask(t) != 0u;
+                    if (t < it.ntiles) {
+                        uint32_t u[8];
+                        tmem_ld8(s_base + 16u * t, u);
+                        tmem_wait_ld8(u);
 #pragma unroll
-                    for (int h = 0; h < G; ++h)
-                        sv[t][h] = valid ? __uint_as_float(u[h]) * c_eff : -INFINITY;
-                } else {
+                        for (int n = 0; n < NR; ++n)
+                            sv[t][n] = valid ? __uint_as_float(u[n]) * c_eff : -INFINITY;
+                    } else {
 #pragma unroll
-                    for (int h = 0; h < G; ++h) sv[t][h] = -INFINITY;
+                        for (int n = 0; n < NR; ++n) sv[t][n] = -INFINITY;
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(BAR(S_EMPTY + x));
+#pragma unroll
+                for (int n = 0; n < NR; ++n) {
+                    float m = sv[0][n];
+#pragma unroll
+                    for (int t = 1; t < MAX_TILES; ++t) m = fmaxf(m, sv[t][n]);
+                    mx[n] = m;
+                }
+            } else {
+                // 16 columns: a first pass over the tiles (two per load) for the max
+#pragma unroll
+                for (int n = 0; n < NR; ++n) mx[n] = -INFINITY;
+                for (int t = 0; t < it.ntiles; t += 2) {
+                    uint32_t u[32];
+                    tmem_ld32(s_base + 16u * t, u);
+                    tmem_wait_ld32(u);
+                    const uint32_t v0 = vis_mask(t), v1 = vis_mask(t + 1);
+#pragma unroll
+                    for (int n = 0; n < NR; ++n) {
+                        const float a = ((v0 >> n) & 1u) ? __uint_as_float(u[n]) * c_eff : -INFINITY;
+                        const float b =
+                            ((v1 >> n) & 1u) ? __uint_as_float(u[16 + n]) * c_eff : -INFINITY;
+                        mx[n] = fmaxf(mx[n], fmaxf(a, b));
+                    }
                 }
             }
-            tc_fence_before();
-            mbar_arrive(BAR(S_EMPTY + x));
-            // exact max per head over the item's keys
-            float mx[G];
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                float m = sv[0][h];
-#pragma unroll
-                for (int t = 1; t < MAX_TILES; ++t) m = fmaxf(m, sv[t][h]);
-#pragma unroll
-                for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-                mx[h] = m;
-            }
-            const float* rt;  // [warp][head]
-            ok = wg_exchange<G>(xch, mx, w4, lane, abort_flag, p.status, rt);
+            // exact max per column over the item's keys
+            tr_reduce<NR, true>(mx, lane);
+            const float* rt;  // [warp][column]
+            ok = wg_exchange_cols<NR, XW>(xch, mx[0], w4, lane, abort_flag, p.status, rt);
             if (!ok) break;
-            float neg[G], l[G];
+            float neg[NR];
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const float m = fmaxf(fmaxf(rt[h], rt[8 + h]), fmaxf(rt[16 + h], rt[24 + h]));
-                mx[h] = m;
-                neg[h] = m == -INFINITY ? 0.f : -m;
-                l[h] = 0.f;
+            for (int n = 0; n < NR; ++n) {
+                const float m = fmaxf(fmaxf(rt[n], rt[XW + n]), fmaxf(rt[2 * XW + n], rt[3 * XW + n]));
+                neg[n] = m == -INFINITY ? 0.f : -m;
             }
+            const float m_c =
+                fmaxf(fmaxf(rt[cl], rt[XW + cl]), fmaxf(rt[2 * XW + cl], rt[3 * XW + cl]));
             // (B) the previous item's epilogue
             if (prev.ntiles > 0) {
                 epilogue(prev, s - 1, prev_m, prev_l);
                 if (!ok) break;
             }
             // (C) P^T tiles, f16, into the ring of NPB buffers the P.V MMAs read
+            float l[NR];
+#pragma unroll
+            for (int n = 0; n < NR; ++n) l[n] = 0.f;
             for (int t = 0; t < it.ntiles; ++t, ++pt) {
                 const uint32_t pb = pt % NPB;
+                float pv[NR];
+                if constexpr (NR == G) {
+#pragma unroll
+                    for (int tt = 0; tt < MAX_TILES; ++tt) {
+                        if (tt == t) {
+#pragma unroll
+                            for (int n = 0; n < NR; ++n) pv[n] = ex2_approx(sv[tt][n] + neg[n]);
+                        }
+                    }
+                } else {
+                    uint32_t u[16];
+                    tmem_ld16(s_base + 16u * t, u);
+                    tmem_wait_ld16(u);
+                    const uint32_t vm = vis_mask(t);
+#pragma unroll
+                    for (int n = 0; n < NR; ++n)
+                        pv[n] = ex2_approx(
+                            (((vm >> n) & 1u) ? __uint_as_float(u[n]) * c_eff : -INFINITY) + neg[n]);
+                }
+#pragma unroll
+                for (int n = 0; n < NR; ++n) l[n] += pv[n];
                 ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(P_EMPTY + pb),
                                                                ((pt / NPB) & 1) ^ 1, abort_flag,
                                                                p.status));
                 if (!ok) break;
-                uint8_t* pp = smem + OFF_P + pb * QP_BYTES;
-#pragma unroll
-                for (int tt = 0; tt < MAX_TILES; ++tt) {
-                    if (tt == t) {
-#pragma unroll
-                        for (int h = 0; h < G; ++h) {
-                            const float pv = ex2_approx(sv[tt][h] + neg[h]);
-                            l[h] += pv;
-                            *reinterpret_cast<__half*>(pp + sw128_off(h, r, QP_CHUNK)) =
-                                __float2half_rn(pv);
-                        }
-                    }
-                }
+                store_p(smem + OFF_P + pb * QP_BYTES, pv);
                 fence_async_smem();
                 mbar_arrive(BAR(P_FULL + pb));
             }
             if (!ok) break;
-            // l over the item's keys: a warp sum, then the four warps (read out at once: the
-            // exchange area is reused two exchanges later)
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-#pragma unroll
-                for (int off = 16; off >= 1; off >>= 1) l[h] += __shfl_xor_sync(0xffffffffu, l[h], off);
+            if constexpr (NR != G) {  // the second pass has read the item's scores
+                tc_fence_before();
+                mbar_arrive(BAR(S_EMPTY + x));
             }
+            // column sums over the item's keys: the warp, then the four warps (read out at
+            // once: the exchange area is reused two exchanges later)
+            tr_reduce<NR, false>(l, lane);
             const float* rl;
-            ok = wg_exchange<G>(xch, l, w4, lane, abort_flag, p.status, rl);
+            ok = wg_exchange_cols<NR, XW>(xch, l[0], w4, lane, abort_flag, p.status, rl);
             if (!ok) break;
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                prev_l[h] = (rl[h] + rl[8 + h]) + (rl[16 + h] + rl[24 + h]);
-                prev_m[h] = mx[h];
-            }
+            prev_l = (rl[cl] + rl[XW + cl]) + (rl[2 * XW + cl] + rl[3 * XW + cl]);
+            prev_m = m_c;
             prev = it;
             ++s;
         }
         if (ok && prev.ntiles > 0) epilogue(prev, s - 1, prev_m, prev_l);
     }
-
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -761,19 +927,27 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
     }
 }
 
-template <int G>
+template <int G, int NR>
 static cudaError_t launch_g(const Params& p, int num_sms, cudaStream_t stream) {
     static std::atomic<bool> configured[64];  // per device, set once (repeats are harmless)
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !configured[dev].load(std::memory_order_acquire)) {
         const cudaError_t e = cudaFuncSetAttribute(
-            decode_mma_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+            decode_mma_kernel<G, NR>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess) return e;
         configured[dev].store(true, std::memory_order_release);
     }
-    decode_mma_kernel<G><<<num_sms, THREADS, SMEM_BYTES, stream>>>(p);
+    decode_mma_kernel<G, NR><<<num_sms, THREADS, SMEM_BYTES, stream>>>(p);
     return cudaGetLastError();
+}
+
+// one query row per request: G columns; several: all 16 (p.max_qo * G <= 16)
+template <int G>
+static cudaError_t launch_rows(const Params& p, int num_sms, cudaStream_t stream) {
+    if (p.max_qo <= 1) return launch_g<G, G>(p, num_sms, stream);
+    if (p.max_qo * G > NH) return cudaErrorInvalidValue;
+    return launch_g<G, NH>(p, num_sms, stream);
 }
 
 }  // namespace mmad
@@ -783,10 +957,10 @@ static cudaError_t launch_g(const Params& p, int num_sms, cudaStream_t stream) {
 // p.v_scale the value scale).
 cudaError_t launch_decode_mma(const Params& p, int group, int num_sms, cudaStream_t stream) {
     switch (group) {
-        case 1: return mmad::launch_g<1>(p, num_sms, stream);
-        case 2: return mmad::launch_g<2>(p, num_sms, stream);
-        case 4: return mmad::launch_g<4>(p, num_sms, stream);
-        case 8: return mmad::launch_g<8>(p, num_sms, stream);
+        case 1: return mmad::launch_rows<1>(p, num_sms, stream);
+        case 2: return mmad::launch_rows<2>(p, num_sms, stream);
+        case 4: return mmad::launch_rows<4>(p, num_sms, stream);
+        case 8: return mmad::launch_rows<8>(p, num_sms, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -197,6 +197,13 @@ struct Params {
     int num_kv_heads;
     float scale_log2;           // sm_scale * log2(e) (* k_scale for E4M3 K/V)
     float v_scale;              // output scale: 1 for bf16 K/V, v_scale for E4M3
+    // query rows: request b owns rows q_off[b] .. q_off[b] + q_len[b] - 1 (sanitised by the
+    // plan); q_off == nullptr: one row per request, row b (decode).  Partial results leave
+    // room for max_qo rows per chunk: slot (chunk * max_qo + i) * Hq + head.
+    const int* q_off;
+    const int* q_len;
+    int max_qo;
+    int causal;
     long long chunk_capacity;
     int chunk;                  // keys per split-KV chunk (chunk_keys)
 };
@@ -209,6 +216,12 @@ struct PlanParams {
     int batch;
     int max_kv;                 // page_table_stride * page_size
     int chunk;                  // keys per split-KV chunk
+    // several query rows per request (nullptr: one row per request): q_indptr [batch + 1]
+    // is checked (non-decreasing, at most max_qo rows per request) into q_off / q_len
+    const int* q_indptr;
+    int* q_off;
+    int* q_len;
+    int max_qo;
 };
 }  // namespace decode
 

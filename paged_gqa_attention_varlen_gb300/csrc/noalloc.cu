@@ -151,6 +151,10 @@ extern "C" int pgqa_paged_decode_bf16_noalloc(
     pp.batch = batch;
     pp.max_kv = page_table_stride * page_size;
     pp.chunk = chunk;
+    pp.q_indptr = nullptr;  // one query row per request
+    pp.q_off = nullptr;
+    pp.q_len = nullptr;
+    pp.max_qo = 1;
     if (decode::launch_plan(pp, st) != cudaSuccess) return PGQA_ERR_CUDA;
 
     decode::Params p;
@@ -173,6 +177,10 @@ extern "C" int pgqa_paged_decode_bf16_noalloc(
     p.num_kv_heads = num_kv_heads;
     p.scale_log2 = sm_scale * 1.4426950408889634f;
     p.v_scale = 1.f;
+    p.q_off = nullptr;
+    p.q_len = nullptr;
+    p.max_qo = 1;
+    p.causal = 1;
     p.chunk_capacity = chunks;
     p.chunk = chunk;
     if (decode::prepare_page_maps(p, k_pages, v_pages, num_pages, num_kv_heads, page_size,

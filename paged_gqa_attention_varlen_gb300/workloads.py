@@ -172,6 +172,24 @@ def paged_case_e4m3(kv_lens, num_qo_heads, num_kv_heads, head_dim, page_size=16,
     return pc
 
 
+def multi_token_case(pc, qo_len, k_pages=None, v_pages=None, seed=0, k_scale=1.0,
+                     v_scale=1.0, name=None):
+    """pc's paged cache (or the given pools, e.g. an E4M3 copy) with qo_len query rows per
+    request: the last qo_len positions of each request's keys, as in multi-token decode.
+    Q is drawn from `seed`; the page table and kv lengths are pc's."""
+    device = pc.q.device
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    qo = [int(qo_len)] * pc.batch
+    q = _randn_bf16((qo_len * pc.batch, pc.num_qo_heads, pc.head_dim), gen, device)
+    return PagedCase(name or f"{pc.name}_x{qo_len}", q, _indptr(qo, device),
+                     pc.k_pages if k_pages is None else k_pages,
+                     pc.v_pages if v_pages is None else v_pages, pc.page_table, pc.kv_lens_t,
+                     list(pc.kv_lens), qo, pc.page_size, pc.num_qo_heads, pc.num_kv_heads,
+                     pc.head_dim, True, pc.sm_scale,
+                     dict(pc.meta, k_scale=float(k_scale), v_scale=float(v_scale)))
+
+
 def _lens(gen, n, lo, hi):
     return [int(x) for x in torch.randint(lo, hi + 1, (n,), generator=gen)]
 

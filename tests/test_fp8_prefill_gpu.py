@@ -1,0 +1,151 @@
+"""GPU parity of the paged prefill with few query rows per request (multi-token decode)
+over an FP8 E4M3 KV cache (pgqa_paged_prefill_e4m3) against the float64 oracle's E4M3
+path.  Ragged queries over a paged cache with bottom-right causal masking are FlashInfer
+documentation, flashinfer.prefill (BatchPrefillWithPagedKVCacheWrapper); the E4M3 cache
+is flashinfer_benchmark.py "Attention Flags" (--kv_dtype fp8_e4m3)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_gqa_attention_varlen_gb300 import api as _api
+from paged_gqa_attention_varlen_gb300 import workloads as W
+from gpu_util import check_rows
+
+pytestmark = pytest.mark.gpu
+
+PGQA_ERR_UNSUPPORTED = -2
+PGQA_ERR_DEVICE_BOUNDS = -6
+
+
+def run(api, pc, max_qo, causal=True, **kw):
+    o, lse = api.paged_prefill(pc.q, pc.k_pages, pc.v_pages, pc.q_indptr, pc.page_table,
+                               pc.kv_lens_t, causal=causal, sm_scale=pc.sm_scale,
+                               k_scale=pc.meta["k_scale"], v_scale=pc.meta["v_scale"],
+                               max_qo_len=max_qo, **kw)
+    torch.cuda.synchronize()
+    return o, lse
+
+
+def oracle_e4m3(pc, causal=True, rows=None):
+    return oracle.paged_attention_e4m3(pc.q, pc.q_indptr, pc.k_pages, pc.v_pages,
+                                       pc.meta["k_scale"], pc.meta["v_scale"], pc.page_table,
+                                       pc.kv_lens_t, pc.num_qo_heads, pc.num_kv_heads, causal,
+                                       pc.sm_scale, rows=rows)
+
+
+def mixed_lens(G, n=10, seed=0):
+    """kv lengths over several chunks and a ragged page tail, query rows 0 .. 16 / G with a
+    few requests holding fewer keys than query rows."""
+    rng = np.random.default_rng(seed)
+    qmax = 16 // G
+    kv = [0, 1, 5, 16, 100, 1023, 1025, 3000, 4097, 2] + [int(x) for x in
+                                                          rng.integers(1, 2500, n - 10)]
+    qo = [int(x) for x in rng.integers(1, qmax + 1, len(kv))]
+    qo[0] = qmax            # rows with no key at all
+    qo[1] = qmax            # one key, seen by the last row only (causal)
+    qo[9] = qmax            # two keys: the first rows see none (causal, qmax > 2)
+    qo[3] = 0               # a request without query rows
+    return kv, qo
+
+
+@pytest.mark.parametrize("G,ps,causal", [(1, 16, True), (2, 64, True), (4, 16, True),
+                                         (8, 32, True), (4, 128, False), (1, 32, False)])
+def test_e4m3_prefill_against_oracle(cuda_lib, G, ps, causal):
+    hk = 8 // G if G < 8 else 2
+    kv, qo = mixed_lens(G, 12, seed=G + ps)
+    pc = W.paged_case_e4m3(kv, G * hk, hk, 128, page_size=ps, qo_lens=qo, seed=301 + G + ps,
+                           device="cuda", k_scale=0.5, v_scale=2.0)
+    o, lse = run(cuda_lib, pc, 16 // G, causal)
+    assert cuda_lib.device_status() == 0
+    ro, rl = oracle_e4m3(pc, causal)
+    check_rows(o.reshape(-1, 128).float().cpu(), lse.reshape(-1).cpu(), ro, rl,
+               f"e4m3 prefill G={G} ps={ps} causal={causal}")
+
+
+@pytest.mark.parametrize("G,max_qo", [(4, 1), (4, 4), (8, 2), (1, 16)])
+def test_one_row_per_request_equals_e4m3_decode_bitwise(cuda_lib, G, max_qo):
+    """One query row per request: the decode's result bit for bit, whether the call is
+    declared with one row per request or with room for more."""
+    hk = 8 // G if G < 8 else 2
+    pc = W.paged_case_e4m3([0, 1, 17, 1024, 3000, 4097, 60], G * hk, hk, 128, page_size=16,
+                           seed=311 + G, device="cuda")
+    od, ld = cuda_lib.paged_decode(pc.q, pc.k_pages, pc.v_pages, pc.page_table, pc.kv_lens_t,
+                                   sm_scale=pc.sm_scale, k_scale=pc.meta["k_scale"],
+                                   v_scale=pc.meta["v_scale"])
+    o, lse = run(cuda_lib, pc, max_qo)
+    assert cuda_lib.device_status() == 0
+    assert torch.equal(o, od) and torch.equal(lse, ld)
+
+
+def test_e4m3_prefill_hnd_and_float8_dtype_match_packed_bitwise(cuda_lib):
+    pc = W.paged_case_e4m3([700, 5, 2100, 33], 32, 8, 128, page_size=32, qo_lens=[4, 3, 1, 4],
+                           seed=321, device="cuda")
+    o, lse = run(cuda_lib, pc, 4)
+    kw = dict(causal=True, sm_scale=pc.sm_scale, k_scale=pc.meta["k_scale"],
+              v_scale=pc.meta["v_scale"], max_qo_len=4)
+    o2, l2 = cuda_lib.paged_prefill(pc.q, pc.k_pages.view(torch.float8_e4m3fn),
+                                    pc.v_pages.view(torch.float8_e4m3fn), pc.q_indptr,
+                                    pc.page_table, pc.kv_lens_t, **kw)
+    kh = pc.k_pages.permute(0, 2, 1, 3).contiguous()
+    vh = pc.v_pages.permute(0, 2, 1, 3).contiguous()
+    o3, l3 = cuda_lib.paged_prefill(pc.q, kh, vh, pc.q_indptr, pc.page_table, pc.kv_lens_t,
+                                    kv_layout="HND", **kw)
+    torch.cuda.synchronize()
+    assert cuda_lib.device_status() == 0
+    for a, b in ((o2, l2), (o3, l3)):
+        assert torch.equal(a, o) and torch.equal(b, lse)
+
+
+def test_multi_token_workload_sampled_rows(cuda_lib):
+    """The 256-request decode workload's cache as FP8 E4M3 (scales 1) with 4 query rows per
+    request, the last 4 positions of each request's keys (the multi-token decode the
+    benchmark times): every request's first and last rows of two heads, and random rows,
+    against the oracle."""
+    pc = W.config("decode", device="cuda")
+    k8 = pc.k_pages.to(torch.float8_e4m3fn).view(torch.uint8)
+    v8 = pc.v_pages.to(torch.float8_e4m3fn).view(torch.uint8)
+    mt = W.multi_token_case(pc, 4, k8, v8, seed=331)
+    o, lse = run(cuda_lib, mt, 4)
+    assert cuda_lib.device_status() == 0
+    rng = np.random.default_rng(333)
+    hq = mt.num_qo_heads
+    rows = set()
+    for b in range(mt.batch):
+        for t in (4 * b, 4 * b + 3):
+            rows.update({t * hq, t * hq + int(rng.integers(0, hq))})
+    rows.update(rng.integers(0, 4 * mt.batch * hq, 512).tolist())
+    rows = np.array(sorted(rows), dtype=np.int64)
+    ro, rl = oracle_e4m3(mt, True, rows=rows)
+    idx = torch.as_tensor(rows, device="cuda")
+    check_rows(o.reshape(-1, 128).index_select(0, idx).float().cpu(),
+               lse.reshape(-1).index_select(0, idx).cpu(), ro, rl, "multi-token workload")
+
+
+def test_rows_beyond_the_declared_maximum_are_refused(cuda_lib):
+    """A request with more query rows than max_qo_len: PGQA_ERR_DEVICE_BOUNDS and none of its
+    rows written; the other requests are computed."""
+    pc = W.paged_case_e4m3([300, 500, 40], 32, 8, 128, page_size=16, qo_lens=[2, 5, 3],
+                           seed=341, device="cuda")
+    o = torch.full_like(pc.q, 7.0)
+    lse = torch.full(pc.q.shape[:2], 9.0, dtype=torch.float32, device="cuda")
+    run(cuda_lib, pc, 4, out=o, lse=lse)
+    assert cuda_lib.device_status() == PGQA_ERR_DEVICE_BOUNDS
+    assert cuda_lib.device_status() == 0
+    assert bool((o[2:7] == 7.0).all()) and bool((lse[2:7] == 9.0).all())
+    keep = np.array([t * 32 + h for t in (0, 1, 7, 8, 9) for h in range(32)], dtype=np.int64)
+    ro, rl = oracle_e4m3(pc, True, rows=keep)
+    idx = torch.as_tensor(keep, device="cuda")
+    check_rows(o.reshape(-1, 128).index_select(0, idx).float().cpu(),
+               lse.reshape(-1).index_select(0, idx).cpu(), ro, rl, "other requests")
+
+
+def test_too_many_rows_for_one_tile_is_unsupported(cuda_lib):
+    pc = W.paged_case_e4m3([100, 200], 32, 8, 128, page_size=16, qo_lens=[5, 2], seed=351,
+                           device="cuda")
+    with pytest.raises(_api.PgqaError) as e:
+        run(cuda_lib, pc, 5)  # 5 rows x 4 heads > 16 columns
+    assert e.value.code == PGQA_ERR_UNSUPPORTED
+    with pytest.raises(ValueError):
+        cuda_lib.paged_prefill(pc.q, pc.k_pages, pc.v_pages, pc.q_indptr, pc.page_table,
+                               pc.kv_lens_t)  # E4M3 pools without max_qo_len
