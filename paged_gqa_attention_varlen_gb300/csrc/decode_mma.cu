@@ -18,12 +18,12 @@
 // half of HBM speed.  Here the dot products run on tcgen05.mma and the CUDA cores only
 // convert bytes, which leaves HBM as the bound.
 //
-// Design (one persistent CTA per SM, 448 threads; work item = one (chunk, kv head) of up
+// Design (one persistent CTA per SM, 512 threads; work item = one (chunk, kv head) of up
 // to 8 tiles of 128 keys; the items of a CTA run as a software pipeline in which step s
 // handles the K tiles of item s and the V tiles of item s - 1):
-//  * warps 0 and 14, producers: stream 128-key tiles of raw E4M3 bytes in step order (K
-//    tiles of item s, then V tiles of item s - 1) through a 5-stage TMA ring, taking
-//    alternate tiles; lane u < 8 loads the 16-key unit u of a tile (a 16-token page, or a
+//  * warps 0, 14 and 15, producers: stream 128-key tiles of raw E4M3 bytes in step order
+//    (K tiles of item s, then V tiles of item s - 1) through a 6-stage TMA ring, each
+//    taking every third tile; lane u < 8 loads the 16-key unit u of a tile (a 16-token page, or a
 //    slice of a larger page) as one 2 KB box, 128-byte swizzled.  Page ids are read one
 //    item ahead.
 //  * warps 2-9, two converter warpgroups, both on every raw tile: E4M3 -> f16 is exact.
@@ -61,17 +61,17 @@ constexpr int D = HEAD_DIM;                 // 128
 constexpr int TK = 128;                     // keys per tile = the MMA's M
 constexpr int NH = 16;                      // query heads per kv head, padded = the MMA's N
 constexpr int UNITS = TK / PAGE;            // 16-key units per tile (8)
-constexpr int RAW_STAGES = 5;
+constexpr int RAW_STAGES = 6;
 constexpr int NKB = 3;                      // K tiles in tensor memory
 constexpr int NVB = 3;                      // converted V tiles in shared memory
-constexpr int NPB = 8;                      // P^T tiles in shared memory (a whole item)
+constexpr int NPB = 4;                      // P^T tiles in shared memory
 constexpr int MAX_TILES = 8;                // tiles per item (chunks of at most 1024 keys)
 constexpr int RAW_BYTES = TK * D;           // 16 KB of E4M3 per K or V tile
 constexpr int CVT_BYTES = TK * D * 2;       // 32 KB of f16
 constexpr int CVT_CHUNK = TK * 128;         // one 64-column chunk of a converted tile
 constexpr int QP_BYTES = NH * D * 2;        // 4 KB: Q (16 x 128 dims) or P^T (128 keys x 16)
 constexpr int QP_CHUNK = NH * 128;          // one 64-column chunk of Q
-constexpr int PRODUCERS = 2;                // TMA producer warps (0 and 14)
+constexpr int PRODUCERS = 3;                // TMA producer warps (0, 14 and 15)
 constexpr int THREADS = 448 + 32 * (PRODUCERS - 1);
 constexpr int CVT_THREADS = 256;            // two converter warpgroups share every tile
 // tensor memory: S^T regions of two items (8 tiles x 16 columns each) at 0 and 128, O^T at
@@ -117,24 +117,53 @@ __device__ __forceinline__ uint32_t sw128_off(int row, int col, int chunk_bytes)
 struct Item {
     int b, g, f, nch, tok0, tok1, ntiles, kv, q0, qo;
 };
-__device__ __forceinline__ Item item_of(const Params& p, long long item) {
+// A role's position in the request list: request b, whose first chunk is c0.  Every role
+// visits its items in increasing order, so the request of the next item is found by
+// walking forward from here.
+struct Cursor {
+    int b = 0, c0 = 0;
+};
+__device__ __forceinline__ Item item_of(const Params& p, long long item, Cursor& cur) {
     Item it;
     const int Hk = p.num_kv_heads;
     it.f = (int)(item / Hk);
     it.g = (int)(item % Hk);
-    int lo = 0, hi = p.batch - 1;  // the request whose chunks contain f
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (__ldg(p.chunk_off + mid) <= it.f) lo = mid;
-        else hi = mid - 1;
+    // the request whose chunks contain f: the next four chunk offsets are loaded at once
+    // (one round trip, where a binary search over the batch takes one per step); only a
+    // longer jump falls back to the search.  Every request has at least one chunk.
+    int b = cur.b, c0 = cur.c0;
+    int nb[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        nb[k] = b + 1 + k < p.batch ? __ldg(p.chunk_off + b + 1 + k) : INT_MAX;
+    int adv = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) adv += nb[k] <= it.f ? 1 : 0;
+    int c1;
+    if (adv < 4) {
+        if (adv > 0) c0 = nb[adv - 1];
+        b += adv;
+        c1 = nb[adv];
+    } else {
+        int lo = b + 4, hi = p.batch - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (__ldg(p.chunk_off + mid) <= it.f) lo = mid;
+            else hi = mid - 1;
+        }
+        b = lo;
+        c0 = __ldg(p.chunk_off + b);
+        c1 = __ldg(p.chunk_off + b + 1);
     }
-    it.b = lo;
-    const int c0 = __ldg(p.chunk_off + lo);
-    it.nch = __ldg(p.chunk_off + lo + 1) - c0;
-    const int kv = __ldg(p.kv_eff + lo);
+    if (b + 1 >= p.batch) c1 = __ldg(p.chunk_off + p.batch);
+    cur.b = b;
+    cur.c0 = c0;
+    it.b = b;
+    it.nch = c1 - c0;
+    const int kv = __ldg(p.kv_eff + b);
     it.kv = kv;
-    it.q0 = p.q_off != nullptr ? __ldg(p.q_off + lo) : lo;
-    it.qo = p.q_off != nullptr ? __ldg(p.q_len + lo) : 1;
+    it.q0 = p.q_off != nullptr ? __ldg(p.q_off + b) : b;
+    it.qo = p.q_off != nullptr ? __ldg(p.q_len + b) : 1;
     it.tok0 = (it.f - c0) * p.chunk;
     it.tok1 = min(kv, it.tok0 + p.chunk);
     it.ntiles = it.tok1 > it.tok0 && it.qo > 0 ? (it.tok1 - it.tok0 + TK - 1) / TK : 0;
@@ -393,30 +422,29 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
                                 key % p.page_size, it.g, pid);
             }
         };
-        auto next_item = [&](long long from) -> long long {
-            for (long long k = from; k < n_items; k += stride)
-                if (item_of(p, k).ntiles > 0) return k;
+        Cursor pos;
+        auto next_item = [&](long long from, Item& out) -> long long {
+            for (long long k = from; k < n_items; k += stride) {
+                out = item_of(p, k, pos);
+                if (out.ntiles > 0) return k;
+            }
             return -1;
         };
-        long long cur = next_item(blockIdx.x);
         Item prev, it;
         prev.ntiles = 0;
         it.ntiles = 0;
         int ids_prev[2] = {-1, -1}, ids[2] = {-1, -1};
-        if (cur >= 0) {
-            it = item_of(p, cur);
-            read_ids(it, ids);
-        }
+        long long cur = next_item(blockIdx.x, it);
+        if (cur >= 0) read_ids(it, ids);
         while (ok && cur >= 0) {
-            const long long nxt = next_item(cur + stride);
+            load_tiles(it, ids, false);
+            // read ahead while these K tiles are in flight: the next item's geometry and
+            // page ids, used by the next step
             Item ni;
             ni.ntiles = 0;
             int ids_next[2] = {-1, -1};
-            if (nxt >= 0) {  // read ahead: used by the next step
-                ni = item_of(p, nxt);
-                read_ids(ni, ids_next);
-            }
-            load_tiles(it, ids, false);
+            const long long nxt = ok ? next_item(cur + stride, ni) : -1;
+            if (nxt >= 0) read_ids(ni, ids_next);
             if (ok && prev.ntiles > 0) load_tiles(prev, ids_prev, true);
             prev = it;
             ids_prev[0] = ids[0];
@@ -490,8 +518,9 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
             };
             Item prev;
             prev.ntiles = 0;
+            Cursor pos;
             for (long long item = blockIdx.x; ok && item < n_items; item += stride) {
-                const Item it = item_of(p, item);
+                const Item it = item_of(p, item, pos);
                 if (it.ntiles == 0) continue;
                 qk_tiles(it);
                 if (ok && prev.ntiles > 0) pv_tiles(prev, s - 1);
@@ -634,28 +663,35 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
                 mbar_arrive(BAR(RAW_EMPTY + st));
             }
         };
-        auto next_item = [&](long long from) -> long long {
-            for (long long k = from; k < n_items; k += stride)
-                if (item_of(p, k).ntiles > 0) return k;
+        Cursor pos;
+        auto next_item = [&](long long from, Item& out) -> long long {
+            for (long long k = from; k < n_items; k += stride) {
+                out = item_of(p, k, pos);
+                if (out.ntiles > 0) return k;
+            }
             return -1;
         };
-        long long cur = next_item(blockIdx.x);
+        Item it;
+        it.ntiles = 0;
+        long long cur = next_item(blockIdx.x, it);
         float qv[NR];
 #pragma unroll
         for (int n = 0; n < NR; ++n) qv[n] = 0.f;
-        if (cur >= 0 && cid == 0) load_q<G, NR>(p, item_of(p, cur), i, qv);
+        if (cur >= 0 && cid == 0) load_q<G, NR>(p, it, i, qv);
         Item prev;
         prev.ntiles = 0;
         while (ok && cur >= 0) {
-            const Item it = item_of(p, cur);
-            const long long nxt = next_item(cur + stride);
+            Item ni;
+            ni.ntiles = 0;
+            const long long nxt = next_item(cur + stride, ni);
             float qn[NR];  // the next item's query rows, loaded while this one converts
 #pragma unroll
             for (int n = 0; n < NR; ++n) qn[n] = 0.f;
-            if (nxt >= 0 && cid == 0) load_q<G, NR>(p, item_of(p, nxt), i, qn);
+            if (nxt >= 0 && cid == 0) load_q<G, NR>(p, ni, i, qn);
             k_tiles(it, qv);
             if (ok && prev.ntiles > 0) v_tiles(prev);
             prev = it;
+            it = ni;
             ++s;
             cur = nxt;
 #pragma unroll
@@ -758,8 +794,9 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
                 }
             }
         };
+        Cursor pos;
         for (long long item = blockIdx.x; ok && item < n_items; item += stride) {
-            const Item it = item_of(p, item);
+            const Item it = item_of(p, item, pos);
             if (it.ntiles == 0) {
                 // no keys: zeros and lse = -inf (a request of a single empty chunk); an item
                 // without query rows writes nothing
