@@ -586,6 +586,21 @@ def bench_extra(api, W, dev, stream, dc, peaks):
                                                   stream=stream), stream)
         out[f"paged_prefill_{name}"] = tensor_line(flops, ms, f"{name} shape, keys in 16-token "
                                                    "pages (random page order)")
+        if name == "prefill_hd128":
+            # the same pages as an FP8 E4M3 cache: converted to bf16 in the workspace, then
+            # the bf16 paged prefill (the conversion is inside the timed call)
+            k8 = pc.k_pages.to(torch.float8_e4m3fn)
+            v8 = pc.v_pages.to(torch.float8_e4m3fn)
+            mq = max(qo)
+            ms = time_calls(lambda: api.paged_prefill(pc.q, k8, v8, pc.q_indptr, pc.page_table,
+                                                      pc.kv_lens_t, causal=True,
+                                                      sm_scale=pc.sm_scale, k_scale=1.0,
+                                                      v_scale=1.0, max_qo_len=mq, out=o,
+                                                      lse=lse, stream=stream), stream)
+            out["paged_prefill_e4m3_prefill_hd128"] = tensor_line(
+                flops, ms, "prefill_hd128 shape over an FP8 E4M3 cache of 16-token pages "
+                "(pages converted to bf16 in the call)")
+            del k8, v8
         if name == "prefix_hd256":
             o2 = torch.empty_like(rc.q)
             l2 = torch.empty(rc.q.shape[:2], dtype=torch.float32, device=dev)

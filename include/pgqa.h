@@ -248,8 +248,7 @@ int pgqa_paged_decode_e4m3(const void* q, const void* k_pages, const void* v_pag
                            int head_dim, float sm_scale, pgqa_stream_t stream);
 
 /*
- * Paged prefill with few query rows per request (multi-token decode, speculative
- * verification) over an FP8 E4M3 KV cache: the computation of pgqa_paged_prefill_bf16 with
+ * Paged prefill over an FP8 E4M3 KV cache: the computation of pgqa_paged_prefill_bf16 with
  * K/V stored as in pgqa_paged_decode_e4m3 (one byte per element, values e4m3 * k_scale and
  * e4m3 * v_scale, strides in elements = bytes, positive multiples of 16).
  *
@@ -259,22 +258,33 @@ int pgqa_paged_decode_e4m3(const void* q, const void* k_pages, const void* v_pag
  * (--kv_dtype fp8_e4m3 for the prefill and decode routines); scale convention as for
  * pgqa_paged_decode_e4m3.
  *
- *   q [total_q, num_qo_heads, 128] bf16 and q_indptr [batch + 1] int32 (device) as for
- *       pgqa_paged_prefill_bf16; every request has at most max_qo_len rows.
+ *   q [total_q, num_qo_heads, head_dim] bf16 and q_indptr [batch + 1] int32 (device) as
+ *       for pgqa_paged_prefill_bf16.
+ *   max_qo_len: the most query rows any request has (q_indptr stays on the device); it
+ *       chooses the path below.
  *   page_table, kv_lens, page_size, num_pages: as for pgqa_paged_prefill_bf16.
- *   o [total_q, num_qo_heads, 128] bf16, lse [total_q, num_qo_heads] fp32 or NULL.
+ *   o [total_q, num_qo_heads, head_dim] bf16, lse [total_q, num_qo_heads] fp32 or NULL.
  *   causal != 0: query row i of a request with qo_len rows and kv_len keys sees key j iff
  *       j <= i + kv_len - qo_len (a row that sees no key gets zeros and lse = -inf).
- * The keys stream once per (request, kv head) for all of its query rows and heads, on the
- * tensor-core E4M3 decode path, with split-KV as for the decode.
  *
- * Supported: head_dim 128; page_size 16, 32, 64 or 128; G = num_qo_heads / num_kv_heads
- * in {1,2,4,8}; max_qo_len * G <= 16, else PGQA_ERR_UNSUPPORTED.  max_qo_len < 1 (with
- * batch > 0), a NULL q_indptr or a NaN / infinite scale is PGQA_ERR_INVALID_ARG; other
- * errors as for pgqa_paged_decode_e4m3.  A request whose q_indptr range is negative or
- * longer than max_qo_len, or whose kv_len is out of range, is reported as
- * PGQA_ERR_DEVICE_BOUNDS by pgqa_get_device_status() and none of its rows is written; a
- * page id outside 0..num_pages-1 is reported the same way and that page is not read.
+ * Two paths, the same results up to rounding:
+ *   - head_dim 128, G in {1,2,4,8} and max_qo_len * G <= 16 (multi-token decode,
+ *     speculative verification): the tensor-core E4M3 decode, each request's query rows
+ *     as the columns of its MMAs, so the keys stream once for all of them; split-KV as for
+ *     the decode.  A request with more than max_qo_len rows is reported as
+ *     PGQA_ERR_DEVICE_BOUNDS and none of its rows is written.
+ *   - otherwise: the pages the call reads are converted to bf16 (exact) into the
+ *     workspace, then the bf16 paged prefill runs over them with k_scale folded into the
+ *     score scale and v_scale into the output scale.  The conversion needs
+ *     2 * P * page_size * num_kv_heads * head_dim * 2 bytes of workspace on top of the
+ *     prefill's own, P = min(num_pages, batch * page_table_stride); a caller workspace
+ *     too small for it gives PGQA_ERR_WORKSPACE.
+ *
+ * Supported: head_dim 128 or 256; page_size 16, 32, 64 or 128; G = num_qo_heads /
+ * num_kv_heads dividing 128.  max_qo_len < 1 (with batch > 0), a NULL q_indptr or a NaN /
+ * infinite scale is PGQA_ERR_INVALID_ARG.  Other errors as for pgqa_paged_prefill_bf16; a
+ * page id outside 0..num_pages-1 is reported as PGQA_ERR_DEVICE_BOUNDS and that page is
+ * not read (the rows that need it are then undefined).
  */
 int pgqa_paged_prefill_e4m3(const void* q, const void* k_pages, const void* v_pages, void* o,
                             float* lse, const int32_t* q_indptr, const int32_t* page_table,

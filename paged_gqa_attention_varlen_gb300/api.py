@@ -204,8 +204,10 @@ def paged_prefill(q, k_pages, v_pages, q_indptr, page_table, kv_lens, causal=Tru
     ("HND"), any strides with d contiguous, bf16 or E4M3 bytes (uint8 / float8_e4m3fn,
     element = e4m3 x k_scale / v_scale); page_table [batch, stride] int32; kv_lens [batch]
     int32 (keys per request, the cached prefix plus the new tokens); all on one CUDA device.
-    E4M3 pools need max_qo_len, the most query rows any request has (q_indptr stays on the
-    device).  Returns (o [total_q, Hq, d] bf16, lse [total_q, Hq] fp32 or None).
+    For E4M3 pools max_qo_len is the most query rows any request has (q_indptr stays on
+    the device; default: total_q, always an upper bound): with max_qo_len * G <= 16 the
+    call takes the tensor-core multi-token path.  Returns (o [total_q, Hq, d] bf16,
+    lse [total_q, Hq] fp32 or None).
     """
     dev = q.device
     _check(q, "q", torch.bfloat16, 3, dev)
@@ -218,7 +220,7 @@ def paged_prefill(q, k_pages, v_pages, q_indptr, page_table, kv_lens, causal=Tru
     e4m3 = k_pages.element_size() == 1
     batch = q_indptr.numel() - 1
     if e4m3 and max_qo_len is None:
-        raise ValueError("an E4M3 paged prefill needs max_qo_len")
+        max_qo_len = max(total_q, 1)
     if dk != d:
         raise ValueError("k_pages / v_pages must have q's head_dim")
     if page_table.shape[0] != batch or kv_lens.numel() != batch:

@@ -19,7 +19,8 @@ INCLUDE = PKG.parent / "include"
 BUILD = PKG / "_build"
 LIB = BUILD / "libpgqa.so"
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["api.cu", "prefill.cu", "decode.cu", "decode_mma.cu", "noalloc.cu", "selftest.cu"]
+SOURCES = ["api.cu", "prefill.cu", "decode.cu", "decode_mma.cu", "dequant.cu", "noalloc.cu",
+           "selftest.cu"]
 
 
 def nvcc() -> str:

@@ -26,6 +26,9 @@ cudaError_t launch_decode_mma(const Params&, int group, int num_sms, cudaStream_
 cudaError_t prepare_page_maps(Params&, const void*, const void*, int, int, int, long long,
                               long long, long long, bool);
 }  // namespace decode
+namespace dequant {
+cudaError_t launch_dequant(const Params&, int num_sms, cudaStream_t);
+}  // namespace dequant
 namespace selftest {
 cudaError_t launch_expired_wait(int* status, cudaStream_t stream);
 }  // namespace selftest
@@ -268,11 +271,13 @@ struct PrefillWs {
     long long part_capacity;
 };
 
-// Carve the workspace: a quarter of the space after the arrays holds the work list
-// (at least what 4096 items need), the rest the partial results.
-PrefillWs prefill_layout(const DeviceState& st, int batch, int head_dim) {
+// Carve the first `usable` bytes of the workspace (all of it by default): a quarter of the
+// space after the arrays holds the work list (at least what 4096 items need), the rest the
+// partial results.
+PrefillWs prefill_layout(const DeviceState& st, int batch, int head_dim, size_t usable = 0) {
     PrefillWs w;
     uint8_t* ws = static_cast<uint8_t*>(st.ws);
+    const size_t ws_bytes = usable != 0 ? usable : st.ws_bytes;
     w.hdr = reinterpret_cast<WsHeader*>(ws + kWsHeader);
     w.tmaps = reinterpret_cast<CUtensorMap*>(ws + kWsTmapOffset);
     const size_t arr = align_up((size_t)(batch + 1) * sizeof(int), 256);
@@ -281,14 +286,14 @@ PrefillWs prefill_layout(const DeviceState& st, int batch, int head_dim) {
     for (int i = 0; i < kPrefillArrays; ++i)
         *arrays[i] = reinterpret_cast<int*>(ws + kWsArrays + i * arr);
     const size_t items_off = kWsArrays + kPrefillArrays * arr;
-    const size_t rest = st.ws_bytes > items_off ? st.ws_bytes - items_off : 0;
+    const size_t rest = ws_bytes > items_off ? ws_bytes - items_off : 0;
     size_t item_bytes = align_up(rest / 4, 256);
     const size_t min_items = 4096 * sizeof(prefill::WorkItem);
     if (item_bytes < min_items) item_bytes = rest < min_items ? rest : min_items;
     w.items = reinterpret_cast<prefill::WorkItem*>(ws + items_off);
     w.item_capacity = (long long)(item_bytes / sizeof(prefill::WorkItem));
     const size_t part_off = items_off + item_bytes;
-    const size_t part_bytes = st.ws_bytes > part_off + 256 ? st.ws_bytes - part_off - 256 : 0;
+    const size_t part_bytes = ws_bytes > part_off + 256 ? ws_bytes - part_off - 256 : 0;
     const long long rows = (long long)(part_bytes / ((size_t)(head_dim + 1) * sizeof(float)));
     w.part_capacity = rows;
     w.part_lse = reinterpret_cast<float*>(ws + part_off);
@@ -348,6 +353,13 @@ int paged_decode_impl(const void* q, const void* k_pages, const void* v_pages,
                       int num_qo_heads, int num_kv_heads, int head_dim, float sm_scale, bool kv8,
                       float k_scale, float v_scale, const int32_t* q_indptr, int max_qo,
                       int causal, pgqa_stream_t stream);
+int paged_prefill_impl(const void* q, const void* k_pages, const void* v_pages, void* o,
+                       float* lse, const int32_t* q_indptr, const int32_t* page_table,
+                       int page_table_stride, const int32_t* kv_lens, int page_size,
+                       int num_pages, int64_t page_stride, int64_t slot_stride,
+                       int64_t head_stride, int batch, int num_qo_heads, int num_kv_heads,
+                       int head_dim, int causal, float sm_scale, bool kv8, float k_scale,
+                       float v_scale, pgqa_stream_t stream);
 }  // namespace
 
 extern "C" {
@@ -537,6 +549,7 @@ int pgqa_ragged_prefill_bf16(const void* q, const void* k, const void* v, void* 
     p.group = group;
     p.causal = causal ? 1 : 0;
     p.scale_log2 = sm_scale * 1.4426950408889634f;
+    p.v_scale = 1.f;
     p.page_table = nullptr;
     p.page_table_stride = 0;
     p.page_size = 0;
@@ -571,122 +584,10 @@ int pgqa_paged_prefill_bf16_strided(const void* q, const void* k_pages, const vo
                                     int64_t page_stride, int64_t slot_stride, int64_t head_stride,
                                     int batch, int num_qo_heads, int num_kv_heads, int head_dim,
                                     int causal, float sm_scale, pgqa_stream_t stream) {
-    if (batch < 0 || num_qo_heads <= 0 || num_kv_heads <= 0 || page_table_stride < 0 ||
-        num_pages < 0)
-        return PGQA_ERR_INVALID_ARG;
-    if (batch > 0 && !kv_strides_ok(page_stride, slot_stride, head_stride))
-        return PGQA_ERR_INVALID_ARG;
-    if (batch == 0) return PGQA_OK;
-    if (!q || !k_pages || !v_pages || !o || !q_indptr || !kv_lens ||
-        (!page_table && page_table_stride > 0))
-        return PGQA_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o) ||
-        (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(q_indptr) & 3u) ||
-        (reinterpret_cast<uintptr_t>(page_table) & 3u) ||
-        (reinterpret_cast<uintptr_t>(kv_lens) & 3u))
-        return PGQA_ERR_INVALID_ARG;
-    if (head_dim != 128 && head_dim != 256) return PGQA_ERR_UNSUPPORTED;
-    if (page_size != 16 && page_size != 32 && page_size != 64 && page_size != 128)
-        return PGQA_ERR_UNSUPPORTED;
-    if (num_qo_heads % num_kv_heads != 0) return PGQA_ERR_UNSUPPORTED;
-    const int group = num_qo_heads / num_kv_heads;
-    if (group > prefill::BM || prefill::BM % group != 0) return PGQA_ERR_UNSUPPORTED;
-    if (!(sm_scale == sm_scale) || sm_scale > 3.0e38f || sm_scale < -3.0e38f)
-        return PGQA_ERR_INVALID_ARG;
-    if ((long long)page_table_stride * page_size > 0x7fffffffLL) return PGQA_ERR_UNSUPPORTED;
-
-    std::lock_guard<std::mutex> lock(g_mutex);
-    int dev;
-    DeviceState* st;
-    int rc = current_device(&dev, &st);
-    if (rc != PGQA_OK) return rc;
-    if ((rc = get_encoder()) != PGQA_OK) return rc;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    rc = ensure_workspace(*st, prefill_ws_bytes(batch, 4096), s);
-    if (rc != PGQA_OK) return rc;
-
-    const PrefillWs lay = prefill_layout(*st, batch, head_dim);
-    WsHeader* hdr = lay.hdr;
-    CUtensorMap* tmaps = lay.tmaps;
-    int* tile_off = lay.tile_off;
-    int* kv_off = lay.kv_off;
-    prefill::WorkItem* items = lay.items;
-    const long long capacity = lay.item_capacity;
-
-    // Q as for the ragged call (row extent patched on the device); K/V as 4-D page pools
-    // {d, slot, head, page}, one box = one page of one head and one 64-column chunk.
-    CUtensorMap tq, tk, tv;
-    const uint32_t tpt = prefill::BM / group;
-    if ((rc = encode_3d(&tq, q, head_dim, num_qo_heads, tpt, (uint64_t)head_dim * 2,
-                        (uint64_t)num_qo_heads * head_dim * 2, 64, group, tpt)) != PGQA_OK)
-        return rc;
-    // head_dim 256 with pages of up to 32 tokens: the grouped stage layout (a 64 KB K/V tile
-    // in 16 boxes of 4 KB rather than 4 * 128 / page_size boxes)
-    const bool grouped = head_dim == 256 && page_size <= 32;
-    int box_keys = 0, page_heads = 0;
-    if (grouped) {
-        if ((rc = encode_pages_grouped(&tk, k_pages, head_dim, page_size, num_kv_heads, num_pages,
-                                       page_stride, slot_stride, head_stride, &box_keys,
-                                       &page_heads)) != PGQA_OK ||
-            (rc = encode_pages_grouped(&tv, v_pages, head_dim, page_size, num_kv_heads, num_pages,
-                                       page_stride, slot_stride, head_stride, &box_keys,
-                                       &page_heads)) != PGQA_OK)
-            return rc;
-    } else {
-        if ((rc = encode_pages_4d(&tk, k_pages, head_dim, page_size, num_kv_heads, num_pages,
-                                  page_stride, slot_stride, head_stride)) != PGQA_OK ||
-            (rc = encode_pages_4d(&tv, v_pages, head_dim, page_size, num_kv_heads, num_pages,
-                                  page_stride, slot_stride, head_stride)) != PGQA_OK)
-            return rc;
-    }
-
-    prefill::PlanParams pp;
-    pp.q_indptr = q_indptr;
-    pp.kv_indptr = nullptr;
-    pp.kv_lens = kv_lens;
-    pp.max_kv = page_table_stride * page_size;
-    pp.kv_off = kv_off;
-    pp.batch = batch;
-    pp.num_kv_heads = num_kv_heads;
-    pp.group = group;
-    pp.causal = causal ? 1 : 0;
-    pp.tiles_per_item = head_dim == 128 ? 2 : 1;
-    pp.hdr = hdr;
-    pp.tile_off = tile_off;
-    pp.items = items;
-    pp.item_capacity = capacity;
-    pp.tm_out = tmaps;
-    cudaError_t e;
-
-    prefill::Params p;
-    p.tm_q = tmaps + 0;
-    p.tm_k = tmaps + 1;
-    p.tm_v = tmaps + 2;
-    p.o = o;
-    p.lse = lse;
-    p.q_indptr = q_indptr;
-    p.kv_indptr = nullptr;
-    p.items = items;
-    p.hdr = hdr;
-    p.status = &hdr->status;
-    p.num_qo_heads = num_qo_heads;
-    p.num_kv_heads = num_kv_heads;
-    p.group = group;
-    p.causal = causal ? 1 : 0;
-    p.scale_log2 = sm_scale * 1.4426950408889634f;
-    p.page_table = page_table;
-    p.page_table_stride = page_table_stride;
-    p.page_size = page_size;
-    p.num_pages = num_pages;
-    p.box_keys = box_keys;
-    p.page_heads = page_heads;
-    fill_split(pp, p, lay, batch, head_dim, num_qo_heads, st->num_sms);
-    e = prefill::launch_plan(pp, tq, tk, tv, s);
-    if (e != cudaSuccess) return PGQA_ERR_CUDA;
-    e = head_dim == 128 ? prefill::launch_attention_pair<true>(p, st->num_sms, s)
-                        : prefill::launch_attention<256, true>(p, st->num_sms, grouped, s);
-    if (e != cudaSuccess) return PGQA_ERR_CUDA;
-    return map_cuda(prefill::launch_merge(p, head_dim, st->num_sms, s));
+    return paged_prefill_impl(q, k_pages, v_pages, o, lse, q_indptr, page_table,
+                              page_table_stride, kv_lens, page_size, num_pages, page_stride,
+                              slot_stride, head_stride, batch, num_qo_heads, num_kv_heads,
+                              head_dim, causal, sm_scale, false, 1.f, 1.f, stream);
 }
 
 int pgqa_paged_decode_bf16(const void* q, const void* k_pages, const void* v_pages,
@@ -739,13 +640,24 @@ int pgqa_paged_prefill_e4m3(const void* q, const void* k_pages, const void* v_pa
     if (!finite_scale(k_scale) || !finite_scale(v_scale)) return PGQA_ERR_INVALID_ARG;
     if (batch > 0 && (max_qo_len < 1 || !q_indptr)) return PGQA_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(q_indptr) & 3u) return PGQA_ERR_INVALID_ARG;
-    if (num_kv_heads > 0 && num_qo_heads % num_kv_heads == 0 && batch > 0 &&
-        (long long)max_qo_len * (num_qo_heads / num_kv_heads) > 16)
-        return PGQA_ERR_UNSUPPORTED;
-    return paged_decode_impl(q, k_pages, v_pages, page_table, kv_lens, page_size,
-                             page_table_stride, num_pages, page_stride, slot_stride, head_stride,
-                             o, lse, batch, num_qo_heads, num_kv_heads, head_dim, sm_scale, true,
-                             k_scale, v_scale, q_indptr, max_qo_len, causal ? 1 : 0, stream);
+    // few query rows per request: the tensor-core E4M3 decode, with every request's rows as
+    // the columns of its MMAs (the keys stream once for all of them)
+    const int group = num_kv_heads > 0 && num_qo_heads % num_kv_heads == 0
+                          ? num_qo_heads / num_kv_heads : 0;
+    const bool few_rows = head_dim == 128 && (group == 1 || group == 2 || group == 4 ||
+                                              group == 8) &&
+                          (long long)max_qo_len * group <= 16;
+    if (few_rows || batch == 0)
+        return paged_decode_impl(q, k_pages, v_pages, page_table, kv_lens, page_size,
+                                 page_table_stride, num_pages, page_stride, slot_stride,
+                                 head_stride, o, lse, batch, num_qo_heads, num_kv_heads, head_dim,
+                                 sm_scale, true, k_scale, v_scale, q_indptr, max_qo_len,
+                                 causal ? 1 : 0, stream);
+    // longer query runs: the bf16 prefill over the converted pages
+    return paged_prefill_impl(q, k_pages, v_pages, o, lse, q_indptr, page_table,
+                              page_table_stride, kv_lens, page_size, num_pages, page_stride,
+                              slot_stride, head_stride, batch, num_qo_heads, num_kv_heads,
+                              head_dim, causal, sm_scale, true, k_scale, v_scale, stream);
 }
 
 }  // extern "C"
@@ -857,6 +769,182 @@ int paged_decode_impl(const void* q, const void* k_pages, const void* v_pages,
             : decode::launch_decode(p, group, st->num_sms, s);
     if (e != cudaSuccess) return PGQA_ERR_CUDA;
     return map_cuda(decode::launch_merge(p, s));
+}
+
+// The paged prefill over bf16 K/V pools (kv8 = false), or over E4M3 pools (kv8 = true):
+// the pages the call reads are then converted into a bf16 pool at the end of the
+// workspace first (dequant.cu), k_scale joins the score scale and v_scale the output
+// scale.
+int paged_prefill_impl(const void* q, const void* k_pages, const void* v_pages, void* o,
+                       float* lse, const int32_t* q_indptr, const int32_t* page_table,
+                       int page_table_stride, const int32_t* kv_lens, int page_size,
+                       int num_pages, int64_t page_stride, int64_t slot_stride,
+                       int64_t head_stride, int batch, int num_qo_heads, int num_kv_heads,
+                       int head_dim, int causal, float sm_scale, bool kv8, float k_scale,
+                       float v_scale, pgqa_stream_t stream) {
+    if (batch < 0 || num_qo_heads <= 0 || num_kv_heads <= 0 || page_table_stride < 0 ||
+        num_pages < 0)
+        return PGQA_ERR_INVALID_ARG;
+    if (batch > 0 && !kv_strides_ok(page_stride, slot_stride, head_stride, kv8 ? 1 : 2))
+        return PGQA_ERR_INVALID_ARG;
+    if (batch == 0) return PGQA_OK;
+    if (!q || !k_pages || !v_pages || !o || !q_indptr || !kv_lens ||
+        (!page_table && page_table_stride > 0))
+        return PGQA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(q_indptr) & 3u) ||
+        (reinterpret_cast<uintptr_t>(page_table) & 3u) ||
+        (reinterpret_cast<uintptr_t>(kv_lens) & 3u))
+        return PGQA_ERR_INVALID_ARG;
+    if (head_dim != 128 && head_dim != 256) return PGQA_ERR_UNSUPPORTED;
+    if (page_size != 16 && page_size != 32 && page_size != 64 && page_size != 128)
+        return PGQA_ERR_UNSUPPORTED;
+    if (num_qo_heads % num_kv_heads != 0) return PGQA_ERR_UNSUPPORTED;
+    const int group = num_qo_heads / num_kv_heads;
+    if (group > prefill::BM || prefill::BM % group != 0) return PGQA_ERR_UNSUPPORTED;
+    if (!(sm_scale == sm_scale) || sm_scale > 3.0e38f || sm_scale < -3.0e38f)
+        return PGQA_ERR_INVALID_ARG;
+    if ((long long)page_table_stride * page_size > 0x7fffffffLL) return PGQA_ERR_UNSUPPORTED;
+
+    std::lock_guard<std::mutex> lock(g_mutex);
+    int dev;
+    DeviceState* st;
+    int rc = current_device(&dev, &st);
+    if (rc != PGQA_OK) return rc;
+    if ((rc = get_encoder()) != PGQA_OK) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // E4M3 pools: a bf16 pool of the pages the call reads (by page when the caller's pool is
+    // the smaller, else by table slot with a rewritten table), after the prefill's own part
+    const long long slots = (long long)batch * page_table_stride;
+    const bool by_page = (long long)num_pages <= slots;
+    long long pool_pages = by_page ? num_pages : slots;
+    if (pool_pages < 1) pool_pages = 1;
+    if (kv8 && pool_pages > 0x7fffffffLL) return PGQA_ERR_UNSUPPORTED;
+    const size_t page_bytes = (size_t)page_size * num_kv_heads * head_dim * 2;
+    const size_t pool_bytes = kv8 ? align_up((size_t)pool_pages * page_bytes, 1024) : 0;
+    const size_t table_bytes = kv8 && !by_page ? align_up((size_t)slots * sizeof(int), 1024) : 0;
+    const size_t tail = 2 * pool_bytes + table_bytes;
+    size_t head_need = prefill_ws_bytes(batch, 4096);
+    if (kv8 && head_need < kDefaultWorkspace) head_need = kDefaultWorkspace;
+    head_need = align_up(head_need, 1024);
+    rc = ensure_workspace(*st, head_need + tail, s);
+    if (rc != PGQA_OK) return rc;
+
+    const size_t usable = kv8 ? ((st->ws_bytes - tail) & ~(size_t)1023) : 0;
+    const PrefillWs lay = prefill_layout(*st, batch, head_dim, usable);
+    if (kv8) {
+        uint8_t* tail_base = static_cast<uint8_t*>(st->ws) + usable;
+        dequant::Params dq;
+        dq.k8 = static_cast<const uint8_t*>(k_pages);
+        dq.v8 = static_cast<const uint8_t*>(v_pages);
+        dq.page_stride = page_stride;
+        dq.slot_stride = slot_stride;
+        dq.head_stride = head_stride;
+        dq.k16 = tail_base;
+        dq.v16 = tail_base + pool_bytes;
+        dq.page_table = page_table;
+        dq.kv_lens = kv_lens;
+        dq.table_out = by_page ? nullptr : reinterpret_cast<int*>(tail_base + 2 * pool_bytes);
+        dq.status = &lay.hdr->status;
+        dq.batch = batch;
+        dq.page_table_stride = page_table_stride;
+        dq.page_size = page_size;
+        dq.num_pages = num_pages;
+        dq.num_kv_heads = num_kv_heads;
+        dq.head_dim = head_dim;
+        if (dequant::launch_dequant(dq, st->num_sms, s) != cudaSuccess) return PGQA_ERR_CUDA;
+        // from here on the call reads the bf16 pool: packed NHD, pool_pages pages
+        k_pages = dq.k16;
+        v_pages = dq.v16;
+        if (!by_page) page_table = dq.table_out;
+        num_pages = (int)pool_pages;
+        page_stride = (int64_t)page_size * num_kv_heads * head_dim;
+        slot_stride = (int64_t)num_kv_heads * head_dim;
+        head_stride = head_dim;
+        sm_scale *= k_scale;
+    }
+    WsHeader* hdr = lay.hdr;
+    CUtensorMap* tmaps = lay.tmaps;
+    int* tile_off = lay.tile_off;
+    int* kv_off = lay.kv_off;
+    prefill::WorkItem* items = lay.items;
+    const long long capacity = lay.item_capacity;
+
+    // Q as for the ragged call (row extent patched on the device); K/V as 4-D page pools
+    // {d, slot, head, page}, one box = one page of one head and one 64-column chunk.
+    CUtensorMap tq, tk, tv;
+    const uint32_t tpt = prefill::BM / group;
+    if ((rc = encode_3d(&tq, q, head_dim, num_qo_heads, tpt, (uint64_t)head_dim * 2,
+                        (uint64_t)num_qo_heads * head_dim * 2, 64, group, tpt)) != PGQA_OK)
+        return rc;
+    // head_dim 256 with pages of up to 32 tokens: the grouped stage layout (a 64 KB K/V tile
+    // in 16 boxes of 4 KB rather than 4 * 128 / page_size boxes)
+    const bool grouped = head_dim == 256 && page_size <= 32;
+    int box_keys = 0, page_heads = 0;
+    if (grouped) {
+        if ((rc = encode_pages_grouped(&tk, k_pages, head_dim, page_size, num_kv_heads, num_pages,
+                                       page_stride, slot_stride, head_stride, &box_keys,
+                                       &page_heads)) != PGQA_OK ||
+            (rc = encode_pages_grouped(&tv, v_pages, head_dim, page_size, num_kv_heads, num_pages,
+                                       page_stride, slot_stride, head_stride, &box_keys,
+                                       &page_heads)) != PGQA_OK)
+            return rc;
+    } else {
+        if ((rc = encode_pages_4d(&tk, k_pages, head_dim, page_size, num_kv_heads, num_pages,
+                                  page_stride, slot_stride, head_stride)) != PGQA_OK ||
+            (rc = encode_pages_4d(&tv, v_pages, head_dim, page_size, num_kv_heads, num_pages,
+                                  page_stride, slot_stride, head_stride)) != PGQA_OK)
+            return rc;
+    }
+
+    prefill::PlanParams pp;
+    pp.q_indptr = q_indptr;
+    pp.kv_indptr = nullptr;
+    pp.kv_lens = kv_lens;
+    pp.max_kv = page_table_stride * page_size;
+    pp.kv_off = kv_off;
+    pp.batch = batch;
+    pp.num_kv_heads = num_kv_heads;
+    pp.group = group;
+    pp.causal = causal ? 1 : 0;
+    pp.tiles_per_item = head_dim == 128 ? 2 : 1;
+    pp.hdr = hdr;
+    pp.tile_off = tile_off;
+    pp.items = items;
+    pp.item_capacity = capacity;
+    pp.tm_out = tmaps;
+    cudaError_t e;
+
+    prefill::Params p;
+    p.tm_q = tmaps + 0;
+    p.tm_k = tmaps + 1;
+    p.tm_v = tmaps + 2;
+    p.o = o;
+    p.lse = lse;
+    p.q_indptr = q_indptr;
+    p.kv_indptr = nullptr;
+    p.items = items;
+    p.hdr = hdr;
+    p.status = &hdr->status;
+    p.num_qo_heads = num_qo_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.group = group;
+    p.causal = causal ? 1 : 0;
+    p.scale_log2 = sm_scale * 1.4426950408889634f;
+    p.v_scale = v_scale;
+    p.page_table = page_table;
+    p.page_table_stride = page_table_stride;
+    p.page_size = page_size;
+    p.num_pages = num_pages;
+    p.box_keys = box_keys;
+    p.page_heads = page_heads;
+    fill_split(pp, p, lay, batch, head_dim, num_qo_heads, st->num_sms);
+    e = prefill::launch_plan(pp, tq, tk, tv, s);
+    if (e != cudaSuccess) return PGQA_ERR_CUDA;
+    e = head_dim == 128 ? prefill::launch_attention_pair<true>(p, st->num_sms, s)
+                        : prefill::launch_attention<256, true>(p, st->num_sms, grouped, s);
+    if (e != cudaSuccess) return PGQA_ERR_CUDA;
+    return map_cuda(prefill::launch_merge(p, head_dim, st->num_sms, s));
 }
 }  // namespace
 

@@ -85,7 +85,8 @@ struct Params {
     int num_kv_heads;
     int group;
     int causal;
-    float scale_log2;          // sm_scale * log2(e)
+    float scale_log2;          // sm_scale * log2(e) (* k_scale for a dequantised FP8 cache)
+    float v_scale;             // output scale (1, or v_scale for a dequantised FP8 cache)
     // paged K/V (paged kernels only): key j of request b is slot j % page_size of page
     // page_table[b * page_table_stride + j / page_size]; the K/V maps view each page pool
     // as a 4-D tensor {d, slot, head, page} (caller strides) with a box of one page of
@@ -224,5 +225,21 @@ struct PlanParams {
     int max_qo;
 };
 }  // namespace decode
+
+namespace dequant {
+// E4M3 K/V pages -> a bf16 pool (dequant.cu)
+struct Params {
+    const uint8_t* k8;           // E4M3 pools with the caller's strides (elements = bytes)
+    const uint8_t* v8;
+    long long page_stride, slot_stride, head_stride;
+    void* k16;                   // bf16 pools, packed NHD [pool pages][page_size][Hk][d]
+    void* v16;
+    const int* page_table;       // [batch][page_table_stride]
+    const int* kv_lens;          // [batch]
+    int* table_out;              // by table slot: [batch][page_table_stride]; by page: null
+    int* status;
+    int batch, page_table_stride, page_size, num_pages, num_kv_heads, head_dim;
+};
+}  // namespace dequant
 
 }  // namespace pgqa

@@ -1035,7 +1035,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
             ++items_done;
             if (!ok) break;
             tc_fence_after();
-            const float inv_l = l > 0.f ? 1.f / l : 0.f;
+            const float inv_l = l > 0.f ? p.v_scale / l : 0.f;
             const float lse_v = l > 0.f ? (m_used + log2f(l)) * 0.69314718055994531f : -INFINITY;
             if (w.part >= 0) {
                 // split-KV partial: O / l in fp32 and the chunk's lse
@@ -1113,7 +1113,9 @@ struct PairCfg {
 };
 
 
-template <bool PAGED>
+// VSCALE: the output takes p.v_scale (a dequantised FP8 cache); a separate instance, so the
+// bf16 paths keep their code unchanged
+template <bool PAGED, bool VSCALE>
 __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const Params p) {
     using C = PairCfg;
     constexpr int D = C::D;
@@ -1459,7 +1461,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
         };
         auto store_pending = [&](const uint32_t (&u)[4][32]) {
             if (!pend_valid) return;
-            const float inv_l = pend_l > 0.f ? 1.f / pend_l : 0.f;
+            const float inv_l = pend_l > 0.f ? (VSCALE ? p.v_scale : 1.f) / pend_l : 0.f;
             if (pend_slot >= 0) {  // split-KV partial: O / l in fp32 and the chunk's lse
                 float4* op = reinterpret_cast<float4*>(p.part_o + pend_slot * D);
 #pragma unroll
@@ -1789,20 +1791,28 @@ cudaError_t launch_attention(const Params& p, int grid, bool grouped, cudaStream
     return launch_attention_t<D, PAGED, false>(p, grid, stream);
 }
 
-template <bool PAGED>
-cudaError_t launch_attention_pair(const Params& p, int grid, cudaStream_t stream) {
+template <bool PAGED, bool VSCALE>
+static cudaError_t launch_pair_t(const Params& p, int grid, cudaStream_t stream) {
     static std::atomic<bool> configured[64];  // per device, set once (repeats are harmless)
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !configured[dev].load(std::memory_order_acquire)) {
-        cudaError_t e = cudaFuncSetAttribute(attention_pair_kernel<PAGED>,
+        cudaError_t e = cudaFuncSetAttribute(attention_pair_kernel<PAGED, VSCALE>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              PairCfg::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         configured[dev].store(true, std::memory_order_release);
     }
-    return launch_dependent(attention_pair_kernel<PAGED>, grid, PAIR_THREADS, PairCfg::SMEM_BYTES,
-                            stream, p);
+    return launch_dependent(attention_pair_kernel<PAGED, VSCALE>, grid, PAIR_THREADS,
+                            PairCfg::SMEM_BYTES, stream, p);
+}
+
+template <bool PAGED>
+cudaError_t launch_attention_pair(const Params& p, int grid, cudaStream_t stream) {
+    if constexpr (PAGED) {
+        if (p.v_scale != 1.f) return launch_pair_t<true, true>(p, grid, stream);
+    }
+    return launch_pair_t<PAGED, false>(p, grid, stream);
 }
 
 cudaError_t launch_merge(const Params& p, int head_dim, int num_sms, cudaStream_t stream) {

@@ -1,20 +1,20 @@
-"""GPU parity of the paged prefill with few query rows per request (multi-token decode)
-over an FP8 E4M3 KV cache (pgqa_paged_prefill_e4m3) against the float64 oracle's E4M3
-path.  Ragged queries over a paged cache with bottom-right causal masking are FlashInfer
-documentation, flashinfer.prefill (BatchPrefillWithPagedKVCacheWrapper); the E4M3 cache
-is flashinfer_benchmark.py "Attention Flags" (--kv_dtype fp8_e4m3)."""
+"""GPU parity of the paged prefill over an FP8 E4M3 KV cache (pgqa_paged_prefill_e4m3)
+against the float64 oracle's E4M3 path, on both of its paths: few query rows per request
+(multi-token decode: the tensor-core E4M3 decode with the rows as MMA columns) and longer
+query runs or head_dim 256 (the pages converted to bf16 in the workspace, then the bf16
+paged prefill).  Ragged queries over a paged cache with bottom-right causal masking are
+FlashInfer documentation, flashinfer.prefill (BatchPrefillWithPagedKVCacheWrapper); the
+E4M3 cache is flashinfer_benchmark.py "Attention Flags" (--kv_dtype fp8_e4m3)."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
-from paged_gqa_attention_varlen_gb300 import api as _api
 from paged_gqa_attention_varlen_gb300 import workloads as W
 from gpu_util import check_rows
 
 pytestmark = pytest.mark.gpu
 
-PGQA_ERR_UNSUPPORTED = -2
 PGQA_ERR_DEVICE_BOUNDS = -6
 
 
@@ -140,12 +140,100 @@ def test_rows_beyond_the_declared_maximum_are_refused(cuda_lib):
                lse.reshape(-1).index_select(0, idx).cpu(), ro, rl, "other requests")
 
 
-def test_too_many_rows_for_one_tile_is_unsupported(cuda_lib):
-    pc = W.paged_case_e4m3([100, 200], 32, 8, 128, page_size=16, qo_lens=[5, 2], seed=351,
+@pytest.mark.parametrize("d,G,ps,causal", [(128, 4, 16, True), (128, 1, 64, True),
+                                           (128, 8, 32, False), (128, 16, 16, True),
+                                           (256, 4, 16, True), (256, 2, 128, False)])
+def test_e4m3_long_prefill_against_oracle(cuda_lib, d, G, ps, causal):
+    """Query runs longer than 16 / G rows (and head_dim 256): the pages are converted to
+    bf16 in the workspace and the bf16 paged prefill runs over them."""
+    hk = 2 if G >= 8 else 4
+    qo, kv = [300, 45, 7, 0, 129], [700, 45, 1300, 20, 129]
+    pc = W.paged_case_e4m3(kv, G * hk, hk, d, page_size=ps, qo_lens=qo, seed=361 + G + d + ps,
+                           device="cuda", k_scale=0.5, v_scale=2.0)
+    o, lse = run(cuda_lib, pc, max(qo), causal)
+    assert cuda_lib.device_status() == 0
+    ro, rl = oracle_e4m3(pc, causal)
+    check_rows(o.reshape(-1, d).float().cpu(), lse.reshape(-1).cpu(), ro, rl,
+               f"e4m3 long prefill d={d} G={G} ps={ps} causal={causal}")
+
+
+def test_dequantised_prefill_equals_bf16_prefill_of_the_same_values_bitwise(cuda_lib):
+    """E4M3 -> bf16 is exact and k_scale = 0.5 folds exactly into the score scale, so with
+    v_scale = 1 the result is the bf16 paged prefill's over the same values, bit for bit."""
+    pc = W.paged_case_e4m3([700, 45, 1300], 16, 4, 128, page_size=16, qo_lens=[200, 45, 7],
+                           seed=371, device="cuda", k_scale=0.5, v_scale=1.0)
+    o8, l8 = run(cuda_lib, pc, 200)
+    kb = pc.k_pages.view(torch.float8_e4m3fn).to(torch.bfloat16)
+    vb = pc.v_pages.view(torch.float8_e4m3fn).to(torch.bfloat16)
+    ob, lb = cuda_lib.paged_prefill(pc.q, kb, vb, pc.q_indptr, pc.page_table, pc.kv_lens_t,
+                                    causal=True, sm_scale=pc.sm_scale * 0.5)
+    torch.cuda.synchronize()
+    assert cuda_lib.device_status() == 0
+    assert torch.equal(o8, ob) and torch.equal(l8, lb)
+
+
+def test_pool_by_page_and_by_table_slot_agree_bitwise(cuda_lib):
+    """The converted pool is indexed by page when the caller's pool is no larger than
+    batch x page_table_stride pages, else by table slot with a rewritten table: same bits."""
+    pc = W.paged_case_e4m3([700], 16, 4, 128, page_size=16, qo_lens=[300], seed=373,
+                           device="cuda", extra_pages=10)  # 54 pages > 1 x 44 slots: by slot
+    o1, l1 = run(cuda_lib, pc, 300)
+    wide = torch.cat([pc.page_table, torch.full((1, 16), -1, dtype=torch.int32, device="cuda")],
+                     dim=1)  # 60 slots >= 54 pages: by page
+    o2, l2 = cuda_lib.paged_prefill(pc.q, pc.k_pages, pc.v_pages, pc.q_indptr, wide,
+                                    pc.kv_lens_t, causal=True, sm_scale=pc.sm_scale,
+                                    k_scale=pc.meta["k_scale"], v_scale=pc.meta["v_scale"],
+                                    max_qo_len=300)
+    torch.cuda.synchronize()
+    assert cuda_lib.device_status() == 0
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    ro, rl = oracle_e4m3(pc, True)
+    check_rows(o1.reshape(-1, 128).float().cpu(), lse_cpu(l1), ro, rl, "by table slot")
+
+
+def lse_cpu(lse):
+    return lse.reshape(-1).cpu()
+
+
+def test_bad_page_id_on_the_conversion_path_is_reported(cuda_lib):
+    pc = W.paged_case_e4m3([300, 500], 32, 8, 128, page_size=16, qo_lens=[100, 50], seed=381,
                            device="cuda")
-    with pytest.raises(_api.PgqaError) as e:
-        run(cuda_lib, pc, 5)  # 5 rows x 4 heads > 16 columns
-    assert e.value.code == PGQA_ERR_UNSUPPORTED
-    with pytest.raises(ValueError):
-        cuda_lib.paged_prefill(pc.q, pc.k_pages, pc.v_pages, pc.q_indptr, pc.page_table,
-                               pc.kv_lens_t)  # E4M3 pools without max_qo_len
+    pc.page_table[1, 3] = pc.num_pages + 3
+    run(cuda_lib, pc, 100)
+    assert cuda_lib.device_status() == PGQA_ERR_DEVICE_BOUNDS
+    assert cuda_lib.device_status() == 0
+
+
+def test_default_max_qo_len_is_the_total_row_count(cuda_lib):
+    """Without max_qo_len the binding passes total_q, an upper bound: here 7 rows x 4 heads
+    > 16 columns, so the conversion path runs; it agrees with the tensor-core path (which
+    the true maximum, 4, selects) to the parity tolerance."""
+    pc = W.paged_case_e4m3([100, 2000], 32, 8, 128, page_size=16, qo_lens=[3, 4], seed=391,
+                           device="cuda")
+    o1, l1 = cuda_lib.paged_prefill(pc.q, pc.k_pages, pc.v_pages, pc.q_indptr, pc.page_table,
+                                    pc.kv_lens_t, sm_scale=pc.sm_scale,
+                                    k_scale=pc.meta["k_scale"], v_scale=pc.meta["v_scale"])
+    o2, l2 = run(cuda_lib, pc, 4)
+    assert cuda_lib.device_status() == 0
+    ro, rl = oracle_e4m3(pc, True)
+    for o, l, what in ((o1, l1, "conversion path"), (o2, l2, "tensor-core path")):
+        check_rows(o.reshape(-1, 128).float().cpu(), l.reshape(-1).cpu(), ro, rl, what)
+
+
+def test_conversion_path_hnd_and_float8_dtype_match_packed_bitwise(cuda_lib):
+    pc = W.paged_case_e4m3([700, 5, 1300], 16, 4, 128, page_size=32, qo_lens=[200, 5, 64],
+                           seed=395, device="cuda")
+    o, lse = run(cuda_lib, pc, 200)
+    kw = dict(causal=True, sm_scale=pc.sm_scale, k_scale=pc.meta["k_scale"],
+              v_scale=pc.meta["v_scale"], max_qo_len=200)
+    o2, l2 = cuda_lib.paged_prefill(pc.q, pc.k_pages.view(torch.float8_e4m3fn),
+                                    pc.v_pages.view(torch.float8_e4m3fn), pc.q_indptr,
+                                    pc.page_table, pc.kv_lens_t, **kw)
+    kh = pc.k_pages.permute(0, 2, 1, 3).contiguous()
+    vh = pc.v_pages.permute(0, 2, 1, 3).contiguous()
+    o3, l3 = cuda_lib.paged_prefill(pc.q, kh, vh, pc.q_indptr, pc.page_table, pc.kv_lens_t,
+                                    kv_layout="HND", **kw)
+    torch.cuda.synchronize()
+    assert cuda_lib.device_status() == 0
+    for a, b in ((o2, l2), (o3, l3)):
+        assert torch.equal(a, o) and torch.equal(b, lse)

@@ -9,6 +9,8 @@ notes).  A caller may hand it a buffer of its own instead (pgqa_set_workspace).
 - A caller buffer gives the same results as the lazy workspace, bit for bit.
 - A caller buffer too small for a call's fixed arrays makes the call return
   PGQA_ERR_WORKSPACE with nothing enqueued.
+- An E4M3 paged prefill whose converted pages do not fit a caller buffer returns
+  PGQA_ERR_WORKSPACE with nothing enqueued.
 - A prefill whose work list outgrows a (small) caller buffer reports
   PGQA_ERR_DEVICE_CAPACITY through the device status and writes nothing.
 - A device status left unread by a call on a non-blocking stream survives a later call
@@ -131,3 +133,22 @@ def test_pending_status_survives_growth_on_a_non_blocking_stream(lazy_after):
     torch.cuda.synchronize()
     assert api.device_status() == PGQA_ERR_DEVICE_BOUNDS
     assert api.device_status() == 0
+
+
+def test_e4m3_conversion_pool_larger_than_the_caller_buffer_is_refused(lazy_after):
+    api = lazy_after
+    # 1875 pages of 16 x 8 x 128: about 123 MB of bf16 K and V besides the prefill's part
+    pc = W.paged_case_e4m3([30000], 32, 8, 128, page_size=16, qo_lens=[300], seed=211,
+                           device="cuda")
+    buf = torch.empty(64 << 20, dtype=torch.uint8, device="cuda")
+    api.set_workspace(buf)
+    o = torch.full_like(pc.q, 7.0)
+    with pytest.raises(_api.PgqaError) as e:
+        api.paged_prefill(pc.q, pc.k_pages, pc.v_pages, pc.q_indptr, pc.page_table,
+                          pc.kv_lens_t, sm_scale=pc.sm_scale, k_scale=0.5, v_scale=2.0,
+                          max_qo_len=300, out=o)
+    assert e.value.code == PGQA_ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert bool((o == 7.0).all())
+    assert api.device_status() == 0
+    api.set_workspace(None)
