@@ -4,7 +4,8 @@ with the float64 oracle on all rows.
 Every case draws its own shapes from a fixed seed:
 - batch size; per-request lengths, including empty requests and kv_len < qo_len;
 - query and kv head counts, head_dim, causal or not, sm_scale;
-- page size, KV layout (NHD / HND) and FP8 scales.
+- page size, KV layout (NHD / HND) and FP8 scales; for the E4M3 paged prefill, short
+  or long query runs (its two paths).
 
 The sweep reaches combinations that the hand-written cases do not list: long and short
 requests mixed in one batch, several KV heads with large groups, and both split regimes
@@ -141,3 +142,38 @@ def test_e4m3_decode_sweep(cuda_lib, case):
                                          pc.sm_scale)
     check_rows(o.reshape(-1, 128), lse.reshape(-1), ro, rl,
                f"e4m3 case {case}: kv {kv} heads {hq}/{hk} page {ps} scales {ks:.2f}/{vs:.2f}")
+
+
+@pytest.mark.parametrize("case", range(N_CASES))
+def test_e4m3_prefill_sweep(cuda_lib, case):
+    """The E4M3 paged prefill on both of its paths: few query rows per request (the
+    tensor-core path, max_qo_len * G <= 16) or longer runs and head_dim 256 (the pages
+    converted to bf16 first); causal or not, both layouts, random scales."""
+    rng = np.random.default_rng(13000 + case)
+    batch = int(rng.integers(1, 6))
+    hq, hk = _heads(rng, [1, 2, 4, 8])
+    g = hq // hk
+    short = rng.random() < 0.5
+    d = 128 if short else int(rng.choice([128, 256]))
+    ps = int(rng.choice([16, 32, 64, 128]))
+    layout = str(rng.choice(["NHD", "HND"]))
+    causal = bool(rng.random() < 0.75)
+    qmax = max(1, 16 // g) if short else 200
+    qo = _lens(rng, batch, 1, qmax, p_zero=0.05)
+    kv = [max(0, q + int(rng.integers(-3, 3000 if short else 500))) for q in qo]
+    ks, vs = float(rng.uniform(0.1, 4.0)), float(rng.uniform(0.1, 4.0))
+    pc = W.paged_case_e4m3(kv, hq, hk, d, page_size=ps, qo_lens=qo, sm_scale=_scale(rng, d),
+                           seed=14000 + case, device="cuda", k_scale=ks, v_scale=vs,
+                           extra_pages=int(rng.integers(0, 5)))
+    k, v = (pc.k_pages, pc.v_pages) if layout == "NHD" else (_hnd(pc.k_pages), _hnd(pc.v_pages))
+    o, lse = cuda_lib.paged_prefill(pc.q, k, v, pc.q_indptr, pc.page_table, pc.kv_lens_t,
+                                    causal=causal, sm_scale=pc.sm_scale, kv_layout=layout,
+                                    k_scale=ks, v_scale=vs, max_qo_len=max(max(qo), 1))
+    torch.cuda.synchronize()
+    assert cuda_lib.device_status() == 0
+    ro, rl = oracle.paged_attention_e4m3(pc.q, pc.q_indptr, pc.k_pages, pc.v_pages, ks, vs,
+                                         pc.page_table, pc.kv_lens_t, hq, hk, causal,
+                                         pc.sm_scale)
+    check_rows(o.reshape(-1, d), lse.reshape(-1), ro, rl,
+               f"e4m3 prefill case {case}: qo {qo} kv {kv} heads {hq}/{hk} d {d} page {ps} "
+               f"{layout} causal {causal} scales {ks:.2f}/{vs:.2f}")
