@@ -692,23 +692,30 @@ def profile_case(args):
         for _ in range(args.reps):
             api.ragged_prefill(c.q, c.k, c.v, c.q_indptr, c.kv_indptr, causal=c.causal,
                                sm_scale=c.sm_scale, out=o, lse=lse)
-    elif args.profile in ("paged_prefill_hd128", "paged_prefix_hd256", "decode_q4"):
+    elif args.profile in ("paged_prefill_hd128", "paged_prefix_hd256", "decode_q4",
+                          "decode_q4_e4m3", "paged_prefill_e4m3_hd128"):
         # paged prefill: the named shape in 16-token pages; decode_q4: 4 query tokens per
-        # request over the first --decode-batch requests of the decode workload
-        if args.profile == "decode_q4":
+        # request over the first --decode-batch requests of the decode workload; the _e4m3
+        # cases store the same pages as FP8 E4M3 (scales 1)
+        e4m3 = args.profile.endswith("e4m3") or "_e4m3_" in args.profile
+        if args.profile.startswith("decode_q4"):
             kv = W.config_lengths("decode")[1][:args.decode_batch]
             c = W.paged_case(kv, 32, 8, 128, page_size=16, qo_lens=[4] * len(kv), seed=0,
                              device=dev)
         else:
-            name = args.profile[len("paged_"):]
+            name = "prefill_hd128" if e4m3 else args.profile[len("paged_"):]
             qo, kv = W.config_lengths(name)
             hq, hk, d = (32, 8, 128) if name == "prefill_hd128" else (16, 4, 256)
             c = W.paged_case(kv, hq, hk, d, page_size=16, qo_lens=qo, seed=0, device=dev)
+        kp, vp, extra = c.k_pages, c.v_pages, {}
+        if e4m3:
+            kp, vp = kp.to(torch.float8_e4m3fn), vp.to(torch.float8_e4m3fn)
+            extra = dict(k_scale=1.0, v_scale=1.0, max_qo_len=max(c.qo_lens))
         o = torch.empty_like(c.q)
         lse = torch.empty(c.q.shape[:2], dtype=torch.float32, device=dev)
         for _ in range(args.reps):
-            api.paged_prefill(c.q, c.k_pages, c.v_pages, c.q_indptr, c.page_table, c.kv_lens_t,
-                              causal=True, sm_scale=c.sm_scale, out=o, lse=lse)
+            api.paged_prefill(c.q, kp, vp, c.q_indptr, c.page_table, c.kv_lens_t,
+                              causal=True, sm_scale=c.sm_scale, out=o, lse=lse, **extra)
     else:  # decode slice: the first --decode-batch requests of the decode workload
         kv = W.config_lengths("decode")[1][:args.decode_batch]
         if args.profile == "decode_e4m3":
@@ -747,7 +754,8 @@ def main(argv=None):
                     help="skip the paged-prefill and multi-token-decode measurements")
     ap.add_argument("--profile", choices=["prefill_hd128", "prefix_hd256", "long", "tiny",
                                           "decode", "paged_prefill_hd128", "paged_prefix_hd256",
-                                          "decode_q4", "decode_e4m3"], default=None,
+                                          "decode_q4", "decode_e4m3", "decode_q4_e4m3",
+                                          "paged_prefill_e4m3_hd128"], default=None,
                     help="run one bounded case --reps times and exit (ncu captures)")
     ap.add_argument("--reps", type=int, default=4)
     ap.add_argument("--decode-batch", type=int, default=32)
