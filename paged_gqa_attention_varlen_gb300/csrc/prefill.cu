@@ -654,10 +654,14 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
     const int n_items = p.hdr->n_items;
     const int G = p.group;
 
-    if (warp == 0) {
+    if (warp == 0 || (PAGED && warp == 3)) {
         // ------------------------------------------------------------ TMA producer
         // Ragged K/V: lane 0 alone.  Paged K/V: the whole warp, lane l loading page l of
-        // each K/V tile (its id read one load ahead); lane 0 arms the barriers.
+        // each K/V tile (its id read one load ahead); lane 0 arms the barriers.  Paged:
+        // warps 0 and 3 take alternate loads (the ring positions load_idx % 2), so two
+        // warps issue boxes; both follow the page ids of every tile.
+        constexpr uint32_t NPROD = PAGED ? 2u : 1u;
+        const uint32_t pw = warp == 0 ? 0u : 1u;
         if (PAGED || lane == 0) {
             auto wait = [&](uint32_t bar, uint32_t par) -> bool {
                 if constexpr (PAGED)
@@ -682,16 +686,18 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
                 const int n = item_tiles(w, x);  // K/V tiles kt0 .. kt0 + n - 1
                 const int kt0 = w.kt0;
                 if (n == 0) continue;
-                ok = wait(BAR(Q_EMPTY), (q_count & 1) ^ 1);
-                if (!ok) break;
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(BAR(Q_FULL), C::TILE_BYTES);
+                if (pw == 0) {
+                    ok = wait(BAR(Q_EMPTY), (q_count & 1) ^ 1);
+                    if (!ok) break;
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(BAR(Q_FULL), C::TILE_BYTES);
 #pragma unroll
-                    for (int c = 0; c < C::CHUNKS; ++c)
-                        tma_load_3d(sQ + c * C::CHUNK_BYTES, p.tm_q, BAR(Q_FULL), c * 64, w.g * G,
-                                    x.q_start + x.t0);
+                        for (int c = 0; c < C::CHUNKS; ++c)
+                            tma_load_3d(sQ + c * C::CHUNK_BYTES, p.tm_q, BAR(Q_FULL), c * 64,
+                                        w.g * G, x.q_start + x.t0);
+                    }
+                    ++q_count;
                 }
-                ++q_count;
                 // consumption order of the MMA warp: K0, (K1, V0), (K2, V1), ..., V_{n-1}
                 // (tile indices relative to kt0)
                 const int nl = 2 * n;
@@ -725,8 +731,6 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
                     const int jr = tile_of(s, is_k);
                     const int j = kt0 + jr;  // absolute K/V tile of the request
                     const uint32_t st = load_idx % C::STAGES;
-                    ok = wait(BAR(KV_EMPTY + st), ((load_idx / C::STAGES) & 1) ^ 1);
-                    if (!ok) break;
                     const CUtensorMap* tm = is_k ? p.tm_k : p.tm_v;
                     if constexpr (PAGED) {
                         int pid;
@@ -739,6 +743,12 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
                         } else {
                             pid = j == k_last ? id_last : id_prev;
                         }
+                        if (load_idx % NPROD != pw) {  // the other producer's load
+                            ++load_idx;
+                            continue;
+                        }
+                        ok = wait(BAR(KV_EMPTY + st), ((load_idx / C::STAGES) & 1) ^ 1);
+                        if (!ok) break;
                         if constexpr (GROUPED) {
                             const bool pg_ok = group_page_ok(pid, j, ps, npg, p.box_keys,
                                                              p.num_pages, lane, p.status);
@@ -755,6 +765,8 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
                         if (lane == 0 && s == nl - 1 && (kt0 + n) * BN > x.kv_len)
                             mbar_arrive(BAR(FIX_READY));
                     } else {
+                        ok = wait(BAR(KV_EMPTY + st), ((load_idx / C::STAGES) & 1) ^ 1);
+                        if (!ok) break;
                         mbar_arrive_expect_tx(BAR(KV_FULL + st), C::TILE_BYTES);
 #pragma unroll
                         for (int c = 0; c < C::CHUNKS; ++c)
@@ -765,12 +777,13 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
                 }
             }
             if (!ok && lane == 0) {
-                // let every copy already issued land before the CTA exits
+                // let every copy this warp issued land before the CTA exits
                 const uint32_t first = load_idx > (uint32_t)C::STAGES ? load_idx - C::STAGES : 0;
                 for (uint32_t k = first; k < load_idx; ++k)
-                    mbar_wait_bounded(BAR(KV_FULL + k % C::STAGES), (k / C::STAGES) & 1, nullptr,
-                                      p.status);
-                if (q_count > 0)
+                    if (k % NPROD == pw)
+                        mbar_wait_bounded(BAR(KV_FULL + k % C::STAGES), (k / C::STAGES) & 1,
+                                          nullptr, p.status);
+                if (pw == 0 && q_count > 0)
                     mbar_wait_bounded(BAR(Q_FULL), (q_count - 1) & 1, nullptr, p.status);
             }
         }
