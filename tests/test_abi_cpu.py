@@ -160,6 +160,41 @@ def test_e4m3_decode_validation(api):
         assert dc() == -7
 
 
+def test_e4m3_prefill_validation(api):
+    """pgqa_paged_prefill_e4m3: argument checks before any CUDA call, on both of its
+    paths (the tensor-core path for max_qo_len * G <= 16 at head_dim 128, the conversion
+    path otherwise)."""
+    p = ctypes.c_void_p
+    lib = api.lib
+
+    def pf(page_s=16 * 8 * 128, slot_s=8 * 128, head_s=128, ks=0.5, vs=2.0, batch=2, ps=16,
+           d=128, max_qo=4, hq=32, hk=8, qi=A, pt=A):
+        if d == 256:
+            page_s, slot_s, head_s = 16 * hk * 256, hk * 256, 256
+        return lib.pgqa_paged_prefill_e4m3(p(A), p(A), p(A), p(A), p(A), p(qi), p(pt), 8, p(A),
+                                           ps, 100, page_s, slot_s, head_s, ks, vs, batch,
+                                           max_qo, hq, hk, d, 1, 0.1, None)
+
+    assert pf(batch=0) == 0
+    assert pf(max_qo=0) == -1                      # max_qo_len < 1
+    assert pf(qi=0) == -1                          # no q_indptr
+    assert pf(qi=A + 2) == -1                      # misaligned q_indptr
+    assert pf(ks=float("nan")) == -1
+    assert pf(vs=float("-inf")) == -1
+    for max_qo in (4, 5, 300):                     # tensor-core path, conversion path
+        assert pf(max_qo=max_qo, head_s=8) == -1   # 8 bytes: not a multiple of 16
+        assert pf(max_qo=max_qo, ps=24) == -2
+        assert pf(max_qo=max_qo, hq=24, hk=8) == -2  # group 3
+    assert pf(d=64, max_qo=300) == -2
+    import torch
+    if not torch.cuda.is_available():
+        # valid on each path: no device here
+        assert pf(max_qo=4) == -7                  # 4 rows x G 4 = 16 columns
+        assert pf(max_qo=5) == -7                  # conversion path
+        assert pf(d=256, max_qo=1) == -7           # head_dim 256: conversion path
+        assert pf(hq=128, hk=8, max_qo=1) == -7    # group 16: conversion path
+
+
 def test_prefill_host_validation(api):
     assert prefill(api, batch=0) == 0                       # empty batch: early return
     assert prefill(api, batch=-1) == -1
