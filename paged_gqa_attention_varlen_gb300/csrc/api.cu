@@ -309,6 +309,7 @@ PrefillWs prefill_layout(const DeviceState& st, int batch, int head_dim, size_t 
 void fill_split(prefill::PlanParams& pp, prefill::Params& p, const PrefillWs& w, int batch,
                 int head_dim, int num_qo_heads, int num_sms) {
     pp.split_ok = 1;
+    pp.split_tiles = p.split_tiles = head_dim == 256 ? 32 : 16;
     pp.num_ctas = num_sms;
     pp.num_qo_heads = num_qo_heads;
     pp.part_capacity = w.part_capacity;

@@ -57,7 +57,6 @@ constexpr int COST_BUCKETS = 4096;
 constexpr int PLAN_SMEM_BATCH = 2048;  // batches up to this size plan out of shared memory
 constexpr int PLAN_STAGE_UNITS = 2048; // work lists up to this many units are staged in smem
 
-constexpr int SPLIT_TILES = 16;   // K/V tiles (2048 keys) per chunk of a split request
 
 // One work item of the prefill: a (request, kv head, first q tile, K/V chunk) plus the
 // request's offsets, written by the plan kernel so the attention roles need no further
@@ -109,6 +108,7 @@ struct Params {
     const int* nch;            // [batch] chunks of each request
     const int* kvl;            // [batch] keys of each request
     int batch;
+    int split_tiles;           // K/V tiles per chunk of a split request
 };
 
 struct PlanParams {
@@ -121,6 +121,8 @@ struct PlanParams {
     int group;
     int causal;
     int tiles_per_item;        // consecutive q tiles one work item covers (1 or 2)
+    int split_tiles;           // K/V tiles per chunk of a split request (16 for head_dim 128,
+                               // 32 for 256)
     WsHeader* hdr;
     int* tile_off;             // [batch + 1]
     int* kv_off;               // paged: [batch + 1] prefix sums of kv_lens (workspace)

@@ -16,7 +16,8 @@
 //    their number of K/V tiles (longest first; records staged in shared memory and
 //    written out in coalesced pieces), and patches the global extents of the TMA tensor
 //    maps from q_indptr[batch] / kv_indptr[batch], so the host never reads device data.
-//    Work lists too short to fill the GPU are split into request-local 2048-key chunks.
+//    Work lists too short to fill the GPU are split into request-local chunks of 2048 keys
+//    (head_dim 128) or 4096 keys (head_dim 256).
 //  * attention_pair_kernel (head_dim 128) is persistent (one CTA per SM) and
 //    warp-specialised, two 128-row q tiles (A, B) per CTA sharing one K/V stream:
 //      warp 0   TMA producer: Q tiles once per item, K/V tiles through a 4-stage ring;
@@ -89,10 +90,10 @@ __device__ __forceinline__ WorkItem load_item(const WorkItem* items, int i) {
     return w;
 }
 
-// K/V chunks of a request of kv_len keys when its work is split
-__host__ __device__ __forceinline__ int split_chunks(int kv_len) {
+// K/V chunks of a request of kv_len keys when its work is split into chunks of st tiles
+__host__ __device__ __forceinline__ int split_chunks(int kv_len, int st) {
     const int tiles = (kv_len + BN - 1) / BN;
-    return tiles > SPLIT_TILES ? (tiles + SPLIT_TILES - 1) / SPLIT_TILES : 1;
+    return tiles > st ? (tiles + st - 1) / st : 1;
 }
 
 __device__ __forceinline__ void prefetch_l1(const void* ptr) {
@@ -250,7 +251,9 @@ __global__ void __launch_bounds__(PLAN_THREADS)
     if (tid == 0) toff[p.batch] = total_tiles;
 
     // Split-KV: a work list too short to fill the grid (decode-like calls: few requests,
-    // few query rows, long keys) has its requests cut into chunks of SPLIT_TILES K/V tiles.
+    // few query rows, long keys) has its requests cut into chunks of split_tiles K/V tiles
+    // (2048 keys for head_dim 128, 4096 for 256: measured on short hd256 lists, the longer
+    // chunks halve the per-item start-up that each chunk pays).
     // The cut depends on the request alone, so within this regime a request's results do
     // not depend on the batch.  Units are (q item, chunk); chunked requests write fp32
     // partial results that the merge kernel combines.  If the partial results would not
@@ -267,7 +270,7 @@ __global__ void __launch_bounds__(PLAN_THREADS)
                 const int qo = qi[b + 1] - qi[b];
                 const int tiles = (int)(((long long)qo * p.group + BM - 1) / BM);
                 const int qitems = (tiles + p.tiles_per_item - 1) / p.tiles_per_item;
-                nc = qo > 0 ? split_chunks(ki[b + 1] - ki[b]) : 1;
+                nc = qo > 0 ? split_chunks(ki[b + 1] - ki[b], p.split_tiles) : 1;
                 units = qitems * nc;
                 if (nc > 1) {
                     prow = nc * qo * p.num_qo_heads;
@@ -326,7 +329,7 @@ __global__ void __launch_bounds__(PLAN_THREADS)
         qt = (local / nc) * p.tiles_per_item;
         c = local % nc;
         const int full = item_cost(p, qi, ki, b, qt);
-        cost = nc > 1 ? max(0, min(full - c * SPLIT_TILES, SPLIT_TILES)) : full;
+        cost = nc > 1 ? max(0, min(full - c * p.split_tiles, p.split_tiles)) : full;
     };
 
     // histogram of unit costs (K/V tiles of the unit's longest q tile)
@@ -381,8 +384,8 @@ __global__ void __launch_bounds__(PLAN_THREADS)
         w.qo_len = qi[b + 1] - q0;
         w.kv_start = k0;
         w.kv_len = ki[b + 1] - k0;
-        w.kt0 = nc > 1 ? c * SPLIT_TILES : 0;
-        w.kt1 = nc > 1 ? (c + 1) * SPLIT_TILES : 0x7fffffff;
+        w.kt0 = nc > 1 ? c * p.split_tiles : 0;
+        w.kt1 = nc > 1 ? (c + 1) * p.split_tiles : 0x7fffffff;
         w.part = nc > 1 ? p.part_off[b] + c * w.qo_len * p.num_qo_heads : -1;
         w.nch = nc;
         if (stage) {
@@ -1698,7 +1701,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const Params p) {
         const int kv = __ldg(p.kvl + b);
         const int nc = __ldg(p.nch + b);
         const int nkeys = p.causal ? max(0, min(kv, t + kv - qo + 1)) : kv;
-        const int nvis = min(nc, (nkeys + SPLIT_TILES * BN - 1) / (SPLIT_TILES * BN));
+        const int nvis = min(nc, (nkeys + p.split_tiles * BN - 1) / (p.split_tiles * BN));
         const long long base = __ldg(p.part_off + b);
         auto slot = [&](int c) { return base + ((long long)c * qo + t) * Hq + h; };
         float mx = -INFINITY;

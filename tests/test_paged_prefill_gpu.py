@@ -181,7 +181,8 @@ def test_bad_page_id_reports_bounds_status(cuda_lib):
 
 
 # ---------------------------------------------------------------- split-KV (short work lists)
-# A work list shorter than two items per SM has its requests cut into chunks of 2048 keys;
+# A work list shorter than two items per SM has its requests cut into chunks of 2048 keys
+# (head_dim 128; 4096 keys for head_dim 256);
 # the chunks' partial results are merged by their LSE weights (FlashInfer documentation,
 # flashinfer.cascade "Merge Attention States").
 
@@ -226,7 +227,7 @@ def test_split_kv_non_causal_and_short_requests(cuda_lib):
 @pytest.mark.parametrize("ps", [16, 64])
 def test_split_kv_hd256_paged_short_list(cuda_lib, ps):
     """Two requests with long cached prefixes (qo 200 / 37 over 9000 / 4100 keys), 16/4
-    heads: 12 q-tile items per kv head, cut into 2048-key chunks; all rows checked."""
+    heads: 12 q-tile items per kv head, cut into 4096-key chunks; all rows checked."""
     pc = W.paged_case([9000, 4100], 16, 4, 256, page_size=ps, qo_lens=[200, 37], seed=111 + ps,
                       device="cuda")
     full_check(cuda_lib, pc, f"split-KV hd256 paged, page {ps}")
