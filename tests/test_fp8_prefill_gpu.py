@@ -237,3 +237,42 @@ def test_conversion_path_hnd_and_float8_dtype_match_packed_bitwise(cuda_lib):
     assert cuda_lib.device_status() == 0
     for a, b in ((o2, l2), (o3, l3)):
         assert torch.equal(a, o) and torch.equal(b, lse)
+
+
+def test_conversion_path_short_list_splits_after_conversion(cuda_lib):
+    """One request of 20 query rows (80 columns at G 4: the conversion path) over 20k keys:
+    a work list short enough for the bf16 prefill to split it into chunks, merged by LSE;
+    every row against the oracle."""
+    pc = W.paged_case_e4m3([20000, 0], 32, 8, 128, page_size=16, qo_lens=[20, 3], seed=397,
+                           device="cuda")
+    o, lse = run(cuda_lib, pc, 20)
+    assert cuda_lib.device_status() == 0
+    ro, rl = oracle_e4m3(pc, True)
+    check_rows(o.reshape(-1, 128).float().cpu(), lse.reshape(-1).cpu(), ro, rl,
+               "conversion path, split-KV")
+
+
+@pytest.mark.parametrize("max_qo", [4, 64])
+def test_e4m3_layer_slice_matches_packed_bitwise(cuda_lib, max_qo):
+    """A per-layer slice of a layer-interleaved E4M3 cache [pages, layers, slots, heads, d]
+    (non-contiguous pages) gives the packed result bit for bit on both paths."""
+    qo = [4, 3] if max_qo == 4 else [64, 17]
+    pc = W.paged_case_e4m3([900, 2500], 16, 4, 128, page_size=16, qo_lens=qo, seed=399,
+                           device="cuda")
+    o, lse = run(cuda_lib, pc, max_qo)
+    layers = 3
+    shape = (pc.num_pages, layers) + tuple(pc.k_pages.shape[1:])
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(5)
+    kst = torch.randint(0, 256, shape, generator=gen, device="cuda", dtype=torch.int32)
+    vst = torch.randint(0, 256, shape, generator=gen, device="cuda", dtype=torch.int32)
+    kst, vst = kst.to(torch.uint8), vst.to(torch.uint8)
+    kst[:, 1] = pc.k_pages
+    vst[:, 1] = pc.v_pages
+    o2, l2 = cuda_lib.paged_prefill(pc.q, kst[:, 1], vst[:, 1], pc.q_indptr, pc.page_table,
+                                    pc.kv_lens_t, causal=True, sm_scale=pc.sm_scale,
+                                    k_scale=pc.meta["k_scale"], v_scale=pc.meta["v_scale"],
+                                    max_qo_len=max_qo)
+    torch.cuda.synchronize()
+    assert cuda_lib.device_status() == 0
+    assert torch.equal(o, o2) and torch.equal(lse, l2)
