@@ -13,41 +13,46 @@
 // never visible); FlashInfer documentation, flashinfer.cascade "Merge Attention States"
 // (the chunk merge).
 //
-// Why tensor cores: on the CUDA cores every E4M3 byte costs a conversion plus G fused
-// multiply-adds per K and V element, so the E4M3 decode ran into the issue rate at about
-// half of HBM speed.  Here the dot products run on tcgen05.mma and the CUDA cores only
-// convert bytes, which leaves HBM as the bound.
+// Why the E4M3 bytes go to the tensor core as they are: the decode streams each K/V byte
+// once, so the kernel is bound by how many bytes each SM keeps in flight.  A stage of the
+// TMA ring that has to be converted (to f16, for kind::f16) is held until the conversion
+// ends, and with in-order consumption every slow conversion delays the stages behind it.
+// Here the MMAs (kind::f8f6f4) read the raw stages: Q . K^T takes the K tile straight from
+// the ring, P . V the V tile as an MN-major operand, and a stage is released by the
+// commit of its MMAs.  The other operand of each product, Q and P, is given as a pair of
+// E4M3 matrices hi + lo (hi = E4M3(x), lo = E4M3(x - hi)), two MMAs accumulating into the
+// same fp32 result: for Q (bf16, scaled by a power of two into [2^7, 2^8)) the pair is
+// exact down to 2^-2, for P (scaled by 2^8) it keeps about 8 significant bits, as the bf16
+// prefill's P does.
 //
-// Design (one persistent CTA per SM, 512 threads; work item = one (chunk, kv head) of up
+// Design (one persistent CTA per SM, 384 threads; work item = one (chunk, kv head) of up
 // to 8 tiles of 128 keys; the items of a CTA run as a software pipeline in which step s
 // handles the K tiles of item s and the V tiles of item s - 1):
-//  * warps 0, 14 and 15, producers: stream 128-key tiles of raw E4M3 bytes in step order
-//    (K tiles of item s, then V tiles of item s - 1) through a 6-stage TMA ring, each
-//    taking every third tile; lane u < 8 loads the 16-key unit u of a tile (a 16-token page, or a
-//    slice of a larger page) as one 2 KB box, 128-byte swizzled.  Page ids are read one
-//    item ahead.
-//  * warps 2-9, two converter warpgroups, both on every raw tile: E4M3 -> f16 is exact.
-//    A K tile goes into tensor memory (lanes = keys, two dims per column), where the MMA
-//    reads its A operand; a V tile goes to shared memory in the 128-byte-swizzled MN-major
-//    layout.  Keys past the chunk or in a page that was not loaded become zeros.  At each
-//    item start warpgroup 0 writes the G query rows as f16, scaled by a power of two 2^e
-//    chosen from max|q| so that they sit well inside f16's range (exact for bf16 inputs).
-//  * warp 1, MMA issuer (swap-AB, keys as M = 128, query heads padded to N = 16; with
-//    several query rows per request, column n is row n / G, head n % G):
-//      S^T_t  = K_t . (2^e Q)^T        A = K tile (K-major), B = Q (K-major)
-//      O^T   += V_t^T . P_t^T          A = V tile (MN-major), B = P^T (MN-major, smem)
-//    Every S^T tile of an item stays in tensor memory (two item regions of 8 x 16 columns)
-//    so the softmax sees the whole item at once; O^T takes 16 more columns and three K
-//    tiles 3 x 64.
-//  * warps 10-13, softmax: thread r owns key r of every tile (TMEM lane r).  Per item: one
+//  * warps 0, 2 and 3, producers: stream 128-key tiles of E4M3 bytes in step order through
+//    a 12-stage TMA ring, each taking every third tile; lane u < 8 loads the 16-key unit u
+//    of a tile (a 16-token page, or a slice of a larger page) as one 2 KB box, 128-byte
+//    swizzled: 128 rows (keys) of 128 bytes (dims).  Page ids are read one item ahead.
+//  * warp 1, MMA (lane 0 issues; swap-AB, keys as M = 128, query columns padded to N =
+//    16; with several query rows per request, column n is row n / G, head n % G):
+//      S^T_t  = K_t . (Qhi + Qlo)^T     A = raw K tile (K-major), B = Q parts (K-major)
+//      O^T   += V_t^T . (Phi + Plo)^T   A = raw V tile (MN-major), B = P^T parts (K-major)
+//    Every S^T tile of an item stays in tensor memory (two item regions of 8 x 16
+//    columns), so the softmax sees the whole item at once; O^T takes 16 more columns.
+//    Keys past the chunk and units whose page was not loaded must not reach P . V as
+//    whatever bytes the stage held (0 * NaN is NaN): before the MMAs of such a V tile the
+//    whole warp zeroes those rows.
+//  * warps 8-11, Q: per item, thread d loads dim d of the item's query rows, finds the
+//    power of two 2^e that puts max|q| into [2^7, 2^8), writes 2^e q as E4M3 hi/lo
+//    operands and records which 16-key units of the item have a valid page.
+//  * warps 4-7, softmax: thread r owns key r of every tile (TMEM lane r).  Per item: one
 //    pass over all its S^T tiles gives the exact max per column (a transposing warp
 //    butterfly and one exchange among the four warps), so no running rescale is needed;
-//    then each tile's P^T = exp2(s - max) goes to shared memory as f16 (key r's columns
-//    in one 32-byte row: the MN-major B operand) while the column sums accumulate; at the
-//    item's end thread r holds row r of O^T: divided by l, scaled by v_scale, it becomes
-//    the bf16 output (single-chunk request) or the fp32 partial and its lse.
-//  While the softmax works on item s - 1, the converter and the tensor core are already on
-//  the K tiles of item s.
+//    then each tile's P^T = 2^8 exp2(s - max) goes to shared memory as E4M3 hi/lo bytes
+//    (row = column n, byte = key) while the column sums accumulate; at the item's end
+//    thread r holds row r of O^T: divided by l, scaled by v_scale, it becomes the bf16
+//    output (single-chunk request) or the fp32 partial and its lse.
+//  While the softmax works on item s - 1, the tensor core is already on the K tiles of
+//  item s.
 #include <atomic>
 #include <climits>
 
@@ -59,56 +64,48 @@ namespace mmad {
 
 constexpr int D = HEAD_DIM;                 // 128
 constexpr int TK = 128;                     // keys per tile = the MMA's M
-constexpr int NH = 16;                      // query heads per kv head, padded = the MMA's N
+constexpr int NH = 16;                      // query columns, padded = the MMA's N
 constexpr int UNITS = TK / PAGE;            // 16-key units per tile (8)
-constexpr int RAW_STAGES = 6;
-constexpr int NKB = 3;                      // K tiles in tensor memory
-constexpr int NVB = 3;                      // converted V tiles in shared memory
+constexpr int RAW_STAGES = 12;
 constexpr int NPB = 4;                      // P^T tiles in shared memory
 constexpr int MAX_TILES = 8;                // tiles per item (chunks of at most 1024 keys)
 constexpr int RAW_BYTES = TK * D;           // 16 KB of E4M3 per K or V tile
-constexpr int CVT_BYTES = TK * D * 2;       // 32 KB of f16
-constexpr int CVT_CHUNK = TK * 128;         // one 64-column chunk of a converted tile
-constexpr int QP_BYTES = NH * D * 2;        // 4 KB: Q (16 x 128 dims) or P^T (128 keys x 16)
-constexpr int QP_CHUNK = NH * 128;          // one 64-column chunk of Q
-constexpr int PRODUCERS = 3;                // TMA producer warps (0, 14 and 15)
-constexpr int THREADS = 448 + 32 * (PRODUCERS - 1);
-constexpr int CVT_THREADS = 256;            // two converter warpgroups share every tile
-// tensor memory: S^T regions of two items (8 tiles x 16 columns each) at 0 and 128, O^T at
-// 256, and NKB K tiles as f16 (128 lanes = keys, 64 columns = 128 dims) from 288 on
+constexpr int OP_BYTES = NH * 128;          // one E4M3 operand: 16 rows x 128 bytes
+constexpr int QP_BYTES = 2 * OP_BYTES;      // its hi and lo parts
+constexpr int PRODUCERS = 3;                // TMA producer warps (0, 2 and 3)
+constexpr int W_SMX = 4;                    // softmax warps 4-7
+constexpr int W_Q = 8;                      // Q warps 8-11
+constexpr int THREADS = 12 * 32;
+constexpr float P_LOG2_SCALE = 8.f;         // P^T holds 2^8 P
+// tensor memory: S^T regions of two items (8 tiles x 16 columns each) at 0 and 128, O^T
+// at 256
 constexpr int TMEM_COLS = 512;
 constexpr int TMEM_O = 256;
-constexpr int TMEM_K = 288;
-static_assert(TMEM_K + 64 * NKB <= TMEM_COLS, "tensor memory columns");
 
 constexpr int OFF_RAW = 0;
-constexpr int OFF_VC = OFF_RAW + RAW_STAGES * RAW_BYTES;  // NVB buffers
-constexpr int OFF_Q = OFF_VC + NVB * CVT_BYTES;           // two buffers
-constexpr int OFF_P = OFF_Q + 2 * QP_BYTES;               // NPB buffers
+constexpr int OFF_Q = OFF_RAW + RAW_STAGES * RAW_BYTES;   // two buffers (hi, lo)
+constexpr int OFF_P = OFF_Q + 2 * QP_BYTES;               // NPB buffers (hi, lo)
 constexpr int OFF_RED = OFF_P + NPB * QP_BYTES;           // exchange areas (1 KB)
-constexpr int OFF_MASK = OFF_RED + 1024;  // loaded-unit bits per raw stage (<= 10 words), the
-                                          // q exponents (2 words at +40) and the per-item
-                                          // unit masks (2 x 64 bits at +48)
-constexpr int OFF_BAR = OFF_MASK + 64;
+constexpr int OFF_MASK = OFF_RED + 1024;  // loaded-unit bits per raw stage (<= 16 words),
+                                          // the q exponents (2 words at +64) and the per-item
+                                          // unit masks (2 x 64 bits at +72)
+constexpr int OFF_BAR = OFF_MASK + 96;
 
 // barrier indices
-constexpr int RAW_FULL = 0, RAW_EMPTY = RAW_FULL + RAW_STAGES, KC_FULL = RAW_EMPTY + RAW_STAGES,
-              KC_EMPTY = KC_FULL + NKB, VC_FULL = KC_EMPTY + NKB, VC_EMPTY = VC_FULL + NVB,
-              Q_FULL = VC_EMPTY + NVB, Q_EMPTY = Q_FULL + 2, S_FULL = Q_EMPTY + 2,
-              S_EMPTY = S_FULL + 2, P_FULL = S_EMPTY + 2, P_EMPTY = P_FULL + NPB,
-              PV_LAST = P_EMPTY + NPB, O_EMPTY = PV_LAST + 1, MMA_DRAIN = O_EMPTY + 1,
-              XCH_CVT = MMA_DRAIN + 1, XCH_SMX = XCH_CVT + 1, MASK_FULL = XCH_SMX + 1,
-              NUM_BARS = MASK_FULL + 2;
+constexpr int RAW_FULL = 0, RAW_EMPTY = RAW_FULL + RAW_STAGES, Q_FULL = RAW_EMPTY + RAW_STAGES,
+              Q_EMPTY = Q_FULL + 2, S_FULL = Q_EMPTY + 2, S_EMPTY = S_FULL + 2,
+              P_FULL = S_EMPTY + 2, P_EMPTY = P_FULL + NPB, PV_LAST = P_EMPTY + NPB,
+              O_EMPTY = PV_LAST + 1,
+              MMA_DRAIN = O_EMPTY + 1, XCH_Q = MMA_DRAIN + 1, XCH_SMX = XCH_Q + 1,
+              NUM_BARS = XCH_SMX + 1;
 constexpr int SMEM_BYTES = 1024 + OFF_BAR + 8 * NUM_BARS + 16;
 static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
-static_assert(RAW_STAGES <= 10, "unit-mask words");
+static_assert(RAW_STAGES <= 16, "unit-mask words");
 
-// Byte offset of element (row, col) of a 128-byte-swizzled K-major tile whose 64-column
-// chunks are chunk_bytes apart (rows of 128 bytes, 16-byte units XORed with row % 8).
-__device__ __forceinline__ uint32_t sw128_off(int row, int col, int chunk_bytes) {
-    const int unit = (col & 63) >> 3;
-    return (uint32_t)((col >> 6) * chunk_bytes + row * 128 + ((unit ^ (row & 7)) << 4) +
-                      ((col & 7) << 1));
+// Byte (row, col) of a 128-byte-swizzled K-major E4M3 operand (rows of 128 bytes, 16-byte
+// units XORed with row % 8, 8-row groups 1 KB apart).
+__device__ __forceinline__ uint32_t sw128_byte(int row, int col) {
+    return (uint32_t)(row * 128 + ((((col >> 4) ^ (row & 7))) << 4) + (col & 15));
 }
 
 // Geometry of work item `item`: request b, kv head g, chunk f (of the request's nch),
@@ -170,6 +167,18 @@ __device__ __forceinline__ Item item_of(const Params& p, long long item, Cursor&
     return it;
 }
 
+// Page id of 16-key unit u of an item (-1 past the item's keys) and whether it was loaded
+// (a page id inside the pool).  The producers and the Q warps both decide with this, so
+// the loads and the softmax's mask agree on which rows of a tile hold data.
+__device__ __forceinline__ int unit_page(const Params& p, const Item& it, int u) {
+    const int key = it.tok0 + u * PAGE;
+    if (key >= it.tok1) return -1;
+    return __ldg(p.page_table + (size_t)it.b * p.page_table_stride + key / p.page_size);
+}
+__device__ __forceinline__ bool page_ok(const Params& p, int pid) {
+    return pid >= 0 && pid < p.num_pages;
+}
+
 // Exchange of per-warp values among the four warps of a warpgroup through shared memory
 // and an mbarrier of count 4 (lane 0 of each warp writes its warp's values, then arrives),
 // with a bounded wait: a warp that has given up never leaves the others waiting forever.
@@ -212,9 +221,9 @@ __device__ __forceinline__ void load_q(const Params& p, const Item& it, int d, f
         qv[n] = n < nrows ? __bfloat162float(q[((size_t)(n / G) * Hq + n % G) * D]) : 0.f;
 }
 
-// Power-of-two exponent e for the query rows of an item: 2^e * max|q| lies in
-// [2^14, 2^15), so the scaled rows fit f16 with bf16's precision intact.  Warpgroup-wide
-// (thread d holds column d of the NR rows).
+// Power-of-two exponent e for the query rows of an item: 2^e * max|q| lies in [2^7, 2^8),
+// inside E4M3's range with room for the rounding of hi.  Warpgroup-wide (thread d holds
+// column d of the NR rows).
 template <int NR>
 __device__ __forceinline__ bool q_exponent(const float (&qv)[NR], int d, WgExchange& x,
                                            volatile int* abort_flag, int* status, int& e) {
@@ -230,17 +239,12 @@ __device__ __forceinline__ bool q_exponent(const float (&qv)[NR], int d, WgExcha
     e = 0;
     if (mm > 0.f && mm < INFINITY) {
         const int ex = ((__float_as_int(mm) >> 23) & 0xff) - 127;  // floor(log2 mm), normal
-        e = max(-100, min(100, 14 - max(ex, -126)));
+        e = max(-100, min(100, 7 - max(ex, -126)));
     }
     return true;
 }
 
 __device__ __forceinline__ float exp2i(int e) { return __int_as_float((e + 127) << 23); }
-
-__device__ __forceinline__ uint32_t half2_bits(float lo, float hi) {
-    const __half2 h = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t*>(&h);
-}
 
 // One step of a transposing butterfly over the lanes: N values per lane become N / 2, each
 // combined (max or sum) over the lane pair (lane, lane ^ OFF); the lane with bit OFF set
@@ -291,19 +295,26 @@ __device__ __forceinline__ bool wg_exchange_cols(WgExchange& x, float val, int w
     return ok;
 }
 
-// 16 E4M3 bytes -> 16 f16 (exact), as two 16-byte units
-__device__ __forceinline__ void e4m3x16_to_f16(const uint4& raw, uint4& lo, uint4& hi) {
-    uint32_t h[8];
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+// Column c of the E4M3 operand(s) for values v[0 .. NR-1], each split into hi + lo, one
+// byte per row.  Packed (NR <= 8): one operand, hi of value n in row n and lo in row 8 + n,
+// so one MMA takes both; otherwise hi in row n of the operand at op, lo in row n of the
+// one at op + OP_BYTES.
+template <int NR, bool PACK>
+__device__ __forceinline__ void store_col_e4m3(uint8_t* op, int c, const float (&v)[NR]) {
+    auto lo_at = [&](int n) -> uint32_t {
+        return PACK ? sw128_byte(n + 8, c) : (uint32_t)OP_BYTES + sw128_byte(n, c);
+    };
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
-            "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
-            : "=r"(h[2 * i]), "=r"(h[2 * i + 1])
-            : "r"(w[i]));
+    for (int n = 0; n < NR; n += 2) {
+        uint32_t h, l;
+        e4m3_split2(v[n], n + 1 < NR ? v[n + 1] : 0.f, h, l);
+        op[sw128_byte(n, c)] = (uint8_t)h;
+        op[lo_at(n)] = (uint8_t)l;
+        if (n + 1 < NR) {
+            op[sw128_byte(n + 1, c)] = (uint8_t)(h >> 8);
+            op[lo_at(n + 1)] = (uint8_t)(l >> 8);
+        }
     }
-    lo = make_uint4(h[0], h[1], h[2], h[3]);
-    hi = make_uint4(h[4], h[5], h[6], h[7]);
 }
 
 // G query heads per kv head; NR = the MMA's used N columns: G (one query row per request)
@@ -311,13 +322,19 @@ __device__ __forceinline__ void e4m3x16_to_f16(const uint4& raw, uint4& lo, uint
 template <int G, int NR>
 __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_constant__ Params p) {
     static_assert(NR == G || NR == NH, "query columns");
+    static_assert((NR <= 8) == (NR == G), "packed operands exactly for one query row");
     constexpr int XW = NR <= 8 ? 8 : 16;  // width of the softmax exchanges
+    // NR <= 8: hi and lo of Q and P^T share one operand (rows n and 8 + n), so one MMA
+    // per 32-element step covers both and S^T / O^T column 8 + n holds column n's lo part
+    constexpr bool PACK = NR <= 8;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
     const uint32_t s0 = smem_u32(smem);
     float* red = reinterpret_cast<float*>(smem + OFF_RED);
     uint32_t* unit_mask = reinterpret_cast<uint32_t*>(smem + OFF_MASK);
+    int* qe_words = reinterpret_cast<int*>(smem + OFF_MASK + 64);
+    uint32_t* km_words = reinterpret_cast<uint32_t*>(smem + OFF_MASK + 72);  // [2][2]
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -329,20 +346,12 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
     if (threadIdx.x == 0) {
         for (int s = 0; s < RAW_STAGES; ++s) {
             mbar_init(BAR(RAW_FULL + s), 1);
-            mbar_init(BAR(RAW_EMPTY + s), CVT_THREADS);
-        }
-        for (int x = 0; x < NKB; ++x) {
-            mbar_init(BAR(KC_FULL + x), CVT_THREADS);
-            mbar_init(BAR(KC_EMPTY + x), 1);
-        }
-        for (int x = 0; x < NVB; ++x) {
-            mbar_init(BAR(VC_FULL + x), CVT_THREADS);
-            mbar_init(BAR(VC_EMPTY + x), 1);
+            mbar_init(BAR(RAW_EMPTY + s), 1);  // the commit of the tile's MMAs
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(BAR(Q_FULL + x), 128);
             // released by the QK MMAs' commit and by the four softmax warps once they have
-            // read the item's q exponent and unit mask (which the converter writes with Q)
+            // read the item's q exponent and unit mask (which the Q warps write with Q)
             mbar_init(BAR(Q_EMPTY + x), 1 + 4);
             mbar_init(BAR(S_FULL + x), 1);
             mbar_init(BAR(S_EMPTY + x), 128);
@@ -354,14 +363,12 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
         mbar_init(BAR(PV_LAST), 1);
         mbar_init(BAR(O_EMPTY), 128);
         mbar_init(BAR(MMA_DRAIN), 1);
-        mbar_init(BAR(XCH_CVT), 4);
+        mbar_init(BAR(XCH_Q), 4);
         mbar_init(BAR(XCH_SMX), 4);
-        mbar_init(BAR(MASK_FULL), 1);
-        mbar_init(BAR(MASK_FULL + 1), 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
-    // Q rows and P^T columns NR..15 stay zero: clear every buffer of both once
+    // Q rows and P^T rows NR..15 stay zero: clear every buffer once
     for (int i = threadIdx.x; i < (2 + NPB) * QP_BYTES / 16; i += THREADS)
         reinterpret_cast<uint4*>(smem + OFF_Q)[i] = make_uint4(0, 0, 0, 0);
     fence_async_smem();
@@ -377,24 +384,28 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
     const int Hq = p.num_qo_heads;
     const long long n_items = (long long)__ldg(p.chunk_off + p.batch) * p.num_kv_heads;
     const long long stride = gridDim.x;
+    // every role walks the CTA's non-empty items in the same order
+    auto next_item = [&](long long from, Item& out, Cursor& pos) -> long long {
+        for (long long k = from; k < n_items; k += stride) {
+            out = item_of(p, k, pos);
+            if (out.ntiles > 0) return k;
+        }
+        return -1;
+    };
 
-    if (warp == 0 || warp >= 14) {
+    if (warp == 0 || warp == 2 || warp == 3) {
         // ------------------------------------------------------------ TMA producers
         // Producer w takes ring positions ld with ld % PRODUCERS == w: a warp issues its
         // boxes one lane after another, so several warps keep more boxes in flight.
-        const uint32_t pw = warp == 0 ? 0u : (uint32_t)(warp - 13);
+        const uint32_t pw = warp == 0 ? 0u : (uint32_t)(warp - 1);
         // step order: the K tiles of item s, then the V tiles of item s - 1.  The page ids of
         // an item (at most 64 units of 16 keys: lane l holds units l and l + 32) are read one
         // item ahead, so no page-table read waits in front of a tile's loads.
         uint32_t ld = 0;  // raw tiles issued (ring position)
         bool ok = true;
         auto read_ids = [&](const Item& it, int (&ids)[2]) {
-            const int* pt_row = p.page_table + (size_t)it.b * p.page_table_stride;
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                const int key = it.tok0 + (lane + 32 * k) * PAGE;
-                ids[k] = key < it.tok1 ? __ldg(pt_row + key / p.page_size) : -1;
-            }
+            for (int k = 0; k < 2; ++k) ids[k] = unit_page(p, it, lane + 32 * k);
         };
         auto load_tiles = [&](const Item& it, const int (&ids)[2], bool v) {
             for (int t = 0; ok && t < it.ntiles; ++t, ++ld) {
@@ -403,7 +414,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
                 const int key = it.tok0 + u * PAGE;
                 const int pid = __shfl_sync(0xffffffffu, ids[t >> 2], u & 31);
                 const bool in_use = lane < UNITS && key < it.tok1;
-                const bool valid = in_use && pid >= 0 && pid < p.num_pages;
+                const bool valid = in_use && page_ok(p, pid);
                 if (!v && in_use && !valid) atomicOr(p.status, PGQA_DEV_BOUNDS);
                 const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
                 const uint32_t st = ld % RAW_STAGES;
@@ -423,18 +434,11 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
             }
         };
         Cursor pos;
-        auto next_item = [&](long long from, Item& out) -> long long {
-            for (long long k = from; k < n_items; k += stride) {
-                out = item_of(p, k, pos);
-                if (out.ntiles > 0) return k;
-            }
-            return -1;
-        };
         Item prev, it;
         prev.ntiles = 0;
         it.ntiles = 0;
         int ids_prev[2] = {-1, -1}, ids[2] = {-1, -1};
-        long long cur = next_item(blockIdx.x, it);
+        long long cur = next_item(blockIdx.x, it, pos);
         if (cur >= 0) read_ids(it, ids);
         while (ok && cur >= 0) {
             load_tiles(it, ids, false);
@@ -443,7 +447,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
             Item ni;
             ni.ntiles = 0;
             int ids_next[2] = {-1, -1};
-            const long long nxt = ok ? next_item(cur + stride, ni) : -1;
+            const long long nxt = ok ? next_item(cur + stride, ni, pos) : -1;
             if (nxt >= 0) read_ids(ni, ids_next);
             if (ok && prev.ntiles > 0) load_tiles(prev, ids_prev, true);
             prev = it;
@@ -464,241 +468,166 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
                                       nullptr, p.status);
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t IDESC_S = idesc_f16_f32(TK, NH, false, false);
-            constexpr uint32_t IDESC_O = idesc_f16_f32(D, NH, true, true);
-            uint32_t kt = 0, vt = 0, s = 0;  // K tiles, V tiles and items so far
-            bool ok = true;
-            auto qk_tiles = [&](const Item& it) {
-                const uint32_t x = s & 1;  // Q buffer and S^T region of item s
-                ok = mbar_wait_bounded(BAR(Q_FULL + x), (s >> 1) & 1, abort_flag, p.status) &&
-                     mbar_wait_bounded(BAR(S_EMPTY + x), ((s >> 1) & 1) ^ 1, abort_flag, p.status);
-                for (int t = 0; ok && t < it.ntiles; ++t, ++kt) {
-                    const uint32_t kb = kt % NKB;
-                    ok = mbar_wait_bounded(BAR(KC_FULL + kb), (kt / NKB) & 1, abort_flag, p.status);
-                    if (!ok) break;
-                    tc_fence_after();
-                    // A = the K tile in tensor memory (lanes = keys, 2 dims per column)
-                    const uint64_t qdesc = sdesc_sw128(s0 + OFF_Q + x * QP_BYTES, 16, 1024);
+        // ------------------------------------------------------------ MMA
+        // The whole warp follows the pipeline (its waits agree through __all_sync); lane 0
+        // issues the MMAs and commits.
+        const bool issuer = lane == 0;
+        constexpr uint32_t IDESC_S = idesc_e4m3_f32(TK, NH, false);
+        constexpr uint32_t IDESC_O = idesc_e4m3_f32(D, NH, true);
+        uint32_t ld = 0, pt = 0, s = 0;  // ring position, P^T tiles, items
+        bool ok = true;
+        auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
+            return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, abort_flag, p.status));
+        };
+        auto qk_tiles = [&](const Item& it) {
+            const uint32_t x = s & 1;  // Q buffer and S^T region of item s
+            ok = wait(BAR(Q_FULL + x), (s >> 1) & 1) && wait(BAR(S_EMPTY + x), ((s >> 1) & 1) ^ 1);
+            // B = the Q parts: 16 rows (columns of S^T) of 128 dims, K-major
+            const uint64_t qh = sdesc_sw128(s0 + OFF_Q + x * QP_BYTES, 16, 1024);
+            const uint64_t ql = sdesc_sw128(s0 + OFF_Q + x * QP_BYTES + OP_BYTES, 16, 1024);
+            for (int t = 0; ok && t < it.ntiles; ++t, ++ld) {
+                const uint32_t st = ld % RAW_STAGES;
+                ok = wait(BAR(RAW_FULL + st), (ld / RAW_STAGES) & 1);
+                if (!ok) break;
+                tc_fence_after();
+                if (issuer) {
+                    // A = the raw K tile: 128 keys of 128 bytes, K-major; 32 dims per MMA
+                    const uint64_t kd = sdesc_sw128(s0 + OFF_RAW + st * RAW_BYTES, 16, 1024);
+                    const uint32_t d_tm = tmem_base + 128u * x + 16u * t;
 #pragma unroll
-                    for (int k = 0; k < D / 16; ++k)
-                        mma_ts(tmem_base + 128u * x + 16u * t, tmem_base + TMEM_K + 64u * kb + 8u * k,
-                               qdesc + (uint64_t)(((k >> 2) * QP_CHUNK + (k & 3) * 32) / 16),
-                               IDESC_S, k > 0 ? 1u : 0u);
-                    mma_commit(BAR(KC_EMPTY + kb));
-                }
-                if (ok) {
-                    mma_commit(BAR(S_FULL + x));
-                    mma_commit(BAR(Q_EMPTY + x));
-                }
-            };
-            auto pv_tiles = [&](const Item& it, uint32_t sp) {  // sp: the item's index
-                if (sp > 0)
-                    ok = mbar_wait_bounded(BAR(O_EMPTY), (sp - 1) & 1, abort_flag, p.status);
-                for (int t = 0; ok && t < it.ntiles; ++t, ++vt) {
-                    const uint32_t x = vt % NPB, xv = vt % NVB;
-                    ok = mbar_wait_bounded(BAR(P_FULL + x), (vt / NPB) & 1, abort_flag, p.status) &&
-                         mbar_wait_bounded(BAR(VC_FULL + xv), (vt / NVB) & 1, abort_flag, p.status);
-                    if (!ok) break;
-                    tc_fence_after();
-                    // A = V^T: MN-major, 64-dim chunks CVT_CHUNK apart, 8-key groups 1 KB
-                    // apart; B = P^T: MN-major with the 32-byte swizzle (the 16 columns of
-                    // a key in one 32-byte row), 8-key groups 256 bytes apart
-                    const uint64_t vdesc = sdesc_sw128(s0 + OFF_VC + xv * CVT_BYTES, CVT_CHUNK, 1024);
-                    const uint64_t pdesc = sdesc_sw32(s0 + OFF_P + x * QP_BYTES, 256, 256);
+                    for (int k = 0; k < D / 32; ++k)
+                        mma_e4m3_ss(d_tm, kd + 2u * k, qh + 2u * k, IDESC_S, k > 0 ? 1u : 0u);
+                    if constexpr (!PACK) {
 #pragma unroll
-                    for (int k = 0; k < TK / 16; ++k)
-                        mma_ss(tmem_base + TMEM_O, vdesc + (uint64_t)(k * 2048 / 16),
-                               pdesc + (uint64_t)(k * 512 / 16), IDESC_O, (t > 0 || k > 0) ? 1u : 0u);
-                    mma_commit(BAR(VC_EMPTY + xv));
-                    mma_commit(BAR(P_EMPTY + x));
+                        for (int k = 0; k < D / 32; ++k)
+                            mma_e4m3_ss(d_tm, kd + 2u * k, ql + 2u * k, IDESC_S, 1u);
+                    }
+                    mma_commit(BAR(RAW_EMPTY + st));
                 }
-                if (ok) mma_commit(BAR(PV_LAST));
-            };
-            Item prev;
-            prev.ntiles = 0;
-            Cursor pos;
-            for (long long item = blockIdx.x; ok && item < n_items; item += stride) {
-                const Item it = item_of(p, item, pos);
-                if (it.ntiles == 0) continue;
-                qk_tiles(it);
-                if (ok && prev.ntiles > 0) pv_tiles(prev, s - 1);
-                prev = it;
-                ++s;
+                __syncwarp();
             }
+            if (ok && issuer) {
+                mma_commit(BAR(S_FULL + x));
+                mma_commit(BAR(Q_EMPTY + x));
+            }
+            __syncwarp();
+        };
+        auto pv_tiles = [&](const Item& it, uint32_t sp) {  // sp: the item's index
+            if (sp > 0) ok = wait(BAR(O_EMPTY), (sp - 1) & 1);
+            for (int t = 0; ok && t < it.ntiles; ++t, ++ld, ++pt) {
+                const uint32_t st = ld % RAW_STAGES, pb = pt % NPB;
+                ok = wait(BAR(P_FULL + pb), (pt / NPB) & 1) &&
+                     wait(BAR(RAW_FULL + st), (ld / RAW_STAGES) & 1);
+                if (!ok) break;
+                // rows past the chunk and rows of units that were not loaded become zeros
+                const int nvalid = min(TK, it.tok1 - (it.tok0 + t * TK));
+                const uint32_t um = unit_mask[st] & 0xffu;
+                if (nvalid < TK || um != 0xffu) {
+                    uint8_t* raw = smem + OFF_RAW + st * RAW_BYTES;
+                    for (int i = lane; i < TK * 8; i += 32) {  // 16-byte pieces, 8 per row
+                        const int row = i >> 3;
+                        if (row >= nvalid || !((um >> (row >> 4)) & 1u))
+                            reinterpret_cast<uint4*>(raw + row * 128)[i & 7] = make_uint4(0, 0, 0, 0);
+                    }
+                    fence_async_smem();
+                    __syncwarp();
+                }
+                tc_fence_after();
+                if (issuer) {
+                    // A = V^T: the raw V tile read MN-major (a key's 128 dims are one
+                    // 128-byte row, 8-key groups 1 KB apart; 32 keys per MMA); B = the P^T
+                    // parts: 16 rows (columns) of 128 keys, K-major
+                    const uint64_t vd = sdesc_sw128(s0 + OFF_RAW + st * RAW_BYTES, RAW_BYTES, 1024);
+                    const uint64_t ph = sdesc_sw128(s0 + OFF_P + pb * QP_BYTES, 16, 1024);
+                    const uint64_t pl = sdesc_sw128(s0 + OFF_P + pb * QP_BYTES + OP_BYTES, 16, 1024);
+#pragma unroll
+                    for (int k = 0; k < TK / 32; ++k)
+                        mma_e4m3_ss(tmem_base + TMEM_O, vd + 256u * k, ph + 2u * k, IDESC_O,
+                                    (t > 0 || k > 0) ? 1u : 0u);
+                    if constexpr (!PACK) {
+#pragma unroll
+                        for (int k = 0; k < TK / 32; ++k)
+                            mma_e4m3_ss(tmem_base + TMEM_O, vd + 256u * k, pl + 2u * k, IDESC_O,
+                                        1u);
+                    }
+                    mma_commit(BAR(RAW_EMPTY + st));
+                    mma_commit(BAR(P_EMPTY + pb));
+                }
+                __syncwarp();
+            }
+            if (ok && issuer) mma_commit(BAR(PV_LAST));
+            __syncwarp();
+        };
+        Item prev;
+        prev.ntiles = 0;
+        Cursor pos;
+        for (long long item = blockIdx.x; ok && item < n_items; item += stride) {
+            const Item it = item_of(p, item, pos);
+            if (it.ntiles == 0) continue;
+            qk_tiles(it);
             if (ok && prev.ntiles > 0) pv_tiles(prev, s - 1);
-            // every MMA issued has completed before tensor memory is released
+            prev = it;
+            ++s;
+        }
+        if (ok && prev.ntiles > 0) pv_tiles(prev, s - 1);
+        // every MMA issued has completed before tensor memory is released
+        if (issuer) {
             mma_commit(BAR(MMA_DRAIN));
             mbar_wait_bounded(BAR(MMA_DRAIN), 0, nullptr, p.status);
         }
-    } else if (warp >= 2 && warp < 10) {
-        // ------------------------------------------------------------ converters
-        // Both warpgroups work on every raw tile.  A K tile goes to tensor memory: the warp
-        // of lane quarter q (warp % 4) and half c (its warpgroup) converts keys 32q .. 32q+31,
-        // dims 64c .. 64c+63 (thread = key = TMEM lane).  A V tile goes to shared memory in
-        // the swizzled MN-major layout, 4 of its 1024 16-byte segments per thread.
-        // Warpgroup 0 also writes each item's Q and records its loaded units.
-        const int cid = (warp - 2) >> 2;
-        const int j = threadIdx.x - 64;          // 0..255 over both warpgroups
-        const int i = j - 128 * cid;             // 0..127 within the warpgroup
-        const int q4 = warp & 3;                 // TMEM lane quarter of this warp
-        const int krow = 32 * q4 + lane;         // key row this thread converts in K tiles
-        WgExchange xch{BAR(XCH_CVT), red, 0};
-        int* qe = reinterpret_cast<int*>(smem + OFF_MASK + 40);
-        unsigned long long* kmask = reinterpret_cast<unsigned long long*>(smem + OFF_MASK + 48);
-        uint32_t cv = 0, kt = 0, vt = 0, s = 0;
+        __syncwarp();
+    } else if (warp >= W_Q && warp < W_Q + 4) {
+        // ------------------------------------------------------------ Q
+        // Per item: its query rows, scaled by 2^e, as the E4M3 hi/lo B operand of Q . K^T
+        // (row n = column n of S^T, byte d = dim d, written by thread d), and its loaded
+        // units (one bit per 16-key unit, for the softmax's mask).
+        const int d = threadIdx.x - 32 * W_Q;  // 0..127
+        const int wq = warp - W_Q;
+        WgExchange xch{BAR(XCH_Q), red, 0};
+        uint32_t s = 0;
         bool ok = true;
-        // raw tiles arrive with the 128-byte swizzle: 16-byte unit u of row r sits at unit
-        // u ^ (r % 8); rows past nvalid and rows of units that were not loaded become zeros
-        auto raw_unit = [&](uint32_t raw, int row, int u, bool use) -> uint4 {
-            uint4 r = make_uint4(0, 0, 0, 0);
-            if (use)
-                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                             : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                             : "r"(raw + row * 128 + ((u ^ (row & 7)) << 4)));
-            return r;
-        };
-        auto wait_raw = [&]() -> uint32_t {
-            const uint32_t st = cv % RAW_STAGES;
-            ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(RAW_FULL + st), (cv / RAW_STAGES) & 1,
-                                                           abort_flag, p.status));
-            return st;
-        };
-        // Q of item s (from query rows already in registers), then its K tiles
-        auto k_tiles = [&](const Item& it, const float (&qv)[NR]) {
-            const uint32_t qb = s & 1;
-            if (cid == 0) {
-                ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(Q_EMPTY + qb),
-                                                               ((s >> 1) & 1) ^ 1, abort_flag,
-                                                               p.status));
-                if (!ok) return;
-                int e;
-                ok = q_exponent<NR>(qv, i, xch, abort_flag, p.status, e);
-                if (!ok) return;
-                const float sc = exp2i(e);
-                uint8_t* qs = smem + OFF_Q + qb * QP_BYTES;
-#pragma unroll
-                for (int n = 0; n < NR; ++n)
-                    *reinterpret_cast<__half*>(qs + sw128_off(n, i, QP_CHUNK)) =
-                        __float2half_rn(qv[n] * sc);
-                if (i == 0) qe[qb] = e;
-                fence_async_smem();
-                mbar_arrive(BAR(Q_FULL + qb));
-            }
-            unsigned long long bits = 0;  // loaded units of every tile (8 bits per tile)
-            for (int t = 0; ok && t < it.ntiles; ++t, ++kt, ++cv) {
-                const uint32_t st = wait_raw();
-                const uint32_t kb = kt % NKB;
-                if (ok)
-                    ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(KC_EMPTY + kb),
-                                                                   ((kt / NKB) & 1) ^ 1, abort_flag,
-                                                                   p.status));
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t um = unit_mask[st];
-                bits |= (unsigned long long)(um & 0xffu) << (8 * t);
-                const int nvalid = min(TK, it.tok1 - (it.tok0 + t * TK));
-                const bool use = krow < nvalid && ((um >> (krow >> 4)) & 1u);
-                const uint32_t raw = s0 + OFF_RAW + st * RAW_BYTES;
-                uint4 rv[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) rv[u] = raw_unit(raw, krow, 4 * cid + u, use);
-                uint32_t f[32];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    uint4 lo, hi;
-                    e4m3x16_to_f16(rv[u], lo, hi);
-                    f[8 * u + 0] = lo.x; f[8 * u + 1] = lo.y; f[8 * u + 2] = lo.z; f[8 * u + 3] = lo.w;
-                    f[8 * u + 4] = hi.x; f[8 * u + 5] = hi.y; f[8 * u + 6] = hi.z; f[8 * u + 7] = hi.w;
-                }
-                tmem_st32(tmem_base + ((uint32_t)(32 * q4) << 16) + TMEM_K + 64u * kb + 32u * cid, f);
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(BAR(KC_FULL + kb));
-                mbar_arrive(BAR(RAW_EMPTY + st));
-            }
-            if (ok && j == 0) {
-                kmask[qb] = bits;
-                mbar_arrive(BAR(MASK_FULL + qb));
-            }
-        };
-        auto v_tiles = [&](const Item& it) {
-            for (int t = 0; ok && t < it.ntiles; ++t, ++vt, ++cv) {
-                const uint32_t st = wait_raw();
-                const uint32_t x = vt % NVB;
-                if (ok)
-                    ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(VC_EMPTY + x),
-                                                                   ((vt / NVB) & 1) ^ 1, abort_flag,
-                                                                   p.status));
-                if (!ok) break;
-                const uint32_t um = unit_mask[st];
-                const int nvalid = min(TK, it.tok1 - (it.tok0 + t * TK));
-                const uint32_t raw = s0 + OFF_RAW + st * RAW_BYTES;
-                const uint32_t dst = s0 + OFF_VC + x * CVT_BYTES;
-                uint4 rv[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {  // all loads first
-                    const int lin = k * CVT_THREADS + j;
-                    const int row = lin >> 3, seg = lin & 7;  // 16 bytes = 16 dims of one key
-                    rv[k] = raw_unit(raw, row, seg, row < nvalid && ((um >> (row >> 4)) & 1u));
-                }
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int lin = k * CVT_THREADS + j;
-                    const int row = lin >> 3, seg = lin & 7;
-                    uint4 lo, hi;
-                    e4m3x16_to_f16(rv[k], lo, hi);
-                    const uint32_t a0 = dst + sw128_off(row, seg * 16, CVT_CHUNK);
-                    const uint32_t a1 = dst + sw128_off(row, seg * 16 + 8, CVT_CHUNK);
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a0), "r"(lo.x),
-                                 "r"(lo.y), "r"(lo.z), "r"(lo.w)
-                                 : "memory");
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a1), "r"(hi.x),
-                                 "r"(hi.y), "r"(hi.z), "r"(hi.w)
-                                 : "memory");
-                }
-                fence_async_smem();
-                mbar_arrive(BAR(VC_FULL + x));
-                mbar_arrive(BAR(RAW_EMPTY + st));
-            }
-        };
         Cursor pos;
-        auto next_item = [&](long long from, Item& out) -> long long {
-            for (long long k = from; k < n_items; k += stride) {
-                out = item_of(p, k, pos);
-                if (out.ntiles > 0) return k;
-            }
-            return -1;
-        };
         Item it;
         it.ntiles = 0;
-        long long cur = next_item(blockIdx.x, it);
+        long long cur = next_item(blockIdx.x, it, pos);
         float qv[NR];
 #pragma unroll
         for (int n = 0; n < NR; ++n) qv[n] = 0.f;
-        if (cur >= 0 && cid == 0) load_q<G, NR>(p, it, i, qv);
-        Item prev;
-        prev.ntiles = 0;
+        if (cur >= 0) load_q<G, NR>(p, it, d, qv);
         while (ok && cur >= 0) {
             Item ni;
             ni.ntiles = 0;
-            const long long nxt = next_item(cur + stride, ni);
-            float qn[NR];  // the next item's query rows, loaded while this one converts
+            const long long nxt = next_item(cur + stride, ni, pos);
+            float qn[NR];  // the next item's query rows, loaded while this one is written
 #pragma unroll
             for (int n = 0; n < NR; ++n) qn[n] = 0.f;
-            if (nxt >= 0 && cid == 0) load_q<G, NR>(p, ni, i, qn);
-            k_tiles(it, qv);
-            if (ok && prev.ntiles > 0) v_tiles(prev);
-            prev = it;
+            if (nxt >= 0) load_q<G, NR>(p, ni, d, qn);
+            // unit d < 64 of the item: loaded or not (warps 0 and 1 of the group)
+            uint32_t bits = 0;
+            if (wq < 2) bits = __ballot_sync(0xffffffffu, page_ok(p, unit_page(p, it, d)));
+            const uint32_t x = s & 1;
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(Q_EMPTY + x), ((s >> 1) & 1) ^ 1,
+                                                           abort_flag, p.status));
+            if (!ok) break;
+            int e;
+            ok = q_exponent<NR>(qv, d, xch, abort_flag, p.status, e);
+            if (!ok) break;
+            const float sc = exp2i(e);
+            float v[NR];
+#pragma unroll
+            for (int n = 0; n < NR; ++n) v[n] = qv[n] * sc;
+            store_col_e4m3<NR, PACK>(smem + OFF_Q + x * QP_BYTES, d, v);
+            if (d == 0) qe_words[x] = e;
+            if (wq < 2 && lane == 0) km_words[2 * x + wq] = bits;
+            fence_async_smem();
+            mbar_arrive(BAR(Q_FULL + x));
             it = ni;
             ++s;
             cur = nxt;
 #pragma unroll
             for (int n = 0; n < NR; ++n) qv[n] = qn[n];
         }
-        if (ok && prev.ntiles > 0) v_tiles(prev);
-    } else if (warp >= 10) {
+    } else if (warp >= W_SMX && warp < W_SMX + 4) {
         // ------------------------------------------------------------ softmax / epilogue
         // Per item s: (A) its S^T tiles and exact max; (B) the epilogue of item s - 1, whose
         // last P.V completes while (A) runs; (C) its P^T tiles and column sums.  Column n
@@ -706,19 +635,15 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
         // the item's scores stay in registers between (A) and (C); with 16 columns (several
         // query rows) (C) reads them from tensor memory a second time.  Column maxima and
         // sums are reduced over a warp by a transposing butterfly and over the four warps
-        // through shared memory; lane n < NR then keeps column n's max and sum.
+        // through shared memory; lane n < NR then keeps column n's max and sum.  P^T holds
+        // 2^8 exp2(s - max), so the sums l carry the same factor, which 1/l cancels and
+        // the lse takes out.
         const int w4 = warp & 3;                                // TMEM lane quarter
         const int r = 32 * w4 + lane;                           // key of a tile = TMEM lane
         const uint32_t lane_base = (uint32_t)(32 * w4) << 16;
         WgExchange xch{BAR(XCH_SMX), red + 64, 0};
-        const int* qe = reinterpret_cast<const int*>(smem + OFF_MASK + 40);
-        const unsigned long long* kmask =
-            reinterpret_cast<const unsigned long long*>(smem + OFF_MASK + 48);
+        const unsigned long long* kmask = reinterpret_cast<const unsigned long long*>(km_words);
         __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.o);
-        // key r's 16 columns in a P^T buffer (MN-major, 32-byte swizzle): 8-key atoms of
-        // 256 bytes, 32 bytes per key, 16-byte unit u at u ^ ((r >> 2) & 1)
-        const uint32_t p_row = (uint32_t)((r >> 3) * 256 + (r & 7) * 32);
-        const uint32_t p_sw = (uint32_t)(((r >> 2) & 1) << 4);
         const int cl = lane < NR ? lane : 0;                    // this lane's column
         uint32_t pt = 0, s = 0;  // P^T tiles written, items
         bool ok = true;
@@ -732,12 +657,12 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
             if (!ok) return;
             tc_fence_after();
             float ov[NR];  // thread r: column r of O, every query column
-            if constexpr (NR <= 8) {
-                uint32_t v[8];
-                tmem_ld8(tmem_base + lane_base + TMEM_O, v);
-                tmem_wait_ld8(v);
+            if constexpr (PACK) {  // hi part + lo part
+                uint32_t v[16];
+                tmem_ld16(tmem_base + lane_base + TMEM_O, v);
+                tmem_wait_ld16(v);
 #pragma unroll
-                for (int n = 0; n < NR; ++n) ov[n] = __uint_as_float(v[n]);
+                for (int n = 0; n < NR; ++n) ov[n] = __uint_as_float(v[n]) + __uint_as_float(v[8 + n]);
             } else {
                 uint32_t v[16];
                 tmem_ld16(tmem_base + lane_base + TMEM_O, v);
@@ -749,7 +674,8 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
             mbar_arrive(BAR(O_EMPTY));
             // lane n < NR: column n's output scale and lse
             const float inv_c = l_c > 0.f ? p.v_scale / l_c : 0.f;
-            const float lse_c = l_c > 0.f ? (m_c + log2f(l_c)) * 0.69314718055994531f : -INFINITY;
+            const float lse_c = l_c > 0.f ? (m_c - P_LOG2_SCALE + log2f(l_c)) * 0.69314718055994531f
+                                          : -INFINITY;
             const int nrows = it.qo * G;
 #pragma unroll
             for (int n = 0; n < NR; ++n) {
@@ -769,28 +695,6 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
                     if (p.lse) p.lse[(size_t)(it.q0 + qi) * Hq + hq] = lse_c;
                 } else {
                     p.part_lse[((size_t)it.f * p.max_qo + qi) * Hq + hq] = lse_c;
-                }
-            }
-        };
-        // P^T values of key r for the NR columns, as f16, into P^T buffer pp (columns past
-        // NR keep the zeros written at start-up)
-        auto store_p = [&](uint8_t* pp, const float (&pv)[NR]) {
-            uint8_t* row = pp + p_row;
-            if constexpr (NR == 1) {
-                *reinterpret_cast<__half*>(row + p_sw) = __float2half_rn(pv[0]);
-            } else {
-                uint32_t h[NR / 2];
-#pragma unroll
-                for (int i = 0; i < NR / 2; ++i) h[i] = half2_bits(pv[2 * i], pv[2 * i + 1]);
-                if constexpr (NR == 2) {
-                    *reinterpret_cast<uint32_t*>(row + p_sw) = h[0];
-                } else if constexpr (NR == 4) {
-                    *reinterpret_cast<uint2*>(row + p_sw) = make_uint2(h[0], h[1]);
-                } else {
-                    *reinterpret_cast<uint4*>(row + p_sw) = make_uint4(h[0], h[1], h[2], h[3]);
-                    if constexpr (NR == 16)
-                        *reinterpret_cast<uint4*>(row + (p_sw ^ 16u)) =
-                            make_uint4(h[4], h[5], h[6], h[7]);
                 }
             }
         };
@@ -814,16 +718,13 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
             ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(Q_FULL + x), (s >> 1) & 1,
                                                            abort_flag, p.status));
             if (ok)
-                ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(MASK_FULL + x), (s >> 1) & 1,
-                                                               abort_flag, p.status));
-            if (ok)
                 ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(S_FULL + x), (s >> 1) & 1,
                                                                abort_flag, p.status));
             if (!ok) break;
-            const float c_eff = p.scale_log2 * exp2i(-qe[x]);  // score units: log2, all scales
+            const float c_eff = p.scale_log2 * exp2i(-qe_words[x]);  // score units: log2
             const unsigned long long km = kmask[x];
-            // the converter may now write the next item of this Q buffer: without this
-            // arrival it could complete Q_FULL / MASK_FULL twice before a slow softmax waits
+            // the Q warps may now write the next item of this Q buffer: without this
+            // arrival they could complete Q_FULL twice before a slow softmax waits
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(Q_EMPTY + x));
             const uint32_t s_base = tmem_base + lane_base + 128u * x;
@@ -846,12 +747,13 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
                 for (int t = 0; t < MAX_TILES; ++t) {
                     const bool valid = t < it.ntiles && vis_mask(t) != 0u;
                     if (t < it.ntiles) {
-                        uint32_t u[8];
-                        tmem_ld8(s_base + 16u * t, u);
-                        tmem_wait_ld8(u);
+                        uint32_t u[16];  // column n: the hi part, column 8 + n: the lo part
+                        tmem_ld16(s_base + 16u * t, u);
+                        tmem_wait_ld16(u);
 #pragma unroll
                         for (int n = 0; n < NR; ++n)
-                            sv[t][n] = valid ? __uint_as_float(u[n]) * c_eff : -INFINITY;
+                            sv[t][n] = valid ? (__uint_as_float(u[n]) + __uint_as_float(u[8 + n])) * c_eff
+                                             : -INFINITY;
                     } else {
 #pragma unroll
                         for (int n = 0; n < NR; ++n) sv[t][n] = -INFINITY;
@@ -889,11 +791,11 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
             const float* rt;  // [warp][column]
             ok = wg_exchange_cols<NR, XW>(xch, mx[0], w4, lane, abort_flag, p.status, rt);
             if (!ok) break;
-            float neg[NR];
+            float neg[NR];  // exp2 offset of column n: 8 - max (P^T = 2^8 exp2(s - max))
 #pragma unroll
             for (int n = 0; n < NR; ++n) {
                 const float m = fmaxf(fmaxf(rt[n], rt[XW + n]), fmaxf(rt[2 * XW + n], rt[3 * XW + n]));
-                neg[n] = m == -INFINITY ? 0.f : -m;
+                neg[n] = (m == -INFINITY ? 0.f : -m) + P_LOG2_SCALE;
             }
             const float m_c =
                 fmaxf(fmaxf(rt[cl], rt[XW + cl]), fmaxf(rt[2 * XW + cl], rt[3 * XW + cl]));
@@ -902,7 +804,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
                 epilogue(prev, s - 1, prev_m, prev_l);
                 if (!ok) break;
             }
-            // (C) P^T tiles, f16, into the ring of NPB buffers the P.V MMAs read
+            // (C) P^T tiles, E4M3 hi/lo, into the ring of NPB buffers the P.V MMAs read
             float l[NR];
 #pragma unroll
             for (int n = 0; n < NR; ++n) l[n] = 0.f;
@@ -933,7 +835,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
                                                                ((pt / NPB) & 1) ^ 1, abort_flag,
                                                                p.status));
                 if (!ok) break;
-                store_p(smem + OFF_P + pb * QP_BYTES, pv);
+                store_col_e4m3<NR, PACK>(smem + OFF_P + pb * QP_BYTES, r, pv);
                 fence_async_smem();
                 mbar_arrive(BAR(P_FULL + pb));
             }

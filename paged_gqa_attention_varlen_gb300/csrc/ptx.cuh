@@ -126,9 +126,6 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map
 __device__ __forceinline__ void tensormap_acquire(const CUtensorMap* map) {
     asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
 }
-__device__ __forceinline__ void tensormap_prefetch(const CUtensorMap* map) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
-}
 // Patch the global extent of dimension `dim` of a tensor map held in shared memory.
 template <int DIM>
 __device__ __forceinline__ void tensormap_set_dim_smem(uint32_t smem_map, uint32_t extent) {
@@ -145,16 +142,6 @@ __device__ __forceinline__ void tensormap_publish(CUtensorMap* gmem_map, uint32_
         " [%0], [%1], 128;" ::"l"(gmem_map),
         "r"(smem_map)
         : "memory");
-}
-
-// Warpgroup register re-split (all 128 threads of a warpgroup execute it).
-template <int N>
-__device__ __forceinline__ void regs_dealloc() {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <int N>
-__device__ __forceinline__ void regs_alloc() {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // make this thread's generic-proxy shared-memory accesses visible / ordered before later
@@ -207,6 +194,16 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// D[tmem] (+)= A[smem] * B[smem]^T, E4M3 inputs (kind::f8f6f4, 32 elements of K per
+// instruction), fp32 accumulate.
+__device__ __forceinline__ void mma_e4m3_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 // Arrive once on `bar` when every tcgen05 op this thread issued so far has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile(
@@ -247,19 +244,7 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         : "memory");
 }
 
-// 32 lanes x 8 consecutive 32-bit columns: thread i of the warp gets lane (base + i).
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
-                   "=r"(r[6]), "=r"(r[7])
-                 : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
-                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
-                 "r"(r[7])
-                 : "memory");
-}
+// Wait for this thread's tcgen05.ld results; naming the registers keeps their uses after it.
 __device__ __forceinline__ void tmem_wait_ld32(uint32_t (&r)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;"
                  : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
@@ -288,15 +273,6 @@ __device__ __forceinline__ void tmem_wait_ld16(uint32_t (&r)[16]) {
                  :
                  : "memory");
 }
-// Wait for this thread's tcgen05.ld results; naming the registers keeps their uses after it.
-__device__ __forceinline__ void tmem_wait_ld8(uint32_t (&r)[8]) {
-    asm volatile("tcgen05.wait::ld.sync.aligned;"
-                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
-                   "+r"(r[6]), "+r"(r[7])
-                 :
-                 : "memory");
-}
-
 // Shared-memory matrix descriptor for tcgen05.mma, 128-byte swizzle (the layout a TMA
 // load with CU_TENSOR_MAP_SWIZZLE_128B writes): start address, leading- and
 // stride-dimension byte offsets (16-byte units), descriptor version 1, swizzle mode 2.
@@ -306,14 +282,6 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
            ((uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
-// The same with the 32-byte swizzle (swizzle mode 6): atoms of 8 rows x 32 bytes, the
-// 16-byte unit u of row r at unit u ^ ((r >> 2) & 1).
-__device__ __forceinline__ uint64_t sdesc_sw32(uint32_t saddr, uint32_t lbo_bytes,
-                                               uint32_t sbo_bytes) {
-    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16) |
-           ((uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (6ull << 61);
-}
-
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 D, dense.
 //   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format (1 = bf16),
 //   bit 15 A major (0 = K), bit 16 B major (1 = MN), 17-22 N >> 3, 24-28 M >> 4.
@@ -321,11 +289,26 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_ma
     return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
-// The same with f16 A and B (format 0), and A's major-ness selectable (bit 15).
-__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool a_mn_major,
-                                                     bool b_mn_major) {
-    return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
-           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+// Instruction descriptor, kind::f8f6f4: E4M3 A and B (format 0), fp32 D, dense; B K-major,
+// A K-major or MN-major (bit 15).  Same field positions as kind::f16.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, bool a_mn_major) {
+    return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
+// Two floats as E4M3 pairs hi + lo: hi = E4M3(x), lo = E4M3(x - hi) with x rounded to f16
+// first (the difference is exact in f16).  hi + lo carries about 8 significant bits, and
+// every bf16 value in [2^-2, 448) exactly.  Byte 0 holds a's part, byte 1 b's.
+__device__ __forceinline__ void e4m3_split2(float a, float b, uint32_t& hi, uint32_t& lo) {
+    uint16_t h, l;
+    uint32_t hf, xf, rf;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(h) : "f"(b), "f"(a));
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hf) : "h"(h));
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(xf) : "f"(b), "f"(a));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(rf) : "r"(xf), "r"(hf));
+    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(l) : "r"(rf));
+    hi = h;
+    lo = l;
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {
