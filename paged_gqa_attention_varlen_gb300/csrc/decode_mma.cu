@@ -89,7 +89,8 @@ constexpr int OFF_RED = OFF_P + NPB * QP_BYTES;           // exchange areas (1 K
 constexpr int OFF_MASK = OFF_RED + 1024;  // loaded-unit bits per raw stage (<= 16 words),
                                           // the q exponents (2 words at +64) and the per-item
                                           // unit masks (2 x 64 bits at +72)
-constexpr int OFF_BAR = OFF_MASK + 96;
+constexpr int OFF_ITEM = OFF_MASK + 96;   // the geometry of the items in the two Q buffers
+constexpr int OFF_BAR = OFF_ITEM + 128;
 
 // barrier indices
 constexpr int RAW_FULL = 0, RAW_EMPTY = RAW_FULL + RAW_STAGES, Q_FULL = RAW_EMPTY + RAW_STAGES,
@@ -335,6 +336,9 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
     uint32_t* unit_mask = reinterpret_cast<uint32_t*>(smem + OFF_MASK);
     int* qe_words = reinterpret_cast<int*>(smem + OFF_MASK + 64);
     uint32_t* km_words = reinterpret_cast<uint32_t*>(smem + OFF_MASK + 72);  // [2][2]
+    // item s's geometry in slot s & 1, written by the Q warps with its Q; ntiles < 0 marks
+    // the end of the CTA's items
+    Item* items = reinterpret_cast<Item*>(smem + OFF_ITEM);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -479,9 +483,9 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
         auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
             return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, abort_flag, p.status));
         };
-        auto qk_tiles = [&](const Item& it) {
+        auto qk_tiles = [&](const Item& it) {  // after Q_FULL of item s
             const uint32_t x = s & 1;  // Q buffer and S^T region of item s
-            ok = wait(BAR(Q_FULL + x), (s >> 1) & 1) && wait(BAR(S_EMPTY + x), ((s >> 1) & 1) ^ 1);
+            ok = wait(BAR(S_EMPTY + x), ((s >> 1) & 1) ^ 1);
             // B = the Q parts: 16 rows (columns of S^T) of 128 dims, K-major
             const uint64_t qh = sdesc_sw128(s0 + OFF_Q + x * QP_BYTES, 16, 1024);
             const uint64_t ql = sdesc_sw128(s0 + OFF_Q + x * QP_BYTES + OP_BYTES, 16, 1024);
@@ -560,10 +564,11 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
         };
         Item prev;
         prev.ntiles = 0;
-        Cursor pos;
-        for (long long item = blockIdx.x; ok && item < n_items; item += stride) {
-            const Item it = item_of(p, item, pos);
-            if (it.ntiles == 0) continue;
+        while (ok) {
+            ok = wait(BAR(Q_FULL + (s & 1)), (s >> 1) & 1);
+            if (!ok) break;
+            const Item it = items[s & 1];
+            if (it.ntiles < 0) break;
             qk_tiles(it);
             if (ok && prev.ntiles > 0) pv_tiles(prev, s - 1);
             prev = it;
@@ -587,9 +592,26 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
         uint32_t s = 0;
         bool ok = true;
         Cursor pos;
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.o);
+        // the next item with keys; items passed over write their rows here: zeros and
+        // lse = -inf for a request of a single empty chunk, nothing for one without rows
+        auto next_q = [&](long long from, Item& nx) -> long long {
+            for (long long k = from; k < n_items; k += stride) {
+                nx = item_of(p, k, pos);
+                if (nx.ntiles > 0) return k;
+                const int nrows = nx.nch == 1 ? nx.qo * G : 0;
+                for (int k2 = d; k2 < nrows * (D / 8); k2 += 128) {
+                    const int n = k2 / (D / 8), c = k2 % (D / 8);
+                    const size_t row = (size_t)(nx.q0 + n / G) * Hq + nx.g * G + n % G;
+                    reinterpret_cast<uint4*>(out + row * D)[c] = make_uint4(0, 0, 0, 0);
+                    if (c == 0 && p.lse) p.lse[row] = -INFINITY;
+                }
+            }
+            return -1;
+        };
         Item it;
         it.ntiles = 0;
-        long long cur = next_item(blockIdx.x, it, pos);
+        long long cur = next_q(blockIdx.x, it);
         float qv[NR];
 #pragma unroll
         for (int n = 0; n < NR; ++n) qv[n] = 0.f;
@@ -597,7 +619,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
         while (ok && cur >= 0) {
             Item ni;
             ni.ntiles = 0;
-            const long long nxt = next_item(cur + stride, ni, pos);
+            const long long nxt = next_q(cur + stride, ni);
             float qn[NR];  // the next item's query rows, loaded while this one is written
 #pragma unroll
             for (int n = 0; n < NR; ++n) qn[n] = 0.f;
@@ -617,7 +639,10 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
 #pragma unroll
             for (int n = 0; n < NR; ++n) v[n] = qv[n] * sc;
             store_col_e4m3<NR, PACK>(smem + OFF_Q + x * QP_BYTES, d, v);
-            if (d == 0) qe_words[x] = e;
+            if (d == 0) {
+                qe_words[x] = e;
+                items[x] = it;
+            }
             if (wq < 2 && lane == 0) km_words[2 * x + wq] = bits;
             fence_async_smem();
             mbar_arrive(BAR(Q_FULL + x));
@@ -626,6 +651,16 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
             cur = nxt;
 #pragma unroll
             for (int n = 0; n < NR; ++n) qv[n] = qn[n];
+        }
+        // the end of the CTA's items, in the next slot once it is free
+        if (ok) {
+            const uint32_t x = s & 1;
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(Q_EMPTY + x), ((s >> 1) & 1) ^ 1,
+                                                           abort_flag, p.status));
+            if (ok) {
+                if (d == 0) items[x].ntiles = -1;
+                mbar_arrive(BAR(Q_FULL + x));
+            }
         }
     } else if (warp >= W_SMX && warp < W_SMX + 4) {
         // ------------------------------------------------------------ softmax / epilogue
@@ -698,28 +733,17 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
                 }
             }
         };
-        Cursor pos;
-        for (long long item = blockIdx.x; ok && item < n_items; item += stride) {
-            const Item it = item_of(p, item, pos);
-            if (it.ntiles == 0) {
-                // no keys: zeros and lse = -inf (a request of a single empty chunk); an item
-                // without query rows writes nothing
-                const int nrows = it.nch == 1 ? it.qo * G : 0;
-                for (int k = r; k < nrows * (D / 8); k += 128) {
-                    const int n = k / (D / 8), c = k % (D / 8);
-                    const size_t row = (size_t)(it.q0 + n / G) * Hq + it.g * G + n % G;
-                    reinterpret_cast<uint4*>(out + row * D)[c] = make_uint4(0, 0, 0, 0);
-                    if (c == 0 && p.lse) p.lse[row] = -INFINITY;
-                }
-                continue;
-            }
-            // (A) the scale of the item's query rows and its loaded units, then its scores
+        while (ok) {
+            // (A) the item (published with its Q), the scale of its query rows and its
+            // loaded units, then its scores
             const uint32_t x = s & 1;
             ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(Q_FULL + x), (s >> 1) & 1,
                                                            abort_flag, p.status));
-            if (ok)
-                ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(S_FULL + x), (s >> 1) & 1,
-                                                               abort_flag, p.status));
+            if (!ok) break;
+            const Item it = items[x];
+            if (it.ntiles < 0) break;
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(S_FULL + x), (s >> 1) & 1,
+                                                           abort_flag, p.status));
             if (!ok) break;
             const float c_eff = p.scale_log2 * exp2i(-qe_words[x]);  // score units: log2
             const unsigned long long km = kmask[x];
