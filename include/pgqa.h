@@ -237,6 +237,11 @@ int pgqa_paged_decode_bf16_strided(const void* q, const void* k_pages, const voi
  * so one float scale per tensor is taken (flashinfer "FP8 GEMM: Per-tensor and groupwise
  * scaling" lists per-tensor scaling as one of its FP8 modes).
  *
+ * Arithmetic: the products run on the tensor cores with E4M3 operands; q (scaled by a power
+ * of two) and the softmax weights enter as sums of two E4M3 values (q exactly down to about
+ * 2^-9 of its largest element, the weights to about 8 significant bits, as a bf16 P), with
+ * fp32 accumulation.  Results are within the tolerance of the other entry points.
+ *
  * Supported: head_dim 128; page_size 16, 32, 64 or 128; G in {1,2,4,8}.  Errors as for
  * pgqa_paged_decode_bf16; a NaN or infinite scale is PGQA_ERR_INVALID_ARG.
  */

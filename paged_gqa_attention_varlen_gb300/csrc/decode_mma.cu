@@ -32,15 +32,15 @@
 //    a 12-stage TMA ring, each taking every third tile; lane u < 8 loads the 16-key unit u
 //    of a tile (a 16-token page, or a slice of a larger page) as one 2 KB box, 128-byte
 //    swizzled: 128 rows (keys) of 128 bytes (dims).  Page ids are read one item ahead.
-//  * warp 1, MMA (lane 0 issues; swap-AB, keys as M = 128, query columns padded to N =
+//  * warp 1, lane 0: MMA issuer (swap-AB, keys as M = 128, query columns padded to N =
 //    16; with several query rows per request, column n is row n / G, head n % G):
 //      S^T_t  = K_t . (Qhi + Qlo)^T     A = raw K tile (K-major), B = Q parts (K-major)
 //      O^T   += V_t^T . (Phi + Plo)^T   A = raw V tile (MN-major), B = P^T parts (K-major)
 //    Every S^T tile of an item stays in tensor memory (two item regions of 8 x 16
 //    columns), so the softmax sees the whole item at once; O^T takes 16 more columns.
 //    Keys past the chunk and units whose page was not loaded must not reach P . V as
-//    whatever bytes the stage held (0 * NaN is NaN): before the MMAs of such a V tile the
-//    whole warp zeroes those rows.
+//    whatever bytes the stage held (0 * NaN is NaN): before the MMAs of such a V tile this
+//    thread zeroes those rows (the last tile of a request: a few per CTA).
 //  * warps 8-11, Q: per item, thread d loads dim d of the item's query rows, finds the
 //    power of two 2^e that puts max|q| into [2^7, 2^8), writes 2^e q as E4M3 hi/lo
 //    operands and records which 16-key units of the item have a valid page.
@@ -67,7 +67,7 @@ constexpr int TK = 128;                     // keys per tile = the MMA's M
 constexpr int NH = 16;                      // query columns, padded = the MMA's N
 constexpr int UNITS = TK / PAGE;            // 16-key units per tile (8)
 constexpr int RAW_STAGES = 12;
-constexpr int NPB = 4;                      // P^T tiles in shared memory
+constexpr int NPB_MAX = 8;                  // P^T buffers: 8 of one operand (packed) or 4 pairs
 constexpr int MAX_TILES = 8;                // tiles per item (chunks of at most 1024 keys)
 constexpr int RAW_BYTES = TK * D;           // 16 KB of E4M3 per K or V tile
 constexpr int OP_BYTES = NH * 128;          // one E4M3 operand: 16 rows x 128 bytes
@@ -84,8 +84,8 @@ constexpr int TMEM_O = 256;
 
 constexpr int OFF_RAW = 0;
 constexpr int OFF_Q = OFF_RAW + RAW_STAGES * RAW_BYTES;   // two buffers (hi, lo)
-constexpr int OFF_P = OFF_Q + 2 * QP_BYTES;               // NPB buffers (hi, lo)
-constexpr int OFF_RED = OFF_P + NPB * QP_BYTES;           // exchange areas (1 KB)
+constexpr int OFF_P = OFF_Q + 2 * QP_BYTES;               // the P^T buffers (16 KB)
+constexpr int OFF_RED = OFF_P + 4 * QP_BYTES;             // exchange areas (1 KB)
 constexpr int OFF_MASK = OFF_RED + 1024;  // loaded-unit bits per raw stage (<= 16 words),
                                           // the q exponents (2 words at +64) and the per-item
                                           // unit masks (2 x 64 bits at +72)
@@ -95,7 +95,7 @@ constexpr int OFF_BAR = OFF_ITEM + 128;
 // barrier indices
 constexpr int RAW_FULL = 0, RAW_EMPTY = RAW_FULL + RAW_STAGES, Q_FULL = RAW_EMPTY + RAW_STAGES,
               Q_EMPTY = Q_FULL + 2, S_FULL = Q_EMPTY + 2, S_EMPTY = S_FULL + 2,
-              P_FULL = S_EMPTY + 2, P_EMPTY = P_FULL + NPB, PV_LAST = P_EMPTY + NPB,
+              P_FULL = S_EMPTY + 2, P_EMPTY = P_FULL + NPB_MAX, PV_LAST = P_EMPTY + NPB_MAX,
               O_EMPTY = PV_LAST + 1,
               MMA_DRAIN = O_EMPTY + 1, XCH_Q = MMA_DRAIN + 1, XCH_SMX = XCH_Q + 1,
               NUM_BARS = XCH_SMX + 1;
@@ -328,6 +328,10 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
     // NR <= 8: hi and lo of Q and P^T share one operand (rows n and 8 + n), so one MMA
     // per 32-element step covers both and S^T / O^T column 8 + n holds column n's lo part
     constexpr bool PACK = NR <= 8;
+    // P^T buffers: packed, 8 of one 2 KB operand, so an item's tiles never wait for one;
+    // otherwise 4 of a hi/lo pair
+    constexpr int NPB = PACK ? NPB_MAX : 4;
+    constexpr uint32_t P_STRIDE = PACK ? (uint32_t)OP_BYTES : (uint32_t)QP_BYTES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -353,19 +357,19 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
             mbar_init(BAR(RAW_EMPTY + s), 1);  // the commit of the tile's MMAs
         }
         for (int x = 0; x < 2; ++x) {
-            mbar_init(BAR(Q_FULL + x), 128);
+            mbar_init(BAR(Q_FULL + x), 4);  // one arrival per warp
             // released by the QK MMAs' commit and by the four softmax warps once they have
             // read the item's q exponent and unit mask (which the Q warps write with Q)
             mbar_init(BAR(Q_EMPTY + x), 1 + 4);
             mbar_init(BAR(S_FULL + x), 1);
-            mbar_init(BAR(S_EMPTY + x), 128);
+            mbar_init(BAR(S_EMPTY + x), 4);
         }
-        for (int x = 0; x < NPB; ++x) {
-            mbar_init(BAR(P_FULL + x), 128);
+        for (int x = 0; x < NPB_MAX; ++x) {
+            mbar_init(BAR(P_FULL + x), 4);
             mbar_init(BAR(P_EMPTY + x), 1);
         }
         mbar_init(BAR(PV_LAST), 1);
-        mbar_init(BAR(O_EMPTY), 128);
+        mbar_init(BAR(O_EMPTY), 4);
         mbar_init(BAR(MMA_DRAIN), 1);
         mbar_init(BAR(XCH_Q), 4);
         mbar_init(BAR(XCH_SMX), 4);
@@ -373,7 +377,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
         fence_barrier_init();
     }
     // Q rows and P^T rows NR..15 stay zero: clear every buffer once
-    for (int i = threadIdx.x; i < (2 + NPB) * QP_BYTES / 16; i += THREADS)
+    for (int i = threadIdx.x; i < (2 + 4) * QP_BYTES / 16; i += THREADS)
         reinterpret_cast<uint4*>(smem + OFF_Q)[i] = make_uint4(0, 0, 0, 0);
     fence_async_smem();
     if (warp == 1) {
@@ -473,28 +477,27 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA
-        // The whole warp follows the pipeline (its waits agree through __all_sync); lane 0
-        // issues the MMAs and commits.
-        const bool issuer = lane == 0;
-        constexpr uint32_t IDESC_S = idesc_e4m3_f32(TK, NH, false);
-        constexpr uint32_t IDESC_O = idesc_e4m3_f32(D, NH, true);
-        uint32_t ld = 0, pt = 0, s = 0;  // ring position, P^T tiles, items
-        bool ok = true;
-        auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
-            return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, abort_flag, p.status));
-        };
-        auto qk_tiles = [&](const Item& it) {  // after Q_FULL of item s
-            const uint32_t x = s & 1;  // Q buffer and S^T region of item s
-            ok = wait(BAR(S_EMPTY + x), ((s >> 1) & 1) ^ 1);
-            // B = the Q parts: 16 rows (columns of S^T) of 128 dims, K-major
-            const uint64_t qh = sdesc_sw128(s0 + OFF_Q + x * QP_BYTES, 16, 1024);
-            const uint64_t ql = sdesc_sw128(s0 + OFF_Q + x * QP_BYTES + OP_BYTES, 16, 1024);
-            for (int t = 0; ok && t < it.ntiles; ++t, ++ld) {
-                const uint32_t st = ld % RAW_STAGES;
-                ok = wait(BAR(RAW_FULL + st), (ld / RAW_STAGES) & 1);
-                if (!ok) break;
-                tc_fence_after();
-                if (issuer) {
+        // One thread: a loop in which the whole warp reconverges around each issue costs
+        // several hundred cycles per tile more (measured), and this thread is the pace.
+        if (lane == 0) {
+            constexpr uint32_t IDESC_S = idesc_e4m3_f32(TK, NH, false);
+            constexpr uint32_t IDESC_O = idesc_e4m3_f32(D, NH, true);
+            uint32_t ld = 0, pt = 0, s = 0;  // ring position, P^T tiles, items
+            bool ok = true;
+            auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
+                return mbar_wait_bounded(bar, parity, abort_flag, p.status);
+            };
+            auto qk_tiles = [&](const Item& it) {  // after Q_FULL of item s
+                const uint32_t x = s & 1;  // Q buffer and S^T region of item s
+                ok = wait(BAR(S_EMPTY + x), ((s >> 1) & 1) ^ 1);
+                // B = the Q parts: 16 rows (columns of S^T) of 128 dims, K-major
+                const uint64_t qh = sdesc_sw128(s0 + OFF_Q + x * QP_BYTES, 16, 1024);
+                const uint64_t ql = sdesc_sw128(s0 + OFF_Q + x * QP_BYTES + OP_BYTES, 16, 1024);
+                for (int t = 0; ok && t < it.ntiles; ++t, ++ld) {
+                    const uint32_t st = ld % RAW_STAGES;
+                    ok = wait(BAR(RAW_FULL + st), (ld / RAW_STAGES) & 1);
+                    if (!ok) break;
+                    tc_fence_after();
                     // A = the raw K tile: 128 keys of 128 bytes, K-major; 32 dims per MMA
                     const uint64_t kd = sdesc_sw128(s0 + OFF_RAW + st * RAW_BYTES, 16, 1024);
                     const uint32_t d_tm = tmem_base + 128u * x + 16u * t;
@@ -508,42 +511,38 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
                     }
                     mma_commit(BAR(RAW_EMPTY + st));
                 }
-                __syncwarp();
-            }
-            if (ok && issuer) {
-                mma_commit(BAR(S_FULL + x));
-                mma_commit(BAR(Q_EMPTY + x));
-            }
-            __syncwarp();
-        };
-        auto pv_tiles = [&](const Item& it, uint32_t sp) {  // sp: the item's index
-            if (sp > 0) ok = wait(BAR(O_EMPTY), (sp - 1) & 1);
-            for (int t = 0; ok && t < it.ntiles; ++t, ++ld, ++pt) {
-                const uint32_t st = ld % RAW_STAGES, pb = pt % NPB;
-                ok = wait(BAR(P_FULL + pb), (pt / NPB) & 1) &&
-                     wait(BAR(RAW_FULL + st), (ld / RAW_STAGES) & 1);
-                if (!ok) break;
-                // rows past the chunk and rows of units that were not loaded become zeros
-                const int nvalid = min(TK, it.tok1 - (it.tok0 + t * TK));
-                const uint32_t um = unit_mask[st] & 0xffu;
-                if (nvalid < TK || um != 0xffu) {
-                    uint8_t* raw = smem + OFF_RAW + st * RAW_BYTES;
-                    for (int i = lane; i < TK * 8; i += 32) {  // 16-byte pieces, 8 per row
-                        const int row = i >> 3;
-                        if (row >= nvalid || !((um >> (row >> 4)) & 1u))
-                            reinterpret_cast<uint4*>(raw + row * 128)[i & 7] = make_uint4(0, 0, 0, 0);
-                    }
-                    fence_async_smem();
-                    __syncwarp();
+                if (ok) {
+                    mma_commit(BAR(S_FULL + x));
+                    mma_commit(BAR(Q_EMPTY + x));
                 }
-                tc_fence_after();
-                if (issuer) {
+            };
+            auto pv_tiles = [&](const Item& it, uint32_t sp) {  // sp: the item's index
+                if (sp > 0) ok = wait(BAR(O_EMPTY), (sp - 1) & 1);
+                for (int t = 0; ok && t < it.ntiles; ++t, ++ld, ++pt) {
+                    const uint32_t st = ld % RAW_STAGES, pb = pt % NPB;
+                    ok = wait(BAR(P_FULL + pb), (pt / NPB) & 1) &&
+                         wait(BAR(RAW_FULL + st), (ld / RAW_STAGES) & 1);
+                    if (!ok) break;
+                    // rows past the chunk and rows of units that were not loaded become
+                    // zeros (only the last tile of a request, or a bad page id)
+                    const int nvalid = min(TK, it.tok1 - (it.tok0 + t * TK));
+                    const uint32_t um = unit_mask[st] & 0xffu;
+                    if (nvalid < TK || um != 0xffu) {
+                        uint4* raw = reinterpret_cast<uint4*>(smem + OFF_RAW + st * RAW_BYTES);
+                        for (int row = 0; row < TK; ++row)
+                            if (row >= nvalid || !((um >> (row >> 4)) & 1u)) {
+#pragma unroll
+                                for (int u = 0; u < 8; ++u) raw[row * 8 + u] = make_uint4(0, 0, 0, 0);
+                            }
+                        fence_async_smem();
+                    }
+                    tc_fence_after();
                     // A = V^T: the raw V tile read MN-major (a key's 128 dims are one
                     // 128-byte row, 8-key groups 1 KB apart; 32 keys per MMA); B = the P^T
                     // parts: 16 rows (columns) of 128 keys, K-major
                     const uint64_t vd = sdesc_sw128(s0 + OFF_RAW + st * RAW_BYTES, RAW_BYTES, 1024);
-                    const uint64_t ph = sdesc_sw128(s0 + OFF_P + pb * QP_BYTES, 16, 1024);
-                    const uint64_t pl = sdesc_sw128(s0 + OFF_P + pb * QP_BYTES + OP_BYTES, 16, 1024);
+                    const uint64_t ph = sdesc_sw128(s0 + OFF_P + pb * P_STRIDE, 16, 1024);
+                    const uint64_t pl = sdesc_sw128(s0 + OFF_P + pb * P_STRIDE + OP_BYTES, 16, 1024);
 #pragma unroll
                     for (int k = 0; k < TK / 32; ++k)
                         mma_e4m3_ss(tmem_base + TMEM_O, vd + 256u * k, ph + 2u * k, IDESC_O,
@@ -557,30 +556,25 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
                     mma_commit(BAR(RAW_EMPTY + st));
                     mma_commit(BAR(P_EMPTY + pb));
                 }
-                __syncwarp();
+                if (ok) mma_commit(BAR(PV_LAST));
+            };
+            Item prev;
+            prev.ntiles = 0;
+            while (ok) {
+                ok = wait(BAR(Q_FULL + (s & 1)), (s >> 1) & 1);
+                if (!ok) break;
+                const Item it = items[s & 1];
+                if (it.ntiles < 0) break;
+                qk_tiles(it);
+                if (ok && prev.ntiles > 0) pv_tiles(prev, s - 1);
+                prev = it;
+                ++s;
             }
-            if (ok && issuer) mma_commit(BAR(PV_LAST));
-            __syncwarp();
-        };
-        Item prev;
-        prev.ntiles = 0;
-        while (ok) {
-            ok = wait(BAR(Q_FULL + (s & 1)), (s >> 1) & 1);
-            if (!ok) break;
-            const Item it = items[s & 1];
-            if (it.ntiles < 0) break;
-            qk_tiles(it);
             if (ok && prev.ntiles > 0) pv_tiles(prev, s - 1);
-            prev = it;
-            ++s;
-        }
-        if (ok && prev.ntiles > 0) pv_tiles(prev, s - 1);
-        // every MMA issued has completed before tensor memory is released
-        if (issuer) {
+            // every MMA issued has completed before tensor memory is released
             mma_commit(BAR(MMA_DRAIN));
             mbar_wait_bounded(BAR(MMA_DRAIN), 0, nullptr, p.status);
         }
-        __syncwarp();
     } else if (warp >= W_Q && warp < W_Q + 4) {
         // ------------------------------------------------------------ Q
         // Per item: its query rows, scaled by 2^e, as the E4M3 hi/lo B operand of Q . K^T
@@ -645,7 +639,8 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
             }
             if (wq < 2 && lane == 0) km_words[2 * x + wq] = bits;
             fence_async_smem();
-            mbar_arrive(BAR(Q_FULL + x));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(Q_FULL + x));
             it = ni;
             ++s;
             cur = nxt;
@@ -659,7 +654,8 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
                                                            abort_flag, p.status));
             if (ok) {
                 if (d == 0) items[x].ntiles = -1;
-                mbar_arrive(BAR(Q_FULL + x));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR(Q_FULL + x));
             }
         }
     } else if (warp >= W_SMX && warp < W_SMX + 4) {
@@ -706,7 +702,8 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
                 for (int n = 0; n < NR; ++n) ov[n] = __uint_as_float(v[n]);
             }
             tc_fence_before();
-            mbar_arrive(BAR(O_EMPTY));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(O_EMPTY));
             // lane n < NR: column n's output scale and lse
             const float inv_c = l_c > 0.f ? p.v_scale / l_c : 0.f;
             const float lse_c = l_c > 0.f ? (m_c - P_LOG2_SCALE + log2f(l_c)) * 0.69314718055994531f
@@ -784,7 +781,8 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
                     }
                 }
                 tc_fence_before();
-                mbar_arrive(BAR(S_EMPTY + x));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR(S_EMPTY + x));
 #pragma unroll
                 for (int n = 0; n < NR; ++n) {
                     float m = sv[0][n];
@@ -859,14 +857,16 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
                                                                ((pt / NPB) & 1) ^ 1, abort_flag,
                                                                p.status));
                 if (!ok) break;
-                store_col_e4m3<NR, PACK>(smem + OFF_P + pb * QP_BYTES, r, pv);
+                store_col_e4m3<NR, PACK>(smem + OFF_P + pb * P_STRIDE, r, pv);
                 fence_async_smem();
-                mbar_arrive(BAR(P_FULL + pb));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR(P_FULL + pb));
             }
             if (!ok) break;
             if constexpr (NR != G) {  // the second pass has read the item's scores
                 tc_fence_before();
-                mbar_arrive(BAR(S_EMPTY + x));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR(S_EMPTY + x));
             }
             // column sums over the item's keys: the warp, then the four warps (read out at
             // once: the exchange area is reused two exchanges later)

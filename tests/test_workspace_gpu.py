@@ -20,7 +20,6 @@ Each test returns the library to its lazy workspace before it ends.
 import pytest
 import torch
 
-from paged_gqa_attention_varlen_gb300 import api as _api
 from paged_gqa_attention_varlen_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -77,11 +76,11 @@ def test_too_small_caller_workspace_is_refused_before_anything_runs(lazy_after):
     buf = torch.empty(100 << 10, dtype=torch.uint8, device="cuda")  # 100 KiB
     api.set_workspace(buf)
     o = torch.full_like(case.q, 7.0)
-    with pytest.raises(_api.PgqaError) as e:
+    with pytest.raises(api.PgqaError) as e:
         _prefill(api, case, out=o)
     assert e.value.code == PGQA_ERR_WORKSPACE
     od = torch.full_like(pc.q, 7.0)
-    with pytest.raises(_api.PgqaError) as e:
+    with pytest.raises(api.PgqaError) as e:
         _decode(api, pc, out=od)
     assert e.value.code == PGQA_ERR_WORKSPACE
     torch.cuda.synchronize()
@@ -143,7 +142,7 @@ def test_e4m3_conversion_pool_larger_than_the_caller_buffer_is_refused(lazy_afte
     buf = torch.empty(64 << 20, dtype=torch.uint8, device="cuda")
     api.set_workspace(buf)
     o = torch.full_like(pc.q, 7.0)
-    with pytest.raises(_api.PgqaError) as e:
+    with pytest.raises(api.PgqaError) as e:
         api.paged_prefill(pc.q, pc.k_pages, pc.v_pages, pc.q_indptr, pc.page_table,
                           pc.kv_lens_t, sm_scale=pc.sm_scale, k_scale=0.5, v_scale=2.0,
                           max_qo_len=300, out=o)
