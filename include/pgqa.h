@@ -331,8 +331,7 @@ int paged_decode_bf16(const void* q, const void* k_pages, const void* v_pages,
  * and output.
  *
  *   - Set-up: the first call on each device, with that device current, looks up the
- *     array's device address (cudaGetSymbolAddress) and keeps it.  Make that first call
- *     before any stream capture.
+ *     array's device address (cudaGetSymbolAddress) and keeps it.
  *   - Limit: returns PGQA_ERR_WORKSPACE, enqueueing nothing, when
  *       1024 + 256-rounded (2*batch+1)*4 + 256-rounded C*Hq*4 + C*Hq*head_dim*4 > 16 MiB,
  *     with C = batch * ceil(page_table_stride * page_size / K) partial chunks and K the

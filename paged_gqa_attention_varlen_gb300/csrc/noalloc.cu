@@ -12,7 +12,7 @@
 // that loads the library holds it until the process exits.  In host code its name is
 // only a host-side stand-in, so the first call on each device resolves the device
 // address with cudaGetSymbolAddress (with that device current) and passes it to the
-// kernels; that first call should come before any stream capture.  The status word the
+// kernels.  The status word the
 // kernels write lives in the array too, so device-side errors of this call (skipped bad
 // page ids, an expired bounded wait) are not reported to the caller.
 #include <cuda_runtime.h>
