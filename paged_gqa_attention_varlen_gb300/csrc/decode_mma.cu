@@ -20,10 +20,10 @@
 // Here the MMAs (kind::f8f6f4) read the raw stages: Q . K^T takes the K tile straight from
 // the ring, P . V the V tile as an MN-major operand, and a stage is released by the
 // commit of its MMAs.  The other operand of each product, Q and P, is given as a pair of
-// E4M3 matrices hi + lo (hi = E4M3(x), lo = E4M3(x - hi)), two MMAs accumulating into the
-// same fp32 result: for Q (bf16, scaled by a power of two into [2^7, 2^8)) the pair is
-// exact down to 2^-2, for P (scaled by 2^8) it keeps about 8 significant bits, as the bf16
-// prefill's P does.
+// E4M3 matrices hi + lo (hi = E4M3(x), lo = E4M3(x - hi)) whose products are summed in
+// fp32 (in one accumulator, or in two accumulator columns added afterwards): for Q (bf16,
+// scaled by a power of two into [2^7, 2^8)) the pair is exact down to 2^-2, for P (scaled
+// by 2^8) it keeps about 8 significant bits, as the bf16 prefill's P does.
 //
 // Design (one persistent CTA per SM, 384 threads; work item = one (chunk, kv head) of up
 // to 8 tiles of 128 keys; the items of a CTA run as a software pipeline in which step s
@@ -37,7 +37,7 @@
 //      S^T_t  = K_t . (Qhi + Qlo)^T     A = raw K tile (K-major), B = Q parts (K-major)
 //      O^T   += V_t^T . (Phi + Plo)^T   A = raw V tile (MN-major), B = P^T parts (K-major)
 //    Every S^T tile of an item stays in tensor memory (two item regions of 8 x 16
-//    columns), so the softmax sees the whole item at once; O^T takes 16 more columns.
+//    columns), so the softmax sees the whole item at once; O^T takes 16 (or 32) more.
 //    Keys past the chunk and units whose page was not loaded must not reach P . V as
 //    whatever bytes the stage held (0 * NaN is NaN): before the MMAs of such a V tile this
 //    thread zeroes those rows (the last tile of a request: a few per CTA).
@@ -78,7 +78,7 @@ constexpr int W_Q = 8;                      // Q warps 8-11
 constexpr int THREADS = 12 * 32;
 constexpr float P_LOG2_SCALE = 8.f;         // P^T holds 2^8 P
 // tensor memory: S^T regions of two items (8 tiles x 16 columns each) at 0 and 128, O^T
-// at 256
+// at 256 (16 columns, or 32 when P's hi and lo parts are separate rows of one operand)
 constexpr int TMEM_COLS = 512;
 constexpr int TMEM_O = 256;
 
@@ -481,7 +481,10 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
         // several hundred cycles per tile more (measured), and this thread is the pace.
         if (lane == 0) {
             constexpr uint32_t IDESC_S = idesc_e4m3_f32(TK, NH, false);
-            constexpr uint32_t IDESC_O = idesc_e4m3_f32(D, NH, true);
+            // P.V: packed, N = 16 (hi and lo rows in one operand); otherwise the hi and lo
+            // operands are rows 0-15 and 16-31 of one 32-row operand: N = 32, O^T columns
+            // n and 16 + n
+            constexpr uint32_t IDESC_O = idesc_e4m3_f32(D, PACK ? NH : 2 * NH, true);
             uint32_t ld = 0, pt = 0, s = 0;  // ring position, P^T tiles, items
             bool ok = true;
             auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
@@ -542,17 +545,10 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
                     // parts: 16 rows (columns) of 128 keys, K-major
                     const uint64_t vd = sdesc_sw128(s0 + OFF_RAW + st * RAW_BYTES, RAW_BYTES, 1024);
                     const uint64_t ph = sdesc_sw128(s0 + OFF_P + pb * P_STRIDE, 16, 1024);
-                    const uint64_t pl = sdesc_sw128(s0 + OFF_P + pb * P_STRIDE + OP_BYTES, 16, 1024);
 #pragma unroll
                     for (int k = 0; k < TK / 32; ++k)
                         mma_e4m3_ss(tmem_base + TMEM_O, vd + 256u * k, ph + 2u * k, IDESC_O,
                                     (t > 0 || k > 0) ? 1u : 0u);
-                    if constexpr (!PACK) {
-#pragma unroll
-                        for (int k = 0; k < TK / 32; ++k)
-                            mma_e4m3_ss(tmem_base + TMEM_O, vd + 256u * k, pl + 2u * k, IDESC_O,
-                                        1u);
-                    }
                     mma_commit(BAR(RAW_EMPTY + st));
                     mma_commit(BAR(P_EMPTY + pb));
                 }
@@ -694,12 +690,12 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
                 tmem_wait_ld16(v);
 #pragma unroll
                 for (int n = 0; n < NR; ++n) ov[n] = __uint_as_float(v[n]) + __uint_as_float(v[8 + n]);
-            } else {
-                uint32_t v[16];
-                tmem_ld16(tmem_base + lane_base + TMEM_O, v);
-                tmem_wait_ld16(v);
+            } else {  // columns n (hi part) and 16 + n (lo part)
+                uint32_t v[32];
+                tmem_ld32(tmem_base + lane_base + TMEM_O, v);
+                tmem_wait_ld32(v);
 #pragma unroll
-                for (int n = 0; n < NR; ++n) ov[n] = __uint_as_float(v[n]);
+                for (int n = 0; n < NR; ++n) ov[n] = __uint_as_float(v[n]) + __uint_as_float(v[NH + n]);
             }
             tc_fence_before();
             __syncwarp();
