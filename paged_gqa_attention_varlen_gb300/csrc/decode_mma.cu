@@ -550,7 +550,10 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
                         mma_e4m3_ss(tmem_base + TMEM_O, vd + 256u * k, ph + 2u * k, IDESC_O,
                                     (t > 0 || k > 0) ? 1u : 0u);
                     mma_commit(BAR(RAW_EMPTY + st));
-                    mma_commit(BAR(P_EMPTY + pb));
+                    // packed: a buffer is next written for the next item, after that item's
+                    // softmax has waited for this item's last P.V (its epilogue), so it
+                    // needs no release of its own
+                    if constexpr (!PACK) mma_commit(BAR(P_EMPTY + pb));
                 }
                 if (ok) mma_commit(BAR(PV_LAST));
             };
@@ -849,10 +852,12 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
                 }
 #pragma unroll
                 for (int n = 0; n < NR; ++n) l[n] += pv[n];
-                ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(P_EMPTY + pb),
-                                                               ((pt / NPB) & 1) ^ 1, abort_flag,
-                                                               p.status));
-                if (!ok) break;
+                if constexpr (!PACK) {
+                    ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(P_EMPTY + pb),
+                                                                   ((pt / NPB) & 1) ^ 1, abort_flag,
+                                                                   p.status));
+                    if (!ok) break;
+                }
                 store_col_e4m3<NR, PACK>(smem + OFF_P + pb * P_STRIDE, r, pv);
                 fence_async_smem();
                 __syncwarp();
