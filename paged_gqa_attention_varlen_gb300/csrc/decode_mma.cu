@@ -43,12 +43,15 @@
 //    thread zeroes those rows (the last tile of a request: a few per CTA).
 //  * warps 8-11, Q: per item, thread d loads dim d of the item's query rows, finds the
 //    power of two 2^e that puts max|q| into [2^7, 2^8), writes 2^e q as E4M3 hi/lo
-//    operands and records which 16-key units of the item have a valid page.
+//    operands, records which 16-key units of the item have a valid page and publishes
+//    the item's geometry beside them, so the MMA thread and the softmax never walk the
+//    request list; they also write the rows of requests without keys.
 //  * warps 4-7, softmax: thread r owns key r of every tile (TMEM lane r).  Per item: one
 //    pass over all its S^T tiles gives the exact max per column (a transposing warp
 //    butterfly and one exchange among the four warps), so no running rescale is needed;
 //    then each tile's P^T = 2^8 exp2(s - max) goes to shared memory as E4M3 hi/lo bytes
-//    (row = column n, byte = key) while the column sums accumulate; at the item's end
+//    (row = column n, byte = key; 8 buffers of one item when packed, 4 otherwise) while
+//    the column sums accumulate; at the item's end
 //    thread r holds row r of O^T: divided by l, scaled by v_scale, it becomes the bf16
 //    output (single-chunk request) or the fp32 partial and its lse.
 //  While the softmax works on item s - 1, the tensor core is already on the K tiles of
@@ -392,7 +395,8 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
     const int Hq = p.num_qo_heads;
     const long long n_items = (long long)__ldg(p.chunk_off + p.batch) * p.num_kv_heads;
     const long long stride = gridDim.x;
-    // every role walks the CTA's non-empty items in the same order
+    // the producers' walk over the CTA's non-empty items (the Q warps walk the same list and
+    // publish each item for the MMA thread and the softmax)
     auto next_item = [&](long long from, Item& out, Cursor& pos) -> long long {
         for (long long k = from; k < n_items; k += stride) {
             out = item_of(p, k, pos);
