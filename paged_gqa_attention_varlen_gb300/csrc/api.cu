@@ -332,10 +332,10 @@ void fill_split(prefill::PlanParams& pp, prefill::Params& p, const PrefillWs& w,
 // room for max_qo query rows each.
 size_t decode_ints(int batch, bool rows) { return (size_t)((rows ? 4 : 2) * (size_t)batch + 1); }
 size_t decode_ws_bytes(int batch, int stride, int page_size, int hq, int d, int hk, bool rows,
-                       int max_qo) {
+                       int max_qo, int chunk_top = decode::CHUNK) {
     const long long max_kv = (long long)stride * page_size;
     const long long chunks =
-        decode::total_chunks(batch, max_kv, decode::chunk_keys(batch, max_kv, hk));
+        decode::total_chunks(batch, max_kv, decode::chunk_keys(batch, max_kv, hk, chunk_top));
     const size_t slots = (size_t)chunks * max_qo * hq;
     const size_t ints = align_up(decode_ints(batch, rows) * sizeof(int), 256);
     return kWsArrays + ints + align_up(slots * sizeof(float), 256) + slots * d * sizeof(float);
@@ -702,8 +702,11 @@ int paged_decode_impl(const void* q, const void* k_pages, const void* v_pages,
     if (rc != PGQA_OK) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const bool rows = q_indptr != nullptr;
+    // the E4M3 tensor-core form with several query rows per request takes chunks of at
+    // most 896 keys
+    const int chunk_top = kv8 && max_qo > 1 ? decode::CHUNK_E4M3_ROWS : decode::CHUNK;
     const size_t need = decode_ws_bytes(batch, page_table_stride, page_size, num_qo_heads, head_dim,
-                                        num_kv_heads, rows, max_qo);
+                                        num_kv_heads, rows, max_qo, chunk_top);
     rc = ensure_workspace(*st, need, s);
     if (rc != PGQA_OK) return rc;
 
@@ -715,7 +718,7 @@ int paged_decode_impl(const void* q, const void* k_pages, const void* v_pages,
     int* q_len = rows ? q_off + batch : nullptr;
     const size_t lse_off = kWsArrays + align_up(decode_ints(batch, rows) * sizeof(int), 256);
     const long long max_kv = (long long)page_table_stride * page_size;
-    const int chunk = decode::chunk_keys(batch, max_kv, num_kv_heads);
+    const int chunk = decode::chunk_keys(batch, max_kv, num_kv_heads, chunk_top);
     const long long chunks = decode::total_chunks(batch, max_kv, chunk);
     float* part_lse = reinterpret_cast<float*>(ws + lse_off);
     float* part_o = reinterpret_cast<float*>(

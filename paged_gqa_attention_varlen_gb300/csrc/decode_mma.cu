@@ -72,6 +72,8 @@ constexpr int UNITS = TK / PAGE;            // 16-key units per tile (8)
 constexpr int RAW_STAGES = 12;
 constexpr int NPB_MAX = 8;                  // P^T buffers: 8 of one operand (packed) or 4 pairs
 constexpr int MAX_TILES = 8;                // tiles per item (chunks of at most 1024 keys)
+constexpr int MAX_TILES_ROWS = CHUNK_E4M3_ROWS / TK;  // ... with several query rows (896 keys)
+static_assert(MAX_TILES_ROWS * TK == CHUNK_E4M3_ROWS, "whole tiles");
 constexpr int RAW_BYTES = TK * D;           // 16 KB of E4M3 per K or V tile
 constexpr int OP_BYTES = NH * 128;          // one E4M3 operand: 16 rows x 128 bytes
 constexpr int QP_BYTES = 2 * OP_BYTES;      // its hi and lo parts
@@ -80,10 +82,11 @@ constexpr int W_SMX = 4;                    // softmax warps 4-7
 constexpr int W_Q = 8;                      // Q warps 8-11
 constexpr int THREADS = 12 * 32;
 constexpr float P_LOG2_SCALE = 8.f;         // P^T holds 2^8 P
-// tensor memory: S^T regions of two items (8 tiles x 16 columns each) at 0 and 128, O^T
-// at 256 (16 columns, or 32 when P's hi and lo parts are separate rows of one operand)
+// tensor memory: S^T regions of two items and O^T.  One query row (packed): tiles of 16
+// columns, regions of 8 tiles at 0 and 128, O^T at 256 (16 columns).  Several rows: tiles
+// of 32 columns (the hi and lo parts of Q side by side), regions of 7 tiles at 0 and 224,
+// O^T at 448 (32 columns, the hi and lo parts of P).
 constexpr int TMEM_COLS = 512;
-constexpr int TMEM_O = 256;
 
 constexpr int OFF_RAW = 0;
 constexpr int OFF_Q = OFF_RAW + RAW_STAGES * RAW_BYTES;   // two buffers (hi, lo)
@@ -335,6 +338,10 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
     // otherwise 4 of a hi/lo pair
     constexpr int NPB = PACK ? NPB_MAX : 4;
     constexpr uint32_t P_STRIDE = PACK ? (uint32_t)OP_BYTES : (uint32_t)QP_BYTES;
+    constexpr uint32_t S_COLS = PACK ? 16u : 32u;  // tensor-memory columns of an S^T tile
+    constexpr uint32_t S_REGION = PACK ? 16u * MAX_TILES : 32u * MAX_TILES_ROWS;
+    constexpr uint32_t TMEM_O = 2u * S_REGION;
+    static_assert(TMEM_O + (PACK ? 16u : 32u) <= (uint32_t)TMEM_COLS, "tensor memory columns");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -484,7 +491,9 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
         // One thread: a loop in which the whole warp reconverges around each issue costs
         // several hundred cycles per tile more (measured), and this thread is the pace.
         if (lane == 0) {
-            constexpr uint32_t IDESC_S = idesc_e4m3_f32(TK, NH, false);
+            // Q.K^T: packed, N = 16 (hi and lo rows in one operand); otherwise N = 32 over
+            // the hi and lo operands (rows 0-15 and 16-31), S^T columns n and 16 + n
+            constexpr uint32_t IDESC_S = idesc_e4m3_f32(TK, PACK ? NH : 2 * NH, false);
             // P.V: packed, N = 16 (hi and lo rows in one operand); otherwise the hi and lo
             // operands are rows 0-15 and 16-31 of one 32-row operand: N = 32, O^T columns
             // n and 16 + n
@@ -497,9 +506,8 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
             auto qk_tiles = [&](const Item& it) {  // after Q_FULL of item s
                 const uint32_t x = s & 1;  // Q buffer and S^T region of item s
                 ok = wait(BAR(S_EMPTY + x), ((s >> 1) & 1) ^ 1);
-                // B = the Q parts: 16 rows (columns of S^T) of 128 dims, K-major
+                // B = the Q parts: rows (columns of S^T) of 128 dims, K-major
                 const uint64_t qh = sdesc_sw128(s0 + OFF_Q + x * QP_BYTES, 16, 1024);
-                const uint64_t ql = sdesc_sw128(s0 + OFF_Q + x * QP_BYTES + OP_BYTES, 16, 1024);
                 for (int t = 0; ok && t < it.ntiles; ++t, ++ld) {
                     const uint32_t st = ld % RAW_STAGES;
                     ok = wait(BAR(RAW_FULL + st), (ld / RAW_STAGES) & 1);
@@ -507,15 +515,10 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
                     tc_fence_after();
                     // A = the raw K tile: 128 keys of 128 bytes, K-major; 32 dims per MMA
                     const uint64_t kd = sdesc_sw128(s0 + OFF_RAW + st * RAW_BYTES, 16, 1024);
-                    const uint32_t d_tm = tmem_base + 128u * x + 16u * t;
+                    const uint32_t d_tm = tmem_base + S_REGION * x + S_COLS * t;
 #pragma unroll
                     for (int k = 0; k < D / 32; ++k)
                         mma_e4m3_ss(d_tm, kd + 2u * k, qh + 2u * k, IDESC_S, k > 0 ? 1u : 0u);
-                    if constexpr (!PACK) {
-#pragma unroll
-                        for (int k = 0; k < D / 32; ++k)
-                            mma_e4m3_ss(d_tm, kd + 2u * k, ql + 2u * k, IDESC_S, 1u);
-                    }
                     mma_commit(BAR(RAW_EMPTY + st));
                 }
                 if (ok) {
@@ -751,7 +754,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
             // arrival they could complete Q_FULL twice before a slow softmax waits
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(Q_EMPTY + x));
-            const uint32_t s_base = tmem_base + lane_base + 128u * x;
+            const uint32_t s_base = tmem_base + lane_base + S_REGION * x;
             tc_fence_after();
             // bit n set: key r of tile t counts for column n (inside the chunk, its unit
             // loaded, and, causal with several query rows, row n / G >= key - (kv - qo))
@@ -794,20 +797,21 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
                     mx[n] = m;
                 }
             } else {
-                // 16 columns: a first pass over the tiles (two per load) for the max
+                // 16 columns: a first pass over the tiles for the max (column n of a tile
+                // is the hi part, column 16 + n the lo part)
 #pragma unroll
                 for (int n = 0; n < NR; ++n) mx[n] = -INFINITY;
-                for (int t = 0; t < it.ntiles; t += 2) {
+                for (int t = 0; t < it.ntiles; ++t) {
                     uint32_t u[32];
-                    tmem_ld32(s_base + 16u * t, u);
+                    tmem_ld32(s_base + S_COLS * t, u);
                     tmem_wait_ld32(u);
-                    const uint32_t v0 = vis_mask(t), v1 = vis_mask(t + 1);
+                    const uint32_t vm = vis_mask(t);
 #pragma unroll
                     for (int n = 0; n < NR; ++n) {
-                        const float a = ((v0 >> n) & 1u) ? __uint_as_float(u[n]) * c_eff : -INFINITY;
-                        const float b =
-                            ((v1 >> n) & 1u) ? __uint_as_float(u[16 + n]) * c_eff : -INFINITY;
-                        mx[n] = fmaxf(mx[n], fmaxf(a, b));
+                        const float a = ((vm >> n) & 1u)
+                                            ? (__uint_as_float(u[n]) + __uint_as_float(u[NH + n])) * c_eff
+                                            : -INFINITY;
+                        mx[n] = fmaxf(mx[n], a);
                     }
                 }
             }
@@ -845,14 +849,16 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
                         }
                     }
                 } else {
-                    uint32_t u[16];
-                    tmem_ld16(s_base + 16u * t, u);
-                    tmem_wait_ld16(u);
+                    uint32_t u[32];
+                    tmem_ld32(s_base + S_COLS * t, u);
+                    tmem_wait_ld32(u);
                     const uint32_t vm = vis_mask(t);
 #pragma unroll
                     for (int n = 0; n < NR; ++n)
                         pv[n] = ex2_approx(
-                            (((vm >> n) & 1u) ? __uint_as_float(u[n]) * c_eff : -INFINITY) + neg[n]);
+                            (((vm >> n) & 1u) ? (__uint_as_float(u[n]) + __uint_as_float(u[NH + n])) * c_eff
+                                              : -INFINITY) +
+                            neg[n]);
                 }
 #pragma unroll
                 for (int n = 0; n < NR; ++n) l[n] += pv[n];
@@ -914,7 +920,7 @@ static cudaError_t launch_g(const Params& p, int num_sms, cudaStream_t stream) {
 template <int G>
 static cudaError_t launch_rows(const Params& p, int num_sms, cudaStream_t stream) {
     if (p.max_qo <= 1) return launch_g<G, G>(p, num_sms, stream);
-    if (p.max_qo * G > NH) return cudaErrorInvalidValue;
+    if (p.max_qo * G > NH || p.chunk > MAX_TILES_ROWS * TK) return cudaErrorInvalidValue;
     return launch_g<G, NH>(p, num_sms, stream);
 }
 

@@ -155,14 +155,17 @@ constexpr int WAVE_ITEMS = 2048;   // (request, chunk, kv head) items of about o
 // wave of (chunk, kv head) warps, so that calls with little work spread over the GPU.  For
 // a given chunk length a request's chunks depend on the request alone, so its results do
 // not depend on the other requests of the batch.
-inline int chunk_keys(int batch, long long max_kv, int num_kv_heads) {
+// `top` caps the longest chunk: the tensor-core E4M3 decode with several query rows per
+// request keeps 7 tiles of 128 keys per item (CHUNK_E4M3_ROWS), so its 1024 becomes 896.
+constexpr int CHUNK_E4M3_ROWS = 896;
+inline int chunk_keys(int batch, long long max_kv, int num_kv_heads, int top = CHUNK) {
     int chunk = CHUNK;
     while (chunk > CHUNK_MIN) {
         const long long per_req = max_kv > 0 ? (max_kv + chunk - 1) / chunk : 1;
         if ((long long)batch * per_req * num_kv_heads >= WAVE_ITEMS) break;
         chunk /= 2;
     }
-    return chunk;
+    return chunk > top ? top : chunk;
 }
 inline long long total_chunks(int batch, long long max_kv, int chunk) {
     return (long long)batch * (max_kv > 0 ? (max_kv + chunk - 1) / chunk : 1);
