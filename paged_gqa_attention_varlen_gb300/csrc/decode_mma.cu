@@ -528,9 +528,12 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
             };
             auto pv_tiles = [&](const Item& it, uint32_t sp) {  // sp: the item's index
                 if (sp > 0) ok = wait(BAR(O_EMPTY), (sp - 1) & 1);
+                // packed: all of the item's P^T tiles are published at once (P_FULL by item
+                // parity); otherwise tile by tile (P_FULL by buffer)
+                if (PACK && ok) ok = wait(BAR(P_FULL + (sp & 1)), (sp >> 1) & 1);
                 for (int t = 0; ok && t < it.ntiles; ++t, ++ld, ++pt) {
                     const uint32_t st = ld % RAW_STAGES, pb = pt % NPB;
-                    ok = wait(BAR(P_FULL + pb), (pt / NPB) & 1) &&
+                    ok = (PACK || wait(BAR(P_FULL + pb), (pt / NPB) & 1)) &&
                          wait(BAR(RAW_FULL + st), (ld / RAW_STAGES) & 1);
                     if (!ok) break;
                     // rows past the chunk and rows of units that were not loaded become
@@ -869,11 +872,18 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
                     if (!ok) break;
                 }
                 store_col_e4m3<NR, PACK>(smem + OFF_P + pb * P_STRIDE, r, pv);
-                fence_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(BAR(P_FULL + pb));
+                if constexpr (!PACK) {
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(BAR(P_FULL + pb));
+                }
             }
             if (!ok) break;
+            if constexpr (PACK) {  // the item's P^T tiles at once
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR(P_FULL + (s & 1)));
+            }
             if constexpr (NR != G) {  // the second pass has read the item's scores
                 tc_fence_before();
                 __syncwarp();
