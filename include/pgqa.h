@@ -276,8 +276,9 @@ int pgqa_paged_decode_e4m3(const void* q, const void* k_pages, const void* v_pag
  *   - head_dim 128, G in {1,2,4,8} and max_qo_len * G <= 16 (multi-token decode,
  *     speculative verification): the tensor-core E4M3 decode, each request's query rows
  *     as the columns of its MMAs, so the keys stream once for all of them; split-KV as for
- *     the decode, with chunks of at most 896 keys when max_qo_len > 1.  A request with more than max_qo_len rows is reported as
- *     PGQA_ERR_DEVICE_BOUNDS and none of its rows is written.
+ *     the decode, with chunks of at most 896 keys when max_qo_len > 1.  A request with
+ *     more than max_qo_len rows is reported as PGQA_ERR_DEVICE_BOUNDS and none of its rows
+ *     is written.
  *   - otherwise: the pages the call reads are converted to bf16 (exact) into the
  *     workspace, then the bf16 paged prefill runs over them with k_scale folded into the
  *     score scale and v_scale into the output scale.  The conversion needs
