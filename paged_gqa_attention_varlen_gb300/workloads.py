@@ -160,12 +160,12 @@ def paged_case(kv_lens, num_qo_heads, num_kv_heads, head_dim, page_size=16, qo_l
 
 def paged_case_e4m3(kv_lens, num_qo_heads, num_kv_heads, head_dim, page_size=16, qo_lens=None,
                     causal=True, sm_scale=None, seed=0, device="cpu", k_scale=0.5, v_scale=2.0,
-                    extra_pages=0, name="custom_e4m3"):
+                    extra_pages=0, stride=None, name="custom_e4m3"):
     """paged_case() with the K/V pages stored as FP8 E4M3 bytes (uint8 tensors): the
     seeded bf16 draws rounded to the nearest E4M3 value by torch's float8_e4m3fn cast.
     The element values are byte value x k_scale / v_scale (stored in meta)."""
     pc = paged_case(kv_lens, num_qo_heads, num_kv_heads, head_dim, page_size, qo_lens, causal,
-                    sm_scale, seed, device, extra_pages=extra_pages, name=name)
+                    sm_scale, seed, device, extra_pages=extra_pages, stride=stride, name=name)
     pc.k_pages = pc.k_pages.float().to(torch.float8_e4m3fn).view(torch.uint8)
     pc.v_pages = pc.v_pages.float().to(torch.float8_e4m3fn).view(torch.uint8)
     pc.meta.update(k_scale=float(k_scale), v_scale=float(v_scale))

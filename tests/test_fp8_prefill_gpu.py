@@ -91,6 +91,27 @@ def test_one_row_per_request_matches_e4m3_decode(cuda_lib, G, max_qo):
     assert (lse[fin] - ld[fin]).abs().max().item() <= 1e-4
 
 
+def test_multi_row_form_with_896_key_chunks(cuda_lib):
+    """Several query rows per request over a call large enough for the longest chunks: the
+    multi-row tensor-core form caps them at 896 keys (7 tiles), so requests end just
+    before, at and just after multiples of 896 here, with 128-token pages split across
+    chunk boundaries."""
+    rng = np.random.default_rng(5)
+    kv = [895, 896, 897, 1791, 1792, 1793, 2688, 2689, 0, 1, 3, 127, 128, 129]
+    kv += [int(x) for x in rng.integers(1, 4000, 64 - len(kv))]
+    qo = [int(x) for x in rng.integers(1, 5, len(kv))]
+    qo[8] = 4  # no keys at all
+    # 256 pages of 128 keys per table row: with 64 requests and one kv head the chunk
+    # ladder stays at its top (1024 keys, 896 for this form)
+    pc = W.paged_case_e4m3(kv, 4, 1, 128, page_size=128, qo_lens=qo, seed=331, device="cuda",
+                           k_scale=0.75, v_scale=1.5, stride=256)
+    o, lse = run(cuda_lib, pc, 4)
+    assert cuda_lib.device_status() == 0
+    ro, rl = oracle_e4m3(pc)
+    check_rows(o.reshape(-1, 128).float().cpu(), lse.reshape(-1).cpu(), ro, rl,
+               "multi-row e4m3, 896-key chunks")
+
+
 def test_e4m3_prefill_hnd_and_float8_dtype_match_packed_bitwise(cuda_lib):
     pc = W.paged_case_e4m3([700, 5, 2100, 33], 32, 8, 128, page_size=32, qo_lens=[4, 3, 1, 4],
                            seed=321, device="cuda")

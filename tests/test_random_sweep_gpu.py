@@ -24,7 +24,7 @@ from gpu_util import check_rows
 
 pytestmark = pytest.mark.gpu
 
-N_CASES = 8
+N_CASES = 12
 
 
 def _lens(rng, batch, lo, hi, p_zero=0.1):
