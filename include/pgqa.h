@@ -279,12 +279,13 @@ int pgqa_paged_decode_e4m3(const void* q, const void* k_pages, const void* v_pag
  *     the decode, with chunks of at most 896 keys when max_qo_len > 1.  A request with
  *     more than max_qo_len rows is reported as PGQA_ERR_DEVICE_BOUNDS and none of its rows
  *     is written.
- *   - otherwise: the pages the call reads are converted to bf16 (exact) into the
- *     workspace, then the bf16 paged prefill runs over them with k_scale folded into the
- *     score scale and v_scale into the output scale.  The conversion needs
- *     2 * P * page_size * num_kv_heads * head_dim * 2 bytes of workspace on top of the
- *     prefill's own, P = min(num_pages, batch * page_table_stride); a caller workspace
- *     too small for it gives PGQA_ERR_WORKSPACE.
+ *   - otherwise: the pages the call reads are converted into the workspace, K to bf16 and
+ *     V to f16 (both exact), then the paged prefill runs over them with k_scale folded into
+ *     the score scale, v_scale into the output scale and the weights P rounded to f16 for
+ *     P.V (at least the accuracy of the bf16 paged prefill over the same values).  The
+ *     conversion needs 2 * P * page_size * num_kv_heads * head_dim * 2 bytes of workspace
+ *     on top of the prefill's own, P = min(num_pages, batch * page_table_stride); a
+ *     caller workspace too small for it gives PGQA_ERR_WORKSPACE.
  *
  * Supported: head_dim 128 or 256; page_size 16, 32, 64 or 128; G = num_qo_heads /
  * num_kv_heads dividing 128.  max_qo_len < 1 (with batch > 0), a NULL q_indptr or a NaN /

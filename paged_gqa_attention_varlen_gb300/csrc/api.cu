@@ -551,6 +551,7 @@ int pgqa_ragged_prefill_bf16(const void* q, const void* k, const void* v, void* 
     p.causal = causal ? 1 : 0;
     p.scale_log2 = sm_scale * 1.4426950408889634f;
     p.v_scale = 1.f;
+    p.f8conv = 0;
     p.page_table = nullptr;
     p.page_table_stride = 0;
     p.page_size = 0;
@@ -936,6 +937,7 @@ int paged_prefill_impl(const void* q, const void* k_pages, const void* v_pages, 
     p.causal = causal ? 1 : 0;
     p.scale_log2 = sm_scale * 1.4426950408889634f;
     p.v_scale = v_scale;
+    p.f8conv = kv8 ? 1 : 0;  // pages converted from E4M3: V is f16
     p.page_table = page_table;
     p.page_table_stride = page_table_stride;
     p.page_size = page_size;

@@ -1,15 +1,17 @@
 // dequant.cu -- the pages of an FP8 E4M3 KV cache that a paged prefill reads, converted to
-// bf16, for sm_103a.
+// K in bf16 and V in f16, for sm_103a.
 //
 // A paged prefill over an E4M3 cache whose requests have more query rows than the
-// tensor-core E4M3 decode takes (16 / G) runs the bf16 prefill kernels: their K/V tiles
-// stream by TMA straight into the tensor cores' swizzled operand layout, which has no
-// room for a conversion stage.  So the pages the call reads are converted first, into a
-// bf16 pool in the workspace.  E4M3 -> bf16 is exact (3 mantissa bits into 7, every E4M3
-// exponent and subnormal inside bf16's range); the scales are not applied here: k_scale
-// joins the score scale and v_scale the output scale of the prefill, as for the decode.
-// The extra traffic (one read of the E4M3 pages, one bf16 write and read) is small next to
-// a long prefill's tensor work.
+// tensor-core E4M3 decode takes (16 / G) runs the prefill kernels' converted-page
+// instances: their K/V tiles stream by TMA straight into the tensor cores' swizzled operand
+// layout, which has no room for a conversion stage.  So the pages the call reads are
+// converted first, into a pool in the workspace.  Both conversions are exact (every E4M3
+// value is a bf16 and an f16 value).  K is bf16 because Q.K^T pairs it with the bf16
+// queries; V is f16 so that P.V can take P rounded to f16 (11 bits) rather than bf16
+// (8 bits).  The scales are not applied here: k_scale joins the score scale and v_scale
+// the output scale of the prefill, as for the decode.  The extra traffic (one read of the
+// E4M3 pages, one write and read of the 2-byte pool) is small next to a long prefill's
+// tensor work.
 // Sources: FlashInfer documentation, flashinfer_benchmark.py "Attention Flags"
 // (--kv_dtype fp8_e4m3 for the prefill routines); FlashInfer documentation,
 // flashinfer.prefill (BatchPrefillWithPagedKVCacheWrapper: the paged prefill itself).
@@ -29,6 +31,20 @@ namespace pgqa {
 namespace dequant {
 
 constexpr int THREADS = 256;
+
+// 16 E4M3 bytes -> 16 f16 (exact: f16 holds every E4M3 value)
+__device__ __forceinline__ void e4m3x16_to_f16(const uint4& raw, uint4& lo, uint4& hi) {
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+    uint32_t out[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+            "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+            : "=r"(out[2 * i]), "=r"(out[2 * i + 1])
+            : "r"(w[i]));
+    lo = make_uint4(out[0], out[1], out[2], out[3]);
+    hi = make_uint4(out[4], out[5], out[6], out[7]);
+}
 
 // 16 E4M3 bytes -> 16 bf16, exactly (through f16, which holds every E4M3 value)
 __device__ __forceinline__ void e4m3x16_to_bf16(const uint4& raw, uint4& lo, uint4& hi) {
@@ -83,7 +99,7 @@ __global__ void __launch_bounds__(THREADS) dequant_pages_kernel(const Params p) 
             e4m3x16_to_bf16(rk, lo, hi);
             reinterpret_cast<uint4*>(kd + (long long)u * 16)[0] = lo;
             reinterpret_cast<uint4*>(kd + (long long)u * 16)[1] = hi;
-            e4m3x16_to_bf16(rv, lo, hi);
+            e4m3x16_to_f16(rv, lo, hi);  // V in f16: P.V then keeps P to f16 precision
             reinterpret_cast<uint4*>(vd + (long long)u * 16)[0] = lo;
             reinterpret_cast<uint4*>(vd + (long long)u * 16)[1] = hi;
         }

@@ -86,6 +86,7 @@ struct Params {
     int causal;
     float scale_log2;          // sm_scale * log2(e) (* k_scale for a dequantised FP8 cache)
     float v_scale;             // output scale (1, or v_scale for a dequantised FP8 cache)
+    int f8conv;                // K/V pages converted from E4M3: V (and so P) is f16 in P.V
     // paged K/V (paged kernels only): key j of request b is slot j % page_size of page
     // page_table[b * page_table_stride + j / page_size]; the K/V maps view each page pool
     // as a 4-D tensor {d, slot, head, page} (caller strides) with a box of one page of

@@ -589,10 +589,13 @@ __device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&r)[32]) {
         : "memory");
 }
 
-template <int D, bool PAGED, bool GROUPED>
+// F8CONV: K/V pages converted from an E4M3 cache, V to f16: P is rounded to f16 (not bf16)
+// and P.V runs on f16 operands, which keeps 11 bits of each weight instead of 8.
+template <int D, bool PAGED, bool GROUPED, bool F8CONV>
 __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
     using C = Cfg<D>;
     static_assert(!GROUPED || PAGED, "the grouped layout is for paged K/V");
+    static_assert(!F8CONV || PAGED, "converted pages are paged");
     // K/V stage layout: byte stride between 64-column chunks and between 8-row groups
     constexpr uint32_t KV_CH = GROUPED ? 1024u : (uint32_t)C::CHUNK_BYTES;
     constexpr uint32_t KV_SBO = GROUPED ? (uint32_t)C::CHUNKS * 1024u : 1024u;
@@ -794,7 +797,8 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, false);
-            constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, true);
+            constexpr uint32_t IDESC_PV =
+                F8CONV ? idesc_f16_f32(BM, D, true) : idesc_bf16_f32(BM, D, true);
             uint32_t load_idx = 0, q_count = 0, tile_ctr = 0, item_cnt = 0, fixes = 0;
             bool ok = true;
             auto issue_pv = [&](int jj, int n, bool fix) -> bool {
@@ -1008,7 +1012,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
                         const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
                         if (i & 1) acc1 = f2_add(acc1, f2_pack(p0, p1));
                         else acc0 = f2_add(acc0, f2_pack(p0, p1));
-                        pk[i] = pack_bf16x2(p0, p1);
+                        pk[i] = F8CONV ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
                     }
                     tmem_st32(s_addr + cc * 32, pk);
                 }
@@ -1129,9 +1133,10 @@ struct PairCfg {
 };
 
 
-// VSCALE: the output takes p.v_scale (a dequantised FP8 cache); a separate instance, so the
-// bf16 paths keep their code unchanged
-template <bool PAGED, bool VSCALE>
+// F8CONV: K/V pages converted from an E4M3 cache (V to f16): the output takes p.v_scale,
+// P is rounded to f16 and P.V runs on f16 operands; a separate instance, so the bf16 paths
+// keep their code unchanged
+template <bool PAGED, bool F8CONV>
 __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const Params p) {
     using C = PairCfg;
     constexpr int D = C::D;
@@ -1323,7 +1328,8 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
         // last P.V).
         if (lane == 0) {
             constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, false);
-            constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, true);
+            constexpr uint32_t IDESC_PV =
+                F8CONV ? idesc_f16_f32(BM, D, true) : idesc_bf16_f32(BM, D, true);
             const uint64_t qdesc0 = sdesc_sw128(sQ, 16, 1024);
             uint32_t load_idx = 0, q_count = 0, step = 0, fixes = 0;
             uint32_t ctr[2] = {0, 0}, items_x[2] = {0, 0};
@@ -1477,7 +1483,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
         };
         auto store_pending = [&](const uint32_t (&u)[4][32]) {
             if (!pend_valid) return;
-            const float inv_l = pend_l > 0.f ? (VSCALE ? p.v_scale : 1.f) / pend_l : 0.f;
+            const float inv_l = pend_l > 0.f ? (F8CONV ? p.v_scale : 1.f) / pend_l : 0.f;
             if (pend_slot >= 0) {  // split-KV partial: O / l in fp32 and the chunk's lse
                 float4* op = reinterpret_cast<float4*>(p.part_o + pend_slot * D);
 #pragma unroll
@@ -1605,7 +1611,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
                         const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
                         if (i & 1) acc1 = f2_add(acc1, f2_pack(p0, p1));
                         else acc0 = f2_add(acc0, f2_pack(p0, p1));
-                        pk[i] = pack_bf16x2(p0, p1);
+                        pk[i] = F8CONV ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
                     }
                     tmem_st32(s_addr + cc * 32, pk);
                     if (cc == 0 && early) {
@@ -1782,51 +1788,55 @@ static cudaError_t launch_dependent(Kernel kernel, int grid, int threads, int sm
     return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
-template <int D, bool PAGED, bool GROUPED>
+template <int D, bool PAGED, bool GROUPED, bool F8CONV>
 static cudaError_t launch_attention_t(const Params& p, int grid, cudaStream_t stream) {
     static std::atomic<bool> configured[64];  // per device, set once (repeats are harmless)
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !configured[dev].load(std::memory_order_acquire)) {
-        cudaError_t e = cudaFuncSetAttribute(attention_kernel<D, PAGED, GROUPED>,
+        cudaError_t e = cudaFuncSetAttribute(attention_kernel<D, PAGED, GROUPED, F8CONV>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              Cfg<D>::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         configured[dev].store(true, std::memory_order_release);
     }
-    return launch_dependent(attention_kernel<D, PAGED, GROUPED>, grid, THREADS,
+    return launch_dependent(attention_kernel<D, PAGED, GROUPED, F8CONV>, grid, THREADS,
                             Cfg<D>::SMEM_BYTES, stream, p);
 }
 
-// grouped: paged K/V through 5-D tensor maps filling the grouped stage layout
+// grouped: paged K/V through 5-D tensor maps filling the grouped stage layout; p.f8conv:
+// pages converted from an E4M3 cache
 template <int D, bool PAGED>
 cudaError_t launch_attention(const Params& p, int grid, bool grouped, cudaStream_t stream) {
     if constexpr (PAGED) {
-        if (grouped) return launch_attention_t<D, true, true>(p, grid, stream);
+        if (p.f8conv)
+            return grouped ? launch_attention_t<D, true, true, true>(p, grid, stream)
+                           : launch_attention_t<D, true, false, true>(p, grid, stream);
+        if (grouped) return launch_attention_t<D, true, true, false>(p, grid, stream);
     }
-    return launch_attention_t<D, PAGED, false>(p, grid, stream);
+    return launch_attention_t<D, PAGED, false, false>(p, grid, stream);
 }
 
-template <bool PAGED, bool VSCALE>
+template <bool PAGED, bool F8CONV>
 static cudaError_t launch_pair_t(const Params& p, int grid, cudaStream_t stream) {
     static std::atomic<bool> configured[64];  // per device, set once (repeats are harmless)
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !configured[dev].load(std::memory_order_acquire)) {
-        cudaError_t e = cudaFuncSetAttribute(attention_pair_kernel<PAGED, VSCALE>,
+        cudaError_t e = cudaFuncSetAttribute(attention_pair_kernel<PAGED, F8CONV>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              PairCfg::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         configured[dev].store(true, std::memory_order_release);
     }
-    return launch_dependent(attention_pair_kernel<PAGED, VSCALE>, grid, PAIR_THREADS,
+    return launch_dependent(attention_pair_kernel<PAGED, F8CONV>, grid, PAIR_THREADS,
                             PairCfg::SMEM_BYTES, stream, p);
 }
 
 template <bool PAGED>
 cudaError_t launch_attention_pair(const Params& p, int grid, cudaStream_t stream) {
     if constexpr (PAGED) {
-        if (p.v_scale != 1.f) return launch_pair_t<true, true>(p, grid, stream);
+        if (p.f8conv) return launch_pair_t<true, true>(p, grid, stream);
     }
     return launch_pair_t<PAGED, false>(p, grid, stream);
 }

@@ -289,6 +289,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_ma
     return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
+// Instruction descriptor, kind::f16 with f16 A and B (format 0), fp32 D; B MN-major when
+// b_mn_major (bit 16).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool b_mn_major) {
+    return (1u << 4) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
 // Instruction descriptor, kind::f8f6f4: E4M3 A and B (format 0), fp32 D, dense; B K-major,
 // A K-major or MN-major (bit 15).  Same field positions as kind::f16.
 __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, bool a_mn_major) {
@@ -346,6 +353,11 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float d;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
     return d;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

@@ -148,7 +148,7 @@ def test_e4m3_decode_sweep(cuda_lib, case):
 def test_e4m3_prefill_sweep(cuda_lib, case):
     """The E4M3 paged prefill on both of its paths: few query rows per request (the
     tensor-core path, max_qo_len * G <= 16) or longer runs and head_dim 256 (the pages
-    converted to bf16 first); causal or not, both layouts, random scales."""
+    converted first, K to bf16 and V to f16); causal or not, both layouts, random scales."""
     rng = np.random.default_rng(13000 + case)
     batch = int(rng.integers(1, 6))
     hq, hk = _heads(rng, [1, 2, 4, 8])
