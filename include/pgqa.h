@@ -89,6 +89,9 @@ enum {
  *
  * Supported: head_dim 128 or 256; num_qo_heads a multiple of num_kv_heads with group
  * size G = num_qo_heads / num_kv_heads dividing 128.  batch == 0 returns PGQA_OK at once.
+ * With batch > 0 every pointer but lse must be non-NULL even where total_q or total_kv is
+ * 0 (the totals are never read on the host); a buffer of one row serves, since no row
+ * outside the indptr ranges is read.
  * Errors: PGQA_ERR_INVALID_ARG for NULL/misaligned pointers or bad counts,
  * PGQA_ERR_UNSUPPORTED for other shapes, PGQA_ERR_WORKSPACE if the workspace is too
  * small while the stream is being captured (or a caller-supplied workspace cannot hold

@@ -96,6 +96,24 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+def _with_rows(t):
+    """t itself, or a one-row stand-in when t has no rows (a tensor without elements has no
+    device address to pass; the calls never read rows their indptr does not cover)."""
+    return t if t.shape[0] > 0 else torch.zeros((1,) + tuple(t.shape[1:]), dtype=t.dtype,
+                                                device=t.device)
+
+
+def _pool_with_page(t, page_size, hk, d, strides):
+    """t itself, or a zeroed stand-in spanning one page under `strides` when the pool has no
+    pages.  The call still gets num_pages = 0, so any page id a request names is reported
+    out of bounds; the stand-in only gives the pool a device address."""
+    if t.shape[0] > 0:
+        return t
+    _, slot_s, head_s = strides
+    span = (page_size - 1) * slot_s + (hk - 1) * head_s + d
+    return torch.zeros(span, dtype=t.dtype, device=t.device)
+
+
 def _stream(stream, dev=None):
     """The stream handle for a call on device `dev` (default: its current stream)."""
     if stream is None:
@@ -183,6 +201,9 @@ def ragged_prefill(q, k, v, q_indptr, kv_indptr, causal=True, sm_scale=None, out
     if lse is not None:
         _check(lse, "lse", torch.float32, 2, dev)
     batch = q_indptr.numel() - 1
+    if total_q == 0:  # no query rows in any request: nothing to compute or write
+        return out, lse
+    k, v = _with_rows(k), _with_rows(v)  # no keys at all: every row gets zeros, lse -inf
     with torch.cuda.device(dev):  # the library works on the current device
         rc = lib.pgqa_ragged_prefill_bf16(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
                                           _ptr(q_indptr), _ptr(kv_indptr), batch, hq, hk, d,
@@ -234,8 +255,12 @@ def paged_prefill(q, k_pages, v_pages, q_indptr, page_table, kv_lens, causal=Tru
         lse = torch.empty((total_q, hq), dtype=torch.float32, device=dev)
     if lse is not None:
         _check(lse, "lse", torch.float32, 2, dev)
+    if total_q == 0:  # no query rows in any request: nothing to compute or write
+        return out, lse
     name = ("pgqa_paged_prefill_e4m3" if e4m3 else
             "pgqa_paged_prefill_bf16" if packed else "pgqa_paged_prefill_bf16_strided")
+    k_pages = _pool_with_page(k_pages, page_size, hk, d, strides)
+    v_pages = _pool_with_page(v_pages, page_size, hk, d, strides)
     with torch.cuda.device(dev):  # the library works on the current device
         st = _stream(stream, dev)
         if e4m3:
@@ -294,6 +319,8 @@ def paged_decode(q, k_pages, v_pages, page_table, kv_lens, sm_scale=None, out=No
         _check(lse, "lse", torch.float32, 2, dev)
     name = ("pgqa_paged_decode_e4m3" if e4m3 else
             "pgqa_paged_decode_bf16" if packed else "pgqa_paged_decode_bf16_strided")
+    k_pages = _pool_with_page(k_pages, page_size, hk, d, strides)
+    v_pages = _pool_with_page(v_pages, page_size, hk, d, strides)
     with torch.cuda.device(dev):  # the library works on the current device
         st = _stream(stream, dev)
         if e4m3:

@@ -169,3 +169,16 @@ def test_pending_status_survives_workspace_growth(cuda_lib):
     run_gpu(cuda_lib, big)
     assert cuda_lib.device_status() == -6
     assert cuda_lib.device_status() == 0
+
+
+@pytest.mark.parametrize("e4m3", [False, True], ids=["bf16", "e4m3"])
+def test_pool_without_pages(cuda_lib, e4m3):
+    """Requests with no keys over a pool with no pages: every row is zeros, lse = -inf."""
+    make = W.paged_case_e4m3 if e4m3 else W.paged_case
+    pc = make([0, 0, 0], 8, 2, 128, seed=10, device="cuda")
+    pc.k_pages, pc.v_pages = pc.k_pages[:0], pc.v_pages[:0]
+    kw = dict(k_scale=pc.meta["k_scale"], v_scale=pc.meta["v_scale"]) if e4m3 else {}
+    o, lse = run_gpu(cuda_lib, pc, **kw)
+    assert cuda_lib.device_status() == 0
+    assert torch.equal(o, torch.zeros_like(o))
+    assert torch.equal(lse, torch.full_like(lse, -float("inf")))

@@ -254,3 +254,23 @@ def test_split_kv_hd256_ragged_and_paged_agree_bitwise(cuda_lib):
     ro, rl = oracle_paged(pc)
     check_rows(o_p.reshape(-1, 256).float().cpu(), l_p.reshape(-1).cpu(), ro, rl,
                "split-KV hd256 decode mix")
+
+
+@pytest.mark.parametrize("e4m3", [False, True], ids=["bf16", "e4m3"])
+def test_calls_with_no_query_rows_or_no_pages(cuda_lib, e4m3):
+    """A call whose requests hold no query rows returns the empty outputs; over a pool with
+    no pages and requests with no keys, every row is zeros with lse = -inf."""
+    make = W.paged_case_e4m3 if e4m3 else W.paged_case
+    pc = make([37, 0], 8, 2, 128, qo_lens=[0, 0], seed=8, device="cuda")
+    kw = dict(k_scale=pc.meta["k_scale"], v_scale=pc.meta["v_scale"]) if e4m3 else {}
+    o, lse = run_gpu(cuda_lib, pc, **kw)
+    assert cuda_lib.device_status() == 0
+    assert o.shape == (0, 8, 128) and lse.shape == (0, 8)
+    for max_qo in ([None, 4] if e4m3 else [None]):  # E4M3: conversion and tensor-core forms
+        pc = make([0, 0], 8, 2, 128, qo_lens=[3, 4], seed=9, device="cuda")
+        pc.k_pages, pc.v_pages = pc.k_pages[:0], pc.v_pages[:0]
+        o, lse = run_gpu(cuda_lib, pc, **kw, **({} if max_qo is None else
+                                                 dict(max_qo_len=max_qo)))
+        assert cuda_lib.device_status() == 0
+        assert torch.equal(o, torch.zeros_like(o))
+        assert torch.equal(lse, torch.full_like(lse, -float("inf")))

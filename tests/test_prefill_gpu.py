@@ -147,3 +147,16 @@ def test_bad_indptr_reports_bounds_status(cuda_lib):
     assert cuda_lib.device_status() == -6
     assert bool((out == 7.0).all())                      # nothing written
     run_gpu(cuda_lib, case)                              # library still usable
+
+
+def test_calls_with_no_query_rows_or_no_keys(cuda_lib):
+    """A call whose requests hold no query rows returns the empty outputs; a call whose
+    requests hold no keys (K/V without rows) gives every row zeros and lse = -inf."""
+    case = W.ragged_case([0], [37], 8, 2, 128, seed=6, device="cuda")
+    o, lse = run_gpu(cuda_lib, case)
+    assert o.shape == (0, 8, 128) and lse.shape == (0, 8)
+    case = W.ragged_case([5, 70], [0, 0], 8, 2, 128, seed=7, device="cuda")
+    assert case.k.shape[0] == 0
+    o, lse = run_gpu(cuda_lib, case)
+    assert torch.equal(o, torch.zeros_like(o))
+    assert torch.equal(lse, torch.full_like(lse, -float("inf")))
