@@ -324,6 +324,23 @@ __device__ __forceinline__ void store_col_e4m3(uint8_t* op, int c, const float (
     }
 }
 
+// Row r (key r) of the P^T operand with 16 query columns, read MN-major with 32-byte swizzle:
+// 32 bytes per key, the hi parts of v[0..15] (N = 0..15) and then their lo parts (N =
+// 16..31), each half one 16-byte unit; the two units swap places in rows 4-7 of every 8.
+__device__ __forceinline__ void store_row_e4m3_sw32(uint8_t* op, int r, const float (&v)[NH]) {
+    uint32_t h[8], l[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) e4m3_split2(v[2 * k], v[2 * k + 1], h[k], l[k]);
+    const uint4 hv = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
+                                h[6] | (h[7] << 16));
+    const uint4 lv = make_uint4(l[0] | (l[1] << 16), l[2] | (l[3] << 16), l[4] | (l[5] << 16),
+                                l[6] | (l[7] << 16));
+    const int sw = (r >> 2) & 1;
+    uint4* row = reinterpret_cast<uint4*>(op + 32 * r);
+    row[sw] = hv;
+    row[sw ^ 1] = lv;
+}
+
 // G query heads per kv head; NR = the MMA's used N columns: G (one query row per request)
 // or 16 (up to 16 / G query rows per request)
 template <int G, int NR>
@@ -494,10 +511,10 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
             // Q.K^T: packed, N = 16 (hi and lo rows in one operand); otherwise N = 32 over
             // the hi and lo operands (rows 0-15 and 16-31), S^T columns n and 16 + n
             constexpr uint32_t IDESC_S = idesc_e4m3_f32(TK, PACK ? NH : 2 * NH, false);
-            // P.V: packed, N = 16 (hi and lo rows in one operand); otherwise the hi and lo
-            // operands are rows 0-15 and 16-31 of one 32-row operand: N = 32, O^T columns
-            // n and 16 + n
-            constexpr uint32_t IDESC_O = idesc_e4m3_f32(D, PACK ? NH : 2 * NH, true);
+            // P.V: packed, N = 16 (hi and lo rows in one K-major operand); otherwise one
+            // MN-major operand of 32 columns per key, the hi parts then the lo parts: N =
+            // 32, O^T columns n and 16 + n
+            constexpr uint32_t IDESC_O = idesc_e4m3_f32(D, PACK ? NH : 2 * NH, true, !PACK);
             uint32_t ld = 0, pt = 0, s = 0;  // ring position, P^T tiles, items
             bool ok = true;
             auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
@@ -552,12 +569,16 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
                     tc_fence_after();
                     // A = V^T: the raw V tile read MN-major (a key's 128 dims are one
                     // 128-byte row, 8-key groups 1 KB apart; 32 keys per MMA); B = the P^T
-                    // parts: 16 rows (columns) of 128 keys, K-major
+                    // parts: packed, 16 rows (columns) of 128 keys, K-major (32 keys = 32
+                    // bytes per MMA); otherwise a 32-byte row per key, MN-major (8-key
+                    // groups 256 bytes apart, 32 keys = 1 KB per MMA)
                     const uint64_t vd = sdesc_sw128(s0 + OFF_RAW + st * RAW_BYTES, RAW_BYTES, 1024);
-                    const uint64_t ph = sdesc_sw128(s0 + OFF_P + pb * P_STRIDE, 16, 1024);
+                    const uint64_t ph = PACK ? sdesc_sw128(s0 + OFF_P + pb * P_STRIDE, 16, 1024)
+                                             : sdesc_sw32(s0 + OFF_P + pb * P_STRIDE, P_STRIDE, 256);
+                    constexpr uint32_t PH_STEP = PACK ? 2u : 64u;  // 16-byte units per MMA
 #pragma unroll
                     for (int k = 0; k < TK / 32; ++k)
-                        mma_e4m3_ss(tmem_base + TMEM_O, vd + 256u * k, ph + 2u * k, IDESC_O,
+                        mma_e4m3_ss(tmem_base + TMEM_O, vd + 256u * k, ph + PH_STEP * k, IDESC_O,
                                     (t > 0 || k > 0) ? 1u : 0u);
                     mma_commit(BAR(RAW_EMPTY + st));
                     // packed: a buffer is next written for the next item, after that item's
@@ -871,7 +892,10 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
                                                                    p.status));
                     if (!ok) break;
                 }
-                store_col_e4m3<NR, PACK>(smem + OFF_P + pb * P_STRIDE, r, pv);
+                if constexpr (PACK)
+                    store_col_e4m3<NR, PACK>(smem + OFF_P + pb * P_STRIDE, r, pv);
+                else
+                    store_row_e4m3_sw32(smem + OFF_P + pb * P_STRIDE, r, pv);
                 if constexpr (!PACK) {
                     fence_async_smem();
                     __syncwarp();

@@ -282,6 +282,14 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
            ((uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// The same with 32-byte swizzle (swizzle mode 6): rows of 32 bytes whose two 16-byte units
+// swap places in rows 4-7 of every 8 (byte address bit 4 XOR bit 7).
+__device__ __forceinline__ uint64_t sdesc_sw32(uint32_t saddr, uint32_t lbo_bytes,
+                                               uint32_t sbo_bytes) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (6ull << 61);
+}
+
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 D, dense.
 //   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format (1 = bf16),
 //   bit 15 A major (0 = K), bit 16 B major (1 = MN), 17-22 N >> 3, 24-28 M >> 4.
@@ -296,11 +304,12 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool b_mn_maj
            ((uint32_t)(M >> 4) << 24);
 }
 
-// Instruction descriptor, kind::f8f6f4: E4M3 A and B (format 0), fp32 D, dense; B K-major,
-// A K-major or MN-major (bit 15).  Same field positions as kind::f16.
-__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, bool a_mn_major) {
-    return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((uint32_t)(N >> 3) << 17) |
-           ((uint32_t)(M >> 4) << 24);
+// Instruction descriptor, kind::f8f6f4: E4M3 A and B (format 0), fp32 D, dense; A and B
+// K-major or MN-major (bits 15 and 16).  Same field positions as kind::f16.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, bool a_mn_major,
+                                                      bool b_mn_major = false) {
+    return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // Two floats as E4M3 pairs hi + lo: hi = E4M3(x), lo = E4M3(x - hi) with x rounded to f16
