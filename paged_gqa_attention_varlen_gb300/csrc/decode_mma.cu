@@ -35,7 +35,7 @@
 //  * warp 1, lane 0: MMA issuer (swap-AB, keys as M = 128, query columns padded to N =
 //    16; with several query rows per request, column n is row n / G, head n % G):
 //      S^T_t  = K_t . (Qhi + Qlo)^T     A = raw K tile (K-major), B = Q parts (K-major)
-//      O^T   += V_t^T . (Phi + Plo)^T   A = raw V tile (MN-major), B = P^T parts (K-major)
+//      O^T   += V_t^T . (Phi + Plo)^T   A = raw V tile (MN-major), B = P^T parts (MN-major)
 //    Every S^T tile of an item stays in tensor memory (two item regions of 8 x 16
 //    columns), so the softmax sees the whole item at once; O^T takes 16 (or 32) more.
 //    Keys past the chunk and units whose page was not loaded must not reach P . V as
@@ -49,8 +49,9 @@
 //  * warps 4-7, softmax: thread r owns key r of every tile (TMEM lane r).  Per item: one
 //    pass over all its S^T tiles gives the exact max per column (a transposing warp
 //    butterfly and one exchange among the four warps), so no running rescale is needed;
-//    then each tile's P^T = 2^8 exp2(s - max) goes to shared memory as E4M3 hi/lo bytes
-//    (row = column n, byte = key; 8 buffers of one item when packed, 4 otherwise) while
+//    then each tile's P^T = 2^8 exp2(s - max) goes to shared memory as E4M3 hi/lo bytes,
+//    one row per key that its thread writes with one or two 16-byte stores (8 buffers of
+//    one item when packed, 4 otherwise) while
 //    the column sums accumulate; at the item's end
 //    thread r holds row r of O^T: divided by l, scaled by v_scale, it becomes the bf16
 //    output (single-chunk request) or the fp32 partial and its lse.
@@ -341,6 +342,21 @@ __device__ __forceinline__ void store_row_e4m3_sw32(uint8_t* op, int r, const fl
     row[sw ^ 1] = lv;
 }
 
+// Row r (key r) of the packed P^T operand (NR <= 8 query columns), read MN-major without
+// swizzle: 16 bytes per key, the hi parts of v[0..7] (N = 0..7) and their lo parts (N =
+// 8..15); columns past NR are zero.
+template <int NR>
+__device__ __forceinline__ void store_row_e4m3_p16(uint8_t* op, int r, const float (&v)[NR]) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        h[k] = l[k] = 0u;
+        if (2 * k < NR) e4m3_split2(v[2 * k], 2 * k + 1 < NR ? v[2 * k + 1] : 0.f, h[k], l[k]);
+    }
+    reinterpret_cast<uint4*>(op)[r] =
+        make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), l[0] | (l[1] << 16), l[2] | (l[3] << 16));
+}
+
 // G query heads per kv head; NR = the MMA's used N columns: G (one query row per request)
 // or 16 (up to 16 / G query rows per request)
 template <int G, int NR>
@@ -511,10 +527,10 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
             // Q.K^T: packed, N = 16 (hi and lo rows in one operand); otherwise N = 32 over
             // the hi and lo operands (rows 0-15 and 16-31), S^T columns n and 16 + n
             constexpr uint32_t IDESC_S = idesc_e4m3_f32(TK, PACK ? NH : 2 * NH, false);
-            // P.V: packed, N = 16 (hi and lo rows in one K-major operand); otherwise one
-            // MN-major operand of 32 columns per key, the hi parts then the lo parts: N =
-            // 32, O^T columns n and 16 + n
-            constexpr uint32_t IDESC_O = idesc_e4m3_f32(D, PACK ? NH : 2 * NH, true, !PACK);
+            // P.V: B = P^T MN-major, a row of columns per key, the hi parts then the lo
+            // parts: packed, N = 16 (O^T columns n and 8 + n); otherwise N = 32 (O^T
+            // columns n and 16 + n)
+            constexpr uint32_t IDESC_O = idesc_e4m3_f32(D, PACK ? NH : 2 * NH, true, true);
             uint32_t ld = 0, pt = 0, s = 0;  // ring position, P^T tiles, items
             bool ok = true;
             auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
@@ -568,14 +584,15 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
                     }
                     tc_fence_after();
                     // A = V^T: the raw V tile read MN-major (a key's 128 dims are one
-                    // 128-byte row, 8-key groups 1 KB apart; 32 keys per MMA); B = the P^T
-                    // parts: packed, 16 rows (columns) of 128 keys, K-major (32 keys = 32
-                    // bytes per MMA); otherwise a 32-byte row per key, MN-major (8-key
-                    // groups 256 bytes apart, 32 keys = 1 KB per MMA)
+                    // 128-byte row, 8-key groups 1 KB apart; 32 keys per MMA); B = P^T,
+                    // MN-major: packed, a 16-byte row per key without swizzle (8-key core
+                    // matrices of 128 bytes, 32 keys = 512 bytes per MMA); otherwise a
+                    // 32-byte row per key with 32-byte swizzle (8-key groups 256 bytes
+                    // apart, 32 keys = 1 KB per MMA)
                     const uint64_t vd = sdesc_sw128(s0 + OFF_RAW + st * RAW_BYTES, RAW_BYTES, 1024);
-                    const uint64_t ph = PACK ? sdesc_sw128(s0 + OFF_P + pb * P_STRIDE, 16, 1024)
+                    const uint64_t ph = PACK ? sdesc_plain(s0 + OFF_P + pb * P_STRIDE, 128, 128)
                                              : sdesc_sw32(s0 + OFF_P + pb * P_STRIDE, P_STRIDE, 256);
-                    constexpr uint32_t PH_STEP = PACK ? 2u : 64u;  // 16-byte units per MMA
+                    constexpr uint32_t PH_STEP = PACK ? 32u : 64u;  // 16-byte units per MMA
 #pragma unroll
                     for (int k = 0; k < TK / 32; ++k)
                         mma_e4m3_ss(tmem_base + TMEM_O, vd + 256u * k, ph + PH_STEP * k, IDESC_O,
@@ -893,7 +910,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
                     if (!ok) break;
                 }
                 if constexpr (PACK)
-                    store_col_e4m3<NR, PACK>(smem + OFF_P + pb * P_STRIDE, r, pv);
+                    store_row_e4m3_p16<NR>(smem + OFF_P + pb * P_STRIDE, r, pv);
                 else
                     store_row_e4m3_sw32(smem + OFF_P + pb * P_STRIDE, r, pv);
                 if constexpr (!PACK) {

@@ -290,6 +290,14 @@ __device__ __forceinline__ uint64_t sdesc_sw32(uint32_t saddr, uint32_t lbo_byte
            ((uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (6ull << 61);
 }
 
+// The same without swizzle (swizzle mode 0): 8-row core matrices of 16-byte rows, 128
+// contiguous bytes each, `lbo_bytes` / `sbo_bytes` apart along the two dimensions.
+__device__ __forceinline__ uint64_t sdesc_plain(uint32_t saddr, uint32_t lbo_bytes,
+                                                uint32_t sbo_bytes) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+}
+
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 D, dense.
 //   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format (1 = bf16),
 //   bit 15 A major (0 = K), bit 16 B major (1 = MN), 17-22 N >> 3, 24-28 M >> 4.
