@@ -29,7 +29,7 @@
 // to 8 tiles of 128 keys; the items of a CTA run as a software pipeline in which step s
 // handles the K tiles of item s and the V tiles of item s - 1):
 //  * warps 0, 2 and 3, producers: stream 128-key tiles of E4M3 bytes in step order through
-//    a 12-stage TMA ring, each taking every third tile; lane u < 8 loads the 16-key unit u
+//    a TMA ring of 12 stages (11 with several query rows), each taking every third tile; lane u < 8 loads the 16-key unit u
 //    of a tile (a 16-token page, or a slice of a larger page) as one 2 KB box, 128-byte
 //    swizzled: 128 rows (keys) of 128 bytes (dims).  Page ids are read one item ahead.
 //  * warp 1, lane 0: MMA issuer (swap-AB, keys as M = 128, query columns padded to N =
@@ -50,8 +50,8 @@
 //    pass over all its S^T tiles gives the exact max per column (a transposing warp
 //    butterfly and one exchange among the four warps), so no running rescale is needed;
 //    then each tile's P^T = 2^8 exp2(s - max) goes to shared memory as E4M3 hi/lo bytes,
-//    one row per key that its thread writes with one or two 16-byte stores (8 buffers of
-//    one item when packed, 4 otherwise) while
+//    one row per key that its thread writes with one or two 16-byte stores (one buffer
+//    per tile of the item) while
 //    the column sums accumulate; at the item's end
 //    thread r holds row r of O^T: divided by l, scaled by v_scale, it becomes the bf16
 //    output (single-chunk request) or the fp32 partial and its lse.
@@ -70,8 +70,6 @@ constexpr int D = HEAD_DIM;                 // 128
 constexpr int TK = 128;                     // keys per tile = the MMA's M
 constexpr int NH = 16;                      // query columns, padded = the MMA's N
 constexpr int UNITS = TK / PAGE;            // 16-key units per tile (8)
-constexpr int RAW_STAGES = 12;
-constexpr int NPB_MAX = 8;                  // P^T buffers: 8 of one operand (packed) or 4 pairs
 constexpr int MAX_TILES = 8;                // tiles per item (chunks of at most 1024 keys)
 constexpr int MAX_TILES_ROWS = CHUNK_E4M3_ROWS / TK;  // ... with several query rows (896 keys)
 static_assert(MAX_TILES_ROWS * TK == CHUNK_E4M3_ROWS, "whole tiles");
@@ -89,26 +87,38 @@ constexpr float P_LOG2_SCALE = 8.f;         // P^T holds 2^8 P
 // O^T at 448 (32 columns, the hi and lo parts of P).
 constexpr int TMEM_COLS = 512;
 
-constexpr int OFF_RAW = 0;
-constexpr int OFF_Q = OFF_RAW + RAW_STAGES * RAW_BYTES;   // two buffers (hi, lo)
-constexpr int OFF_P = OFF_Q + 2 * QP_BYTES;               // the P^T buffers (16 KB)
-constexpr int OFF_RED = OFF_P + 4 * QP_BYTES;             // exchange areas (1 KB)
-constexpr int OFF_MASK = OFF_RED + 1024;  // loaded-unit bits per raw stage (<= 16 words),
-                                          // the q exponents (2 words at +64) and the per-item
-                                          // unit masks (2 x 64 bits at +72)
-constexpr int OFF_ITEM = OFF_MASK + 96;   // the geometry of the items in the two Q buffers
-constexpr int OFF_BAR = OFF_ITEM + 128;
-
-// barrier indices
-constexpr int RAW_FULL = 0, RAW_EMPTY = RAW_FULL + RAW_STAGES, Q_FULL = RAW_EMPTY + RAW_STAGES,
-              Q_EMPTY = Q_FULL + 2, S_FULL = Q_EMPTY + 2, S_EMPTY = S_FULL + 2,
-              P_FULL = S_EMPTY + 2, P_EMPTY = P_FULL + NPB_MAX, PV_LAST = P_EMPTY + NPB_MAX,
-              O_EMPTY = PV_LAST + 1,
-              MMA_DRAIN = O_EMPTY + 1, XCH_Q = MMA_DRAIN + 1, XCH_SMX = XCH_Q + 1,
-              NUM_BARS = XCH_SMX + 1;
-constexpr int SMEM_BYTES = 1024 + OFF_BAR + 8 * NUM_BARS + 16;
-static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
-static_assert(RAW_STAGES <= 16, "unit-mask words");
+// Shared memory.  Every tile of an item has its own P^T buffer, and the softmax writes an
+// item's P^T only after the previous item's last P . V has completed (its epilogue waits
+// for that), so no buffer needs a release of its own.  Packed (one query row): 8 buffers
+// of 2 KB beside a 12-stage raw ring, an item's tiles published at once; several query
+// rows: 7 buffers of 4 KB (items of at most 896 keys) beside 11 raw stages, each tile
+// published as it is written.
+template <bool PACK>
+struct Layout {
+    static constexpr int RAW_STAGES = PACK ? 12 : 11;
+    static constexpr int NPB = PACK ? MAX_TILES : MAX_TILES_ROWS;   // P^T buffers
+    static constexpr uint32_t P_STRIDE = PACK ? (uint32_t)OP_BYTES : (uint32_t)QP_BYTES;
+    static constexpr int OFF_RAW = 0;
+    static constexpr int OFF_Q = OFF_RAW + RAW_STAGES * RAW_BYTES;  // two buffers (hi, lo)
+    static constexpr int OFF_P = OFF_Q + 2 * QP_BYTES;              // the P^T buffers
+    static constexpr int OFF_RED = OFF_P + NPB * (int)P_STRIDE;     // exchange areas (1 KB)
+    // loaded-unit bits per raw stage (<= 16 words), the q exponents (2 words at +64) and
+    // the per-item unit masks (2 x 64 bits at +72)
+    static constexpr int OFF_MASK = OFF_RED + 1024;
+    static constexpr int OFF_ITEM = OFF_MASK + 96;  // the items in the two Q buffers
+    static constexpr int OFF_BAR = OFF_ITEM + 128;
+    // barrier indices; P_FULL: by item parity (packed) or by buffer
+    static constexpr int RAW_FULL = 0, RAW_EMPTY = RAW_FULL + RAW_STAGES,
+                         Q_FULL = RAW_EMPTY + RAW_STAGES, Q_EMPTY = Q_FULL + 2,
+                         S_FULL = Q_EMPTY + 2, S_EMPTY = S_FULL + 2, P_FULL = S_EMPTY + 2,
+                         N_PFULL = PACK ? 2 : NPB, PV_LAST = P_FULL + N_PFULL,
+                         O_EMPTY = PV_LAST + 1, MMA_DRAIN = O_EMPTY + 1, XCH_Q = MMA_DRAIN + 1,
+                         XCH_SMX = XCH_Q + 1, NUM_BARS = XCH_SMX + 1;
+    static constexpr int SMEM_BYTES = 1024 + OFF_BAR + 8 * NUM_BARS + 16;
+    static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+    static_assert(RAW_STAGES <= 16, "unit-mask words");
+    static_assert(OFF_P % 1024 == 0 && P_STRIDE % 1024 == 0, "operand alignment");
+};
 
 // Byte (row, col) of a 128-byte-swizzled K-major E4M3 operand (rows of 128 bytes, 16-byte
 // units XORed with row % 8, 8-row groups 1 KB apart).
@@ -367,10 +377,16 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
     // NR <= 8: hi and lo of Q and P^T share one operand (rows n and 8 + n), so one MMA
     // per 32-element step covers both and S^T / O^T column 8 + n holds column n's lo part
     constexpr bool PACK = NR <= 8;
-    // P^T buffers: packed, 8 of one 2 KB operand, so an item's tiles never wait for one;
-    // otherwise 4 of a hi/lo pair
-    constexpr int NPB = PACK ? NPB_MAX : 4;
-    constexpr uint32_t P_STRIDE = PACK ? (uint32_t)OP_BYTES : (uint32_t)QP_BYTES;
+    using L = Layout<PACK>;
+    constexpr int RAW_STAGES = L::RAW_STAGES, NPB = L::NPB;
+    constexpr uint32_t P_STRIDE = L::P_STRIDE;
+    constexpr int OFF_RAW = L::OFF_RAW, OFF_Q = L::OFF_Q, OFF_P = L::OFF_P, OFF_RED = L::OFF_RED,
+                  OFF_MASK = L::OFF_MASK, OFF_ITEM = L::OFF_ITEM, OFF_BAR = L::OFF_BAR;
+    constexpr int RAW_FULL = L::RAW_FULL, RAW_EMPTY = L::RAW_EMPTY, Q_FULL = L::Q_FULL,
+                  Q_EMPTY = L::Q_EMPTY, S_FULL = L::S_FULL, S_EMPTY = L::S_EMPTY,
+                  P_FULL = L::P_FULL, PV_LAST = L::PV_LAST, O_EMPTY = L::O_EMPTY,
+                  MMA_DRAIN = L::MMA_DRAIN, XCH_Q = L::XCH_Q, XCH_SMX = L::XCH_SMX,
+                  NUM_BARS = L::NUM_BARS;
     constexpr uint32_t S_COLS = PACK ? 16u : 32u;  // tensor-memory columns of an S^T tile
     constexpr uint32_t S_REGION = PACK ? 16u * MAX_TILES : 32u * MAX_TILES_ROWS;
     constexpr uint32_t TMEM_O = 2u * S_REGION;
@@ -407,10 +423,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
             mbar_init(BAR(S_FULL + x), 1);
             mbar_init(BAR(S_EMPTY + x), 4);
         }
-        for (int x = 0; x < NPB_MAX; ++x) {
-            mbar_init(BAR(P_FULL + x), 4);
-            mbar_init(BAR(P_EMPTY + x), 1);
-        }
+        for (int x = 0; x < L::N_PFULL; ++x) mbar_init(BAR(P_FULL + x), 4);
         mbar_init(BAR(PV_LAST), 1);
         mbar_init(BAR(O_EMPTY), 4);
         mbar_init(BAR(MMA_DRAIN), 1);
@@ -420,7 +433,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
         fence_barrier_init();
     }
     // Q rows and P^T rows NR..15 stay zero: clear every buffer once
-    for (int i = threadIdx.x; i < (2 + 4) * QP_BYTES / 16; i += THREADS)
+    for (int i = threadIdx.x; i < (2 * QP_BYTES + NPB * (int)P_STRIDE) / 16; i += THREADS)
         reinterpret_cast<uint4*>(smem + OFF_Q)[i] = make_uint4(0, 0, 0, 0);
     fence_async_smem();
     if (warp == 1) {
@@ -597,11 +610,10 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
                     for (int k = 0; k < TK / 32; ++k)
                         mma_e4m3_ss(tmem_base + TMEM_O, vd + 256u * k, ph + PH_STEP * k, IDESC_O,
                                     (t > 0 || k > 0) ? 1u : 0u);
-                    mma_commit(BAR(RAW_EMPTY + st));
-                    // packed: a buffer is next written for the next item, after that item's
+                    // a P^T buffer is next written for the next item, after that item's
                     // softmax has waited for this item's last P.V (its epilogue), so it
                     // needs no release of its own
-                    if constexpr (!PACK) mma_commit(BAR(P_EMPTY + pb));
+                    mma_commit(BAR(RAW_EMPTY + st));
                 }
                 if (ok) mma_commit(BAR(PV_LAST));
             };
@@ -874,7 +886,8 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
                 epilogue(prev, s - 1, prev_m, prev_l);
                 if (!ok) break;
             }
-            // (C) P^T tiles, E4M3 hi/lo, into the ring of NPB buffers the P.V MMAs read
+            // (C) P^T tiles, E4M3 hi/lo, one buffer per tile (the previous item's last P.V
+            // has completed: the epilogue waited for it)
             float l[NR];
 #pragma unroll
             for (int n = 0; n < NR; ++n) l[n] = 0.f;
@@ -903,12 +916,6 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
                 }
 #pragma unroll
                 for (int n = 0; n < NR; ++n) l[n] += pv[n];
-                if constexpr (!PACK) {
-                    ok = __all_sync(0xffffffffu, mbar_wait_bounded(BAR(P_EMPTY + pb),
-                                                                   ((pt / NPB) & 1) ^ 1, abort_flag,
-                                                                   p.status));
-                    if (!ok) break;
-                }
                 if constexpr (PACK)
                     store_row_e4m3_p16<NR>(smem + OFF_P + pb * P_STRIDE, r, pv);
                 else
@@ -955,6 +962,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
 template <int G, int NR>
 static cudaError_t launch_g(const Params& p, int num_sms, cudaStream_t stream) {
     static std::atomic<bool> configured[64];  // per device, set once (repeats are harmless)
+    constexpr int SMEM_BYTES = Layout<(NR <= 8)>::SMEM_BYTES;
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !configured[dev].load(std::memory_order_acquire)) {
