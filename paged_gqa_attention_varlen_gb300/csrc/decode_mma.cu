@@ -854,17 +854,27 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
                 // is the hi part, column 16 + n the lo part)
 #pragma unroll
                 for (int n = 0; n < NR; ++n) mx[n] = -INFINITY;
+                const uint64_t c2 = f2_pack(c_eff, c_eff);
                 for (int t = 0; t < it.ntiles; ++t) {
                     uint32_t u[32];
                     tmem_ld32(s_base + S_COLS * t, u);
                     tmem_wait_ld32(u);
                     const uint32_t vm = vis_mask(t);
+                    float a[NR];  // scores (hi + lo) in log2 units, pairs of columns at once
 #pragma unroll
-                    for (int n = 0; n < NR; ++n) {
-                        const float a = ((vm >> n) & 1u)
-                                            ? (__uint_as_float(u[n]) + __uint_as_float(u[NH + n])) * c_eff
-                                            : -INFINITY;
-                        mx[n] = fmaxf(mx[n], a);
+                    for (int n = 0; n < NR; n += 2)
+                        f2_unpack(f2_mul(f2_add(f2_pack(__uint_as_float(u[n]), __uint_as_float(u[n + 1])),
+                                                f2_pack(__uint_as_float(u[NH + n]),
+                                                        __uint_as_float(u[NH + n + 1]))),
+                                         c2),
+                                  a[n], a[n + 1]);
+                    if (vm == 0xFFFFu) {  // every column sees key r (all but edge tiles)
+#pragma unroll
+                        for (int n = 0; n < NR; ++n) mx[n] = fmaxf(mx[n], a[n]);
+                    } else {
+#pragma unroll
+                        for (int n = 0; n < NR; ++n)
+                            mx[n] = fmaxf(mx[n], ((vm >> n) & 1u) ? a[n] : -INFINITY);
                     }
                 }
             }
@@ -907,12 +917,22 @@ __global__ void __launch_bounds__(THREADS, 1) decode_mma_kernel(const __grid_con
                     tmem_ld32(s_base + S_COLS * t, u);
                     tmem_wait_ld32(u);
                     const uint32_t vm = vis_mask(t);
+                    const uint64_t c2 = f2_pack(c_eff, c_eff);
+                    float e[NR];  // exponents: score - max + 8, pairs of columns at once
 #pragma unroll
-                    for (int n = 0; n < NR; ++n)
-                        pv[n] = ex2_approx(
-                            (((vm >> n) & 1u) ? (__uint_as_float(u[n]) + __uint_as_float(u[NH + n])) * c_eff
-                                              : -INFINITY) +
-                            neg[n]);
+                    for (int n = 0; n < NR; n += 2)
+                        f2_unpack(f2_fma(f2_add(f2_pack(__uint_as_float(u[n]), __uint_as_float(u[n + 1])),
+                                                f2_pack(__uint_as_float(u[NH + n]),
+                                                        __uint_as_float(u[NH + n + 1]))),
+                                         c2, f2_pack(neg[n], neg[n + 1])),
+                                  e[n], e[n + 1]);
+                    if (vm == 0xFFFFu) {  // every column sees key r (all but edge tiles)
+#pragma unroll
+                        for (int n = 0; n < NR; ++n) pv[n] = ex2_approx(e[n]);
+                    } else {
+#pragma unroll
+                        for (int n = 0; n < NR; ++n) pv[n] = ((vm >> n) & 1u) ? ex2_approx(e[n]) : 0.f;
+                    }
                 }
 #pragma unroll
                 for (int n = 0; n < NR; ++n) l[n] += pv[n];
