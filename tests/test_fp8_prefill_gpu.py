@@ -333,3 +333,22 @@ def test_e4m3_layer_slice_matches_packed_bitwise(cuda_lib, max_qo):
     torch.cuda.synchronize()
     assert cuda_lib.device_status() == 0
     assert torch.equal(o, o2) and torch.equal(lse, l2)
+
+
+@pytest.mark.parametrize("max_qo", [4, None], ids=["tensor-core", "conversion"])
+def test_nan_bytes_in_unused_tail_slots_are_invisible(cuda_lib, max_qo):
+    """E4M3 NaN bytes in the key slots past each request's last key (its last page's tail)
+    change nothing: the scores of those slots are masked and their V rows never reach
+    P.V (0 * NaN would be NaN)."""
+    kv, qo = [20, 1030, 3, 901], [4, 3, 2, 4]
+    pc = W.paged_case_e4m3(kv, 16, 4, 128, page_size=16, qo_lens=qo, seed=131, device="cuda")
+    mq = max_qo if max_qo is not None else sum(qo)
+    o1, l1 = run(cuda_lib, pc, mq)
+    for b, n in enumerate(pc.kv_lens):
+        last = int(pc.page_table[b, (n - 1) // 16])
+        pc.k_pages[last, n % 16:] = 0x7F   # E4M3 NaN
+        pc.v_pages[last, n % 16:] = 0xFF
+    o2, l2 = run(cuda_lib, pc, mq)
+    assert cuda_lib.device_status() == 0
+    assert torch.isfinite(o2.float()).all()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
