@@ -837,9 +837,9 @@ int paged_prefill_impl(const void* q, const void* k_pages, const void* v_pages, 
 
     const size_t usable = kv8 ? ((st->ws_bytes - tail) & ~(size_t)1023) : 0;
     const PrefillWs lay = prefill_layout(*st, batch, head_dim, usable);
+    dequant::Params dq;  // E4M3 pools: launched right after the plan, beside it
     if (kv8) {
         uint8_t* tail_base = static_cast<uint8_t*>(st->ws) + usable;
-        dequant::Params dq;
         dq.k8 = static_cast<const uint8_t*>(k_pages);
         dq.v8 = static_cast<const uint8_t*>(v_pages);
         dq.page_stride = page_stride;
@@ -857,8 +857,7 @@ int paged_prefill_impl(const void* q, const void* k_pages, const void* v_pages, 
         dq.num_pages = num_pages;
         dq.num_kv_heads = num_kv_heads;
         dq.head_dim = head_dim;
-        if (dequant::launch_dequant(dq, st->num_sms, s) != cudaSuccess) return PGQA_ERR_CUDA;
-        // from here on the call reads the bf16 pool: packed NHD, pool_pages pages
+        // from here on the call reads the converted pool: packed NHD, pool_pages pages
         k_pages = dq.k16;
         v_pages = dq.v16;
         if (!by_page) page_table = dq.table_out;
@@ -947,6 +946,9 @@ int paged_prefill_impl(const void* q, const void* k_pages, const void* v_pages, 
     fill_split(pp, p, lay, batch, head_dim, num_qo_heads, st->num_sms);
     e = prefill::launch_plan(pp, tq, tk, tv, s);
     if (e != cudaSuccess) return PGQA_ERR_CUDA;
+    // the plan needs nothing of the conversion (it reads q_indptr and kv_lens), and the
+    // conversion nothing of the plan
+    if (kv8 && dequant::launch_dequant(dq, st->num_sms, s) != cudaSuccess) return PGQA_ERR_CUDA;
     e = head_dim == 128 ? prefill::launch_attention_pair<true>(p, st->num_sms, s)
                         : prefill::launch_attention<256, true>(p, st->num_sms, grouped, s);
     if (e != cudaSuccess) return PGQA_ERR_CUDA;

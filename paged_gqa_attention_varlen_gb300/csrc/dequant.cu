@@ -25,6 +25,11 @@
 // Only the slots below ceil(kv_len / page_size) of each request are converted.  A kv_len
 // outside 0..stride * page_size converts nothing (the prefill's plan reports it); a page
 // id outside 0..num_pages-1 is reported as PGQA_DEV_BOUNDS and not read.
+//
+// The conversion runs beside the prefill's plan: the plan (one CTA) starts first and lets
+// this grid launch at once; each CTA of this grid waits for the plan to complete before
+// it exits, so that the attention kernel, which waits for this grid, sees the plan's work
+// list as well as the pool.
 #include "ptx.cuh"
 
 namespace pgqa {
@@ -104,14 +109,26 @@ __global__ void __launch_bounds__(THREADS) dequant_pages_kernel(const Params p) 
             reinterpret_cast<uint4*>(vd + (long long)u * 16)[1] = hi;
         }
     }
+    // the plan launched before this grid has completed, and its writes are visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 cudaError_t launch_dequant(const Params& p, int num_sms, cudaStream_t stream) {
     const long long slots = (long long)p.batch * p.page_table_stride;
     if (slots <= 0) return cudaSuccess;
     const long long grid = slots < (long long)num_sms * 16 ? slots : (long long)num_sms * 16;
-    dequant_pages_kernel<<<(unsigned)grid, THREADS, 0, stream>>>(p);
-    return cudaGetLastError();
+    // programmatic dependent launch: the grid may start while the plan still runs
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, dequant_pages_kernel, p);
 }
 
 }  // namespace dequant
