@@ -118,17 +118,7 @@ cudaError_t launch_dequant(const Params& p, int num_sms, cudaStream_t stream) {
     if (slots <= 0) return cudaSuccess;
     const long long grid = slots < (long long)num_sms * 16 ? slots : (long long)num_sms * 16;
     // programmatic dependent launch: the grid may start while the plan still runs
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, dequant_pages_kernel, p);
+    return launch_dependent(dequant_pages_kernel, (unsigned)grid, THREADS, 0, stream, p);
 }
 
 }  // namespace dequant

@@ -1770,23 +1770,8 @@ __global__ void __launch_bounds__(256) merge_kernel(const Params p) {
 }
 
 // ------------------------------------------------------------------ host launchers
-// Launch with programmatic dependent launch: the grid may start while the previous kernel
-// in the stream (the plan) still runs; it calls griddepcontrol.wait before using its output.
-template <typename Kernel>
-static cudaError_t launch_dependent(Kernel kernel, int grid, int threads, int smem,
-                                   cudaStream_t stream, const Params& p) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(threads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, p);
-}
+// The attention and merge kernels are launched with launch_dependent (ptx.cuh): they may
+// start while the plan still runs and execute griddepcontrol.wait before using its output.
 
 template <int D, bool PAGED, bool GROUPED, bool F8CONV>
 static cudaError_t launch_attention_t(const Params& p, int grid, cudaStream_t stream) {

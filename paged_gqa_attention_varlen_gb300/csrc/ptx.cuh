@@ -335,6 +335,26 @@ __device__ __forceinline__ void e4m3_split2(float a, float b, uint32_t& hi, uint
     lo = l;
 }
 
+// Launch with programmatic dependent launch: the grid may start while the kernel before it
+// in the stream still runs (once that kernel has executed griddepcontrol.launch_dependents,
+// or has ended); the kernel executes griddepcontrol.wait before it reads that kernel's
+// output.
+template <typename Kernel, typename Arg>
+static inline cudaError_t launch_dependent(Kernel kernel, unsigned grid, unsigned threads,
+                                           size_t smem, cudaStream_t stream, const Arg& arg) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, arg);
+}
+
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

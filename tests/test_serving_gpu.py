@@ -227,3 +227,66 @@ def test_batches_beyond_the_plans_shared_memory_path(cuda_lib):
                                     dc.kv_lens_t, 8, 2, True, dc.sm_scale, rows=drows)
     didx = torch.as_tensor(drows, device="cuda")
     check_rows(do.reshape(-1, 128)[didx], dl.reshape(-1)[didx], ro, rl, "decode, 3000 requests")
+
+
+@pytest.mark.parametrize("rows", [4, 48], ids=["tensor-core", "conversion"])
+def test_cuda_graph_replay_e4m3_paged_prefill(cuda_lib, rows):
+    """The E4M3 paged prefill captured once and replayed over rewritten inputs (pages,
+    page table, kv_lens and queries of two different calls, alternating) gives the eager
+    results bit for bit, on both of its paths (rows query rows per request: 4 x G = 16 is
+    the tensor-core form, 48 the conversion of the pages the call reads)."""
+    api = cuda_lib
+    dev = torch.device("cuda")
+    qo = [rows] * 3
+    ca = W.paged_case_e4m3([900, 40, 2100], 16, 4, 128, page_size=16, qo_lens=qo, seed=81,
+                           extra_pages=30, device=dev)
+    cb = W.paged_case_e4m3([3000, 700, 9], 16, 4, 128, page_size=16, qo_lens=qo, seed=82,
+                           device=dev)
+    npages = max(ca.num_pages, cb.num_pages)
+    stride = max(ca.page_table.shape[1], cb.page_table.shape[1])
+    kp = torch.zeros((npages, 16, 4, 128), dtype=torch.uint8, device=dev)
+    vp = torch.zeros_like(kp)
+    pt = torch.full((3, stride), -1, dtype=torch.int32, device=dev)
+    kl = torch.zeros(3, dtype=torch.int32, device=dev)
+    q = torch.zeros_like(ca.q)
+    o = torch.zeros_like(q)
+    lse = torch.zeros(q.shape[:2], dtype=torch.float32, device=dev)
+    qi = ca.q_indptr.clone()
+
+    def load(c):
+        kp.zero_(); vp.zero_(); pt.fill_(-1)
+        kp[:c.num_pages].copy_(c.k_pages)
+        vp[:c.num_pages].copy_(c.v_pages)
+        pt[:, :c.page_table.shape[1]].copy_(c.page_table)
+        kl.copy_(c.kv_lens_t)
+        q.copy_(c.q)
+
+    def step():
+        api.paged_prefill(q, kp, vp, qi, pt, kl, causal=True, sm_scale=ca.sm_scale,
+                          k_scale=ca.meta["k_scale"], v_scale=ca.meta["v_scale"],
+                          max_qo_len=rows, out=o, lse=lse)
+
+    refs = {}
+    for name, c in (("a", ca), ("b", cb)):
+        load(c)
+        step()
+        torch.cuda.synchronize()
+        assert api.device_status() == 0
+        refs[name] = (o.clone(), lse.clone())
+
+    load(ca)
+    graph = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()  # warm-up on the capture stream
+    torch.cuda.current_stream().wait_stream(s)
+    with torch.cuda.graph(graph):
+        step()
+    for idx, (name, c) in enumerate((("b", cb), ("a", ca), ("b", cb), ("a", ca))):
+        o.zero_(); lse.zero_()
+        load(c)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert api.device_status() == 0
+        assert torch.equal(o, refs[name][0]) and torch.equal(lse, refs[name][1]), (idx, name)
