@@ -80,9 +80,13 @@ __device__ __forceinline__ Geo geo_of(const WorkItem& w, int dt, int group, int 
     return tile_geometry(w.q_start, w.qo_len, w.kv_start, w.kv_len, w.qt + dt, group, causal);
 }
 
+// The attention kernels start while the plan still writes the work list (programmatic
+// dependent launch), so it is read through L2 (ld.global.cg), never through the
+// non-coherent read-only path, whose contract is data that no one writes while the
+// kernel runs.
 __device__ __forceinline__ WorkItem load_item(const WorkItem* items, int i) {
     const int4* v = reinterpret_cast<const int4*>(items + i);
-    const int4 a = __ldg(v), c = __ldg(v + 1), e = __ldg(v + 2);
+    const int4 a = __ldcg(v), c = __ldcg(v + 1), e = __ldcg(v + 2);
     WorkItem w;
     w.b = a.x; w.g = a.y; w.qt = a.z; w.cost = a.w;
     w.q_start = c.x; w.qo_len = c.y; w.kv_start = c.z; w.kv_len = c.w;
@@ -444,7 +448,7 @@ __global__ void __launch_bounds__(PLAN_THREADS)
 // Page id of lane l for tile j (-1 if that page holds no key of the request).
 __device__ __forceinline__ int lane_page_id(const int* pt_row, int j, int ppt, int npg, int lane) {
     const int pg = j * ppt + lane;
-    return lane < ppt && pg < npg ? __ldg(pt_row + pg) : -1;
+    return lane < ppt && pg < npg ? __ldcg(pt_row + pg) : -1;  // see load_item
 }
 // Whether lane l's page of tile j is in use, reporting an id outside the page pool
 // (PGQA_DEV_BOUNDS; that page is then not loaded).
@@ -510,7 +514,7 @@ __device__ __forceinline__ void zero_stage_rows(uint32_t stage, int r0, int lane
 __device__ __forceinline__ int group_page_id(const int* pt_row, int j, int ps, int npg, int bk,
                                              int lane) {
     const int pg = (j * BN + bk * lane) / ps;
-    return lane < BN / bk && pg < npg ? __ldg(pt_row + pg) : -1;
+    return lane < BN / bk && pg < npg ? __ldcg(pt_row + pg) : -1;  // see load_item
 }
 __device__ __forceinline__ bool group_page_ok(int id, int j, int ps, int npg, int bk,
                                               int num_pages, int lane, int* status) {
@@ -657,7 +661,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint32_t tmem_base = *tmem_slot;
 
-    const int n_items = p.hdr->n_items;
+    const int n_items = __ldcg(&p.hdr->n_items);  // written by the plan
     const int G = p.group;
 
     if (warp == 0 || (PAGED && warp == 3)) {
@@ -1201,7 +1205,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
     // the prologue above overlapped the plan kernel; its outputs are read from here on
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint32_t tmem_base = *tmem_slot;
-    const int n_items = p.hdr->n_items;
+    const int n_items = __ldcg(&p.hdr->n_items);  // written by the plan
     const int G = p.group;
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
