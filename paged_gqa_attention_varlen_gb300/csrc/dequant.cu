@@ -29,7 +29,8 @@
 // The conversion runs beside the prefill's plan: the plan (one CTA) starts first and lets
 // this grid launch at once; each CTA of this grid waits for the plan to complete before
 // it exits, so that the attention kernel, which waits for this grid, sees the plan's work
-// list as well as the pool.
+// list as well as the pool.  Launched that way, the grid starts before the kernel ahead of
+// it has ended, so it reads global memory through L2 (ld.global.cg) only.
 #include "ptx.cuh"
 
 namespace pgqa {
@@ -80,10 +81,10 @@ __global__ void __launch_bounds__(THREADS) dequant_pages_kernel(const Params p) 
         const int b = (int)(sl / p.page_table_stride);
         const int j = (int)(sl % p.page_table_stride);
         if (p.table_out != nullptr && threadIdx.x == 0) p.table_out[sl] = (int)sl;
-        int kv = __ldg(p.kv_lens + b);
+        int kv = __ldcg(p.kv_lens + b);
         if (kv < 0 || (long long)kv > (long long)p.page_table_stride * p.page_size) kv = 0;
         if ((long long)j * p.page_size >= kv) continue;  // uniform per CTA
-        const int pid = __ldg(p.page_table + sl);
+        const int pid = __ldcg(p.page_table + sl);
         if (pid < 0 || pid >= p.num_pages) {
             if (threadIdx.x == 0) atomicOr(p.status, PGQA_DEV_BOUNDS);
             continue;
@@ -98,8 +99,8 @@ __global__ void __launch_bounds__(THREADS) dequant_pages_kernel(const Params p) 
             const int h = r / (p.head_dim / 16), c = r % (p.head_dim / 16);
             const long long src =
                 (long long)slot * p.slot_stride + (long long)h * p.head_stride + c * 16;
-            const uint4 rk = *reinterpret_cast<const uint4*>(ks + src);
-            const uint4 rv = *reinterpret_cast<const uint4*>(vs + src);
+            const uint4 rk = __ldcg(reinterpret_cast<const uint4*>(ks + src));
+            const uint4 rv = __ldcg(reinterpret_cast<const uint4*>(vs + src));
             uint4 lo, hi;
             e4m3x16_to_bf16(rk, lo, hi);
             reinterpret_cast<uint4*>(kd + (long long)u * 16)[0] = lo;

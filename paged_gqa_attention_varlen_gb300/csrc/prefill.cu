@@ -100,9 +100,6 @@ __host__ __device__ __forceinline__ int split_chunks(int kv_len, int st) {
     return tiles > st ? (tiles + st - 1) / st : 1;
 }
 
-__device__ __forceinline__ void prefetch_l1(const void* ptr) {
-    asm volatile("prefetch.global.L1 [%0];" ::"l"(ptr));
-}
 
 // Items are sorted longest first; CTA c walks them in "snake" order (rounds of gridDim
 // items, alternate rounds reversed), which balances the per-CTA totals of an LPT-sorted
@@ -691,7 +688,6 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
             while (ok && it >= 0) {
                 const WorkItem w = load_item(p.items, it);
                 it = snake_next(rr, n_items);
-                if (it >= 0) prefetch_l1(p.items + it);
                 const Geo x = geo_of(w, 0, G, p.causal);
                 const int n = item_tiles(w, x);  // K/V tiles kt0 .. kt0 + n - 1
                 const int kt0 = w.kt0;
@@ -844,7 +840,6 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
             while (ok && it >= 0) {
                 const WorkItem w = load_item(p.items, it);
                 it = snake_next(rr, n_items);
-                if (it >= 0) prefetch_l1(p.items + it);
                 const Geo x = geo_of(w, 0, G, p.causal);
                 const int n = item_tiles(w, x);
                 if (n == 0) continue;
@@ -937,7 +932,6 @@ __global__ void __launch_bounds__(THREADS, 1) attention_kernel(const Params p) {
         while (ok && it >= 0) {
             const WorkItem w = load_item(p.items, it);
             it = snake_next(rr, n_items);
-            if (it >= 0) prefetch_l1(p.items + it);
             const Geo x = geo_of(w, 0, G, p.causal);
             const int row_t = x.t0 + r / G;
             const int row_h = w.g * G + r % G;
@@ -1234,7 +1228,6 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
             while (ok && it >= 0) {
                 const WorkItem w = load_item(p.items, it);
                 it = snake_next(rr, n_items);
-                if (it >= 0) prefetch_l1(p.items + it);
                 const Geo a = geo_of(w, 0, G, p.causal);
                 const Geo bq = geo_of(w, 1, G, p.causal);
                 const int nA = item_tiles(w, a);
@@ -1343,7 +1336,6 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
             while (ok && it >= 0) {
                 const WorkItem w = load_item(p.items, it);
                 it = snake_next(rr, n_items);
-                if (it >= 0) prefetch_l1(p.items + it);
                 const Geo a = geo_of(w, 0, G, p.causal);
                 const Geo bq = geo_of(w, 1, G, p.causal);
                 const int nx[2] = {item_tiles(w, a), bq.t0 < bq.qo_len ? item_tiles(w, bq) : 0};
@@ -1530,7 +1522,6 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) attention_pair_kernel(const P
         while (ok && it >= 0) {
             const WorkItem w = load_item(p.items, it);
             it = snake_next(rr, n_items);
-            if (it >= 0) prefetch_l1(p.items + it);
             const Geo x = geo_of(w, X, G, p.causal);
             if (x.t0 >= x.qo_len) continue;  // this item has no tile B
             const int row_t = x.t0 + r / G;
