@@ -29,9 +29,10 @@
 // to 8 tiles of 128 keys; the items of a CTA run as a software pipeline in which step s
 // handles the K tiles of item s and the V tiles of item s - 1):
 //  * warps 0, 2 and 3, producers: stream 128-key tiles of E4M3 bytes in step order through
-//    a TMA ring of 12 stages (11 with several query rows), each taking every third tile; lane u < 8 loads the 16-key unit u
-//    of a tile (a 16-token page, or a slice of a larger page) as one 2 KB box, 128-byte
-//    swizzled: 128 rows (keys) of 128 bytes (dims).  Page ids are read one item ahead.
+//    a TMA ring of 12 stages (11 with several query rows), each taking every third tile;
+//    lane u < 8 loads the 16-key unit u of a tile (a 16-token page, or a slice of a
+//    larger page) as one 2 KB box, 128-byte swizzled: 128 rows (keys) of 128 bytes
+//    (dims).  Page ids are read one item ahead.
 //  * warp 1, lane 0: MMA issuer (swap-AB, keys as M = 128, query columns padded to N =
 //    16; with several query rows per request, column n is row n / G, head n % G):
 //      S^T_t  = K_t . (Qhi + Qlo)^T     A = raw K tile (K-major), B = Q parts (K-major)
@@ -50,11 +51,10 @@
 //    pass over all its S^T tiles gives the exact max per column (a transposing warp
 //    butterfly and one exchange among the four warps), so no running rescale is needed;
 //    then each tile's P^T = 2^8 exp2(s - max) goes to shared memory as E4M3 hi/lo bytes,
-//    one row per key that its thread writes with one or two 16-byte stores (one buffer
-//    per tile of the item) while
-//    the column sums accumulate; at the item's end
-//    thread r holds row r of O^T: divided by l, scaled by v_scale, it becomes the bf16
-//    output (single-chunk request) or the fp32 partial and its lse.
+//    one row per key that its thread writes with one or two 16-byte stores (a buffer per
+//    tile of the item), while the column sums accumulate; at the item's end thread r
+//    holds row r of O^T: divided by l, scaled by v_scale, it becomes the bf16 output
+//    (single-chunk request) or the fp32 partial and its lse.
 //  While the softmax works on item s - 1, the tensor core is already on the K tiles of
 //  item s.
 #include <atomic>
