@@ -55,6 +55,8 @@ SMALL = [
     ([4] * 8, [1000, 17, 129, 4096, 5, 2048, 3000, 64], 32, 8, 128, True, 16),  # 4-token decode
     ([1] * 5, [1, 16, 17, 300, 1029], 8, 2, 128, True, 32),  # one-token decode shape
     ([3, 7], [2000, 131], 16, 4, 256, True, 32),         # hd256 multi-token decode
+    ([37, 5, 130], [200, 90, 130], 64, 1, 128, True, 16),  # G = 64
+    ([9, 40], [300, 41], 128, 1, 256, True, 32),         # G = 128, hd256
 ]
 
 

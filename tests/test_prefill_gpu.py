@@ -51,6 +51,11 @@ SMALL = [
     ([260, 31], [260, 31], 32, 2, 128, True),        # G = 16
     ([129, 200], [129, 700], 8, 2, 256, True),       # hd256
     ([64, 300], [64, 300], 4, 1, 256, False),
+    ([37, 5, 130], [200, 5, 130], 64, 2, 128, True),    # G = 32: 4 tokens per q tile
+    ([37, 5, 130], [200, 90, 130], 64, 1, 128, False),  # G = 64: 2 tokens per q tile
+    ([9, 3, 40], [300, 3, 41], 128, 1, 128, True),      # G = 128: one token per q tile
+    ([21, 6], [150, 6], 128, 1, 256, True),             # G = 128, hd256
+    ([33, 70], [400, 70], 64, 2, 256, False),           # G = 32, hd256
 ]
 
 
