@@ -176,7 +176,8 @@ def test_rows_beyond_the_declared_maximum_are_refused(cuda_lib):
 
 @pytest.mark.parametrize("d,G,ps,causal", [(128, 4, 16, True), (128, 1, 64, True),
                                            (128, 8, 32, False), (128, 16, 16, True),
-                                           (256, 4, 16, True), (256, 2, 128, False)])
+                                           (256, 4, 16, True), (256, 2, 128, False),
+                                           (128, 64, 16, True), (256, 32, 32, True)])
 def test_e4m3_long_prefill_against_oracle(cuda_lib, d, G, ps, causal):
     """Query runs longer than 16 / G rows (and head_dim 256): the pages are converted in
     the workspace (K to bf16, V to f16) and the paged prefill runs over them."""
