@@ -297,3 +297,22 @@ def test_the_product_package_never_imports_the_oracle():
             elif isinstance(node, ast.ImportFrom):
                 names = [node.module or ""]
             assert not any(n == "oracle" or n.startswith("oracle.") for n in names), path
+
+
+def test_empty_tensor_stand_ins(api):
+    """Tensors without rows get a device address from a stand-in: one row of the same
+    shape, or (a page pool without pages) a zeroed span that covers one page under the
+    pool's strides; tensors with rows are passed as they are."""
+    import torch
+    k = torch.zeros(0, 4, 128, dtype=torch.bfloat16)
+    s = api._with_rows(k)
+    assert s.shape == (1, 4, 128) and s.dtype == k.dtype and bool((s == 0).all())
+    full = torch.ones(3, 4, 128, dtype=torch.bfloat16)
+    assert api._with_rows(full) is full
+    # an HND pool slice with padded strides: slot stride 160, head stride 16 * 160
+    pool = torch.zeros(0, 8, 16, 160, dtype=torch.uint8)[..., :128]
+    strides = (pool.stride(0), pool.stride(2), pool.stride(1))  # page, slot, head
+    st = api._pool_with_page(pool, 16, 8, 128, strides)
+    assert st.dim() == 1 and st.numel() == 15 * strides[1] + 7 * strides[2] + 128
+    pages = torch.zeros(2, 16, 8, 128, dtype=torch.bfloat16)
+    assert api._pool_with_page(pages, 16, 8, 128, (16 * 8 * 128, 8 * 128, 128)) is pages
